@@ -1,0 +1,361 @@
+/*
+ * dsa_oracle.c -- plain, slow CPU oracle for the DSA layer hot path.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product path may call this code:
+ * only the test suite, the smoke check and the CPU-baseline leg of the
+ * benchmark load it.  It shares no code, header, table or constant generator
+ * with the CUDA library; the two meet only at the byte layouts of their
+ * inputs and outputs.
+ *
+ * What it computes (source: vLLM blog "Day-0 support for Kimi K3.1 Pro",
+ * section "Sparse attention in K3.1 Pro" (Fig. 1), "One KV cache, three
+ * states", "Low-latency decode: fused DSA decode path", and the AMD section
+ * "Quantization: native MXFP4 indexer"):
+ *
+ *   indexer   logit[r,t] = sum_h w[r,h] * max(0, s_t * <q[r,h,:], k_t>)
+ *             for every earlier token t < L_r (L_r counts the query itself)
+ *   top-k     the k = 2048 highest logits of [0, L_r); ties go to the lower
+ *             token index; fewer than k visible tokens -> all of them
+ *   slots     physical slot = block_table[req][t / 64] * 64 + t % 64
+ *   sparse    exact attention of each of the 96 query heads over only the
+ *   MLA       selected tokens' 576-dim latents (512 latent + 64 RoPE dims);
+ *             the latent itself is the value (absorbed MLA), so
+ *             O[h] = sum_t softmax_t(S[h,t]) * kv[t, 0:512],
+ *             S[h,t] = sm_scale * <q[h,:], kv[t,:]>.
+ *
+ * Every floating-point sum runs in double, in index order.  Cache entries are
+ * decoded exactly from their stored bytes; the codec definitions are written
+ * from the OCP 8-bit floating point spec (E4M3, "FN" variant: no infinities,
+ * S.1111.111 is NaN) and the OCP Microscaling v1.0 spec (E2M1 elements, E8M0
+ * scales with 0xFF = NaN, as the SM120 MXFP4 experiment log restates in its
+ * "NaN/Inf decision record").
+ *
+ * Byte layouts of one 64-token page (the pages fix the per-token widths:
+ * FP8 index key 132 B, MXFP4 index key 68 B, FP8 latent 576 B, NVFP4 latent
+ * 352 B; the arrangement inside a page is this library's reading):
+ *   index FP8   [64 x 128 B e4m3 codes][64 x fp32 scale]            8448 B
+ *   index MXFP4 [64 x 64 B e2m1 pairs][64 x 4 B e8m0 (one per 32)]  4352 B
+ *   latent FP8  [64 x 576 B e4m3], one per-tensor fp32 scale       36864 B
+ *   latent NVFP4 [64 x 256 B e2m1 pairs][64 x 32 B e4m3 scale (one per 16)]
+ *                [64 x 64 B e4m3 RoPE dims, per-tensor scale]       22528 B
+ * Packed e2m1 pairs hold element 2j in the low nibble, 2j+1 in the high one.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define OR_OK 0
+#define OR_ERR_ARG -1
+#define OR_ERR_BOUNDS -6
+
+#define OR_KEY_FP8 1
+#define OR_KEY_MXFP4 2
+#define OR_LATENT_FP8 3
+#define OR_LATENT_NVFP4 4
+
+#define OR_PAGE 64
+#define OR_IDX_DIM 128
+#define OR_IDX_HEADS 32
+#define OR_LAT_DIM 576
+#define OR_V_DIM 512
+
+/* ---------------------------------------------------------------- codecs */
+
+/* E4M3 (OCP FP8, "FN"): 1 sign, 4 exponent (bias 7), 3 mantissa bits.
+ * Exponent field 0 is subnormal (m/8 * 2^-6); 0x7F / 0xFF are NaN. */
+double oracle_e4m3_decode(uint8_t b) {
+    int s = (b >> 7) & 1, e = (b >> 3) & 15, m = b & 7;
+    double v;
+    if (e == 15 && m == 7) return NAN;
+    if (e == 0) v = ldexp((double)m / 8.0, -6);
+    else v = ldexp(1.0 + (double)m / 8.0, e - 7);
+    return s ? -v : v;
+}
+
+/* E2M1 (OCP MX FP4): 1 sign, 2 exponent (bias 1), 1 mantissa bit; no
+ * specials.  Exponent 0 is subnormal: m * 0.5. */
+double oracle_e2m1_decode(uint8_t nib) {
+    int s = (nib >> 3) & 1, e = (nib >> 1) & 3, m = nib & 1;
+    double v = (e == 0) ? 0.5 * m : ldexp(1.0 + 0.5 * m, e - 1);
+    return s ? -v : v;
+}
+
+/* E8M0 (OCP MX shared scale): 2^(e-127); 0xFF is NaN. */
+double oracle_e8m0_decode(uint8_t b) {
+    if (b == 0xFF) return NAN;
+    return ldexp(1.0, (int)b - 127);
+}
+
+/* bf16: the upper half of an IEEE binary32. */
+double oracle_bf16_decode(uint16_t h) {
+    uint32_t u = (uint32_t)h << 16;
+    float f;
+    memcpy(&f, &u, 4);
+    return (double)f;
+}
+
+static double rd_f32(const uint8_t *p) {
+    float f;
+    memcpy(&f, p, 4);
+    return (double)f;
+}
+
+/* ------------------------------------------------------- cache addressing */
+
+int64_t oracle_index_page_bytes(int fmt) {
+    if (fmt == OR_KEY_FP8) return OR_PAGE * (OR_IDX_DIM + 4);
+    if (fmt == OR_KEY_MXFP4) return OR_PAGE * (OR_IDX_DIM / 2 + OR_IDX_DIM / 32);
+    return -1;
+}
+
+int64_t oracle_latent_page_bytes(int fmt) {
+    if (fmt == OR_LATENT_FP8) return OR_PAGE * OR_LAT_DIM;
+    if (fmt == OR_LATENT_NVFP4) return OR_PAGE * (OR_V_DIM / 2 + OR_V_DIM / 16 + (OR_LAT_DIM - OR_V_DIM));
+    return -1;
+}
+
+/* Decode the index key of slot (page, j) into k[128] and its per-token scale.
+ * FP8: k = e4m3 code values, scale = the stored fp32.
+ * MXFP4: k = e2m1 * 2^(E-127) per 32-element block, scale = 1. */
+static void decode_index_key(const uint8_t *pool, int fmt, int64_t page, int j, double *k, double *scale) {
+    const uint8_t *pg = pool + page * oracle_index_page_bytes(fmt);
+    if (fmt == OR_KEY_FP8) {
+        const uint8_t *codes = pg + (int64_t)j * OR_IDX_DIM;
+        for (int i = 0; i < OR_IDX_DIM; ++i) k[i] = oracle_e4m3_decode(codes[i]);
+        *scale = rd_f32(pg + OR_PAGE * OR_IDX_DIM + 4 * j);
+    } else {
+        const uint8_t *pairs = pg + (int64_t)j * (OR_IDX_DIM / 2);
+        const uint8_t *sc = pg + OR_PAGE * (OR_IDX_DIM / 2) + (int64_t)j * (OR_IDX_DIM / 32);
+        for (int i = 0; i < OR_IDX_DIM; ++i) {
+            uint8_t byte = pairs[i / 2];
+            uint8_t nib = (i & 1) ? (byte >> 4) : (byte & 15);
+            k[i] = oracle_e2m1_decode(nib) * oracle_e8m0_decode(sc[i / 32]);
+        }
+        *scale = 1.0;
+    }
+}
+
+/* Decode the latent of a physical slot into kv[576] (exact, in double).
+ * FP8: e4m3 * tensor_scale for all 576 dims.
+ * NVFP4: dims 0..511 are e2m1 * (e4m3 scale of their 16-block); the 64 RoPE
+ * dims are e4m3 * tensor_scale. */
+static void decode_latent(const uint8_t *pool, int fmt, int64_t slot, double tensor_scale, double *kv) {
+    int64_t page = slot / OR_PAGE;
+    int j = (int)(slot % OR_PAGE);
+    const uint8_t *pg = pool + page * oracle_latent_page_bytes(fmt);
+    if (fmt == OR_LATENT_FP8) {
+        const uint8_t *codes = pg + (int64_t)j * OR_LAT_DIM;
+        for (int i = 0; i < OR_LAT_DIM; ++i) kv[i] = oracle_e4m3_decode(codes[i]) * tensor_scale;
+    } else {
+        const uint8_t *pairs = pg + (int64_t)j * (OR_V_DIM / 2);
+        const uint8_t *sc = pg + OR_PAGE * (OR_V_DIM / 2) + (int64_t)j * (OR_V_DIM / 16);
+        const uint8_t *rope = pg + OR_PAGE * (OR_V_DIM / 2 + OR_V_DIM / 16) + (int64_t)j * (OR_LAT_DIM - OR_V_DIM);
+        for (int i = 0; i < OR_V_DIM; ++i) {
+            uint8_t byte = pairs[i / 2];
+            uint8_t nib = (i & 1) ? (byte >> 4) : (byte & 15);
+            kv[i] = oracle_e2m1_decode(nib) * oracle_e4m3_decode(sc[i / 16]);
+        }
+        for (int i = OR_V_DIM; i < OR_LAT_DIM; ++i) kv[i] = oracle_e4m3_decode(rope[i - OR_V_DIM]) * tensor_scale;
+    }
+}
+
+/* ---------------------------------------------------------------- indexer */
+
+/* logits[r * stride + t] for t < row_ctx[r]; entries at t >= row_ctx[r] are
+ * left untouched.  q_idx is [R, 32, 128] e4m3 (no query scale: the head
+ * weights carry it), w is [R, 32] fp32.  Returns OR_ERR_BOUNDS if a block
+ * table entry a row needs is outside [0, num_pages). */
+int oracle_indexer_logits(const uint8_t *pool, int fmt, int64_t num_pages,
+                          const int32_t *block_table, int64_t bt_stride,
+                          const int32_t *row_req, const int32_t *row_ctx, int num_rows,
+                          const uint8_t *q_idx, const float *w,
+                          double *logits, int64_t stride) {
+    if (oracle_index_page_bytes(fmt) < 0) return OR_ERR_ARG;
+    int err = OR_OK;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int r = 0; r < num_rows; ++r) {
+        double q[OR_IDX_HEADS][OR_IDX_DIM], k[OR_IDX_DIM], s;
+        for (int h = 0; h < OR_IDX_HEADS; ++h)
+            for (int i = 0; i < OR_IDX_DIM; ++i)
+                q[h][i] = oracle_e4m3_decode(q_idx[((int64_t)r * OR_IDX_HEADS + h) * OR_IDX_DIM + i]);
+        const int32_t *bt = block_table + (int64_t)row_req[r] * bt_stride;
+        for (int t = 0; t < row_ctx[r]; ++t) {
+            int64_t page = bt[t / OR_PAGE];
+            if (page < 0 || page >= num_pages) {
+#pragma omp atomic write
+                err = OR_ERR_BOUNDS;
+                continue;
+            }
+            decode_index_key(pool, fmt, page, t % OR_PAGE, k, &s);
+            double logit = 0.0;
+            for (int h = 0; h < OR_IDX_HEADS; ++h) {
+                double dot = 0.0;
+                for (int i = 0; i < OR_IDX_DIM; ++i) dot += q[h][i] * k[i];
+                double a = s * dot;
+                logit += (double)w[(int64_t)r * OR_IDX_HEADS + h] * (a > 0.0 ? a : 0.0);
+            }
+            logits[(int64_t)r * stride + t] = logit;
+        }
+    }
+    return err;
+}
+
+/* ------------------------------------------------------------------ top-k */
+
+typedef struct {
+    double v;
+    int32_t t;
+} scored;
+
+/* descending value, ascending index: the selection order the method uses */
+static int cmp_scored(const void *a, const void *b) {
+    const scored *x = (const scored *)a, *y = (const scored *)b;
+    if (x->v > y->v) return -1;
+    if (x->v < y->v) return 1;
+    return (x->t > y->t) - (x->t < y->t);
+}
+
+static int cmp_i32(const void *a, const void *b) {
+    int32_t x = *(const int32_t *)a, y = *(const int32_t *)b;
+    return (x > y) - (x < y);
+}
+
+/* One row: select the first min(k, n) of (value desc, index asc), then
+ * report them sorted by token index, padded with -1 up to k.  Signed zero
+ * compares equal (the C comparison already does so). */
+static void topk_row(const double *vals, int n, int k, int32_t *out) {
+    scored *buf = (scored *)malloc(sizeof(scored) * (size_t)(n > 0 ? n : 1));
+    for (int t = 0; t < n; ++t) {
+        buf[t].v = vals[t];
+        buf[t].t = t;
+    }
+    qsort(buf, (size_t)n, sizeof(scored), cmp_scored);
+    int m = n < k ? n : k;
+    for (int i = 0; i < m; ++i) out[i] = buf[i].t;
+    qsort(out, (size_t)m, sizeof(int32_t), cmp_i32);
+    for (int i = m; i < k; ++i) out[i] = -1;
+    free(buf);
+}
+
+/* top-k over fp32 logits (the decision is taken in the precision the
+ * logits are stored in). */
+int oracle_topk_f32(const float *logits, int64_t stride, const int32_t *row_ctx, int num_rows, int k, int32_t *out) {
+    if (k <= 0) return OR_ERR_ARG;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int r = 0; r < num_rows; ++r) {
+        int n = row_ctx[r];
+        double *v = (double *)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1));
+        for (int t = 0; t < n; ++t) v[t] = (double)logits[(int64_t)r * stride + t];
+        topk_row(v, n, k, out + (int64_t)r * k);
+        free(v);
+    }
+    return OR_OK;
+}
+
+/* top-k over double logits (end-to-end oracle path). */
+int oracle_topk_f64(const double *logits, int64_t stride, const int32_t *row_ctx, int num_rows, int k, int32_t *out) {
+    if (k <= 0) return OR_ERR_ARG;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int r = 0; r < num_rows; ++r)
+        topk_row(logits + (int64_t)r * stride, row_ctx[r], k, out + (int64_t)r * k);
+    return OR_OK;
+}
+
+/* ------------------------------------------------------------------ slots */
+
+/* slot = block_table[req][t / 64] * 64 + t % 64; -1 stays -1. */
+int oracle_page_to_slot(const int32_t *block_table, int64_t bt_stride, const int32_t *row_req, int num_rows,
+                        const int32_t *idx, int k, int32_t *slots) {
+    for (int r = 0; r < num_rows; ++r) {
+        const int32_t *bt = block_table + (int64_t)row_req[r] * bt_stride;
+        for (int i = 0; i < k; ++i) {
+            int32_t t = idx[(int64_t)r * k + i];
+            slots[(int64_t)r * k + i] = t < 0 ? -1 : bt[t / OR_PAGE] * OR_PAGE + t % OR_PAGE;
+        }
+    }
+    return OR_OK;
+}
+
+/* ------------------------------------------------------------- sparse MLA */
+
+/* q is [R, H, 576] bf16 bits; slots is [R, k] physical slots, -1 = unused.
+ * out is [R, H, 512], lse is [R, H] (natural log).  An empty selection gives
+ * out = 0 and lse = -inf. */
+int oracle_sparse_mla(const uint8_t *pool, int fmt, int64_t num_pages, double tensor_scale,
+                      const uint16_t *q, int num_heads, const int32_t *slots, int num_rows, int k,
+                      double sm_scale, double *out, double *lse) {
+    if (oracle_latent_page_bytes(fmt) < 0 || num_heads <= 0) return OR_ERR_ARG;
+    int err = OR_OK;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int r = 0; r < num_rows; ++r) {
+        const int32_t *sl = slots + (int64_t)r * k;
+        int n = 0;
+        for (int i = 0; i < k; ++i) n += sl[i] >= 0;
+        double *kv = (double *)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1) * OR_LAT_DIM);
+        double *sc = (double *)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1));
+        int j = 0;
+        for (int i = 0; i < k; ++i) {
+            if (sl[i] < 0) continue;
+            if ((int64_t)sl[i] >= num_pages * OR_PAGE) {
+#pragma omp atomic write
+                err = OR_ERR_BOUNDS;
+                continue;
+            }
+            decode_latent(pool, fmt, sl[i], tensor_scale, kv + (int64_t)j * OR_LAT_DIM);
+            ++j;
+        }
+        n = j;
+        for (int h = 0; h < num_heads; ++h) {
+            double qh[OR_LAT_DIM];
+            const uint16_t *qp = q + ((int64_t)r * num_heads + h) * OR_LAT_DIM;
+            for (int i = 0; i < OR_LAT_DIM; ++i) qh[i] = oracle_bf16_decode(qp[i]);
+            double *o = out + ((int64_t)r * num_heads + h) * OR_V_DIM;
+            for (int d = 0; d < OR_V_DIM; ++d) o[d] = 0.0;
+            if (n == 0) {
+                if (lse) lse[(int64_t)r * num_heads + h] = -INFINITY;
+                continue;
+            }
+            double m = -INFINITY;
+            for (int t = 0; t < n; ++t) {
+                double s = 0.0;
+                for (int i = 0; i < OR_LAT_DIM; ++i) s += qh[i] * kv[(int64_t)t * OR_LAT_DIM + i];
+                sc[t] = sm_scale * s;
+                if (sc[t] > m) m = sc[t];
+            }
+            double l = 0.0;
+            for (int t = 0; t < n; ++t) {
+                double p = exp(sc[t] - m);
+                l += p;
+                for (int d = 0; d < OR_V_DIM; ++d) o[d] += p * kv[(int64_t)t * OR_LAT_DIM + d];
+            }
+            for (int d = 0; d < OR_V_DIM; ++d) o[d] /= l;
+            if (lse) lse[(int64_t)r * num_heads + h] = m + log(l);
+        }
+        free(kv);
+        free(sc);
+    }
+    return err;
+}
+
+/* ------------------------------------------------------------------- misc */
+
+int oracle_num_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+void oracle_set_num_threads(int n) {
+#ifdef _OPENMP
+    if (n > 0) omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}

@@ -1,0 +1,346 @@
+"""Pins of the CPU oracle against facts that do not come from the oracle.
+
+Each ``pin_*`` function takes a loaded oracle library (so the planted-mistake
+test can hand it a deliberately broken build) and raises AssertionError when
+the oracle disagrees with:
+
+* library routines (torch's float8_e4m3fn and bfloat16 decoders, numpy
+  matmul/softmax/argsort),
+* the pages' printed figures (tests/golden/*.txt, each with its source),
+* brute force on tiny inputs, written independently here,
+* closed forms and invariants of the method (one-hot head weights, k >= L
+  giving dense attention, a single selected token, equal scores, paging
+  and head-padding invariance).
+"""
+from __future__ import annotations
+
+import math
+import os
+
+import numpy as np
+import torch
+
+import oracle
+from prefill_dsa_indexer_gb300 import inputs as I
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def _golden(name):
+    rows = []
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if line and not line.startswith("#"):
+                rows.append(line.split())
+    return rows
+
+
+# ------------------------------------------------------- independent decoders
+
+def ref_e4m3(codes) -> np.ndarray:
+    t = torch.from_numpy(np.ascontiguousarray(codes, dtype=np.uint8))
+    return t.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+
+
+E2M1 = np.array([float(v) for _, v in _golden("e2m1_values.txt")])
+
+
+def ref_e8m0(codes) -> np.ndarray:
+    c = np.asarray(codes, dtype=np.int64)
+    return np.where(c == 255, np.nan, np.ldexp(1.0, (c - 127).astype(np.int32)))
+
+
+def _unpack(packed) -> np.ndarray:
+    p = np.asarray(packed, dtype=np.uint8)
+    out = np.empty(p.shape[:-1] + (p.shape[-1] * 2,), dtype=np.uint8)
+    out[..., 0::2] = p & 15
+    out[..., 1::2] = p >> 4
+    return out
+
+
+def ref_index_keys(pool, fmt, slots):
+    """Decode index keys of physical slots -> (k [n,128] f64, scale [n])."""
+    pool = np.asarray(pool)
+    pages, j = slots // 64, slots % 64
+    if fmt == I.KEY_FP8:
+        codes = pool[:, :64 * 128].reshape(-1, 64, 128)[pages, j]
+        sc = pool[:, 64 * 128:].copy().view(np.float32).reshape(-1, 64)[pages, j].astype(np.float64)
+        return ref_e4m3(codes), sc
+    codes = _unpack(pool[:, :64 * 64].reshape(-1, 64, 64)[pages, j])
+    e = pool[:, 64 * 64:].reshape(-1, 64, 4)[pages, j]
+    k = E2M1[codes] * np.repeat(ref_e8m0(e), 32, axis=-1)
+    return k, np.ones(len(slots))
+
+
+def ref_latents(pool, fmt, tensor_scale, slots):
+    pool = np.asarray(pool)
+    pages, j = slots // 64, slots % 64
+    if fmt == I.LATENT_FP8:
+        return ref_e4m3(pool.reshape(-1, 64, 576)[pages, j]) * tensor_scale
+    codes = _unpack(pool[:, :64 * 256].reshape(-1, 64, 256)[pages, j])
+    sc = ref_e4m3(pool[:, 64 * 256:64 * 288].reshape(-1, 64, 32)[pages, j])
+    rope = ref_e4m3(pool[:, 64 * 288:].reshape(-1, 64, 64)[pages, j]) * tensor_scale
+    return np.concatenate([E2M1[codes] * np.repeat(sc, 16, axis=-1), rope], axis=-1)
+
+
+def ref_bf16(bits) -> np.ndarray:
+    t = torch.from_numpy(np.ascontiguousarray(bits, dtype=np.uint16).view(np.int16))
+    return t.view(torch.bfloat16).to(torch.float64).numpy()
+
+
+# ------------------------------------------------------------- brute force
+
+def brute_logits(inp: I.Inputs):
+    """sum_h w_h * relu(s_t * q_h . k_t), numpy float64."""
+    bt, rq, rc = inp.np("block_table"), inp.np("row_req"), inp.np("row_ctx")
+    q = ref_e4m3(inp.np("q_idx"))
+    w = inp.np("head_w").astype(np.float64)
+    out = np.full((len(rc), int(rc.max())), np.nan)
+    for r in range(len(rc)):
+        t = np.arange(rc[r])
+        slots = bt[rq[r], t // 64].astype(np.int64) * 64 + t % 64
+        k, s = ref_index_keys(inp.np("idx_pool"), inp.wl.key_fmt, slots)
+        a = (q[r] @ k.T) * s[None, :]
+        out[r, :rc[r]] = (w[r][:, None] * np.maximum(a, 0.0)).sum(axis=0)
+    return out
+
+
+def brute_topk(vals, n, k):
+    v = np.asarray(vals[:n], dtype=np.float64)
+    order = np.lexsort((np.arange(n), -v))
+    sel = np.sort(order[:min(k, n)]).astype(np.int32)
+    return np.concatenate([sel, -np.ones(k - len(sel), dtype=np.int32)])
+
+
+def dense_attention(q, kv, sm_scale):
+    """q [H,576], kv [n,576] -> (O [H,512], lse [H]) with numpy softmax."""
+    s = (q @ kv.T) * sm_scale
+    m = s.max(axis=1, keepdims=True)
+    p = np.exp(s - m)
+    l = p.sum(axis=1, keepdims=True)
+    return (p / l) @ kv[:, :512], (m + np.log(l))[:, 0]
+
+
+def _tiny(fmt_key=I.KEY_FP8, fmt_lat=I.LATENT_FP8, ctx=(150, 77), rows=1, heads=8, seed=3):
+    wl = I.small_workload("tiny", list(ctx), rows_per_req=rows, rows_per_group=rows, key_fmt=fmt_key,
+                          lat_fmt=fmt_lat, k=64, heads=heads, seed=seed)
+    return I.make_inputs(wl)
+
+
+# -------------------------------------------------------------------- pins
+
+def pin_e4m3(lib):
+    ref = ref_e4m3(np.arange(256, dtype=np.uint8))
+    got = np.array([oracle.e4m3_decode(c, lib) for c in range(256)])
+    assert np.array_equal(np.isnan(got), np.isnan(ref)), "e4m3 NaN codes"
+    ok = ~np.isnan(ref)
+    assert np.array_equal(got[ok], ref[ok]), "e4m3 values"
+    assert np.array_equal(np.signbit(got[ok]), np.signbit(ref[ok])), "e4m3 signs"
+
+
+def pin_e2m1(lib):
+    got = np.array([oracle.e2m1_decode(c, lib) for c in range(16)])
+    assert np.array_equal(got, E2M1) and np.array_equal(np.signbit(got), np.signbit(E2M1)), "e2m1 table"
+
+
+def pin_e8m0(lib):
+    for code, val in _golden("e8m0_semantics.txt"):
+        got = oracle.e8m0_decode(int(code, 16), lib)
+        if val == "nan":
+            assert math.isnan(got), code
+        else:
+            assert got == 2.0 ** int(val), (code, got)
+    allc = np.array([oracle.e8m0_decode(c, lib) for c in range(256)])
+    ref = ref_e8m0(np.arange(256))
+    assert np.array_equal(np.isnan(allc), np.isnan(ref)) and np.array_equal(allc[:255], ref[:255])
+
+
+def pin_bf16(lib):
+    rng = np.random.default_rng(5)
+    bits = np.concatenate([rng.integers(0, 1 << 16, 2000), [0, 0x8000, 0x3F80, 0x7F7F, 0x0001]]).astype(np.uint16)
+    ref = ref_bf16(bits)
+    got = np.array([oracle.bf16_decode(int(b), lib) for b in bits])
+    ok = ~np.isnan(ref)
+    assert np.array_equal(got[ok], ref[ok]) and np.array_equal(np.isnan(got), np.isnan(ref))
+
+
+def pin_byte_widths(lib):
+    g = {k: float(v) for k, v in _golden("byte_widths.txt")}
+    assert oracle.index_page_bytes(oracle.KEY_FP8, lib) == 64 * g["index_fp8"]
+    assert oracle.index_page_bytes(oracle.KEY_MXFP4, lib) == 64 * g["index_mxfp4"]
+    assert oracle.latent_page_bytes(oracle.LATENT_FP8, lib) == 64 * g["latent_fp8"]
+    assert oracle.latent_page_bytes(oracle.LATENT_NVFP4, lib) == 64 * g["latent_nvfp4"]
+    # the generator's layouts agree with the oracle's
+    assert I.index_page_bytes(I.KEY_FP8) == oracle.index_page_bytes(oracle.KEY_FP8, lib)
+    assert I.index_page_bytes(I.KEY_MXFP4) == oracle.index_page_bytes(oracle.KEY_MXFP4, lib)
+    assert I.latent_page_bytes(I.LATENT_FP8) == oracle.latent_page_bytes(oracle.LATENT_FP8, lib)
+    assert I.latent_page_bytes(I.LATENT_NVFP4) == oracle.latent_page_bytes(oracle.LATENT_NVFP4, lib)
+    # derived figures: MXFP4 saving and the long-context DSA byte fraction
+    assert round(100 * (1 - g["index_mxfp4"] / g["index_fp8"]), 1) == g["mxfp4_index_saving_pct"]
+    L = 1 << 30
+    frac = (g["index_fp8"] * L + g["latent_fp8"] * 2048) / (g["latent_fp8"] * L)
+    assert round(100 * frac) == g["dsa_fraction_long_ctx_pct"]
+    # 2048 candidates: 8 B (fp32 score + int32 id) vs 4 B (score only)
+    assert g["candidates"] * 8 / 1024 == g["candidate_exchange_kib_before"]
+    assert g["candidates"] * 4 / 1024 == g["candidate_exchange_kib_after"]
+
+
+def pin_indexer_bruteforce(lib, fmt=I.KEY_FP8):
+    inp = _tiny(fmt_key=fmt, ctx=(150, 77, 64, 1), seed=11)
+    got = oracle.indexer_logits(inp.np("idx_pool"), fmt, inp.np("block_table"), inp.np("row_req"),
+                                inp.np("row_ctx"), inp.np("q_idx"), inp.np("head_w"), lib=lib)
+    ref = brute_logits(inp)
+    assert np.array_equal(np.isnan(got), np.isnan(ref)), "causal extent"
+    ok = ~np.isnan(ref)
+    np.testing.assert_allclose(got[ok], ref[ok], rtol=1e-12, atol=0)
+
+
+def pin_indexer_special_cases(lib):
+    inp = _tiny(ctx=(200,), seed=12)
+    w = np.zeros((1, 32), dtype=np.float32)
+    w[0, 5] = 1.0
+    got = oracle.indexer_logits(inp.np("idx_pool"), 1, inp.np("block_table"), inp.np("row_req"),
+                                inp.np("row_ctx"), inp.np("q_idx"), w, lib=lib)[0]
+    t = np.arange(200)
+    slots = inp.np("block_table")[0, t // 64].astype(np.int64) * 64 + t % 64
+    k, s = ref_index_keys(inp.np("idx_pool"), 1, slots)
+    q5 = ref_e4m3(inp.np("q_idx")[0, 5])
+    assert np.array_equal(got, np.maximum(s * (k @ q5), 0.0)), "one-hot head weight"
+    # negating the query flips every dot: relu keeps exactly the other half
+    q_neg = inp.np("q_idx").copy() ^ np.uint8(0x80)
+    got_n = oracle.indexer_logits(inp.np("idx_pool"), 1, inp.np("block_table"), inp.np("row_req"),
+                                  inp.np("row_ctx"), q_neg, w, lib=lib)[0]
+    assert np.array_equal(got_n, np.maximum(-s * (k @ q5), 0.0)), "sign of the dot"
+    assert np.all((got == 0) | (got_n == 0)), "relu: a dot and its negation cannot both survive"
+
+
+def pin_indexer_paging_invariance(lib):
+    a = _tiny(ctx=(300, 130), seed=13)
+    # same values, different physical pages: rebuild the pools under a permutation
+    perm = np.random.default_rng(1).permutation(a.num_pages).astype(np.int32)
+    inv = np.argsort(perm)
+    pool_b = a.np("idx_pool")[inv]           # page p moves to perm[p]
+    bt_b = perm[a.np("block_table")]
+    la = oracle.indexer_logits(a.np("idx_pool"), 1, a.np("block_table"), a.np("row_req"), a.np("row_ctx"),
+                               a.np("q_idx"), a.np("head_w"), lib=lib)
+    lb = oracle.indexer_logits(pool_b, 1, bt_b, a.np("row_req"), a.np("row_ctx"), a.np("q_idx"),
+                               a.np("head_w"), lib=lib)
+    assert np.array_equal(la, lb, equal_nan=True), "paging invariance"
+
+
+def pin_topk(lib):
+    rng = np.random.default_rng(21)
+    n_rows, width, k = 6, 500, 64
+    vals = rng.integers(-20, 20, size=(n_rows, width)).astype(np.float32) / 4  # many ties
+    vals[1] = 0.0
+    vals[1, ::7] = -0.0                                                        # signed zeros tie
+    ctx = np.array([500, 500, 64, 63, 1, 0], dtype=np.int32)
+    got = oracle.topk_f32(vals, ctx, k, lib=lib)
+    for r in range(n_rows):
+        assert np.array_equal(got[r], brute_topk(vals[r], ctx[r], k)), r
+    assert np.array_equal(got[1], np.arange(k)), "ties go to the lower index"
+    assert np.array_equal(got[3, :63], np.arange(63)) and np.all(got[3, 63:] == -1), "k >= L returns all"
+    got64 = oracle.topk_f64(vals.astype(np.float64), ctx, k, lib=lib)
+    assert np.array_equal(got, got64)
+
+
+def pin_page_to_slot(lib):
+    bt = np.array([[5, 2, 9], [7, 0, 3]], dtype=np.int32)
+    idx = np.array([[0, 63, 64, 130, -1], [1, 70, 191, -1, -1]], dtype=np.int32)
+    got = oracle.page_to_slot(bt, np.array([0, 1], dtype=np.int32), idx, lib=lib)
+    want = np.array([[320, 383, 128, 578, -1], [449, 6, 255, -1, -1]], dtype=np.int32)
+    assert np.array_equal(got, want)
+
+
+def _mla_case(lib, fmt=I.LATENT_FP8, seed=31, n_sel=40, heads=8):
+    inp = _tiny(fmt_lat=fmt, ctx=(150,), heads=heads, seed=seed)
+    rng = np.random.default_rng(seed)
+    t = np.sort(rng.choice(150, size=n_sel, replace=False))
+    slots = inp.np("block_table")[0, t // 64].astype(np.int64) * 64 + t % 64
+    sl = np.full((1, 64), -1, dtype=np.int32)
+    sl[0, :n_sel] = slots
+    return inp, sl, slots
+
+
+def pin_mla_dense_restricted(lib, fmt=I.LATENT_FP8):
+    inp, sl, slots = _mla_case(lib, fmt)
+    sm = 1 / math.sqrt(192)
+    out, lse = oracle.sparse_mla(inp.np("lat_pool"), fmt, inp.tensor_scale, inp.np("q_mla"), sl, sm, lib=lib)
+    kv = ref_latents(inp.np("lat_pool"), fmt, inp.tensor_scale, slots)
+    o_ref, lse_ref = dense_attention(ref_bf16(inp.np("q_mla")[0]), kv, sm)
+    np.testing.assert_allclose(out[0], o_ref, rtol=1e-9, atol=1e-12)
+    np.testing.assert_allclose(lse[0], lse_ref, rtol=1e-12, atol=1e-12)
+
+
+def pin_mla_full_selection_is_dense_causal(lib):
+    # k >= L: the selection is every visible token -> dense causal MLA
+    inp = _tiny(ctx=(100,), heads=4, seed=33)
+    logits = oracle.indexer_logits(inp.np("idx_pool"), 1, inp.np("block_table"), inp.np("row_req"),
+                                   inp.np("row_ctx"), inp.np("q_idx"), inp.np("head_w"), lib=lib)
+    idx = oracle.topk_f64(logits, inp.np("row_ctx"), 128, lib=lib)
+    assert np.array_equal(idx[0, :100], np.arange(100)) and np.all(idx[0, 100:] == -1)
+    sl = oracle.page_to_slot(inp.np("block_table"), inp.np("row_req"), idx, lib=lib)
+    sm = 1 / math.sqrt(192)
+    out, _ = oracle.sparse_mla(inp.np("lat_pool"), 3, inp.tensor_scale, inp.np("q_mla"), sl, sm, lib=lib)
+    t = np.arange(100)
+    slots = inp.np("block_table")[0, t // 64].astype(np.int64) * 64 + t % 64
+    kv = ref_latents(inp.np("lat_pool"), 3, inp.tensor_scale, slots)
+    o_ref, _ = dense_attention(ref_bf16(inp.np("q_mla")[0]), kv, sm)
+    np.testing.assert_allclose(out[0], o_ref, rtol=1e-9, atol=1e-12)
+
+
+def pin_mla_closed_forms(lib):
+    inp, sl, slots = _mla_case(lib, seed=35)
+    sm = 1 / math.sqrt(192)
+    kv = ref_latents(inp.np("lat_pool"), 3, inp.tensor_scale, slots)
+    one = np.full_like(sl, -1)
+    one[0, 0] = sl[0, 3]
+    out, lse = oracle.sparse_mla(inp.np("lat_pool"), 3, inp.tensor_scale, inp.np("q_mla"), one, sm, lib=lib)
+    assert np.array_equal(out[0], np.broadcast_to(kv[3, :512], out[0].shape)), "single token -> its latent"
+    s3 = ref_bf16(inp.np("q_mla")[0]) @ kv[3] * sm
+    np.testing.assert_allclose(lse[0], s3, rtol=1e-12, atol=1e-12)
+    zq = np.zeros_like(inp.np("q_mla"))
+    out, lse = oracle.sparse_mla(inp.np("lat_pool"), 3, inp.tensor_scale, zq, sl, sm, lib=lib)
+    np.testing.assert_allclose(out[0], np.broadcast_to(kv[:, :512].mean(axis=0), out[0].shape), rtol=1e-12,
+                               atol=1e-14)
+    np.testing.assert_allclose(lse[0], np.log(len(slots)), rtol=1e-12)
+    empty = np.full_like(sl, -1)
+    out, lse = oracle.sparse_mla(inp.np("lat_pool"), 3, inp.tensor_scale, inp.np("q_mla"), empty, sm, lib=lib)
+    assert np.all(out == 0) and np.all(np.isneginf(lse)), "empty selection"
+
+
+def pin_mla_invariances(lib):
+    inp, sl, slots = _mla_case(lib, seed=37, heads=6)
+    sm = 1 / math.sqrt(192)
+    q = inp.np("q_mla")
+    out, lse = oracle.sparse_mla(inp.np("lat_pool"), 3, inp.tensor_scale, q, sl, sm, lib=lib)
+    # head padding: adding heads leaves the original heads bit-identical
+    qpad = np.concatenate([q, np.zeros((1, 2, 576), dtype=np.uint16)], axis=1)
+    out_p, lse_p = oracle.sparse_mla(inp.np("lat_pool"), 3, inp.tensor_scale, qpad, sl, sm, lib=lib)
+    assert np.array_equal(out_p[:, :6], out) and np.array_equal(lse_p[:, :6], lse)
+    # selection order does not matter (up to rounding)
+    perm = sl.copy()
+    perm[0, :len(slots)] = sl[0, :len(slots)][::-1]
+    out_r, _ = oracle.sparse_mla(inp.np("lat_pool"), 3, inp.tensor_scale, q, perm, sm, lib=lib)
+    np.testing.assert_allclose(out_r, out, rtol=1e-12, atol=1e-13)
+
+
+ALL_PINS = {
+    "e4m3": pin_e4m3,
+    "e2m1": pin_e2m1,
+    "e8m0": pin_e8m0,
+    "bf16": pin_bf16,
+    "byte_widths": pin_byte_widths,
+    "indexer_fp8": pin_indexer_bruteforce,
+    "indexer_mxfp4": lambda lib: pin_indexer_bruteforce(lib, I.KEY_MXFP4),
+    "indexer_special": pin_indexer_special_cases,
+    "indexer_paging": pin_indexer_paging_invariance,
+    "topk": pin_topk,
+    "page_to_slot": pin_page_to_slot,
+    "mla_dense_fp8": pin_mla_dense_restricted,
+    "mla_dense_nvfp4": lambda lib: pin_mla_dense_restricted(lib, I.LATENT_NVFP4),
+    "mla_full_selection": pin_mla_full_selection_is_dense_causal,
+    "mla_closed_forms": pin_mla_closed_forms,
+    "mla_invariances": pin_mla_invariances,
+}
