@@ -1,0 +1,363 @@
+"""Benchmark of one DSA layer step (indexer -> top-k -> slots -> sparse MLA).
+
+Default workload: decode at 128K context, batch 8, FP8 latents (576 B) and
+FP8 index keys (132 B), 96 MLA heads, 32 indexer heads, top-k 2048, page 64.
+Prints ONE JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
+
+value      query-tokens/s of the whole job (inputs resident in HBM)
+e2e        the same through the C ABI with host buffers: pinned host -> device
+           copies of the step's queries and metadata and device -> host copies of
+           the outputs inside the timed region
+roofline   the indexer (the dominant kernel): algorithmic bytes per launch /
+           its CUDA-event time, against the measured HBM copy bandwidth
+cpu_baseline  the CPU oracle on a bounded sample of the same workload
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+METRIC = "DSA decode query-tokens/s per layer at 128K ctx; achieved HBM GB/s vs ~8 TB/s"
+UNIT = "query-tokens/s"
+FALLBACK_HBM_GBS = 6800.0
+ROTATE = 4  # independent copies of the caches; a step never re-reads what the last 3 steps read
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d.get("hbm_gbs", FALLBACK_HBM_GBS)), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index, self.proc, self.lines = index, None, []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except (FileNotFoundError, OSError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) != 6:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[2:]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def indexer_algorithmic_bytes(wl, token_bytes: int) -> int:
+    """Bytes the indexer must move per launch: every cached key of every row group once
+    (132 B/token FP8), the block-table entries, the queries and head weights, and the
+    fp32 logits it writes."""
+    R = wl.num_rows
+    rc = wl.row_ctx()
+    groups = R // wl.rows_per_group
+    gmax = [int(rc[g * wl.rows_per_group:(g + 1) * wl.rows_per_group].max()) for g in range(groups)]
+    keys = sum(token_bytes * L + 4 * ((L + 63) // 64) for L in gmax)
+    return keys + R * (32 * 128 + 32 * 4) + 4 * int(rc.sum())
+
+
+def layer_algorithmic_bytes(wl, idx_bytes: int, lat_bytes: int) -> int:
+    """The method's own traffic for one layer step: index keys once per row group, the
+    selected latents (min(L, k) per row; union over a group's rows is approximated by the
+    largest row), queries, outputs and block-table entries.  Logits and indices are
+    implementation overhead and are not counted."""
+    rc = wl.row_ctx()
+    G = wl.rows_per_group
+    tot = 0
+    for g in range(wl.num_rows // G):
+        Lg = int(rc[g * G:(g + 1) * G].max())
+        tot += idx_bytes * Lg + 4 * ((Lg + 63) // 64) + lat_bytes * min(Lg, wl.k)
+    R = wl.num_rows
+    tot += R * (32 * 128 + 32 * 4)          # indexer query + head weights
+    tot += R * wl.heads * 576 * 2           # MLA query (bf16)
+    tot += R * wl.heads * (512 + 1) * 4     # output + lse (fp32)
+    return tot
+
+
+def run_reference(args, wl, rank):
+    """CPU oracle on a bounded sample of the workload (rows of one step)."""
+    import oracle
+    from prefill_dsa_indexer_gb300 import inputs as I
+    sample_rows = int(os.environ.get("DSA_BENCH_ORACLE_ROWS", "2"))
+    inp = I.make_inputs(wl, device="cuda" if torch.cuda.is_available() else "cpu")
+    host = {n: inp.np(n) for n in ("idx_pool", "lat_pool", "block_table", "row_req", "row_ctx", "q_idx", "head_w",
+                                    "q_mla")}
+    rows = np.arange(min(sample_rows, wl.num_rows))
+
+    def step():
+        lg = oracle.indexer_logits(host["idx_pool"], wl.key_fmt, host["block_table"], host["row_req"][rows],
+                                   host["row_ctx"][rows], host["q_idx"][rows], host["head_w"][rows])
+        idx = oracle.topk_f64(lg, host["row_ctx"][rows], wl.k)
+        sl = oracle.page_to_slot(host["block_table"], host["row_req"][rows], idx)
+        oracle.sparse_mla(host["lat_pool"], 3 if wl.lat_fmt == 3 else 4, inp.tensor_scale, host["q_mla"][rows], sl,
+                          1.0 / np.sqrt(192.0))
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = time.perf_counter() - t0
+    value = len(rows) * args.steps / dt
+    cores = oracle.num_threads()
+    sample = f"{len(rows)} of {wl.num_rows} query rows per step of {wl.name} (full indexer scan, top-k, MLA per row)"
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * dt / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": wl.name, "rows": wl.num_rows, "ctx": wl.ctx[0], "k": wl.k, "heads": wl.heads},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def cpu_baseline(wl, inp, budget_s=20.0):
+    """Time the oracle on whole rows of the workload until ~budget_s of CPU work."""
+    import oracle
+    host = {n: inp.np(n) for n in ("idx_pool", "lat_pool", "block_table", "row_req", "row_ctx", "q_idx", "head_w",
+                                    "q_mla")}
+    threads = oracle.num_threads()
+    done, t_used, n = 0, 0.0, max(1, min(threads, wl.num_rows))
+    while t_used < budget_s and done < wl.num_rows:
+        rows = np.arange(done, min(wl.num_rows, done + n))
+        t0 = time.perf_counter()
+        lg = oracle.indexer_logits(host["idx_pool"], wl.key_fmt, host["block_table"], host["row_req"][rows],
+                                   host["row_ctx"][rows], host["q_idx"][rows], host["head_w"][rows])
+        idx = oracle.topk_f64(lg, host["row_ctx"][rows], wl.k)
+        sl = oracle.page_to_slot(host["block_table"], host["row_req"][rows], idx)
+        oracle.sparse_mla(host["lat_pool"], wl.lat_fmt, inp.tensor_scale, host["q_mla"][rows], sl,
+                          1.0 / np.sqrt(192.0))
+        t_used += time.perf_counter() - t0
+        done += len(rows)
+    return {"value": done / t_used, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": f"{done} of {wl.num_rows} query rows of {wl.name} (full indexer scan, top-k, MLA), "
+                      f"{t_used:.1f} s"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="decode_b8_128k_fp8")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    assert args.warmup >= 3 or args.impl == "reference", "at least 3 warm-up steps"
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if args.impl == "ours" else "gloo")
+
+    from prefill_dsa_indexer_gb300 import inputs as I
+    wl = I.workload(args.workload)
+
+    if args.impl == "reference":
+        if rank == 0:
+            run_reference(args, wl, rank)
+        if dist is not None:
+            dist.destroy_process_group()
+        return
+
+    torch.cuda.set_device(local)
+    import __graft_entry__
+    __graft_entry__.build()
+    import prefill_dsa_indexer_gb300 as P
+
+    inp = I.make_inputs(wl, device="cuda")
+    prefill = wl.rows_per_group == 8 and wl.rows_per_req > 8
+    layers = []
+    for c in range(ROTATE):
+        idx_pool = inp.idx_pool if c == 0 else inp.idx_pool.clone()
+        lat_pool = inp.lat_pool if c == 0 else inp.lat_pool.clone()
+        layers.append(P.Layer(idx_pool, wl.key_fmt, lat_pool, wl.lat_fmt, inp.tensor_scale, inp.block_table,
+                              inp.max_ctx, wl.num_rows, wl.heads, wl.k, wl.rows_per_group, prefill=prefill))
+    stream = torch.cuda.current_stream()
+
+    def step(i, ev=None):
+        L = layers[i % ROTATE]
+        if ev is not None:
+            ev[0].record(stream)
+        P.indexer_logits(L.idx_pool, L.key_fmt, L.block_table, inp.row_req, inp.row_ctx, L.max_ctx, inp.q_idx,
+                         inp.head_w, L.rows_per_group, logits=L.logits, status=L.status, stream=stream)
+        if ev is not None:
+            ev[1].record(stream)
+        P.topk(L.logits, inp.row_ctx, L.max_ctx, L.k, out=L.idx, status=L.status, stream=stream)
+        P.page_to_slot(L.block_table, inp.row_req, inp.row_ctx, L.max_ctx, L.lat_pool.shape[0], L.idx, out=L.slots,
+                       status=L.status, stream=stream)
+        if L.prefill:
+            P.sparse_mla_prefill(L.lat_pool, L.lat_fmt, L.tensor_scale, inp.q_mla, L.slots, L.sm_scale, out=L.out,
+                                 lse=L.lse, status=L.status, stream=stream)
+        else:
+            P.sparse_mla_decode(L.lat_pool, L.lat_fmt, L.tensor_scale, inp.q_mla, L.slots, L.sm_scale, out=L.out,
+                                lse=L.lse, workspace=L.workspace, status=L.status, stream=stream)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    for L in layers:
+        P.check_status(L.status, "warm-up")
+
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    t_start, t_stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        t_start.record(stream)
+        for i in range(args.steps):
+            step(i, evs[i])
+        t_stop.record(stream)
+        torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    total_ms = t_start.elapsed_time(t_stop)
+    idx_ms = sum(a.elapsed_time(b) for a, b in evs) / args.steps
+    for L in layers:
+        P.check_status(L.status, "timed steps")
+    if dist is not None:
+        t = torch.tensor([total_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    value = world * wl.num_rows * args.steps / (total_ms / 1000.0)
+
+    # ---- end to end through the C ABI with host buffers
+    pinned = {n: getattr(inp, n).cpu().pin_memory() for n in ("row_req", "row_ctx", "q_idx", "head_w", "q_mla")}
+    dev_in = {n: torch.empty_like(getattr(inp, n)) for n in pinned}
+    host_out = torch.empty(layers[0].out.shape, dtype=torch.float32).pin_memory()
+    host_lse = torch.empty(layers[0].lse.shape, dtype=torch.float32).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in pinned.values())
+    d2h = host_out.numel() * 4 + host_lse.numel() * 4
+
+    def e2e_step(i):
+        L = layers[i % ROTATE]
+        for n, t in pinned.items():
+            dev_in[n].copy_(t, non_blocking=True)
+        L.run(dev_in["row_req"], dev_in["row_ctx"], dev_in["q_idx"], dev_in["head_w"], dev_in["q_mla"],
+              stream=stream)
+        host_out.copy_(L.out, non_blocking=True)
+        host_lse.copy_(L.lse, non_blocking=True)
+
+    for i in range(args.warmup):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(args.steps):
+        e2e_step(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    if dist is not None:
+        t = torch.tensor([e2e_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    for L in layers:
+        P.check_status(L.status, "e2e steps")
+    e2e_value = world * wl.num_rows * args.steps / (e2e_ms / 1000.0)
+
+    idx_tok = I.INDEX_TOKEN_BYTES[wl.key_fmt]
+    lat_tok = I.LATENT_TOKEN_BYTES[wl.lat_fmt]
+    idx_bytes = indexer_algorithmic_bytes(wl, idx_tok)
+    layer_bytes = layer_algorithmic_bytes(wl, idx_tok, lat_tok)
+    peak, peak_kind = _peaks()
+    achieved = idx_bytes / (idx_ms / 1000.0) / 1e9
+    traffic = None
+    tfile = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(tfile):
+        with open(tfile) as f:
+            traffic = json.load(f).get(wl.name)
+    launches_per_step = 5 if not prefill else 4  # indexer, top-k, slots, MLA (+ split merge in decode)
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "e4m3xe4m3->f32 (indexer), f16xf16->f32 (mla)", "data": "synthetic",
+        "config": {"workload": wl.name, "batch": len(wl.ctx), "rows": wl.num_rows, "ctx": wl.ctx[0], "k": wl.k,
+                   "heads": wl.heads, "index_heads": 32, "page": 64, "key_bytes": idx_tok, "latent_bytes": lat_tok,
+                   "parallelism": f"replicas{world}" if world > 1 else "single-gpu",
+                   "l2": f"inputs > L2: {ROTATE} rotating copies of the caches "
+                         f"({(inp.idx_pool.numel() + inp.lat_pool.numel()) * ROTATE / 1e9:.2f} GB)"},
+        "layer_hbm_gbs": layer_bytes / (ms_per_step / 1000.0) / 1e9,
+        "layer_algorithmic_bytes": layer_bytes,
+        "layer_frac_of_8tbs": layer_bytes / (ms_per_step / 1000.0) / 8e12,
+        "roofline": {"kernel": "indexer_fp8_kernel", "bound": "hbm", "achieved": achieved, "peak": peak,
+                     "unit": "GB/s", "frac": achieved / peak, "peak_kind": peak_kind, "traffic": traffic,
+                     "algorithmic_bytes": idx_bytes, "ms_per_launch": idx_ms},
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": e2e_ms / args.steps},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk.summary(),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(wl, inp)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,206 @@
+/*
+ * dsa.h -- C ABI of libdsa, a single-GPU (sm_103a) implementation of the
+ * DeepSeek-style sparse attention (DSA) layer as used in Kimi K3.1 Pro.
+ *
+ * The layer (vLLM blog "Day-0 support for Kimi K3.1 Pro", section "Sparse
+ * attention in K3.1 Pro", Fig. 1): for every query row a small indexer with
+ * 32 FP8 heads scores every earlier token against that token's FP8 index key
+ * (132 B with its scale); a top-k step keeps the 2,048 best tokens; exact
+ * absorbed-MLA attention of 96 query heads then runs over only those tokens'
+ * 576-byte latents (512 latent + 64 RoPE dims).  Both caches are paged and
+ * are read through a block table that is translated to physical slots
+ * before the attention step (section "One KV cache, three states"; in the
+ * fused decode path the scorer and the top-k hand attention the physical
+ * cache rows to read, section "Low-latency decode: fused DSA decode path").
+ *
+ * Conventions shared by every entry point
+ *   - Every pointer argument is a DEVICE pointer owned by the caller, unless
+ *     its comment says "host".  Struct arguments themselves are host memory
+ *     and are read only during the call.  The library allocates no device
+ *     memory and keeps no state between calls (per-device tensor-map encoder
+ *     lookup aside).
+ *   - `stream` is a cudaStream_t passed as void*; NULL means the legacy
+ *     default stream.  Every call only enqueues work and returns; nothing
+ *     synchronises with the host.
+ *   - The int return value is a host-side status: arguments are checked
+ *     before anything is launched, and a launch error is reported as
+ *     DSA_ERR_CUDA.  No exceptions cross the boundary.
+ *   - Errors the kernels find in device data (a page id outside the pool, a
+ *     context longer than max_ctx, a timed-out wait) are written to the
+ *     optional `dev_status` word (int32, device memory): the first error
+ *     code is kept (compare-and-swap from 0), later ones are dropped.  The
+ *     caller zeroes it before the calls and reads it after synchronising.
+ *     Outputs of a call that reported a device error are unspecified.
+ *   - Results are deterministic, and a row's results do not depend on the
+ *     other rows of the batch (batch invariance).
+ *
+ * Cache page layouts (page_size 64; the per-token widths are the blog's,
+ * "One KV cache, three states": index key 132 B FP8 / 68 B MXFP4, latent
+ * 576 B FP8 / 352 B NVFP4; the arrangement within a page is this library's):
+ *   DSA_KEY_FP8      [64 x 128 B e4m3 key][64 x fp32 per-token scale]   8448 B
+ *   DSA_KEY_MXFP4    [64 x 64 B e2m1 pairs][64 x 4 B e8m0, one per 32]  4352 B
+ *   DSA_LATENT_FP8   [64 x 576 B e4m3], scale = dsa_cache.tensor_scale 36864 B
+ *   DSA_LATENT_NVFP4 [64 x 256 B e2m1 pairs][64 x 32 B e4m3 scale, one per 16]
+ *                    [64 x 64 B e4m3 RoPE dims, scale = tensor_scale]   22528 B
+ * e2m1 pairs hold element 2j in the low nibble.  Token t of a request lives
+ * in page block_table[req][t / 64], row t % 64; its physical slot is
+ * page * 64 + t % 64, the same slot id in the index and the latent pool.
+ */
+#ifndef DSA_H_
+#define DSA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes */
+#define DSA_OK 0
+#define DSA_ERR_INVALID_ARG (-1)  /* host: null pointer, bad size or stride */
+#define DSA_ERR_UNSUPPORTED (-2)  /* host: format, page size, head count or k not supported */
+#define DSA_ERR_CUDA (-3)         /* host: a CUDA call or launch failed */
+#define DSA_ERR_WORKSPACE (-4)    /* host: workspace smaller than dsa_*_workspace_size() */
+#define DSA_ERR_TIMEOUT (-5)      /* device: a bounded wait inside a kernel gave up */
+#define DSA_ERR_BOUNDS (-6)       /* device: page id, slot or context outside its range */
+#define DSA_ERR_RANGE (-7)        /* device: a value the kernel cannot represent (e.g. |q| > 65504) */
+
+/* ---- cache formats */
+#define DSA_KEY_FP8 1
+#define DSA_KEY_MXFP4 2
+#define DSA_LATENT_FP8 3
+#define DSA_LATENT_NVFP4 4
+
+/* ---- fixed dimensions of the layer */
+#define DSA_PAGE_SIZE 64
+#define DSA_INDEX_HEADS 32
+#define DSA_INDEX_DIM 128
+#define DSA_LATENT_DIM 576 /* 512 latent + 64 RoPE dims */
+#define DSA_VALUE_DIM 512
+#define DSA_MAX_HEADS 128  /* MLA query heads per row, multiple of 16 */
+#define DSA_MAX_TOPK 2048
+
+/* One paged cache pool (index keys or latents). */
+typedef struct dsa_cache {
+    const void *base;     /* device, num_pages * page bytes, 16-byte aligned */
+    int32_t format;       /* DSA_KEY_* for an index pool, DSA_LATENT_* for a latent pool */
+    int32_t page_size;    /* must be DSA_PAGE_SIZE */
+    int64_t num_pages;
+    float tensor_scale;   /* latent pools: per-tensor scale of the e4m3 codes; ignored for index pools */
+} dsa_cache;
+
+/* Query rows and their addressing. */
+typedef struct dsa_rows {
+    const int32_t *block_table; /* device [num_requests, bt_stride] physical page ids */
+    int64_t bt_stride;          /* entries per request, >= ceil(max_ctx / 64) */
+    int32_t num_requests;       /* rows of block_table; row_req outside [0, num_requests) is DSA_ERR_BOUNDS */
+    const int32_t *row_req;     /* device [num_rows] request of each row */
+    const int32_t *row_ctx;     /* device [num_rows] visible tokens L_r (positions 0..L_r-1, incl. itself) */
+    int32_t num_rows;
+    int32_t max_ctx;            /* host bound on every row_ctx; larger values are DSA_ERR_BOUNDS */
+    int32_t rows_per_group;     /* 1, 2, 4 or 8: consecutive rows of one request that the indexer
+                                   scores against one read of the keys (speculative-verify rows,
+                                   prefill query blocks); num_rows must be a multiple of it */
+} dsa_rows;
+
+/*
+ * Indexer logits (blog section "Sparse attention in K3.1 Pro"; the weighted,
+ * fp32-accumulated reduction across heads is the AMD section "Quantization:
+ * native MXFP4 indexer"; the query carries no scale because the head
+ * weights are folded into its quantisation, section "Low-latency decode:
+ * fused DSA decode path"):
+ *
+ *   logits[r * logits_stride + t] = sum_{h<32} head_w[r,h] * max(0, s_t * <q_idx[r,h,:], k_t>)
+ *   for 0 <= t < row_ctx[r]
+ *
+ * k_t is token t's decoded key (e4m3 codes with s_t its fp32 scale, or
+ * MXFP4 e2m1 * 2^(e8m0-127) with s_t = 1).  q_idx: [num_rows, 32, 128] e4m3
+ * codes (16-byte aligned); head_w: [num_rows, 32] fp32; logits: fp32 with
+ * row stride logits_stride >= max_ctx.  Entries at t >= row_ctx[r] are not
+ * written.  Products are exact and accumulate in fp32 on the tensor cores,
+ * so a logit differs from an exact evaluation by accumulation rounding only.
+ */
+int dsa_indexer_logits(const dsa_cache *index_cache, const dsa_rows *rows, const uint8_t *q_idx,
+                       const float *head_w, float *logits, int64_t logits_stride, int32_t *dev_status,
+                       void *stream);
+
+/*
+ * Top-k (blog section "Sparse attention in K3.1 Pro": only the 2,048 best
+ * scored tokens are kept; the fused path's selection is exact, section
+ * "Low-latency decode"):
+ *
+ *   idx_out[r, 0..k) = the min(k, row_ctx[r]) positions t < row_ctx[r] with
+ *   the largest logits[r * logits_stride + t], ties broken toward the lower t,
+ *   written in ascending order of t and padded with -1.
+ *
+ * Logits compare as floats (-0 == +0); they must be finite.  k in
+ * [1, DSA_MAX_TOPK].  Exact and deterministic: given identical logits the
+ * result is bit-identical.
+ */
+int dsa_topk(const float *logits, int64_t logits_stride, const int32_t *row_ctx, int32_t num_rows,
+             int32_t max_ctx, int32_t k, int32_t *idx_out, int32_t *dev_status, void *stream);
+
+/*
+ * Page -> slot translation (blog section "One KV cache, three states": the
+ * block table and cache slots are translated to kernel page addresses
+ * before each step):
+ *
+ *   slots[r, i] = block_table[row_req[r]][t / 64] * 64 + t % 64 for t = idx[r, i] >= 0,
+ *   slots[r, i] = -1 for t = -1.
+ *
+ * idx and slots are [num_rows, k] int32.  A position t >= row_ctx[r], or a
+ * page id outside [0, pool_pages) (the page count of the pools the slots
+ * will address), is DSA_ERR_BOUNDS and yields slot -1.
+ */
+int dsa_page_to_slot(const dsa_rows *rows, int64_t pool_pages, const int32_t *idx, int32_t k, int32_t *slots,
+                     int32_t *dev_status, void *stream);
+
+/*
+ * Sparse absorbed MLA (blog section "Sparse attention in K3.1 Pro": MLA
+ * attention runs exactly, but only over the selected tokens; the latent is
+ * both key and value, section "Low-latency decode": absorbed key
+ * projection):
+ *
+ *   S[h, t] = sm_scale * <q[r,h,:], kv_t>                     (576 dims)
+ *   out[r,h,:] = sum_t softmax_t(S[h, .]) * kv_t[0:512]      over t in slots[r, :] with slot >= 0
+ *   lse[r,h] = ln sum_t exp(S[h,t])
+ *
+ * kv_t is the decoded latent of slot t (FP8: e4m3 * tensor_scale; NVFP4:
+ * e2m1 * per-16 e4m3 scale for dims 0..511 and e4m3 * tensor_scale for the
+ * RoPE dims).  q: [num_rows, num_heads, 576] bf16 bits, num_heads a multiple
+ * of 16 and <= 128; slots: [num_rows, k] int32, -1 = unused; out:
+ * [num_rows, num_heads, 512] fp32; lse: [num_rows, num_heads] fp32 or NULL.
+ * A row with no valid slot gets out = 0 and lse = -inf.  The contraction
+ * runs on the tensor cores in fp16 x fp16 -> fp32: latents decode to fp16
+ * exactly, q rounds from bf16 to fp16 (|q| > 65504 is DSA_ERR_RANGE).
+ *
+ * _decode splits each row's k tokens over several CTAs and merges the parts
+ * by log-sum-exp; it needs a workspace of dsa_sparse_mla_workspace_size()
+ * bytes (device, 256-byte aligned).  _prefill runs one CTA per row, needs no
+ * workspace (pass NULL, 0) and suits many rows.  The split is fixed, so both
+ * are batch-invariant; their results differ from each other by rounding.
+ */
+int dsa_sparse_mla_decode(const dsa_cache *latent_cache, const uint16_t *q, int32_t num_heads,
+                          const int32_t *slots, int32_t num_rows, int32_t k, float sm_scale, float *out,
+                          float *lse, int32_t *dev_status, void *workspace, size_t workspace_bytes, void *stream);
+
+int dsa_sparse_mla_prefill(const dsa_cache *latent_cache, const uint16_t *q, int32_t num_heads,
+                           const int32_t *slots, int32_t num_rows, int32_t k, float sm_scale, float *out,
+                           float *lse, int32_t *dev_status, void *workspace, size_t workspace_bytes,
+                           void *stream);
+
+/* Workspace bytes dsa_sparse_mla_decode needs for num_rows rows of k slots. */
+size_t dsa_sparse_mla_workspace_size(int32_t num_rows, int32_t num_heads, int32_t k);
+
+/* Human-readable text of a status code (static storage). */
+const char *dsa_status_string(int status);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int dsa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DSA_H_ */

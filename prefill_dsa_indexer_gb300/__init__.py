@@ -1,0 +1,237 @@
+"""prefill_dsa_indexer_gb300: the DSA sparse-attention layer on one GB300 GPU.
+
+Python binding of libdsa (include/dsa.h).  Every function here only
+marshals torch tensors into pointers and sizes and calls the C ABI of the
+same name; all arithmetic runs in the library's CUDA kernels.  There is no
+CPU fallback: importing the package on a machine without the built library
+raises, and calling it with CPU tensors raises.
+
+The layer (vLLM blog "Day-0 support for Kimi K3.1 Pro", section "Sparse
+attention in K3.1 Pro"): indexer logits over every cached token -> exact
+top-k (2,048) -> page-to-slot translation -> sparse absorbed MLA over the
+selected tokens' latents.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+import torch
+
+from . import inputs  # noqa: F401  (seeded synthetic inputs)
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libdsa.so")
+
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_WORKSPACE, ERR_TIMEOUT, ERR_BOUNDS, ERR_RANGE = \
+    0, -1, -2, -3, -4, -5, -6, -7
+KEY_FP8, KEY_MXFP4, LATENT_FP8, LATENT_NVFP4 = 1, 2, 3, 4
+PAGE_SIZE = 64
+INDEX_HEADS, INDEX_DIM, LATENT_DIM, VALUE_DIM = 32, 128, 576, 512
+DEFAULT_SM_SCALE = 1.0 / math.sqrt(192.0)
+
+
+class DsaError(RuntimeError):
+    pass
+
+
+class _Cache(ctypes.Structure):
+    _fields_ = [("base", ctypes.c_void_p), ("format", ctypes.c_int32), ("page_size", ctypes.c_int32),
+                ("num_pages", ctypes.c_int64), ("tensor_scale", ctypes.c_float)]
+
+
+class _Rows(ctypes.Structure):
+    _fields_ = [("block_table", ctypes.c_void_p), ("bt_stride", ctypes.c_int64), ("num_requests", ctypes.c_int32),
+                ("row_req", ctypes.c_void_p), ("row_ctx", ctypes.c_void_p), ("num_rows", ctypes.c_int32),
+                ("max_ctx", ctypes.c_int32), ("rows_per_group", ctypes.c_int32)]
+
+
+_lib = None
+
+
+def load_library(path: str | None = None):
+    """Load libdsa.so; raises if it has not been built (no fallback)."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise DsaError(f"libdsa.so not found at {p}: build it with prefill_dsa_indexer_gb300.build.build()")
+    lib = ctypes.CDLL(p)
+    P, I32, I64, F = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float
+    lib.dsa_version.restype = ctypes.c_int
+    lib.dsa_status_string.restype = ctypes.c_char_p
+    lib.dsa_status_string.argtypes = [ctypes.c_int]
+    lib.dsa_indexer_logits.restype = ctypes.c_int
+    lib.dsa_indexer_logits.argtypes = [ctypes.POINTER(_Cache), ctypes.POINTER(_Rows), P, P, P, I64, P, P]
+    lib.dsa_topk.restype = ctypes.c_int
+    lib.dsa_topk.argtypes = [P, I64, P, I32, I32, I32, P, P, P]
+    lib.dsa_page_to_slot.restype = ctypes.c_int
+    lib.dsa_page_to_slot.argtypes = [ctypes.POINTER(_Rows), I64, P, I32, P, P, P]
+    for name in ("dsa_sparse_mla_decode", "dsa_sparse_mla_prefill"):
+        fn = getattr(lib, name)
+        fn.restype = ctypes.c_int
+        fn.argtypes = [ctypes.POINTER(_Cache), P, I32, P, I32, I32, F, P, P, P, P, ctypes.c_size_t, P]
+    lib.dsa_sparse_mla_workspace_size.restype = ctypes.c_size_t
+    lib.dsa_sparse_mla_workspace_size.argtypes = [I32, I32, I32]
+    if path is None:
+        _lib = lib
+    return lib
+
+
+EXPORTED = ("dsa_version", "dsa_status_string", "dsa_indexer_logits", "dsa_topk", "dsa_page_to_slot",
+            "dsa_sparse_mla_decode", "dsa_sparse_mla_prefill", "dsa_sparse_mla_workspace_size")
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise DsaError("libdsa takes device tensors only")
+    if not t.is_contiguous():
+        raise DsaError("libdsa takes contiguous tensors only")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check(rc: int, what: str):
+    if rc != OK:
+        msg = load_library().dsa_status_string(rc).decode()
+        raise DsaError(f"{what}: {msg} ({rc})")
+
+
+def new_status(device=None) -> torch.Tensor:
+    return torch.zeros(1, dtype=torch.int32, device=device or "cuda")
+
+
+def check_status(status: torch.Tensor, what: str = "device status"):
+    """Synchronise-free read of a device status word (the caller has synchronised)."""
+    v = int(status.item())
+    if v != OK:
+        raise DsaError(f"{what}: {load_library().dsa_status_string(v).decode()} ({v})")
+
+
+def _cache(pool: torch.Tensor, fmt: int, tensor_scale: float = 1.0) -> _Cache:
+    return _Cache(_ptr(pool), fmt, PAGE_SIZE, pool.shape[0], tensor_scale)
+
+
+def _rows(block_table, row_req, row_ctx, max_ctx, rows_per_group=1) -> _Rows:
+    return _Rows(_ptr(block_table), block_table.shape[1], block_table.shape[0], _ptr(row_req), _ptr(row_ctx),
+                 row_ctx.shape[0], int(max_ctx), int(rows_per_group))
+
+
+def indexer_logits(index_pool, key_fmt, block_table, row_req, row_ctx, max_ctx, q_idx, head_w, rows_per_group=1,
+                   logits=None, status=None, stream=None):
+    """dsa_indexer_logits: fp32 logits [R, max_ctx] (t >= row_ctx[r] untouched)."""
+    R = row_ctx.shape[0]
+    if logits is None:
+        logits = torch.empty((R, max(int(max_ctx), 1)), dtype=torch.float32, device=q_idx.device)
+    c, r = _cache(index_pool, key_fmt), _rows(block_table, row_req, row_ctx, max_ctx, rows_per_group)
+    rc = load_library().dsa_indexer_logits(ctypes.byref(c), ctypes.byref(r), _ptr(q_idx), _ptr(head_w),
+                                           _ptr(logits), logits.stride(0), _ptr(status), _stream(stream))
+    _check(rc, "dsa_indexer_logits")
+    return logits
+
+
+def topk(logits, row_ctx, max_ctx, k=2048, out=None, status=None, stream=None):
+    """dsa_topk: int32 [R, k] selected positions, ascending, -1 padded."""
+    R = row_ctx.shape[0]
+    if out is None:
+        out = torch.empty((R, k), dtype=torch.int32, device=logits.device)
+    rc = load_library().dsa_topk(_ptr(logits), logits.stride(0), _ptr(row_ctx), R, int(max_ctx), int(k), _ptr(out),
+                                 _ptr(status), _stream(stream))
+    _check(rc, "dsa_topk")
+    return out
+
+
+def page_to_slot(block_table, row_req, row_ctx, max_ctx, pool_pages, idx, out=None, status=None, stream=None):
+    """dsa_page_to_slot: int32 [R, k] physical slots (-1 stays -1)."""
+    if out is None:
+        out = torch.empty_like(idx)
+    r = _rows(block_table, row_req, row_ctx, max_ctx)
+    rc = load_library().dsa_page_to_slot(ctypes.byref(r), int(pool_pages), _ptr(idx), idx.shape[1], _ptr(out),
+                                         _ptr(status), _stream(stream))
+    _check(rc, "dsa_page_to_slot")
+    return out
+
+
+def sparse_mla_workspace_size(num_rows, num_heads, k) -> int:
+    return int(load_library().dsa_sparse_mla_workspace_size(num_rows, num_heads, k))
+
+
+def _mla(name, lat_pool, lat_fmt, tensor_scale, q, slots, sm_scale, out, lse, workspace, status, stream):
+    R, H, _ = q.shape
+    k = slots.shape[1]
+    if out is None:
+        out = torch.empty((R, H, VALUE_DIM), dtype=torch.float32, device=q.device)
+    if lse is None:
+        lse = torch.empty((R, H), dtype=torch.float32, device=q.device)
+    ws_ptr, ws_bytes = None, 0
+    if name == "dsa_sparse_mla_decode":
+        need = sparse_mla_workspace_size(R, H, k)
+        if workspace is None and need:
+            workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+        if workspace is not None:
+            ws_ptr, ws_bytes = _ptr(workspace), workspace.numel() * workspace.element_size()
+    c = _cache(lat_pool, lat_fmt, tensor_scale)
+    rc = getattr(load_library(), name)(ctypes.byref(c), _ptr(q), H, _ptr(slots), R, k, float(sm_scale), _ptr(out),
+                                       _ptr(lse), _ptr(status), ws_ptr, ws_bytes, _stream(stream))
+    _check(rc, name)
+    return out, lse
+
+
+def sparse_mla_decode(lat_pool, lat_fmt, tensor_scale, q, slots, sm_scale=DEFAULT_SM_SCALE, out=None, lse=None,
+                      workspace=None, status=None, stream=None):
+    """dsa_sparse_mla_decode: (out fp32 [R, H, 512], lse fp32 [R, H]); q is bf16 (or its int16 bits)."""
+    return _mla("dsa_sparse_mla_decode", lat_pool, lat_fmt, tensor_scale, q, slots, sm_scale, out, lse, workspace,
+                status, stream)
+
+
+def sparse_mla_prefill(lat_pool, lat_fmt, tensor_scale, q, slots, sm_scale=DEFAULT_SM_SCALE, out=None, lse=None,
+                       status=None, stream=None):
+    return _mla("dsa_sparse_mla_prefill", lat_pool, lat_fmt, tensor_scale, q, slots, sm_scale, out, lse, None,
+                status, stream)
+
+
+class Layer:
+    """One DSA layer invocation over resident caches: indexer -> top-k -> slots -> sparse MLA.
+
+    Buffers are allocated once per shape and reused, so repeated calls (and
+    CUDA-graph capture of `run`) allocate nothing.
+    """
+
+    def __init__(self, idx_pool, key_fmt, lat_pool, lat_fmt, tensor_scale, block_table, max_ctx, num_rows,
+                 num_heads=96, k=2048, rows_per_group=1, prefill=False, sm_scale=DEFAULT_SM_SCALE, device="cuda"):
+        self.idx_pool, self.key_fmt = idx_pool, key_fmt
+        self.lat_pool, self.lat_fmt, self.tensor_scale = lat_pool, lat_fmt, float(tensor_scale)
+        self.block_table, self.max_ctx, self.k = block_table, int(max_ctx), int(k)
+        self.rows_per_group, self.prefill, self.sm_scale = rows_per_group, prefill, sm_scale
+        R, H = int(num_rows), int(num_heads)
+        self.logits = torch.empty((R, max(self.max_ctx, 1)), dtype=torch.float32, device=device)
+        self.idx = torch.empty((R, self.k), dtype=torch.int32, device=device)
+        self.slots = torch.empty((R, self.k), dtype=torch.int32, device=device)
+        self.out = torch.empty((R, H, VALUE_DIM), dtype=torch.float32, device=device)
+        self.lse = torch.empty((R, H), dtype=torch.float32, device=device)
+        need = 0 if prefill else sparse_mla_workspace_size(R, H, self.k)
+        self.workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=device)
+        self.status = new_status(device)
+
+    def run(self, row_req, row_ctx, q_idx, head_w, q_mla, stream=None):
+        indexer_logits(self.idx_pool, self.key_fmt, self.block_table, row_req, row_ctx, self.max_ctx, q_idx, head_w,
+                       self.rows_per_group, logits=self.logits, status=self.status, stream=stream)
+        topk(self.logits, row_ctx, self.max_ctx, self.k, out=self.idx, status=self.status, stream=stream)
+        page_to_slot(self.block_table, row_req, row_ctx, self.max_ctx, self.lat_pool.shape[0], self.idx,
+                     out=self.slots, status=self.status, stream=stream)
+        if self.prefill:
+            sparse_mla_prefill(self.lat_pool, self.lat_fmt, self.tensor_scale, q_mla, self.slots, self.sm_scale,
+                               out=self.out, lse=self.lse, status=self.status, stream=stream)
+        else:
+            sparse_mla_decode(self.lat_pool, self.lat_fmt, self.tensor_scale, q_mla, self.slots, self.sm_scale,
+                              out=self.out, lse=self.lse, workspace=self.workspace, status=self.status,
+                              stream=stream)
+        return self.out, self.lse

@@ -1,0 +1,236 @@
+// api.cu -- the extern "C" entry points of libdsa declared in include/dsa.h.
+//
+// Each call validates its arguments on the host, encodes the TMA tensor maps
+// it needs, and enqueues its kernels on the caller's stream.  Nothing here
+// allocates device memory or synchronises with the device.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/dsa.h"
+#include "kernels.h"
+
+namespace dsa {
+
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// 2D byte tensor [rows, 128 B] with a [box_rows, 128 B] box, 128-byte swizzle.
+bool encode_rows128(CUtensorMap *map, const void *base, uint64_t rows, uint32_t box_rows) {
+    auto enc = get_encoder();
+    if (enc == nullptr) return false;
+    const cuuint64_t dims[2] = {128, rows};
+    const cuuint64_t strides[1] = {128};
+    const cuuint32_t box[2] = {128, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int check_rows(const dsa_rows *rows) {
+    if (rows == nullptr) return DSA_ERR_INVALID_ARG;
+    if (rows->num_rows < 0 || rows->max_ctx < 0 || rows->num_requests < 0) return DSA_ERR_INVALID_ARG;
+    if (rows->num_rows == 0) return DSA_OK;
+    if (!rows->block_table || !rows->row_req || !rows->row_ctx) return DSA_ERR_INVALID_ARG;
+    const int64_t need_pages = (static_cast<int64_t>(rows->max_ctx) + DSA_PAGE_SIZE - 1) / DSA_PAGE_SIZE;
+    if (rows->bt_stride < need_pages) return DSA_ERR_INVALID_ARG;
+    return DSA_OK;
+}
+
+int launch_status(cudaError_t e) { return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA; }
+
+}  // namespace
+
+int device_sm_count() {
+    static int counts[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (dev < 0 || dev >= 64) return 0;
+    if (counts[dev] == 0) {
+        int n = 0;
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        counts[dev] = n;
+    }
+    return counts[dev];
+}
+
+}  // namespace dsa
+
+using namespace dsa;
+
+extern "C" {
+
+int dsa_version(void) { return 100; }
+
+const char *dsa_status_string(int status) {
+    switch (status) {
+        case DSA_OK: return "ok";
+        case DSA_ERR_INVALID_ARG: return "invalid argument";
+        case DSA_ERR_UNSUPPORTED: return "unsupported configuration";
+        case DSA_ERR_CUDA: return "CUDA error";
+        case DSA_ERR_WORKSPACE: return "workspace too small";
+        case DSA_ERR_TIMEOUT: return "device wait timed out";
+        case DSA_ERR_BOUNDS: return "index out of bounds in device data";
+        case DSA_ERR_RANGE: return "value out of representable range";
+        default: return "unknown status";
+    }
+}
+
+int dsa_indexer_logits(const dsa_cache *index_cache, const dsa_rows *rows, const uint8_t *q_idx,
+                       const float *head_w, float *logits, int64_t logits_stride, int32_t *dev_status,
+                       void *stream) {
+    if (index_cache == nullptr) return DSA_ERR_INVALID_ARG;
+    int rc = check_rows(rows);
+    if (rc != DSA_OK) return rc;
+    if (index_cache->page_size != DSA_PAGE_SIZE) return DSA_ERR_UNSUPPORTED;
+    if (index_cache->format != DSA_KEY_FP8) return DSA_ERR_UNSUPPORTED;
+    const int G = rows->rows_per_group;
+    if (G != 1 && G != 2 && G != 4 && G != 8) return DSA_ERR_UNSUPPORTED;
+    if (rows->num_rows % G != 0) return DSA_ERR_INVALID_ARG;
+    if (rows->num_rows == 0) return DSA_OK;
+    if (!index_cache->base || index_cache->num_pages <= 0 || !q_idx || !head_w || !logits)
+        return DSA_ERR_INVALID_ARG;
+    if (!aligned(index_cache->base, 16) || !aligned(q_idx, 16)) return DSA_ERR_INVALID_ARG;
+    if (logits_stride < rows->max_ctx) return DSA_ERR_INVALID_ARG;
+    const uint64_t pool_rows = static_cast<uint64_t>(index_cache->num_pages) * 66u;
+    if (pool_rows >= (1ull << 31)) return DSA_ERR_UNSUPPORTED;
+    const int sms = device_sm_count();
+    if (sms <= 0) return DSA_ERR_CUDA;
+
+    CUtensorMap key_map, q_map;
+    if (!encode_rows128(&key_map, index_cache->base, pool_rows, DSA_PAGE_SIZE)) return DSA_ERR_CUDA;
+    if (!encode_rows128(&q_map, q_idx, static_cast<uint64_t>(rows->num_rows) * DSA_INDEX_HEADS,
+                        static_cast<uint32_t>(G * DSA_INDEX_HEADS)))
+        return DSA_ERR_CUDA;
+    IndexerArgs a;
+    a.pool = static_cast<const uint8_t *>(index_cache->base);
+    a.num_pages = index_cache->num_pages;
+    a.block_table = rows->block_table;
+    a.bt_stride = rows->bt_stride;
+    a.num_requests = rows->num_requests;
+    a.row_req = rows->row_req;
+    a.row_ctx = rows->row_ctx;
+    a.max_ctx = rows->max_ctx;
+    a.head_w = head_w;
+    a.logits = logits;
+    a.logits_stride = logits_stride;
+    a.status = dev_status;
+    const int num_groups = rows->num_rows / G;
+    for (int g0 = 0; g0 < num_groups; g0 += kIndexerMaxGroups) {
+        a.group0 = g0;
+        a.num_groups = num_groups - g0 < kIndexerMaxGroups ? num_groups - g0 : kIndexerMaxGroups;
+        cudaError_t e = launch_indexer_fp8(key_map, q_map, a, G, sms, static_cast<cudaStream_t>(stream));
+        if (e != cudaSuccess) return DSA_ERR_CUDA;
+    }
+    return DSA_OK;
+}
+
+int dsa_topk(const float *logits, int64_t logits_stride, const int32_t *row_ctx, int32_t num_rows,
+             int32_t max_ctx, int32_t k, int32_t *idx_out, int32_t *dev_status, void *stream) {
+    if (num_rows < 0 || max_ctx < 0) return DSA_ERR_INVALID_ARG;
+    if (k < 1 || k > DSA_MAX_TOPK) return DSA_ERR_UNSUPPORTED;
+    if (num_rows == 0) return DSA_OK;
+    if (!logits || !row_ctx || !idx_out || logits_stride < max_ctx) return DSA_ERR_INVALID_ARG;
+    TopkArgs a{logits, logits_stride, row_ctx, num_rows, max_ctx, k, idx_out, dev_status};
+    return launch_status(launch_topk(a, static_cast<cudaStream_t>(stream)));
+}
+
+int dsa_page_to_slot(const dsa_rows *rows, int64_t pool_pages, const int32_t *idx, int32_t k, int32_t *slots,
+                     int32_t *dev_status, void *stream) {
+    int rc = check_rows(rows);
+    if (rc != DSA_OK) return rc;
+    if (k < 1) return DSA_ERR_INVALID_ARG;
+    if (rows->num_rows == 0) return DSA_OK;
+    if (!idx || !slots || pool_pages <= 0) return DSA_ERR_INVALID_ARG;
+    if (pool_pages * DSA_PAGE_SIZE > INT32_MAX) return DSA_ERR_UNSUPPORTED;
+    SlotArgs a{rows->block_table, rows->bt_stride, rows->num_requests, rows->row_req, rows->row_ctx, rows->num_rows,
+               rows->max_ctx, pool_pages, idx, k, slots, dev_status};
+    return launch_status(launch_page_to_slot(a, static_cast<cudaStream_t>(stream)));
+}
+
+size_t dsa_sparse_mla_workspace_size(int32_t num_rows, int32_t num_heads, int32_t k) {
+    if (num_rows <= 0 || num_heads <= 0 || k <= 0) return 0;
+    return mla_workspace_bytes(num_rows, num_heads, k);
+}
+
+static int sparse_mla_common(const dsa_cache *lat, const uint16_t *q, int32_t num_heads, const int32_t *slots,
+                             int32_t num_rows, int32_t k, float sm_scale, float *out, float *lse,
+                             int32_t *dev_status, void *ws, size_t ws_bytes, void *stream, bool decode) {
+    if (lat == nullptr || num_rows < 0) return DSA_ERR_INVALID_ARG;
+    if (lat->page_size != DSA_PAGE_SIZE) return DSA_ERR_UNSUPPORTED;
+    if (lat->format != DSA_LATENT_FP8 && lat->format != DSA_LATENT_NVFP4) return DSA_ERR_UNSUPPORTED;
+    if (num_heads < 16 || num_heads > 96 || num_heads % 16 != 0) return DSA_ERR_UNSUPPORTED;
+    if (k < 1) return DSA_ERR_INVALID_ARG;
+    if (num_rows == 0) return DSA_OK;
+    if (!lat->base || lat->num_pages <= 0 || !q || !slots || !out) return DSA_ERR_INVALID_ARG;
+    if (!aligned(lat->base, 16) || !aligned(q, 16)) return DSA_ERR_INVALID_ARG;
+    if (!std::isfinite(sm_scale) || !std::isfinite(lat->tensor_scale)) return DSA_ERR_INVALID_ARG;
+    MlaArgs a{};
+    a.pool = static_cast<const uint8_t *>(lat->base);
+    a.format = lat->format;
+    a.num_pages = lat->num_pages;
+    a.tensor_scale = lat->tensor_scale;
+    a.q = q;
+    a.num_heads = num_heads;
+    a.slots = slots;
+    a.num_rows = num_rows;
+    a.k = k;
+    a.sm_scale = sm_scale;
+    a.out = out;
+    a.lse = lse;
+    a.status = dev_status;
+    a.splits = 1;
+    if (decode) {
+        const int splits = (k + kMlaTokensPerSplit - 1) / kMlaTokensPerSplit;
+        if (splits > 1) {
+            const size_t need = mla_workspace_bytes(num_rows, num_heads, k);
+            if (ws == nullptr || ws_bytes < need) return DSA_ERR_WORKSPACE;
+            if (!aligned(ws, 256)) return DSA_ERR_INVALID_ARG;
+            const size_t o_bytes =
+                (static_cast<size_t>(num_rows) * splits * num_heads * DSA_VALUE_DIM * sizeof(float) + 255) / 256 * 256;
+            a.part_o = static_cast<float *>(ws);
+            a.part_ml = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + o_bytes);
+            a.splits = splits;
+        }
+    }
+    return launch_status(launch_sparse_mla(a, static_cast<cudaStream_t>(stream)));
+}
+
+int dsa_sparse_mla_decode(const dsa_cache *latent_cache, const uint16_t *q, int32_t num_heads,
+                          const int32_t *slots, int32_t num_rows, int32_t k, float sm_scale, float *out,
+                          float *lse, int32_t *dev_status, void *workspace, size_t workspace_bytes, void *stream) {
+    return sparse_mla_common(latent_cache, q, num_heads, slots, num_rows, k, sm_scale, out, lse, dev_status,
+                             workspace, workspace_bytes, stream, true);
+}
+
+int dsa_sparse_mla_prefill(const dsa_cache *latent_cache, const uint16_t *q, int32_t num_heads,
+                           const int32_t *slots, int32_t num_rows, int32_t k, float sm_scale, float *out,
+                           float *lse, int32_t *dev_status, void *workspace, size_t workspace_bytes,
+                           void *stream) {
+    return sparse_mla_common(latent_cache, q, num_heads, slots, num_rows, k, sm_scale, out, lse, dev_status,
+                             workspace, workspace_bytes, stream, false);
+}
+
+}  // extern "C"

@@ -1,0 +1,346 @@
+// indexer.cu -- DSA indexer logits on the sm_103a tensor cores.
+//
+// What it computes (vLLM blog "Day-0 support for Kimi K3.1 Pro", section
+// "Sparse attention in K3.1 Pro"; weighted fp32 reduction across heads from
+// the AMD section "Quantization: native MXFP4 indexer"):
+//     logit[r, t] = sum_h w[r, h] * max(0, s_t * <q[r, h, :], k_t>)
+// for every cached token t < L_r of the row's request.
+//
+// Design (GB300): the scan over all cached index keys is the dominant HBM
+// stream of the layer (132 B per token per row group), so the kernel is a
+// persistent, key-balanced pipeline:
+//   * work = (row group g, 128-key tile); the tiles of all groups form one
+//     list that is split evenly over one CTA per SM (the blog's scorer is
+//     "key-balanced" too, section "Low-latency decode");
+//   * warp 0 streams key tiles with TMA (two 64-token pages -> one 128-row,
+//     128-byte-swizzled operand) plus the pages' fp32 scales into a ring of
+//     shared-memory stages;
+//   * warp 1 issues tcgen05.mma kind::f8f6f4 (e4m3 x e4m3 -> fp32) with the
+//     KEYS on M = 128 and the group's G rows x 32 heads on N, K = 128, into a
+//     double-buffered TMEM accumulator; a group's G rows (speculative-verify
+//     rows or a prefill query block) share every key read;
+//   * 4 or 8 epilogue warps read one key lane each from TMEM, so the head
+//     reduction sum_h w_h * relu(acc_h) runs in registers, scale by s_t
+//     (s_t > 0 commutes with the relu), mask t >= L_r and write coalesced
+//     fp32 logits.
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace dsa {
+
+namespace {
+
+constexpr int kTileKeys = 128;
+constexpr int kIdxPageBytes = DSA_PAGE_SIZE * (DSA_INDEX_DIM + 4);  // 8448
+constexpr int kIdxPageRows = kIdxPageBytes / 128;                    // 66 rows of 128 B
+
+template <int G>
+struct IdxCfg {
+    static constexpr int N = 32 * G;
+    static constexpr int kStages = G >= 8 ? 5 : (G >= 4 ? 6 : 8);
+    static constexpr int kEpiSplit = G >= 8 ? 2 : 1;
+    static constexpr int kEpiWarps = 4 * kEpiSplit;
+    static constexpr int kRowsPerEpiWarp = G / kEpiSplit;
+    static constexpr int kThreads = 128 + 32 * kEpiWarps;
+    static constexpr uint32_t kTmemCols = (2 * N < 32) ? 32u : static_cast<uint32_t>(2 * N);
+    static constexpr int kKeyBytes = kTileKeys * 128;
+    static constexpr int kQBytes = N * 128;
+    static constexpr int OFF_KEYS = 0;
+    static constexpr int OFF_Q = OFF_KEYS + kStages * kKeyBytes;
+    static constexpr int OFF_SCALES = OFF_Q + 2 * kQBytes;
+    static constexpr int OFF_W = OFF_SCALES + kStages * kTileKeys * 4;
+    static constexpr int OFF_PREFIX = OFF_W + 2 * N * 4;
+    static constexpr int OFF_GREQ = OFF_PREFIX + (kIndexerMaxGroups + 4) * 4;
+    static constexpr int OFF_GMAX = OFF_GREQ + kIndexerMaxGroups * 4;
+    static constexpr int OFF_BARS = OFF_GMAX + kIndexerMaxGroups * 4;
+    static constexpr int kNumBars = 2 * kStages + 9;
+    static constexpr int OFF_MISC = OFF_BARS + kNumBars * 8;
+    static constexpr int kSmemBytes = OFF_MISC + 64 + 1024;  // + slack for 1024-byte alignment
+    static_assert(kTmemCols == 32 || kTmemCols == 64 || kTmemCols == 128 || kTmemCols == 256 ||
+                      kTmemCols == 512,
+                  "TMEM allocation must be a power of two >= 32");
+    static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+};
+
+// Sequential walk over a CTA's contiguous range of the global tile list.
+struct TileWalker {
+    const int32_t *prefix;  // [num_groups + 1] tile prefix sums (shared memory)
+    int g;
+    __device__ void seek(int32_t w, int num_groups) {
+        int lo = 0, hi = num_groups;  // find g with prefix[g] <= w < prefix[g+1]
+        while (hi - lo > 1) {
+            int mid = (lo + hi) >> 1;
+            if (prefix[mid] <= w) lo = mid;
+            else hi = mid;
+        }
+        g = lo;
+    }
+    __device__ void advance(int32_t w) {
+        while (prefix[g + 1] <= w) ++g;
+    }
+};
+
+template <int G>
+__global__ void __launch_bounds__(IdxCfg<G>::kThreads, 1)
+    indexer_fp8_kernel(const __grid_constant__ CUtensorMap key_map, const __grid_constant__ CUtensorMap q_map,
+                       const IndexerArgs a) {
+    using C = IdxCfg<G>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *keys = smem + C::OFF_KEYS;
+    uint8_t *qbuf = smem + C::OFF_Q;
+    float *scales = reinterpret_cast<float *>(smem + C::OFF_SCALES);
+    float *wbuf = reinterpret_cast<float *>(smem + C::OFF_W);
+    int32_t *prefix = reinterpret_cast<int32_t *>(smem + C::OFF_PREFIX);
+    int32_t *greq = reinterpret_cast<int32_t *>(smem + C::OFF_GREQ);
+    int32_t *gmax = reinterpret_cast<int32_t *>(smem + C::OFF_GMAX);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::OFF_BARS);
+    uint64_t *full = bars;                      // [kStages] TMA -> MMA
+    uint64_t *empty = bars + C::kStages;        // [kStages] MMA + epilogue -> TMA
+    uint64_t *tfull = bars + 2 * C::kStages;    // [2] MMA -> epilogue
+    uint64_t *tempty = tfull + 2;               // [2] epilogue -> MMA
+    uint64_t *qfull = tfull + 4;                // [2] TMA -> MMA (query of a group)
+    uint64_t *qempty = tfull + 6;               // [2] MMA -> TMA
+    uint64_t *mma_done = tfull + 8;             // [1] all MMAs retired
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
+    volatile int *abort = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 4);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int ng = a.num_groups;
+
+    // ---- prologue: per-group request, longest context, tile counts and their prefix sums
+    for (int g = tid; g < ng; g += blockDim.x) {
+        const int row0 = (a.group0 + g) * G;
+        const int req = a.row_req[row0];
+        int mx = 0;
+        bool bad = req < 0 || req >= a.num_requests;
+        for (int j = 0; j < G; ++j) {
+            int c = a.row_ctx[row0 + j];
+            if (a.row_req[row0 + j] != req || c < 0 || c > a.max_ctx) bad = true;
+            mx = max(mx, min(max(c, 0), a.max_ctx));
+        }
+        if (bad) {
+            report(a.status, DSA_ERR_BOUNDS);
+            mx = 0;
+        }
+        greq[g] = req;
+        gmax[g] = mx;
+        prefix[g + 1] = (mx + kTileKeys - 1) / kTileKeys;
+    }
+    if (tid == 0) {
+        prefix[0] = 0;
+        *abort = 0;
+        for (int s = 0; s < C::kStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1 + C::kEpiWarps);  // MMA commit + one arrival per epilogue warp
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&tfull[i], 1);
+            mbar_init(&tempty[i], C::kEpiWarps);
+            mbar_init(&qfull[i], 1);
+            mbar_init(&qempty[i], 1);
+        }
+        mbar_init(mma_done, 1);
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, C::kTmemCols);
+        tmem_relinquish();
+    }
+    __syncthreads();
+    if (warp == 0) {  // inclusive scan of prefix[1..ng] by one warp
+        const int per = (ng + 31) / 32;
+        const int b = 1 + lane * per, e = min(ng + 1, b + per);
+        int sum = 0;
+        for (int i = b; i < e; ++i) sum += prefix[i];
+        int incl = sum;
+        for (int o = 1; o < 32; o <<= 1) {
+            int v = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += v;
+        }
+        int run = incl - sum;
+        for (int i = b; i < e; ++i) {
+            run += prefix[i];
+            prefix[i] = run;
+        }
+    }
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    const int32_t total = prefix[ng];
+    const int32_t per = total / gridDim.x, rem = total % gridDim.x;
+    const int32_t w_begin = blockIdx.x * per + (static_cast<int32_t>(blockIdx.x) < rem ? static_cast<int32_t>(blockIdx.x) : rem);
+    const int32_t w_end = w_begin + per + (blockIdx.x < rem ? 1 : 0);
+
+    constexpr uint32_t kIdesc = make_idesc(128, C::N, 0, 0, false, false);
+
+    if (w_begin < w_end) {
+        if (warp == 0 && lane == 0) {
+            // ------------------------------------------------ TMA producer
+            prefetch_tensormap(&key_map);
+            prefetch_tensormap(&q_map);
+            TileWalker wk{prefix, 0};
+            wk.seek(w_begin, ng);
+            int cur = -1, gc = -1;
+            int32_t it = 0;
+            for (int32_t w = w_begin; w < w_end; ++w, ++it) {
+                wk.advance(w);
+                const int g = wk.g;
+                if (g != cur) {
+                    ++gc;
+                    cur = g;
+                    const int qb = gc & 1;
+                    if (!mbar_wait(&qempty[qb], ((gc >> 1) & 1) ^ 1, abort, a.status)) break;
+                    mbar_arrive_expect_tx(&qfull[qb], C::kQBytes);
+                    tma_load_2d(qbuf + qb * C::kQBytes, &q_map, &qfull[qb], 0, (a.group0 + g) * G * DSA_INDEX_HEADS);
+                }
+                const int stage = it % C::kStages;
+                if (!mbar_wait(&empty[stage], ((it / C::kStages) & 1) ^ 1, abort, a.status)) break;
+                const int kt = w - prefix[g];
+                const int nkeys = min(kTileKeys, gmax[g] - kt * kTileKeys);
+                const int32_t *bt = a.block_table + static_cast<int64_t>(greq[g]) * a.bt_stride;
+                const int npages = (nkeys + DSA_PAGE_SIZE - 1) / DSA_PAGE_SIZE;
+                mbar_arrive_expect_tx(&full[stage], npages * (DSA_PAGE_SIZE * 128 + DSA_PAGE_SIZE * 4));
+                for (int p = 0; p < npages; ++p) {
+                    int32_t page = bt[kt * 2 + p];
+                    if (page < 0 || page >= a.num_pages) {
+                        report(a.status, DSA_ERR_BOUNDS);
+                        page = 0;
+                    }
+                    tma_load_2d(keys + stage * C::kKeyBytes + p * (DSA_PAGE_SIZE * 128), &key_map, &full[stage], 0,
+                                page * kIdxPageRows);
+                    bulk_load(scales + stage * kTileKeys + p * DSA_PAGE_SIZE,
+                              a.pool + static_cast<int64_t>(page) * kIdxPageBytes + DSA_PAGE_SIZE * 128,
+                              DSA_PAGE_SIZE * 4, &full[stage]);
+                }
+            }
+        } else if (warp == 1 && lane == 0) {
+            // ------------------------------------------------ MMA issuer
+            TileWalker wk{prefix, 0};
+            wk.seek(w_begin, ng);
+            int cur = -1, gc = -1;
+            int32_t it = 0;
+            for (int32_t w = w_begin; w < w_end; ++w, ++it) {
+                wk.advance(w);
+                const int g = wk.g;
+                if (g != cur) {
+                    ++gc;
+                    cur = g;
+                    if (!mbar_wait(&qfull[gc & 1], (gc >> 1) & 1, abort, a.status)) break;
+                }
+                const int qb = gc & 1;
+                const int stage = it % C::kStages, as = it & 1;
+                if (!mbar_wait(&tempty[as], ((it >> 1) & 1) ^ 1, abort, a.status)) break;
+                if (!mbar_wait(&full[stage], (it / C::kStages) & 1, abort, a.status)) break;
+                tc_fence_after();
+                const uint32_t a_addr = smem_u32(keys + stage * C::kKeyBytes);
+                const uint32_t b_addr = smem_u32(qbuf + qb * C::kQBytes);
+#pragma unroll
+                for (int kk = 0; kk < DSA_INDEX_DIM / 32; ++kk) {
+                    mma_f8(tmem_base + as * C::N, sdesc_sw128(a_addr + kk * 32, 16, 1024),
+                           sdesc_sw128(b_addr + kk * 32, 16, 1024), kIdesc, kk > 0 ? 1u : 0u);
+                }
+                mma_commit(&empty[stage]);
+                mma_commit(&tfull[as]);
+                const bool last_of_group = (w + 1 == w_end) || (prefix[g + 1] <= w + 1);
+                if (last_of_group) mma_commit(&qempty[qb]);
+            }
+            mma_commit(mma_done);
+            mbar_wait(mma_done, 0, abort, a.status);
+        } else if (warp >= 4) {
+            // ------------------------------------------------ epilogue
+            const int e = warp - 4;
+            const int quad = warp & 3;
+            const int rbeg = (e >> 2) * C::kRowsPerEpiWarp;
+            const int key_lane = quad * 32 + lane;
+            TileWalker wk{prefix, 0};
+            wk.seek(w_begin, ng);
+            int cur = -1, gc = -1;
+            int ctx[C::kRowsPerEpiWarp];
+            int64_t row_off[C::kRowsPerEpiWarp];
+            int32_t it = 0;
+            for (int32_t w = w_begin; w < w_end; ++w, ++it) {
+                wk.advance(w);
+                const int g = wk.g;
+                if (g != cur) {
+                    ++gc;
+                    cur = g;
+                    float *wb = wbuf + (gc & 1) * C::N;
+                    const int row0 = (a.group0 + g) * G;
+                    for (int i = tid - 128; i < C::N; i += 32 * C::kEpiWarps)
+                        wb[i] = a.head_w[static_cast<int64_t>(row0) * DSA_INDEX_HEADS + i];
+                    named_bar_sync(1, 32 * C::kEpiWarps);
+#pragma unroll
+                    for (int j = 0; j < C::kRowsPerEpiWarp; ++j) {
+                        ctx[j] = min(a.row_ctx[row0 + rbeg + j], a.max_ctx);
+                        row_off[j] = static_cast<int64_t>(row0 + rbeg + j) * a.logits_stride;
+                    }
+                }
+                const float *wb = wbuf + (gc & 1) * C::N;
+                const int stage = it % C::kStages, as = it & 1;
+                if (!mbar_wait(&tfull[as], (it >> 1) & 1, abort, a.status)) break;
+                // the stage's TMA phase is complete (the MMA waited for it) and cannot be
+                // re-armed before this warp arrives on empty[stage]; waiting on it here makes
+                // the bulk-copied scales visible to this thread.
+                if (!mbar_wait(&full[stage], (it / C::kStages) & 1, abort, a.status)) break;
+                tc_fence_after();
+                const float s_t = scales[stage * kTileKeys + key_lane];
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty[stage]);
+                const int t = (w - prefix[g]) * kTileKeys + key_lane;
+#pragma unroll
+                for (int j = 0; j < C::kRowsPerEpiWarp; ++j) {
+                    uint32_t acc[32];
+                    tmem_ld32(tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + as * C::N + (rbeg + j) * 32, acc);
+                    tmem_ld_wait();
+                    const float *wr = wb + (rbeg + j) * 32;
+                    float sum = 0.f;
+#pragma unroll
+                    for (int h = 0; h < 32; ++h) sum = fmaf(wr[h], fmaxf(__uint_as_float(acc[h]), 0.f), sum);
+                    if (t < ctx[j]) a.logits[row_off[j] + t] = sum * s_t;
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&tempty[as]);
+            }
+        }
+    }
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, C::kTmemCols);
+    }
+}
+
+template <int G>
+cudaError_t launch_g(const CUtensorMap &key_map, const CUtensorMap &q_map, const IndexerArgs &a, int num_sms,
+                     cudaStream_t s) {
+    using C = IdxCfg<G>;
+    static int configured_device = -1;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (configured_device != dev) {
+        cudaError_t e = cudaFuncSetAttribute(indexer_fp8_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             C::kSmemBytes);
+        if (e != cudaSuccess) return e;
+        configured_device = dev;
+    }
+    indexer_fp8_kernel<G><<<num_sms, C::kThreads, C::kSmemBytes, s>>>(key_map, q_map, a);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_indexer_fp8(const CUtensorMap &key_map, const CUtensorMap &q_map, const IndexerArgs &a,
+                               int rows_per_group, int num_sms, cudaStream_t s) {
+    switch (rows_per_group) {
+        case 1: return launch_g<1>(key_map, q_map, a, num_sms, s);
+        case 2: return launch_g<2>(key_map, q_map, a, num_sms, s);
+        case 4: return launch_g<4>(key_map, q_map, a, num_sms, s);
+        case 8: return launch_g<8>(key_map, q_map, a, num_sms, s);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace dsa

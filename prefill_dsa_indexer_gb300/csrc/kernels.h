@@ -1,0 +1,94 @@
+// kernels.h -- launchers shared between the C-ABI layer (api.cu) and the
+// kernel translation units.  Internal to libdsa.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "../../include/dsa.h"
+
+namespace dsa {
+
+struct IndexerArgs {
+    const uint8_t *pool;        // index pool base
+    int64_t num_pages;
+    const int32_t *block_table;
+    int64_t bt_stride;
+    int32_t num_requests;
+    const int32_t *row_req;
+    const int32_t *row_ctx;
+    int32_t max_ctx;
+    int32_t group0;             // first group of this launch
+    int32_t num_groups;         // groups in this launch (<= kIndexerMaxGroups)
+    const float *head_w;
+    float *logits;
+    int64_t logits_stride;
+    int32_t *status;
+};
+
+constexpr int kIndexerMaxGroups = 1024;
+
+// Launch the FP8-key indexer for groups of `rows_per_group` rows.
+cudaError_t launch_indexer_fp8(const CUtensorMap &key_map, const CUtensorMap &q_map, const IndexerArgs &a,
+                               int rows_per_group, int num_sms, cudaStream_t s);
+
+struct TopkArgs {
+    const float *logits;
+    int64_t logits_stride;
+    const int32_t *row_ctx;
+    int32_t num_rows;
+    int32_t max_ctx;
+    int32_t k;
+    int32_t *idx_out;
+    int32_t *status;
+};
+
+cudaError_t launch_topk(const TopkArgs &a, cudaStream_t s);
+
+struct SlotArgs {
+    const int32_t *block_table;
+    int64_t bt_stride;
+    int32_t num_requests;
+    const int32_t *row_req;
+    const int32_t *row_ctx;
+    int32_t num_rows;
+    int32_t max_ctx;
+    int64_t pool_pages;
+    const int32_t *idx;
+    int32_t k;
+    int32_t *slots;
+    int32_t *status;
+};
+
+cudaError_t launch_page_to_slot(const SlotArgs &a, cudaStream_t s);
+
+struct MlaArgs {
+    const uint8_t *pool;
+    int32_t format;
+    int64_t num_pages;
+    float tensor_scale;
+    const uint16_t *q;
+    int32_t num_heads;
+    const int32_t *slots;
+    int32_t num_rows;
+    int32_t k;
+    float sm_scale;
+    float *out;
+    float *lse;
+    int32_t *status;
+    float *part_o;      // decode: [R, splits, H, 512] unnormalised partial outputs
+    float *part_ml;     // decode: [R, splits, H, 2] running max (log2 units) and sum
+    int32_t splits;     // 1 = write the final output directly
+};
+
+constexpr int kMlaTokensPerSplit = 256;
+
+cudaError_t launch_sparse_mla(const MlaArgs &a, cudaStream_t s);
+
+size_t mla_workspace_bytes(int32_t num_rows, int32_t num_heads, int32_t k);
+
+int device_sm_count();
+
+}  // namespace dsa

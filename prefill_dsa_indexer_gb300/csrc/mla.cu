@@ -1,0 +1,551 @@
+// mla.cu -- sparse absorbed-MLA attention over the selected tokens.
+//
+// What it computes (vLLM blog "Day-0 support for Kimi K3.1 Pro", section
+// "Sparse attention in K3.1 Pro": exact MLA attention, only over the 2,048
+// selected tokens, 576-byte FP8 latents of 512 latent + 64 RoPE dims; the
+// latent is the value because the key projection is absorbed, section
+// "Low-latency decode: fused DSA decode path"):
+//     S[h, t] = sm_scale * <q[h, :576], kv_t>,   O[h] = sum_t softmax_t(S[h, .]) kv_t[:512]
+//
+// Design (GB300):
+//   * one CTA per (row, split of the row's selected tokens); 64-token tiles;
+//   * four gather warps load the tile's latent rows (16-byte vector loads,
+//     two lanes per 32-byte sector), decode them exactly into fp16
+//     (cvt e4m3x2 -> f16x2; NVFP4 e2m1 * e4m3 scale is exact in fp16 too) and
+//     store them 128-byte swizzled, so one shared-memory image serves as the
+//     K-major B operand of S and the MN-major A operand of PV;
+//   * one thread issues tcgen05.mma kind::f16:
+//       S  [heads (M=128) x 64 tokens]    = Q[128 x 576] . KV^T   (36 MMAs)
+//       O^T[dims (4 x M=128) x heads (N=H)] += KV^T . P^T         (16 MMAs)
+//     S keeps heads on TMEM lanes, so each softmax thread owns one head row
+//     and reduces over tokens in registers; O is kept transposed so that
+//     S (2 x 64 columns) and O^T (4 x 96 columns) fit the 512 TMEM columns
+//     without padding the 96 heads to 128 in the PV product;
+//   * four softmax warps run an online softmax in log2 units with a lazy
+//     rescale of O^T (only when a head's running max grows by more than
+//     2^8), write P in fp16 and keep the row sums;
+//   * Q's rows beyond the real heads only feed S rows nobody reads, so Q's
+//     128-row operand is packed at a stride of H rows per 64-dim block and
+//     the unused rows alias the next block.
+// Decode splits a row's tokens over several CTAs (fixed split size, so the
+// result does not depend on the batch) and merges the parts by log-sum-exp
+// in a second kernel; prefill writes the output directly.
+#include <cuda_fp16.h>
+
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace dsa {
+
+namespace {
+
+constexpr int kTok = 64;                  // tokens per tile
+constexpr int kChunks = DSA_LATENT_DIM / 64;  // 9 blocks of 64 dims
+constexpr int kMaxH = 96;
+constexpr int kThreads = 384;             // warp 0 MMA, 4-7 softmax, 8-11 gather/epilogue
+constexpr float kLazyRescaleLog2 = 8.0f;  // rescale O only when a max grows by > 2^8
+
+constexpr int kKvBytes = kChunks * kTok * 128;  // 73,728: fp16 tile, [chunk][token][64 dims]
+constexpr int kPBytes = kMaxH * 128;            // 12,288: fp16 P, [head][64 tokens]
+constexpr int OFF_Q = 0;
+constexpr int kQBytesMax = kChunks * kMaxH * 128 + (128 - 16) * 128;  // room for the aliased tail rows
+constexpr int OFF_KV = (OFF_Q + kQBytesMax + 1023) / 1024 * 1024;
+constexpr int OFF_P = OFF_KV + kKvBytes;
+constexpr int OFF_ALPHA = OFF_P + kPBytes;
+constexpr int OFF_L = OFF_ALPHA + 128 * 4;
+constexpr int OFF_MASK = OFF_L + 128 * 4;
+constexpr int OFF_FLAG = OFF_MASK + 16;
+constexpr int OFF_BARS = OFF_FLAG + 16;
+constexpr int kNumBars = 8;
+constexpr int OFF_MISC = OFF_BARS + kNumBars * 8;
+constexpr int kSmemBytes = OFF_MISC + 32 + 1024;
+static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kTmemO = 2 * kTok;  // O^T starts after two S buffers
+
+__device__ __forceinline__ uint32_t cvt_e4m3x2_f16x2(uint32_t two_bytes) {
+    uint32_t r;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(static_cast<uint16_t>(two_bytes)));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t cvt_e2m1x2_f16x2(uint32_t byte) {
+    uint32_t r;
+    asm("{\n\t.reg .b8 b;\n\tcvt.u8.u32 b, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, b;\n\t}" : "=r"(r) : "r"(byte));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t b) {
+    __half2 r = __hmul2(*reinterpret_cast<__half2 *>(&a), *reinterpret_cast<__half2 *>(&b));
+    return *reinterpret_cast<uint32_t *>(&r);
+}
+
+// Byte offset of 16-byte unit `u` (0..7) of row `row` in a 128-byte-swizzled
+// tile whose 8-row groups are 1024 bytes apart.
+__device__ __forceinline__ uint32_t sw128(int row, int u) {
+    return static_cast<uint32_t>(row * 128 + ((u ^ (row & 7)) << 4));
+}
+
+struct GatherRegs {
+    int4 v[18];
+    int32_t slot;
+};
+
+template <int FMT>
+__device__ __forceinline__ void gather_load(const MlaArgs &a, const int32_t *row_slots, int t0, int n_tok,
+                                            int gtid, GatherRegs &g) {
+    const int t = gtid >> 1, half = gtid & 1;
+    int32_t slot = (t0 + t < n_tok) ? row_slots[t0 + t] : -1;
+    if (slot >= 0 && static_cast<int64_t>(slot) >= a.num_pages * DSA_PAGE_SIZE) {
+        report(a.status, DSA_ERR_BOUNDS);
+        slot = -1;
+    }
+    g.slot = slot;
+    if (slot < 0) return;
+    if (FMT == DSA_LATENT_FP8) {
+        const uint8_t *src = a.pool + static_cast<int64_t>(slot) * DSA_LATENT_DIM;
+#pragma unroll
+        for (int i = 0; i < 18; ++i) g.v[i] = ldg_nc_v4(src + (half + 2 * i) * 16);
+    } else {
+        // NVFP4 page: [64 x 256 B e2m1][64 x 32 B e4m3 scales][64 x 64 B e4m3 RoPE]
+        const int64_t page = slot / DSA_PAGE_SIZE, j = slot % DSA_PAGE_SIZE;
+        const uint8_t *pg = a.pool + page * (DSA_PAGE_SIZE * 352);
+        const uint8_t *codes = pg + j * 256;
+        const uint8_t *sc = pg + DSA_PAGE_SIZE * 256 + j * 32;
+        const uint8_t *rope = pg + DSA_PAGE_SIZE * 288 + j * 64;
+        // this thread: code units half, half+2, ..., both 16-byte scale units, RoPE units half, half+2
+#pragma unroll
+        for (int i = 0; i < 8; ++i) g.v[i] = ldg_nc_v4(codes + (half + 2 * i) * 16);
+        g.v[8] = ldg_nc_v4(sc);
+        g.v[9] = ldg_nc_v4(sc + 16);
+        g.v[10] = ldg_nc_v4(rope + half * 16);
+        g.v[11] = ldg_nc_v4(rope + (half + 2) * 16);
+    }
+}
+
+template <int FMT>
+__device__ __forceinline__ void gather_store(uint8_t *kv, int gtid, const GatherRegs &g) {
+    const int t = gtid >> 1, half = gtid & 1;
+    if (g.slot < 0) {
+        const int4 z = make_int4(0, 0, 0, 0);
+        // zero this thread's share of the token row (all 9 chunks, 8 units each)
+        for (int c = 0; c < kChunks; ++c)
+#pragma unroll
+            for (int u = half * 4; u < half * 4 + 4; ++u)
+                *reinterpret_cast<int4 *>(kv + c * (kTok * 128) + sw128(t, u)) = z;
+        return;
+    }
+    if (FMT == DSA_LATENT_FP8) {
+#pragma unroll
+        for (int i = 0; i < 18; ++i) {
+            const int u = half + 2 * i;  // 16-dim unit of the 576-dim row
+            const int c = u >> 2, gq = u & 3;
+            const uint32_t w[4] = {static_cast<uint32_t>(g.v[i].x), static_cast<uint32_t>(g.v[i].y),
+                                   static_cast<uint32_t>(g.v[i].z), static_cast<uint32_t>(g.v[i].w)};
+            int4 o0, o1;
+            o0.x = cvt_e4m3x2_f16x2(w[0] & 0xffffu);
+            o0.y = cvt_e4m3x2_f16x2(w[0] >> 16);
+            o0.z = cvt_e4m3x2_f16x2(w[1] & 0xffffu);
+            o0.w = cvt_e4m3x2_f16x2(w[1] >> 16);
+            o1.x = cvt_e4m3x2_f16x2(w[2] & 0xffffu);
+            o1.y = cvt_e4m3x2_f16x2(w[2] >> 16);
+            o1.z = cvt_e4m3x2_f16x2(w[3] & 0xffffu);
+            o1.w = cvt_e4m3x2_f16x2(w[3] >> 16);
+            uint8_t *base = kv + c * (kTok * 128);
+            *reinterpret_cast<int4 *>(base + sw128(t, 2 * gq)) = o0;
+            *reinterpret_cast<int4 *>(base + sw128(t, 2 * gq + 1)) = o1;
+        }
+    } else {
+        // 32 e4m3 scales, one per 16 latent dims
+        const uint32_t scw[8] = {static_cast<uint32_t>(g.v[8].x), static_cast<uint32_t>(g.v[8].y),
+                                 static_cast<uint32_t>(g.v[8].z), static_cast<uint32_t>(g.v[8].w),
+                                 static_cast<uint32_t>(g.v[9].x), static_cast<uint32_t>(g.v[9].y),
+                                 static_cast<uint32_t>(g.v[9].z), static_cast<uint32_t>(g.v[9].w)};
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int cu = half + 2 * i;  // code unit: dims [32 cu, 32 cu + 32)
+            const uint32_t w[4] = {static_cast<uint32_t>(g.v[i].x), static_cast<uint32_t>(g.v[i].y),
+                                   static_cast<uint32_t>(g.v[i].z), static_cast<uint32_t>(g.v[i].w)};
+            uint32_t o[16];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int sidx = 2 * cu + (q >> 1);  // word q holds dims 32cu + 8q .. +8
+                const uint32_t sbyte = (scw[sidx >> 2] >> (8 * (sidx & 3))) & 0xffu;
+                const uint32_t sh2 = cvt_e4m3x2_f16x2(sbyte | (sbyte << 8));
+#pragma unroll
+                for (int b = 0; b < 4; ++b)
+                    o[4 * q + b] = hmul2_u32(cvt_e2m1x2_f16x2((w[q] >> (8 * b)) & 0xffu), sh2);
+            }
+            // 32 dims = 64 B of fp16 = 4 swizzle units of chunk cu / 2
+            const int c = cu >> 1, u0 = (cu & 1) * 4;
+            uint8_t *base = kv + c * (kTok * 128);
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                *reinterpret_cast<int4 *>(base + sw128(t, u0 + q)) =
+                    make_int4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+        }
+        // RoPE dims 512..575 (chunk 8): 64 e4m3 bytes; this thread holds units half and half+2
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const int u = half + 2 * i;  // 16-dim unit of the RoPE block
+            const int4 v = g.v[10 + i];
+            const uint32_t w[4] = {static_cast<uint32_t>(v.x), static_cast<uint32_t>(v.y),
+                                   static_cast<uint32_t>(v.z), static_cast<uint32_t>(v.w)};
+            int4 o0, o1;
+            o0.x = cvt_e4m3x2_f16x2(w[0] & 0xffffu);
+            o0.y = cvt_e4m3x2_f16x2(w[0] >> 16);
+            o0.z = cvt_e4m3x2_f16x2(w[1] & 0xffffu);
+            o0.w = cvt_e4m3x2_f16x2(w[1] >> 16);
+            o1.x = cvt_e4m3x2_f16x2(w[2] & 0xffffu);
+            o1.y = cvt_e4m3x2_f16x2(w[2] >> 16);
+            o1.z = cvt_e4m3x2_f16x2(w[3] & 0xffffu);
+            o1.w = cvt_e4m3x2_f16x2(w[3] >> 16);
+            uint8_t *base = kv + 8 * (kTok * 128);
+            *reinterpret_cast<int4 *>(base + sw128(t, 2 * u)) = o0;
+            *reinterpret_cast<int4 *>(base + sw128(t, 2 * u + 1)) = o1;
+        }
+    }
+}
+
+template <int FMT>
+__global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const MlaArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *qs = smem + OFF_Q;
+    uint8_t *kv = smem + OFF_KV;
+    uint8_t *ps = smem + OFF_P;
+    float *alpha = reinterpret_cast<float *>(smem + OFF_ALPHA);
+    float *lsum = reinterpret_cast<float *>(smem + OFF_L);
+    unsigned long long *mask = reinterpret_cast<unsigned long long *>(smem + OFF_MASK);
+    int *flag = reinterpret_cast<int *>(smem + OFF_FLAG);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + OFF_BARS);
+    uint64_t *kv_full = bars + 0;   // gather -> MMA, softmax          (count 4)
+    uint64_t *s_full = bars + 1;    // [2] MMA -> softmax               (commit)
+    uint64_t *s_free = bars + 3;    // [2] softmax -> MMA               (count 4)
+    uint64_t *p_full = bars + 5;    // softmax -> MMA                   (count 4)
+    uint64_t *pv_done = bars + 6;   // MMA -> gather, softmax           (commit)
+    uint64_t *stats = bars + 7;     // softmax -> epilogue              (count 4)
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + OFF_MISC);
+    volatile int *abort = reinterpret_cast<volatile int *>(smem + OFF_MISC + 4);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int H = a.num_heads;
+    const int row = blockIdx.x / a.splits, split = blockIdx.x % a.splits;
+    const int tps = (a.k + a.splits - 1) / a.splits;
+    const int t_begin = split * tps, t_end = min(a.k, t_begin + tps);
+    const int n_tok = t_end - t_begin;
+    const int n_tiles = (n_tok + kTok - 1) / kTok;
+    const int32_t *row_slots = a.slots + static_cast<int64_t>(row) * a.k + t_begin;
+    const float ts = a.tensor_scale;
+    // FP8 latents stay as raw e4m3 values in fp16; their per-tensor scale is applied to S and O.
+    const float s_scale = (FMT == DSA_LATENT_FP8 ? ts : 1.0f) * a.sm_scale * 1.4426950408889634f;
+    const float o_scale = (FMT == DSA_LATENT_FP8 ? ts : 1.0f);
+    const float q_rope_scale = (FMT == DSA_LATENT_FP8 ? 1.0f : ts);
+
+    if (tid == 0) {
+        *abort = 0;
+        flag[0] = flag[1] = 0;
+        mbar_init(kv_full, 4);
+        mbar_init(&s_full[0], 1);
+        mbar_init(&s_full[1], 1);
+        mbar_init(&s_free[0], 4);
+        mbar_init(&s_free[1], 4);
+        mbar_init(p_full, 4);
+        mbar_init(pv_done, 1);
+        mbar_init(stats, 4);
+        fence_mbar_init();
+    }
+    if (warp == 0) {
+        tmem_alloc(tmem_slot, kTmemCols);
+        tmem_relinquish();
+    }
+    // ---- Q: bf16 -> fp16, 128-byte swizzled K-major, block c (64 dims) at c * H * 128
+    {
+        const uint16_t *qg = a.q + static_cast<int64_t>(row) * H * DSA_LATENT_DIM;
+        bool range_err = false;
+        for (int e = tid; e < H * (DSA_LATENT_DIM / 8); e += kThreads) {
+            const int h = e / (DSA_LATENT_DIM / 8), u = e % (DSA_LATENT_DIM / 8);  // 8-dim unit
+            const int4 v = *reinterpret_cast<const int4 *>(qg + h * DSA_LATENT_DIM + u * 8);
+            const uint32_t w[4] = {static_cast<uint32_t>(v.x), static_cast<uint32_t>(v.y),
+                                   static_cast<uint32_t>(v.z), static_cast<uint32_t>(v.w)};
+            const float sc = (u >= DSA_VALUE_DIM / 8) ? q_rope_scale : 1.0f;
+            uint32_t o[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float lo = __uint_as_float(w[i] << 16) * sc, hi = __uint_as_float(w[i] & 0xffff0000u) * sc;
+                if (!(fabsf(lo) <= 65504.f) || !(fabsf(hi) <= 65504.f)) range_err = true;
+                __half2 hh = __floats2half2_rn(lo, hi);
+                o[i] = *reinterpret_cast<uint32_t *>(&hh);
+            }
+            const int c = u >> 3, uu = u & 7;
+            *reinterpret_cast<int4 *>(qs + c * H * 128 + sw128(h, uu)) = make_int4(o[0], o[1], o[2], o[3]);
+        }
+        if (range_err) report(a.status, DSA_ERR_RANGE);
+    }
+    fence_async_smem();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        if (lane == 0 && n_tiles > 0) {
+            // ------------------------------------------------------------ MMA issuer
+            const uint32_t idesc_s = make_idesc(128, kTok, 0, 0, false, false);
+            const uint32_t idesc_pv = make_idesc(128, H, 0, 0, true, false);
+            const uint32_t q_addr = smem_u32(qs), kv_addr = smem_u32(kv), p_addr = smem_u32(ps);
+            for (int i = 0; i < n_tiles; ++i) {
+                const int sb = i & 1;
+                if (!mbar_wait(kv_full, i & 1, abort, a.status)) break;
+                if (!mbar_wait(&s_free[sb], ((i >> 1) & 1) ^ 1, abort, a.status)) break;
+                tc_fence_after();
+                for (int c = 0; c < kChunks; ++c) {
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const uint64_t ad = sdesc_sw128(q_addr + c * H * 128 + kk * 32, 16, 1024);
+                        const uint64_t bd = sdesc_sw128(kv_addr + c * (kTok * 128) + kk * 32, 16, 1024);
+                        mma_f16(tmem + sb * kTok, ad, bd, idesc_s, (c | kk) ? 1u : 0u);
+                    }
+                }
+                mma_commit(&s_full[sb]);
+                if (!mbar_wait(p_full, i & 1, abort, a.status)) break;
+                tc_fence_after();
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+#pragma unroll
+                    for (int ks = 0; ks < kTok / 16; ++ks) {
+                        // A = V^T block j: dims [128j, 128j+128) x 16 tokens, MN-major:
+                        // 64-dim blocks 8 KB apart (LBO), 8-token groups 1 KB apart (SBO)
+                        const uint64_t ad = sdesc_sw128(kv_addr + (2 * j) * (kTok * 128) + ks * 2048, kTok * 128, 1024);
+                        const uint64_t bd = sdesc_sw128(p_addr + ks * 32, 16, 1024);
+                        mma_f16(tmem + kTmemO + j * H, ad, bd, idesc_pv, (i | ks) ? 1u : 0u);
+                    }
+                }
+                mma_commit(pv_done);
+            }
+        }
+    } else if (warp >= 4 && warp < 8) {
+        // ---------------------------------------------------------------- softmax
+        const int quad = warp & 3;
+        const int h = quad * 32 + lane;
+        float m = -INFINITY, l = 0.f;
+        for (int i = 0; i < n_tiles; ++i) {
+            const int sb = i & 1;
+            if (!mbar_wait(&s_full[sb], (i >> 1) & 1, abort, a.status)) break;
+            if (!mbar_wait(kv_full, i & 1, abort, a.status)) break;
+            tc_fence_after();
+            uint32_t sr[64];
+            tmem_ld32(tmem + (static_cast<uint32_t>(quad * 32) << 16) + sb * kTok, *reinterpret_cast<uint32_t(*)[32]>(sr));
+            tmem_ld32(tmem + (static_cast<uint32_t>(quad * 32) << 16) + sb * kTok + 32,
+                      *reinterpret_cast<uint32_t(*)[32]>(sr + 32));
+            tmem_ld_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&s_free[sb]);
+            const unsigned long long msk = *mask;
+            float mt = -INFINITY;
+#pragma unroll
+            for (int j = 0; j < kTok; ++j) {
+                const float s = ((msk >> j) & 1ull) ? __uint_as_float(sr[j]) * s_scale : -INFINITY;
+                sr[j] = __float_as_uint(s);
+                mt = fmaxf(mt, s);
+            }
+            float al = 1.f;
+            bool resc = false;
+            if (mt > m + kLazyRescaleLog2 || (m == -INFINITY && mt > -INFINITY)) {
+                if (m > -INFINITY) {
+                    al = exp2f(m - mt);
+                    resc = true;
+                }
+                l *= al;
+                m = mt;
+            }
+            alpha[h] = al;
+            if (__any_sync(0xffffffffu, resc && h < H) && lane == 0) atomicOr(&flag[i & 1], 1);
+            named_bar_sync(1, 128);
+            const bool do_resc = flag[i & 1] != 0;
+            if (quad == 0 && lane == 0) flag[(i + 1) & 1] = 0;
+            if (i > 0 && !mbar_wait(pv_done, (i - 1) & 1, abort, a.status)) break;
+            if (do_resc) {
+                // rescale O^T columns by alpha[head]: this warp owns TMEM lanes (dims) 32q..32q+31
+                tc_fence_after();
+                for (int j = 0; j < 4; ++j) {
+                    for (int c = 0; c < H / 16; ++c) {
+                        const uint32_t ta = tmem + (static_cast<uint32_t>(quad * 32) << 16) + kTmemO + j * H + c * 16;
+                        uint32_t v[16];
+                        tmem_ld16(ta, v);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int x = 0; x < 16; ++x) v[x] = __float_as_uint(__uint_as_float(v[x]) * alpha[c * 16 + x]);
+                        tmem_st16(ta, v);
+                    }
+                }
+                tmem_st_wait();
+            }
+            // P = 2^(s - m) in fp16, row h of the [head][64 tokens] swizzled operand
+            float ls = 0.f;
+            uint32_t pk[32];
+#pragma unroll
+            for (int j = 0; j < kTok; j += 2) {
+                const float s0 = __uint_as_float(sr[j]), s1 = __uint_as_float(sr[j + 1]);
+                const float p0 = (s0 == -INFINITY) ? 0.f : exp2f(s0 - m);
+                const float p1 = (s1 == -INFINITY) ? 0.f : exp2f(s1 - m);
+                __half2 hh = __floats2half2_rn(p0, p1);
+                // the sum uses the fp16-rounded p, the values the PV product sees
+                const float2 back = __half22float2(hh);
+                ls += back.x + back.y;
+                pk[j / 2] = *reinterpret_cast<uint32_t *>(&hh);
+            }
+            l += ls;
+            if (h < H) {
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
+                    *reinterpret_cast<int4 *>(ps + sw128(h, u)) =
+                        make_int4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+            }
+            fence_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(p_full);
+        }
+        // final statistics
+        lsum[h] = l;
+        if (h < H) {
+            const float lse2 = (l > 0.f) ? m + log2f(l) : -INFINITY;
+            if (a.splits == 1) {
+                if (a.lse) a.lse[static_cast<int64_t>(row) * H + h] = lse2 * 0.6931471805599453f;
+            } else {
+                float *ml = a.part_ml + (static_cast<int64_t>(row) * a.splits + split) * H * 2;
+                ml[2 * h] = (l > 0.f) ? m : -INFINITY;
+                ml[2 * h + 1] = l;
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(stats);
+    } else if (warp >= 8) {
+        // ---------------------------------------------------------------- gather + epilogue
+        const int gtid = tid - 256;  // 0..127
+        const int quad = warp & 3;
+        GatherRegs g;
+        if (n_tiles > 0) gather_load<FMT>(a, row_slots, 0, n_tok, gtid, g);
+        bool ok = true;
+        for (int i = 0; i < n_tiles; ++i) {
+            if (i > 0 && !mbar_wait(pv_done, (i - 1) & 1, abort, a.status)) {
+                ok = false;
+                break;
+            }
+            gather_store<FMT>(kv, gtid, g);
+            const unsigned long long vm = __ballot_sync(0xffffffffu, g.slot >= 0);
+            // lanes 2t, 2t+1 hold token t of this warp's 16 tokens: keep even lanes' bits
+            unsigned long long tok = 0;
+#pragma unroll
+            for (int b = 0; b < 16; ++b) tok |= ((vm >> (2 * b)) & 1ull) << b;
+            if (lane == 0) reinterpret_cast<unsigned short *>(mask)[quad] = static_cast<unsigned short>(tok);
+            fence_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(kv_full);
+            if (i + 1 < n_tiles) gather_load<FMT>(a, row_slots, (i + 1) * kTok, n_tok, gtid, g);
+        }
+        if (ok && n_tiles > 0) ok = mbar_wait(pv_done, (n_tiles - 1) & 1, abort, a.status);
+        if (ok) ok = mbar_wait(stats, 0, abort, a.status);
+        if (ok) {
+            tc_fence_after();
+            float *dst;
+            int64_t hstride;
+            if (a.splits == 1) {
+                dst = a.out + static_cast<int64_t>(row) * H * DSA_VALUE_DIM;
+            } else {
+                dst = a.part_o + (static_cast<int64_t>(row) * a.splits + split) * H * DSA_VALUE_DIM;
+            }
+            hstride = DSA_VALUE_DIM;
+            for (int j = 0; j < 4; ++j) {
+                const int d = 128 * j + 32 * quad + lane;
+                for (int c = 0; c < H / 16; ++c) {
+                    uint32_t v[16];
+                    if (n_tiles > 0) {
+                        tmem_ld16(tmem + (static_cast<uint32_t>(quad * 32) << 16) + kTmemO + j * H + c * 16, v);
+                        tmem_ld_wait();
+                    }
+#pragma unroll
+                    for (int x = 0; x < 16; ++x) {
+                        const int hh = c * 16 + x;
+                        const float lh = lsum[hh];
+                        const float o = (n_tiles > 0 && lh > 0.f) ? __uint_as_float(v[x]) * (o_scale / lh) : 0.f;
+                        dst[hh * hstride + d] = o;
+                    }
+                }
+            }
+        }
+    }
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// Merge the splits of each row: O = sum_s w_s O_s / sum_s w_s, w_s = l_s 2^(m_s - M).
+__global__ void mla_combine_kernel(const MlaArgs a) {
+    const int row = blockIdx.x, H = a.num_heads, S = a.splits;
+    const float *ml = a.part_ml + static_cast<int64_t>(row) * S * H * 2;
+    for (int h = 0; h < H; ++h) {
+        float M = -INFINITY;
+        for (int s = 0; s < S; ++s) M = fmaxf(M, ml[(s * H + h) * 2]);
+        float wsum = 0.f;
+        for (int s = 0; s < S; ++s) {
+            const float ms = ml[(s * H + h) * 2];
+            wsum += (ms == -INFINITY) ? 0.f : ml[(s * H + h) * 2 + 1] * exp2f(ms - M);
+        }
+        for (int d = threadIdx.x; d < DSA_VALUE_DIM; d += blockDim.x) {
+            float acc = 0.f;
+            for (int s = 0; s < S; ++s) {
+                const float ms = ml[(s * H + h) * 2];
+                if (ms == -INFINITY) continue;
+                const float w = ml[(s * H + h) * 2 + 1] * exp2f(ms - M);
+                acc += w * a.part_o[((static_cast<int64_t>(row) * S + s) * H + h) * DSA_VALUE_DIM + d];
+            }
+            a.out[(static_cast<int64_t>(row) * H + h) * DSA_VALUE_DIM + d] = wsum > 0.f ? acc / wsum : 0.f;
+        }
+        if (threadIdx.x == 0 && a.lse)
+            a.lse[static_cast<int64_t>(row) * H + h] =
+                wsum > 0.f ? (M + log2f(wsum)) * 0.6931471805599453f : -INFINITY;
+    }
+}
+
+template <int FMT>
+cudaError_t launch_fmt(const MlaArgs &a, cudaStream_t s) {
+    static int configured_device = -1;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (configured_device != dev) {
+        cudaError_t e =
+            cudaFuncSetAttribute(sparse_mla_kernel<FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        if (e != cudaSuccess) return e;
+        configured_device = dev;
+    }
+    sparse_mla_kernel<FMT><<<a.num_rows * a.splits, kThreads, kSmemBytes, s>>>(a);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess || a.splits == 1) return e;
+    mla_combine_kernel<<<a.num_rows, 256, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t mla_workspace_bytes(int32_t num_rows, int32_t num_heads, int32_t k) {
+    const int splits = (k + kMlaTokensPerSplit - 1) / kMlaTokensPerSplit;
+    if (splits <= 1) return 0;
+    const size_t o = static_cast<size_t>(num_rows) * splits * num_heads * DSA_VALUE_DIM * sizeof(float);
+    const size_t ml = static_cast<size_t>(num_rows) * splits * num_heads * 2 * sizeof(float);
+    return (o + 255) / 256 * 256 + ml;
+}
+
+cudaError_t launch_sparse_mla(const MlaArgs &a, cudaStream_t s) {
+    if (a.num_rows == 0) return cudaSuccess;
+    if (a.num_heads < 16 || a.num_heads > kMaxH || a.num_heads % 16 != 0) return cudaErrorInvalidValue;
+    if (a.format == DSA_LATENT_FP8) return launch_fmt<DSA_LATENT_FP8>(a, s);
+    if (a.format == DSA_LATENT_NVFP4) return launch_fmt<DSA_LATENT_NVFP4>(a, s);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace dsa

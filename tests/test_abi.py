@@ -1,0 +1,104 @@
+"""The C-ABI library loads and exports every entry point include/dsa.h
+declares; host-side argument checks reject bad calls before any launch.
+No test here needs a GPU: every call below fails validation on the host
+(or is pure host logic), so no CUDA context is created."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from prefill_dsa_indexer_gb300 import build as B
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    B.build()
+    import prefill_dsa_indexer_gb300 as P
+    return P.load_library()
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "dsa.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[\w]+\s*\*?\s*(dsa_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_layer_calls():
+    names = declared_functions()
+    for n in ("dsa_indexer_logits", "dsa_topk", "dsa_page_to_slot", "dsa_sparse_mla_decode", "dsa_sparse_mla_prefill"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for n in declared_functions():
+        assert hasattr(lib, n), n
+
+
+def test_python_binding_names_match_the_abi():
+    import prefill_dsa_indexer_gb300 as P
+    for n in declared_functions():
+        if n in ("dsa_version", "dsa_status_string"):
+            continue
+        assert hasattr(P, n[len("dsa_"):]), n
+    assert set(P.EXPORTED) == set(declared_functions())
+
+
+def test_status_strings_and_version(lib):
+    assert lib.dsa_version() >= 100
+    for code in range(-7, 1):
+        assert lib.dsa_status_string(code).decode() not in ("", "unknown status")
+    assert lib.dsa_status_string(-99).decode() == "unknown status"
+
+
+def test_workspace_size_is_host_logic(lib):
+    # 2048 tokens split 256 per CTA -> 8 partial outputs of 96 x 512 fp32 plus (max, sum) per head
+    got = lib.dsa_sparse_mla_workspace_size(4, 96, 2048)
+    assert got >= 4 * 8 * 96 * 512 * 4 + 4 * 8 * 96 * 2 * 4
+    assert lib.dsa_sparse_mla_workspace_size(4, 96, 256) == 0  # one split: no workspace
+    assert lib.dsa_sparse_mla_workspace_size(0, 96, 2048) == 0
+
+
+def test_host_validation_rejects_before_launch(lib):
+    import prefill_dsa_indexer_gb300 as P
+    fake = ctypes.c_void_p(0x10000)
+    # top-k: k outside [1, 2048]
+    assert lib.dsa_topk(fake, 4096, fake, 1, 4096, 0, fake, None, None) == P.ERR_UNSUPPORTED
+    assert lib.dsa_topk(fake, 4096, fake, 1, 4096, 4096, fake, None, None) == P.ERR_UNSUPPORTED
+    # top-k: logits stride shorter than max_ctx
+    assert lib.dsa_topk(fake, 100, fake, 1, 4096, 16, fake, None, None) == P.ERR_INVALID_ARG
+    # top-k: nothing to do
+    assert lib.dsa_topk(None, 0, None, 0, 0, 16, None, None, None) == P.OK
+    # indexer: unsupported page size, rows_per_group, bt too narrow, null cache
+    c = P._Cache(fake, P.KEY_FP8, 32, 10, 1.0)
+    r = P._Rows(fake, 1, 1, fake, fake, 1, 64, 1)
+    assert lib.dsa_indexer_logits(ctypes.byref(c), ctypes.byref(r), fake, fake, fake, 64, None, None) == P.ERR_UNSUPPORTED
+    c = P._Cache(fake, P.KEY_FP8, 64, 10, 1.0)
+    r = P._Rows(fake, 1, 1, fake, fake, 3, 64, 3)
+    assert lib.dsa_indexer_logits(ctypes.byref(c), ctypes.byref(r), fake, fake, fake, 64, None, None) == P.ERR_UNSUPPORTED
+    r = P._Rows(fake, 1, 1, fake, fake, 1, 4096, 1)
+    assert lib.dsa_indexer_logits(ctypes.byref(c), ctypes.byref(r), fake, fake, fake, 4096, None, None) == P.ERR_INVALID_ARG
+    assert lib.dsa_indexer_logits(None, ctypes.byref(r), fake, fake, fake, 4096, None, None) == P.ERR_INVALID_ARG
+    # sparse MLA: head count not a multiple of 16 / too many heads; decode without workspace
+    lc = P._Cache(fake, P.LATENT_FP8, 64, 10, 0.01)
+    for H in (8, 100, 128):
+        assert lib.dsa_sparse_mla_decode(ctypes.byref(lc), fake, H, fake, 1, 2048, 0.07, fake, fake, None, None, 0,
+                                         None) == P.ERR_UNSUPPORTED
+    assert lib.dsa_sparse_mla_decode(ctypes.byref(lc), fake, 96, fake, 1, 2048, 0.07, fake, fake, None, None, 0,
+                                     None) == P.ERR_WORKSPACE
+    bad = P._Cache(fake, 9, 64, 10, 0.01)
+    assert lib.dsa_sparse_mla_prefill(ctypes.byref(bad), fake, 96, fake, 1, 2048, 0.07, fake, fake, None, None, 0,
+                                      None) == P.ERR_UNSUPPORTED
+    # page -> slot: k < 1
+    r = P._Rows(fake, 1, 1, fake, fake, 1, 64, 1)
+    assert lib.dsa_page_to_slot(ctypes.byref(r), 10, fake, 0, fake, None, None) == P.ERR_INVALID_ARG
+
+
+def test_python_binding_refuses_cpu_tensors():
+    import torch
+    import prefill_dsa_indexer_gb300 as P
+    x = torch.zeros(4, 8)
+    with pytest.raises(P.DsaError):
+        P.topk(x, torch.zeros(4, dtype=torch.int32), 8, 4)

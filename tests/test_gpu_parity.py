@@ -1,0 +1,248 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle.
+
+Tolerances (written here, derived from the arithmetic and the method's
+stated bounds):
+  * indexer logits: FP8 products are exact and accumulate in fp32 on the
+    tensor cores, so |gpu - exact| <= 2^-13 * sum_h w_h s_t sum_i |q_hi k_ti|;
+  * top-k: bit-exact against the oracle's selection on the SAME (gpu) logits;
+  * end to end, a token selected by only one side must score within 1e-3
+    relative of the k-th oracle score;
+  * sparse MLA: max-abs <= 2e-2 and rel-L2 <= 1e-2 (FP8 latents), 3e-2
+    (NVFP4 latents); lse within 2e-3.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import prefill_dsa_indexer_gb300 as P
+from prefill_dsa_indexer_gb300 import inputs as I
+from tests import gpu_util as U
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from prefill_dsa_indexer_gb300 import build
+    build.build()
+    P.load_library()
+
+
+def _wl(name, ctx, rows=1, group=1, lat=I.LATENT_FP8, heads=96, k=2048, seed=5):
+    return I.small_workload(name, ctx, rows_per_req=rows, rows_per_group=group, lat_fmt=lat, heads=heads, k=k,
+                            seed=seed)
+
+
+INDEXER_CASES = {
+    "tiny_4k": I.workload("decode_tiny_4k"),
+    "ragged": _wl("ragged", [1, 63, 64, 65, 127, 128, 129, 2047, 2048, 2049, 3000, 5000]),
+    "verify_g4": _wl("verify", [3000, 4100], rows=4, group=4),
+    "pairs_g2": _wl("pairs", [700, 1500, 2500], rows=2, group=2),
+    "prefill_g8": _wl("prefill", [3000], rows=64, group=8),
+}
+
+
+def _check_logits(inp, got):
+    ref = U.oracle_logits(inp)
+    bound = U.logit_bound(inp)
+    rc = inp.np("row_ctx")
+    for r in range(len(rc)):
+        g = got[r, :rc[r]].astype(np.float64)
+        d = np.abs(g - ref[r, :rc[r]])
+        assert np.all(d <= bound[r]), (r, float(d.max()), float((d / bound[r]).max()))
+
+
+@pytest.mark.parametrize("case", sorted(INDEXER_CASES))
+def test_indexer_logits(case):
+    inp = U.gpu_inputs(INDEXER_CASES[case])
+    st = P.new_status()
+    lg = U.run_indexer(inp, st)
+    torch.cuda.synchronize()
+    P.check_status(st)
+    _check_logits(inp, lg.cpu().numpy())
+
+
+def test_indexer_leaves_masked_entries_untouched():
+    inp = U.gpu_inputs(_wl("mask", [100, 1000]))
+    lg = torch.full((2, 1000), 12345.0, device="cuda")
+    P.indexer_logits(inp.idx_pool, I.KEY_FP8, inp.block_table, inp.row_req, inp.row_ctx, inp.max_ctx, inp.q_idx,
+                     inp.head_w, logits=lg)
+    torch.cuda.synchronize()
+    assert torch.all(lg[0, 100:] == 12345.0)
+    assert torch.all(lg[0, :100] != 12345.0)
+
+
+def _topk_cases():
+    rng = np.random.default_rng(3)
+    cases = {}
+    v = rng.standard_normal((6, 9000)).astype(np.float32)
+    cases["normal"] = (v, np.array([9000, 8999, 4096, 2049, 2048, 17], dtype=np.int32), 2048)
+    t = (rng.integers(0, 50, (4, 6000)) / 8).astype(np.float32)  # heavy ties
+    cases["ties"] = (t, np.array([6000, 5000, 3000, 2100], dtype=np.int32), 2048)
+    c = np.zeros((2, 5000), dtype=np.float32)
+    c[1, ::3] = -0.0
+    cases["all_equal_signed_zero"] = (c, np.array([5000, 5000], dtype=np.int32), 2048)
+    big = (rng.standard_normal((2, 200000)) * 10 + 100).astype(np.float32)  # beyond the shared-memory row cache
+    cases["long_rows"] = (big, np.array([200000, 150001], dtype=np.int32), 2048)
+    s = rng.standard_normal((3, 3000)).astype(np.float32)
+    cases["small_k"] = (s, np.array([3000, 10, 1], dtype=np.int32), 5)
+    w = np.concatenate([np.full((1, 3000), 1e30, np.float32), np.full((1, 3000), -1e30, np.float32)])
+    w[0, 1500:] = np.float32(1e-30)
+    cases["extremes"] = (w, np.array([3000, 3000], dtype=np.int32), 2048)
+    return cases
+
+
+TOPK_CASES = _topk_cases()
+
+
+@pytest.mark.parametrize("case", sorted(TOPK_CASES))
+def test_topk_bit_exact(case):
+    v, ctx, k = TOPK_CASES[case]
+    st = P.new_status()
+    got = P.topk(torch.from_numpy(v).cuda(), torch.from_numpy(ctx).cuda(), v.shape[1], k, status=st)
+    torch.cuda.synchronize()
+    P.check_status(st)
+    ref = oracle.topk_f32(v, ctx, k)
+    assert np.array_equal(got.cpu().numpy(), ref)
+
+
+def test_topk_on_indexer_logits_bit_exact():
+    inp = U.gpu_inputs(INDEXER_CASES["ragged"])
+    lg = U.run_indexer(inp)
+    idx = P.topk(lg, inp.row_ctx, inp.max_ctx, 2048)
+    torch.cuda.synchronize()
+    ref = oracle.topk_f32(lg.cpu().numpy(), inp.np("row_ctx"), 2048)
+    assert np.array_equal(idx.cpu().numpy(), ref)
+
+
+def test_page_to_slot_exact():
+    inp = U.gpu_inputs(INDEXER_CASES["ragged"])
+    rng = np.random.default_rng(9)
+    rc = inp.np("row_ctx")
+    idx = np.full((len(rc), 64), -1, dtype=np.int32)
+    for r, L in enumerate(rc):
+        n = min(64, L)
+        idx[r, :n] = np.sort(rng.choice(L, size=n, replace=False))
+    st = P.new_status()
+    got = P.page_to_slot(inp.block_table, inp.row_req, inp.row_ctx, inp.max_ctx, inp.num_pages,
+                         torch.from_numpy(idx).cuda(), status=st)
+    torch.cuda.synchronize()
+    P.check_status(st)
+    ref = oracle.page_to_slot(inp.np("block_table"), inp.np("row_req"), idx)
+    assert np.array_equal(got.cpu().numpy(), ref)
+
+
+def test_page_to_slot_reports_bounds():
+    inp = U.gpu_inputs(_wl("b", [100]))
+    idx = torch.tensor([[0, 99, 100, -1]], dtype=torch.int32, device="cuda")  # 100 >= ctx
+    st = P.new_status()
+    got = P.page_to_slot(inp.block_table, inp.row_req, inp.row_ctx, inp.max_ctx, inp.num_pages, idx, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == P.ERR_BOUNDS
+    assert got[0, 2].item() == -1 and got[0, 3].item() == -1
+
+
+def _mla_case(inp, k, n_valid=None, seed=0):
+    """Random distinct positions per row (sorted), -1 padded; physical slots."""
+    rng = np.random.default_rng(seed)
+    rc, bt, rq = inp.np("row_ctx"), inp.np("block_table"), inp.np("row_req")
+    idx = np.full((len(rc), k), -1, dtype=np.int32)
+    for r, L in enumerate(rc):
+        n = min(k, L) if n_valid is None else min(n_valid, L)
+        idx[r, :n] = np.sort(rng.choice(L, size=n, replace=False))
+    return oracle.page_to_slot(bt, rq, idx)
+
+
+MLA_CASES = {
+    "fp8_decode_k2048": (_wl("m1", [3000, 5000, 2100]), 2048, None, "decode"),
+    "fp8_decode_ragged": (_wl("m2", [3000, 70, 1]), 2048, None, "decode"),
+    "fp8_prefill_k2048": (_wl("m3", [2500, 4000]), 2048, None, "prefill"),
+    "fp8_decode_partial": (_wl("m4", [3000, 3000]), 2048, 1000, "decode"),
+    "fp8_prefill_k100": (_wl("m5", [3000, 40]), 100, None, "prefill"),
+    "fp8_heads64": (_wl("m6", [3000], heads=64), 2048, None, "decode"),
+    "fp8_heads16": (_wl("m7", [3000], heads=16), 512, None, "prefill"),
+    "nvfp4_decode": (_wl("m8", [3000, 2500], lat=I.LATENT_NVFP4), 2048, None, "decode"),
+    "nvfp4_prefill": (_wl("m9", [2600], lat=I.LATENT_NVFP4), 2048, None, "prefill"),
+}
+
+
+@pytest.mark.parametrize("case", sorted(MLA_CASES))
+def test_sparse_mla(case):
+    wl, k, nv, mode = MLA_CASES[case]
+    inp = U.gpu_inputs(wl)
+    slots = _mla_case(inp, k, nv)
+    st = P.new_status()
+    fn = P.sparse_mla_decode if mode == "decode" else P.sparse_mla_prefill
+    out, lse = fn(inp.lat_pool, wl.lat_fmt, inp.tensor_scale, inp.q_mla, torch.from_numpy(slots).cuda(),
+                  U.SM_SCALE, status=st)
+    torch.cuda.synchronize()
+    P.check_status(st)
+    ref_o, ref_l = oracle.sparse_mla(inp.np("lat_pool"), U.ORACLE_FMT[wl.lat_fmt], inp.tensor_scale, inp.np("q_mla"),
+                                     slots, U.SM_SCALE)
+    tol = 3e-2 if wl.lat_fmt == I.LATENT_NVFP4 else 1e-2
+    max_abs, rel = U.mla_errors(out.cpu().numpy(), ref_o)
+    assert max_abs <= 2e-2 and rel <= tol, (max_abs, rel)
+    gl = lse.cpu().numpy()
+    assert np.array_equal(np.isneginf(gl), np.isneginf(ref_l))
+    fin = np.isfinite(ref_l)
+    assert np.all(np.abs(gl[fin] - ref_l[fin]) <= 2e-3)
+
+
+def test_sparse_mla_empty_rows():
+    inp = U.gpu_inputs(_wl("e", [300, 300]))
+    slots = np.full((2, 2048), -1, dtype=np.int32)
+    slots[1, :5] = U.oracle.page_to_slot(inp.np("block_table"), inp.np("row_req")[1:], np.arange(5, dtype=np.int32)[None])
+    out, lse = P.sparse_mla_decode(inp.lat_pool, I.LATENT_FP8, inp.tensor_scale, inp.q_mla,
+                                   torch.from_numpy(slots).cuda())
+    torch.cuda.synchronize()
+    assert torch.all(out[0] == 0) and torch.all(torch.isneginf(lse[0]))
+    assert torch.all(torch.isfinite(lse[1]))
+
+
+@pytest.mark.parametrize("name", ["decode_tiny_4k", "ragged", "verify_g4", "prefill_g8"])
+def test_layer_end_to_end(name):
+    wl = INDEXER_CASES.get(name) or I.workload(name)
+    inp = U.gpu_inputs(wl)
+    prefill = wl.rows_per_group == 8
+    layer = P.Layer(inp.idx_pool, wl.key_fmt, inp.lat_pool, wl.lat_fmt, inp.tensor_scale, inp.block_table,
+                    inp.max_ctx, wl.num_rows, wl.heads, wl.k, wl.rows_per_group, prefill=prefill)
+    out, lse = layer.run(inp.row_req, inp.row_ctx, inp.q_idx, inp.head_w, inp.q_mla)
+    torch.cuda.synchronize()
+    P.check_status(layer.status)
+    ref_lg = U.oracle_logits(inp)
+    ora_idx = oracle.topk_f64(np.nan_to_num(ref_lg, nan=-np.inf), inp.np("row_ctx"), wl.k)
+    gpu_idx = layer.idx.cpu().numpy()
+    for r in range(wl.num_rows):
+        ok, nd = U.set_diff_within_band(gpu_idx[r], ora_idx[r], ref_lg[r], wl.k)
+        assert ok, (r, nd)
+    # attention parity on the GPU's own selection
+    gslots = layer.slots.cpu().numpy()
+    ref_o, _ = oracle.sparse_mla(inp.np("lat_pool"), U.ORACLE_FMT[wl.lat_fmt], inp.tensor_scale, inp.np("q_mla"),
+                                 gslots, U.SM_SCALE)
+    max_abs, rel = U.mla_errors(out.cpu().numpy(), ref_o)
+    assert max_abs <= 2e-2 and rel <= 1e-2, (max_abs, rel)
+
+
+def test_layer_deterministic_and_batch_invariant():
+    wl = _wl("inv", [3000, 5000, 4100, 2200], seed=21)
+    inp = U.gpu_inputs(wl)
+    layer = P.Layer(inp.idx_pool, wl.key_fmt, inp.lat_pool, wl.lat_fmt, inp.tensor_scale, inp.block_table,
+                    inp.max_ctx, wl.num_rows)
+    runs = []
+    for _ in range(3):
+        o, l = layer.run(inp.row_req, inp.row_ctx, inp.q_idx, inp.head_w, inp.q_mla)
+        runs.append((o.clone(), l.clone(), layer.idx.clone()))
+    torch.cuda.synchronize()
+    for o, l, i in runs[1:]:
+        assert torch.equal(o, runs[0][0]) and torch.equal(l, runs[0][1]) and torch.equal(i, runs[0][2])
+    # row 2 alone gives the bit-identical result
+    one = P.Layer(inp.idx_pool, wl.key_fmt, inp.lat_pool, wl.lat_fmt, inp.tensor_scale, inp.block_table,
+                  inp.max_ctx, 1)
+    o1, l1 = one.run(inp.row_req[2:3].contiguous(), inp.row_ctx[2:3].contiguous(), inp.q_idx[2:3].contiguous(),
+                     inp.head_w[2:3].contiguous(), inp.q_mla[2:3].contiguous())
+    torch.cuda.synchronize()
+    assert torch.equal(one.idx[0], runs[0][2][2])
+    assert torch.equal(o1[0], runs[0][0][2]) and torch.equal(l1[0], runs[0][1][2])
