@@ -105,7 +105,8 @@ int dsa_indexer_logits(const dsa_cache *index_cache, const dsa_rows *rows, const
     int rc = check_rows(rows);
     if (rc != DSA_OK) return rc;
     if (index_cache->page_size != DSA_PAGE_SIZE) return DSA_ERR_UNSUPPORTED;
-    if (index_cache->format != DSA_KEY_FP8) return DSA_ERR_UNSUPPORTED;
+    if (index_cache->format != DSA_KEY_FP8 && index_cache->format != DSA_KEY_MXFP4) return DSA_ERR_UNSUPPORTED;
+    const bool mx = index_cache->format == DSA_KEY_MXFP4;
     const int G = rows->rows_per_group;
     if (G != 1 && G != 2 && G != 4 && G != 8) return DSA_ERR_UNSUPPORTED;
     if (rows->num_rows % G != 0) return DSA_ERR_INVALID_ARG;
@@ -120,7 +121,7 @@ int dsa_indexer_logits(const dsa_cache *index_cache, const dsa_rows *rows, const
     if (sms <= 0) return DSA_ERR_CUDA;
 
     CUtensorMap key_map, q_map;
-    if (!encode_rows128(&key_map, index_cache->base, pool_rows, DSA_PAGE_SIZE)) return DSA_ERR_CUDA;
+    if (!mx && !encode_rows128(&key_map, index_cache->base, pool_rows, DSA_PAGE_SIZE)) return DSA_ERR_CUDA;
     if (!encode_rows128(&q_map, q_idx, static_cast<uint64_t>(rows->num_rows) * DSA_INDEX_HEADS,
                         static_cast<uint32_t>(G * DSA_INDEX_HEADS)))
         return DSA_ERR_CUDA;
@@ -141,7 +142,8 @@ int dsa_indexer_logits(const dsa_cache *index_cache, const dsa_rows *rows, const
     for (int g0 = 0; g0 < num_groups; g0 += kIndexerMaxGroups) {
         a.group0 = g0;
         a.num_groups = num_groups - g0 < kIndexerMaxGroups ? num_groups - g0 : kIndexerMaxGroups;
-        cudaError_t e = launch_indexer_fp8(key_map, q_map, a, G, sms, static_cast<cudaStream_t>(stream));
+        cudaError_t e = mx ? launch_indexer_mxfp4(q_map, a, G, sms, static_cast<cudaStream_t>(stream))
+                           : launch_indexer_fp8(key_map, q_map, a, G, sms, static_cast<cudaStream_t>(stream));
         if (e != cudaSuccess) return DSA_ERR_CUDA;
     }
     return DSA_OK;

@@ -34,6 +34,10 @@ constexpr int kIndexerMaxGroups = 1024;
 cudaError_t launch_indexer_fp8(const CUtensorMap &key_map, const CUtensorMap &q_map, const IndexerArgs &a,
                                int rows_per_group, int num_sms, cudaStream_t s);
 
+// Launch the MXFP4-key indexer (in-kernel dequantisation to e4m3).
+cudaError_t launch_indexer_mxfp4(const CUtensorMap &q_map, const IndexerArgs &a, int rows_per_group, int num_sms,
+                                 cudaStream_t s);
+
 struct TopkArgs {
     const float *logits;
     int64_t logits_stride;
