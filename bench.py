@@ -37,17 +37,30 @@ FALLBACK_HBM_GBS = 6800.0
 ROTATE = 4  # independent copies of the caches; a step never re-reads what the last 3 steps read
 
 
+FALLBACK_BF16_TFLOPS = 1900.0
+FP8_OVER_BF16 = 2.0  # nominal dense ratio (4.5 vs 2.25 PFLOP/s)
+
+
 def _peaks():
+    """(HBM GB/s, dense FP8 TFLOP/s, source): measured copy bandwidth and cuBLAS bf16 burst
+    throughput of the GB300s; FP8 = measured bf16 x the nominal FP8/bf16 ratio."""
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
         with open(p) as f:
             d = json.load(f)
-        return float(d.get("hbm_gbs", FALLBACK_HBM_GBS)), "measured"
-    return FALLBACK_HBM_GBS, "fallback"
+        return (float(d.get("hbm_gbs", FALLBACK_HBM_GBS)),
+                float(d.get("bf16_tflops", FALLBACK_BF16_TFLOPS)) * FP8_OVER_BF16, "measured")
+    return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS * FP8_OVER_BF16, "fallback"
+
+
+def indexer_flops(wl) -> int:
+    """2 * 32 heads * 128 dims per (query row, visible key) pair."""
+    return int(2 * 32 * 128 * int(wl.row_ctx().astype(np.int64).sum()))
 
 
 class ClockSampler:
-    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+    """nvidia-smi samples (every 20 ms) of SM clock and throttle reasons, each stamped with
+    the host time it arrived; `summary(t0, t1)` keeps those taken during [t0, t1]."""
 
     FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -59,7 +72,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", "20"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
         except (FileNotFoundError, OSError):
@@ -68,7 +81,12 @@ class ClockSampler:
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.time(), line.strip()))
+
+    def wait_first(self, timeout=5.0):
+        t_end = time.time() + timeout
+        while self.proc is not None and not self.lines and time.time() < t_end:
+            time.sleep(0.01)
 
     def __exit__(self, *exc):
         if self.proc is not None:
@@ -78,10 +96,11 @@ class ClockSampler:
             except subprocess.TimeoutExpired:
                 self.proc.kill()
 
-    def summary(self):
+    def summary(self, t0, t1):
         sm, mx, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        window = [(t, ln) for t, ln in self.lines if t0 <= t <= t1 + 0.05]
+        for _, ln in window:
             parts = [p.strip() for p in ln.split(",")]
             if len(parts) != 6:
                 continue
@@ -130,34 +149,55 @@ def layer_algorithmic_bytes(wl, idx_bytes: int, lat_bytes: int) -> int:
 
 
 def run_reference(args, wl, rank):
-    """CPU oracle on a bounded sample of the workload (rows of one step)."""
+    """The CPU oracle, as it stands, on a bounded sample per step of the same workload.
+
+    Each step takes one query row: the indexer scan over a contiguous slice of S of its
+    cached keys, the top-k and slots of that slice, and the sparse MLA of H_s of its heads
+    over the 2048 selected tokens.  S and H_s are sized so the K + W steps take about two
+    and a half minutes; the row's full cost is extrapolated linearly in keys (indexer,
+    top-k) and in heads (MLA)."""
     import oracle
     from prefill_dsa_indexer_gb300 import inputs as I
-    sample_rows = int(os.environ.get("DSA_BENCH_ORACLE_ROWS", "2"))
     inp = I.make_inputs(wl, device="cuda" if torch.cuda.is_available() else "cpu")
     host = {n: inp.np(n) for n in ("idx_pool", "lat_pool", "block_table", "row_req", "row_ctx", "q_idx", "head_w",
                                     "q_mla")}
-    rows = np.arange(min(sample_rows, wl.num_rows))
+    L = int(host["row_ctx"][0])
+    H = wl.heads
+    sm = 1.0 / np.sqrt(192.0)
 
-    def step():
-        lg = oracle.indexer_logits(host["idx_pool"], wl.key_fmt, host["block_table"], host["row_req"][rows],
-                                   host["row_ctx"][rows], host["q_idx"][rows], host["head_w"][rows])
-        idx = oracle.topk_f64(lg, host["row_ctx"][rows], wl.k)
-        sl = oracle.page_to_slot(host["block_table"], host["row_req"][rows], idx)
-        oracle.sparse_mla(host["lat_pool"], 3 if wl.lat_fmt == 3 else 4, inp.tensor_scale, host["q_mla"][rows], sl,
-                          1.0 / np.sqrt(192.0))
+    def part(S, Hs, r=0):
+        rr = np.array([r])
+        ctx = np.array([S], dtype=np.int32)
+        t0 = time.perf_counter()
+        lg = oracle.indexer_logits(host["idx_pool"], wl.key_fmt, host["block_table"], host["row_req"][rr], ctx,
+                                   host["q_idx"][rr], host["head_w"][rr])
+        idx = oracle.topk_f64(lg, ctx, wl.k)
+        sl = oracle.page_to_slot(host["block_table"], host["row_req"][rr], idx)
+        t1 = time.perf_counter()
+        oracle.sparse_mla(host["lat_pool"], wl.lat_fmt, inp.tensor_scale,
+                          np.ascontiguousarray(host["q_mla"][rr, :Hs]), sl, sm)
+        t2 = time.perf_counter()
+        return t1 - t0, t2 - t1
 
+    budget = max(0.01, min(2.0, 150.0 / max(1, args.steps + args.warmup)))
+    ti, tm = part(min(L, 8192), 1)
+    S = int(min(L, max(wl.k, (0.5 * budget / max(ti, 1e-6)) * min(L, 8192))))
+    Hs = int(max(1, min(H, (0.5 * budget / max(tm, 1e-6)))))
     for _ in range(args.warmup):
-        step()
+        part(S, Hs)
+    est, wall = 0.0, 0.0
     t0 = time.perf_counter()
-    for _ in range(args.steps):
-        step()
-    dt = time.perf_counter() - t0
-    value = len(rows) * args.steps / dt
-    cores = oracle.num_threads()
-    sample = f"{len(rows)} of {wl.num_rows} query rows per step of {wl.name} (full indexer scan, top-k, MLA per row)"
+    for i in range(args.steps):
+        a, b = part(S, Hs, i % wl.num_rows)
+        est += a * L / S + b * H / Hs
+    wall = time.perf_counter() - t0
+    value = args.steps / est
+    cores = 1  # one query row per step: the oracle's OpenMP loop over rows runs one thread
+    sample = (f"per step 1 of {wl.num_rows} query rows of {wl.name}: indexer + top-k over {S} of its {L} keys, "
+              f"sparse MLA of {Hs} of {H} heads over the selected tokens; full-row time extrapolated linearly "
+              f"(keys, heads); {wall:.1f} s of CPU work")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * dt / args.steps,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * est / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": wl.name, "rows": wl.num_rows, "ctx": wl.ctx[0], "k": wl.k, "heads": wl.heads},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
@@ -166,15 +206,16 @@ def run_reference(args, wl, rank):
         print(json.dumps(line), flush=True)
 
 
-def cpu_baseline(wl, inp, budget_s=20.0):
-    """Time the oracle on whole rows of the workload until ~budget_s of CPU work."""
+def cpu_baseline(wl, inp, budget_s=12.0):
+    """The oracle on whole rows of the workload (all host threads, OpenMP over rows), cycling
+    over the rows until about budget_s of wall time."""
     import oracle
     host = {n: inp.np(n) for n in ("idx_pool", "lat_pool", "block_table", "row_req", "row_ctx", "q_idx", "head_w",
                                     "q_mla")}
     threads = oracle.num_threads()
     done, t_used, n = 0, 0.0, max(1, min(threads, wl.num_rows))
-    while t_used < budget_s and done < wl.num_rows:
-        rows = np.arange(done, min(wl.num_rows, done + n))
+    while t_used < budget_s:
+        rows = (np.arange(n) + done) % wl.num_rows
         t0 = time.perf_counter()
         lg = oracle.indexer_logits(host["idx_pool"], wl.key_fmt, host["block_table"], host["row_req"][rows],
                                    host["row_ctx"][rows], host["q_idx"][rows], host["head_w"][rows])
@@ -184,16 +225,17 @@ def cpu_baseline(wl, inp, budget_s=20.0):
                           1.0 / np.sqrt(192.0))
         t_used += time.perf_counter() - t0
         done += len(rows)
-    return {"value": done / t_used, "unit": UNIT, "cores": threads, "kind": "oracle",
-            "sample": f"{done} of {wl.num_rows} query rows of {wl.name} (full indexer scan, top-k, MLA), "
+    return {"value": done / t_used, "unit": UNIT, "cores": n, "kind": "oracle",
+            "sample": f"{done} query rows of {wl.name} (whole rows: full indexer scan, top-k, MLA), "
                       f"{t_used:.1f} s"}
 
 
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--copies", type=int, default=ROTATE, help="independent cache copies rotated across steps")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="decode_b8_128k_fp8")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -224,9 +266,10 @@ def main():
     import prefill_dsa_indexer_gb300 as P
 
     inp = I.make_inputs(wl, device="cuda")
-    prefill = wl.rows_per_group == 8 and wl.rows_per_req > 8
+    prefill = wl.rows_per_req > 8
     layers = []
-    for c in range(ROTATE):
+    copies = max(1, args.copies)
+    for c in range(copies):
         idx_pool = inp.idx_pool if c == 0 else inp.idx_pool.clone()
         lat_pool = inp.lat_pool if c == 0 else inp.lat_pool.clone()
         layers.append(P.Layer(idx_pool, wl.key_fmt, lat_pool, wl.lat_fmt, inp.tensor_scale, inp.block_table,
@@ -234,7 +277,7 @@ def main():
     stream = torch.cuda.current_stream()
 
     def step(i, ev=None):
-        L = layers[i % ROTATE]
+        L = layers[i % len(layers)]
         if ev is not None:
             ev[0].record(stream)
         P.indexer_logits(L.idx_pool, L.key_fmt, L.block_table, inp.row_req, inp.row_ctx, L.max_ctx, inp.q_idx,
@@ -263,11 +306,14 @@ def main():
         dist.barrier()
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
+        clk.wait_first()
+        h0 = time.time()
         t_start.record(stream)
         for i in range(args.steps):
             step(i, evs[i])
         t_stop.record(stream)
         torch.cuda.synchronize()
+        h1 = time.time()
     if dist is not None:
         dist.barrier()
     total_ms = t_start.elapsed_time(t_stop)
@@ -290,7 +336,7 @@ def main():
     d2h = host_out.numel() * 4 + host_lse.numel() * 4
 
     def e2e_step(i):
-        L = layers[i % ROTATE]
+        L = layers[i % len(layers)]
         for n, t in pinned.items():
             dev_in[n].copy_(t, non_blocking=True)
         L.run(dev_in["row_req"], dev_in["row_ctx"], dev_in["q_idx"], dev_in["head_w"], dev_in["q_mla"],
@@ -322,8 +368,19 @@ def main():
     lat_tok = I.LATENT_TOKEN_BYTES[wl.lat_fmt]
     idx_bytes = indexer_algorithmic_bytes(wl, idx_tok)
     layer_bytes = layer_algorithmic_bytes(wl, idx_tok, lat_tok)
-    peak, peak_kind = _peaks()
-    achieved = idx_bytes / (idx_ms / 1000.0) / 1e9
+    hbm_peak, fp8_peak, peak_kind = _peaks()
+    if prefill:
+        flops = indexer_flops(wl)
+        achieved = flops / (idx_ms / 1000.0) / 1e12
+        roof = {"kernel": "indexer_fp8_kernel<8>", "bound": "tensor", "achieved": achieved, "peak": fp8_peak,
+                "unit": "TFLOP/s", "frac": achieved / fp8_peak,
+                "peak_kind": f"{peak_kind} bf16 burst x {FP8_OVER_BF16} (FP8/bf16 nominal)",
+                "algorithmic_flops": flops, "ms_per_launch": idx_ms}
+    else:
+        achieved = idx_bytes / (idx_ms / 1000.0) / 1e9
+        roof = {"kernel": "indexer_fp8_kernel<1>" if wl.key_fmt == I.KEY_FP8 else "indexer_mxfp4_kernel<1>",
+                "bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
+                "peak_kind": peak_kind, "algorithmic_bytes": idx_bytes, "ms_per_launch": idx_ms}
     traffic = None
     tfile = os.path.join(ROOT, "profiles", "traffic.json")
     if os.path.exists(tfile):
@@ -338,18 +395,16 @@ def main():
         "config": {"workload": wl.name, "batch": len(wl.ctx), "rows": wl.num_rows, "ctx": wl.ctx[0], "k": wl.k,
                    "heads": wl.heads, "index_heads": 32, "page": 64, "key_bytes": idx_tok, "latent_bytes": lat_tok,
                    "parallelism": f"replicas{world}" if world > 1 else "single-gpu",
-                   "l2": f"inputs > L2: {ROTATE} rotating copies of the caches "
-                         f"({(inp.idx_pool.numel() + inp.lat_pool.numel()) * ROTATE / 1e9:.2f} GB)"},
+                   "l2": f"inputs > L2: {copies} rotating copies of the caches "
+                         f"({(inp.idx_pool.numel() + inp.lat_pool.numel()) * copies / 1e9:.2f} GB)"},
         "layer_hbm_gbs": layer_bytes / (ms_per_step / 1000.0) / 1e9,
         "layer_algorithmic_bytes": layer_bytes,
         "layer_frac_of_8tbs": layer_bytes / (ms_per_step / 1000.0) / 8e12,
-        "roofline": {"kernel": "indexer_fp8_kernel", "bound": "hbm", "achieved": achieved, "peak": peak,
-                     "unit": "GB/s", "frac": achieved / peak, "peak_kind": peak_kind, "traffic": traffic,
-                     "algorithmic_bytes": idx_bytes, "ms_per_launch": idx_ms},
+        "roofline": dict(roof, traffic=traffic),
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e2e_ms / args.steps},
         "gpu_launches": launches_per_step * args.steps,
-        "clocks": clk.summary(),
+        "clocks": clk.summary(h0, h1),
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl, inp)

@@ -260,23 +260,35 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const MlaArgs a
         tmem_alloc(tmem_slot, kTmemCols);
         tmem_relinquish();
     }
-    // ---- Q: bf16 -> fp16, 128-byte swizzled K-major, block c (64 dims) at c * H * 128
+    // ---- Q: bf16 -> fp16, 128-byte swizzled K-major, block c (64 dims) at c * H * 128.
+    // All of a thread's loads are issued before any conversion (one HBM latency, not 18).
     {
+        constexpr int kUnits = DSA_LATENT_DIM / 8;                       // 8-dim units per head
+        constexpr int kPerThread = (kMaxH * kUnits + kThreads - 1) / kThreads;  // 18
         const uint16_t *qg = a.q + static_cast<int64_t>(row) * H * DSA_LATENT_DIM;
+        const int total = H * kUnits;
+        int4 v[kPerThread];
+#pragma unroll
+        for (int i = 0; i < kPerThread; ++i) {
+            const int e = tid + i * kThreads;
+            if (e < total) v[i] = *reinterpret_cast<const int4 *>(qg + static_cast<int64_t>(e) * 8);
+        }
         bool range_err = false;
-        for (int e = tid; e < H * (DSA_LATENT_DIM / 8); e += kThreads) {
-            const int h = e / (DSA_LATENT_DIM / 8), u = e % (DSA_LATENT_DIM / 8);  // 8-dim unit
-            const int4 v = *reinterpret_cast<const int4 *>(qg + h * DSA_LATENT_DIM + u * 8);
-            const uint32_t w[4] = {static_cast<uint32_t>(v.x), static_cast<uint32_t>(v.y),
-                                   static_cast<uint32_t>(v.z), static_cast<uint32_t>(v.w)};
+#pragma unroll
+        for (int i = 0; i < kPerThread; ++i) {
+            const int e = tid + i * kThreads;
+            if (e >= total) break;
+            const int h = e / kUnits, u = e % kUnits;
+            const uint32_t w[4] = {static_cast<uint32_t>(v[i].x), static_cast<uint32_t>(v[i].y),
+                                   static_cast<uint32_t>(v[i].z), static_cast<uint32_t>(v[i].w)};
             const float sc = (u >= DSA_VALUE_DIM / 8) ? q_rope_scale : 1.0f;
             uint32_t o[4];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const float lo = __uint_as_float(w[i] << 16) * sc, hi = __uint_as_float(w[i] & 0xffff0000u) * sc;
+            for (int j = 0; j < 4; ++j) {
+                const float lo = __uint_as_float(w[j] << 16) * sc, hi = __uint_as_float(w[j] & 0xffff0000u) * sc;
                 if (!(fabsf(lo) <= 65504.f) || !(fabsf(hi) <= 65504.f)) range_err = true;
                 __half2 hh = __floats2half2_rn(lo, hi);
-                o[i] = *reinterpret_cast<uint32_t *>(&hh);
+                o[j] = *reinterpret_cast<uint32_t *>(&hh);
             }
             const int c = u >> 3, uu = u & 7;
             *reinterpret_cast<int4 *>(qs + c * H * 128 + sw128(h, uu)) = make_int4(o[0], o[1], o[2], o[3]);
@@ -484,32 +496,34 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const MlaArgs a
     }
 }
 
-// Merge the splits of each row: O = sum_s w_s O_s / sum_s w_s, w_s = l_s 2^(m_s - M).
-__global__ void mla_combine_kernel(const MlaArgs a) {
-    const int row = blockIdx.x, H = a.num_heads, S = a.splits;
+// Merge the splits of each (row, head): O = sum_s w_s O_s / sum_s w_s with
+// w_s = l_s 2^(m_s - M), M = max_s m_s (log2 units).  One CTA per (row, head),
+// four output dims per thread.
+__global__ void __launch_bounds__(128) mla_combine_kernel(const MlaArgs a) {
+    const int H = a.num_heads, S = a.splits;
+    const int row = blockIdx.x / H, h = blockIdx.x % H;
     const float *ml = a.part_ml + static_cast<int64_t>(row) * S * H * 2;
-    for (int h = 0; h < H; ++h) {
-        float M = -INFINITY;
-        for (int s = 0; s < S; ++s) M = fmaxf(M, ml[(s * H + h) * 2]);
-        float wsum = 0.f;
-        for (int s = 0; s < S; ++s) {
-            const float ms = ml[(s * H + h) * 2];
-            wsum += (ms == -INFINITY) ? 0.f : ml[(s * H + h) * 2 + 1] * exp2f(ms - M);
-        }
-        for (int d = threadIdx.x; d < DSA_VALUE_DIM; d += blockDim.x) {
-            float acc = 0.f;
-            for (int s = 0; s < S; ++s) {
-                const float ms = ml[(s * H + h) * 2];
-                if (ms == -INFINITY) continue;
-                const float w = ml[(s * H + h) * 2 + 1] * exp2f(ms - M);
-                acc += w * a.part_o[((static_cast<int64_t>(row) * S + s) * H + h) * DSA_VALUE_DIM + d];
-            }
-            a.out[(static_cast<int64_t>(row) * H + h) * DSA_VALUE_DIM + d] = wsum > 0.f ? acc / wsum : 0.f;
-        }
-        if (threadIdx.x == 0 && a.lse)
-            a.lse[static_cast<int64_t>(row) * H + h] =
-                wsum > 0.f ? (M + log2f(wsum)) * 0.6931471805599453f : -INFINITY;
+    float M = -INFINITY;
+    for (int s = 0; s < S; ++s) M = fmaxf(M, ml[(s * H + h) * 2]);
+    float wsum = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s = 0; s < S; ++s) {
+        const float ms = ml[(s * H + h) * 2];
+        if (ms == -INFINITY) continue;
+        const float w = ml[(s * H + h) * 2 + 1] * exp2f(ms - M);
+        wsum += w;
+        const float4 o = reinterpret_cast<const float4 *>(
+            a.part_o + ((static_cast<int64_t>(row) * S + s) * H + h) * DSA_VALUE_DIM)[threadIdx.x];
+        acc.x = fmaf(w, o.x, acc.x);
+        acc.y = fmaf(w, o.y, acc.y);
+        acc.z = fmaf(w, o.z, acc.z);
+        acc.w = fmaf(w, o.w, acc.w);
     }
+    const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+    reinterpret_cast<float4 *>(a.out + (static_cast<int64_t>(row) * H + h) * DSA_VALUE_DIM)[threadIdx.x] =
+        make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+    if (threadIdx.x == 0 && a.lse)
+        a.lse[static_cast<int64_t>(row) * H + h] = wsum > 0.f ? (M + log2f(wsum)) * 0.6931471805599453f : -INFINITY;
 }
 
 template <int FMT>
@@ -526,7 +540,7 @@ cudaError_t launch_fmt(const MlaArgs &a, cudaStream_t s) {
     sparse_mla_kernel<FMT><<<a.num_rows * a.splits, kThreads, kSmemBytes, s>>>(a);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess || a.splits == 1) return e;
-    mla_combine_kernel<<<a.num_rows, 256, 0, s>>>(a);
+    mla_combine_kernel<<<a.num_rows * a.num_heads, DSA_VALUE_DIM / 4, 0, s>>>(a);
     return cudaGetLastError();
 }
 

@@ -6,18 +6,26 @@
 // section "Day-0 zero-mismatch RL"): the k largest logits of [0, L_r), ties
 // to the lower position, reported in ascending position order, -1 padded.
 //
-// Method: radix selection on order-preserving 32-bit keys.  The first
-// histogram spans the row's actual key range [min, max] (2048 bins, bin
-// width a power of two), so the bins spread even when all logits sit within a
-// few octaves; the bin holding the k-th key is refined on a compacted
-// candidate list in shared memory until its width is one key, which gives
-// the exact threshold key T and how many keys equal to T are taken.  A last
-// pass compacts the selection in position order with a block-wide prefix
-// sum, so the output is deterministic and independent of thread timing.
-// Rows up to kCacheElems keys are read from HBM once and kept in shared
-// memory for all passes.
+// Method: radix selection on order-preserving 32-bit keys, one thread-block
+// cluster per row.  The row is cut into one contiguous chunk per CTA of the
+// cluster (2..8 CTAs for long rows), so a row is read by several SMs at once;
+// a chunk of up to kCacheElems keys is read from HBM once and kept in
+// shared memory for every pass.  Each pass builds a local 2048-bin histogram;
+// the CTAs add each other's histograms through distributed shared memory, so
+// every CTA reaches the same decision.  The first histogram spans the row's
+// actual key range [min, max] with power-of-two bins, so the bins spread even
+// when all logits sit within a few octaves; the bin holding the k-th key is
+// compacted into a candidate list per CTA and refined (at most three rounds)
+// down to the exact threshold key T and the number of keys equal to T to
+// take.  A last pass writes the selection in position order: block prefix
+// sums inside a chunk, the counts of the lower-ranked CTAs of the cluster as
+// the chunk's offset.  Output order and values never depend on timing.
+#include <cooperative_groups.h>
+
 #include "kernels.h"
 #include "ptx.cuh"
+
+namespace cg = cooperative_groups;
 
 namespace dsa {
 
@@ -28,21 +36,23 @@ constexpr int kWarps = kThreads / 32;
 constexpr int kBins = 2048;
 constexpr int kCacheElems = 40960;
 constexpr int kCandCap = 4096;
+constexpr int kMaxCluster = 8;
 
 struct TopkSmem {
     uint32_t cache[kCacheElems];
     uint32_t hist[kBins];
-    uint32_t cand_key[kCandCap];
-    int32_t cand_idx[kCandCap];
+    uint32_t cand[kCandCap];
     unsigned long long scan[kWarps + 1];
     uint32_t red[2 * kWarps];
+    uint32_t mm[2];   // this CTA's chunk key range (read by the cluster)
+    uint32_t cnt[2];  // this CTA's chunk counts of keys > T and == T (read by the cluster)
     uint32_t sel_bin, sel_above, sel_count;
     uint32_t ncand;
     int32_t bad;
 };
 
 // Order-preserving map float -> uint32 (larger float -> larger key);
-// -0 folds onto +0; NaN maps below every number.
+// -0 folds onto +0; NaN maps below every number and is reported.
 __device__ __forceinline__ uint32_t f2key(float f, bool &nan) {
     uint32_t u = __float_as_uint(f);
     if (f != f) {
@@ -62,7 +72,7 @@ __device__ __forceinline__ unsigned long long warp_incl_scan(unsigned long long 
     return v;
 }
 
-// Exclusive block-wide prefix sum; `total` receives the sum over the block.
+// Exclusive block-wide prefix sum; `total` receives the block's sum.
 __device__ unsigned long long block_excl_scan(unsigned long long v, TopkSmem &s, unsigned long long &total) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     unsigned long long incl = warp_incl_scan(v, lane);
@@ -81,38 +91,83 @@ __device__ unsigned long long block_excl_scan(unsigned long long v, TopkSmem &s,
     return r;
 }
 
+// Calls f(i, key) for every key of the chunk: from the shared-memory copy, or
+// from global memory (16-byte loads, four per thread in flight) when the chunk
+// is longer than the copy.
+template <typename F>
+__device__ __forceinline__ void for_each_key(const TopkSmem &s, const float *src, int n, bool cached, bool &nan,
+                                             F &&f) {
+    if (cached) {
+        for (int i = threadIdx.x; i < n; i += kThreads) f(i, s.cache[i]);
+        return;
+    }
+    const bool vec = (reinterpret_cast<uintptr_t>(src) & 15) == 0;
+    int i0 = 0;
+    if (vec) {
+        const int n16 = n & ~(16 * kThreads - 1);
+        for (; i0 < n16; i0 += 16 * kThreads) {
+            float4 v[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                v[u] = reinterpret_cast<const float4 *>(src + i0)[u * kThreads + threadIdx.x];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int i = i0 + 4 * (u * kThreads + threadIdx.x);
+                f(i, f2key(v[u].x, nan));
+                f(i + 1, f2key(v[u].y, nan));
+                f(i + 2, f2key(v[u].z, nan));
+                f(i + 3, f2key(v[u].w, nan));
+            }
+        }
+    }
+    for (int i = i0 + threadIdx.x; i < n; i += kThreads) f(i, f2key(src[i], nan));
+}
+
+__device__ __forceinline__ uint32_t key_at(const TopkSmem &s, const float *src, int i, bool cached) {
+    bool nan = false;
+    return cached ? s.cache[i] : f2key(src[i], nan);
+}
+
 __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const TopkArgs a) {
     extern __shared__ uint8_t smem_raw[];
     TopkSmem &s = *reinterpret_cast<TopkSmem *>(smem_raw);
+    cg::cluster_group cluster = cg::this_cluster();
+    const int CL = static_cast<int>(cluster.num_blocks());
+    const int crank = static_cast<int>(cluster.block_rank());
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int row = blockIdx.x;
+    const int row = blockIdx.x / CL;
     const int k = a.k;
     int32_t *out = a.idx_out + static_cast<int64_t>(row) * k;
     int n = a.row_ctx[row];
     if (n < 0 || n > a.max_ctx) {
-        if (tid == 0) report(a.status, DSA_ERR_BOUNDS);
+        if (tid == 0 && crank == 0) report(a.status, DSA_ERR_BOUNDS);
         n = min(max(n, 0), a.max_ctx);
     }
-    if (n <= k) {
-        for (int i = tid; i < k; i += kThreads) out[i] = i < n ? i : -1;
+    if (n <= k) {  // the same branch for every CTA of the cluster: no cluster barrier below
+        if (crank == 0)
+            for (int i = tid; i < k; i += kThreads) out[i] = i < n ? i : -1;
         return;
     }
-    const float *src = a.logits + static_cast<int64_t>(row) * a.logits_stride;
-    const bool cached = n <= kCacheElems;
+    // this CTA's chunk [c0, c0 + nloc) of the row; chunk starts are multiples of 4 elements
+    const int ch = ((n + CL - 1) / CL + 3) & ~3;
+    const int c0 = min(n, crank * ch);
+    const int nloc = min(n, c0 + ch) - c0;
+    const float *src = a.logits + static_cast<int64_t>(row) * a.logits_stride + c0;
+    const bool cached = ch <= kCacheElems;
     if (tid == 0) {
         s.bad = 0;
         s.ncand = 0;
     }
+    __syncthreads();
 
-    // ---- pass A: key range (and the shared-memory copy of the row)
+    // ---- key range of the chunk (and its shared-memory copy)
     uint32_t lo = 0xffffffffu, hi = 0u;
-    bool nan = false;
-    for (int i = tid; i < n; i += kThreads) {
-        uint32_t key = f2key(src[i], nan);
+    bool nan = false, ignore = false;
+    for_each_key(s, src, nloc, false, nan, [&](int i, uint32_t key) {
         if (cached) s.cache[i] = key;
         lo = min(lo, key);
         hi = max(hi, key);
-    }
+    });
     if (nan) s.bad = 1;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
@@ -133,18 +188,21 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const TopkArgs a) {
             hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, o));
         }
         if (lane == 0) {
-            s.red[0] = lo;
-            s.red[1] = hi;
+            s.mm[0] = lo;
+            s.mm[1] = hi;
         }
     }
-    __syncthreads();
     if (tid == 0 && s.bad) report(a.status, DSA_ERR_RANGE);
-    uint32_t base = s.red[0];
-    uint32_t top = s.red[1];  // current key interval [base, top]
+    cluster.sync();
+    uint32_t base = 0xffffffffu, top = 0u;
+    for (int r = 0; r < CL; ++r) {
+        const uint32_t *mm = cluster.map_shared_rank(s.mm, r);
+        base = min(base, mm[0]);
+        top = max(top, mm[1]);
+    }
     uint32_t need = static_cast<uint32_t>(k);
-    __syncthreads();
 
-    // ---- refine the interval holding the k-th largest key down to one key
+    // ---- refine the key interval [base, top] holding the k-th largest key down to one key
     bool use_cand = false;
     while (top > base) {
         const uint32_t span = top - base;
@@ -155,85 +213,106 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const TopkArgs a) {
         if (use_cand) {
             const int nc = static_cast<int>(s.ncand);
             for (int i = tid; i < nc; i += kThreads) {
-                uint32_t key = s.cand_key[i];
+                const uint32_t key = s.cand[i];
                 if (key >= base && key <= top) atomicAdd(&s.hist[(key - base) >> shift], 1u);
             }
         } else {
-            for (int i = tid; i < n; i += kThreads) {
-                bool dummy = false;
-                uint32_t key = cached ? s.cache[i] : f2key(src[i], dummy);
+            for_each_key(s, src, nloc, cached, ignore, [&](int, uint32_t key) {
                 if (key >= base && key <= top) atomicAdd(&s.hist[(key - base) >> shift], 1u);
-            }
+            });
         }
-        __syncthreads();
-        // suffix counts from the top bin: thread t owns bins 2047-2t and 2046-2t
+        cluster.sync();
+        // cluster-wide counts of this thread's two bins (2047-2t and 2046-2t)
         const int b1 = kBins - 1 - 2 * tid, b0 = b1 - 1;
-        const uint32_t c1 = s.hist[b1], c0 = s.hist[b0];
+        uint32_t c1 = 0, c0v = 0;
+        for (int r = 0; r < CL; ++r) {
+            const uint32_t *h = cluster.map_shared_rank(s.hist, r);
+            c1 += h[b1];
+            c0v += h[b0];
+        }
         unsigned long long tot;
-        const uint32_t above1 = static_cast<uint32_t>(block_excl_scan(c1 + c0, s, tot));
+        const uint32_t above1 = static_cast<uint32_t>(block_excl_scan(c1 + c0v, s, tot));
         if (above1 < need && need <= above1 + c1) {
             s.sel_bin = b1;
             s.sel_above = above1;
             s.sel_count = c1;
-        } else if (above1 + c1 < need && need <= above1 + c1 + c0) {
+        } else if (above1 + c1 < need && need <= above1 + c1 + c0v) {
             s.sel_bin = b0;
             s.sel_above = above1 + c1;
-            s.sel_count = c0;
+            s.sel_count = c0v;
         }
-        __syncthreads();
+        cluster.sync();  // every CTA has read every histogram; selection visible block-wide
         const uint32_t sb = s.sel_bin, sa = s.sel_above, sc = s.sel_count;
         need -= sa;
         const uint32_t nbase = base + (sb << shift);
         const unsigned long long bin_top = static_cast<unsigned long long>(nbase) + (1ull << shift) - 1ull;
-        const uint32_t ntop = static_cast<uint32_t>(min(static_cast<unsigned long long>(top), bin_top));
         base = nbase;
-        top = ntop;
+        top = static_cast<uint32_t>(min(static_cast<unsigned long long>(top), bin_top));
         if (top > base && !use_cand && sc <= static_cast<uint32_t>(kCandCap)) {
-            for (int i = tid; i < n; i += kThreads) {
-                bool dummy = false;
-                uint32_t key = cached ? s.cache[i] : f2key(src[i], dummy);
-                if (key >= base && key <= top) {
-                    uint32_t p = atomicAdd(&s.ncand, 1u);
-                    s.cand_key[p] = key;
-                    s.cand_idx[p] = i;
-                }
-            }
+            // the cluster holds at most kCandCap keys in [base, top]; so does this chunk
+            for_each_key(s, src, nloc, cached, ignore, [&](int, uint32_t key) {
+                if (key >= base && key <= top) s.cand[atomicAdd(&s.ncand, 1u)] = key;
+            });
             use_cand = true;
         }
         __syncthreads();
     }
-    const uint32_t T = base;  // exact threshold key; `need` keys equal to T are taken
+    const uint32_t T = base;  // exact threshold key; `need` keys equal to T are taken (lowest positions)
 
+    // ---- counts per chunk, then the chunk's offset from the lower-ranked CTAs
+    uint32_t my_gt = 0, my_eq = 0;
+    for_each_key(s, src, nloc, cached, ignore, [&](int, uint32_t key) {
+        my_gt += key > T;
+        my_eq += key == T;
+    });
+    {
+        unsigned long long tot;
+        block_excl_scan((static_cast<unsigned long long>(my_gt) << 32) | my_eq, s, tot);
+        if (tid == 0) {
+            s.cnt[0] = static_cast<uint32_t>(tot >> 32);
+            s.cnt[1] = static_cast<uint32_t>(tot);
+        }
+    }
+    cluster.sync();
+    unsigned long long run = 0;  // (keys > T) << 32 | (keys == T) before the current position
+    for (int r = 0; r < crank; ++r) {
+        const uint32_t *c = cluster.map_shared_rank(s.cnt, r);
+        run += (static_cast<unsigned long long>(c[0]) << 32) | c[1];
+    }
     // ---- ordered compaction: every key > T, plus the first `need` keys == T
-    unsigned long long run = 0;  // (count of keys > T) << 32 | (count of keys == T) before this chunk
-    for (int c0 = 0; c0 < n; c0 += 4 * kThreads) {
+    for (int b0 = 0; b0 < nloc; b0 += 4 * kThreads) {
         uint32_t kv[4];
         uint32_t ngt = 0, neq = 0;
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            const int i = c0 + 4 * tid + j;
-            bool dummy = false;
-            kv[j] = i < n ? (cached ? s.cache[i] : f2key(src[i], dummy)) : 0u;
-            if (i < n) {
+            const int i = b0 + 4 * tid + j;
+            kv[j] = i < nloc ? key_at(s, src, i, cached) : 0u;
+            if (i < nloc) {
                 ngt += kv[j] > T;
                 neq += kv[j] == T;
             }
         }
         unsigned long long tot;
-        unsigned long long pre = block_excl_scan((static_cast<unsigned long long>(ngt) << 32) | neq, s, tot);
-        pre += run;
+        unsigned long long pre = block_excl_scan((static_cast<unsigned long long>(ngt) << 32) | neq, s, tot) + run;
         uint32_t gt_before = static_cast<uint32_t>(pre >> 32), eq_before = static_cast<uint32_t>(pre);
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            const int i = c0 + 4 * tid + j;
-            if (i >= n) break;
+            const int i = b0 + 4 * tid + j;
+            if (i >= nloc) break;
             const bool gt = kv[j] > T, eq = kv[j] == T;
-            if (gt || (eq && eq_before < need)) out[gt_before + min(eq_before, need)] = i;
+            if (gt || (eq && eq_before < need)) out[gt_before + min(eq_before, need)] = c0 + i;
             gt_before += gt;
             eq_before += eq;
         }
         run += tot;
     }
+    cluster.sync();  // no CTA leaves while a peer may still read its shared memory
+}
+
+int cluster_size_for(int max_ctx) {
+    int cl = 1;
+    while (cl < kMaxCluster && (max_ctx + cl - 1) / cl > kCacheElems) cl *= 2;
+    return cl;
 }
 
 }  // namespace
@@ -249,8 +328,20 @@ cudaError_t launch_topk(const TopkArgs &a, cudaStream_t s) {
         configured_device = dev;
     }
     if (a.num_rows == 0) return cudaSuccess;
-    topk_kernel<<<a.num_rows, kThreads, sizeof(TopkSmem), s>>>(a);
-    return cudaGetLastError();
+    const int cl = cluster_size_for(a.max_ctx);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(a.num_rows * cl));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = sizeof(TopkSmem);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = cl;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, topk_kernel, a);
 }
 
 }  // namespace dsa
