@@ -190,6 +190,30 @@ int dsa_sparse_mla_prefill(const dsa_cache *latent_cache, const uint16_t *q, int
                            float *lse, int32_t *dev_status, void *workspace, size_t workspace_bytes,
                            void *stream);
 
+/*
+ * dsa_sparse_mla_decode without a caller workspace.  The paper has no
+ * counterpart to this call; it exists for callers that cannot allocate
+ * device memory: a host framework whose allocator has reserved the device's
+ * memory for its own pools and hands out no extra buffers, a plugin that
+ * only sees the tensors it is given, or a latency-critical loop that must not
+ * call cudaMalloc (it can block and synchronise the device).
+ *
+ * Same arguments, semantics and results as dsa_sparse_mla_decode, minus the
+ * workspace.  The split-K partial outputs live in a fixed array in the
+ * library's own device memory, sized for DSA_NOALLOC_MAX_ROWS rows of
+ * k <= 2048 tokens and num_heads <= 96 (12,632,064 bytes, held by every GPU
+ * that loads the library until the process exits).  Larger calls return
+ * DSA_ERR_WORKSPACE without launching.  The first call on a device looks up
+ * the array's address with that device current; make it before capturing
+ * any stream.  All calls share the array: calls whose kernels may overlap on
+ * the GPU (unordered streams) race on it; calls ordered on one stream do not.
+ * No part of the array needs to start zeroed.
+ */
+#define DSA_NOALLOC_MAX_ROWS 8
+int dsa_sparse_mla_decode_noalloc(const dsa_cache *latent_cache, const uint16_t *q, int32_t num_heads,
+                                  const int32_t *slots, int32_t num_rows, int32_t k, float sm_scale, float *out,
+                                  float *lse, int32_t *dev_status, void *stream);
+
 /* Workspace bytes dsa_sparse_mla_decode needs for num_rows rows of k slots. */
 size_t dsa_sparse_mla_workspace_size(int32_t num_rows, int32_t num_heads, int32_t k);
 

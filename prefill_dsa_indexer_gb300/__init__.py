@@ -73,6 +73,8 @@ def load_library(path: str | None = None):
         fn = getattr(lib, name)
         fn.restype = ctypes.c_int
         fn.argtypes = [ctypes.POINTER(_Cache), P, I32, P, I32, I32, F, P, P, P, P, ctypes.c_size_t, P]
+    lib.dsa_sparse_mla_decode_noalloc.restype = ctypes.c_int
+    lib.dsa_sparse_mla_decode_noalloc.argtypes = [ctypes.POINTER(_Cache), P, I32, P, I32, I32, F, P, P, P, P]
     lib.dsa_sparse_mla_workspace_size.restype = ctypes.c_size_t
     lib.dsa_sparse_mla_workspace_size.argtypes = [I32, I32, I32]
     if path is None:
@@ -81,7 +83,9 @@ def load_library(path: str | None = None):
 
 
 EXPORTED = ("dsa_version", "dsa_status_string", "dsa_indexer_logits", "dsa_topk", "dsa_page_to_slot",
-            "dsa_sparse_mla_decode", "dsa_sparse_mla_prefill", "dsa_sparse_mla_workspace_size")
+            "dsa_sparse_mla_decode", "dsa_sparse_mla_prefill", "dsa_sparse_mla_workspace_size",
+            "dsa_sparse_mla_decode_noalloc")
+NOALLOC_MAX_ROWS = 8
 
 
 def _ptr(t):
@@ -190,6 +194,20 @@ def sparse_mla_decode(lat_pool, lat_fmt, tensor_scale, q, slots, sm_scale=DEFAUL
     """dsa_sparse_mla_decode: (out fp32 [R, H, 512], lse fp32 [R, H]); q is bf16 (or its int16 bits)."""
     return _mla("dsa_sparse_mla_decode", lat_pool, lat_fmt, tensor_scale, q, slots, sm_scale, out, lse, workspace,
                 status, stream)
+
+
+def sparse_mla_decode_noalloc(lat_pool, lat_fmt, tensor_scale, q, slots, out, lse, sm_scale=DEFAULT_SM_SCALE,
+                              status=None, stream=None):
+    """dsa_sparse_mla_decode_noalloc: as sparse_mla_decode, with the split-K scratch kept in the
+    library's own fixed device array instead of a workspace (for callers that cannot allocate;
+    at most NOALLOC_MAX_ROWS rows).  `out` and `lse` must be preallocated."""
+    R, H, _ = q.shape
+    c = _cache(lat_pool, lat_fmt, tensor_scale)
+    rc = load_library().dsa_sparse_mla_decode_noalloc(ctypes.byref(c), _ptr(q), H, _ptr(slots), R, slots.shape[1],
+                                                      float(sm_scale), _ptr(out), _ptr(lse), _ptr(status),
+                                                      _stream(stream))
+    _check(rc, "dsa_sparse_mla_decode_noalloc")
+    return out, lse
 
 
 def sparse_mla_prefill(lat_pool, lat_fmt, tensor_scale, q, slots, sm_scale=DEFAULT_SM_SCALE, out=None, lse=None,
