@@ -35,7 +35,7 @@ def build(force: bool = False, extra_flags: tuple[str, ...] = (), out: str | Non
     if not force and os.path.exists(out) and os.path.getmtime(out) >= os.path.getmtime(_SRC):
         return out
     tmp = out + ".tmp"
-    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp", *extra_flags, _SRC, "-o", tmp, "-lm"]
+    cmd = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fPIC", "-shared", "-fopenmp", *extra_flags, _SRC, "-o", tmp, "-lm"]
     subprocess.run(cmd, check=True)
     os.replace(tmp, out)
     return out
@@ -70,6 +70,12 @@ def load(path: str | None = None):
         lib.oracle_page_to_slot.argtypes = [P, I64, P, I32, P, I32, P]
         lib.oracle_sparse_mla.restype = I32
         lib.oracle_sparse_mla.argtypes = [P, I32, I64, D, P, I32, P, I32, I32, D, P, P]
+        lib.oracle_e4m3_encode.restype = ctypes.c_uint8
+        lib.oracle_e4m3_encode.argtypes = [ctypes.c_float]
+        lib.oracle_e2m1_encode.restype = ctypes.c_uint8
+        lib.oracle_e2m1_encode.argtypes = [ctypes.c_float]
+        lib.oracle_cache_insert.restype = I32
+        lib.oracle_cache_insert.argtypes = [P, I32, P, I32, ctypes.c_float, I64, P, I32, P, P]
         lib.oracle_num_threads.restype = I32
         lib.oracle_set_num_threads.argtypes = [I32]
         if path is None:
@@ -175,6 +181,30 @@ def sparse_mla(lat_pool, fmt, tensor_scale, q_bf16_bits, slots, sm_scale, lib=No
     if rcode != OK:
         raise ValueError(f"oracle_sparse_mla failed: {rcode}")
     return out, lse
+
+
+def e4m3_encode(x: float, lib=None) -> int:
+    return (lib or load()).oracle_e4m3_encode(x)
+
+
+def e2m1_encode(x: float, lib=None) -> int:
+    return (lib or load()).oracle_e2m1_encode(x)
+
+
+def cache_insert(idx_pool, key_fmt, lat_pool, lat_fmt, tensor_scale, slots, keys_bf16_bits, lat_bf16_bits, lib=None):
+    """Write new tokens into copies of the pools; returns (idx_pool, lat_pool) numpy copies."""
+    lib = lib or load()
+    ip = np.array(idx_pool, dtype=np.uint8, copy=True, order="C")
+    lp = np.array(lat_pool, dtype=np.uint8, copy=True, order="C")
+    sl = _c(slots, np.int32)
+    k = _c(keys_bf16_bits, np.uint16)
+    x = _c(lat_bf16_bits, np.uint16)
+    num_pages = ip.shape[0] if ip.ndim == 2 else ip.size // index_page_bytes(key_fmt, lib)
+    rc = lib.oracle_cache_insert(_p(ip), key_fmt, _p(lp), lat_fmt, float(tensor_scale), num_pages, _p(sl),
+                                 sl.shape[0], _p(k), _p(x))
+    if rc != OK:
+        raise ValueError(f"oracle_cache_insert failed: {rc}")
+    return ip, lp
 
 
 def num_threads(lib=None) -> int:

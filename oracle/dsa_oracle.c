@@ -342,6 +342,144 @@ int oracle_sparse_mla(const uint8_t *pool, int fmt, int64_t num_pages, double te
     return err;
 }
 
+/* ---------------------------------------------------------------- encoders
+ *
+ * Quantisation of a new token before it is written into the caches (the
+ * fused decode front end quantises the index key and writes the new token's
+ * key and latent, vLLM blog "Day-0 support for Kimi K3.1 Pro", section
+ * "Low-latency decode: fused DSA decode path").  Inputs are bf16; every
+ * scale and quotient is computed in fp32 in the order written here, and the
+ * rounding to a code is round-to-nearest-even from that fp32 value, so an
+ * implementation that follows the same order reproduces the bytes exactly.
+ */
+
+/* fp32 -> e4m3 code, round to nearest even, saturating to +-448; NaN -> 0x7F. */
+uint8_t oracle_e4m3_encode(float xf) {
+    double x = xf;
+    if (x != x) return 0x7F;
+    int s = signbit(x) ? 1 : 0;
+    double a = fabs(x);
+    if (a >= 448.0) return (uint8_t)((s << 7) | 0x7E);
+    if (a == 0.0) return (uint8_t)(s << 7);
+    int e;
+    frexp(a, &e);           /* a in [2^(e-1), 2^e) */
+    int ue = e - 1;
+    if (ue < -6) ue = -6;   /* below the normal range the quantum stays 2^-9 */
+    double q = ldexp(1.0, ue - 3);
+    double r = nearbyint(a / q) * q;
+    if (r == 0.0) return (uint8_t)(s << 7);
+    if (r > 448.0) r = 448.0;
+    frexp(r, &e);
+    ue = e - 1;
+    uint8_t code;
+    if (ue < -6) code = (uint8_t)nearbyint(r / ldexp(1.0, -9));              /* subnormal: m * 2^-9 */
+    else code = (uint8_t)(((ue + 7) << 3) | (int)nearbyint((r / ldexp(1.0, ue) - 1.0) * 8.0));
+    return (uint8_t)((s << 7) | code);
+}
+
+/* fp32 -> e2m1 nibble, round to nearest even, saturating to +-6. */
+uint8_t oracle_e2m1_encode(float xf) {
+    double x = xf;
+    int s = signbit(x) ? 1 : 0;
+    double a = fabs(x);
+    if (a != a) a = 0.0;
+    double q = a < 2.0 ? 0.5 : (a < 4.0 ? 1.0 : 2.0);
+    double r = nearbyint(a / q) * q;
+    if (r > 6.0) r = 6.0;
+    static const double mag[8] = {0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0};
+    uint8_t code = 0;
+    for (uint8_t c = 0; c < 8; ++c)
+        if (mag[c] == r) code = c;
+    return (uint8_t)((s << 3) | code);
+}
+
+static float bf16_to_f32(uint16_t h) {
+    uint32_t u = (uint32_t)h << 16;
+    float f;
+    memcpy(&f, &u, 4);
+    return f;
+}
+
+/* Write n new tokens into the caches at physical slots[i] (-1: skipped).
+ * keys: [n, 128] bf16; latents: [n, 576] bf16.
+ *   FP8 key:     s = amax/448 (1 if amax = 0), code = e4m3(x / s), scale stored fp32
+ *   MXFP4 key:   per 32 values E = floor(log2 amax) - 2 + 127 clamped to [0, 254]
+ *                (E = 0 for an all-zero block), code = e2m1(x * 2^(127 - E))
+ *   FP8 latent:  code = e4m3(x / tensor_scale)
+ *   NVFP4 latent: per 16 values scale code = e4m3(amax / 6), code = e2m1(x / scale)
+ *                (all codes 0 when the scale is 0); RoPE dims e4m3(x / tensor_scale). */
+int oracle_cache_insert(uint8_t *idx_pool, int key_fmt, uint8_t *lat_pool, int lat_fmt, float tensor_scale,
+                        int64_t num_pages, const int32_t *slots, int n, const uint16_t *keys,
+                        const uint16_t *latents) {
+    if (oracle_index_page_bytes(key_fmt) < 0 || oracle_latent_page_bytes(lat_fmt) < 0) return OR_ERR_ARG;
+    int err = OR_OK;
+    for (int i = 0; i < n; ++i) {
+        int32_t slot = slots[i];
+        if (slot < 0) continue;
+        if ((int64_t)slot >= num_pages * OR_PAGE) {
+            err = OR_ERR_BOUNDS;
+            continue;
+        }
+        int64_t page = slot / OR_PAGE;
+        int j = slot % OR_PAGE;
+        const uint16_t *k = keys + (int64_t)i * OR_IDX_DIM;
+        uint8_t *ip = idx_pool + page * oracle_index_page_bytes(key_fmt);
+        if (key_fmt == OR_KEY_FP8) {
+            float amax = 0.0f;
+            for (int d = 0; d < OR_IDX_DIM; ++d) amax = fmaxf(amax, fabsf(bf16_to_f32(k[d])));
+            float sc = amax > 0.0f ? amax / 448.0f : 1.0f;
+            for (int d = 0; d < OR_IDX_DIM; ++d) ip[(int64_t)j * OR_IDX_DIM + d] = oracle_e4m3_encode(bf16_to_f32(k[d]) / sc);
+            memcpy(ip + OR_PAGE * OR_IDX_DIM + 4 * j, &sc, 4);
+        } else {
+            uint8_t *codes = ip + (int64_t)j * (OR_IDX_DIM / 2);
+            uint8_t *es = ip + OR_PAGE * (OR_IDX_DIM / 2) + (int64_t)j * (OR_IDX_DIM / 32);
+            for (int b = 0; b < OR_IDX_DIM / 32; ++b) {
+                float amax = 0.0f;
+                for (int d = 0; d < 32; ++d) amax = fmaxf(amax, fabsf(bf16_to_f32(k[32 * b + d])));
+                int E = 0;
+                if (amax > 0.0f) {
+                    int e;
+                    frexpf(amax, &e);
+                    E = (e - 1) - 2 + 127;
+                    if (E < 0) E = 0;
+                    if (E > 254) E = 254;
+                }
+                es[b] = (uint8_t)E;
+                for (int d = 0; d < 32; d += 2) {
+                    uint8_t lo = oracle_e2m1_encode(ldexpf(bf16_to_f32(k[32 * b + d]), 127 - E));
+                    uint8_t hi = oracle_e2m1_encode(ldexpf(bf16_to_f32(k[32 * b + d + 1]), 127 - E));
+                    codes[(32 * b + d) / 2] = (uint8_t)(lo | (hi << 4));
+                }
+            }
+        }
+        const uint16_t *x = latents + (int64_t)i * OR_LAT_DIM;
+        uint8_t *lp = lat_pool + page * oracle_latent_page_bytes(lat_fmt);
+        if (lat_fmt == OR_LATENT_FP8) {
+            for (int d = 0; d < OR_LAT_DIM; ++d)
+                lp[(int64_t)j * OR_LAT_DIM + d] = oracle_e4m3_encode(bf16_to_f32(x[d]) / tensor_scale);
+        } else {
+            uint8_t *codes = lp + (int64_t)j * (OR_V_DIM / 2);
+            uint8_t *scs = lp + OR_PAGE * (OR_V_DIM / 2) + (int64_t)j * (OR_V_DIM / 16);
+            uint8_t *rope = lp + OR_PAGE * (OR_V_DIM / 2 + OR_V_DIM / 16) + (int64_t)j * (OR_LAT_DIM - OR_V_DIM);
+            for (int b = 0; b < OR_V_DIM / 16; ++b) {
+                float amax = 0.0f;
+                for (int d = 0; d < 16; ++d) amax = fmaxf(amax, fabsf(bf16_to_f32(x[16 * b + d])));
+                uint8_t scode = oracle_e4m3_encode(amax / 6.0f);
+                float sc = (float)oracle_e4m3_decode(scode);
+                scs[b] = scode;
+                for (int d = 0; d < 16; d += 2) {
+                    uint8_t lo = sc > 0.0f ? oracle_e2m1_encode(bf16_to_f32(x[16 * b + d]) / sc) : 0;
+                    uint8_t hi = sc > 0.0f ? oracle_e2m1_encode(bf16_to_f32(x[16 * b + d + 1]) / sc) : 0;
+                    codes[(16 * b + d) / 2] = (uint8_t)(lo | (hi << 4));
+                }
+            }
+            for (int d = 0; d < OR_LAT_DIM - OR_V_DIM; ++d)
+                rope[d] = oracle_e4m3_encode(bf16_to_f32(x[OR_V_DIM + d]) / tensor_scale);
+        }
+    }
+    return err;
+}
+
 /* ------------------------------------------------------------------- misc */
 
 int oracle_num_threads(void) {

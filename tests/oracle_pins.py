@@ -326,6 +326,110 @@ def pin_mla_invariances(lib):
     np.testing.assert_allclose(out_r, out, rtol=1e-12, atol=1e-13)
 
 
+def _nearest_even(x, values, codes):
+    """Brute force: the representable value closest to x; ties to the code with an even
+    mantissa bit (lowest code bit 0)."""
+    d = [abs(x - v) for v in values]
+    best = min(d)
+    cands = [c for c, dd in zip(codes, d) if dd == best]
+    even = [c for c in cands if c % 2 == 0]
+    return (even or cands)[0]
+
+
+def pin_e4m3_encode(lib):
+    rng = np.random.default_rng(17)
+    xs = np.concatenate([rng.standard_normal(4000) * 50, rng.standard_normal(2000) * 1e-2,
+                         rng.uniform(-460, 460, 2000)]).astype(np.float32)
+    # every midpoint between neighbouring finite codes (ties) and every code value itself
+    vals = ref_e4m3(np.arange(0x7F, dtype=np.uint8))
+    mids = ((vals[1:] + vals[:-1]) / 2).astype(np.float32)
+    xs = np.concatenate([xs, vals.astype(np.float32), mids, -mids, [0.0, -0.0]]).astype(np.float32)
+    got = np.array([oracle.e4m3_encode(float(x), lib) for x in xs], dtype=np.uint8)
+    ref = torch.from_numpy(xs).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(got, ref), "e4m3 encode vs torch cast (RNE)"
+    for big in (448.0, 463.9, 464.0, 1e6, -1e6):
+        assert oracle.e4m3_encode(big, lib) == (0x7E | (0x80 if big < 0 else 0)), "saturation"
+    assert oracle.e4m3_encode(float("nan"), lib) == 0x7F
+
+
+def pin_e2m1_encode(lib):
+    mags = list(E2M1[:8])
+    rng = np.random.default_rng(18)
+    xs = np.concatenate([rng.uniform(-7, 7, 3000), [0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0, 6.0, 9.0, -5.0]])
+    for x in xs.astype(np.float32):
+        a = min(abs(float(x)), 6.0)
+        want = _nearest_even(a, mags, list(range(8))) | (8 if np.signbit(x) else 0)
+        assert oracle.e2m1_encode(float(x), lib) == want, float(x)
+
+
+def _bf16_bits(x):
+    return torch.from_numpy(np.asarray(x, dtype=np.float32)).to(torch.bfloat16).view(torch.int16).numpy().view(
+        np.uint16)
+
+
+def pin_cache_insert(lib):
+    """New tokens written into each format: FP8 bytes equal torch's RNE cast of the fp32
+    quotients; MXFP4/NVFP4 codes equal brute-force nearest-even choices; every written
+    value decodes back within half a code step."""
+    rng = np.random.default_rng(19)
+    n, pages = 40, 4
+    keys = _bf16_bits(rng.standard_normal((n, 128)) * rng.uniform(0.01, 10, (n, 1)))
+    lats = _bf16_bits(rng.standard_normal((n, 576)))
+    keys[3, :] = 0  # an all-zero key
+    slots = rng.permutation(pages * 64)[:n].astype(np.int32)
+    slots[5] = -1
+    ts = 0.0123
+    kf = ref_bf16(keys).astype(np.float32)
+    xf = ref_bf16(lats).astype(np.float32)
+    for kfmt, lfmt in ((oracle.KEY_FP8, oracle.LATENT_FP8), (oracle.KEY_MXFP4, oracle.LATENT_NVFP4)):
+        ip0 = np.zeros((pages, oracle.index_page_bytes(kfmt, lib)), np.uint8)
+        lp0 = np.zeros((pages, oracle.latent_page_bytes(lfmt, lib)), np.uint8)
+        ip, lp = oracle.cache_insert(ip0, kfmt, lp0, lfmt, ts, slots, keys, lats, lib=lib)
+        ok = slots >= 0
+        sl = slots[ok]
+        if kfmt == oracle.KEY_FP8:
+            amax = np.abs(kf[ok]).max(axis=1)
+            sc = np.where(amax > 0, amax / np.float32(448.0), np.float32(1.0)).astype(np.float32)
+            want = torch.from_numpy((kf[ok] / sc[:, None]).astype(np.float32)).to(torch.float8_e4m3fn).view(
+                torch.uint8).numpy()
+            codes = ip[:, :64 * 128].reshape(-1, 64, 128)[sl // 64, sl % 64]
+            got_sc = ip[:, 64 * 128:].copy().view(np.float32).reshape(-1, 64)[sl // 64, sl % 64]
+            assert np.array_equal(codes, want) and np.array_equal(got_sc, sc), "FP8 key insert"
+            wantl = torch.from_numpy((xf[ok] / np.float32(ts)).astype(np.float32)).to(torch.float8_e4m3fn).view(
+                torch.uint8).numpy()
+            assert np.array_equal(lp.reshape(-1, 64, 576)[sl // 64, sl % 64], wantl), "FP8 latent insert"
+        else:
+            k, _ = ref_index_keys(ip, kfmt, sl.astype(np.int64))
+            e = ip[:, 64 * 64:].reshape(-1, 64, 4)[sl // 64, sl % 64].astype(np.int64)
+            for t in range(len(sl)):
+                for b in range(4):
+                    blk = kf[ok][t, 32 * b:32 * b + 32].astype(np.float64)
+                    am = np.abs(blk).max()
+                    E = 0 if am == 0 else int(np.clip(np.floor(np.log2(am)) - 2 + 127, 0, 254))
+                    assert e[t, b] == E, "MX scale"
+                    step = 2.0 ** (E - 127)
+                    for d in range(0, 32, 7):
+                        x = blk[d] / step
+                        want = _nearest_even(min(abs(x), 6.0), mags := list(E2M1[:8]), list(range(8)))
+                        assert abs(k[t, 32 * b + d]) == E2M1[want] * step, "MX element"
+            kv = ref_latents(lp, lfmt, ts, sl.astype(np.int64))
+            scs = ref_e4m3(lp[:, 64 * 256:64 * 288].reshape(-1, 64, 32)[sl // 64, sl % 64])
+            for t in range(len(sl)):
+                for b in range(0, 32, 5):
+                    blk = xf[ok][t, 16 * b:16 * b + 16]
+                    am = np.float32(np.abs(blk).max())
+                    want_sc = torch.tensor([am / np.float32(6.0)], dtype=torch.float32).to(torch.float8_e4m3fn).to(
+                        torch.float64).item()
+                    assert scs[t, b] == want_sc, "NV scale"
+                    for d in range(16):
+                        x = float(np.float32(blk[d] / np.float32(want_sc))) if want_sc > 0 else 0.0
+                        want = _nearest_even(min(abs(x), 6.0), list(E2M1[:8]), list(range(8)))
+                        assert abs(kv[t, 16 * b + d]) == E2M1[want] * want_sc, "NV element"
+            wantr = torch.from_numpy((xf[ok][:, 512:] / np.float32(ts)).astype(np.float32)).to(
+                torch.float8_e4m3fn).to(torch.float64).numpy() * ts
+            assert np.array_equal(kv[:, 512:], wantr), "NVFP4 RoPE dims"
+
+
 ALL_PINS = {
     "e4m3": pin_e4m3,
     "e2m1": pin_e2m1,
@@ -343,4 +447,7 @@ ALL_PINS = {
     "mla_full_selection": pin_mla_full_selection_is_dense_causal,
     "mla_closed_forms": pin_mla_closed_forms,
     "mla_invariances": pin_mla_invariances,
+    "e4m3_encode": pin_e4m3_encode,
+    "e2m1_encode": pin_e2m1_encode,
+    "cache_insert": pin_cache_insert,
 }

@@ -53,6 +53,17 @@ MUTATIONS = [
     ("output not normalised", "o[d] /= l;", "o[d] /= 1.0;"),
     ("value uses rope dims", "o[d] += p * kv[(int64_t)t * OR_LAT_DIM + d];",
      "o[d] += p * kv[(int64_t)t * OR_LAT_DIM + d + 64];"),
+    ("e4m3 rounds half away from zero", "double r = nearbyint(a / q) * q;\n    if (r == 0.0)",
+     "double r = floor(a / q + 0.5) * q;\n    if (r == 0.0)"),
+    ("e4m3 saturates to 480", "if (a >= 448.0) return (uint8_t)((s << 7) | 0x7E);",
+     "if (a >= 480.0) return (uint8_t)((s << 7) | 0x7F);"),
+    ("e4m3 subnormal quantum", "if (ue < -6) ue = -6;   /* below", "if (ue < -7) ue = -7;   /* below"),
+    ("e2m1 binade boundary", "double q = a < 2.0 ? 0.5 : (a < 4.0 ? 1.0 : 2.0);",
+     "double q = a < 1.0 ? 0.5 : (a < 4.0 ? 1.0 : 2.0);"),
+    ("FP8 key scale over 240", "float sc = amax > 0.0f ? amax / 448.0f : 1.0f;", "float sc = amax > 0.0f ? amax / 240.0f : 1.0f;"),
+    ("MX exponent offset", "E = (e - 1) - 2 + 127;", "E = (e - 1) - 1 + 127;"),
+    ("NVFP4 scale over 4", "uint8_t scode = oracle_e4m3_encode(amax / 6.0f);", "uint8_t scode = oracle_e4m3_encode(amax / 4.0f);"),
+    ("insert nibble order", "codes[(16 * b + d) / 2] = (uint8_t)(lo | (hi << 4));", "codes[(16 * b + d) / 2] = (uint8_t)(hi | (lo << 4));"),
 ]
 
 
@@ -61,7 +72,8 @@ def _build_mutant(src_text, tmpdir, i):
     with open(path, "w") as f:
         f.write(src_text)
     so = os.path.join(tmpdir, f"m{i}.so")
-    subprocess.run(["gcc", "-O1", "-std=c11", "-fPIC", "-shared", "-fopenmp", path, "-o", so, "-lm"], check=True)
+    subprocess.run(["gcc", "-O1", "-std=c11", "-ffp-contract=off", "-fPIC", "-shared", "-fopenmp", path, "-o", so,
+                    "-lm"], check=True)
     return so
 
 
