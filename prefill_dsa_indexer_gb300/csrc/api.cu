@@ -206,6 +206,7 @@ static int sparse_mla_common(const dsa_cache *lat, const uint16_t *q, int32_t nu
     a.splits = 1;
     if (decode) {
         const int splits = (k + kMlaTokensPerSplit - 1) / kMlaTokensPerSplit;
+        if (splits > 16) return DSA_ERR_UNSUPPORTED;  // the split merge holds at most 16 parts
         if (splits > 1) {
             const size_t need = mla_workspace_bytes(num_rows, num_heads, k);
             if (ws == nullptr || ws_bytes < need) return DSA_ERR_WORKSPACE;

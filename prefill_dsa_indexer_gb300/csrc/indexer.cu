@@ -23,14 +23,13 @@
 //     reduction sum_h w_h * relu(acc_h) runs in registers, scale by s_t
 //     (s_t > 0 commutes with the relu), mask t >= L_r and write coalesced
 //     fp32 logits.
-#include "kernels.h"
-#include "ptx.cuh"
+#include "indexer_common.cuh"
 
 namespace dsa {
 
 namespace {
 
-constexpr int kTileKeys = 128;
+constexpr int kTileKeys = kIdxTileKeys;
 constexpr int kIdxPageBytes = DSA_PAGE_SIZE * (DSA_INDEX_DIM + 4);  // 8448
 constexpr int kIdxPageRows = kIdxPageBytes / 128;                    // 66 rows of 128 B
 
@@ -62,24 +61,6 @@ struct IdxCfg {
     static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 };
 
-// Sequential walk over a CTA's contiguous range of the global tile list.
-struct TileWalker {
-    const int32_t *prefix;  // [num_groups + 1] tile prefix sums (shared memory)
-    int g;
-    __device__ void seek(int32_t w, int num_groups) {
-        int lo = 0, hi = num_groups;  // find g with prefix[g] <= w < prefix[g+1]
-        while (hi - lo > 1) {
-            int mid = (lo + hi) >> 1;
-            if (prefix[mid] <= w) lo = mid;
-            else hi = mid;
-        }
-        g = lo;
-    }
-    __device__ void advance(int32_t w) {
-        while (prefix[g + 1] <= w) ++g;
-    }
-};
-
 template <int G>
 __global__ void __launch_bounds__(IdxCfg<G>::kThreads, 1)
     indexer_fp8_kernel(const __grid_constant__ CUtensorMap key_map, const __grid_constant__ CUtensorMap q_map,
@@ -108,27 +89,8 @@ __global__ void __launch_bounds__(IdxCfg<G>::kThreads, 1)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int ng = a.num_groups;
 
-    // ---- prologue: per-group request, longest context, tile counts and their prefix sums
-    for (int g = tid; g < ng; g += blockDim.x) {
-        const int row0 = (a.group0 + g) * G;
-        const int req = a.row_req[row0];
-        int mx = 0;
-        bool bad = req < 0 || req >= a.num_requests;
-        for (int j = 0; j < G; ++j) {
-            int c = a.row_ctx[row0 + j];
-            if (a.row_req[row0 + j] != req || c < 0 || c > a.max_ctx) bad = true;
-            mx = max(mx, min(max(c, 0), a.max_ctx));
-        }
-        if (bad) {
-            report(a.status, DSA_ERR_BOUNDS);
-            mx = 0;
-        }
-        greq[g] = req;
-        gmax[g] = mx;
-        prefix[g + 1] = (mx + kTileKeys - 1) / kTileKeys;
-    }
+    plan_groups<G>(a, prefix, greq, gmax);
     if (tid == 0) {
-        prefix[0] = 0;
         *abort = 0;
         for (int s = 0; s < C::kStages; ++s) {
             mbar_init(&full[s], 1);
@@ -148,71 +110,90 @@ __global__ void __launch_bounds__(IdxCfg<G>::kThreads, 1)
         tmem_relinquish();
     }
     __syncthreads();
-    if (warp == 0) {  // inclusive scan of prefix[1..ng] by one warp
-        const int per = (ng + 31) / 32;
-        const int b = 1 + lane * per, e = min(ng + 1, b + per);
-        int sum = 0;
-        for (int i = b; i < e; ++i) sum += prefix[i];
-        int incl = sum;
-        for (int o = 1; o < 32; o <<= 1) {
-            int v = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += v;
-        }
-        int run = incl - sum;
-        for (int i = b; i < e; ++i) {
-            run += prefix[i];
-            prefix[i] = run;
-        }
-    }
+    if (warp == 0) plan_scan(prefix, ng, lane);
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
-    const int32_t total = prefix[ng];
-    const int32_t per = total / gridDim.x, rem = total % gridDim.x;
-    const int32_t w_begin = blockIdx.x * per + (static_cast<int32_t>(blockIdx.x) < rem ? static_cast<int32_t>(blockIdx.x) : rem);
-    const int32_t w_end = w_begin + per + (blockIdx.x < rem ? 1 : 0);
+    int32_t w_begin, w_end;
+    plan_share(prefix[ng], w_begin, w_end);
 
     constexpr uint32_t kIdesc = make_idesc(128, C::N, 0, 0, false, false);
 
     if (w_begin < w_end) {
-        if (warp == 0 && lane == 0) {
-            // ------------------------------------------------ TMA producer
-            prefetch_tensormap(&key_map);
-            prefetch_tensormap(&q_map);
+        if (warp == 0) {
+            // ------------------------------------------------ TMA producer (whole warp)
+            // Lane j looks up the page ids of tile base + j ahead of time (one coalesced
+            // batch of block-table reads per 32 tiles); lane 0 issues the copies.
+            if (lane == 0) {
+                prefetch_tensormap(&key_map);
+                prefetch_tensormap(&q_map);
+            }
             TileWalker wk{prefix, 0};
             wk.seek(w_begin, ng);
             int cur = -1, gc = -1;
             int32_t it = 0;
-            for (int32_t w = w_begin; w < w_end; ++w, ++it) {
-                wk.advance(w);
-                const int g = wk.g;
-                if (g != cur) {
-                    ++gc;
-                    cur = g;
-                    const int qb = gc & 1;
-                    if (!mbar_wait(&qempty[qb], ((gc >> 1) & 1) ^ 1, abort, a.status)) break;
-                    mbar_arrive_expect_tx(&qfull[qb], C::kQBytes);
-                    tma_load_2d(qbuf + qb * C::kQBytes, &q_map, &qfull[qb], 0, (a.group0 + g) * G * DSA_INDEX_HEADS);
-                }
-                const int stage = it % C::kStages;
-                if (!mbar_wait(&empty[stage], ((it / C::kStages) & 1) ^ 1, abort, a.status)) break;
-                const int kt = w - prefix[g];
-                const int nkeys = min(kTileKeys, gmax[g] - kt * kTileKeys);
-                const int32_t *bt = a.block_table + static_cast<int64_t>(greq[g]) * a.bt_stride;
-                const int npages = (nkeys + DSA_PAGE_SIZE - 1) / DSA_PAGE_SIZE;
-                mbar_arrive_expect_tx(&full[stage], npages * (DSA_PAGE_SIZE * 128 + DSA_PAGE_SIZE * 4));
-                for (int p = 0; p < npages; ++p) {
-                    int32_t page = bt[kt * 2 + p];
-                    if (page < 0 || page >= a.num_pages) {
+            bool ok = true;
+            for (int32_t base = w_begin; ok && base < w_end; base += 32) {
+                int32_t pg0 = 0, pg1 = 0;
+                if (base + lane < w_end) {
+                    TileWalker mine{prefix, 0};
+                    mine.seek(base + lane, ng);
+                    const int g = mine.g, kt = base + lane - prefix[g];
+                    const int nkeys = min(kTileKeys, gmax[g] - kt * kTileKeys);
+                    const int32_t *bt = a.block_table + static_cast<int64_t>(greq[g]) * a.bt_stride;
+                    pg0 = bt[kt * 2];
+                    pg1 = nkeys > DSA_PAGE_SIZE ? bt[kt * 2 + 1] : 0;
+                    if (pg0 < 0 || pg0 >= a.num_pages || pg1 < 0 || pg1 >= a.num_pages) {
                         report(a.status, DSA_ERR_BOUNDS);
-                        page = 0;
+                        pg0 = (pg0 < 0 || pg0 >= a.num_pages) ? 0 : pg0;
+                        pg1 = (pg1 < 0 || pg1 >= a.num_pages) ? 0 : pg1;
                     }
-                    tma_load_2d(keys + stage * C::kKeyBytes + p * (DSA_PAGE_SIZE * 128), &key_map, &full[stage], 0,
-                                page * kIdxPageRows);
-                    bulk_load(scales + stage * kTileKeys + p * DSA_PAGE_SIZE,
-                              a.pool + static_cast<int64_t>(page) * kIdxPageBytes + DSA_PAGE_SIZE * 128,
-                              DSA_PAGE_SIZE * 4, &full[stage]);
+                }
+                const int cnt = min(32, w_end - base);
+                for (int j = 0; j < cnt; ++j, ++it) {
+                    const int32_t w = base + j;
+                    const int32_t p0 = __shfl_sync(0xffffffffu, pg0, j), p1 = __shfl_sync(0xffffffffu, pg1, j);
+                    wk.advance(w);
+                    const int g = wk.g;
+                    if (g != cur) {
+                        ++gc;
+                        cur = g;
+                        const int qb = gc & 1;
+                        int got = 0;
+                        if (lane == 0) got = mbar_wait(&qempty[qb], ((gc >> 1) & 1) ^ 1, abort, a.status);
+                        if (!__shfl_sync(0xffffffffu, got, 0)) {
+                            ok = false;
+                            break;
+                        }
+                        if (lane == 0) {
+                            mbar_arrive_expect_tx(&qfull[qb], C::kQBytes);
+                            tma_load_2d(qbuf + qb * C::kQBytes, &q_map, &qfull[qb], 0,
+                                        (a.group0 + g) * G * DSA_INDEX_HEADS);
+                        }
+                    }
+                    const int stage = it % C::kStages;
+                    int got = 0;
+                    if (lane == 0) got = mbar_wait(&empty[stage], ((it / C::kStages) & 1) ^ 1, abort, a.status);
+                    if (!__shfl_sync(0xffffffffu, got, 0)) {
+                        ok = false;
+                        break;
+                    }
+                    if (lane == 0) {
+                        const int kt = w - prefix[g];
+                        const int nkeys = min(kTileKeys, gmax[g] - kt * kTileKeys);
+                        const int npages = (nkeys + DSA_PAGE_SIZE - 1) / DSA_PAGE_SIZE;
+                        mbar_arrive_expect_tx(&full[stage], npages * (DSA_PAGE_SIZE * 128 + DSA_PAGE_SIZE * 4));
+                        for (int p = 0; p < npages; ++p) {
+                            const int32_t page = p == 0 ? p0 : p1;
+                            tma_load_2d(keys + stage * C::kKeyBytes + p * (DSA_PAGE_SIZE * 128), &key_map,
+                                        &full[stage], 0, page * kIdxPageRows);
+                            bulk_load(scales + stage * kTileKeys + p * DSA_PAGE_SIZE,
+                                      a.pool + static_cast<int64_t>(page) * kIdxPageBytes + DSA_PAGE_SIZE * 128,
+                                      DSA_PAGE_SIZE * 4, &full[stage]);
+                        }
+                    }
+                    __syncwarp();
                 }
             }
         } else if (warp == 1 && lane == 0) {
@@ -279,11 +260,11 @@ __global__ void __launch_bounds__(IdxCfg<G>::kThreads, 1)
                 }
                 const float *wb = wbuf + (gc & 1) * C::N;
                 const int stage = it % C::kStages, as = it & 1;
-                if (!mbar_wait(&tfull[as], (it >> 1) & 1, abort, a.status)) break;
+                if (!mbar_wait_warp(&tfull[as], (it >> 1) & 1, abort, a.status)) break;
                 // the stage's TMA phase is complete (the MMA waited for it) and cannot be
                 // re-armed before this warp arrives on empty[stage]; waiting on it here makes
                 // the bulk-copied scales visible to this thread.
-                if (!mbar_wait(&full[stage], (it / C::kStages) & 1, abort, a.status)) break;
+                if (!mbar_wait_warp(&full[stage], (it / C::kStages) & 1, abort, a.status)) break;
                 tc_fence_after();
                 const float s_t = scales[stage * kTileKeys + key_lane];
                 __syncwarp();

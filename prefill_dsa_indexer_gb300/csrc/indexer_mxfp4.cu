@@ -139,39 +139,71 @@ __global__ void __launch_bounds__(MxCfg<G>::kThreads, 1)
     constexpr uint32_t kIdesc = make_idesc(128, C::N, 0, 0, false, false);
 
     if (w_begin < w_end) {
-        if (warp == 0 && lane == 0) {
-            // ------------------------------------------------ bulk-copy producer
-            prefetch_tensormap(&q_map);
+        if (warp == 0) {
+            // ------------------------------------------------ bulk-copy producer (whole warp)
+            // Lane j looks up the page ids of tile base + j ahead of time; lane 0 issues.
+            if (lane == 0) prefetch_tensormap(&q_map);
             TileWalker wk{prefix, 0};
             wk.seek(w_begin, ng);
             int cur = -1, gc = -1;
             int32_t it = 0;
-            for (int32_t w = w_begin; w < w_end; ++w, ++it) {
-                wk.advance(w);
-                const int g = wk.g;
-                if (g != cur) {
-                    ++gc;
-                    cur = g;
-                    const int qb = gc & 1;
-                    if (!mbar_wait(&qempty[qb], ((gc >> 1) & 1) ^ 1, abort, a.status)) break;
-                    mbar_arrive_expect_tx(&qfull[qb], C::kQBytes);
-                    tma_load_2d(qbuf + qb * C::kQBytes, &q_map, &qfull[qb], 0, (a.group0 + g) * G * DSA_INDEX_HEADS);
-                }
-                const int rs = it % C::kRaw;
-                if (!mbar_wait(&raw_empty[rs], ((it / C::kRaw) & 1) ^ 1, abort, a.status)) break;
-                const int kt = w - prefix[g];
-                const int nkeys = min(kIdxTileKeys, gmax[g] - kt * kIdxTileKeys);
-                const int npages = (nkeys + DSA_PAGE_SIZE - 1) / DSA_PAGE_SIZE;
-                const int32_t *bt = a.block_table + static_cast<int64_t>(greq[g]) * a.bt_stride;
-                mbar_arrive_expect_tx(&raw_full[rs], npages * kMxPageBytes);
-                for (int p = 0; p < npages; ++p) {
-                    int32_t page = bt[kt * 2 + p];
-                    if (page < 0 || page >= a.num_pages) {
+            bool ok = true;
+            for (int32_t base = w_begin; ok && base < w_end; base += 32) {
+                int32_t pg0 = 0, pg1 = 0;
+                if (base + lane < w_end) {
+                    TileWalker mine{prefix, 0};
+                    mine.seek(base + lane, ng);
+                    const int g = mine.g, kt = base + lane - prefix[g];
+                    const int nkeys = min(kIdxTileKeys, gmax[g] - kt * kIdxTileKeys);
+                    const int32_t *bt = a.block_table + static_cast<int64_t>(greq[g]) * a.bt_stride;
+                    pg0 = bt[kt * 2];
+                    pg1 = nkeys > DSA_PAGE_SIZE ? bt[kt * 2 + 1] : 0;
+                    if (pg0 < 0 || pg0 >= a.num_pages || pg1 < 0 || pg1 >= a.num_pages) {
                         report(a.status, DSA_ERR_BOUNDS);
-                        page = 0;
+                        pg0 = (pg0 < 0 || pg0 >= a.num_pages) ? 0 : pg0;
+                        pg1 = (pg1 < 0 || pg1 >= a.num_pages) ? 0 : pg1;
                     }
-                    bulk_load(raw + rs * C::kRawBytes + p * kMxPageBytes,
-                              a.pool + static_cast<int64_t>(page) * kMxPageBytes, kMxPageBytes, &raw_full[rs]);
+                }
+                const int cnt = min(32, w_end - base);
+                for (int j = 0; j < cnt; ++j, ++it) {
+                    const int32_t w = base + j;
+                    const int32_t p0 = __shfl_sync(0xffffffffu, pg0, j), p1 = __shfl_sync(0xffffffffu, pg1, j);
+                    wk.advance(w);
+                    const int g = wk.g;
+                    if (g != cur) {
+                        ++gc;
+                        cur = g;
+                        const int qb = gc & 1;
+                        int got = 0;
+                        if (lane == 0) got = mbar_wait(&qempty[qb], ((gc >> 1) & 1) ^ 1, abort, a.status);
+                        if (!__shfl_sync(0xffffffffu, got, 0)) {
+                            ok = false;
+                            break;
+                        }
+                        if (lane == 0) {
+                            mbar_arrive_expect_tx(&qfull[qb], C::kQBytes);
+                            tma_load_2d(qbuf + qb * C::kQBytes, &q_map, &qfull[qb], 0,
+                                        (a.group0 + g) * G * DSA_INDEX_HEADS);
+                        }
+                    }
+                    const int rs = it % C::kRaw;
+                    int got = 0;
+                    if (lane == 0) got = mbar_wait(&raw_empty[rs], ((it / C::kRaw) & 1) ^ 1, abort, a.status);
+                    if (!__shfl_sync(0xffffffffu, got, 0)) {
+                        ok = false;
+                        break;
+                    }
+                    if (lane == 0) {
+                        const int kt = w - prefix[g];
+                        const int nkeys = min(kIdxTileKeys, gmax[g] - kt * kIdxTileKeys);
+                        const int npages = (nkeys + DSA_PAGE_SIZE - 1) / DSA_PAGE_SIZE;
+                        mbar_arrive_expect_tx(&raw_full[rs], npages * kMxPageBytes);
+                        for (int p = 0; p < npages; ++p)
+                            bulk_load(raw + rs * C::kRawBytes + p * kMxPageBytes,
+                                      a.pool + static_cast<int64_t>(p == 0 ? p0 : p1) * kMxPageBytes, kMxPageBytes,
+                                      &raw_full[rs]);
+                    }
+                    __syncwarp();
                 }
             }
         } else if (warp == 1 && lane == 0) {
@@ -218,8 +250,8 @@ __global__ void __launch_bounds__(MxCfg<G>::kThreads, 1)
                 wk.advance(w);
                 const int g = wk.g;
                 const int rs = it % C::kRaw, os = it % C::kOps;
-                if (!mbar_wait(&raw_full[rs], (it / C::kRaw) & 1, abort, a.status)) break;
-                if (!mbar_wait(&op_empty[os], ((it / C::kOps) & 1) ^ 1, abort, a.status)) break;
+                if (!mbar_wait_warp(&raw_full[rs], (it / C::kRaw) & 1, abort, a.status)) break;
+                if (!mbar_wait_warp(&op_empty[os], ((it / C::kOps) & 1) ^ 1, abort, a.status)) break;
                 const int kt = w - prefix[g];
                 const int nkeys = min(kIdxTileKeys, gmax[g] - kt * kIdxTileKeys);
                 float s_t = 0.f;
@@ -288,8 +320,8 @@ __global__ void __launch_bounds__(MxCfg<G>::kThreads, 1)
                 }
                 const float *wb = wbuf + (gc & 1) * C::N;
                 const int os = it % C::kOps, as = it & 1;
-                if (!mbar_wait(&tfull[as], (it >> 1) & 1, abort, a.status)) break;
-                if (!mbar_wait(&op_full[os], (it / C::kOps) & 1, abort, a.status)) break;
+                if (!mbar_wait_warp(&tfull[as], (it >> 1) & 1, abort, a.status)) break;
+                if (!mbar_wait_warp(&op_full[os], (it / C::kOps) & 1, abort, a.status)) break;
                 tc_fence_after();
                 const float s_t = opsc[os * kIdxTileKeys + key_lane];
                 __syncwarp();

@@ -52,8 +52,8 @@ constexpr int kQBytesMax = kChunks * kMaxH * 128 + (128 - 16) * 128;  // room fo
 constexpr int OFF_KV = (OFF_Q + kQBytesMax + 1023) / 1024 * 1024;
 constexpr int OFF_P = OFF_KV + kKvBytes;
 constexpr int OFF_ALPHA = OFF_P + kPBytes;
-constexpr int OFF_L = OFF_ALPHA + 128 * 4;
-constexpr int OFF_MASK = OFF_L + 128 * 4;
+constexpr int OFF_INVL = OFF_ALPHA + 128 * 4;
+constexpr int OFF_MASK = OFF_INVL + 128 * 4;
 constexpr int OFF_FLAG = OFF_MASK + 16;
 constexpr int OFF_BARS = OFF_FLAG + 16;
 constexpr int kNumBars = 8;
@@ -62,7 +62,7 @@ constexpr int kSmemBytes = OFF_MISC + 32 + 1024;
 static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kTmemO = 2 * kTok;  // O^T starts after two S buffers
+constexpr uint32_t kTmemO = 2 * kTok;  // O^T starts after the two S accumulators
 
 __device__ __forceinline__ uint32_t cvt_e4m3x2_f16x2(uint32_t two_bytes) {
     uint32_t r;
@@ -74,6 +74,13 @@ __device__ __forceinline__ uint32_t cvt_e2m1x2_f16x2(uint32_t byte) {
     uint32_t r;
     asm("{\n\t.reg .b8 b;\n\tcvt.u8.u32 b, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, b;\n\t}" : "=r"(r) : "r"(byte));
     return r;
+}
+
+// 2^x by the hardware approximation (relative error ~2^-22); 2^-inf = 0.
+__device__ __forceinline__ float fast_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
 }
 
 __device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t b) {
@@ -216,13 +223,13 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const MlaArgs a
     uint8_t *kv = smem + OFF_KV;
     uint8_t *ps = smem + OFF_P;
     float *alpha = reinterpret_cast<float *>(smem + OFF_ALPHA);
-    float *lsum = reinterpret_cast<float *>(smem + OFF_L);
+    float *inv_l = reinterpret_cast<float *>(smem + OFF_INVL);  // o_scale / l per head
     unsigned long long *mask = reinterpret_cast<unsigned long long *>(smem + OFF_MASK);
     int *flag = reinterpret_cast<int *>(smem + OFF_FLAG);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + OFF_BARS);
     uint64_t *kv_full = bars + 0;   // gather -> MMA, softmax          (count 4)
-    uint64_t *s_full = bars + 1;    // [2] MMA -> softmax               (commit)
-    uint64_t *s_free = bars + 3;    // [2] softmax -> MMA               (count 4)
+    uint64_t *s_full = bars + 1;    // MMA -> softmax                   (commit)
+    uint64_t *s_free = bars + 3;    // softmax -> MMA                   (count 4)
     uint64_t *p_full = bars + 5;    // softmax -> MMA                   (count 4)
     uint64_t *pv_done = bars + 6;   // MMA -> gather, softmax           (commit)
     uint64_t *stats = bars + 7;     // softmax -> epilogue              (count 4)
@@ -247,10 +254,8 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const MlaArgs a
         *abort = 0;
         flag[0] = flag[1] = 0;
         mbar_init(kv_full, 4);
-        mbar_init(&s_full[0], 1);
-        mbar_init(&s_full[1], 1);
-        mbar_init(&s_free[0], 4);
-        mbar_init(&s_free[1], 4);
+        mbar_init(s_full, 1);
+        mbar_init(s_free, 4);
         mbar_init(p_full, 4);
         mbar_init(pv_done, 1);
         mbar_init(stats, 4);
@@ -260,38 +265,44 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const MlaArgs a
         tmem_alloc(tmem_slot, kTmemCols);
         tmem_relinquish();
     }
-    // ---- Q: bf16 -> fp16, 128-byte swizzled K-major, block c (64 dims) at c * H * 128.
-    // All of a thread's loads are issued before any conversion (one HBM latency, not 18).
-    {
-        constexpr int kUnits = DSA_LATENT_DIM / 8;                       // 8-dim units per head
-        constexpr int kPerThread = (kMaxH * kUnits + kThreads - 1) / kThreads;  // 18
+    // ---- gather warps start tile 0's latent loads; the other warps convert Q meanwhile
+    GatherRegs g;
+    const int gtid = tid - 256;  // 0..127 in the gather warps
+    if (warp >= 8 && n_tiles > 0) gather_load<FMT>(a, row_slots, 0, n_tok, gtid, g);
+    // ---- Q: bf16 -> fp16, 128-byte swizzled K-major, block c (64 dims) at c * H * 128;
+    // loads of a batch are all issued before any conversion
+    if (warp < 8) {
+        constexpr int kUnits = DSA_LATENT_DIM / 8;  // 8-dim units per head
+        constexpr int kBatch = 9;
         const uint16_t *qg = a.q + static_cast<int64_t>(row) * H * DSA_LATENT_DIM;
         const int total = H * kUnits;
-        int4 v[kPerThread];
-#pragma unroll
-        for (int i = 0; i < kPerThread; ++i) {
-            const int e = tid + i * kThreads;
-            if (e < total) v[i] = *reinterpret_cast<const int4 *>(qg + static_cast<int64_t>(e) * 8);
-        }
         bool range_err = false;
+        for (int e0 = tid; e0 < total; e0 += 256 * kBatch) {
+            int4 v[kBatch];
 #pragma unroll
-        for (int i = 0; i < kPerThread; ++i) {
-            const int e = tid + i * kThreads;
-            if (e >= total) break;
-            const int h = e / kUnits, u = e % kUnits;
-            const uint32_t w[4] = {static_cast<uint32_t>(v[i].x), static_cast<uint32_t>(v[i].y),
-                                   static_cast<uint32_t>(v[i].z), static_cast<uint32_t>(v[i].w)};
-            const float sc = (u >= DSA_VALUE_DIM / 8) ? q_rope_scale : 1.0f;
-            uint32_t o[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const float lo = __uint_as_float(w[j] << 16) * sc, hi = __uint_as_float(w[j] & 0xffff0000u) * sc;
-                if (!(fabsf(lo) <= 65504.f) || !(fabsf(hi) <= 65504.f)) range_err = true;
-                __half2 hh = __floats2half2_rn(lo, hi);
-                o[j] = *reinterpret_cast<uint32_t *>(&hh);
+            for (int i = 0; i < kBatch; ++i) {
+                const int e = e0 + i * 256;
+                if (e < total) v[i] = *reinterpret_cast<const int4 *>(qg + static_cast<int64_t>(e) * 8);
             }
-            const int c = u >> 3, uu = u & 7;
-            *reinterpret_cast<int4 *>(qs + c * H * 128 + sw128(h, uu)) = make_int4(o[0], o[1], o[2], o[3]);
+#pragma unroll
+            for (int i = 0; i < kBatch; ++i) {
+                const int e = e0 + i * 256;
+                if (e >= total) break;
+                const int h = e / kUnits, u = e % kUnits;
+                const uint32_t w[4] = {static_cast<uint32_t>(v[i].x), static_cast<uint32_t>(v[i].y),
+                                       static_cast<uint32_t>(v[i].z), static_cast<uint32_t>(v[i].w)};
+                const float sc = (u >= DSA_VALUE_DIM / 8) ? q_rope_scale : 1.0f;
+                uint32_t o[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const float lo = __uint_as_float(w[j] << 16) * sc, hi = __uint_as_float(w[j] & 0xffff0000u) * sc;
+                    if (!(fabsf(lo) <= 65504.f) || !(fabsf(hi) <= 65504.f)) range_err = true;
+                    __half2 hh = __floats2half2_rn(lo, hi);
+                    o[j] = *reinterpret_cast<uint32_t *>(&hh);
+                }
+                const int c = u >> 3, uu = u & 7;
+                *reinterpret_cast<int4 *>(qs + c * H * 128 + sw128(h, uu)) = make_int4(o[0], o[1], o[2], o[3]);
+            }
         }
         if (range_err) report(a.status, DSA_ERR_RANGE);
     }
@@ -303,187 +314,219 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const MlaArgs a
     if (warp == 0) {
         if (lane == 0 && n_tiles > 0) {
             // ------------------------------------------------------------ MMA issuer
+            // S = Q . KV^T accumulates into two TMEM accumulators (even / odd 64-dim blocks)
+            // issued alternately, and PV issues its four independent output blocks
+            // round-robin, so consecutive MMAs never wait on each other's accumulator.
+            // Descriptors are built once and advanced by their 16-byte address field.
             const uint32_t idesc_s = make_idesc(128, kTok, 0, 0, false, false);
             const uint32_t idesc_pv = make_idesc(128, H, 0, 0, true, false);
-            const uint32_t q_addr = smem_u32(qs), kv_addr = smem_u32(kv), p_addr = smem_u32(ps);
+            const uint64_t q_desc = sdesc_sw128(smem_u32(qs), 16, 1024);
+            const uint64_t kv_desc = sdesc_sw128(smem_u32(kv), 16, 1024);
+            const uint64_t v_desc = sdesc_sw128(smem_u32(kv), kTok * 128, 1024);
+            const uint64_t p_desc = sdesc_sw128(smem_u32(ps), 16, 1024);
+            const uint32_t q_blk = (H * 128) >> 4, kv_blk = (kTok * 128) >> 4;  // 16-byte units
             for (int i = 0; i < n_tiles; ++i) {
-                const int sb = i & 1;
                 if (!mbar_wait(kv_full, i & 1, abort, a.status)) break;
-                if (!mbar_wait(&s_free[sb], ((i >> 1) & 1) ^ 1, abort, a.status)) break;
+                if (!mbar_wait(s_free, (i & 1) ^ 1, abort, a.status)) break;
                 tc_fence_after();
-                for (int c = 0; c < kChunks; ++c) {
+                for (int c0 = 0; c0 < kChunks; c0 += 2) {
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
-                        const uint64_t ad = sdesc_sw128(q_addr + c * H * 128 + kk * 32, 16, 1024);
-                        const uint64_t bd = sdesc_sw128(kv_addr + c * (kTok * 128) + kk * 32, 16, 1024);
-                        mma_f16(tmem + sb * kTok, ad, bd, idesc_s, (c | kk) ? 1u : 0u);
+#pragma unroll
+                        for (int e = 0; e < 2; ++e) {
+                            const int c = c0 + e;
+                            if (c < kChunks) {
+                                const uint64_t off_q = c * q_blk + kk * 2, off_kv = c * kv_blk + kk * 2;
+                                mma_f16(tmem + e * kTok, q_desc + off_q, kv_desc + off_kv, idesc_s,
+                                        (c0 | kk) ? 1u : 0u);
+                            }
+                        }
                     }
                 }
-                mma_commit(&s_full[sb]);
+                mma_commit(s_full);
                 if (!mbar_wait(p_full, i & 1, abort, a.status)) break;
                 tc_fence_after();
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
+                for (int ks = 0; ks < kTok / 16; ++ks) {
 #pragma unroll
-                    for (int ks = 0; ks < kTok / 16; ++ks) {
+                    for (int j = 0; j < 4; ++j) {
                         // A = V^T block j: dims [128j, 128j+128) x 16 tokens, MN-major:
                         // 64-dim blocks 8 KB apart (LBO), 8-token groups 1 KB apart (SBO)
-                        const uint64_t ad = sdesc_sw128(kv_addr + (2 * j) * (kTok * 128) + ks * 2048, kTok * 128, 1024);
-                        const uint64_t bd = sdesc_sw128(p_addr + ks * 32, 16, 1024);
-                        mma_f16(tmem + kTmemO + j * H, ad, bd, idesc_pv, (i | ks) ? 1u : 0u);
+                        const uint64_t off_v = (2 * j) * kv_blk + ks * (2048 >> 4), off_p = ks * 2;
+                        mma_f16(tmem + kTmemO + j * H, v_desc + off_v, p_desc + off_p, idesc_pv, (i | ks) ? 1u : 0u);
                     }
                 }
                 mma_commit(pv_done);
             }
         }
-    } else if (warp >= 4 && warp < 8) {
-        // ---------------------------------------------------------------- softmax
+    } else if (warp >= 4) {
+        const bool is_softmax = warp < 8;
         const int quad = warp & 3;
-        const int h = quad * 32 + lane;
-        float m = -INFINITY, l = 0.f;
-        for (int i = 0; i < n_tiles; ++i) {
-            const int sb = i & 1;
-            if (!mbar_wait(&s_full[sb], (i >> 1) & 1, abort, a.status)) break;
-            if (!mbar_wait(kv_full, i & 1, abort, a.status)) break;
-            tc_fence_after();
-            uint32_t sr[64];
-            tmem_ld32(tmem + (static_cast<uint32_t>(quad * 32) << 16) + sb * kTok, *reinterpret_cast<uint32_t(*)[32]>(sr));
-            tmem_ld32(tmem + (static_cast<uint32_t>(quad * 32) << 16) + sb * kTok + 32,
-                      *reinterpret_cast<uint32_t(*)[32]>(sr + 32));
-            tmem_ld_wait();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&s_free[sb]);
-            const unsigned long long msk = *mask;
-            float mt = -INFINITY;
-#pragma unroll
-            for (int j = 0; j < kTok; ++j) {
-                const float s = ((msk >> j) & 1ull) ? __uint_as_float(sr[j]) * s_scale : -INFINITY;
-                sr[j] = __float_as_uint(s);
-                mt = fmaxf(mt, s);
-            }
-            float al = 1.f;
-            bool resc = false;
-            if (mt > m + kLazyRescaleLog2 || (m == -INFINITY && mt > -INFINITY)) {
-                if (m > -INFINITY) {
-                    al = exp2f(m - mt);
-                    resc = true;
+        bool ok = true;
+        if (is_softmax) {
+            // ------------------------------------------------------------ softmax
+            const int h = quad * 32 + lane;
+            float m = -INFINITY, l = 0.f;
+            for (int i = 0; i < n_tiles; ++i) {
+                if (!mbar_wait_warp(s_full, i & 1, abort, a.status) || !mbar_wait_warp(kv_full, i & 1, abort, a.status)) {
+                    ok = false;
+                    break;
                 }
-                l *= al;
-                m = mt;
-            }
-            alpha[h] = al;
-            if (__any_sync(0xffffffffu, resc && h < H) && lane == 0) atomicOr(&flag[i & 1], 1);
-            named_bar_sync(1, 128);
-            const bool do_resc = flag[i & 1] != 0;
-            if (quad == 0 && lane == 0) flag[(i + 1) & 1] = 0;
-            if (i > 0 && !mbar_wait(pv_done, (i - 1) & 1, abort, a.status)) break;
-            if (do_resc) {
-                // rescale O^T columns by alpha[head]: this warp owns TMEM lanes (dims) 32q..32q+31
                 tc_fence_after();
-                for (int j = 0; j < 4; ++j) {
-                    for (int c = 0; c < H / 16; ++c) {
-                        const uint32_t ta = tmem + (static_cast<uint32_t>(quad * 32) << 16) + kTmemO + j * H + c * 16;
-                        uint32_t v[16];
-                        tmem_ld16(ta, v);
-                        tmem_ld_wait();
+                uint32_t sr[64], s2[64];
+                const uint32_t srow = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+                tmem_ld32(srow, *reinterpret_cast<uint32_t(*)[32]>(sr));
+                tmem_ld32(srow + 32, *reinterpret_cast<uint32_t(*)[32]>(sr + 32));
+                tmem_ld32(srow + kTok, *reinterpret_cast<uint32_t(*)[32]>(s2));
+                tmem_ld32(srow + kTok + 32, *reinterpret_cast<uint32_t(*)[32]>(s2 + 32));
+                tmem_ld_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(s_free);
+                const unsigned long long msk = *mask;
+                float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+                if (msk == ~0ull) {
 #pragma unroll
-                        for (int x = 0; x < 16; ++x) v[x] = __float_as_uint(__uint_as_float(v[x]) * alpha[c * 16 + x]);
-                        tmem_st16(ta, v);
+                    for (int j = 0; j < kTok; ++j) {
+                        const float sv = (__uint_as_float(sr[j]) + __uint_as_float(s2[j])) * s_scale;
+                        sr[j] = __float_as_uint(sv);
+                        mx[j & 3] = fmaxf(mx[j & 3], sv);
+                    }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < kTok; ++j) {
+                        const float sv = ((msk >> j) & 1ull)
+                                             ? (__uint_as_float(sr[j]) + __uint_as_float(s2[j])) * s_scale
+                                             : -INFINITY;
+                        sr[j] = __float_as_uint(sv);
+                        mx[j & 3] = fmaxf(mx[j & 3], sv);
                     }
                 }
-                tmem_st_wait();
-            }
-            // P = 2^(s - m) in fp16, row h of the [head][64 tokens] swizzled operand
-            float ls = 0.f;
-            uint32_t pk[32];
+                const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+                float al = 1.f;
+                bool resc = false;
+                if (mt > m + kLazyRescaleLog2 || (m == -INFINITY && mt > -INFINITY)) {
+                    if (m > -INFINITY) {
+                        al = exp2f(m - mt);
+                        resc = true;
+                    }
+                    l *= al;
+                    m = mt;
+                }
+                alpha[h] = al;
+                if (__any_sync(0xffffffffu, resc && h < H) && lane == 0) atomicOr(&flag[i & 1], 1);
+                named_bar_sync(1, 128);
+                const bool do_resc = flag[i & 1] != 0;
+                if (quad == 0 && lane == 0) flag[(i + 1) & 1] = 0;
+                // P's buffer is free (and O^T stable) once the previous PV product is done
+                if (i > 0 && !mbar_wait_warp(pv_done, (i - 1) & 1, abort, a.status)) {
+                    ok = false;
+                    break;
+                }
+                if (do_resc) {
+                    // rescale O^T columns by alpha[head]: this warp owns TMEM lanes (dims) 32q..32q+31
+                    tc_fence_after();
+                    for (int j = 0; j < 4; ++j) {
+                        for (int c = 0; c < H / 16; ++c) {
+                            const uint32_t ta =
+                                tmem + (static_cast<uint32_t>(quad * 32) << 16) + kTmemO + j * H + c * 16;
+                            uint32_t v[16];
+                            tmem_ld16(ta, v);
+                            tmem_ld_wait();
 #pragma unroll
-            for (int j = 0; j < kTok; j += 2) {
-                const float s0 = __uint_as_float(sr[j]), s1 = __uint_as_float(sr[j + 1]);
-                const float p0 = (s0 == -INFINITY) ? 0.f : exp2f(s0 - m);
-                const float p1 = (s1 == -INFINITY) ? 0.f : exp2f(s1 - m);
-                __half2 hh = __floats2half2_rn(p0, p1);
-                // the sum uses the fp16-rounded p, the values the PV product sees
-                const float2 back = __half22float2(hh);
-                ls += back.x + back.y;
-                pk[j / 2] = *reinterpret_cast<uint32_t *>(&hh);
+                            for (int x = 0; x < 16; ++x)
+                                v[x] = __float_as_uint(__uint_as_float(v[x]) * alpha[c * 16 + x]);
+                            tmem_st16(ta, v);
+                        }
+                    }
+                    tmem_st_wait();
+                }
+                // P = 2^(s - m) in fp16, row h of the [head][64 tokens] swizzled operand.
+                // Masked scores are -inf and give 0; m = -inf means this tile is all masked.
+                float ls[4] = {0.f, 0.f, 0.f, 0.f};
+                uint32_t pk[32];
+                const float msub = (m == -INFINITY) ? 0.f : m;
+#pragma unroll
+                for (int j = 0; j < kTok; j += 2) {
+                    const float p0 = fast_exp2(__uint_as_float(sr[j]) - msub);
+                    const float p1 = fast_exp2(__uint_as_float(sr[j + 1]) - msub);
+                    __half2 hh = __floats2half2_rn(p0, p1);
+                    ls[(j >> 1) & 3] += p0 + p1;
+                    pk[j / 2] = *reinterpret_cast<uint32_t *>(&hh);
+                }
+                l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+                if (h < H) {
+#pragma unroll
+                    for (int u = 0; u < 8; ++u)
+                        *reinterpret_cast<int4 *>(ps + sw128(h, u)) =
+                            make_int4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+                }
+                fence_async_smem();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(p_full);
             }
-            l += ls;
+            // final statistics of this head
+            inv_l[h] = (l > 0.f) ? o_scale / l : 0.f;
             if (h < H) {
-#pragma unroll
-                for (int u = 0; u < 8; ++u)
-                    *reinterpret_cast<int4 *>(ps + sw128(h, u)) =
-                        make_int4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+                const float lse2 = (l > 0.f) ? m + log2f(l) : -INFINITY;
+                if (a.splits == 1) {
+                    if (a.lse) a.lse[static_cast<int64_t>(row) * H + h] = lse2 * 0.6931471805599453f;
+                } else {
+                    float *ml = a.part_ml + (static_cast<int64_t>(row) * a.splits + split) * H * 2;
+                    ml[2 * h] = (l > 0.f) ? m : -INFINITY;
+                    ml[2 * h + 1] = l;
+                }
             }
-            fence_async_smem();
-            tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(p_full);
-        }
-        // final statistics
-        lsum[h] = l;
-        if (h < H) {
-            const float lse2 = (l > 0.f) ? m + log2f(l) : -INFINITY;
-            if (a.splits == 1) {
-                if (a.lse) a.lse[static_cast<int64_t>(row) * H + h] = lse2 * 0.6931471805599453f;
-            } else {
-                float *ml = a.part_ml + (static_cast<int64_t>(row) * a.splits + split) * H * 2;
-                ml[2 * h] = (l > 0.f) ? m : -INFINITY;
-                ml[2 * h + 1] = l;
-            }
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(stats);
-    } else if (warp >= 8) {
-        // ---------------------------------------------------------------- gather + epilogue
-        const int gtid = tid - 256;  // 0..127
-        const int quad = warp & 3;
-        GatherRegs g;
-        if (n_tiles > 0) gather_load<FMT>(a, row_slots, 0, n_tok, gtid, g);
-        bool ok = true;
-        for (int i = 0; i < n_tiles; ++i) {
-            if (i > 0 && !mbar_wait(pv_done, (i - 1) & 1, abort, a.status)) {
-                ok = false;
-                break;
-            }
-            gather_store<FMT>(kv, gtid, g);
-            const unsigned long long vm = __ballot_sync(0xffffffffu, g.slot >= 0);
-            // lanes 2t, 2t+1 hold token t of this warp's 16 tokens: keep even lanes' bits
-            unsigned long long tok = 0;
+            if (lane == 0) mbar_arrive(stats);
+        } else {
+            // ------------------------------------------------------------ gather
+            for (int i = 0; i < n_tiles; ++i) {
+                if (i > 0 && !mbar_wait_warp(pv_done, (i - 1) & 1, abort, a.status)) {
+                    ok = false;
+                    break;
+                }
+                gather_store<FMT>(kv, gtid, g);
+                const unsigned long long vm = __ballot_sync(0xffffffffu, g.slot >= 0);
+                // lanes 2t, 2t+1 hold token t of this warp's 16 tokens: keep even lanes' bits
+                unsigned long long tok = 0;
 #pragma unroll
-            for (int b = 0; b < 16; ++b) tok |= ((vm >> (2 * b)) & 1ull) << b;
-            if (lane == 0) reinterpret_cast<unsigned short *>(mask)[quad] = static_cast<unsigned short>(tok);
-            fence_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(kv_full);
-            if (i + 1 < n_tiles) gather_load<FMT>(a, row_slots, (i + 1) * kTok, n_tok, gtid, g);
+                for (int b = 0; b < 16; ++b) tok |= ((vm >> (2 * b)) & 1ull) << b;
+                if (lane == 0) reinterpret_cast<unsigned short *>(mask)[quad] = static_cast<unsigned short>(tok);
+                fence_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(kv_full);
+                if (i + 1 < n_tiles) gather_load<FMT>(a, row_slots, (i + 1) * kTok, n_tok, gtid, g);
+            }
         }
-        if (ok && n_tiles > 0) ok = mbar_wait(pv_done, (n_tiles - 1) & 1, abort, a.status);
-        if (ok) ok = mbar_wait(stats, 0, abort, a.status);
+        // ---------------------------------------------------------------- epilogue, 8 warps:
+        // softmax warps store dim blocks 0 and 1 of O, gather warps blocks 2 and 3;
+        // lane = dim, one store instruction writes 32 consecutive dims of one head
+        if (ok && n_tiles > 0) ok = mbar_wait_warp(pv_done, (n_tiles - 1) & 1, abort, a.status);
+        if (ok) ok = mbar_wait_warp(stats, 0, abort, a.status);
         if (ok) {
             tc_fence_after();
-            float *dst;
-            int64_t hstride;
-            if (a.splits == 1) {
-                dst = a.out + static_cast<int64_t>(row) * H * DSA_VALUE_DIM;
-            } else {
-                dst = a.part_o + (static_cast<int64_t>(row) * a.splits + split) * H * DSA_VALUE_DIM;
-            }
-            hstride = DSA_VALUE_DIM;
-            for (int j = 0; j < 4; ++j) {
+            float *dst = (a.splits == 1)
+                             ? a.out + static_cast<int64_t>(row) * H * DSA_VALUE_DIM
+                             : a.part_o + (static_cast<int64_t>(row) * a.splits + split) * H * DSA_VALUE_DIM;
+            const int j0 = is_softmax ? 0 : 2;
+            for (int j = j0; j < j0 + 2; ++j) {
                 const int d = 128 * j + 32 * quad + lane;
-                for (int c = 0; c < H / 16; ++c) {
-                    uint32_t v[16];
+                const uint32_t tb = tmem + (static_cast<uint32_t>(quad * 32) << 16) + kTmemO + j * H;
+                for (int c = 0; c < H; c += 32) {
+                    uint32_t v[32];
+                    const bool full32 = c + 32 <= H;
                     if (n_tiles > 0) {
-                        tmem_ld16(tmem + (static_cast<uint32_t>(quad * 32) << 16) + kTmemO + j * H + c * 16, v);
+                        if (full32) tmem_ld32(tb + c, v);
+                        else tmem_ld16(tb + c, *reinterpret_cast<uint32_t(*)[16]>(v));
                         tmem_ld_wait();
                     }
 #pragma unroll
-                    for (int x = 0; x < 16; ++x) {
-                        const int hh = c * 16 + x;
-                        const float lh = lsum[hh];
-                        const float o = (n_tiles > 0 && lh > 0.f) ? __uint_as_float(v[x]) * (o_scale / lh) : 0.f;
-                        dst[hh * hstride + d] = o;
+                    for (int x = 0; x < 32; ++x) {
+                        if (x >= 16 && !full32) break;
+                        const float o = (n_tiles > 0) ? __uint_as_float(v[x]) * inv_l[c + x] : 0.f;
+                        dst[static_cast<int64_t>(c + x) * DSA_VALUE_DIM + d] = o;
                     }
                 }
             }
@@ -500,24 +543,37 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const MlaArgs a
 // w_s = l_s 2^(m_s - M), M = max_s m_s (log2 units).  One CTA per (row, head),
 // four output dims per thread.
 __global__ void __launch_bounds__(128) mla_combine_kernel(const MlaArgs a) {
+    constexpr int kMaxSplits = 16;
     const int H = a.num_heads, S = a.splits;
     const int row = blockIdx.x / H, h = blockIdx.x % H;
     const float *ml = a.part_ml + static_cast<int64_t>(row) * S * H * 2;
+    // all partial loads in flight at once
+    float4 o[kMaxSplits];
+    float ms[kMaxSplits], ls[kMaxSplits];
+#pragma unroll
+    for (int s = 0; s < kMaxSplits; ++s) {
+        if (s < S) {
+            ms[s] = ml[(s * H + h) * 2];
+            ls[s] = ml[(s * H + h) * 2 + 1];
+            o[s] = reinterpret_cast<const float4 *>(
+                a.part_o + ((static_cast<int64_t>(row) * S + s) * H + h) * DSA_VALUE_DIM)[threadIdx.x];
+        }
+    }
     float M = -INFINITY;
-    for (int s = 0; s < S; ++s) M = fmaxf(M, ml[(s * H + h) * 2]);
+#pragma unroll
+    for (int s = 0; s < kMaxSplits; ++s)
+        if (s < S) M = fmaxf(M, ms[s]);
     float wsum = 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int s = 0; s < S; ++s) {
-        const float ms = ml[(s * H + h) * 2];
-        if (ms == -INFINITY) continue;
-        const float w = ml[(s * H + h) * 2 + 1] * exp2f(ms - M);
+#pragma unroll
+    for (int s = 0; s < kMaxSplits; ++s) {
+        if (s >= S || ms[s] == -INFINITY) continue;
+        const float w = ls[s] * exp2f(ms[s] - M);
         wsum += w;
-        const float4 o = reinterpret_cast<const float4 *>(
-            a.part_o + ((static_cast<int64_t>(row) * S + s) * H + h) * DSA_VALUE_DIM)[threadIdx.x];
-        acc.x = fmaf(w, o.x, acc.x);
-        acc.y = fmaf(w, o.y, acc.y);
-        acc.z = fmaf(w, o.z, acc.z);
-        acc.w = fmaf(w, o.w, acc.w);
+        acc.x = fmaf(w, o[s].x, acc.x);
+        acc.y = fmaf(w, o[s].y, acc.y);
+        acc.z = fmaf(w, o[s].z, acc.z);
+        acc.w = fmaf(w, o[s].w, acc.w);
     }
     const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
     reinterpret_cast<float4 *>(a.out + (static_cast<int64_t>(row) * H + h) * DSA_VALUE_DIM)[threadIdx.x] =

@@ -41,6 +41,8 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t by
                  : "memory");
 }
 
+// One test of the phase (the hardware may briefly suspend the thread while
+// the phase is incomplete).
 __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
@@ -69,6 +71,17 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volati
             return false;
         }
     }
+}
+
+// Warp-collective bounded wait: lane 0 waits, the result is broadcast, so a
+// waiting warp polls the barrier once instead of 32 times.
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t *bar, uint32_t parity, volatile int *abort,
+                                               int32_t *status) {
+    int ok = 0;
+    if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, abort, status);
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    __syncwarp();  // orders lane 0's acquire before every lane's later reads
+    return ok != 0;
 }
 
 // ------------------------------------------------------------------ TMA

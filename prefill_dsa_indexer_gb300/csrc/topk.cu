@@ -41,13 +41,15 @@ constexpr int kMaxCluster = 8;
 struct TopkSmem {
     uint32_t cache[kCacheElems];
     uint32_t hist[kBins];
-    uint32_t cand[kCandCap];
+    uint32_t cand[kCandCap];      // this CTA's keys inside the threshold bin
+    uint32_t cand_all[kCandCap];  // the cluster's candidates, gathered into every CTA
+    uint32_t wcnt[2 * kWarps];    // per-warp counts of keys > T and == T
     unsigned long long scan[kWarps + 1];
     uint32_t red[2 * kWarps];
     uint32_t mm[2];   // this CTA's chunk key range (read by the cluster)
     uint32_t cnt[2];  // this CTA's chunk counts of keys > T and == T (read by the cluster)
     uint32_t sel_bin, sel_above, sel_count;
-    uint32_t ncand;
+    uint32_t ncand, ncand_all;
     int32_t bad;
 };
 
@@ -202,33 +204,58 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const TopkArgs a) {
     }
     uint32_t need = static_cast<uint32_t>(k);
 
-    // ---- refine the key interval [base, top] holding the k-th largest key down to one key
-    bool use_cand = false;
+    // ---- refine the key interval [base, top] holding the k-th largest key down to one key.
+    // While the interval's keys are too many to gather, each round histograms every CTA's
+    // chunk and sums the histograms across the cluster.  Once they fit, the keys inside the
+    // interval are gathered into every CTA, which then refines alone (identically).
+    bool gathered = false;
     while (top > base) {
         const uint32_t span = top - base;
         const int bits = 32 - __clz(span);            // span < 2^bits
         const int shift = bits > 11 ? bits - 11 : 0;  // (span >> shift) < 2048
         for (int b = tid; b < kBins; b += kThreads) s.hist[b] = 0;
         __syncthreads();
-        if (use_cand) {
-            const int nc = static_cast<int>(s.ncand);
-            for (int i = tid; i < nc; i += kThreads) {
-                const uint32_t key = s.cand[i];
-                if (key >= base && key <= top) atomicAdd(&s.hist[(key - base) >> shift], 1u);
+        if (gathered) {
+            const int nc = static_cast<int>(s.ncand_all);
+            for (int i0 = 0; i0 < nc; i0 += kThreads) {
+                const int i = i0 + tid;
+                const uint32_t key = i < nc ? s.cand_all[i] : 0u;
+                const bool in = i < nc && key >= base && key <= top;
+                const uint32_t bin = in ? (key - base) >> shift : 0xffffffffu;
+                const unsigned peers = __match_any_sync(0xffffffffu, bin);
+                if (in && lane == __ffs(peers) - 1) atomicAdd(&s.hist[bin], __popc(peers));
             }
         } else {
-            for_each_key(s, src, nloc, cached, ignore, [&](int, uint32_t key) {
-                if (key >= base && key <= top) atomicAdd(&s.hist[(key - base) >> shift], 1u);
-            });
+            // warp-aggregated histogram over the chunk (keys in lane order)
+            if (cached) {
+                for (int i0 = 0; i0 < nloc; i0 += kThreads) {
+                    const int i = i0 + tid;
+                    const uint32_t key = i < nloc ? s.cache[i] : 0u;
+                    const bool in = i < nloc && key >= base && key <= top;
+                    const uint32_t bin = in ? (key - base) >> shift : 0xffffffffu;
+                    const unsigned peers = __match_any_sync(0xffffffffu, bin);
+                    if (in && lane == __ffs(peers) - 1) atomicAdd(&s.hist[bin], __popc(peers));
+                }
+            } else {
+                for_each_key(s, src, nloc, false, ignore, [&](int, uint32_t key) {
+                    if (key >= base && key <= top) atomicAdd(&s.hist[(key - base) >> shift], 1u);
+                });
+            }
         }
-        cluster.sync();
-        // cluster-wide counts of this thread's two bins (2047-2t and 2046-2t)
+        if (!gathered) cluster.sync();
+        else __syncthreads();
+        // counts of this thread's two bins (2047-2t and 2046-2t), cluster-wide unless gathered
         const int b1 = kBins - 1 - 2 * tid, b0 = b1 - 1;
         uint32_t c1 = 0, c0v = 0;
-        for (int r = 0; r < CL; ++r) {
-            const uint32_t *h = cluster.map_shared_rank(s.hist, r);
-            c1 += h[b1];
-            c0v += h[b0];
+        if (gathered) {
+            c1 = s.hist[b1];
+            c0v = s.hist[b0];
+        } else {
+            for (int r = 0; r < CL; ++r) {
+                const uint32_t *h = cluster.map_shared_rank(s.hist, r);
+                c1 += h[b1];
+                c0v += h[b0];
+            }
         }
         unsigned long long tot;
         const uint32_t above1 = static_cast<uint32_t>(block_excl_scan(c1 + c0v, s, tot));
@@ -241,70 +268,91 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const TopkArgs a) {
             s.sel_above = above1 + c1;
             s.sel_count = c0v;
         }
-        cluster.sync();  // every CTA has read every histogram; selection visible block-wide
+        if (!gathered) cluster.sync();  // every CTA has read every histogram
+        else __syncthreads();
         const uint32_t sb = s.sel_bin, sa = s.sel_above, sc = s.sel_count;
         need -= sa;
         const uint32_t nbase = base + (sb << shift);
         const unsigned long long bin_top = static_cast<unsigned long long>(nbase) + (1ull << shift) - 1ull;
         base = nbase;
         top = static_cast<uint32_t>(min(static_cast<unsigned long long>(top), bin_top));
-        if (top > base && !use_cand && sc <= static_cast<uint32_t>(kCandCap)) {
-            // the cluster holds at most kCandCap keys in [base, top]; so does this chunk
-            for_each_key(s, src, nloc, cached, ignore, [&](int, uint32_t key) {
-                if (key >= base && key <= top) s.cand[atomicAdd(&s.ncand, 1u)] = key;
-            });
-            use_cand = true;
+        if (top > base && !gathered && sc <= static_cast<uint32_t>(kCandCap)) {
+            // the cluster holds sc <= kCandCap keys in [base, top]: collect this chunk's share
+            // (one shared atomic per warp), then gather every CTA's share into every CTA
+            for (int i0 = 0; i0 < nloc; i0 += kThreads) {
+                const int i = i0 + tid;
+                const uint32_t key = i < nloc ? key_at(s, src, i, cached) : 0u;
+                const bool in = i < nloc && key >= base && key <= top;
+                const unsigned m = __ballot_sync(0xffffffffu, in);
+                uint32_t wbase = 0;
+                if (lane == 0 && m) wbase = atomicAdd(&s.ncand, static_cast<uint32_t>(__popc(m)));
+                wbase = __shfl_sync(0xffffffffu, wbase, 0);
+                if (in) s.cand[wbase + __popc(m & ((1u << lane) - 1u))] = key;
+            }
+            cluster.sync();
+            uint32_t off = 0;
+            for (int r = 0; r < CL; ++r) {
+                const TopkSmem *peer = cluster.map_shared_rank(&s, r);
+                const int n_r = static_cast<int>(peer->ncand);
+                for (int i = tid; i < n_r; i += kThreads) s.cand_all[off + i] = peer->cand[i];
+                off += n_r;
+            }
+            if (tid == 0) s.ncand_all = off;
+            gathered = true;
         }
         __syncthreads();
     }
     const uint32_t T = base;  // exact threshold key; `need` keys equal to T are taken (lowest positions)
 
-    // ---- counts per chunk, then the chunk's offset from the lower-ranked CTAs
-    uint32_t my_gt = 0, my_eq = 0;
-    for_each_key(s, src, nloc, cached, ignore, [&](int, uint32_t key) {
-        my_gt += key > T;
-        my_eq += key == T;
-    });
-    {
-        unsigned long long tot;
-        block_excl_scan((static_cast<unsigned long long>(my_gt) << 32) | my_eq, s, tot);
-        if (tid == 0) {
-            s.cnt[0] = static_cast<uint32_t>(tot >> 32);
-            s.cnt[1] = static_cast<uint32_t>(tot);
+    // ---- ordered compaction.  Warp w owns a contiguous segment of the chunk and walks it
+    // 32 keys at a time (lane order = position order): pass 1 counts keys > T and == T per
+    // warp, pass 2 writes positions.  A warp's offset adds the counts of the lower warps of
+    // this CTA and of the lower-ranked CTAs of the cluster.
+    const int seg = ((nloc + kWarps - 1) / kWarps + 31) & ~31;
+    const int w0 = min(nloc, warp * seg), w1 = min(nloc, w0 + seg);
+    uint32_t ngt = 0, neq = 0;
+    for (int i0 = w0; i0 < w1; i0 += 32) {
+        const int i = i0 + lane;
+        const uint32_t key = i < w1 ? key_at(s, src, i, cached) : 0u;
+        ngt += __popc(__ballot_sync(0xffffffffu, i < w1 && key > T));
+        neq += __popc(__ballot_sync(0xffffffffu, i < w1 && key == T));
+    }
+    if (lane == 0) {
+        s.wcnt[warp] = ngt;
+        s.wcnt[kWarps + warp] = neq;
+    }
+    __syncthreads();
+    if (tid == 0) {
+        uint32_t g = 0, e = 0;
+        for (int w = 0; w < kWarps; ++w) {
+            g += s.wcnt[w];
+            e += s.wcnt[kWarps + w];
         }
+        s.cnt[0] = g;
+        s.cnt[1] = e;
     }
     cluster.sync();
-    unsigned long long run = 0;  // (keys > T) << 32 | (keys == T) before the current position
+    uint32_t gt_before = 0, eq_before = 0;
     for (int r = 0; r < crank; ++r) {
         const uint32_t *c = cluster.map_shared_rank(s.cnt, r);
-        run += (static_cast<unsigned long long>(c[0]) << 32) | c[1];
+        gt_before += c[0];
+        eq_before += c[1];
     }
-    // ---- ordered compaction: every key > T, plus the first `need` keys == T
-    for (int b0 = 0; b0 < nloc; b0 += 4 * kThreads) {
-        uint32_t kv[4];
-        uint32_t ngt = 0, neq = 0;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int i = b0 + 4 * tid + j;
-            kv[j] = i < nloc ? key_at(s, src, i, cached) : 0u;
-            if (i < nloc) {
-                ngt += kv[j] > T;
-                neq += kv[j] == T;
-            }
-        }
-        unsigned long long tot;
-        unsigned long long pre = block_excl_scan((static_cast<unsigned long long>(ngt) << 32) | neq, s, tot) + run;
-        uint32_t gt_before = static_cast<uint32_t>(pre >> 32), eq_before = static_cast<uint32_t>(pre);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int i = b0 + 4 * tid + j;
-            if (i >= nloc) break;
-            const bool gt = kv[j] > T, eq = kv[j] == T;
-            if (gt || (eq && eq_before < need)) out[gt_before + min(eq_before, need)] = c0 + i;
-            gt_before += gt;
-            eq_before += eq;
-        }
-        run += tot;
+    for (int w = 0; w < warp; ++w) {
+        gt_before += s.wcnt[w];
+        eq_before += s.wcnt[kWarps + w];
+    }
+    for (int i0 = w0; i0 < w1; i0 += 32) {
+        const int i = i0 + lane;
+        const uint32_t key = i < w1 ? key_at(s, src, i, cached) : 0u;
+        const unsigned mg = __ballot_sync(0xffffffffu, i < w1 && key > T);
+        const unsigned me = __ballot_sync(0xffffffffu, i < w1 && key == T);
+        const unsigned below = (1u << lane) - 1u;
+        const uint32_t g = gt_before + __popc(mg & below), e = eq_before + __popc(me & below);
+        const bool gt = (mg >> lane) & 1u, eq = (me >> lane) & 1u;
+        if (gt || (eq && e < need)) out[g + min(e, need)] = c0 + i;
+        gt_before += __popc(mg);
+        eq_before += __popc(me);
     }
     cluster.sync();  // no CTA leaves while a peer may still read its shared memory
 }
