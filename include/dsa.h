@@ -214,6 +214,29 @@ int dsa_sparse_mla_decode_noalloc(const dsa_cache *latent_cache, const uint16_t 
                                   const int32_t *slots, int32_t num_rows, int32_t k, float sm_scale, float *out,
                                   float *lse, int32_t *dev_status, void *stream);
 
+/*
+ * Quantise new tokens and write them into the caches (blog section
+ * "Low-latency decode: fused DSA decode path": the front end quantises the
+ * new token's index key, FP8 or MXFP4, and the new latent is written into
+ * the cache before the indexer scores).  For each i with slots[i] >= 0 the
+ * token's index key index_keys[i, 0:128] (bf16 bits) and latent
+ * latents[i, 0:576] (bf16 bits) are written at that physical slot of the two
+ * pools (the pools' base pointers are written through):
+ *   DSA_KEY_FP8:      s = amax / 448 (1 if amax = 0), code = e4m3(x / s), s stored as fp32
+ *   DSA_KEY_MXFP4:    per 32 values E = floor(log2 amax) - 2 + 127 clamped to [0, 254]
+ *                     (0 for an all-zero block), code = e2m1(x * 2^(127 - E))
+ *   DSA_LATENT_FP8:   code = e4m3(x / tensor_scale)
+ *   DSA_LATENT_NVFP4: per 16 values scale code = e4m3(amax / 6), code = e2m1(x / scale)
+ *                     (0 when the scale is 0); RoPE dims e4m3(x / tensor_scale)
+ * Scales and quotients are IEEE fp32 operations; codes are round-to-nearest-
+ * even with saturation (e4m3 to +-448, e2m1 to +-6), so the bytes are exact.
+ * Both pools must have the same num_pages; tensor_scale > 0 comes from the
+ * latent pool.  A slot outside the pools is DSA_ERR_BOUNDS (not written).
+ */
+int dsa_cache_insert(const dsa_cache *index_cache, const dsa_cache *latent_cache, const int32_t *slots,
+                     int32_t num_tokens, const uint16_t *index_keys, const uint16_t *latents, int32_t *dev_status,
+                     void *stream);
+
 /* Workspace bytes dsa_sparse_mla_decode needs for num_rows rows of k slots. */
 size_t dsa_sparse_mla_workspace_size(int32_t num_rows, int32_t num_heads, int32_t k);
 

@@ -75,6 +75,8 @@ def load_library(path: str | None = None):
         fn.argtypes = [ctypes.POINTER(_Cache), P, I32, P, I32, I32, F, P, P, P, P, ctypes.c_size_t, P]
     lib.dsa_sparse_mla_decode_noalloc.restype = ctypes.c_int
     lib.dsa_sparse_mla_decode_noalloc.argtypes = [ctypes.POINTER(_Cache), P, I32, P, I32, I32, F, P, P, P, P]
+    lib.dsa_cache_insert.restype = ctypes.c_int
+    lib.dsa_cache_insert.argtypes = [ctypes.POINTER(_Cache), ctypes.POINTER(_Cache), P, I32, P, P, P, P]
     lib.dsa_sparse_mla_workspace_size.restype = ctypes.c_size_t
     lib.dsa_sparse_mla_workspace_size.argtypes = [I32, I32, I32]
     if path is None:
@@ -84,7 +86,7 @@ def load_library(path: str | None = None):
 
 EXPORTED = ("dsa_version", "dsa_status_string", "dsa_indexer_logits", "dsa_topk", "dsa_page_to_slot",
             "dsa_sparse_mla_decode", "dsa_sparse_mla_prefill", "dsa_sparse_mla_workspace_size",
-            "dsa_sparse_mla_decode_noalloc")
+            "dsa_sparse_mla_decode_noalloc", "dsa_cache_insert")
 NOALLOC_MAX_ROWS = 8
 
 
@@ -162,6 +164,15 @@ def page_to_slot(block_table, row_req, row_ctx, max_ctx, pool_pages, idx, out=No
                                          _ptr(status), _stream(stream))
     _check(rc, "dsa_page_to_slot")
     return out
+
+
+def cache_insert(idx_pool, key_fmt, lat_pool, lat_fmt, tensor_scale, slots, index_keys, latents, status=None,
+                 stream=None):
+    """dsa_cache_insert: quantise new tokens (bf16 [n,128] keys, [n,576] latents) into the pools in place."""
+    ci, cl = _cache(idx_pool, key_fmt), _cache(lat_pool, lat_fmt, tensor_scale)
+    rc = load_library().dsa_cache_insert(ctypes.byref(ci), ctypes.byref(cl), _ptr(slots), slots.shape[0],
+                                         _ptr(index_keys), _ptr(latents), _ptr(status), _stream(stream))
+    _check(rc, "dsa_cache_insert")
 
 
 def sparse_mla_workspace_size(num_rows, num_heads, k) -> int:

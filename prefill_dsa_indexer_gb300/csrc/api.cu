@@ -236,4 +236,33 @@ int dsa_sparse_mla_prefill(const dsa_cache *latent_cache, const uint16_t *q, int
                              workspace, workspace_bytes, stream, false);
 }
 
+int dsa_cache_insert(const dsa_cache *index_cache, const dsa_cache *latent_cache, const int32_t *slots,
+                     int32_t num_tokens, const uint16_t *index_keys, const uint16_t *latents, int32_t *dev_status,
+                     void *stream) {
+    if (index_cache == nullptr || latent_cache == nullptr || num_tokens < 0) return DSA_ERR_INVALID_ARG;
+    if (index_cache->page_size != DSA_PAGE_SIZE || latent_cache->page_size != DSA_PAGE_SIZE) return DSA_ERR_UNSUPPORTED;
+    if (index_cache->format != DSA_KEY_FP8 && index_cache->format != DSA_KEY_MXFP4) return DSA_ERR_UNSUPPORTED;
+    if (latent_cache->format != DSA_LATENT_FP8 && latent_cache->format != DSA_LATENT_NVFP4) return DSA_ERR_UNSUPPORTED;
+    if (num_tokens == 0) return DSA_OK;
+    if (!index_cache->base || !latent_cache->base || !slots || !index_keys || !latents) return DSA_ERR_INVALID_ARG;
+    if (index_cache->num_pages != latent_cache->num_pages || index_cache->num_pages <= 0) return DSA_ERR_INVALID_ARG;
+    if (!aligned(index_cache->base, 16) || !aligned(latent_cache->base, 16) || !aligned(index_keys, 16) ||
+        !aligned(latents, 16))
+        return DSA_ERR_INVALID_ARG;
+    if (!std::isfinite(latent_cache->tensor_scale) || !(latent_cache->tensor_scale > 0.f)) return DSA_ERR_INVALID_ARG;
+    InsertArgs a;
+    a.idx_pool = static_cast<uint8_t *>(const_cast<void *>(index_cache->base));
+    a.key_fmt = index_cache->format;
+    a.lat_pool = static_cast<uint8_t *>(const_cast<void *>(latent_cache->base));
+    a.lat_fmt = latent_cache->format;
+    a.tensor_scale = latent_cache->tensor_scale;
+    a.num_pages = index_cache->num_pages;
+    a.slots = slots;
+    a.num_tokens = num_tokens;
+    a.keys = index_keys;
+    a.latents = latents;
+    a.status = dev_status;
+    return launch_status(launch_cache_insert(a, static_cast<cudaStream_t>(stream)));
+}
+
 }  // extern "C"

@@ -93,6 +93,22 @@ cudaError_t launch_sparse_mla(const MlaArgs &a, cudaStream_t s);
 
 size_t mla_workspace_bytes(int32_t num_rows, int32_t num_heads, int32_t k);
 
+struct InsertArgs {
+    uint8_t *idx_pool;
+    int32_t key_fmt;
+    uint8_t *lat_pool;
+    int32_t lat_fmt;
+    float tensor_scale;
+    int64_t num_pages;
+    const int32_t *slots;
+    int32_t num_tokens;
+    const uint16_t *keys;     // [n, 128] bf16 bits
+    const uint16_t *latents;  // [n, 576] bf16 bits
+    int32_t *status;
+};
+
+cudaError_t launch_cache_insert(const InsertArgs &a, cudaStream_t s);
+
 int device_sm_count();
 
 }  // namespace dsa
