@@ -169,17 +169,20 @@ int dsa_page_to_slot(const dsa_rows *rows, int64_t pool_pages, const int32_t *id
  * kv_t is the decoded latent of slot t (FP8: e4m3 * tensor_scale; NVFP4:
  * e2m1 * per-16 e4m3 scale for dims 0..511 and e4m3 * tensor_scale for the
  * RoPE dims).  q: [num_rows, num_heads, 576] bf16 bits, num_heads a multiple
- * of 16 and <= 128; slots: [num_rows, k] int32, -1 = unused; out:
+ * of 16 and <= 96; slots: [num_rows, k] int32, -1 = unused; out:
  * [num_rows, num_heads, 512] fp32; lse: [num_rows, num_heads] fp32 or NULL.
  * A row with no valid slot gets out = 0 and lse = -inf.  The contraction
  * runs on the tensor cores in fp16 x fp16 -> fp32: latents decode to fp16
  * exactly, q rounds from bf16 to fp16 (|q| > 65504 is DSA_ERR_RANGE).
  *
- * _decode splits each row's k tokens over several CTAs and merges the parts
- * by log-sum-exp; it needs a workspace of dsa_sparse_mla_workspace_size()
- * bytes (device, 256-byte aligned).  _prefill runs one CTA per row, needs no
- * workspace (pass NULL, 0) and suits many rows.  The split is fixed, so both
- * are batch-invariant; their results differ from each other by rounding.
+ * _decode splits each row's k tokens into parts of 128 (k <= 2048, else
+ * DSA_ERR_UNSUPPORTED), one CTA per part, keeps each part's normalised
+ * output in fp16 and merges the parts by log-sum-exp; it needs a workspace
+ * of dsa_sparse_mla_workspace_size() bytes (device, 256-byte aligned, no
+ * initial contents; it also holds the rows' queries converted once to the
+ * kernel's fp16 layout).  _prefill runs one CTA per row, needs no workspace
+ * (pass NULL, 0) and suits many rows.  The split is fixed, so both are
+ * batch-invariant; their results differ from each other by rounding.
  */
 int dsa_sparse_mla_decode(const dsa_cache *latent_cache, const uint16_t *q, int32_t num_heads,
                           const int32_t *slots, int32_t num_rows, int32_t k, float sm_scale, float *out,
@@ -201,7 +204,7 @@ int dsa_sparse_mla_prefill(const dsa_cache *latent_cache, const uint16_t *q, int
  * Same arguments, semantics and results as dsa_sparse_mla_decode, minus the
  * workspace.  The split-K partial outputs live in a fixed array in the
  * library's own device memory, sized for DSA_NOALLOC_MAX_ROWS rows of
- * k <= 2048 tokens and num_heads <= 96 (12,632,064 bytes, held by every GPU
+ * k <= 2048 tokens and num_heads <= 96 (13,565,952 bytes, held by every GPU
  * that loads the library until the process exits).  Larger calls return
  * DSA_ERR_WORKSPACE without launching.  The first call on a device looks up
  * the array's address with that device current; make it before capturing

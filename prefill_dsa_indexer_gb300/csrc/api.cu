@@ -205,17 +205,19 @@ static int sparse_mla_common(const dsa_cache *lat, const uint16_t *q, int32_t nu
     a.status = dev_status;
     a.splits = 1;
     if (decode) {
-        const int splits = (k + kMlaTokensPerSplit - 1) / kMlaTokensPerSplit;
-        if (splits > 16) return DSA_ERR_UNSUPPORTED;  // the split merge holds at most 16 parts
+        const size_t splits = mla_splits(static_cast<size_t>(k));
+        if (splits > static_cast<size_t>(kMlaMaxSplits)) return DSA_ERR_UNSUPPORTED;
         if (splits > 1) {
             const size_t need = mla_workspace_bytes(num_rows, num_heads, k);
             if (ws == nullptr || ws_bytes < need) return DSA_ERR_WORKSPACE;
             if (!aligned(ws, 256)) return DSA_ERR_INVALID_ARG;
-            const size_t o_bytes =
-                (static_cast<size_t>(num_rows) * splits * num_heads * DSA_VALUE_DIM * sizeof(float) + 255) / 256 * 256;
-            a.part_o = static_cast<float *>(ws);
-            a.part_ml = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + o_bytes);
-            a.splits = splits;
+            uint8_t *w = static_cast<uint8_t *>(ws);
+            a.part_o = reinterpret_cast<uint16_t *>(w);
+            w += mla_part_o_bytes(num_rows, num_heads, splits);
+            a.part_ml = reinterpret_cast<float *>(w);
+            w += mla_part_ml_bytes(num_rows, num_heads, splits);
+            a.qprep = w;
+            a.splits = static_cast<int32_t>(splits);
         }
     }
     return launch_status(launch_sparse_mla(a, static_cast<cudaStream_t>(stream)));

@@ -82,12 +82,27 @@ struct MlaArgs {
     float *out;
     float *lse;
     int32_t *status;
-    float *part_o;      // decode: [R, splits, H, 512] unnormalised partial outputs
+    uint16_t *part_o;   // decode: [R, splits, H, 512] fp16 partial outputs (normalised by their own sum)
     float *part_ml;     // decode: [R, splits, H, 2] running max (log2 units) and sum
+    uint8_t *qprep;     // decode: [R, 9 * H * 128] fp16 query images, laid out as the kernel's operand
     int32_t splits;     // 1 = write the final output directly
 };
 
-constexpr int kMlaTokensPerSplit = 256;
+// Decode splits every row's selected tokens into parts of this many tokens (fixed, so a row's
+// result does not depend on the batch), merged by log-sum-exp.
+constexpr int kMlaTokensPerSplit = 128;
+constexpr int kMlaMaxSplits = 16;
+
+constexpr size_t align256(size_t x) { return (x + 255) / 256 * 256; }
+constexpr size_t mla_part_o_bytes(size_t R, size_t H, size_t S) { return align256(R * S * H * 512 * 2); }
+constexpr size_t mla_part_ml_bytes(size_t R, size_t H, size_t S) { return align256(R * S * H * 2 * 4); }
+constexpr size_t mla_qprep_bytes(size_t R, size_t H) { return align256(R * 9 * H * 128); }
+constexpr size_t mla_splits(size_t k) { return (k + kMlaTokensPerSplit - 1) / kMlaTokensPerSplit; }
+constexpr size_t mla_workspace_bytes_for(size_t R, size_t H, size_t k) {
+    return mla_splits(k) <= 1 ? 0
+                               : mla_part_o_bytes(R, H, mla_splits(k)) + mla_part_ml_bytes(R, H, mla_splits(k)) +
+                                     mla_qprep_bytes(R, H);
+}
 
 cudaError_t launch_sparse_mla(const MlaArgs &a, cudaStream_t s);
 

@@ -27,9 +27,11 @@
 //   * Q's rows beyond the real heads only feed S rows nobody reads, so Q's
 //     128-row operand is packed at a stride of H rows per 64-dim block and
 //     the unused rows alias the next block.
-// Decode splits a row's tokens over several CTAs (fixed split size, so the
-// result does not depend on the batch) and merges the parts by log-sum-exp
-// in a second kernel; prefill writes the output directly.
+// Decode converts each row's query once into the kernel's fp16 operand image
+// (a small prep kernel), splits a row's tokens over several CTAs (fixed split
+// size, so the result does not depend on the batch), keeps each part's
+// normalised output in fp16 and merges the parts by log-sum-exp in a third
+// kernel; prefill converts Q in the kernel and writes the output directly.
 #include <cuda_fp16.h>
 
 #include "kernels.h"
@@ -92,6 +94,21 @@ __device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t b) {
 // tile whose 8-row groups are 1024 bytes apart.
 __device__ __forceinline__ uint32_t sw128(int row, int u) {
     return static_cast<uint32_t>(row * 128 + ((u ^ (row & 7)) << 4));
+}
+
+// Eight bf16 query values -> fp16 (times `sc`), flagging values outside fp16's finite range.
+__device__ __forceinline__ int4 q_unit_to_f16(int4 v, float sc, bool &range_err) {
+    const uint32_t w[4] = {static_cast<uint32_t>(v.x), static_cast<uint32_t>(v.y), static_cast<uint32_t>(v.z),
+                           static_cast<uint32_t>(v.w)};
+    uint32_t o[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const float lo = __uint_as_float(w[j] << 16) * sc, hi = __uint_as_float(w[j] & 0xffff0000u) * sc;
+        if (!(fabsf(lo) <= 65504.f) || !(fabsf(hi) <= 65504.f)) range_err = true;
+        __half2 hh = __floats2half2_rn(lo, hi);
+        o[j] = *reinterpret_cast<uint32_t *>(&hh);
+    }
+    return make_int4(o[0], o[1], o[2], o[3]);
 }
 
 struct GatherRegs {
@@ -229,6 +246,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const MlaArgs a
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + OFF_BARS);
     uint64_t *kv_full = bars + 0;   // gather -> MMA, softmax          (count 4)
     uint64_t *s_full = bars + 1;    // MMA -> softmax                   (commit)
+    uint64_t *q_full = bars + 2;    // bulk copy of the prepared Q -> MMA (tx bytes)
     uint64_t *s_free = bars + 3;    // softmax -> MMA                   (count 4)
     uint64_t *p_full = bars + 5;    // softmax -> MMA                   (count 4)
     uint64_t *pv_done = bars + 6;   // MMA -> gather, softmax           (commit)
@@ -255,6 +273,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const MlaArgs a
         flag[0] = flag[1] = 0;
         mbar_init(kv_full, 4);
         mbar_init(s_full, 1);
+        mbar_init(q_full, 1);
         mbar_init(s_free, 4);
         mbar_init(p_full, 4);
         mbar_init(pv_done, 1);
@@ -269,9 +288,17 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const MlaArgs a
     GatherRegs g;
     const int gtid = tid - 256;  // 0..127 in the gather warps
     if (warp >= 8 && n_tiles > 0) gather_load<FMT>(a, row_slots, 0, n_tok, gtid, g);
-    // ---- Q: bf16 -> fp16, 128-byte swizzled K-major, block c (64 dims) at c * H * 128;
-    // loads of a batch are all issued before any conversion
-    if (warp < 8) {
+    // ---- Q: fp16, 128-byte swizzled K-major, block c (64 dims) at c * H * 128.  Decode
+    // copies the image the prep kernel made for this row; prefill converts from bf16 here,
+    // issuing all loads of a batch before any conversion.
+    if (a.qprep != nullptr) {
+        if (tid == 0 && n_tiles > 0) {
+            const uint32_t blk = static_cast<uint32_t>(H) * 128;
+            const uint8_t *src = a.qprep + static_cast<int64_t>(row) * kChunks * blk;
+            mbar_arrive_expect_tx(q_full, kChunks * blk);
+            for (int c = 0; c < kChunks; ++c) bulk_load(qs + c * blk, src + c * blk, blk, q_full);
+        }
+    } else if (warp < 8) {
         constexpr int kUnits = DSA_LATENT_DIM / 8;  // 8-dim units per head
         constexpr int kBatch = 9;
         const uint16_t *qg = a.q + static_cast<int64_t>(row) * H * DSA_LATENT_DIM;
@@ -289,19 +316,9 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const MlaArgs a
                 const int e = e0 + i * 256;
                 if (e >= total) break;
                 const int h = e / kUnits, u = e % kUnits;
-                const uint32_t w[4] = {static_cast<uint32_t>(v[i].x), static_cast<uint32_t>(v[i].y),
-                                       static_cast<uint32_t>(v[i].z), static_cast<uint32_t>(v[i].w)};
                 const float sc = (u >= DSA_VALUE_DIM / 8) ? q_rope_scale : 1.0f;
-                uint32_t o[4];
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const float lo = __uint_as_float(w[j] << 16) * sc, hi = __uint_as_float(w[j] & 0xffff0000u) * sc;
-                    if (!(fabsf(lo) <= 65504.f) || !(fabsf(hi) <= 65504.f)) range_err = true;
-                    __half2 hh = __floats2half2_rn(lo, hi);
-                    o[j] = *reinterpret_cast<uint32_t *>(&hh);
-                }
                 const int c = u >> 3, uu = u & 7;
-                *reinterpret_cast<int4 *>(qs + c * H * 128 + sw128(h, uu)) = make_int4(o[0], o[1], o[2], o[3]);
+                *reinterpret_cast<int4 *>(qs + c * H * 128 + sw128(h, uu)) = q_unit_to_f16(v[i], sc, range_err);
             }
         }
         if (range_err) report(a.status, DSA_ERR_RANGE);
@@ -325,7 +342,9 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const MlaArgs a
             const uint64_t v_desc = sdesc_sw128(smem_u32(kv), kTok * 128, 1024);
             const uint64_t p_desc = sdesc_sw128(smem_u32(ps), 16, 1024);
             const uint32_t q_blk = (H * 128) >> 4, kv_blk = (kTok * 128) >> 4;  // 16-byte units
-            for (int i = 0; i < n_tiles; ++i) {
+            // the copied Q must land before the first S product (and before this CTA can exit)
+            const bool q_ok = a.qprep == nullptr || mbar_wait(q_full, 0, abort, a.status);
+            for (int i = 0; q_ok && i < n_tiles; ++i) {
                 if (!mbar_wait(kv_full, i & 1, abort, a.status)) break;
                 if (!mbar_wait(s_free, (i & 1) ^ 1, abort, a.status)) break;
                 tc_fence_after();
@@ -467,7 +486,9 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const MlaArgs a
                 if (lane == 0) mbar_arrive(p_full);
             }
             // final statistics of this head
-            inv_l[h] = (l > 0.f) ? o_scale / l : 0.f;
+            // a split's part stays in decoded-latent units (|value| <= 2688, safe in fp16);
+            // the merge applies the tensor scale
+            inv_l[h] = (l > 0.f) ? (a.splits == 1 ? o_scale : 1.0f) / l : 0.f;
             if (h < H) {
                 const float lse2 = (l > 0.f) ? m + log2f(l) : -INFINITY;
                 if (a.splits == 1) {
@@ -507,9 +528,10 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const MlaArgs a
         if (ok) ok = mbar_wait_warp(stats, 0, abort, a.status);
         if (ok) {
             tc_fence_after();
-            float *dst = (a.splits == 1)
-                             ? a.out + static_cast<int64_t>(row) * H * DSA_VALUE_DIM
-                             : a.part_o + (static_cast<int64_t>(row) * a.splits + split) * H * DSA_VALUE_DIM;
+            float *dst = a.out + static_cast<int64_t>(row) * H * DSA_VALUE_DIM;
+            __half *dst_h = reinterpret_cast<__half *>(a.part_o) +
+                            (static_cast<int64_t>(row) * a.splits + split) * H * DSA_VALUE_DIM;
+            const bool to_part = a.splits > 1;
             const int j0 = is_softmax ? 0 : 2;
             for (int j = j0; j < j0 + 2; ++j) {
                 const int d = 128 * j + 32 * quad + lane;
@@ -526,7 +548,9 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const MlaArgs a
                     for (int x = 0; x < 32; ++x) {
                         if (x >= 16 && !full32) break;
                         const float o = (n_tiles > 0) ? __uint_as_float(v[x]) * inv_l[c + x] : 0.f;
-                        dst[static_cast<int64_t>(c + x) * DSA_VALUE_DIM + d] = o;
+                        const int64_t at = static_cast<int64_t>(c + x) * DSA_VALUE_DIM + d;
+                        if (to_part) dst_h[at] = __float2half_rn(o);
+                        else dst[at] = o;
                     }
                 }
             }
@@ -539,47 +563,73 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const MlaArgs a
     }
 }
 
-// Merge the splits of each (row, head): O = sum_s w_s O_s / sum_s w_s with
-// w_s = l_s 2^(m_s - M), M = max_s m_s (log2 units).  One CTA per (row, head),
-// four output dims per thread.
+// Merge the splits of each (row, head): O = o_scale * sum_s w_s O_s / sum_s w_s with
+// w_s = l_s 2^(m_s - M), M = max_s m_s (log2 units), O_s the split's normalised
+// fp16 output.  One CTA per (row, head), four output dims per thread.
 __global__ void __launch_bounds__(128) mla_combine_kernel(const MlaArgs a) {
-    constexpr int kMaxSplits = 16;
     const int H = a.num_heads, S = a.splits;
     const int row = blockIdx.x / H, h = blockIdx.x % H;
     const float *ml = a.part_ml + static_cast<int64_t>(row) * S * H * 2;
+    const float o_scale = a.format == DSA_LATENT_FP8 ? a.tensor_scale : 1.0f;
     // all partial loads in flight at once
-    float4 o[kMaxSplits];
-    float ms[kMaxSplits], ls[kMaxSplits];
+    uint2 o[kMlaMaxSplits];
+    float ms[kMlaMaxSplits], ls[kMlaMaxSplits];
 #pragma unroll
-    for (int s = 0; s < kMaxSplits; ++s) {
+    for (int s = 0; s < kMlaMaxSplits; ++s) {
         if (s < S) {
             ms[s] = ml[(s * H + h) * 2];
             ls[s] = ml[(s * H + h) * 2 + 1];
-            o[s] = reinterpret_cast<const float4 *>(
+            o[s] = reinterpret_cast<const uint2 *>(
                 a.part_o + ((static_cast<int64_t>(row) * S + s) * H + h) * DSA_VALUE_DIM)[threadIdx.x];
         }
     }
     float M = -INFINITY;
 #pragma unroll
-    for (int s = 0; s < kMaxSplits; ++s)
+    for (int s = 0; s < kMlaMaxSplits; ++s)
         if (s < S) M = fmaxf(M, ms[s]);
     float wsum = 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-    for (int s = 0; s < kMaxSplits; ++s) {
+    for (int s = 0; s < kMlaMaxSplits; ++s) {
         if (s >= S || ms[s] == -INFINITY) continue;
         const float w = ls[s] * exp2f(ms[s] - M);
+        const float2 lo = __half22float2(*reinterpret_cast<const __half2 *>(&o[s].x));
+        const float2 hi = __half22float2(*reinterpret_cast<const __half2 *>(&o[s].y));
         wsum += w;
-        acc.x = fmaf(w, o[s].x, acc.x);
-        acc.y = fmaf(w, o[s].y, acc.y);
-        acc.z = fmaf(w, o[s].z, acc.z);
-        acc.w = fmaf(w, o[s].w, acc.w);
+        acc.x = fmaf(w, lo.x, acc.x);
+        acc.y = fmaf(w, lo.y, acc.y);
+        acc.z = fmaf(w, hi.x, acc.z);
+        acc.w = fmaf(w, hi.y, acc.w);
     }
-    const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+    const float inv = wsum > 0.f ? o_scale / wsum : 0.f;
     reinterpret_cast<float4 *>(a.out + (static_cast<int64_t>(row) * H + h) * DSA_VALUE_DIM)[threadIdx.x] =
         make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
     if (threadIdx.x == 0 && a.lse)
         a.lse[static_cast<int64_t>(row) * H + h] = wsum > 0.f ? (M + log2f(wsum)) * 0.6931471805599453f : -INFINITY;
+}
+
+// Decode query preparation: each row's bf16 query becomes, once, the exact fp16 shared-memory
+// image the attention kernel's Q operand needs (RoPE dims of NVFP4 latents times the tensor
+// scale), so every split of the row starts with one bulk copy instead of its own conversion.
+__global__ void __launch_bounds__(256) mla_qprep_kernel(const MlaArgs a) {
+    constexpr int kUnits = DSA_LATENT_DIM / 8;  // 8-dim units per head
+    const int H = a.num_heads;
+    const int64_t total = static_cast<int64_t>(a.num_rows) * H * kUnits;
+    const float q_rope_scale = (a.format == DSA_LATENT_FP8) ? 1.0f : a.tensor_scale;
+    bool range_err = false;
+    for (int64_t e = static_cast<int64_t>(blockIdx.x) * 256 + threadIdx.x; e < total;
+         e += static_cast<int64_t>(gridDim.x) * 256) {
+        const int64_t rh = e / kUnits;
+        const int u = static_cast<int>(e % kUnits);
+        const int64_t row = rh / H;
+        const int h = static_cast<int>(rh % H);
+        const int4 v = *reinterpret_cast<const int4 *>(a.q + e * 8);
+        const float sc = (u >= DSA_VALUE_DIM / 8) ? q_rope_scale : 1.0f;
+        const int c = u >> 3, uu = u & 7;
+        uint8_t *dst = a.qprep + row * (kChunks * H * 128) + c * H * 128 + sw128(h, uu);
+        *reinterpret_cast<int4 *>(dst) = q_unit_to_f16(v, sc, range_err);
+    }
+    if (range_err) report(a.status, DSA_ERR_RANGE);
 }
 
 template <int FMT>
@@ -593,6 +643,13 @@ cudaError_t launch_fmt(const MlaArgs &a, cudaStream_t s) {
         if (e != cudaSuccess) return e;
         configured_device = dev;
     }
+    if (a.qprep != nullptr) {
+        const int64_t units = static_cast<int64_t>(a.num_rows) * a.num_heads * (DSA_LATENT_DIM / 8);
+        const int blocks = static_cast<int>(units / 256 < 4096 ? (units + 255) / 256 : 4096);
+        mla_qprep_kernel<<<blocks, 256, 0, s>>>(a);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
     sparse_mla_kernel<FMT><<<a.num_rows * a.splits, kThreads, kSmemBytes, s>>>(a);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess || a.splits == 1) return e;
@@ -603,11 +660,8 @@ cudaError_t launch_fmt(const MlaArgs &a, cudaStream_t s) {
 }  // namespace
 
 size_t mla_workspace_bytes(int32_t num_rows, int32_t num_heads, int32_t k) {
-    const int splits = (k + kMlaTokensPerSplit - 1) / kMlaTokensPerSplit;
-    if (splits <= 1) return 0;
-    const size_t o = static_cast<size_t>(num_rows) * splits * num_heads * DSA_VALUE_DIM * sizeof(float);
-    const size_t ml = static_cast<size_t>(num_rows) * splits * num_heads * 2 * sizeof(float);
-    return (o + 255) / 256 * 256 + ml;
+    return mla_workspace_bytes_for(static_cast<size_t>(num_rows), static_cast<size_t>(num_heads),
+                                   static_cast<size_t>(k));
 }
 
 cudaError_t launch_sparse_mla(const MlaArgs &a, cudaStream_t s) {

@@ -28,9 +28,10 @@
 namespace dsa {
 namespace {
 
-// Sized for DSA_NOALLOC_MAX_ROWS rows of k <= 2048 selected tokens and
-// <= 96 heads: 8 splits x 96 heads x (512 partial outputs + max + sum) fp32.
-constexpr size_t kNoAllocScratchBytes = static_cast<size_t>(DSA_NOALLOC_MAX_ROWS) * 8 * 96 * (512 + 2) * 4;
+// Sized for DSA_NOALLOC_MAX_ROWS rows of k <= 2048 selected tokens and <= 96 heads (the
+// split partial outputs, their maxima and sums, and the rows' prepared queries).
+constexpr size_t kNoAllocScratchBytes = mla_workspace_bytes_for(DSA_NOALLOC_MAX_ROWS, 96, 2048);
+static_assert(kNoAllocScratchBytes == 13565952, "the size the header documents");
 
 static __device__ __align__(256) unsigned char g_mla_scratch[kNoAllocScratchBytes];
 

@@ -217,30 +217,14 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const TopkArgs a) {
         __syncthreads();
         if (gathered) {
             const int nc = static_cast<int>(s.ncand_all);
-            for (int i0 = 0; i0 < nc; i0 += kThreads) {
-                const int i = i0 + tid;
-                const uint32_t key = i < nc ? s.cand_all[i] : 0u;
-                const bool in = i < nc && key >= base && key <= top;
-                const uint32_t bin = in ? (key - base) >> shift : 0xffffffffu;
-                const unsigned peers = __match_any_sync(0xffffffffu, bin);
-                if (in && lane == __ffs(peers) - 1) atomicAdd(&s.hist[bin], __popc(peers));
+            for (int i = tid; i < nc; i += kThreads) {
+                const uint32_t key = s.cand_all[i];
+                if (key >= base && key <= top) atomicAdd(&s.hist[(key - base) >> shift], 1u);
             }
         } else {
-            // warp-aggregated histogram over the chunk (keys in lane order)
-            if (cached) {
-                for (int i0 = 0; i0 < nloc; i0 += kThreads) {
-                    const int i = i0 + tid;
-                    const uint32_t key = i < nloc ? s.cache[i] : 0u;
-                    const bool in = i < nloc && key >= base && key <= top;
-                    const uint32_t bin = in ? (key - base) >> shift : 0xffffffffu;
-                    const unsigned peers = __match_any_sync(0xffffffffu, bin);
-                    if (in && lane == __ffs(peers) - 1) atomicAdd(&s.hist[bin], __popc(peers));
-                }
-            } else {
-                for_each_key(s, src, nloc, false, ignore, [&](int, uint32_t key) {
-                    if (key >= base && key <= top) atomicAdd(&s.hist[(key - base) >> shift], 1u);
-                });
-            }
+            for_each_key(s, src, nloc, cached, ignore, [&](int, uint32_t key) {
+                if (key >= base && key <= top) atomicAdd(&s.hist[(key - base) >> shift], 1u);
+            });
         }
         if (!gathered) cluster.sync();
         else __syncthreads();

@@ -54,10 +54,12 @@ def test_status_strings_and_version(lib):
 
 
 def test_workspace_size_is_host_logic(lib):
-    # 2048 tokens split 256 per CTA -> 8 partial outputs of 96 x 512 fp32 plus (max, sum) per head
+    # 2048 tokens split 128 per CTA -> 16 partial outputs of 96 x 512 fp16, (max, sum) per head
+    # in fp32, and each row's query as 96 x 576 fp16
     got = lib.dsa_sparse_mla_workspace_size(4, 96, 2048)
-    assert got >= 4 * 8 * 96 * 512 * 4 + 4 * 8 * 96 * 2 * 4
-    assert lib.dsa_sparse_mla_workspace_size(4, 96, 256) == 0  # one split: no workspace
+    assert got >= 4 * 16 * 96 * 512 * 2 + 4 * 16 * 96 * 2 * 4 + 4 * 96 * 576 * 2
+    assert lib.dsa_sparse_mla_workspace_size(4, 96, 128) == 0  # one split: no workspace
+    assert lib.dsa_sparse_mla_workspace_size(4, 96, 129) > 0
     assert lib.dsa_sparse_mla_workspace_size(0, 96, 2048) == 0
 
 
