@@ -17,48 +17,75 @@
 //     shared-memory stages;
 //   * warp 1 issues tcgen05.mma kind::f8f6f4 (e4m3 x e4m3 -> fp32) with the
 //     KEYS on M = 128 and the group's G rows x 32 heads on N, K = 128, into a
-//     double-buffered TMEM accumulator; a group's G rows (speculative-verify
-//     rows or a prefill query block) share every key read;
-//   * 4 or 8 epilogue warps read one key lane each from TMEM, so the head
-//     reduction sum_h w_h * relu(acc_h) runs in registers, scale by s_t
+//     ring of up to 8 TMEM accumulators, so the MMA runs ahead of the
+//     read-out; a group's G rows (speculative-verify rows or a prefill query
+//     block) share every key read;
+//   * 8 epilogue warps read one key lane each from TMEM (two sets of four
+//     taking alternate tiles, or for G = 8 splitting a tile's rows), so the
+//     head reduction sum_h w_h * relu(acc_h) runs in registers, scale by s_t
 //     (s_t > 0 commutes with the relu), mask t >= L_r and write coalesced
-//     fp32 logits.
+//     fp32 logits; the warps that read a tile also release its stage.
 #include "indexer_common.cuh"
 
 namespace dsa {
 
 namespace {
 
-constexpr int kTileKeys = kIdxTileKeys;
 constexpr int kIdxPageBytes = DSA_PAGE_SIZE * (DSA_INDEX_DIM + 4);  // 8448
 constexpr int kIdxPageRows = kIdxPageBytes / 128;                    // 66 rows of 128 B
 
 template <int G>
 struct IdxCfg {
     static constexpr int N = 32 * G;
-    static constexpr int kStages = G >= 8 ? 5 : (G >= 4 ? 6 : 8);
+    // keys per tile: 256 (four pages, two M = 128 products) halves every per-tile cost of the
+    // pipeline for decode and verify; prefill's N = 256 accumulators keep 128-key tiles
+    static constexpr int kTileKeys = G >= 8 ? 128 : 256;
+    static constexpr int kPagesPerTile = kTileKeys / DSA_PAGE_SIZE;
+    static constexpr int kHalves = kTileKeys / 128;
+    // Epilogue: 8 warps.  G = 8 splits a tile's rows over two sets of 4 warps; smaller G lets
+    // two sets of 4 warps take alternate tiles, so one tile's TMEM read-out overlaps the next.
     static constexpr int kEpiSplit = G >= 8 ? 2 : 1;
-    static constexpr int kEpiWarps = 4 * kEpiSplit;
+    static constexpr int kEpiGroups = G >= 8 ? 1 : 2;
+    static constexpr int kWarpsPerTile = 4 * kEpiSplit;
+    static constexpr int kEpiWarps = kWarpsPerTile * kEpiGroups;
     static constexpr int kRowsPerEpiWarp = G / kEpiSplit;
     static constexpr int kThreads = 128 + 32 * kEpiWarps;
-    static constexpr uint32_t kTmemCols = (2 * N < 32) ? 32u : static_cast<uint32_t>(2 * N);
+    // TMEM accumulators (kHalves x N columns each): enough that the MMA runs several tiles ahead
+    static constexpr int kAccCols = kHalves * N;
+    static constexpr int kAcc = (512 / kAccCols) < 8 ? (512 / kAccCols) : 8;
+    static constexpr uint32_t kTmemCols = static_cast<uint32_t>(kAcc * kAccCols);
     static constexpr int kKeyBytes = kTileKeys * 128;
     static constexpr int kQBytes = N * 128;
+    static constexpr int kNumBarsFor(int st) { return 2 * st + 2 * kAcc + 5; }
+    // shared memory for `st` key stages (layout below)
+    static constexpr int smem_for(int st) {
+        return st * kKeyBytes + 2 * kQBytes + st * kTileKeys * 4 + kEpiGroups * 2 * N * 4 +
+               (kIndexerMaxGroups + 4) * 4 + 2 * kIndexerMaxGroups * 4 + kNumBarsFor(st) * 8 + 64 + 1024;
+    }
+    // as many key stages as fit (up to 12 x 128 keys)
+    static constexpr int pick_stages() {
+        int st = 12 / kHalves;
+        while (smem_for(st) > 227 * 1024) --st;
+        return st;
+    }
+    static constexpr int kStages = pick_stages();
     static constexpr int OFF_KEYS = 0;
     static constexpr int OFF_Q = OFF_KEYS + kStages * kKeyBytes;
     static constexpr int OFF_SCALES = OFF_Q + 2 * kQBytes;
     static constexpr int OFF_W = OFF_SCALES + kStages * kTileKeys * 4;
-    static constexpr int OFF_PREFIX = OFF_W + 2 * N * 4;
+    static constexpr int OFF_PREFIX = OFF_W + kEpiGroups * 2 * N * 4;
     static constexpr int OFF_GREQ = OFF_PREFIX + (kIndexerMaxGroups + 4) * 4;
     static constexpr int OFF_GMAX = OFF_GREQ + kIndexerMaxGroups * 4;
     static constexpr int OFF_BARS = OFF_GMAX + kIndexerMaxGroups * 4;
-    static constexpr int kNumBars = 2 * kStages + 9;
+    static constexpr int kNumBars = kNumBarsFor(kStages);
     static constexpr int OFF_MISC = OFF_BARS + kNumBars * 8;
     static constexpr int kSmemBytes = OFF_MISC + 64 + 1024;  // + slack for 1024-byte alignment
     static_assert(kTmemCols == 32 || kTmemCols == 64 || kTmemCols == 128 || kTmemCols == 256 ||
                       kTmemCols == 512,
                   "TMEM allocation must be a power of two >= 32");
+    static_assert(kAcc % kEpiGroups == 0, "an accumulator always belongs to the same epilogue set");
     static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+    static_assert(kSmemBytes == smem_for(kStages), "stage sizing matches the layout");
 };
 
 template <int G>
@@ -76,29 +103,34 @@ __global__ void __launch_bounds__(IdxCfg<G>::kThreads, 1)
     int32_t *greq = reinterpret_cast<int32_t *>(smem + C::OFF_GREQ);
     int32_t *gmax = reinterpret_cast<int32_t *>(smem + C::OFF_GMAX);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::OFF_BARS);
-    uint64_t *full = bars;                      // [kStages] TMA -> MMA
-    uint64_t *empty = bars + C::kStages;        // [kStages] MMA + epilogue -> TMA
-    uint64_t *tfull = bars + 2 * C::kStages;    // [2] MMA -> epilogue
-    uint64_t *tempty = tfull + 2;               // [2] epilogue -> MMA
-    uint64_t *qfull = tfull + 4;                // [2] TMA -> MMA (query of a group)
-    uint64_t *qempty = tfull + 6;               // [2] MMA -> TMA
-    uint64_t *mma_done = tfull + 8;             // [1] all MMAs retired
+    uint64_t *full = bars;                       // [kStages] TMA -> MMA, epilogue
+    uint64_t *empty = bars + C::kStages;         // [kStages] epilogue -> TMA
+    uint64_t *tfull = bars + 2 * C::kStages;     // [kAcc] MMA -> epilogue
+    uint64_t *tempty = tfull + C::kAcc;          // [kAcc] epilogue -> MMA
+    uint64_t *qfull = tempty + C::kAcc;          // [2] TMA -> MMA (query of a group)
+    uint64_t *qempty = qfull + 2;                // [2] MMA -> TMA
+    uint64_t *mma_done = qempty + 2;             // [1] all MMAs retired
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
     volatile int *abort = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 4);
+    volatile int *epi_ok = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 8);  // [2]
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int ng = a.num_groups;
 
-    plan_groups<G>(a, prefix, greq, gmax);
+    plan_groups<G, C::kTileKeys>(a, prefix, greq, gmax);
     if (tid == 0) {
         *abort = 0;
         for (int s = 0; s < C::kStages; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 1 + C::kEpiWarps);  // MMA commit + one arrival per epilogue warp
+            // the epilogue set that read a tile releases its stage: it saw the MMA's
+            // completion (so the keys are consumed) and has read the scales
+            mbar_init(&empty[s], 1);
+        }
+        for (int i = 0; i < C::kAcc; ++i) {
+            mbar_init(&tfull[i], 1);
+            mbar_init(&tempty[i], 1);
         }
         for (int i = 0; i < 2; ++i) {
-            mbar_init(&tfull[i], 1);
-            mbar_init(&tempty[i], C::kEpiWarps);
             mbar_init(&qfull[i], 1);
             mbar_init(&qempty[i], 1);
         }
@@ -134,26 +166,43 @@ __global__ void __launch_bounds__(IdxCfg<G>::kThreads, 1)
             int cur = -1, gc = -1;
             int32_t it = 0;
             bool ok = true;
-            for (int32_t base = w_begin; ok && base < w_end; base += 32) {
-                int32_t pg0 = 0, pg1 = 0;
+            // page ids of tile `base + lane`; the next batch is in flight while this one is issued
+            constexpr int PPT = C::kPagesPerTile;
+            auto fetch = [&](int32_t base, int32_t (&pg)[PPT]) {
+#pragma unroll
+                for (int p = 0; p < PPT; ++p) pg[p] = 0;
                 if (base + lane < w_end) {
                     TileWalker mine{prefix, 0};
                     mine.seek(base + lane, ng);
                     const int g = mine.g, kt = base + lane - prefix[g];
-                    const int nkeys = min(kTileKeys, gmax[g] - kt * kTileKeys);
+                    const int nkeys = min(C::kTileKeys, gmax[g] - kt * C::kTileKeys);
                     const int32_t *bt = a.block_table + static_cast<int64_t>(greq[g]) * a.bt_stride;
-                    pg0 = bt[kt * 2];
-                    pg1 = nkeys > DSA_PAGE_SIZE ? bt[kt * 2 + 1] : 0;
-                    if (pg0 < 0 || pg0 >= a.num_pages || pg1 < 0 || pg1 >= a.num_pages) {
-                        report(a.status, DSA_ERR_BOUNDS);
-                        pg0 = (pg0 < 0 || pg0 >= a.num_pages) ? 0 : pg0;
-                        pg1 = (pg1 < 0 || pg1 >= a.num_pages) ? 0 : pg1;
+#pragma unroll
+                    for (int p = 0; p < PPT; ++p)
+                        if (p * DSA_PAGE_SIZE < nkeys) pg[p] = bt[kt * PPT + p];
+                }
+            };
+            int32_t nx[PPT];
+            fetch(w_begin, nx);
+            for (int32_t base = w_begin; ok && base < w_end; base += 32) {
+                int32_t pg[PPT];
+                bool bad = false;
+#pragma unroll
+                for (int p = 0; p < PPT; ++p) {
+                    pg[p] = nx[p];
+                    if (pg[p] < 0 || pg[p] >= a.num_pages) {
+                        bad = true;
+                        pg[p] = 0;
                     }
                 }
+                if (bad) report(a.status, DSA_ERR_BOUNDS);
+                if (base + 32 < w_end) fetch(base + 32, nx);
                 const int cnt = min(32, w_end - base);
                 for (int j = 0; j < cnt; ++j, ++it) {
                     const int32_t w = base + j;
-                    const int32_t p0 = __shfl_sync(0xffffffffu, pg0, j), p1 = __shfl_sync(0xffffffffu, pg1, j);
+                    int32_t pj[PPT];
+#pragma unroll
+                    for (int p = 0; p < PPT; ++p) pj[p] = __shfl_sync(0xffffffffu, pg[p], j);
                     wk.advance(w);
                     const int g = wk.g;
                     if (g != cur) {
@@ -181,15 +230,16 @@ __global__ void __launch_bounds__(IdxCfg<G>::kThreads, 1)
                     }
                     if (lane == 0) {
                         const int kt = w - prefix[g];
-                        const int nkeys = min(kTileKeys, gmax[g] - kt * kTileKeys);
+                        const int nkeys = min(C::kTileKeys, gmax[g] - kt * C::kTileKeys);
                         const int npages = (nkeys + DSA_PAGE_SIZE - 1) / DSA_PAGE_SIZE;
                         mbar_arrive_expect_tx(&full[stage], npages * (DSA_PAGE_SIZE * 128 + DSA_PAGE_SIZE * 4));
-                        for (int p = 0; p < npages; ++p) {
-                            const int32_t page = p == 0 ? p0 : p1;
+#pragma unroll
+                        for (int p = 0; p < PPT; ++p) {
+                            if (p >= npages) break;
                             tma_load_2d(keys + stage * C::kKeyBytes + p * (DSA_PAGE_SIZE * 128), &key_map,
-                                        &full[stage], 0, page * kIdxPageRows);
-                            bulk_load(scales + stage * kTileKeys + p * DSA_PAGE_SIZE,
-                                      a.pool + static_cast<int64_t>(page) * kIdxPageBytes + DSA_PAGE_SIZE * 128,
+                                        &full[stage], 0, pj[p] * kIdxPageRows);
+                            bulk_load(scales + stage * C::kTileKeys + p * DSA_PAGE_SIZE,
+                                      a.pool + static_cast<int64_t>(pj[p]) * kIdxPageBytes + DSA_PAGE_SIZE * 128,
                                       DSA_PAGE_SIZE * 4, &full[stage]);
                         }
                     }
@@ -211,19 +261,25 @@ __global__ void __launch_bounds__(IdxCfg<G>::kThreads, 1)
                     if (!mbar_wait(&qfull[gc & 1], (gc >> 1) & 1, abort, a.status)) break;
                 }
                 const int qb = gc & 1;
-                const int stage = it % C::kStages, as = it & 1;
-                if (!mbar_wait(&tempty[as], ((it >> 1) & 1) ^ 1, abort, a.status)) break;
+                const int stage = it % C::kStages, b = it % C::kAcc;
+                if (!mbar_wait(&tempty[b], ((it / C::kAcc) & 1) ^ 1, abort, a.status)) break;
                 if (!mbar_wait(&full[stage], (it / C::kStages) & 1, abort, a.status)) break;
                 tc_fence_after();
                 const uint32_t a_addr = smem_u32(keys + stage * C::kKeyBytes);
                 const uint32_t b_addr = smem_u32(qbuf + qb * C::kQBytes);
+                const int kt = w - prefix[g];
+                const int nkeys = min(C::kTileKeys, gmax[g] - kt * C::kTileKeys);
 #pragma unroll
-                for (int kk = 0; kk < DSA_INDEX_DIM / 32; ++kk) {
-                    mma_f8(tmem_base + as * C::N, sdesc_sw128(a_addr + kk * 32, 16, 1024),
-                           sdesc_sw128(b_addr + kk * 32, 16, 1024), kIdesc, kk > 0 ? 1u : 0u);
+                for (int hf = 0; hf < C::kHalves; ++hf) {
+                    if (hf * 128 >= nkeys) break;  // a half past the context's end is not loaded
+#pragma unroll
+                    for (int kk = 0; kk < DSA_INDEX_DIM / 32; ++kk) {
+                        mma_f8(tmem_base + b * C::kAccCols + hf * C::N,
+                               sdesc_sw128(a_addr + hf * (128 * 128) + kk * 32, 16, 1024),
+                               sdesc_sw128(b_addr + kk * 32, 16, 1024), kIdesc, kk > 0 ? 1u : 0u);
+                    }
                 }
-                mma_commit(&empty[stage]);
-                mma_commit(&tfull[as]);
+                mma_commit(&tfull[b]);
                 const bool last_of_group = (w + 1 == w_end) || (prefix[g + 1] <= w + 1);
                 if (last_of_group) mma_commit(&qempty[qb]);
             }
@@ -232,58 +288,76 @@ __global__ void __launch_bounds__(IdxCfg<G>::kThreads, 1)
         } else if (warp >= 4) {
             // ------------------------------------------------ epilogue
             const int e = warp - 4;
-            const int quad = warp & 3;
-            const int rbeg = (e >> 2) * C::kRowsPerEpiWarp;
+            const int grp = e / C::kWarpsPerTile;  // this set takes tiles it = grp (mod kEpiGroups)
+            const int sub = e % C::kWarpsPerTile;
+            const int quad = warp & 3;             // TMEM lane quadrant this warp may read
+            const int rbeg = (sub >> 2) * C::kRowsPerEpiWarp;
             const int key_lane = quad * 32 + lane;
             TileWalker wk{prefix, 0};
             wk.seek(w_begin, ng);
             int cur = -1, gc = -1;
             int ctx[C::kRowsPerEpiWarp];
             int64_t row_off[C::kRowsPerEpiWarp];
-            int32_t it = 0;
-            for (int32_t w = w_begin; w < w_end; ++w, ++it) {
+            for (int32_t it = grp, w = w_begin + grp; w < w_end; it += C::kEpiGroups, w += C::kEpiGroups) {
                 wk.advance(w);
                 const int g = wk.g;
                 if (g != cur) {
                     ++gc;
                     cur = g;
-                    float *wb = wbuf + (gc & 1) * C::N;
+                    float *wb = wbuf + (grp * 2 + (gc & 1)) * C::N;
                     const int row0 = (a.group0 + g) * G;
-                    for (int i = tid - 128; i < C::N; i += 32 * C::kEpiWarps)
+                    for (int i = sub * 32 + lane; i < C::N; i += 32 * C::kWarpsPerTile)
                         wb[i] = a.head_w[static_cast<int64_t>(row0) * DSA_INDEX_HEADS + i];
-                    named_bar_sync(1, 32 * C::kEpiWarps);
+                    named_bar_sync(1 + grp, 32 * C::kWarpsPerTile);
 #pragma unroll
                     for (int j = 0; j < C::kRowsPerEpiWarp; ++j) {
                         ctx[j] = min(a.row_ctx[row0 + rbeg + j], a.max_ctx);
                         row_off[j] = static_cast<int64_t>(row0 + rbeg + j) * a.logits_stride;
                     }
                 }
-                const float *wb = wbuf + (gc & 1) * C::N;
-                const int stage = it % C::kStages, as = it & 1;
-                if (!mbar_wait_warp(&tfull[as], (it >> 1) & 1, abort, a.status)) break;
-                // the stage's TMA phase is complete (the MMA waited for it) and cannot be
-                // re-armed before this warp arrives on empty[stage]; waiting on it here makes
-                // the bulk-copied scales visible to this thread.
-                if (!mbar_wait_warp(&full[stage], (it / C::kStages) & 1, abort, a.status)) break;
+                const float *wb = wbuf + (grp * 2 + (gc & 1)) * C::N;
+                const int stage = it % C::kStages, b = it % C::kAcc;
+                // one thread of the set waits for the accumulator and the stage (the stage's TMA
+                // phase is complete, as the MMA waited for it, and cannot be re-armed before this
+                // set releases it; waiting on it orders the bulk-copied scales); the set's
+                // named barrier passes the acquire on to the other warps
+                if (sub == 0 && lane == 0) {
+                    const bool ok = mbar_wait(&tfull[b], (it / C::kAcc) & 1, abort, a.status) &&
+                                    mbar_wait(&full[stage], (it / C::kStages) & 1, abort, a.status);
+                    epi_ok[grp] = ok ? 1 : 0;
+                }
+                named_bar_sync(1 + grp, 32 * C::kWarpsPerTile);
+                if (!epi_ok[grp]) break;
                 tc_fence_after();
-                const float s_t = scales[stage * kTileKeys + key_lane];
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&empty[stage]);
-                const int t = (w - prefix[g]) * kTileKeys + key_lane;
+                const int t0 = (w - prefix[g]) * C::kTileKeys;
+                const int nkeys = min(C::kTileKeys, gmax[g] - t0);
 #pragma unroll
-                for (int j = 0; j < C::kRowsPerEpiWarp; ++j) {
-                    uint32_t acc[32];
-                    tmem_ld32(tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + as * C::N + (rbeg + j) * 32, acc);
-                    tmem_ld_wait();
-                    const float *wr = wb + (rbeg + j) * 32;
-                    float sum = 0.f;
+                for (int hf = 0; hf < C::kHalves; ++hf) {
+                    if (hf * 128 >= nkeys) break;  // never computed (and never loaded)
+                    const float s_t = scales[stage * C::kTileKeys + hf * 128 + key_lane];
+                    const int t = t0 + hf * 128 + key_lane;
 #pragma unroll
-                    for (int h = 0; h < 32; ++h) sum = fmaf(wr[h], fmaxf(__uint_as_float(acc[h]), 0.f), sum);
-                    if (t < ctx[j]) a.logits[row_off[j] + t] = sum * s_t;
+                    for (int j = 0; j < C::kRowsPerEpiWarp; ++j) {
+                        uint32_t acc[32];
+                        tmem_ld32(tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + b * C::kAccCols + hf * C::N +
+                                      (rbeg + j) * 32,
+                                  acc);
+                        tmem_ld_wait();
+                        const float *wr = wb + (rbeg + j) * 32;
+                        float s4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                        for (int h = 0; h < 32; ++h)
+                            s4[h & 3] = fmaf(wr[h], fmaxf(__uint_as_float(acc[h]), 0.f), s4[h & 3]);
+                        const float sum = (s4[0] + s4[1]) + (s4[2] + s4[3]);
+                        if (t < ctx[j]) a.logits[row_off[j] + t] = sum * s_t;
+                    }
                 }
                 tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&tempty[as]);
+                named_bar_sync(1 + grp, 32 * C::kWarpsPerTile);  // the set is done with the stage and the accumulator
+                if (sub == 0 && lane == 0) {
+                    mbar_arrive(&empty[stage]);
+                    mbar_arrive(&tempty[b]);
+                }
             }
         }
     }

@@ -2,8 +2,8 @@
 //
 // A launch covers groups [group0, group0 + num_groups) of G consecutive rows
 // (one request each).  Every CTA computes, in shared memory, each group's
-// request, its longest visible context and the prefix sums of its 128-key
-// tile counts; the tiles of all groups then form one list that the
+// request, its longest visible context and the prefix sums of its key-tile
+// counts (128 or 256 keys per tile); the tiles of all groups then form one list that the
 // persistent grid splits into equal contiguous shares (key-balanced).
 #pragma once
 
@@ -34,7 +34,7 @@ struct TileWalker {
 
 // Fill greq/gmax/prefix for the launch's groups.  Must be followed by
 // __syncthreads() and then plan_scan() by warp 0.
-template <int G>
+template <int G, int TK = kIdxTileKeys>
 __device__ __forceinline__ void plan_groups(const IndexerArgs &a, int32_t *prefix, int32_t *greq, int32_t *gmax) {
     for (int g = threadIdx.x; g < a.num_groups; g += blockDim.x) {
         const int row0 = (a.group0 + g) * G;
@@ -52,7 +52,7 @@ __device__ __forceinline__ void plan_groups(const IndexerArgs &a, int32_t *prefi
         }
         greq[g] = req;
         gmax[g] = mx;
-        prefix[g + 1] = (mx + kIdxTileKeys - 1) / kIdxTileKeys;
+        prefix[g + 1] = (mx + TK - 1) / TK;
     }
     if (threadIdx.x == 0) prefix[0] = 0;
 }

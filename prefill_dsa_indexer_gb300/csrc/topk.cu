@@ -7,19 +7,27 @@
 // to the lower position, reported in ascending position order, -1 padded.
 //
 // Method: radix selection on order-preserving 32-bit keys, one thread-block
-// cluster per row.  The row is cut into one contiguous chunk per CTA of the
-// cluster (2..8 CTAs for long rows), so a row is read by several SMs at once;
-// a chunk of up to kCacheElems keys is read from HBM once and kept in
-// shared memory for every pass.  Each pass builds a local 2048-bin histogram;
-// the CTAs add each other's histograms through distributed shared memory, so
-// every CTA reaches the same decision.  The first histogram spans the row's
-// actual key range [min, max] with power-of-two bins, so the bins spread even
-// when all logits sit within a few octaves; the bin holding the k-th key is
-// compacted into a candidate list per CTA and refined (at most three rounds)
-// down to the exact threshold key T and the number of keys equal to T to
-// take.  A last pass writes the selection in position order: block prefix
-// sums inside a chunk, the counts of the lower-ranked CTAs of the cluster as
-// the chunk's offset.  Output order and values never depend on timing.
+// cluster of CL = 1..16 CTAs per row (CL chosen on the host so that a batch
+// of rows covers the SMs).  The row is cut into one contiguous chunk per CTA;
+// the first kCacheElems keys of a chunk are read from memory once and kept in
+// shared memory for every later pass.
+//   1. The cluster agrees on the row's key range [min, max].
+//   2. Cluster rounds: every CTA histograms its chunk into 2048 bins spanning
+//      the current interval (power-of-two bin width); the histograms are summed
+//      by a reduce-scatter over distributed shared memory (CTA r adds up bin
+//      slice r of every CTA and writes the sums back to all of them), so every
+//      CTA reaches the same decision: the bin holding the k-th key becomes the
+//      next interval.  Each CTA also tracks how many of its own keys lie above
+//      the interval.
+//   3. Once the interval holds at most kCandCap keys, every CTA publishes its
+//      keys inside it (its candidates) and its count above it; every CTA then
+//      gathers all of them in rank order and refines alone (identically) down
+//      to the exact threshold key T and the number of keys equal to T to take.
+//      The gathered candidates also give every CTA the number of selected keys
+//      in the lower-ranked chunks, so no further cluster barrier is needed.
+//   4. The selection is written in position order: warp-contiguous segments,
+//      ballot counts, warp prefix sums.  Output order and values never depend
+//      on timing.
 #include <cooperative_groups.h>
 
 #include "kernels.h"
@@ -36,20 +44,25 @@ constexpr int kWarps = kThreads / 32;
 constexpr int kBins = 2048;
 constexpr int kCacheElems = 40960;
 constexpr int kCandCap = 4096;
-constexpr int kMaxCluster = 8;
+constexpr int kMaxCluster = 16;
+constexpr int kMinChunk = 4096;  // a row is not cut into chunks shorter than this
 
 struct TopkSmem {
     uint32_t cache[kCacheElems];
-    uint32_t hist[kBins];
-    uint32_t cand[kCandCap];      // this CTA's keys inside the threshold bin
-    uint32_t cand_all[kCandCap];  // the cluster's candidates, gathered into every CTA
-    uint32_t wcnt[2 * kWarps];    // per-warp counts of keys > T and == T
-    unsigned long long scan[kWarps + 1];
+    uint32_t hist[kBins];         // this CTA's histogram (read by the cluster's reduce-scatter)
+    uint32_t hsum[kBins];         // the cluster's histogram (written by the cluster)
+    uint32_t cand[kCandCap];      // this CTA's keys inside the interval (read by the cluster)
+    uint32_t cand_all[kCandCap];  // every CTA's candidates, in rank order
+    unsigned long long wsum[kWarps];
+    uint32_t wgt[kWarps], weq[kWarps];
     uint32_t red[2 * kWarps];
-    uint32_t mm[2];   // this CTA's chunk key range (read by the cluster)
-    uint32_t cnt[2];  // this CTA's chunk counts of keys > T and == T (read by the cluster)
-    uint32_t sel_bin, sel_above, sel_count;
-    uint32_t ncand, ncand_all;
+    uint32_t roff[kMaxCluster + 1];  // rank r's candidates start at cand_all[roff[r]]
+    uint32_t mm[2];      // this CTA's chunk key range (read by the cluster)
+    uint32_t pub[3];     // published: candidates, keys above the interval, keys == T (read by the cluster)
+    uint32_t sel[5];     // selected bin, cluster keys above / in it, local keys above / in it
+    uint32_t ncand;
+    uint32_t range[2];
+    uint32_t before[2];  // selected keys > T and == T in the lower-ranked chunks
     int32_t bad;
 };
 
@@ -68,66 +81,146 @@ __device__ __forceinline__ uint32_t f2key(float f, bool &nan) {
 __device__ __forceinline__ unsigned long long warp_incl_scan(unsigned long long v, int lane) {
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-        unsigned long long t = __shfl_up_sync(0xffffffffu, v, o);
+        const unsigned long long t = __shfl_up_sync(0xffffffffu, v, o);
         if (lane >= o) v += t;
     }
     return v;
 }
 
-// Exclusive block-wide prefix sum; `total` receives the block's sum.
-__device__ unsigned long long block_excl_scan(unsigned long long v, TopkSmem &s, unsigned long long &total) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    unsigned long long incl = warp_incl_scan(v, lane);
-    if (lane == 31) s.scan[warp] = incl;
-    __syncthreads();
-    if (warp == 0) {
-        unsigned long long w = s.scan[lane];
-        unsigned long long wi = warp_incl_scan(w, lane);
-        s.scan[lane] = wi - w;
-        if (lane == 31) s.scan[kWarps] = wi;
+__device__ __forceinline__ uint32_t warp_incl_scan32(uint32_t v, int lane) {
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t t = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += t;
     }
-    __syncthreads();
-    unsigned long long r = s.scan[warp] + incl - v;
-    total = s.scan[kWarps];
-    __syncthreads();
-    return r;
+    return v;
 }
 
-// Calls f(i, key) for every key of the chunk: from the shared-memory copy, or
-// from global memory (16-byte loads, four per thread in flight) when the chunk
-// is longer than the copy.
-template <typename F>
-__device__ __forceinline__ void for_each_key(const TopkSmem &s, const float *src, int n, bool cached, bool &nan,
-                                             F &&f) {
-    if (cached) {
-        for (int i = threadIdx.x; i < n; i += kThreads) f(i, s.cache[i]);
-        return;
+// 32-bit shared::cluster address of `p` in the shared memory of CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t peer_addr(const void *p, uint32_t rank) {
+    uint32_t a;
+    asm("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(smem_u32(p)), "r"(rank));
+    return a;
+}
+__device__ __forceinline__ uint32_t ld_peer(uint32_t addr) {
+    uint32_t v;
+    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_peer(uint32_t addr, uint32_t v) {
+    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory"); }
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
+
+// The chunk's keys [0, n): the first kCacheElems from shared memory, the rest from global memory.
+struct Chunk {
+    const float *src;
+    int n, ncache;
+    __device__ __forceinline__ uint32_t key(const TopkSmem &s, int i) const {
+        bool nan = false;
+        return i < ncache ? s.cache[i] : f2key(src[i], nan);
     }
-    const bool vec = (reinterpret_cast<uintptr_t>(src) & 15) == 0;
+};
+
+// Keys i .. i+3 of the chunk (i a multiple of 4); positions >= lim read as 0 and are
+// flagged out of range.
+__device__ __forceinline__ void keys4(const TopkSmem &s, const Chunk &c, int i, int lim, uint32_t (&k)[4]) {
+    if (i + 3 < c.ncache && i + 3 < lim) {
+        const uint4 v = *reinterpret_cast<const uint4 *>(&s.cache[i]);
+        k[0] = v.x;
+        k[1] = v.y;
+        k[2] = v.z;
+        k[3] = v.w;
+    } else {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) k[q] = (i + q < lim) ? c.key(s, i + q) : 0u;
+    }
+}
+
+// First pass: reads every key of the chunk (16-byte loads, four per thread in
+// flight), fills the shared-memory copy and calls f(key).
+template <typename F>
+__device__ __forceinline__ void first_pass(TopkSmem &s, const Chunk &c, bool &nan, F &&f) {
+    const bool vec = (reinterpret_cast<uintptr_t>(c.src) & 15) == 0;
     int i0 = 0;
     if (vec) {
-        const int n16 = n & ~(16 * kThreads - 1);
+        const int n16 = c.n & ~(16 * kThreads - 1);
         for (; i0 < n16; i0 += 16 * kThreads) {
             float4 v[4];
 #pragma unroll
-            for (int u = 0; u < 4; ++u)
-                v[u] = reinterpret_cast<const float4 *>(src + i0)[u * kThreads + threadIdx.x];
+            for (int u = 0; u < 4; ++u) v[u] = reinterpret_cast<const float4 *>(c.src + i0)[u * kThreads + threadIdx.x];
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
                 const int i = i0 + 4 * (u * kThreads + threadIdx.x);
-                f(i, f2key(v[u].x, nan));
-                f(i + 1, f2key(v[u].y, nan));
-                f(i + 2, f2key(v[u].z, nan));
-                f(i + 3, f2key(v[u].w, nan));
+                const uint32_t k4[4] = {f2key(v[u].x, nan), f2key(v[u].y, nan), f2key(v[u].z, nan),
+                                        f2key(v[u].w, nan)};
+                if (i + 3 < c.ncache) {
+                    *reinterpret_cast<uint4 *>(&s.cache[i]) = make_uint4(k4[0], k4[1], k4[2], k4[3]);
+                } else {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        if (i + q < c.ncache) s.cache[i + q] = k4[q];
+                }
+#pragma unroll
+                for (int q = 0; q < 4; ++q) f(k4[q]);
             }
         }
     }
-    for (int i = i0 + threadIdx.x; i < n; i += kThreads) f(i, f2key(src[i], nan));
+    for (int i = i0 + threadIdx.x; i < c.n; i += kThreads) {
+        const uint32_t key = f2key(c.src[i], nan);
+        if (i < c.ncache) s.cache[i] = key;
+        f(key);
+    }
 }
 
-__device__ __forceinline__ uint32_t key_at(const TopkSmem &s, const float *src, int i, bool cached) {
-    bool nan = false;
-    return cached ? s.cache[i] : f2key(src[i], nan);
+// Calls f(key) for every key of the chunk (order irrelevant).
+template <typename F>
+__device__ __forceinline__ void each_key(const TopkSmem &s, const Chunk &c, F &&f) {
+    const int nc4 = c.ncache & ~3;
+    for (int i = 4 * threadIdx.x; i < nc4; i += 4 * kThreads) {
+        const uint4 k4 = *reinterpret_cast<const uint4 *>(&s.cache[i]);
+        f(k4.x);
+        f(k4.y);
+        f(k4.z);
+        f(k4.w);
+    }
+    for (int i = nc4 + threadIdx.x; i < c.n; i += kThreads) f(c.key(s, i));
+}
+
+// Finds the bin holding the need-th largest key, scanning bins from the top.
+// cl: the counts deciding the selection; s.hist: this CTA's own counts (the
+// same array when the CTA decides alone), left zeroed for the next round.
+// Result in s.sel.
+__device__ void select_bin(TopkSmem &s, const uint32_t *cl, uint32_t need) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int b1 = kBins - 1 - 2 * tid, b0 = b1 - 1;
+    const uint32_t c1 = cl[b1], c0 = cl[b0], l1 = s.hist[b1], l0 = s.hist[b0];
+    const unsigned long long v = (static_cast<unsigned long long>(l1 + l0) << 32) | (c1 + c0);
+    const unsigned long long incl = warp_incl_scan(v, lane);
+    if (lane == 31) s.wsum[warp] = incl;
+    __syncthreads();
+    s.hist[b1] = 0;  // every thread has read its bins
+    s.hist[b0] = 0;
+    const unsigned long long wincl = warp_incl_scan(s.wsum[lane], lane);
+    const unsigned long long wex = warp == 0 ? 0ull : __shfl_sync(0xffffffffu, wincl, (warp + 31) & 31);
+    const unsigned long long above = wex + incl - v;
+    const uint32_t ca = static_cast<uint32_t>(above), la = static_cast<uint32_t>(above >> 32);
+    if (ca < need && need <= ca + c1) {
+        s.sel[0] = b1;
+        s.sel[1] = ca;
+        s.sel[2] = c1;
+        s.sel[3] = la;
+        s.sel[4] = l1;
+    } else if (ca + c1 < need && need <= ca + c1 + c0) {
+        s.sel[0] = b0;
+        s.sel[1] = ca + c1;
+        s.sel[2] = c0;
+        s.sel[3] = la + l1;
+        s.sel[4] = l0;
+    }
+    __syncthreads();
 }
 
 __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const TopkArgs a) {
@@ -154,19 +247,18 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const TopkArgs a) {
     const int ch = ((n + CL - 1) / CL + 3) & ~3;
     const int c0 = min(n, crank * ch);
     const int nloc = min(n, c0 + ch) - c0;
-    const float *src = a.logits + static_cast<int64_t>(row) * a.logits_stride + c0;
-    const bool cached = ch <= kCacheElems;
+    Chunk chunk{a.logits + static_cast<int64_t>(row) * a.logits_stride + c0, nloc, min(nloc, kCacheElems)};
     if (tid == 0) {
         s.bad = 0;
         s.ncand = 0;
     }
+    for (int b = tid; b < kBins; b += kThreads) s.hist[b] = 0;
     __syncthreads();
 
-    // ---- key range of the chunk (and its shared-memory copy)
+    // ---- 1. key range of the chunk (and its shared-memory copy), then of the row
     uint32_t lo = 0xffffffffu, hi = 0u;
-    bool nan = false, ignore = false;
-    for_each_key(s, src, nloc, false, nan, [&](int i, uint32_t key) {
-        if (cached) s.cache[i] = key;
+    bool nan = false;
+    first_pass(s, chunk, nan, [&](uint32_t key) {
         lo = min(lo, key);
         hi = max(hi, key);
     });
@@ -196,171 +288,315 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const TopkArgs a) {
     }
     if (tid == 0 && s.bad) report(a.status, DSA_ERR_RANGE);
     cluster.sync();
-    uint32_t base = 0xffffffffu, top = 0u;
-    for (int r = 0; r < CL; ++r) {
-        const uint32_t *mm = cluster.map_shared_rank(s.mm, r);
-        base = min(base, mm[0]);
-        top = max(top, mm[1]);
+    if (warp == 0) {
+        lo = 0xffffffffu;
+        hi = 0u;
+        if (lane < CL) {
+            const uint32_t *mm = cluster.map_shared_rank(s.mm, lane);
+            lo = mm[0];
+            hi = mm[1];
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+            hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+        }
+        if (lane == 0) {
+            s.range[0] = lo;
+            s.range[1] = hi;
+        }
     }
+    __syncthreads();
+    uint32_t base = s.range[0], top = s.range[1];
     uint32_t need = static_cast<uint32_t>(k);
+    uint32_t my_above = 0;                         // this chunk's keys above [base, top]
+    uint32_t my_in = static_cast<uint32_t>(nloc);  // this chunk's keys inside it
 
-    // ---- refine the key interval [base, top] holding the k-th largest key down to one key.
-    // While the interval's keys are too many to gather, each round histograms every CTA's
-    // chunk and sums the histograms across the cluster.  Once they fit, the keys inside the
-    // interval are gathered into every CTA, which then refines alone (identically).
+    // ---- 2. cluster rounds, until the interval is one key or few enough keys to gather
     bool gathered = false;
     while (top > base) {
         const uint32_t span = top - base;
         const int bits = 32 - __clz(span);            // span < 2^bits
         const int shift = bits > 11 ? bits - 11 : 0;  // (span >> shift) < 2048
-        for (int b = tid; b < kBins; b += kThreads) s.hist[b] = 0;
-        __syncthreads();
-        if (gathered) {
-            const int nc = static_cast<int>(s.ncand_all);
-            for (int i = tid; i < nc; i += kThreads) {
-                const uint32_t key = s.cand_all[i];
-                if (key >= base && key <= top) atomicAdd(&s.hist[(key - base) >> shift], 1u);
+        each_key(s, chunk, [&](uint32_t key) {
+            if (key >= base && key <= top) atomicAdd(&s.hist[(key - base) >> shift], 1u);
+        });
+        const uint32_t *cl_counts = s.hist;
+        if (CL > 1) {
+            cluster.sync();  // every chunk's histogram is complete
+            // reduce-scatter: this CTA sums bin slice `crank` over the cluster, writes it to all
+            const int slice = kBins / CL;
+            if (tid < slice) {
+                const int b = crank * slice + tid;
+                uint32_t v[kMaxCluster];
+#pragma unroll
+                for (int r = 0; r < kMaxCluster; ++r)
+                    if (r < CL) v[r] = ld_peer(peer_addr(&s.hist[b], r));
+                uint32_t sum = 0;
+#pragma unroll
+                for (int r = 0; r < kMaxCluster; ++r)
+                    if (r < CL) sum += v[r];
+#pragma unroll
+                for (int r = 0; r < kMaxCluster; ++r)
+                    if (r < CL) st_peer(peer_addr(&s.hsum[b], r), sum);
             }
+            cluster.sync();  // every CTA holds the cluster histogram
+            cl_counts = s.hsum;
         } else {
-            for_each_key(s, src, nloc, cached, ignore, [&](int, uint32_t key) {
-                if (key >= base && key <= top) atomicAdd(&s.hist[(key - base) >> shift], 1u);
-            });
+            __syncthreads();
         }
-        if (!gathered) cluster.sync();
-        else __syncthreads();
-        // counts of this thread's two bins (2047-2t and 2046-2t), cluster-wide unless gathered
-        const int b1 = kBins - 1 - 2 * tid, b0 = b1 - 1;
-        uint32_t c1 = 0, c0v = 0;
-        if (gathered) {
-            c1 = s.hist[b1];
-            c0v = s.hist[b0];
-        } else {
-            for (int r = 0; r < CL; ++r) {
-                const uint32_t *h = cluster.map_shared_rank(s.hist, r);
-                c1 += h[b1];
-                c0v += h[b0];
-            }
-        }
-        unsigned long long tot;
-        const uint32_t above1 = static_cast<uint32_t>(block_excl_scan(c1 + c0v, s, tot));
-        if (above1 < need && need <= above1 + c1) {
-            s.sel_bin = b1;
-            s.sel_above = above1;
-            s.sel_count = c1;
-        } else if (above1 + c1 < need && need <= above1 + c1 + c0v) {
-            s.sel_bin = b0;
-            s.sel_above = above1 + c1;
-            s.sel_count = c0v;
-        }
-        if (!gathered) cluster.sync();  // every CTA has read every histogram
-        else __syncthreads();
-        const uint32_t sb = s.sel_bin, sa = s.sel_above, sc = s.sel_count;
+        select_bin(s, cl_counts, need);
+        const uint32_t sb = s.sel[0], sa = s.sel[1], sc = s.sel[2];
+        my_above += s.sel[3];
+        my_in = s.sel[4];
         need -= sa;
         const uint32_t nbase = base + (sb << shift);
         const unsigned long long bin_top = static_cast<unsigned long long>(nbase) + (1ull << shift) - 1ull;
         base = nbase;
         top = static_cast<uint32_t>(min(static_cast<unsigned long long>(top), bin_top));
-        if (top > base && !gathered && sc <= static_cast<uint32_t>(kCandCap)) {
-            // the cluster holds sc <= kCandCap keys in [base, top]: collect this chunk's share
-            // (one shared atomic per warp), then gather every CTA's share into every CTA
-            for (int i0 = 0; i0 < nloc; i0 += kThreads) {
-                const int i = i0 + tid;
-                const uint32_t key = i < nloc ? key_at(s, src, i, cached) : 0u;
-                const bool in = i < nloc && key >= base && key <= top;
-                const unsigned m = __ballot_sync(0xffffffffu, in);
+        if (top > base && sc <= static_cast<uint32_t>(kCandCap)) {
+            // publish this chunk's keys inside [base, top] (one shared atomic per warp) and its
+            // count above, then gather every CTA's share in rank order
+            for (int i0 = 0; i0 < nloc; i0 += 4 * kThreads) {
+                const int i = i0 + 4 * tid;
+                uint32_t kq[4];
+                keys4(s, chunk, i, nloc, kq);
+                uint32_t c = 0;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) c += (i + q < nloc && kq[q] >= base && kq[q] <= top) ? 1u : 0u;
+                const uint32_t incl = warp_incl_scan32(c, lane);
+                const uint32_t wtot = __shfl_sync(0xffffffffu, incl, 31);
                 uint32_t wbase = 0;
-                if (lane == 0 && m) wbase = atomicAdd(&s.ncand, static_cast<uint32_t>(__popc(m)));
-                wbase = __shfl_sync(0xffffffffu, wbase, 0);
-                if (in) s.cand[wbase + __popc(m & ((1u << lane) - 1u))] = key;
+                if (lane == 0 && wtot) wbase = atomicAdd(&s.ncand, wtot);
+                uint32_t at = __shfl_sync(0xffffffffu, wbase, 0) + incl - c;
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    if (i + q < nloc && kq[q] >= base && kq[q] <= top) s.cand[at++] = kq[q];
             }
+            if (tid == 0) s.pub[1] = my_above;
+            __syncthreads();
+            if (tid == 0) s.pub[0] = s.ncand;
             cluster.sync();
-            uint32_t off = 0;
-            for (int r = 0; r < CL; ++r) {
-                const TopkSmem *peer = cluster.map_shared_rank(&s, r);
-                const int n_r = static_cast<int>(peer->ncand);
-                for (int i = tid; i < n_r; i += kThreads) s.cand_all[off + i] = peer->cand[i];
-                off += n_r;
+            if (warp == 0) {
+                uint32_t nr = 0, ar = 0;
+                if (lane < CL) {
+                    const uint32_t *pub = cluster.map_shared_rank(s.pub, lane);
+                    nr = pub[0];
+                    ar = pub[1];
+                }
+                const uint32_t incl = warp_incl_scan32(nr, lane);
+                if (lane < CL) s.roff[lane] = incl - nr;
+                if (lane == CL - 1) s.roff[CL] = incl;
+                // selected keys above the interval in the lower-ranked chunks
+                const uint32_t ab = warp_incl_scan32(lane < crank ? ar : 0u, lane);
+                if (lane == 31) s.before[0] = ab;
             }
-            if (tid == 0) s.ncand_all = off;
+            __syncthreads();
+            const uint32_t total = s.roff[CL];
+            constexpr int kPer = kCandCap / kThreads;
+            uint32_t v[kPer];
+#pragma unroll
+            for (int u = 0; u < kPer; ++u) {  // all peer loads in flight before any store
+                const uint32_t j = tid + u * kThreads;
+                if (j < total) {
+                    int r = 0;
+                    while (r + 1 < CL && s.roff[r + 1] <= j) ++r;
+                    v[u] = ld_peer(peer_addr(&s.cand[j - s.roff[r]], r));
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < kPer; ++u)
+                if (tid + u * kThreads < total) s.cand_all[tid + u * kThreads] = v[u];
+            cluster_arrive();  // this CTA reads no peer memory after this point
             gathered = true;
+            __syncthreads();
+            break;
+        }
+    }
+
+    // ---- 3. refine alone on the gathered candidates
+    uint32_t gt_before = 0, eq_before = 0;
+    if (gathered) {
+        const int nc = static_cast<int>(s.roff[CL]);
+        while (top > base) {
+            const uint32_t span = top - base;
+            const int bits = 32 - __clz(span);
+            const int shift = bits > 11 ? bits - 11 : 0;
+            for (int i = tid; i < nc; i += kThreads) {
+                const uint32_t key = s.cand_all[i];
+                if (key >= base && key <= top) atomicAdd(&s.hist[(key - base) >> shift], 1u);
+            }
+            __syncthreads();
+            select_bin(s, s.hist, need);
+            need -= s.sel[1];
+            const uint32_t nbase = base + (s.sel[0] << shift);
+            const unsigned long long bin_top = static_cast<unsigned long long>(nbase) + (1ull << shift) - 1ull;
+            base = nbase;
+            top = static_cast<uint32_t>(min(static_cast<unsigned long long>(top), bin_top));
+        }
+        // the lower-ranked chunks' candidates above / equal to T
+        const uint32_t T = base;
+        const int lower = static_cast<int>(s.roff[crank]);
+        uint32_t g = 0, e = 0;
+        for (int i = tid; i < lower; i += kThreads) {
+            const uint32_t key = s.cand_all[i];
+            g += key > T;
+            e += key == T;
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            g += __shfl_xor_sync(0xffffffffu, g, o);
+            e += __shfl_xor_sync(0xffffffffu, e, o);
+        }
+        if (lane == 0) {
+            s.red[warp] = g;
+            s.red[kWarps + warp] = e;
         }
         __syncthreads();
+        g = s.red[lane];
+        e = s.red[kWarps + lane];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            g += __shfl_xor_sync(0xffffffffu, g, o);
+            e += __shfl_xor_sync(0xffffffffu, e, o);
+        }
+        gt_before = s.before[0] + g;
+        eq_before = e;
+    } else {
+        // the cluster rounds reached one key: publish this chunk's counts, read the lower ranks'
+        if (tid == 0) {
+            s.pub[1] = my_above;
+            s.pub[2] = my_in;
+        }
+        cluster.sync();
+        uint32_t g = 0, e = 0;
+        if (lane < crank) {
+            const uint32_t *pub = cluster.map_shared_rank(s.pub, lane);
+            g = pub[1];
+            e = pub[2];
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            g += __shfl_xor_sync(0xffffffffu, g, o);
+            e += __shfl_xor_sync(0xffffffffu, e, o);
+        }
+        gt_before = g;
+        eq_before = e;
+        cluster_arrive();
     }
     const uint32_t T = base;  // exact threshold key; `need` keys equal to T are taken (lowest positions)
 
-    // ---- ordered compaction.  Warp w owns a contiguous segment of the chunk and walks it
-    // 32 keys at a time (lane order = position order): pass 1 counts keys > T and == T per
-    // warp, pass 2 writes positions.  A warp's offset adds the counts of the lower warps of
-    // this CTA and of the lower-ranked CTAs of the cluster.
-    const int seg = ((nloc + kWarps - 1) / kWarps + 31) & ~31;
+    // ---- 4. ordered compaction.  Warp w owns a contiguous segment of the chunk and walks it
+    // 128 keys at a time, four consecutive keys per lane (lane order = position order):
+    // pass 1 counts keys > T and == T per warp, pass 2 writes positions after the lower
+    // warps' and lower chunks' selections.
+    const int seg = ((nloc + kWarps - 1) / kWarps + 127) & ~127;
     const int w0 = min(nloc, warp * seg), w1 = min(nloc, w0 + seg);
     uint32_t ngt = 0, neq = 0;
-    for (int i0 = w0; i0 < w1; i0 += 32) {
-        const int i = i0 + lane;
-        const uint32_t key = i < w1 ? key_at(s, src, i, cached) : 0u;
-        ngt += __popc(__ballot_sync(0xffffffffu, i < w1 && key > T));
-        neq += __popc(__ballot_sync(0xffffffffu, i < w1 && key == T));
+    for (int i0 = w0; i0 < w1; i0 += 128) {
+        const int i = i0 + 4 * lane;
+        uint32_t kq[4];
+        keys4(s, chunk, i, w1, kq);
+        uint32_t g = 0, e = 0;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            g += (i + q < w1 && kq[q] > T) ? 1u : 0u;
+            e += (i + q < w1 && kq[q] == T) ? 1u : 0u;
+        }
+        ngt += __reduce_add_sync(0xffffffffu, g);
+        neq += __reduce_add_sync(0xffffffffu, e);
     }
     if (lane == 0) {
-        s.wcnt[warp] = ngt;
-        s.wcnt[kWarps + warp] = neq;
+        s.wgt[warp] = ngt;
+        s.weq[warp] = neq;
     }
     __syncthreads();
-    if (tid == 0) {
+    {
+        const uint32_t vg = s.wgt[lane], ve = s.weq[lane];
+        const uint32_t ig = warp_incl_scan32(vg, lane), ie = warp_incl_scan32(ve, lane);
+        gt_before += __shfl_sync(0xffffffffu, ig - vg, warp);
+        eq_before += __shfl_sync(0xffffffffu, ie - ve, warp);
+    }
+    for (int i0 = w0; i0 < w1; i0 += 128) {
+        const int i = i0 + 4 * lane;
+        uint32_t kq[4];
+        keys4(s, chunk, i, w1, kq);
         uint32_t g = 0, e = 0;
-        for (int w = 0; w < kWarps; ++w) {
-            g += s.wcnt[w];
-            e += s.wcnt[kWarps + w];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            g += (i + q < w1 && kq[q] > T) ? 1u : 0u;
+            e += (i + q < w1 && kq[q] == T) ? 1u : 0u;
         }
-        s.cnt[0] = g;
-        s.cnt[1] = e;
+        // counts of >T and ==T packed in one word: at most 128 each per warp step
+        const uint32_t packed = g | (e << 16);
+        const uint32_t incl = warp_incl_scan32(packed, lane);
+        const uint32_t tot = __shfl_sync(0xffffffffu, incl, 31);
+        uint32_t gb = gt_before + ((incl - packed) & 0xffffu), eb = eq_before + ((incl - packed) >> 16);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const bool in = i + q < w1;
+            const bool gt = in && kq[q] > T, eq = in && kq[q] == T;
+            if (gt || (eq && eb < need)) {
+                const uint32_t pos = gb + min(eb, need);
+                if (pos < static_cast<uint32_t>(k)) out[pos] = c0 + i + q;
+                else report(a.status, DSA_ERR_BOUNDS);  // inconsistent counts: never expected
+            }
+            gb += gt ? 1u : 0u;
+            eb += eq ? 1u : 0u;
+        }
+        gt_before += tot & 0xffffu;
+        eq_before += tot >> 16;
     }
-    cluster.sync();
-    uint32_t gt_before = 0, eq_before = 0;
-    for (int r = 0; r < crank; ++r) {
-        const uint32_t *c = cluster.map_shared_rank(s.cnt, r);
-        gt_before += c[0];
-        eq_before += c[1];
-    }
-    for (int w = 0; w < warp; ++w) {
-        gt_before += s.wcnt[w];
-        eq_before += s.wcnt[kWarps + w];
-    }
-    for (int i0 = w0; i0 < w1; i0 += 32) {
-        const int i = i0 + lane;
-        const uint32_t key = i < w1 ? key_at(s, src, i, cached) : 0u;
-        const unsigned mg = __ballot_sync(0xffffffffu, i < w1 && key > T);
-        const unsigned me = __ballot_sync(0xffffffffu, i < w1 && key == T);
-        const unsigned below = (1u << lane) - 1u;
-        const uint32_t g = gt_before + __popc(mg & below), e = eq_before + __popc(me & below);
-        const bool gt = (mg >> lane) & 1u, eq = (me >> lane) & 1u;
-        if (gt || (eq && e < need)) out[g + min(e, need)] = c0 + i;
-        gt_before += __popc(mg);
-        eq_before += __popc(me);
-    }
-    cluster.sync();  // no CTA leaves while a peer may still read its shared memory
+    cluster_wait();  // no CTA leaves while a peer may still read its shared memory
 }
 
-int cluster_size_for(int max_ctx) {
-    int cl = 1;
-    while (cl < kMaxCluster && (max_ctx + cl - 1) / cl > kCacheElems) cl *= 2;
+struct ClusterLimits {
+    int device = -1;
+    int max16 = 0;  // co-resident clusters of 16 (0: not available)
+};
+
+int cluster_size_for(const TopkArgs &a, int sms, int max16) {
+    int cl = 1;  // enough CTAs that a chunk fits the shared-memory copy
+    while (cl < kMaxCluster && (a.max_ctx + cl - 1) / cl > kCacheElems) cl *= 2;
+    int par = 1;  // enough CTAs that the batch covers the SMs, chunks not shorter than kMinChunk
+    while (par < kMaxCluster && 2 * par * a.num_rows <= sms && a.max_ctx / (2 * par) >= kMinChunk) par *= 2;
+    cl = max(cl, par);
+    if (cl == 16 && max16 < a.num_rows) cl = 8;  // clusters of 16 would not all be co-resident
     return cl;
 }
 
 }  // namespace
 
 cudaError_t launch_topk(const TopkArgs &a, cudaStream_t s) {
-    static int configured_device = -1;
+    static ClusterLimits lim;
     int dev = 0;
     cudaGetDevice(&dev);
-    if (configured_device != dev) {
+    if (lim.device != dev) {
         cudaError_t e =
             cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, sizeof(TopkSmem));
         if (e != cudaSuccess) return e;
-        configured_device = dev;
+        e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        int max16 = 0;
+        if (e == cudaSuccess) {
+            cudaLaunchConfig_t probe = {};
+            probe.gridDim = dim3(16);
+            probe.blockDim = dim3(kThreads);
+            probe.dynamicSmemBytes = sizeof(TopkSmem);
+            cudaLaunchAttribute at[1];
+            at[0].id = cudaLaunchAttributeClusterDimension;
+            at[0].val.clusterDim.x = 16;
+            at[0].val.clusterDim.y = 1;
+            at[0].val.clusterDim.z = 1;
+            probe.attrs = at;
+            probe.numAttrs = 1;
+            if (cudaOccupancyMaxActiveClusters(&max16, topk_kernel, &probe) != cudaSuccess) max16 = 0;
+        }
+        cudaGetLastError();  // a refused cluster size only disables it
+        lim.max16 = max16;
+        lim.device = dev;
     }
     if (a.num_rows == 0) return cudaSuccess;
-    const int cl = cluster_size_for(a.max_ctx);
+    const int cl = cluster_size_for(a, device_sm_count(), lim.max16);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(a.num_rows * cl));
     cfg.blockDim = dim3(kThreads);

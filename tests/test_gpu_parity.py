@@ -38,7 +38,7 @@ def _wl(name, ctx, rows=1, group=1, lat=I.LATENT_FP8, heads=96, k=2048, seed=5, 
 
 INDEXER_CASES = {
     "tiny_4k": I.workload("decode_tiny_4k"),
-    "ragged": _wl("ragged", [1, 63, 64, 65, 127, 128, 129, 2047, 2048, 2049, 3000, 5000]),
+    "ragged": _wl("ragged", [1, 63, 64, 65, 127, 128, 129, 193, 255, 256, 257, 2047, 2048, 2049, 3000, 5000]),
     "verify_g4": _wl("verify", [3000, 4100], rows=4, group=4),
     "pairs_g2": _wl("pairs", [700, 1500, 2500], rows=2, group=2),
     "prefill_g8": _wl("prefill", [3000], rows=64, group=8),
@@ -88,8 +88,20 @@ def _topk_cases():
     c = np.zeros((2, 5000), dtype=np.float32)
     c[1, ::3] = -0.0
     cases["all_equal_signed_zero"] = (c, np.array([5000, 5000], dtype=np.int32), 2048)
-    big = (rng.standard_normal((2, 200000)) * 10 + 100).astype(np.float32)  # beyond the shared-memory row cache
+    big = (rng.standard_normal((2, 200000)) * 10 + 100).astype(np.float32)  # several CTAs per row
     cases["long_rows"] = (big, np.array([200000, 150001], dtype=np.int32), 2048)
+    # chunks longer than the shared-memory copy: each CTA re-reads its tail from global memory
+    tail = rng.standard_normal((2, 700000)).astype(np.float32)
+    cases["cached_tail"] = (tail, np.array([700000, 400003], dtype=np.int32), 2048)
+    # more keys equal to the threshold than the candidate list holds: the cluster refines alone
+    # to a single key, every CTA counting its own keys above and equal to it
+    tb = rng.uniform(0.0, 3.0, (3, 100000)).astype(np.float32)
+    tb[0, :20000] = rng.uniform(-1.0, 1.0, 20000)
+    tb[0, rng.choice(20000, 5000, replace=False)] = 2.0
+    tb[1, rng.choice(100000, 8000, replace=False)] = 3.5
+    tb[2, :] = 1.0
+    tb[2, rng.choice(100000, 50, replace=False)] = 9.0
+    cases["ties_beyond_candidates"] = (tb, np.array([20000, 100000, 100000], dtype=np.int32), 2048)
     s = rng.standard_normal((3, 3000)).astype(np.float32)
     cases["small_k"] = (s, np.array([3000, 10, 1], dtype=np.int32), 5)
     w = np.concatenate([np.full((1, 3000), 1e30, np.float32), np.full((1, 3000), -1e30, np.float32)])
