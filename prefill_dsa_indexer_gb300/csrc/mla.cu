@@ -9,8 +9,9 @@
 //
 // Design (GB300):
 //   * one CTA per (row, split of the row's selected tokens); 64-token tiles;
-//   * four gather warps load the tile's latent rows (16-byte vector loads,
-//     two lanes per 32-byte sector), decode them exactly into fp16
+//   * four gather warps load the tile's latent rows (FP8: one token's 512
+//     latent bytes per warp load instruction, so a load touches four
+//     128-byte lines; NVFP4: two lanes per token), decode them exactly into fp16
 //     (cvt e4m3x2 -> f16x2; NVFP4 e2m1 * e4m3 scale is exact in fp16 too) and
 //     store them 128-byte swizzled, so one shared-memory image serves as the
 //     K-major B operand of S and the MN-major A operand of PV;
@@ -116,6 +117,75 @@ struct GatherRegs {
     int32_t slot;
 };
 
+// FP8 latents, gather warp gw (0..3) loads tokens [16 gw, 16 gw + 16) of the tile: each
+// token's 512 latent bytes are one 32-lane x 16-byte row load (four 128-byte lines per
+// instruction), and the 64 RoPE bytes of eight tokens one more.  Lanes 0..15 hold the slots;
+// an unused or rejected slot loads zeros, which decode to a zero row.
+__device__ __forceinline__ void gather_load_fp8(const MlaArgs &a, const int32_t *row_slots, int t0, int n_tok,
+                                                int gw, int lane, GatherRegs &g) {
+    int32_t slot = -1;
+    if (lane < 16) {
+        const int t = t0 + 16 * gw + lane;
+        slot = t < n_tok ? row_slots[t] : -1;
+        if (slot >= 0 && static_cast<int64_t>(slot) >= a.num_pages * DSA_PAGE_SIZE) {
+            report(a.status, DSA_ERR_BOUNDS);
+            slot = -1;
+        }
+    }
+    g.slot = slot;
+    const int4 z = make_int4(0, 0, 0, 0);
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+        const int32_t sj = __shfl_sync(0xffffffffu, slot, j);
+        g.v[j] = sj >= 0 ? ldg_nc_v4(a.pool + static_cast<int64_t>(sj) * DSA_LATENT_DIM + lane * 16) : z;
+    }
+#pragma unroll
+    for (int b = 0; b < 2; ++b) {
+        const int32_t sj = __shfl_sync(0xffffffffu, slot, 8 * b + (lane >> 2));
+        g.v[16 + b] = sj >= 0 ? ldg_nc_v4(a.pool + static_cast<int64_t>(sj) * DSA_LATENT_DIM + DSA_VALUE_DIM +
+                                          (lane & 3) * 16)
+                              : z;
+    }
+}
+
+__device__ __forceinline__ void e4m3x16_to_f16(const int4 v, int4 &o0, int4 &o1) {
+    const uint32_t w[4] = {static_cast<uint32_t>(v.x), static_cast<uint32_t>(v.y), static_cast<uint32_t>(v.z),
+                           static_cast<uint32_t>(v.w)};
+    o0.x = cvt_e4m3x2_f16x2(w[0] & 0xffffu);
+    o0.y = cvt_e4m3x2_f16x2(w[0] >> 16);
+    o0.z = cvt_e4m3x2_f16x2(w[1] & 0xffffu);
+    o0.w = cvt_e4m3x2_f16x2(w[1] >> 16);
+    o1.x = cvt_e4m3x2_f16x2(w[2] & 0xffffu);
+    o1.y = cvt_e4m3x2_f16x2(w[2] >> 16);
+    o1.z = cvt_e4m3x2_f16x2(w[3] & 0xffffu);
+    o1.w = cvt_e4m3x2_f16x2(w[3] >> 16);
+}
+
+// Lane l's 16 latent dims [16 l, 16 l + 16) of token j go to 64-dim block l / 4, 16-byte units
+// 2 (l % 4) and 2 (l % 4) + 1 of the token's 128-byte row; RoPE lanes fill block 8.
+__device__ __forceinline__ void gather_store_fp8(uint8_t *kv, int gw, int lane, const GatherRegs &g) {
+    const int c = lane >> 2, u = 2 * (lane & 3);
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+        const int t = 16 * gw + j;
+        int4 o0, o1;
+        e4m3x16_to_f16(g.v[j], o0, o1);
+        uint8_t *base = kv + c * (kTok * 128);
+        *reinterpret_cast<int4 *>(base + sw128(t, u)) = o0;
+        *reinterpret_cast<int4 *>(base + sw128(t, u + 1)) = o1;
+    }
+#pragma unroll
+    for (int b = 0; b < 2; ++b) {
+        const int t = 16 * gw + 8 * b + (lane >> 2);
+        int4 o0, o1;
+        e4m3x16_to_f16(g.v[16 + b], o0, o1);
+        uint8_t *base = kv + 8 * (kTok * 128);
+        *reinterpret_cast<int4 *>(base + sw128(t, u)) = o0;
+        *reinterpret_cast<int4 *>(base + sw128(t, u + 1)) = o1;
+    }
+}
+
+// NVFP4 latents: two lanes per token (lanes 2t, 2t+1 of the gather warps hold token t).
 template <int FMT>
 __device__ __forceinline__ void gather_load(const MlaArgs &a, const int32_t *row_slots, int t0, int n_tok,
                                             int gtid, GatherRegs &g) {
@@ -287,7 +357,10 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const MlaArgs a
     // ---- gather warps start tile 0's latent loads; the other warps convert Q meanwhile
     GatherRegs g;
     const int gtid = tid - 256;  // 0..127 in the gather warps
-    if (warp >= 8 && n_tiles > 0) gather_load<FMT>(a, row_slots, 0, n_tok, gtid, g);
+    if (warp >= 8 && n_tiles > 0) {
+        if (FMT == DSA_LATENT_FP8) gather_load_fp8(a, row_slots, 0, n_tok, warp - 8, lane, g);
+        else gather_load<FMT>(a, row_slots, 0, n_tok, gtid, g);
+    }
     // ---- Q: fp16, 128-byte swizzled K-major, block c (64 dims) at c * H * 128.  Decode
     // copies the image the prep kernel made for this row; prefill converts from bf16 here,
     // issuing all loads of a batch before any conversion.
@@ -508,17 +581,25 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const MlaArgs a
                     ok = false;
                     break;
                 }
-                gather_store<FMT>(kv, gtid, g);
-                const unsigned long long vm = __ballot_sync(0xffffffffu, g.slot >= 0);
-                // lanes 2t, 2t+1 hold token t of this warp's 16 tokens: keep even lanes' bits
                 unsigned long long tok = 0;
+                const unsigned long long vm = __ballot_sync(0xffffffffu, g.slot >= 0);
+                if (FMT == DSA_LATENT_FP8) {
+                    gather_store_fp8(kv, quad, lane, g);
+                    tok = vm & 0xffffull;  // lanes 0..15 hold this warp's 16 tokens
+                } else {
+                    gather_store<FMT>(kv, gtid, g);
+                    // lanes 2t, 2t+1 hold token t of this warp's 16 tokens: keep even lanes' bits
 #pragma unroll
-                for (int b = 0; b < 16; ++b) tok |= ((vm >> (2 * b)) & 1ull) << b;
+                    for (int b = 0; b < 16; ++b) tok |= ((vm >> (2 * b)) & 1ull) << b;
+                }
                 if (lane == 0) reinterpret_cast<unsigned short *>(mask)[quad] = static_cast<unsigned short>(tok);
                 fence_async_smem();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(kv_full);
-                if (i + 1 < n_tiles) gather_load<FMT>(a, row_slots, (i + 1) * kTok, n_tok, gtid, g);
+                if (i + 1 < n_tiles) {
+                    if (FMT == DSA_LATENT_FP8) gather_load_fp8(a, row_slots, (i + 1) * kTok, n_tok, quad, lane, g);
+                    else gather_load<FMT>(a, row_slots, (i + 1) * kTok, n_tok, gtid, g);
+                }
             }
         }
         // ---------------------------------------------------------------- epilogue, 8 warps:
@@ -526,12 +607,16 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const MlaArgs a
         // lane = dim, one store instruction writes 32 consecutive dims of one head
         if (ok && n_tiles > 0) ok = mbar_wait_warp(pv_done, (n_tiles - 1) & 1, abort, a.status);
         if (ok) ok = mbar_wait_warp(stats, 0, abort, a.status);
+        // A split's part is written as fp16: neighbouring lanes (dims d, d + 1) swap one value
+        // so that each lane stores a 4-byte pair of dims of one head (two heads per step).
+        // The direct output is written as fp32 rows.
         if (ok) {
             tc_fence_after();
+            const bool to_part = a.splits > 1;
             float *dst = a.out + static_cast<int64_t>(row) * H * DSA_VALUE_DIM;
             __half *dst_h = reinterpret_cast<__half *>(a.part_o) +
                             (static_cast<int64_t>(row) * a.splits + split) * H * DSA_VALUE_DIM;
-            const bool to_part = a.splits > 1;
+            const bool odd = (lane & 1) != 0;
             const int j0 = is_softmax ? 0 : 2;
             for (int j = j0; j < j0 + 2; ++j) {
                 const int d = 128 * j + 32 * quad + lane;
@@ -544,13 +629,37 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const MlaArgs a
                         else tmem_ld16(tb + c, *reinterpret_cast<uint32_t(*)[16]>(v));
                         tmem_ld_wait();
                     }
+                    // the 32 heads' factors into registers first: the stores below may alias
+                    // inv_l as far as the compiler knows, which would serialise every element
+                    float il[32];
 #pragma unroll
-                    for (int x = 0; x < 32; ++x) {
-                        if (x >= 16 && !full32) break;
-                        const float o = (n_tiles > 0) ? __uint_as_float(v[x]) * inv_l[c + x] : 0.f;
-                        const int64_t at = static_cast<int64_t>(c + x) * DSA_VALUE_DIM + d;
-                        if (to_part) dst_h[at] = __float2half_rn(o);
-                        else dst[at] = o;
+                    for (int x = 0; x < 32; x += 4) {
+                        const float4 f = (x < 16 || full32) ? *reinterpret_cast<const float4 *>(inv_l + c + x)
+                                                            : make_float4(0.f, 0.f, 0.f, 0.f);
+                        il[x] = f.x;
+                        il[x + 1] = f.y;
+                        il[x + 2] = f.z;
+                        il[x + 3] = f.w;
+                    }
+                    if (to_part) {
+#pragma unroll
+                        for (int x = 0; x < 32; x += 2) {
+                            if (x >= 16 && !full32) break;
+                            const float o0 = (n_tiles > 0) ? __uint_as_float(v[x]) * il[x] : 0.f;
+                            const float o1 = (n_tiles > 0) ? __uint_as_float(v[x + 1]) * il[x + 1] : 0.f;
+                            const float got = __shfl_xor_sync(0xffffffffu, odd ? o0 : o1, 1);
+                            // even lane: head c+x, dims (d, d+1); odd lane: head c+x+1, dims (d-1, d)
+                            const __half2 hh = odd ? __floats2half2_rn(got, o1) : __floats2half2_rn(o0, got);
+                            const int at = (c + x + (odd ? 1 : 0)) * DSA_VALUE_DIM + (d & ~1);
+                            *reinterpret_cast<__half2 *>(dst_h + at) = hh;
+                        }
+                    } else {
+#pragma unroll
+                        for (int x = 0; x < 32; ++x) {
+                            if (x >= 16 && !full32) break;
+                            const float o = (n_tiles > 0) ? __uint_as_float(v[x]) * il[x] : 0.f;
+                            dst[(c + x) * DSA_VALUE_DIM + d] = o;
+                        }
                     }
                 }
             }
