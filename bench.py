@@ -428,7 +428,8 @@ def main():
     if os.path.exists(tfile):
         with open(tfile) as f:
             traffic = json.load(f).get(wl.name)
-    launches_per_step = 5 if not prefill else 4  # indexer, top-k, slots, MLA (+ split merge in decode)
+    # indexer, top-k, page->slot, sparse MLA; decode with split rows adds the query prep and the merge
+    launches_per_step = 4 + (2 if (not prefill and P.sparse_mla_workspace_size(wl.num_rows, wl.heads, wl.k) > 0) else 0)
 
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,

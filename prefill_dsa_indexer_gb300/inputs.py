@@ -102,11 +102,13 @@ def workload(name: str) -> Workload:
         return Workload(name, [131072] * 8, 1, 1, seed=1003)
     if name == "prefill_8k_on_56k":
         return Workload(name, [65536], 8192, 8, seed=1004)
+    if name == "prefill_1k_on_15k":  # the prefill shape at an eighth of the rows (profiling size)
+        return Workload(name, [16384], 1024, 8, seed=1005)
     raise KeyError(name)
 
 
 WORKLOADS = ("decode_tiny_4k", "decode_b32_16k_64k", "verify_b4_256k", "verify_b1_1m",
-             "decode_b8_128k_fp4", "decode_b8_128k_fp8", "prefill_8k_on_56k")
+             "decode_b8_128k_fp4", "decode_b8_128k_fp8", "prefill_8k_on_56k", "prefill_1k_on_15k")
 
 
 @dataclass
