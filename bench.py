@@ -301,45 +301,79 @@ def main():
     for L in layers:
         P.check_status(L.status, "warm-up")
 
-    # One step per cache copy captured as two CUDA graphs (the indexer, then top-k, slots
-    # and sparse MLA), so host launch overhead stays out of the step and the indexer's
-    # own time can be bracketed by events between the two replays.
-    graphs = []
+    # Runs of consecutive steps (cycling the cache copies, as a captured multi-layer forward
+    # would) are captured as one CUDA graph each, with event-record nodes around every indexer
+    # launch: the indexer's time is then read on the device, free of host and graph-launch
+    # latency.  Without event-record nodes (older torch) each step is two graphs with stream
+    # events between them.
+    def ext_event():
+        return torch.cuda.Event(enable_timing=True, external=True)
+
+    def rest_of_step(L, s=None):
+        P.topk(L.logits, inp.row_ctx, L.max_ctx, L.k, out=L.idx, status=L.status, stream=s)
+        P.page_to_slot(L.block_table, inp.row_req, inp.row_ctx, L.max_ctx, L.lat_pool.shape[0], L.idx, out=L.slots,
+                       status=L.status, stream=s)
+        if L.prefill:
+            P.sparse_mla_prefill(L.lat_pool, L.lat_fmt, L.tensor_scale, inp.q_mla, L.slots, L.sm_scale, out=L.out,
+                                 lse=L.lse, status=L.status, stream=s)
+        else:
+            P.sparse_mla_decode(L.lat_pool, L.lat_fmt, L.tensor_scale, inp.q_mla, L.slots, L.sm_scale, out=L.out,
+                                lse=L.lse, workspace=L.workspace, status=L.status, stream=s)
+
+    def indexer(L, s=None):
+        P.indexer_logits(L.idx_pool, L.key_fmt, L.block_table, inp.row_req, inp.row_ctx, L.max_ctx, inp.q_idx,
+                         inp.head_w, L.rows_per_group, logits=L.logits, status=L.status, stream=s)
+
+    graph_mode = "eager"
+    runs = []  # (graph, [(event before, event after) per step])
     if not args.no_graph:
         cap = torch.cuda.Stream()
         cap.wait_stream(stream)
-        for c in range(len(layers)):
-            g_idx, g_rest = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+        per_graph = 16 * len(layers)
+        try:
+            ext_event()
+            graph_mode = "multi-step"
+        except TypeError:
+            graph_mode = "two-graphs"
+
+        def capture(n):
+            g = torch.cuda.CUDAGraph()
+            evp = [(ext_event(), ext_event()) for _ in range(n)]
             with torch.cuda.stream(cap):
-                L = layers[c]
-                with torch.cuda.graph(g_idx, stream=cap):
-                    P.indexer_logits(L.idx_pool, L.key_fmt, L.block_table, inp.row_req, inp.row_ctx, L.max_ctx,
-                                     inp.q_idx, inp.head_w, L.rows_per_group, logits=L.logits, status=L.status)
-                with torch.cuda.graph(g_rest, stream=cap):
-                    P.topk(L.logits, inp.row_ctx, L.max_ctx, L.k, out=L.idx, status=L.status)
-                    P.page_to_slot(L.block_table, inp.row_req, inp.row_ctx, L.max_ctx, L.lat_pool.shape[0], L.idx,
-                                   out=L.slots, status=L.status)
-                    if L.prefill:
-                        P.sparse_mla_prefill(L.lat_pool, L.lat_fmt, L.tensor_scale, inp.q_mla, L.slots, L.sm_scale,
-                                             out=L.out, lse=L.lse, status=L.status)
-                    else:
-                        P.sparse_mla_decode(L.lat_pool, L.lat_fmt, L.tensor_scale, inp.q_mla, L.slots, L.sm_scale,
-                                            out=L.out, lse=L.lse, workspace=L.workspace, status=L.status)
-            graphs.append((g_idx, g_rest))
+                with torch.cuda.graph(g, stream=cap):
+                    for k in range(n):
+                        L = layers[k % len(layers)]
+                        evp[k][0].record(cap)
+                        indexer(L)
+                        evp[k][1].record(cap)
+                        rest_of_step(L)
+            return g, evp
+
+        if graph_mode == "multi-step":
+            full, tail = divmod(args.steps, per_graph)
+            if full:
+                runs.append((capture(per_graph), full))
+            if tail:
+                runs.append((capture(tail), 1))
+        else:
+            pairs = []
+            for c in range(len(layers)):
+                g_idx, g_rest = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+                with torch.cuda.stream(cap):
+                    with torch.cuda.graph(g_idx, stream=cap):
+                        indexer(layers[c])
+                    with torch.cuda.graph(g_rest, stream=cap):
+                        rest_of_step(layers[c])
+                pairs.append((g_idx, g_rest))
         stream.wait_stream(cap)
         torch.cuda.synchronize()
-
-        def step(i, ev=None):  # noqa: F811  (graph replay of the same work)
-            g_idx, g_rest = graphs[i % len(graphs)]
-            if ev is not None:
-                ev[0].record(stream)
-            g_idx.replay()
-            if ev is not None:
-                ev[1].record(stream)
-            g_rest.replay()
-
-        for i in range(args.warmup):
-            step(i)
+        for (g, _), _n in runs:  # graph warm-up: one replay of each run
+            g.replay()
+        if graph_mode == "two-graphs":
+            for i in range(args.warmup):
+                g_idx, g_rest = pairs[i % len(pairs)]
+                g_idx.replay()
+                g_rest.replay()
         torch.cuda.synchronize()
 
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
@@ -351,15 +385,32 @@ def main():
         clk.wait_first()
         h0 = time.time()
         t_start.record(stream)
-        for i in range(args.steps):
-            step(i, evs[i])
+        if graph_mode == "multi-step":
+            for (g, _), reps in runs:
+                for _r in range(reps):
+                    g.replay()
+        elif graph_mode == "two-graphs":
+            for i in range(args.steps):
+                g_idx, g_rest = pairs[i % len(pairs)]
+                evs[i][0].record(stream)
+                g_idx.replay()
+                evs[i][1].record(stream)
+                g_rest.replay()
+        else:
+            for i in range(args.steps):
+                step(i, evs[i])
         t_stop.record(stream)
         torch.cuda.synchronize()
         h1 = time.time()
     if dist is not None:
         dist.barrier()
     total_ms = t_start.elapsed_time(t_stop)
-    idx_ms = sum(a.elapsed_time(b) for a, b in evs) / args.steps
+    if graph_mode == "multi-step":
+        # every step of each run's last replay (the final 16 x copies steps of the timed loop)
+        samples = [a.elapsed_time(b) for (g, evp), _r in runs for a, b in evp]
+    else:
+        samples = [a.elapsed_time(b) for a, b in evs]
+    idx_ms = sum(samples) / len(samples)
     for L in layers:
         P.check_status(L.status, "timed steps")
     if dist is not None:
@@ -447,7 +498,10 @@ def main():
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e2e_ms / args.steps},
         "gpu_launches": launches_per_step * args.steps,
-        "launch": "cuda-graph replay (indexer graph + rest-of-step graph)" if graphs else "eager",
+        "launch": {"multi-step": f"CUDA graphs of {16 * copies} consecutive steps; indexer timed by event nodes "
+                                 f"inside the graph ({len(samples)} launches sampled)",
+                   "two-graphs": "CUDA-graph replay (indexer graph + rest-of-step graph), stream events between",
+                   "eager": "eager launches, stream events around the indexer"}[graph_mode],
         "clocks": clk.summary(h0, h1),
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -161,6 +161,7 @@ __global__ void __launch_bounds__(IdxCfg<G>::kThreads, 1)
                 prefetch_tensormap(&key_map);
                 prefetch_tensormap(&q_map);
             }
+            const uint64_t stream_policy = l2_evict_first_policy();
             TileWalker wk{prefix, 0};
             wk.seek(w_begin, ng);
             int cur = -1, gc = -1;
@@ -236,11 +237,12 @@ __global__ void __launch_bounds__(IdxCfg<G>::kThreads, 1)
 #pragma unroll
                         for (int p = 0; p < PPT; ++p) {
                             if (p >= npages) break;
-                            tma_load_2d(keys + stage * C::kKeyBytes + p * (DSA_PAGE_SIZE * 128), &key_map,
-                                        &full[stage], 0, pj[p] * kIdxPageRows);
-                            bulk_load(scales + stage * C::kTileKeys + p * DSA_PAGE_SIZE,
-                                      a.pool + static_cast<int64_t>(pj[p]) * kIdxPageBytes + DSA_PAGE_SIZE * 128,
-                                      DSA_PAGE_SIZE * 4, &full[stage]);
+                            // keys are read once per launch: evict them first, keep the rest of L2
+                            tma_load_2d_hint(keys + stage * C::kKeyBytes + p * (DSA_PAGE_SIZE * 128), &key_map,
+                                             &full[stage], 0, pj[p] * kIdxPageRows, stream_policy);
+                            bulk_load_hint(scales + stage * C::kTileKeys + p * DSA_PAGE_SIZE,
+                                           a.pool + static_cast<int64_t>(pj[p]) * kIdxPageBytes + DSA_PAGE_SIZE * 128,
+                                           DSA_PAGE_SIZE * 4, &full[stage], stream_policy);
                         }
                     }
                     __syncwarp();

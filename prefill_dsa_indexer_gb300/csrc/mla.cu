@@ -713,6 +713,12 @@ __global__ void __launch_bounds__(128) mla_combine_kernel(const MlaArgs a) {
     const float inv = wsum > 0.f ? o_scale / wsum : 0.f;
     reinterpret_cast<float4 *>(a.out + (static_cast<int64_t>(row) * H + h) * DSA_VALUE_DIM)[threadIdx.x] =
         make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+    // The partials are workspace scratch, dead once read: drop their L2 lines unwritten
+    // (S x 8 lines of 128 B for this head) so they cost no HBM write-back.
+    __syncthreads();
+    if (threadIdx.x < S * 8)
+        l2_discard_line(a.part_o + ((static_cast<int64_t>(row) * S + (threadIdx.x >> 3)) * H + h) * DSA_VALUE_DIM +
+                        (threadIdx.x & 7) * 64);
     if (threadIdx.x == 0 && a.lse)
         a.lse[static_cast<int64_t>(row) * H + h] = wsum > 0.f ? (M + log2f(wsum)) * 0.6931471805599453f : -INFINITY;
 }
