@@ -240,6 +240,8 @@ def main():
     ap.add_argument("--workload", default="decode_b8_128k_fp8")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="launch kernels one by one instead of graph replays")
+    ap.add_argument("--single-pass", action="store_true",
+                    help="scorer builds each row's logit histogram and the top-k starts from it")
     args = ap.parse_args()
     assert args.warmup >= 3 or args.impl == "reference", "at least 3 warm-up steps"
 
@@ -274,26 +276,18 @@ def main():
         idx_pool = inp.idx_pool if c == 0 else inp.idx_pool.clone()
         lat_pool = inp.lat_pool if c == 0 else inp.lat_pool.clone()
         layers.append(P.Layer(idx_pool, wl.key_fmt, lat_pool, wl.lat_fmt, inp.tensor_scale, inp.block_table,
-                              inp.max_ctx, wl.num_rows, wl.heads, wl.k, wl.rows_per_group, prefill=prefill))
+                              inp.max_ctx, wl.num_rows, wl.heads, wl.k, wl.rows_per_group, prefill=prefill,
+                              single_pass=args.single_pass))
     stream = torch.cuda.current_stream()
 
     def step(i, ev=None):
         L = layers[i % len(layers)]
         if ev is not None:
             ev[0].record(stream)
-        P.indexer_logits(L.idx_pool, L.key_fmt, L.block_table, inp.row_req, inp.row_ctx, L.max_ctx, inp.q_idx,
-                         inp.head_w, L.rows_per_group, logits=L.logits, status=L.status, stream=stream)
+        L.score(inp.row_req, inp.row_ctx, inp.q_idx, inp.head_w, stream=stream)
         if ev is not None:
             ev[1].record(stream)
-        P.topk(L.logits, inp.row_ctx, L.max_ctx, L.k, out=L.idx, status=L.status, stream=stream)
-        P.page_to_slot(L.block_table, inp.row_req, inp.row_ctx, L.max_ctx, L.lat_pool.shape[0], L.idx, out=L.slots,
-                       status=L.status, stream=stream)
-        if L.prefill:
-            P.sparse_mla_prefill(L.lat_pool, L.lat_fmt, L.tensor_scale, inp.q_mla, L.slots, L.sm_scale, out=L.out,
-                                 lse=L.lse, status=L.status, stream=stream)
-        else:
-            P.sparse_mla_decode(L.lat_pool, L.lat_fmt, L.tensor_scale, inp.q_mla, L.slots, L.sm_scale, out=L.out,
-                                lse=L.lse, workspace=L.workspace, status=L.status, stream=stream)
+        L.select(inp.row_req, inp.row_ctx, inp.q_mla, stream=stream)
 
     for i in range(args.warmup):
         step(i)
@@ -309,20 +303,11 @@ def main():
     def ext_event():
         return torch.cuda.Event(enable_timing=True, external=True)
 
-    def rest_of_step(L, s=None):
-        P.topk(L.logits, inp.row_ctx, L.max_ctx, L.k, out=L.idx, status=L.status, stream=s)
-        P.page_to_slot(L.block_table, inp.row_req, inp.row_ctx, L.max_ctx, L.lat_pool.shape[0], L.idx, out=L.slots,
-                       status=L.status, stream=s)
-        if L.prefill:
-            P.sparse_mla_prefill(L.lat_pool, L.lat_fmt, L.tensor_scale, inp.q_mla, L.slots, L.sm_scale, out=L.out,
-                                 lse=L.lse, status=L.status, stream=s)
-        else:
-            P.sparse_mla_decode(L.lat_pool, L.lat_fmt, L.tensor_scale, inp.q_mla, L.slots, L.sm_scale, out=L.out,
-                                lse=L.lse, workspace=L.workspace, status=L.status, stream=s)
+    def rest_of_step(L, s=None):  # top-k (from the scorer's histogram), page -> slot, sparse MLA
+        L.select(inp.row_req, inp.row_ctx, inp.q_mla, stream=s)
 
-    def indexer(L, s=None):
-        P.indexer_logits(L.idx_pool, L.key_fmt, L.block_table, inp.row_req, inp.row_ctx, L.max_ctx, inp.q_idx,
-                         inp.head_w, L.rows_per_group, logits=L.logits, status=L.status, stream=s)
+    def indexer(L, s=None):  # scorer: logits and their per-row histogram
+        L.score(inp.row_req, inp.row_ctx, inp.q_idx, inp.head_w, stream=s)
 
     graph_mode = "eager"
     runs = []  # (graph, [(event before, event after) per step])
@@ -489,6 +474,7 @@ def main():
         "config": {"workload": wl.name, "batch": len(wl.ctx), "rows": wl.num_rows, "ctx": wl.ctx[0], "k": wl.k,
                    "heads": wl.heads, "index_heads": 32, "page": 64, "key_bytes": idx_tok, "latent_bytes": lat_tok,
                    "parallelism": f"replicas{world}" if world > 1 else "single-gpu",
+                   "topk": "single pass (scorer histogram)" if args.single_pass else "cluster radix select",
                    "l2": f"inputs > L2: {copies} rotating copies of the caches "
                          f"({(inp.idx_pool.numel() + inp.lat_pool.numel()) * copies / 1e9:.2f} GB)"},
         "layer_hbm_gbs": layer_bytes / (ms_per_step / 1000.0) / 1e9,

@@ -142,6 +142,44 @@ int dsa_topk(const float *logits, int64_t logits_stride, const int32_t *row_ctx,
              int32_t max_ctx, int32_t k, int32_t *idx_out, int32_t *dev_status, void *stream);
 
 /*
+ * Single-pass scorer + top-k (blog section "Low-latency decode: fused DSA
+ * decode path": the scorer feeds a batch-invariant exact top-k; here the
+ * scorer's epilogue also builds the histogram the selection starts from).
+ *
+ * DSA_HIST_BINS bins per row of the top 16 bits of each logit's
+ * order-preserving 32-bit key (larger float, larger key; -0 folds onto +0).
+ *
+ * dsa_indexer_logits_hist: dsa_indexer_logits, and for every logit it writes
+ *   hist[r * DSA_HIST_BINS + (key(logit) >> 16)] += 1.
+ *   hist: [num_rows, DSA_HIST_BINS] uint32, device, all zero on entry.
+ *
+ * dsa_topk_hist: dsa_topk (same arguments and result), starting from that
+ *   histogram: the bin holding the k-th key is read off it, one pass over the
+ *   logits collects that bin's keys, and the selection finishes on those.
+ *   hist must be the histogram dsa_indexer_logits_hist produced for exactly
+ *   these logits and row_ctx (otherwise the result is undefined); the call
+ *   leaves it all zero, ready for the next scorer call.  A bin holding more
+ *   keys than the candidate list falls back to refinement rounds.
+ *
+ * dsa_indexer_topk: both calls in one, with the logits and the histogram in
+ *   a workspace of dsa_indexer_topk_workspace_size() bytes (device, 256-byte
+ *   aligned) that must be all zero before the first call; every call leaves
+ *   its histogram part zero again, and the logits part holds no defined
+ *   contents afterwards (their L2 lines are dropped once read, so they cost no
+ *   HBM write-back).
+ */
+#define DSA_HIST_BINS 65536
+int dsa_indexer_logits_hist(const dsa_cache *index_cache, const dsa_rows *rows, const uint8_t *q_idx,
+                            const float *head_w, float *logits, int64_t logits_stride, uint32_t *hist,
+                            int32_t *dev_status, void *stream);
+int dsa_topk_hist(const float *logits, int64_t logits_stride, const int32_t *row_ctx, int32_t num_rows,
+                  int32_t max_ctx, int32_t k, uint32_t *hist, int32_t *idx_out, int32_t *dev_status, void *stream);
+int dsa_indexer_topk(const dsa_cache *index_cache, const dsa_rows *rows, const uint8_t *q_idx, const float *head_w,
+                     int32_t k, int32_t *idx_out, int32_t *dev_status, void *workspace, size_t workspace_bytes,
+                     void *stream);
+size_t dsa_indexer_topk_workspace_size(int32_t num_rows, int32_t max_ctx);
+
+/*
  * Page -> slot translation (blog section "One KV cache, three states": the
  * block table and cache slots are translated to kernel page addresses
  * before each step):

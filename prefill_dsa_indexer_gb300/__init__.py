@@ -79,6 +79,15 @@ def load_library(path: str | None = None):
     lib.dsa_cache_insert.argtypes = [ctypes.POINTER(_Cache), ctypes.POINTER(_Cache), P, I32, P, P, P, P]
     lib.dsa_sparse_mla_workspace_size.restype = ctypes.c_size_t
     lib.dsa_sparse_mla_workspace_size.argtypes = [I32, I32, I32]
+    lib.dsa_indexer_logits_hist.restype = ctypes.c_int
+    lib.dsa_indexer_logits_hist.argtypes = [ctypes.POINTER(_Cache), ctypes.POINTER(_Rows), P, P, P, I64, P, P, P]
+    lib.dsa_topk_hist.restype = ctypes.c_int
+    lib.dsa_topk_hist.argtypes = [P, I64, P, I32, I32, I32, P, P, P, P]
+    lib.dsa_indexer_topk.restype = ctypes.c_int
+    lib.dsa_indexer_topk.argtypes = [ctypes.POINTER(_Cache), ctypes.POINTER(_Rows), P, P, I32, P, P, P,
+                                     ctypes.c_size_t, P]
+    lib.dsa_indexer_topk_workspace_size.restype = ctypes.c_size_t
+    lib.dsa_indexer_topk_workspace_size.argtypes = [I32, I32]
     if path is None:
         _lib = lib
     return lib
@@ -86,7 +95,9 @@ def load_library(path: str | None = None):
 
 EXPORTED = ("dsa_version", "dsa_status_string", "dsa_indexer_logits", "dsa_topk", "dsa_page_to_slot",
             "dsa_sparse_mla_decode", "dsa_sparse_mla_prefill", "dsa_sparse_mla_workspace_size",
-            "dsa_sparse_mla_decode_noalloc", "dsa_cache_insert")
+            "dsa_sparse_mla_decode_noalloc", "dsa_cache_insert", "dsa_indexer_logits_hist", "dsa_topk_hist",
+            "dsa_indexer_topk", "dsa_indexer_topk_workspace_size")
+HIST_BINS = 65536
 NOALLOC_MAX_ROWS = 8
 
 
@@ -152,6 +163,54 @@ def topk(logits, row_ctx, max_ctx, k=2048, out=None, status=None, stream=None):
     rc = load_library().dsa_topk(_ptr(logits), logits.stride(0), _ptr(row_ctx), R, int(max_ctx), int(k), _ptr(out),
                                  _ptr(status), _stream(stream))
     _check(rc, "dsa_topk")
+    return out
+
+
+def new_hist(num_rows: int, device=None) -> torch.Tensor:
+    """A zeroed per-row histogram for indexer_logits_hist / topk_hist (uint32 bits in int32)."""
+    return torch.zeros((num_rows, HIST_BINS), dtype=torch.int32, device=device or "cuda")
+
+
+def indexer_logits_hist(index_pool, key_fmt, block_table, row_req, row_ctx, max_ctx, q_idx, head_w, hist,
+                        rows_per_group=1, logits=None, status=None, stream=None):
+    """dsa_indexer_logits_hist: indexer_logits that also adds every logit to the zeroed histogram `hist`."""
+    R = row_ctx.shape[0]
+    if logits is None:
+        logits = torch.empty((R, max(int(max_ctx), 1)), dtype=torch.float32, device=q_idx.device)
+    c, r = _cache(index_pool, key_fmt), _rows(block_table, row_req, row_ctx, max_ctx, rows_per_group)
+    rc = load_library().dsa_indexer_logits_hist(ctypes.byref(c), ctypes.byref(r), _ptr(q_idx), _ptr(head_w),
+                                                _ptr(logits), logits.stride(0), _ptr(hist), _ptr(status),
+                                                _stream(stream))
+    _check(rc, "dsa_indexer_logits_hist")
+    return logits
+
+
+def topk_hist(logits, row_ctx, max_ctx, hist, k=2048, out=None, status=None, stream=None):
+    """dsa_topk_hist: topk starting from the scorer's histogram of these logits (left zeroed)."""
+    R = row_ctx.shape[0]
+    if out is None:
+        out = torch.empty((R, k), dtype=torch.int32, device=logits.device)
+    rc = load_library().dsa_topk_hist(_ptr(logits), logits.stride(0), _ptr(row_ctx), R, int(max_ctx), int(k),
+                                      _ptr(hist), _ptr(out), _ptr(status), _stream(stream))
+    _check(rc, "dsa_topk_hist")
+    return out
+
+
+def indexer_topk_workspace_size(num_rows: int, max_ctx: int) -> int:
+    return int(load_library().dsa_indexer_topk_workspace_size(int(num_rows), int(max_ctx)))
+
+
+def indexer_topk(index_pool, key_fmt, block_table, row_req, row_ctx, max_ctx, q_idx, head_w, workspace, k=2048,
+                 rows_per_group=1, out=None, status=None, stream=None):
+    """dsa_indexer_topk: scorer + top-k in one call; `workspace` (uint8, zeroed before its first use)."""
+    R = row_ctx.shape[0]
+    if out is None:
+        out = torch.empty((R, k), dtype=torch.int32, device=q_idx.device)
+    c, r = _cache(index_pool, key_fmt), _rows(block_table, row_req, row_ctx, max_ctx, rows_per_group)
+    rc = load_library().dsa_indexer_topk(ctypes.byref(c), ctypes.byref(r), _ptr(q_idx), _ptr(head_w), int(k),
+                                         _ptr(out), _ptr(status), _ptr(workspace), workspace.numel(),
+                                         _stream(stream))
+    _check(rc, "dsa_indexer_topk")
     return out
 
 
@@ -235,7 +294,8 @@ class Layer:
     """
 
     def __init__(self, idx_pool, key_fmt, lat_pool, lat_fmt, tensor_scale, block_table, max_ctx, num_rows,
-                 num_heads=96, k=2048, rows_per_group=1, prefill=False, sm_scale=DEFAULT_SM_SCALE, device="cuda"):
+                 num_heads=96, k=2048, rows_per_group=1, prefill=False, sm_scale=DEFAULT_SM_SCALE, device="cuda",
+                 single_pass=False):
         self.idx_pool, self.key_fmt = idx_pool, key_fmt
         self.lat_pool, self.lat_fmt, self.tensor_scale = lat_pool, lat_fmt, float(tensor_scale)
         self.block_table, self.max_ctx, self.k = block_table, int(max_ctx), int(k)
@@ -249,11 +309,28 @@ class Layer:
         need = 0 if prefill else sparse_mla_workspace_size(R, H, self.k)
         self.workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=device)
         self.status = new_status(device)
+        # single pass: the scorer builds each row's histogram and the top-k starts from it (opt-in:
+        # on one GB300 the scorer's histogram atomics cost more than the selection saves)
+        self.single_pass = single_pass
+        self.hist = new_hist(R, device) if single_pass else None
 
-    def run(self, row_req, row_ctx, q_idx, head_w, q_mla, stream=None):
-        indexer_logits(self.idx_pool, self.key_fmt, self.block_table, row_req, row_ctx, self.max_ctx, q_idx, head_w,
-                       self.rows_per_group, logits=self.logits, status=self.status, stream=stream)
-        topk(self.logits, row_ctx, self.max_ctx, self.k, out=self.idx, status=self.status, stream=stream)
+    def score(self, row_req, row_ctx, q_idx, head_w, stream=None):
+        """Indexer logits (and, single pass, their histogram)."""
+        if self.single_pass:
+            indexer_logits_hist(self.idx_pool, self.key_fmt, self.block_table, row_req, row_ctx, self.max_ctx, q_idx,
+                                head_w, self.hist, self.rows_per_group, logits=self.logits, status=self.status,
+                                stream=stream)
+        else:
+            indexer_logits(self.idx_pool, self.key_fmt, self.block_table, row_req, row_ctx, self.max_ctx, q_idx,
+                           head_w, self.rows_per_group, logits=self.logits, status=self.status, stream=stream)
+
+    def select(self, row_req, row_ctx, q_mla, stream=None):
+        """Top-k, page -> slot and sparse MLA over the scored logits."""
+        if self.single_pass:
+            topk_hist(self.logits, row_ctx, self.max_ctx, self.hist, self.k, out=self.idx, status=self.status,
+                      stream=stream)
+        else:
+            topk(self.logits, row_ctx, self.max_ctx, self.k, out=self.idx, status=self.status, stream=stream)
         page_to_slot(self.block_table, row_req, row_ctx, self.max_ctx, self.lat_pool.shape[0], self.idx,
                      out=self.slots, status=self.status, stream=stream)
         if self.prefill:
@@ -264,3 +341,7 @@ class Layer:
                               out=self.out, lse=self.lse, workspace=self.workspace, status=self.status,
                               stream=stream)
         return self.out, self.lse
+
+    def run(self, row_req, row_ctx, q_idx, head_w, q_mla, stream=None):
+        self.score(row_req, row_ctx, q_idx, head_w, stream=stream)
+        return self.select(row_req, row_ctx, q_mla, stream=stream)

@@ -19,6 +19,8 @@ namespace dsa {
 
 namespace {
 
+static_assert(DSA_HIST_BINS == kHistBins, "the header and the kernels agree on the histogram size");
+
 PFN_cuTensorMapEncodeTiled_v12000 get_encoder() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
     static std::once_flag once;
@@ -98,9 +100,9 @@ const char *dsa_status_string(int status) {
     }
 }
 
-int dsa_indexer_logits(const dsa_cache *index_cache, const dsa_rows *rows, const uint8_t *q_idx,
-                       const float *head_w, float *logits, int64_t logits_stride, int32_t *dev_status,
-                       void *stream) {
+static int indexer_common(const dsa_cache *index_cache, const dsa_rows *rows, const uint8_t *q_idx,
+                          const float *head_w, float *logits, int64_t logits_stride, uint32_t *hist,
+                          int32_t *dev_status, void *stream) {
     if (index_cache == nullptr) return DSA_ERR_INVALID_ARG;
     int rc = check_rows(rows);
     if (rc != DSA_OK) return rc;
@@ -138,6 +140,7 @@ int dsa_indexer_logits(const dsa_cache *index_cache, const dsa_rows *rows, const
     a.logits = logits;
     a.logits_stride = logits_stride;
     a.status = dev_status;
+    a.hist = hist;
     const int num_groups = rows->num_rows / G;
     for (int g0 = 0; g0 < num_groups; g0 += kIndexerMaxGroups) {
         a.group0 = g0;
@@ -149,14 +152,71 @@ int dsa_indexer_logits(const dsa_cache *index_cache, const dsa_rows *rows, const
     return DSA_OK;
 }
 
-int dsa_topk(const float *logits, int64_t logits_stride, const int32_t *row_ctx, int32_t num_rows,
-             int32_t max_ctx, int32_t k, int32_t *idx_out, int32_t *dev_status, void *stream) {
+int dsa_indexer_logits(const dsa_cache *index_cache, const dsa_rows *rows, const uint8_t *q_idx,
+                       const float *head_w, float *logits, int64_t logits_stride, int32_t *dev_status,
+                       void *stream) {
+    return indexer_common(index_cache, rows, q_idx, head_w, logits, logits_stride, nullptr, dev_status, stream);
+}
+
+int dsa_indexer_logits_hist(const dsa_cache *index_cache, const dsa_rows *rows, const uint8_t *q_idx,
+                            const float *head_w, float *logits, int64_t logits_stride, uint32_t *hist,
+                            int32_t *dev_status, void *stream) {
+    if (hist == nullptr && rows != nullptr && rows->num_rows > 0) return DSA_ERR_INVALID_ARG;
+    return indexer_common(index_cache, rows, q_idx, head_w, logits, logits_stride, hist, dev_status, stream);
+}
+
+static int topk_common(const float *logits, int64_t logits_stride, const int32_t *row_ctx, int32_t num_rows,
+                       int32_t max_ctx, int32_t k, uint32_t *hist, bool discard, int32_t *idx_out,
+                       int32_t *dev_status, void *stream) {
     if (num_rows < 0 || max_ctx < 0) return DSA_ERR_INVALID_ARG;
     if (k < 1 || k > DSA_MAX_TOPK) return DSA_ERR_UNSUPPORTED;
     if (num_rows == 0) return DSA_OK;
     if (!logits || !row_ctx || !idx_out || logits_stride < max_ctx) return DSA_ERR_INVALID_ARG;
-    TopkArgs a{logits, logits_stride, row_ctx, num_rows, max_ctx, k, idx_out, dev_status};
+    TopkArgs a{logits, logits_stride, row_ctx, num_rows, max_ctx, k, idx_out, dev_status, hist, discard};
     return launch_status(launch_topk(a, static_cast<cudaStream_t>(stream)));
+}
+
+int dsa_topk(const float *logits, int64_t logits_stride, const int32_t *row_ctx, int32_t num_rows,
+             int32_t max_ctx, int32_t k, int32_t *idx_out, int32_t *dev_status, void *stream) {
+    return topk_common(logits, logits_stride, row_ctx, num_rows, max_ctx, k, nullptr, false, idx_out, dev_status,
+                       stream);
+}
+
+int dsa_topk_hist(const float *logits, int64_t logits_stride, const int32_t *row_ctx, int32_t num_rows,
+                  int32_t max_ctx, int32_t k, uint32_t *hist, int32_t *idx_out, int32_t *dev_status, void *stream) {
+    if (hist == nullptr && num_rows > 0) return DSA_ERR_INVALID_ARG;
+    return topk_common(logits, logits_stride, row_ctx, num_rows, max_ctx, k, hist, false, idx_out, dev_status,
+                       stream);
+}
+
+// Workspace of dsa_indexer_topk: [histogram rows x DSA_HIST_BINS u32][logits rows x stride fp32],
+// the logits row stride rounded up to 32 floats (128-byte rows).
+static int64_t fused_logits_stride(int32_t max_ctx) { return (static_cast<int64_t>(max_ctx) + 31) / 32 * 32; }
+
+size_t dsa_indexer_topk_workspace_size(int32_t num_rows, int32_t max_ctx) {
+    if (num_rows <= 0 || max_ctx <= 0) return 0;
+    return align256(static_cast<size_t>(num_rows) * DSA_HIST_BINS * 4) +
+           align256(static_cast<size_t>(num_rows) * static_cast<size_t>(fused_logits_stride(max_ctx)) * 4);
+}
+
+int dsa_indexer_topk(const dsa_cache *index_cache, const dsa_rows *rows, const uint8_t *q_idx, const float *head_w,
+                     int32_t k, int32_t *idx_out, int32_t *dev_status, void *workspace, size_t workspace_bytes,
+                     void *stream) {
+    int rc = check_rows(rows);
+    if (rc != DSA_OK) return rc;
+    if (k < 1 || k > DSA_MAX_TOPK) return DSA_ERR_UNSUPPORTED;
+    if (rows->num_rows == 0) return DSA_OK;
+    if (workspace == nullptr || !aligned(workspace, 256) ||
+        workspace_bytes < dsa_indexer_topk_workspace_size(rows->num_rows, rows->max_ctx))
+        return DSA_ERR_WORKSPACE;
+    uint32_t *hist = static_cast<uint32_t *>(workspace);
+    float *logits = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) +
+                                              align256(static_cast<size_t>(rows->num_rows) * DSA_HIST_BINS * 4));
+    const int64_t stride = fused_logits_stride(rows->max_ctx);
+    rc = indexer_common(index_cache, rows, q_idx, head_w, logits, stride, hist, dev_status, stream);
+    if (rc != DSA_OK) return rc;
+    return topk_common(logits, stride, rows->row_ctx, rows->num_rows, rows->max_ctx, k, hist, true, idx_out,
+                       dev_status, stream);
 }
 
 int dsa_page_to_slot(const dsa_rows *rows, int64_t pool_pages, const int32_t *idx, int32_t k, int32_t *slots,

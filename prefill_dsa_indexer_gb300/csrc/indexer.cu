@@ -300,6 +300,7 @@ __global__ void __launch_bounds__(IdxCfg<G>::kThreads, 1)
             int cur = -1, gc = -1;
             int ctx[C::kRowsPerEpiWarp];
             int64_t row_off[C::kRowsPerEpiWarp];
+            int hrow[C::kRowsPerEpiWarp];  // global row of each of this warp's rows
             for (int32_t it = grp, w = w_begin + grp; w < w_end; it += C::kEpiGroups, w += C::kEpiGroups) {
                 wk.advance(w);
                 const int g = wk.g;
@@ -315,6 +316,7 @@ __global__ void __launch_bounds__(IdxCfg<G>::kThreads, 1)
                     for (int j = 0; j < C::kRowsPerEpiWarp; ++j) {
                         ctx[j] = min(a.row_ctx[row0 + rbeg + j], a.max_ctx);
                         row_off[j] = static_cast<int64_t>(row0 + rbeg + j) * a.logits_stride;
+                        hrow[j] = row0 + rbeg + j;
                     }
                 }
                 const float *wb = wbuf + (grp * 2 + (gc & 1)) * C::N;
@@ -351,7 +353,12 @@ __global__ void __launch_bounds__(IdxCfg<G>::kThreads, 1)
                         for (int h = 0; h < 32; ++h)
                             s4[h & 3] = fmaf(wr[h], fmaxf(__uint_as_float(acc[h]), 0.f), s4[h & 3]);
                         const float sum = (s4[0] + s4[1]) + (s4[2] + s4[3]);
-                        if (t < ctx[j]) a.logits[row_off[j] + t] = sum * s_t;
+                        if (t < ctx[j]) {
+                            const float v = sum * s_t;
+                            a.logits[row_off[j] + t] = v;
+                            if (a.hist)
+                                atomicAdd(a.hist + static_cast<int64_t>(hrow[j]) * kHistBins + (order_key(v) >> 16), 1u);
+                        }
                     }
                 }
                 tc_fence_before();

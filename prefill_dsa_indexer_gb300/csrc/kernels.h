@@ -26,9 +26,23 @@ struct IndexerArgs {
     float *logits;
     int64_t logits_stride;
     int32_t *status;
+    uint32_t *hist;             // optional [rows][kHistBins]: each written logit adds 1 at its key's top 16 bits
 };
 
 constexpr int kIndexerMaxGroups = 1024;
+
+// Per-row histogram shared by the scorer and the top-k: 65,536 bins of the top 16 bits of the
+// order-preserving key of each logit.
+constexpr int kHistBins = 65536;
+
+// Order-preserving map fp32 -> uint32 (a larger float gives a larger key); -0 folds onto +0
+// and NaN maps to 0, below every number.  The scorer and the top-k must agree on it exactly.
+__device__ __forceinline__ uint32_t order_key(float f) {
+    uint32_t u = __float_as_uint(f);
+    if (f != f) return 0u;
+    if (u == 0x80000000u) u = 0u;
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
 
 // Launch the FP8-key indexer for groups of `rows_per_group` rows.
 cudaError_t launch_indexer_fp8(const CUtensorMap &key_map, const CUtensorMap &q_map, const IndexerArgs &a,
@@ -47,6 +61,8 @@ struct TopkArgs {
     int32_t k;
     int32_t *idx_out;
     int32_t *status;
+    uint32_t *hist;             // optional: the scorer's histogram of exactly these logits (read, left zeroed)
+    bool discard_logits;        // the logits are library scratch: drop their L2 lines once read
 };
 
 cudaError_t launch_topk(const TopkArgs &a, cudaStream_t s);

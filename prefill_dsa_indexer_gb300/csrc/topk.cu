@@ -63,6 +63,9 @@ struct TopkSmem {
     uint32_t ncand;
     uint32_t range[2];
     uint32_t before[2];  // selected keys > T and == T in the lower-ranked chunks
+    uint32_t hpub;       // histogram path: this CTA's slice total (read by the cluster)
+    uint32_t hsel[2];    // histogram path: owner rank, the cluster's keys above its slice
+    uint32_t hres[3];    // histogram path, owner: the bin, the cluster's keys above it / in it
     int32_t bad;
 };
 
@@ -238,9 +241,13 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const TopkArgs a) {
         if (tid == 0 && crank == 0) report(a.status, DSA_ERR_BOUNDS);
         n = min(max(n, 0), a.max_ctx);
     }
+    const int hspan = kHistBins / CL;  // histogram path: this CTA's slice of the row's bins
+    uint32_t *hrow = a.hist ? a.hist + static_cast<int64_t>(row) * kHistBins : nullptr;
     if (n <= k) {  // the same branch for every CTA of the cluster: no cluster barrier below
         if (crank == 0)
             for (int i = tid; i < k; i += kThreads) out[i] = i < n ? i : -1;
+        if (hrow)  // leave the scorer's histogram zeroed for the next call
+            for (int b = tid; b < hspan; b += kThreads) hrow[crank * hspan + b] = 0u;
         return;
     }
     // this CTA's chunk [c0, c0 + nloc) of the row; chunk starts are multiples of 4 elements
@@ -255,66 +262,240 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const TopkArgs a) {
     for (int b = tid; b < kBins; b += kThreads) s.hist[b] = 0;
     __syncthreads();
 
-    // ---- 1. key range of the chunk (and its shared-memory copy), then of the row
-    uint32_t lo = 0xffffffffu, hi = 0u;
-    bool nan = false;
-    first_pass(s, chunk, nan, [&](uint32_t key) {
-        lo = min(lo, key);
-        hi = max(hi, key);
-    });
-    if (nan) s.bad = 1;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, o));
-        hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, o));
-    }
-    if (lane == 0) {
-        s.red[warp] = lo;
-        s.red[kWarps + warp] = hi;
-    }
-    __syncthreads();
-    if (warp == 0) {
-        lo = s.red[lane];
-        hi = s.red[kWarps + lane];
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, o));
-            hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, o));
-        }
-        if (lane == 0) {
-            s.mm[0] = lo;
-            s.mm[1] = hi;
-        }
-    }
-    if (tid == 0 && s.bad) report(a.status, DSA_ERR_RANGE);
-    cluster.sync();
-    if (warp == 0) {
-        lo = 0xffffffffu;
-        hi = 0u;
-        if (lane < CL) {
-            const uint32_t *mm = cluster.map_shared_rank(s.mm, lane);
-            lo = mm[0];
-            hi = mm[1];
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, o));
-            hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, o));
-        }
-        if (lane == 0) {
-            s.range[0] = lo;
-            s.range[1] = hi;
-        }
-    }
-    __syncthreads();
-    uint32_t base = s.range[0], top = s.range[1];
+    uint32_t base = 0, top = 0;
     uint32_t need = static_cast<uint32_t>(k);
     uint32_t my_above = 0;                         // this chunk's keys above [base, top]
     uint32_t my_in = static_cast<uint32_t>(nloc);  // this chunk's keys inside it
+    uint32_t hist_sc = 0xffffffffu;                // histogram path: the cluster's keys in [base, top]
+    bool nan = false;
+    if (hrow) {
+        // ---- 1h. the scorer's histogram of this row fixes the 16-bit bin of the k-th key.
+        // CTA r scans bin slice r (its threads take `per` consecutive bins each, thread 0 the
+        // slice's top ones), the cluster combines the slice totals from the highest slice
+        // down, and the owning CTA finds the bin.
+        const int per = hspan / kThreads;  // >= 4
+        const int hb0 = crank * hspan + hspan - (tid + 1) * per;
+        uint32_t tsum = 0;
+        for (int q = 0; q < per; ++q) tsum += hrow[hb0 + q];
+        const uint32_t tincl = warp_incl_scan32(tsum, lane);
+        if (lane == 31) s.red[warp] = tincl;
+        __syncthreads();
+        const uint32_t wincl = warp_incl_scan32(s.red[lane], lane);
+        const uint32_t wex = warp == 0 ? 0u : __shfl_sync(0xffffffffu, wincl, (warp + 31) & 31);
+        const uint32_t t_above = wex + tincl - tsum;  // this slice's keys above my bins
+        const uint32_t slice_total = __shfl_sync(0xffffffffu, wincl, 31);  // every lane takes part
+        if (tid == 0) s.hpub = slice_total;
+        cluster.sync();
+        if (warp == 0) {
+            uint32_t tot = 0;
+            if (lane < CL) tot = ld_peer(peer_addr(&s.hpub, lane));
+            // slices from the highest rank down: keys above slice r = totals of the ranks > r
+            // (an exclusive suffix sum over the lanes)
+            uint32_t suf = tot;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const uint32_t t2 = __shfl_down_sync(0xffffffffu, suf, o);
+                if (lane + o < 32) suf += t2;
+            }
+            const uint32_t above_r = suf - tot;
+            const bool mine = lane < CL && above_r < need && need <= above_r + tot;
+            const unsigned m = __ballot_sync(0xffffffffu, mine);
+            const int owner = m ? __ffs(m) - 1 : 0;
+            if (lane == owner) {
+                s.hsel[0] = static_cast<uint32_t>(owner);
+                s.hsel[1] = above_r;
+            }
+            if (lane == 0) s.hres[0] = 0xffffffffu;  // "not found" unless the owner finds the bin
+        }
+        __syncthreads();
+        const int owner = static_cast<int>(s.hsel[0]);
+        if (crank == owner) {
+            const uint32_t need_s = need - s.hsel[1];  // rank of the k-th key inside this slice
+            if (t_above < need_s && need_s <= t_above + tsum) {
+                uint32_t acc = t_above;
+                for (int q = per - 1; q >= 0; --q) {
+                    const uint32_t c = hrow[hb0 + q];
+                    if (acc < need_s && need_s <= acc + c) {
+                        s.hres[0] = static_cast<uint32_t>(hb0 + q);  // the bin
+                        s.hres[1] = acc + (need - need_s);           // the cluster's keys above it
+                        s.hres[2] = c;                               // the cluster's keys in it
+                        break;
+                    }
+                    acc += c;
+                }
+            }
+        }
+        cluster.sync();
+        if (tid == 0) {
+            const uint32_t *hs = cluster.map_shared_rank(s.hres, owner);
+            s.range[0] = hs[0];
+            s.range[1] = hs[1];
+            s.mm[0] = hs[2];
+        }
+        for (int q = 0; q < per; ++q) hrow[hb0 + q] = 0u;  // left zeroed for the next call
+        __syncthreads();
+        if (s.range[0] == 0xffffffffu) {
+            // the histogram does not describe these logits: report it and search the whole range
+            if (tid == 0 && crank == 0) report(a.status, DSA_ERR_RANGE);
+            base = 0u;
+            top = 0xffffffffu;
+        } else {
+            need -= s.range[1];
+            hist_sc = s.mm[0];
+            base = s.range[0] << 16;
+            top = base | 0xffffu;
+        }
+        // one pass over the chunk: shared-memory copy, this chunk's keys above / inside the bin,
+        // and its candidates when the cluster's bin fits the candidate list
+        const bool collect = hist_sc <= static_cast<uint32_t>(kCandCap);
+        uint32_t na = 0, ni = 0;
+        first_pass(s, chunk, nan, [&](uint32_t key) {
+            if (key > top) {
+                ++na;
+            } else if (key >= base) {
+                ++ni;
+                if (collect) {
+                    const uint32_t at = atomicAdd(&s.ncand, 1u);
+                    if (at < static_cast<uint32_t>(kCandCap)) s.cand[at] = key;
+                }
+            }
+        });
+        if (nan) s.bad = 1;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            na += __shfl_xor_sync(0xffffffffu, na, o);
+            ni += __shfl_xor_sync(0xffffffffu, ni, o);
+        }
+        __syncthreads();  // s.red is reused
+        if (lane == 0) {
+            s.red[warp] = na;
+            s.red[kWarps + warp] = ni;
+        }
+        __syncthreads();
+        na = s.red[lane];
+        ni = s.red[kWarps + lane];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            na += __shfl_xor_sync(0xffffffffu, na, o);
+            ni += __shfl_xor_sync(0xffffffffu, ni, o);
+        }
+        my_above = na;
+        my_in = ni;
+        if (tid == 0 && s.bad) report(a.status, DSA_ERR_RANGE);
+    } else {
+        // ---- 1. key range of the chunk (and its shared-memory copy), then of the row
+        uint32_t lo = 0xffffffffu, hi = 0u;
+        first_pass(s, chunk, nan, [&](uint32_t key) {
+            lo = min(lo, key);
+            hi = max(hi, key);
+        });
+        if (nan) s.bad = 1;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+            hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+        }
+        if (lane == 0) {
+            s.red[warp] = lo;
+            s.red[kWarps + warp] = hi;
+        }
+        __syncthreads();
+        if (warp == 0) {
+            lo = s.red[lane];
+            hi = s.red[kWarps + lane];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+                hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+            }
+            if (lane == 0) {
+                s.mm[0] = lo;
+                s.mm[1] = hi;
+            }
+        }
+        if (tid == 0 && s.bad) report(a.status, DSA_ERR_RANGE);
+        cluster.sync();
+        if (warp == 0) {
+            lo = 0xffffffffu;
+            hi = 0u;
+            if (lane < CL) {
+                const uint32_t *mm = cluster.map_shared_rank(s.mm, lane);
+                lo = mm[0];
+                hi = mm[1];
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+                hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+            }
+            if (lane == 0) {
+                s.range[0] = lo;
+                s.range[1] = hi;
+            }
+        }
+        __syncthreads();
+            base = s.range[0];
+            top = s.range[1];
+    }
+    if (a.discard_logits && chunk.ncache == nloc) {
+        // the chunk now lives in shared memory and the logits are scratch: drop the L2 lines
+        // that lie wholly inside this chunk, unwritten
+        __syncthreads();
+        const uintptr_t p0 = (reinterpret_cast<uintptr_t>(chunk.src) + 127) & ~uintptr_t(127);
+        const uintptr_t p1 = (reinterpret_cast<uintptr_t>(chunk.src + nloc)) & ~uintptr_t(127);
+        for (uintptr_t p = p0 + 128 * static_cast<uintptr_t>(tid); p < p1; p += 128 * kThreads)
+            l2_discard_line(reinterpret_cast<const void *>(p));
+    }
+
+    // Publish this chunk's candidates and its count above the interval, gather every CTA's
+    // candidates in rank order, and arrive on the closing cluster barrier.
+    auto publish_and_gather = [&]() {
+        if (tid == 0) s.pub[1] = my_above;
+        __syncthreads();
+        if (tid == 0) s.pub[0] = min(s.ncand, static_cast<uint32_t>(kCandCap));
+        cluster.sync();
+        if (warp == 0) {
+            uint32_t nr = 0, ar = 0;
+            if (lane < CL) {
+                const uint32_t *pub = cluster.map_shared_rank(s.pub, lane);
+                nr = pub[0];
+                ar = pub[1];
+            }
+            const uint32_t incl = warp_incl_scan32(nr, lane);
+            if (lane < CL) s.roff[lane] = incl - nr;
+            if (lane == CL - 1) s.roff[CL] = incl;
+            // selected keys above the interval in the lower-ranked chunks
+            const uint32_t ab = warp_incl_scan32(lane < crank ? ar : 0u, lane);
+            if (lane == 31) s.before[0] = ab;
+        }
+        __syncthreads();
+        const uint32_t total = s.roff[CL];
+        constexpr int kPer = kCandCap / kThreads;
+        uint32_t v[kPer];
+#pragma unroll
+        for (int u = 0; u < kPer; ++u) {  // all peer loads in flight before any store
+            const uint32_t j = tid + u * kThreads;
+            if (j < total) {
+                int r = 0;
+                while (r + 1 < CL && s.roff[r + 1] <= j) ++r;
+                v[u] = ld_peer(peer_addr(&s.cand[j - s.roff[r]], r));
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kPer; ++u)
+            if (tid + u * kThreads < total) s.cand_all[tid + u * kThreads] = v[u];
+        cluster_arrive();  // this CTA reads no peer memory after this point
+        __syncthreads();
+    };
+
+    bool gathered = false;
+    if (hrow && hist_sc <= static_cast<uint32_t>(kCandCap) && top > base) {
+        publish_and_gather();  // the bin's candidates were collected in the first pass
+        gathered = true;
+    }
 
     // ---- 2. cluster rounds, until the interval is one key or few enough keys to gather
-    bool gathered = false;
-    while (top > base) {
+    while (!gathered && top > base) {
         const uint32_t span = top - base;
         const int bits = 32 - __clz(span);            // span < 2^bits
         const int shift = bits > 11 ? bits - 11 : 0;  // (span >> shift) < 2048
@@ -373,43 +554,8 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const TopkArgs a) {
                 for (int q = 0; q < 4; ++q)
                     if (i + q < nloc && kq[q] >= base && kq[q] <= top) s.cand[at++] = kq[q];
             }
-            if (tid == 0) s.pub[1] = my_above;
-            __syncthreads();
-            if (tid == 0) s.pub[0] = s.ncand;
-            cluster.sync();
-            if (warp == 0) {
-                uint32_t nr = 0, ar = 0;
-                if (lane < CL) {
-                    const uint32_t *pub = cluster.map_shared_rank(s.pub, lane);
-                    nr = pub[0];
-                    ar = pub[1];
-                }
-                const uint32_t incl = warp_incl_scan32(nr, lane);
-                if (lane < CL) s.roff[lane] = incl - nr;
-                if (lane == CL - 1) s.roff[CL] = incl;
-                // selected keys above the interval in the lower-ranked chunks
-                const uint32_t ab = warp_incl_scan32(lane < crank ? ar : 0u, lane);
-                if (lane == 31) s.before[0] = ab;
-            }
-            __syncthreads();
-            const uint32_t total = s.roff[CL];
-            constexpr int kPer = kCandCap / kThreads;
-            uint32_t v[kPer];
-#pragma unroll
-            for (int u = 0; u < kPer; ++u) {  // all peer loads in flight before any store
-                const uint32_t j = tid + u * kThreads;
-                if (j < total) {
-                    int r = 0;
-                    while (r + 1 < CL && s.roff[r + 1] <= j) ++r;
-                    v[u] = ld_peer(peer_addr(&s.cand[j - s.roff[r]], r));
-                }
-            }
-#pragma unroll
-            for (int u = 0; u < kPer; ++u)
-                if (tid + u * kThreads < total) s.cand_all[tid + u * kThreads] = v[u];
-            cluster_arrive();  // this CTA reads no peer memory after this point
+            publish_and_gather();
             gathered = true;
-            __syncthreads();
             break;
         }
     }
@@ -417,7 +563,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const TopkArgs a) {
     // ---- 3. refine alone on the gathered candidates
     uint32_t gt_before = 0, eq_before = 0;
     if (gathered) {
-        const int nc = static_cast<int>(s.roff[CL]);
+        const int nc = static_cast<int>(min(s.roff[CL], static_cast<uint32_t>(kCandCap)));
         while (top > base) {
             const uint32_t span = top - base;
             const int bits = 32 - __clz(span);
@@ -436,7 +582,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const TopkArgs a) {
         }
         // the lower-ranked chunks' candidates above / equal to T
         const uint32_t T = base;
-        const int lower = static_cast<int>(s.roff[crank]);
+        const int lower = static_cast<int>(min(s.roff[crank], static_cast<uint32_t>(kCandCap)));
         uint32_t g = 0, e = 0;
         for (int i = tid; i < lower; i += kThreads) {
             const uint32_t key = s.cand_all[i];
