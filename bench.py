@@ -321,17 +321,28 @@ def main():
         except TypeError:
             graph_mode = "two-graphs"
 
+        side = torch.cuda.Stream()
+
         def capture(n):
+            # per step: the decode query prep forks onto a side branch (it needs only the query)
+            # and joins before the attention; scorer -> top-k+slots -> attention on the main branch
             g = torch.cuda.CUDAGraph()
             evp = [(ext_event(), ext_event()) for _ in range(n)]
             with torch.cuda.stream(cap):
                 with torch.cuda.graph(g, stream=cap):
                     for k in range(n):
                         L = layers[k % len(layers)]
+                        fork = not L.prefill
+                        if fork:
+                            side.wait_stream(cap)
+                            with torch.cuda.stream(side):
+                                L.prepare(inp.q_mla)
                         evp[k][0].record(cap)
                         indexer(L)
                         evp[k][1].record(cap)
-                        rest_of_step(L)
+                        if fork:
+                            cap.wait_stream(side)
+                        L.select(inp.row_req, inp.row_ctx, inp.q_mla, prepared=fork)
             return g, evp
 
         if graph_mode == "multi-step":
@@ -464,8 +475,10 @@ def main():
     if os.path.exists(tfile):
         with open(tfile) as f:
             traffic = json.load(f).get(wl.name)
-    # indexer, top-k, page->slot, sparse MLA; decode with split rows adds the query prep and the merge
-    launches_per_step = 4 + (2 if (not prefill and P.sparse_mla_workspace_size(wl.num_rows, wl.heads, wl.k) > 0) else 0)
+    # scorer, top-k (with page -> slot unless single pass, which launches it apart), sparse MLA;
+    # decode with split rows adds the query prep and the merge
+    launches_per_step = 3 + (1 if args.single_pass else 0) + (
+        2 if (not prefill and P.sparse_mla_workspace_size(wl.num_rows, wl.heads, wl.k) > 0) else 0)
 
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -484,8 +497,9 @@ def main():
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e2e_ms / args.steps},
         "gpu_launches": launches_per_step * args.steps,
-        "launch": {"multi-step": f"CUDA graphs of {16 * copies} consecutive steps; indexer timed by event nodes "
-                                 f"inside the graph ({len(samples)} launches sampled)",
+        "launch": {"multi-step": f"CUDA graphs of {16 * copies} consecutive steps (decode query prep on a "
+                                 f"parallel branch); indexer timed by event nodes inside the graph "
+                                 f"({len(samples)} launches sampled)",
                    "two-graphs": "CUDA-graph replay (indexer graph + rest-of-step graph), stream events between",
                    "eager": "eager launches, stream events around the indexer"}[graph_mode],
         "clocks": clk.summary(h0, h1),

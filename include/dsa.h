@@ -142,6 +142,17 @@ int dsa_topk(const float *logits, int64_t logits_stride, const int32_t *row_ctx,
              int32_t max_ctx, int32_t k, int32_t *idx_out, int32_t *dev_status, void *stream);
 
 /*
+ * Top-k and page -> slot in one call (the two steps below, dsa_topk then
+ * dsa_page_to_slot, with the translation done where the selection is
+ * written): idx_out as dsa_topk over rows->row_ctx / rows->max_ctx, and
+ * slots_out[r, i] = block_table[row_req[r]][t / 64] * 64 + t % 64 for each
+ * selected t = idx_out[r, i] (-1 where idx_out is -1).  A page id outside
+ * [0, pool_pages) or a bad row_req is DSA_ERR_BOUNDS with slot -1.
+ */
+int dsa_topk_slots(const float *logits, int64_t logits_stride, const dsa_rows *rows, int64_t pool_pages, int32_t k,
+                   int32_t *idx_out, int32_t *slots_out, int32_t *dev_status, void *stream);
+
+/*
  * Single-pass scorer + top-k (blog section "Low-latency decode: fused DSA
  * decode path": the scorer feeds a batch-invariant exact top-k; here the
  * scorer's epilogue also builds the histogram the selection starts from).
@@ -230,6 +241,25 @@ int dsa_sparse_mla_prefill(const dsa_cache *latent_cache, const uint16_t *q, int
                            const int32_t *slots, int32_t num_rows, int32_t k, float sm_scale, float *out,
                            float *lse, int32_t *dev_status, void *workspace, size_t workspace_bytes,
                            void *stream);
+
+/*
+ * dsa_sparse_mla_decode in two parts, so the query conversion can run ahead
+ * of (or beside) the scorer and the top-k, which it does not depend on:
+ * _prepare writes each row's query, converted once to the attention
+ * kernel's fp16 operand layout, into the workspace (nothing when k <= 128,
+ * where decode uses no workspace); _prepared then runs the attention on it.
+ * Both take the arguments of dsa_sparse_mla_decode (_prepare ignores the
+ * slots, outputs and sm_scale) and the same workspace; _prepared must be
+ * ordered after _prepare with the same q, num_heads, num_rows and k.  The
+ * result equals dsa_sparse_mla_decode's bit for bit.
+ */
+int dsa_sparse_mla_decode_prepare(const dsa_cache *latent_cache, const uint16_t *q, int32_t num_heads,
+                                  int32_t num_rows, int32_t k, int32_t *dev_status, void *workspace,
+                                  size_t workspace_bytes, void *stream);
+int dsa_sparse_mla_decode_prepared(const dsa_cache *latent_cache, const uint16_t *q, int32_t num_heads,
+                                   const int32_t *slots, int32_t num_rows, int32_t k, float sm_scale, float *out,
+                                   float *lse, int32_t *dev_status, void *workspace, size_t workspace_bytes,
+                                   void *stream);
 
 /*
  * dsa_sparse_mla_decode without a caller workspace.  The paper has no

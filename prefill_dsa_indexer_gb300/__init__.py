@@ -88,6 +88,13 @@ def load_library(path: str | None = None):
                                      ctypes.c_size_t, P]
     lib.dsa_indexer_topk_workspace_size.restype = ctypes.c_size_t
     lib.dsa_indexer_topk_workspace_size.argtypes = [I32, I32]
+    lib.dsa_topk_slots.restype = ctypes.c_int
+    lib.dsa_topk_slots.argtypes = [P, I64, ctypes.POINTER(_Rows), I64, I32, P, P, P, P]
+    lib.dsa_sparse_mla_decode_prepare.restype = ctypes.c_int
+    lib.dsa_sparse_mla_decode_prepare.argtypes = [ctypes.POINTER(_Cache), P, I32, I32, I32, P, P, ctypes.c_size_t, P]
+    lib.dsa_sparse_mla_decode_prepared.restype = ctypes.c_int
+    lib.dsa_sparse_mla_decode_prepared.argtypes = [ctypes.POINTER(_Cache), P, I32, P, I32, I32, F, P, P, P, P,
+                                                   ctypes.c_size_t, P]
     if path is None:
         _lib = lib
     return lib
@@ -96,7 +103,8 @@ def load_library(path: str | None = None):
 EXPORTED = ("dsa_version", "dsa_status_string", "dsa_indexer_logits", "dsa_topk", "dsa_page_to_slot",
             "dsa_sparse_mla_decode", "dsa_sparse_mla_prefill", "dsa_sparse_mla_workspace_size",
             "dsa_sparse_mla_decode_noalloc", "dsa_cache_insert", "dsa_indexer_logits_hist", "dsa_topk_hist",
-            "dsa_indexer_topk", "dsa_indexer_topk_workspace_size")
+            "dsa_indexer_topk", "dsa_indexer_topk_workspace_size", "dsa_topk_slots",
+            "dsa_sparse_mla_decode_prepare", "dsa_sparse_mla_decode_prepared")
 HIST_BINS = 65536
 NOALLOC_MAX_ROWS = 8
 
@@ -214,6 +222,21 @@ def indexer_topk(index_pool, key_fmt, block_table, row_req, row_ctx, max_ctx, q_
     return out
 
 
+def topk_slots(logits, block_table, row_req, row_ctx, max_ctx, pool_pages, k=2048, out=None, slots=None,
+               status=None, stream=None):
+    """dsa_topk_slots: (idx int32 [R, k], slots int32 [R, k]) — top-k with the page -> slot translation."""
+    R = row_ctx.shape[0]
+    if out is None:
+        out = torch.empty((R, k), dtype=torch.int32, device=logits.device)
+    if slots is None:
+        slots = torch.empty((R, k), dtype=torch.int32, device=logits.device)
+    r = _rows(block_table, row_req, row_ctx, max_ctx)
+    rc = load_library().dsa_topk_slots(_ptr(logits), logits.stride(0), ctypes.byref(r), int(pool_pages), int(k),
+                                       _ptr(out), _ptr(slots), _ptr(status), _stream(stream))
+    _check(rc, "dsa_topk_slots")
+    return out, slots
+
+
 def page_to_slot(block_table, row_req, row_ctx, max_ctx, pool_pages, idx, out=None, status=None, stream=None):
     """dsa_page_to_slot: int32 [R, k] physical slots (-1 stays -1)."""
     if out is None:
@@ -246,7 +269,7 @@ def _mla(name, lat_pool, lat_fmt, tensor_scale, q, slots, sm_scale, out, lse, wo
     if lse is None:
         lse = torch.empty((R, H), dtype=torch.float32, device=q.device)
     ws_ptr, ws_bytes = None, 0
-    if name == "dsa_sparse_mla_decode":
+    if name in ("dsa_sparse_mla_decode", "dsa_sparse_mla_decode_prepared"):
         need = sparse_mla_workspace_size(R, H, k)
         if workspace is None and need:
             workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
@@ -278,6 +301,23 @@ def sparse_mla_decode_noalloc(lat_pool, lat_fmt, tensor_scale, q, slots, out, ls
                                                       _stream(stream))
     _check(rc, "dsa_sparse_mla_decode_noalloc")
     return out, lse
+
+
+def sparse_mla_decode_prepare(lat_pool, lat_fmt, tensor_scale, q, k, workspace, status=None, stream=None):
+    """dsa_sparse_mla_decode_prepare: the rows' queries into the workspace in the kernel's layout."""
+    R, H, _ = q.shape
+    c = _cache(lat_pool, lat_fmt, tensor_scale)
+    rc = load_library().dsa_sparse_mla_decode_prepare(ctypes.byref(c), _ptr(q), H, R, int(k), _ptr(status),
+                                                      _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                                      _stream(stream))
+    _check(rc, "dsa_sparse_mla_decode_prepare")
+
+
+def sparse_mla_decode_prepared(lat_pool, lat_fmt, tensor_scale, q, slots, sm_scale=DEFAULT_SM_SCALE, out=None,
+                               lse=None, workspace=None, status=None, stream=None):
+    """dsa_sparse_mla_decode_prepared: sparse_mla_decode after sparse_mla_decode_prepare on `workspace`."""
+    return _mla("dsa_sparse_mla_decode_prepared", lat_pool, lat_fmt, tensor_scale, q, slots, sm_scale, out, lse,
+                workspace, status, stream)
 
 
 def sparse_mla_prefill(lat_pool, lat_fmt, tensor_scale, q, slots, sm_scale=DEFAULT_SM_SCALE, out=None, lse=None,
@@ -324,23 +364,34 @@ class Layer:
             indexer_logits(self.idx_pool, self.key_fmt, self.block_table, row_req, row_ctx, self.max_ctx, q_idx,
                            head_w, self.rows_per_group, logits=self.logits, status=self.status, stream=stream)
 
-    def select(self, row_req, row_ctx, q_mla, stream=None):
-        """Top-k, page -> slot and sparse MLA over the scored logits."""
+    def select(self, row_req, row_ctx, q_mla, stream=None, prepared=False):
+        """Top-k, page -> slot and sparse MLA over the scored logits (`prepared`: prepare() ran already)."""
         if self.single_pass:
             topk_hist(self.logits, row_ctx, self.max_ctx, self.hist, self.k, out=self.idx, status=self.status,
                       stream=stream)
-        else:
-            topk(self.logits, row_ctx, self.max_ctx, self.k, out=self.idx, status=self.status, stream=stream)
-        page_to_slot(self.block_table, row_req, row_ctx, self.max_ctx, self.lat_pool.shape[0], self.idx,
-                     out=self.slots, status=self.status, stream=stream)
+            page_to_slot(self.block_table, row_req, row_ctx, self.max_ctx, self.lat_pool.shape[0], self.idx,
+                         out=self.slots, status=self.status, stream=stream)
+        else:  # top-k with the page -> slot translation in its output pass
+            topk_slots(self.logits, self.block_table, row_req, row_ctx, self.max_ctx, self.lat_pool.shape[0], self.k,
+                       out=self.idx, slots=self.slots, status=self.status, stream=stream)
         if self.prefill:
             sparse_mla_prefill(self.lat_pool, self.lat_fmt, self.tensor_scale, q_mla, self.slots, self.sm_scale,
                                out=self.out, lse=self.lse, status=self.status, stream=stream)
+        elif prepared:
+            sparse_mla_decode_prepared(self.lat_pool, self.lat_fmt, self.tensor_scale, q_mla, self.slots,
+                                       self.sm_scale, out=self.out, lse=self.lse, workspace=self.workspace,
+                                       status=self.status, stream=stream)
         else:
             sparse_mla_decode(self.lat_pool, self.lat_fmt, self.tensor_scale, q_mla, self.slots, self.sm_scale,
                               out=self.out, lse=self.lse, workspace=self.workspace, status=self.status,
                               stream=stream)
         return self.out, self.lse
+
+    def prepare(self, q_mla, stream=None):
+        """Decode query conversion (independent of the scorer and the top-k; may run beside them)."""
+        if not self.prefill:
+            sparse_mla_decode_prepare(self.lat_pool, self.lat_fmt, self.tensor_scale, q_mla, self.k, self.workspace,
+                                      status=self.status, stream=stream)
 
     def run(self, row_req, row_ctx, q_idx, head_w, q_mla, stream=None):
         self.score(row_req, row_ctx, q_idx, head_w, stream=stream)

@@ -167,13 +167,34 @@ int dsa_indexer_logits_hist(const dsa_cache *index_cache, const dsa_rows *rows, 
 
 static int topk_common(const float *logits, int64_t logits_stride, const int32_t *row_ctx, int32_t num_rows,
                        int32_t max_ctx, int32_t k, uint32_t *hist, bool discard, int32_t *idx_out,
-                       int32_t *dev_status, void *stream) {
+                       int32_t *dev_status, void *stream, const dsa_rows *slot_rows = nullptr,
+                       int64_t pool_pages = 0, int32_t *slots_out = nullptr) {
     if (num_rows < 0 || max_ctx < 0) return DSA_ERR_INVALID_ARG;
     if (k < 1 || k > DSA_MAX_TOPK) return DSA_ERR_UNSUPPORTED;
     if (num_rows == 0) return DSA_OK;
     if (!logits || !row_ctx || !idx_out || logits_stride < max_ctx) return DSA_ERR_INVALID_ARG;
-    TopkArgs a{logits, logits_stride, row_ctx, num_rows, max_ctx, k, idx_out, dev_status, hist, discard};
+    TopkArgs a{logits, logits_stride, row_ctx, num_rows, max_ctx, k, idx_out, dev_status, hist, discard,
+               nullptr, nullptr, 0, nullptr, 0, 0};
+    if (slots_out != nullptr) {
+        if (slot_rows == nullptr || pool_pages <= 0) return DSA_ERR_INVALID_ARG;
+        if (pool_pages * DSA_PAGE_SIZE > INT32_MAX) return DSA_ERR_UNSUPPORTED;
+        a.slots_out = slots_out;
+        a.block_table = slot_rows->block_table;
+        a.bt_stride = slot_rows->bt_stride;
+        a.row_req = slot_rows->row_req;
+        a.num_requests = slot_rows->num_requests;
+        a.pool_pages = pool_pages;
+    }
     return launch_status(launch_topk(a, static_cast<cudaStream_t>(stream)));
+}
+
+int dsa_topk_slots(const float *logits, int64_t logits_stride, const dsa_rows *rows, int64_t pool_pages, int32_t k,
+                   int32_t *idx_out, int32_t *slots_out, int32_t *dev_status, void *stream) {
+    int rc = check_rows(rows);
+    if (rc != DSA_OK) return rc;
+    if (rows->num_rows > 0 && slots_out == nullptr) return DSA_ERR_INVALID_ARG;
+    return topk_common(logits, logits_stride, rows->row_ctx, rows->num_rows, rows->max_ctx, k, nullptr, false,
+                       idx_out, dev_status, stream, rows, pool_pages, slots_out);
 }
 
 int dsa_topk(const float *logits, int64_t logits_stride, const int32_t *row_ctx, int32_t num_rows,
@@ -237,16 +258,20 @@ size_t dsa_sparse_mla_workspace_size(int32_t num_rows, int32_t num_heads, int32_
     return mla_workspace_bytes(num_rows, num_heads, k);
 }
 
+enum class MlaMode { kPrefill, kDecode, kDecodePrepareOnly, kDecodePrepared };
+
 static int sparse_mla_common(const dsa_cache *lat, const uint16_t *q, int32_t num_heads, const int32_t *slots,
                              int32_t num_rows, int32_t k, float sm_scale, float *out, float *lse,
-                             int32_t *dev_status, void *ws, size_t ws_bytes, void *stream, bool decode) {
+                             int32_t *dev_status, void *ws, size_t ws_bytes, void *stream, MlaMode mode) {
+    const bool decode = mode != MlaMode::kPrefill;
+    const bool prep_only = mode == MlaMode::kDecodePrepareOnly;
     if (lat == nullptr || num_rows < 0) return DSA_ERR_INVALID_ARG;
     if (lat->page_size != DSA_PAGE_SIZE) return DSA_ERR_UNSUPPORTED;
     if (lat->format != DSA_LATENT_FP8 && lat->format != DSA_LATENT_NVFP4) return DSA_ERR_UNSUPPORTED;
     if (num_heads < 16 || num_heads > 96 || num_heads % 16 != 0) return DSA_ERR_UNSUPPORTED;
     if (k < 1) return DSA_ERR_INVALID_ARG;
     if (num_rows == 0) return DSA_OK;
-    if (!lat->base || lat->num_pages <= 0 || !q || !slots || !out) return DSA_ERR_INVALID_ARG;
+    if (!lat->base || lat->num_pages <= 0 || !q || (!prep_only && (!slots || !out))) return DSA_ERR_INVALID_ARG;
     if (!aligned(lat->base, 16) || !aligned(q, 16)) return DSA_ERR_INVALID_ARG;
     if (!std::isfinite(sm_scale) || !std::isfinite(lat->tensor_scale)) return DSA_ERR_INVALID_ARG;
     MlaArgs a{};
@@ -280,6 +305,8 @@ static int sparse_mla_common(const dsa_cache *lat, const uint16_t *q, int32_t nu
             a.splits = static_cast<int32_t>(splits);
         }
     }
+    if (prep_only) return launch_status(launch_mla_qprep(a, static_cast<cudaStream_t>(stream)));
+    a.q_prepared = mode == MlaMode::kDecodePrepared;
     return launch_status(launch_sparse_mla(a, static_cast<cudaStream_t>(stream)));
 }
 
@@ -287,7 +314,22 @@ int dsa_sparse_mla_decode(const dsa_cache *latent_cache, const uint16_t *q, int3
                           const int32_t *slots, int32_t num_rows, int32_t k, float sm_scale, float *out,
                           float *lse, int32_t *dev_status, void *workspace, size_t workspace_bytes, void *stream) {
     return sparse_mla_common(latent_cache, q, num_heads, slots, num_rows, k, sm_scale, out, lse, dev_status,
-                             workspace, workspace_bytes, stream, true);
+                             workspace, workspace_bytes, stream, MlaMode::kDecode);
+}
+
+int dsa_sparse_mla_decode_prepare(const dsa_cache *latent_cache, const uint16_t *q, int32_t num_heads,
+                                  int32_t num_rows, int32_t k, int32_t *dev_status, void *workspace,
+                                  size_t workspace_bytes, void *stream) {
+    return sparse_mla_common(latent_cache, q, num_heads, nullptr, num_rows, k, 1.0f, nullptr, nullptr, dev_status,
+                             workspace, workspace_bytes, stream, MlaMode::kDecodePrepareOnly);
+}
+
+int dsa_sparse_mla_decode_prepared(const dsa_cache *latent_cache, const uint16_t *q, int32_t num_heads,
+                                   const int32_t *slots, int32_t num_rows, int32_t k, float sm_scale, float *out,
+                                   float *lse, int32_t *dev_status, void *workspace, size_t workspace_bytes,
+                                   void *stream) {
+    return sparse_mla_common(latent_cache, q, num_heads, slots, num_rows, k, sm_scale, out, lse, dev_status,
+                             workspace, workspace_bytes, stream, MlaMode::kDecodePrepared);
 }
 
 int dsa_sparse_mla_prefill(const dsa_cache *latent_cache, const uint16_t *q, int32_t num_heads,
@@ -295,7 +337,7 @@ int dsa_sparse_mla_prefill(const dsa_cache *latent_cache, const uint16_t *q, int
                            float *lse, int32_t *dev_status, void *workspace, size_t workspace_bytes,
                            void *stream) {
     return sparse_mla_common(latent_cache, q, num_heads, slots, num_rows, k, sm_scale, out, lse, dev_status,
-                             workspace, workspace_bytes, stream, false);
+                             workspace, workspace_bytes, stream, MlaMode::kPrefill);
 }
 
 int dsa_cache_insert(const dsa_cache *index_cache, const dsa_cache *latent_cache, const int32_t *slots,

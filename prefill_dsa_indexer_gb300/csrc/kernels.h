@@ -63,6 +63,13 @@ struct TopkArgs {
     int32_t *status;
     uint32_t *hist;             // optional: the scorer's histogram of exactly these logits (read, left zeroed)
     bool discard_logits;        // the logits are library scratch: drop their L2 lines once read
+    // optional page -> slot translation of the selection (slots_out == nullptr: none)
+    int32_t *slots_out;         // [num_rows, k]: block_table[row_req[r]][t / 64] * 64 + t % 64, -1 padded
+    const int32_t *block_table;
+    int64_t bt_stride;
+    const int32_t *row_req;
+    int32_t num_requests;
+    int64_t pool_pages;
 };
 
 cudaError_t launch_topk(const TopkArgs &a, cudaStream_t s);
@@ -102,7 +109,11 @@ struct MlaArgs {
     float *part_ml;     // decode: [R, splits, H, 2] running max (log2 units) and sum
     uint8_t *qprep;     // decode: [R, 9 * H * 128] fp16 query images, laid out as the kernel's operand
     int32_t splits;     // 1 = write the final output directly
+    bool q_prepared;    // decode: the query images are already in qprep (no prep launch)
 };
+
+// Decode query preparation alone (bf16 query -> the fp16 operand images in a.qprep).
+cudaError_t launch_mla_qprep(const MlaArgs &a, cudaStream_t s);
 
 // Decode splits every row's selected tokens into parts of this many tokens (fixed, so a row's
 // result does not depend on the batch), merged by log-sum-exp.

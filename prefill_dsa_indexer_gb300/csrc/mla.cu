@@ -758,11 +758,8 @@ cudaError_t launch_fmt(const MlaArgs &a, cudaStream_t s) {
         if (e != cudaSuccess) return e;
         configured_device = dev;
     }
-    if (a.qprep != nullptr) {
-        const int64_t units = static_cast<int64_t>(a.num_rows) * a.num_heads * (DSA_LATENT_DIM / 8);
-        const int blocks = static_cast<int>(units / 256 < 4096 ? (units + 255) / 256 : 4096);
-        mla_qprep_kernel<<<blocks, 256, 0, s>>>(a);
-        cudaError_t e = cudaGetLastError();
+    if (a.qprep != nullptr && !a.q_prepared) {
+        cudaError_t e = launch_mla_qprep(a, s);
         if (e != cudaSuccess) return e;
     }
     sparse_mla_kernel<FMT><<<a.num_rows * a.splits, kThreads, kSmemBytes, s>>>(a);
@@ -773,6 +770,14 @@ cudaError_t launch_fmt(const MlaArgs &a, cudaStream_t s) {
 }
 
 }  // namespace
+
+cudaError_t launch_mla_qprep(const MlaArgs &a, cudaStream_t s) {
+    if (a.num_rows == 0 || a.qprep == nullptr) return cudaSuccess;
+    const int64_t units = static_cast<int64_t>(a.num_rows) * a.num_heads * (DSA_LATENT_DIM / 8);
+    const int blocks = static_cast<int>(units / 256 < 4096 ? (units + 255) / 256 : 4096);
+    mla_qprep_kernel<<<blocks, 256, 0, s>>>(a);
+    return cudaGetLastError();
+}
 
 size_t mla_workspace_bytes(int32_t num_rows, int32_t num_heads, int32_t k) {
     return mla_workspace_bytes_for(static_cast<size_t>(num_rows), static_cast<size_t>(num_heads),

@@ -226,6 +226,21 @@ __device__ void select_bin(TopkSmem &s, const uint32_t *cl, uint32_t need) {
     __syncthreads();
 }
 
+// Physical slot of position t of a request's block-table row (-1 and a status report when the
+// page id is outside the pool), the translation of slots.cu done where the selection is written.
+__device__ __forceinline__ int32_t slot_of(const TopkArgs &a, const int32_t *bt_row, int32_t t) {
+    if (bt_row == nullptr) {
+        report(a.status, DSA_ERR_BOUNDS);
+        return -1;
+    }
+    const int32_t page = bt_row[t / DSA_PAGE_SIZE];
+    if (page < 0 || page >= a.pool_pages) {
+        report(a.status, DSA_ERR_BOUNDS);
+        return -1;
+    }
+    return page * DSA_PAGE_SIZE + t % DSA_PAGE_SIZE;
+}
+
 __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const TopkArgs a) {
     extern __shared__ uint8_t smem_raw[];
     TopkSmem &s = *reinterpret_cast<TopkSmem *>(smem_raw);
@@ -236,6 +251,12 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const TopkArgs a) {
     const int row = blockIdx.x / CL;
     const int k = a.k;
     int32_t *out = a.idx_out + static_cast<int64_t>(row) * k;
+    int32_t *sout = a.slots_out ? a.slots_out + static_cast<int64_t>(row) * k : nullptr;
+    const int32_t *bt_row = nullptr;  // this row's block-table row, when slots are wanted
+    if (sout) {
+        const int32_t req = a.row_req[row];
+        if (req >= 0 && req < a.num_requests) bt_row = a.block_table + static_cast<int64_t>(req) * a.bt_stride;
+    }
     int n = a.row_ctx[row];
     if (n < 0 || n > a.max_ctx) {
         if (tid == 0 && crank == 0) report(a.status, DSA_ERR_BOUNDS);
@@ -245,7 +266,10 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const TopkArgs a) {
     uint32_t *hrow = a.hist ? a.hist + static_cast<int64_t>(row) * kHistBins : nullptr;
     if (n <= k) {  // the same branch for every CTA of the cluster: no cluster barrier below
         if (crank == 0)
-            for (int i = tid; i < k; i += kThreads) out[i] = i < n ? i : -1;
+            for (int i = tid; i < k; i += kThreads) {
+                out[i] = i < n ? i : -1;
+                if (sout) sout[i] = i < n ? slot_of(a, bt_row, i) : -1;
+            }
         if (hrow)  // leave the scorer's histogram zeroed for the next call
             for (int b = tid; b < hspan; b += kThreads) hrow[crank * hspan + b] = 0u;
         return;
@@ -684,8 +708,12 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const TopkArgs a) {
             const bool gt = in && kq[q] > T, eq = in && kq[q] == T;
             if (gt || (eq && eb < need)) {
                 const uint32_t pos = gb + min(eb, need);
-                if (pos < static_cast<uint32_t>(k)) out[pos] = c0 + i + q;
-                else report(a.status, DSA_ERR_BOUNDS);  // inconsistent counts: never expected
+                if (pos < static_cast<uint32_t>(k)) {
+                    out[pos] = c0 + i + q;
+                    if (sout) sout[pos] = slot_of(a, bt_row, c0 + i + q);
+                } else {
+                    report(a.status, DSA_ERR_BOUNDS);  // inconsistent counts: never expected
+                }
             }
             gb += gt ? 1u : 0u;
             eb += eq ? 1u : 0u;
