@@ -88,7 +88,7 @@ struct IdxCfg {
     static_assert(kSmemBytes == smem_for(kStages), "stage sizing matches the layout");
 };
 
-template <int G>
+template <int G, bool kHist>
 __global__ void __launch_bounds__(IdxCfg<G>::kThreads, 1)
     indexer_fp8_kernel(const __grid_constant__ CUtensorMap key_map, const __grid_constant__ CUtensorMap q_map,
                        const IndexerArgs a) {
@@ -356,7 +356,7 @@ __global__ void __launch_bounds__(IdxCfg<G>::kThreads, 1)
                         if (t < ctx[j]) {
                             const float v = sum * s_t;
                             a.logits[row_off[j] + t] = v;
-                            if (a.hist)
+                            if constexpr (kHist)
                                 atomicAdd(a.hist + static_cast<int64_t>(hrow[j]) * kHistBins + (order_key(v) >> 16), 1u);
                         }
                     }
@@ -377,21 +377,27 @@ __global__ void __launch_bounds__(IdxCfg<G>::kThreads, 1)
     }
 }
 
-template <int G>
-cudaError_t launch_g(const CUtensorMap &key_map, const CUtensorMap &q_map, const IndexerArgs &a, int num_sms,
-                     cudaStream_t s) {
+template <int G, bool kHist>
+cudaError_t launch_gh(const CUtensorMap &key_map, const CUtensorMap &q_map, const IndexerArgs &a, int num_sms,
+                      cudaStream_t s) {
     using C = IdxCfg<G>;
     static int configured_device = -1;
     int dev = 0;
     cudaGetDevice(&dev);
     if (configured_device != dev) {
-        cudaError_t e = cudaFuncSetAttribute(indexer_fp8_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaError_t e = cudaFuncSetAttribute(indexer_fp8_kernel<G, kHist>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              C::kSmemBytes);
         if (e != cudaSuccess) return e;
         configured_device = dev;
     }
-    indexer_fp8_kernel<G><<<num_sms, C::kThreads, C::kSmemBytes, s>>>(key_map, q_map, a);
+    indexer_fp8_kernel<G, kHist><<<num_sms, C::kThreads, C::kSmemBytes, s>>>(key_map, q_map, a);
     return cudaGetLastError();
+}
+
+template <int G>
+cudaError_t launch_g(const CUtensorMap &key_map, const CUtensorMap &q_map, const IndexerArgs &a, int num_sms,
+                     cudaStream_t s) {
+    return a.hist ? launch_gh<G, true>(key_map, q_map, a, num_sms, s) : launch_gh<G, false>(key_map, q_map, a, num_sms, s);
 }
 
 }  // namespace

@@ -46,6 +46,7 @@ constexpr int kCacheElems = 40960;
 constexpr int kCandCap = 4096;
 constexpr int kMaxCluster = 16;
 constexpr int kMinChunk = 4096;  // a row is not cut into chunks shorter than this
+constexpr int kBtCache = 1026;   // block-table entries of a chunk kept in shared memory (64K keys)
 
 struct TopkSmem {
     uint32_t cache[kCacheElems];
@@ -63,6 +64,7 @@ struct TopkSmem {
     uint32_t ncand;
     uint32_t range[2];
     uint32_t before[2];  // selected keys > T and == T in the lower-ranked chunks
+    int32_t bt_cache[kBtCache];  // page ids of this chunk's pages, when slots are written
     uint32_t hpub;       // histogram path: this CTA's slice total (read by the cluster)
     uint32_t hsel[2];    // histogram path: owner rank, the cluster's keys above its slice
     uint32_t hres[3];    // histogram path, owner: the bin, the cluster's keys above it / in it
@@ -228,12 +230,15 @@ __device__ void select_bin(TopkSmem &s, const uint32_t *cl, uint32_t need) {
 
 // Physical slot of position t of a request's block-table row (-1 and a status report when the
 // page id is outside the pool), the translation of slots.cu done where the selection is written.
-__device__ __forceinline__ int32_t slot_of(const TopkArgs &a, const int32_t *bt_row, int32_t t) {
+// Pages [pg0, pg0 + npg) come from the shared-memory copy of the chunk's entries.
+__device__ __forceinline__ int32_t slot_of(const TopkArgs &a, const int32_t *bt_row, const int32_t *bt_cache,
+                                           int pg0, int npg, int32_t t) {
     if (bt_row == nullptr) {
         report(a.status, DSA_ERR_BOUNDS);
         return -1;
     }
-    const int32_t page = bt_row[t / DSA_PAGE_SIZE];
+    const int pi = t / DSA_PAGE_SIZE;
+    const int32_t page = (pi - pg0 >= 0 && pi - pg0 < npg) ? bt_cache[pi - pg0] : bt_row[pi];
     if (page < 0 || page >= a.pool_pages) {
         report(a.status, DSA_ERR_BOUNDS);
         return -1;
@@ -241,6 +246,8 @@ __device__ __forceinline__ int32_t slot_of(const TopkArgs &a, const int32_t *bt_
     return page * DSA_PAGE_SIZE + t % DSA_PAGE_SIZE;
 }
 
+// kHist: start from the scorer's histogram (a.hist); kSlots: also write the slots (a.slots_out).
+template <bool kHist, bool kSlots>
 __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const TopkArgs a) {
     extern __shared__ uint8_t smem_raw[];
     TopkSmem &s = *reinterpret_cast<TopkSmem *>(smem_raw);
@@ -251,9 +258,9 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const TopkArgs a) {
     const int row = blockIdx.x / CL;
     const int k = a.k;
     int32_t *out = a.idx_out + static_cast<int64_t>(row) * k;
-    int32_t *sout = a.slots_out ? a.slots_out + static_cast<int64_t>(row) * k : nullptr;
+    int32_t *sout = kSlots ? a.slots_out + static_cast<int64_t>(row) * k : nullptr;
     const int32_t *bt_row = nullptr;  // this row's block-table row, when slots are wanted
-    if (sout) {
+    if constexpr (kSlots) {
         const int32_t req = a.row_req[row];
         if (req >= 0 && req < a.num_requests) bt_row = a.block_table + static_cast<int64_t>(req) * a.bt_stride;
     }
@@ -263,14 +270,14 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const TopkArgs a) {
         n = min(max(n, 0), a.max_ctx);
     }
     const int hspan = kHistBins / CL;  // histogram path: this CTA's slice of the row's bins
-    uint32_t *hrow = a.hist ? a.hist + static_cast<int64_t>(row) * kHistBins : nullptr;
+    uint32_t *hrow = kHist ? a.hist + static_cast<int64_t>(row) * kHistBins : nullptr;
     if (n <= k) {  // the same branch for every CTA of the cluster: no cluster barrier below
         if (crank == 0)
             for (int i = tid; i < k; i += kThreads) {
                 out[i] = i < n ? i : -1;
-                if (sout) sout[i] = i < n ? slot_of(a, bt_row, i) : -1;
+                if constexpr (kSlots) sout[i] = i < n ? slot_of(a, bt_row, nullptr, 0, 0, i) : -1;
             }
-        if (hrow)  // leave the scorer's histogram zeroed for the next call
+        if constexpr (kHist)  // leave the scorer's histogram zeroed for the next call
             for (int b = tid; b < hspan; b += kThreads) hrow[crank * hspan + b] = 0u;
         return;
     }
@@ -284,6 +291,12 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const TopkArgs a) {
         s.ncand = 0;
     }
     for (int b = tid; b < kBins; b += kThreads) s.hist[b] = 0;
+    // the chunk's block-table entries, read now so that writing slots at the end stays local
+    const int pg0 = c0 / DSA_PAGE_SIZE;
+    const int npg = (bt_row != nullptr && nloc > 0)
+                        ? min(kBtCache, (c0 + nloc - 1) / DSA_PAGE_SIZE - pg0 + 1)
+                        : 0;
+    for (int i = tid; i < npg; i += kThreads) s.bt_cache[i] = bt_row[pg0 + i];
     __syncthreads();
 
     uint32_t base = 0, top = 0;
@@ -292,7 +305,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const TopkArgs a) {
     uint32_t my_in = static_cast<uint32_t>(nloc);  // this chunk's keys inside it
     uint32_t hist_sc = 0xffffffffu;                // histogram path: the cluster's keys in [base, top]
     bool nan = false;
-    if (hrow) {
+    if constexpr (kHist) {
         // ---- 1h. the scorer's histogram of this row fixes the 16-bit bin of the k-th key.
         // CTA r scans bin slice r (its threads take `per` consecutive bins each, thread 0 the
         // slice's top ones), the cluster combines the slice totals from the highest slice
@@ -513,7 +526,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const TopkArgs a) {
     };
 
     bool gathered = false;
-    if (hrow && hist_sc <= static_cast<uint32_t>(kCandCap) && top > base) {
+    if (kHist && hist_sc <= static_cast<uint32_t>(kCandCap) && top > base) {
         publish_and_gather();  // the bin's candidates were collected in the first pass
         gathered = true;
     }
@@ -710,7 +723,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const TopkArgs a) {
                 const uint32_t pos = gb + min(eb, need);
                 if (pos < static_cast<uint32_t>(k)) {
                     out[pos] = c0 + i + q;
-                    if (sout) sout[pos] = slot_of(a, bt_row, c0 + i + q);
+                    if constexpr (kSlots) sout[pos] = slot_of(a, bt_row, s.bt_cache, pg0, npg, c0 + i + q);
                 } else {
                     report(a.status, DSA_ERR_BOUNDS);  // inconsistent counts: never expected
                 }
@@ -739,17 +752,16 @@ int cluster_size_for(const TopkArgs &a, int sms, int max16) {
     return cl;
 }
 
-}  // namespace
-
-cudaError_t launch_topk(const TopkArgs &a, cudaStream_t s) {
+template <bool kHist, bool kSlots>
+cudaError_t launch_variant(const TopkArgs &a, cudaStream_t s) {
     static ClusterLimits lim;
+    auto kern = topk_kernel<kHist, kSlots>;
     int dev = 0;
     cudaGetDevice(&dev);
     if (lim.device != dev) {
-        cudaError_t e =
-            cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, sizeof(TopkSmem));
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, sizeof(TopkSmem));
         if (e != cudaSuccess) return e;
-        e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
         int max16 = 0;
         if (e == cudaSuccess) {
             cudaLaunchConfig_t probe = {};
@@ -763,13 +775,12 @@ cudaError_t launch_topk(const TopkArgs &a, cudaStream_t s) {
             at[0].val.clusterDim.z = 1;
             probe.attrs = at;
             probe.numAttrs = 1;
-            if (cudaOccupancyMaxActiveClusters(&max16, topk_kernel, &probe) != cudaSuccess) max16 = 0;
+            if (cudaOccupancyMaxActiveClusters(&max16, kern, &probe) != cudaSuccess) max16 = 0;
         }
         cudaGetLastError();  // a refused cluster size only disables it
         lim.max16 = max16;
         lim.device = dev;
     }
-    if (a.num_rows == 0) return cudaSuccess;
     const int cl = cluster_size_for(a, device_sm_count(), lim.max16);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(a.num_rows * cl));
@@ -783,7 +794,18 @@ cudaError_t launch_topk(const TopkArgs &a, cudaStream_t s) {
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, topk_kernel, a);
+    return cudaLaunchKernelEx(&cfg, kern, a);
+}
+
+}  // namespace
+
+cudaError_t launch_topk(const TopkArgs &a, cudaStream_t s) {
+    if (a.num_rows == 0) return cudaSuccess;
+    const bool h = a.hist != nullptr, sl = a.slots_out != nullptr;
+    if (h && sl) return launch_variant<true, true>(a, s);
+    if (h) return launch_variant<true, false>(a, s);
+    if (sl) return launch_variant<false, true>(a, s);
+    return launch_variant<false, false>(a, s);
 }
 
 }  // namespace dsa
