@@ -7,8 +7,10 @@ its Python binding) never imports it and shares no code with it.
 The arithmetic lives in ``dsa_oracle.c`` (plain C, double precision, OpenMP
 over rows).  This module compiles it with gcc on first use and exposes thin
 numpy wrappers.  Source of every definition: the vLLM blog post "Day-0
-support for Kimi K3.1 Pro", section "Sparse attention in K3.1 Pro"; the
-formulas are restated in the header of ``dsa_oracle.c``.
+support for Kimi K3.1 Pro", section "Sparse attention in K3.1 Pro", and for
+the block-sparse variant the vLLM blog post "Day-0 support for
+MiniMax-M3.1-Flash", section "MSA primer"; the formulas are restated in
+``dsa_oracle.c``.
 """
 from __future__ import annotations
 
@@ -76,6 +78,18 @@ def load(path: str | None = None):
         lib.oracle_e2m1_encode.argtypes = [ctypes.c_float]
         lib.oracle_cache_insert.restype = I32
         lib.oracle_cache_insert.argtypes = [P, I32, P, I32, ctypes.c_float, I64, P, I32, P, P]
+        lib.oracle_msa_index_page_bytes.restype = I64
+        lib.oracle_msa_index_page_bytes.argtypes = []
+        lib.oracle_msa_kv_page_bytes.restype = I64
+        lib.oracle_msa_kv_page_bytes.argtypes = []
+        lib.oracle_msa_block_scores.restype = I32
+        lib.oracle_msa_block_scores.argtypes = [P, I64, P, I64, P, P, I32, P, P, I64]
+        lib.oracle_msa_select_f64.restype = I32
+        lib.oracle_msa_select_f64.argtypes = [P, I64, P, I32, P]
+        lib.oracle_msa_select_f32.restype = I32
+        lib.oracle_msa_select_f32.argtypes = [P, I64, P, I32, P]
+        lib.oracle_msa_attention.restype = I32
+        lib.oracle_msa_attention.argtypes = [P, I64, D, D, P, I64, P, P, I32, P, I32, P, D, P, P]
         lib.oracle_num_threads.restype = I32
         lib.oracle_set_num_threads.argtypes = [I32]
         if path is None:
@@ -205,6 +219,60 @@ def cache_insert(idx_pool, key_fmt, lat_pool, lat_fmt, tensor_scale, slots, keys
     if rc != OK:
         raise ValueError(f"oracle_cache_insert failed: {rc}")
     return ip, lp
+
+
+# ------------------------------------------------------------------ MSA
+
+MSA_GROUPS, MSA_BLOCKS, MSA_PAGE = 4, 16, 128
+
+
+def msa_block_scores(idx_pool, block_table, row_req, row_ctx, q_idx, lib=None):
+    """float64 block scores [R, 4, ceil(max(row_ctx) / 128)] (NaN past a row's blocks)."""
+    lib = lib or load()
+    pool = _c(idx_pool, np.uint8)
+    bt, rq, rc = _c(block_table, np.int32), _c(row_req, np.int32), _c(row_ctx, np.int32)
+    q = _c(q_idx, np.uint8)
+    R = rc.shape[0]
+    width = max((int(rc.max()) + MSA_PAGE - 1) // MSA_PAGE if R else 0, 1)
+    out = np.full((R, MSA_GROUPS, width), np.nan, dtype=np.float64)
+    num_pages = pool.size // lib.oracle_msa_index_page_bytes()
+    rcode = lib.oracle_msa_block_scores(_p(pool), num_pages, _p(bt), bt.shape[1], _p(rq), _p(rc), R, _p(q),
+                                        _p(out), width)
+    if rcode != OK:
+        raise ValueError(f"oracle_msa_block_scores failed: {rcode}")
+    return out
+
+
+def msa_select(scores, row_ctx, lib=None):
+    """Selected blocks int32 [R, 4, 16] from block scores [R, 4, W] (float32: decided in fp32)."""
+    lib = lib or load()
+    sc = np.asarray(scores)
+    fn = lib.oracle_msa_select_f32 if sc.dtype == np.float32 else lib.oracle_msa_select_f64
+    sc = _c(sc, np.float32 if sc.dtype == np.float32 else np.float64)
+    rc = _c(row_ctx, np.int32)
+    R = rc.shape[0]
+    out = np.empty((R, MSA_GROUPS, MSA_BLOCKS), dtype=np.int32)
+    fn(_p(sc), sc.shape[-1], _p(rc), R, _p(out))
+    return out
+
+
+def msa_attention(kv_pool, k_scale, v_scale, block_table, row_req, row_ctx, q_bf16_bits, blocks, sm_scale, lib=None):
+    """q_bf16_bits: uint16 [R, 4 * hpg, 128]; blocks: int32 [R, 4, 16].
+    Returns (out float64 [R, H, 128], lse float64 [R, H])."""
+    lib = lib or load()
+    pool = _c(kv_pool, np.uint8)
+    bt, rq, rc = _c(block_table, np.int32), _c(row_req, np.int32), _c(row_ctx, np.int32)
+    q, bl = _c(q_bf16_bits, np.uint16), _c(blocks, np.int32)
+    R, H, _ = q.shape
+    out = np.empty((R, H, 128), dtype=np.float64)
+    lse = np.empty((R, H), dtype=np.float64)
+    num_pages = pool.size // lib.oracle_msa_kv_page_bytes()
+    rcode = lib.oracle_msa_attention(_p(pool), num_pages, float(k_scale), float(v_scale), _p(bt), bt.shape[1],
+                                     _p(rq), _p(rc), R, _p(q), H // MSA_GROUPS, _p(bl), float(sm_scale), _p(out),
+                                     _p(lse))
+    if rcode != OK:
+        raise ValueError(f"oracle_msa_attention failed: {rcode}")
+    return out, lse
 
 
 def num_threads(lib=None) -> int:

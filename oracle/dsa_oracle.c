@@ -480,6 +480,202 @@ int oracle_cache_insert(uint8_t *idx_pool, int key_fmt, uint8_t *lat_pool, int l
     return err;
 }
 
+/* ------------------------------------------------- MSA (block-sparse variant)
+ *
+ * MiniMax sparse attention (vLLM blog "Day-0 support for MiniMax-M3.1-Flash",
+ * section "MSA primer", and its Fig. 1): the cache is cut into 128-token
+ * blocks; one index query per GQA group scores every visible key against the
+ * one index-key head all groups share; the scores are max-pooled to one score
+ * per block; each group's query heads then attend, exactly, to that group's
+ * selected blocks only: the most recent block always, plus the best of the
+ * others, at most 2,048 keys (16 blocks) in all.
+ *
+ *   score      s[r,g,t] = <qi[r,g,:], ki_t>                          t < L_r
+ *   block      S[r,g,b] = max of s[r,g,t] over t in [128b, 128b + 128), t < L_r
+ *              (a NaN score never wins; a block of NaNs scores -inf)
+ *   select     nb = ceil(L_r / 128).  nb <= 16: every block.  Otherwise block
+ *              nb - 1 and the 15 highest S among blocks 0 .. nb - 2, ties to
+ *              the lower block.  Listed ascending, -1 padded to 16.
+ *   attention  O[r,h,:] = sum_t softmax_t(sm_scale * <q[r,h,:], K_g,t>) V_g,t
+ *              over t < L_r in the selected blocks of group g = h / (H / 4)
+ *
+ * Byte layouts of one 128-token MSA page (the block is the page; the index
+ * key is 128 B/token and K/V are 4 KV heads x 128 dims in FP8, 1,024 B/token,
+ * as the page states; the arrangement inside a page is this library's reading):
+ *   index  [128 x 128 B e4m3]                                          16384 B
+ *   kv     [4 heads] x ([K: 128 x 128 B e4m3] [V: 128 x 128 B e4m3])  131072 B
+ * K and V codes are scaled by one per-tensor fp32 factor each (k_scale,
+ * v_scale); the index key has no scale (a positive factor would not change
+ * the selection).
+ */
+#define OR_MSA_PAGE 128
+#define OR_MSA_DIM 128
+#define OR_MSA_GROUPS 4
+#define OR_MSA_BLOCKS 16
+
+int64_t oracle_msa_index_page_bytes(void) { return (int64_t)OR_MSA_PAGE * OR_MSA_DIM; }
+
+int64_t oracle_msa_kv_page_bytes(void) { return (int64_t)OR_MSA_GROUPS * 2 * OR_MSA_PAGE * OR_MSA_DIM; }
+
+static int msa_num_blocks(int L) { return L > 0 ? (L + OR_MSA_PAGE - 1) / OR_MSA_PAGE : 0; }
+
+/* scores[(r * 4 + g) * stride + b] for b < ceil(L_r / 128); q_idx is
+ * [R, 4, 128] e4m3.  Returns OR_ERR_BOUNDS for a page id outside the pool. */
+int oracle_msa_block_scores(const uint8_t *idx_pool, int64_t num_pages, const int32_t *block_table,
+                            int64_t bt_stride, const int32_t *row_req, const int32_t *row_ctx, int num_rows,
+                            const uint8_t *q_idx, double *scores, int64_t stride) {
+    int err = OR_OK;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int r = 0; r < num_rows; ++r) {
+        double q[OR_MSA_GROUPS][OR_MSA_DIM];
+        for (int g = 0; g < OR_MSA_GROUPS; ++g)
+            for (int i = 0; i < OR_MSA_DIM; ++i)
+                q[g][i] = oracle_e4m3_decode(q_idx[((int64_t)r * OR_MSA_GROUPS + g) * OR_MSA_DIM + i]);
+        const int32_t *bt = block_table + (int64_t)row_req[r] * bt_stride;
+        const int L = row_ctx[r];
+        for (int b = 0; b < msa_num_blocks(L); ++b) {
+            double best[OR_MSA_GROUPS];
+            for (int g = 0; g < OR_MSA_GROUPS; ++g) best[g] = -INFINITY;
+            const int64_t page = bt[b];
+            if (page < 0 || page >= num_pages) {
+#pragma omp atomic write
+                err = OR_ERR_BOUNDS;
+            } else {
+                for (int t = b * OR_MSA_PAGE; t < L && t < (b + 1) * OR_MSA_PAGE; ++t) {
+                    const uint8_t *key = idx_pool + page * oracle_msa_index_page_bytes() +
+                                         (int64_t)(t % OR_MSA_PAGE) * OR_MSA_DIM;
+                    for (int g = 0; g < OR_MSA_GROUPS; ++g) {
+                        double dot = 0.0;
+                        for (int i = 0; i < OR_MSA_DIM; ++i) dot += q[g][i] * oracle_e4m3_decode(key[i]);
+                        if (dot > best[g]) best[g] = dot;
+                    }
+                }
+            }
+            for (int g = 0; g < OR_MSA_GROUPS; ++g) scores[((int64_t)r * OR_MSA_GROUPS + g) * stride + b] = best[g];
+        }
+    }
+    return err;
+}
+
+/* One (row, group): choose the blocks as the header states. */
+static void msa_select_one(const double *S, int nb, int32_t *out) {
+    int m = 0;
+    if (nb <= OR_MSA_BLOCKS) {
+        for (int b = 0; b < nb; ++b) out[m++] = b;
+    } else {
+        scored *buf = (scored *)malloc(sizeof(scored) * (size_t)(nb - 1));
+        for (int b = 0; b < nb - 1; ++b) {
+            buf[b].v = S[b] != S[b] ? -INFINITY : S[b];
+            buf[b].t = b;
+        }
+        qsort(buf, (size_t)(nb - 1), sizeof(scored), cmp_scored);
+        for (int i = 0; i < OR_MSA_BLOCKS - 1; ++i) out[m++] = buf[i].t;
+        out[m++] = nb - 1;
+        free(buf);
+        qsort(out, (size_t)m, sizeof(int32_t), cmp_i32);
+    }
+    for (int i = m; i < OR_MSA_BLOCKS; ++i) out[i] = -1;
+}
+
+/* blocks[(r * 4 + g) * 16 + i] from double block scores (end-to-end path). */
+int oracle_msa_select_f64(const double *scores, int64_t stride, const int32_t *row_ctx, int num_rows,
+                          int32_t *blocks) {
+    for (int r = 0; r < num_rows; ++r)
+        for (int g = 0; g < OR_MSA_GROUPS; ++g)
+            msa_select_one(scores + ((int64_t)r * OR_MSA_GROUPS + g) * stride, msa_num_blocks(row_ctx[r]),
+                           blocks + ((int64_t)r * OR_MSA_GROUPS + g) * OR_MSA_BLOCKS);
+    return OR_OK;
+}
+
+/* The same decision over fp32 block scores (the precision they are stored in). */
+int oracle_msa_select_f32(const float *scores, int64_t stride, const int32_t *row_ctx, int num_rows,
+                          int32_t *blocks) {
+    for (int r = 0; r < num_rows; ++r) {
+        const int nb = msa_num_blocks(row_ctx[r]);
+        double *S = (double *)malloc(sizeof(double) * (size_t)(nb > 0 ? nb : 1));
+        for (int g = 0; g < OR_MSA_GROUPS; ++g) {
+            for (int b = 0; b < nb; ++b) S[b] = (double)scores[((int64_t)r * OR_MSA_GROUPS + g) * stride + b];
+            msa_select_one(S, nb, blocks + ((int64_t)r * OR_MSA_GROUPS + g) * OR_MSA_BLOCKS);
+        }
+        free(S);
+    }
+    return OR_OK;
+}
+
+/* q: [R, 4 * hpg, 128] bf16 bits; blocks: [R, 4, 16] logical block ids (-1
+ * unused).  out: [R, 4 * hpg, 128], lse: [R, 4 * hpg] (natural log).  A head
+ * with no visible selected token gets out = 0, lse = -inf.  A block id at or
+ * past ceil(L_r / 128), or a page id outside the pool, is OR_ERR_BOUNDS. */
+int oracle_msa_attention(const uint8_t *kv_pool, int64_t num_pages, double k_scale, double v_scale,
+                         const int32_t *block_table, int64_t bt_stride, const int32_t *row_req,
+                         const int32_t *row_ctx, int num_rows, const uint16_t *q, int heads_per_group,
+                         const int32_t *blocks, double sm_scale, double *out, double *lse) {
+    if (heads_per_group <= 0) return OR_ERR_ARG;
+    const int H = OR_MSA_GROUPS * heads_per_group;
+    const int64_t head_bytes = 2 * OR_MSA_PAGE * OR_MSA_DIM;
+    int err = OR_OK;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int r = 0; r < num_rows; ++r) {
+        const int32_t *bt = block_table + (int64_t)row_req[r] * bt_stride;
+        const int L = row_ctx[r];
+        double *K = (double *)malloc(sizeof(double) * OR_MSA_BLOCKS * OR_MSA_PAGE * OR_MSA_DIM);
+        double *V = (double *)malloc(sizeof(double) * OR_MSA_BLOCKS * OR_MSA_PAGE * OR_MSA_DIM);
+        double *sc = (double *)malloc(sizeof(double) * OR_MSA_BLOCKS * OR_MSA_PAGE);
+        for (int g = 0; g < OR_MSA_GROUPS; ++g) {
+            const int32_t *bl = blocks + ((int64_t)r * OR_MSA_GROUPS + g) * OR_MSA_BLOCKS;
+            int n = 0;  /* gather the group's visible tokens, decoded */
+            for (int i = 0; i < OR_MSA_BLOCKS; ++i) {
+                const int b = bl[i];
+                if (b < 0) continue;
+                if (b >= msa_num_blocks(L) || bt[b] < 0 || bt[b] >= num_pages) {
+#pragma omp atomic write
+                    err = OR_ERR_BOUNDS;
+                    continue;
+                }
+                const uint8_t *kp = kv_pool + (int64_t)bt[b] * oracle_msa_kv_page_bytes() + g * head_bytes;
+                const uint8_t *vp = kp + OR_MSA_PAGE * OR_MSA_DIM;
+                for (int t = b * OR_MSA_PAGE; t < L && t < (b + 1) * OR_MSA_PAGE; ++t, ++n) {
+                    const int j = t % OR_MSA_PAGE;
+                    for (int d = 0; d < OR_MSA_DIM; ++d) {
+                        K[(int64_t)n * OR_MSA_DIM + d] = oracle_e4m3_decode(kp[j * OR_MSA_DIM + d]) * k_scale;
+                        V[(int64_t)n * OR_MSA_DIM + d] = oracle_e4m3_decode(vp[j * OR_MSA_DIM + d]) * v_scale;
+                    }
+                }
+            }
+            for (int hh = 0; hh < heads_per_group; ++hh) {
+                const int h = g * heads_per_group + hh;
+                double qh[OR_MSA_DIM];
+                for (int d = 0; d < OR_MSA_DIM; ++d) qh[d] = oracle_bf16_decode(q[((int64_t)r * H + h) * OR_MSA_DIM + d]);
+                double *o = out + ((int64_t)r * H + h) * OR_MSA_DIM;
+                for (int d = 0; d < OR_MSA_DIM; ++d) o[d] = 0.0;
+                if (n == 0) {
+                    lse[(int64_t)r * H + h] = -INFINITY;
+                    continue;
+                }
+                double m = -INFINITY;
+                for (int t = 0; t < n; ++t) {
+                    double s = 0.0;
+                    for (int d = 0; d < OR_MSA_DIM; ++d) s += qh[d] * K[(int64_t)t * OR_MSA_DIM + d];
+                    sc[t] = s * sm_scale;
+                    if (sc[t] > m) m = sc[t];
+                }
+                double l = 0.0;
+                for (int t = 0; t < n; ++t) {
+                    const double p = exp(sc[t] - m);
+                    l += p;
+                    for (int d = 0; d < OR_MSA_DIM; ++d) o[d] += p * V[(int64_t)t * OR_MSA_DIM + d];
+                }
+                for (int d = 0; d < OR_MSA_DIM; ++d) o[d] = o[d] / l;
+                lse[(int64_t)r * H + h] = m + log(l);
+            }
+        }
+        free(K);
+        free(V);
+        free(sc);
+    }
+    return err;
+}
+
 /* ------------------------------------------------------------------- misc */
 
 int oracle_num_threads(void) {

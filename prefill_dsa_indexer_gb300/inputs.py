@@ -209,9 +209,9 @@ def _gen(device, seed: int) -> torch.Generator:
     return g
 
 
-def _paging(wl: Workload):
+def _paging(wl, page: int = PAGE):
     rng = np.random.default_rng(wl.seed * 7 + 1)
-    npages = [(L + PAGE - 1) // PAGE for L in wl.ctx]
+    npages = [(L + page - 1) // page for L in wl.ctx]
     used = sum(npages)
     total = used + max(1, int(used * wl.extra_pages))
     perm = rng.permutation(total).astype(np.int32)
@@ -327,3 +327,132 @@ def small_workload(name: str, ctx: list[int], rows_per_req: int = 1, rows_per_gr
                    seed: int = 7, extra_pages: float = 0.5) -> Workload:
     """An ad-hoc workload for tests (edge cases, ragged tails)."""
     return Workload(name, list(ctx), rows_per_req, rows_per_group, key_fmt, lat_fmt, k, heads, seed, extra_pages)
+
+
+# ------------------------------------------------------------------ MSA
+#
+# The block-sparse variant (vLLM blog "Day-0 support for MiniMax-M3.1-Flash",
+# section "MSA primer"): 128-token blocks, which are also the cache pages; one
+# shared index-key head of 128 FP8 values per token (128 B, no scale); K and V
+# of 4 KV heads x 128 dims in FP8 with one per-tensor scale each (1,024 B per
+# token); one FP8 index query per GQA group; bf16 attention queries,
+# heads_per_group of them per group.  Values are N(0,1) before encoding.
+
+MSA_PAGE, MSA_DIM, MSA_GROUPS, MSA_BLOCKS = 128, 128, 4, 16
+MSA_INDEX_PAGE_BYTES = MSA_PAGE * MSA_DIM
+MSA_KV_PAGE_BYTES = MSA_GROUPS * 2 * MSA_PAGE * MSA_DIM
+
+
+@dataclass
+class MsaWorkload:
+    name: str
+    ctx: list[int]
+    rows_per_req: int
+    rows_per_group: int
+    heads_per_group: int = 16
+    seed: int = 0
+    extra_pages: float = 0.25
+
+    @property
+    def num_rows(self) -> int:
+        return len(self.ctx) * self.rows_per_req
+
+    def row_ctx(self) -> np.ndarray:
+        n = self.rows_per_req
+        return np.asarray([L - n + 1 + i for L in self.ctx for i in range(n)], dtype=np.int32)
+
+    def row_req(self) -> np.ndarray:
+        return np.repeat(np.arange(len(self.ctx), dtype=np.int32), self.rows_per_req)
+
+
+def msa_workload(name: str) -> MsaWorkload:
+    if name == "msa_decode_tiny_4k":
+        return MsaWorkload(name, [4096], 1, 1, seed=1100, extra_pages=1.0)
+    if name == "msa_decode_b8_128k":
+        return MsaWorkload(name, [131072] * 8, 1, 1, seed=1101)
+    if name == "msa_verify_b4_64k":
+        return MsaWorkload(name, [65536] * 4, 8, 8, seed=1102)
+    if name == "msa_decode_b32_16k_64k":
+        return MsaWorkload(name, _ctx_uniform(1103, 32, 16384, 65536), 1, 1, seed=1103)
+    raise KeyError(name)
+
+
+MSA_WORKLOADS = ("msa_decode_tiny_4k", "msa_decode_b8_128k", "msa_verify_b4_64k", "msa_decode_b32_16k_64k")
+
+
+@dataclass
+class MsaInputs:
+    wl: MsaWorkload
+    idx_pool: torch.Tensor        # uint8 [num_pages, 16384]
+    kv_pool: torch.Tensor         # uint8 [num_pages, 131072]
+    k_scale: float
+    v_scale: float
+    block_table: torch.Tensor     # int32 [B, max_pages] (128-token pages)
+    row_req: torch.Tensor         # int32 [R]
+    row_ctx: torch.Tensor         # int32 [R]
+    q_idx: torch.Tensor           # uint8 [R, 4, 128] e4m3 codes
+    q: torch.Tensor               # int16 [R, 4 * heads_per_group, 128] bf16 bits
+
+    @property
+    def max_ctx(self) -> int:
+        return max(self.wl.ctx)
+
+    def np(self, name: str) -> np.ndarray:
+        t = getattr(self, name)
+        return t.cpu().numpy().view(np.uint16) if name == "q" else t.cpu().numpy()
+
+    def to(self, device) -> "MsaInputs":
+        mv = {n: getattr(self, n).to(device) for n in
+              ("idx_pool", "kv_pool", "block_table", "row_req", "row_ctx", "q_idx", "q")}
+        return MsaInputs(self.wl, k_scale=self.k_scale, v_scale=self.v_scale, **mv)
+
+
+def make_msa_inputs(wl: MsaWorkload, device="cpu", chunk_tokens: int = 1 << 16) -> MsaInputs:
+    device = torch.device(device)
+    bt_np, num_pages = _paging(wl, MSA_PAGE)
+    slots = []
+    for b, L in enumerate(wl.ctx):
+        t = np.arange(L, dtype=np.int64)
+        slots.append(bt_np[b, t // MSA_PAGE].astype(np.int64) * MSA_PAGE + t % MSA_PAGE)
+    slots = torch.from_numpy(np.concatenate(slots)).to(device)
+    T = slots.numel()
+    pg, j = slots // MSA_PAGE, slots % MSA_PAGE
+
+    idx_pool = torch.full((num_pages, MSA_INDEX_PAGE_BYTES), 0x7F, dtype=torch.uint8, device=device)
+    idx_v = idx_pool.view(num_pages, MSA_PAGE, MSA_DIM)
+    gk = _gen(device, wl.seed * 100 + 1)
+    for s0 in range(0, T, chunk_tokens):
+        s1 = min(T, s0 + chunk_tokens)
+        idx_v[pg[s0:s1], j[s0:s1]] = e4m3_codes(torch.randn((s1 - s0, MSA_DIM), generator=gk, device=device))
+
+    # K and V: per-tensor scale = amax / 448 over the used tokens (pass 1 records
+    # amax, pass 2 redraws the same stream and encodes)
+    kv_pool = torch.full((num_pages, MSA_KV_PAGE_BYTES), 0x7F, dtype=torch.uint8, device=device)
+    kv_v = kv_pool.view(num_pages, MSA_GROUPS, 2, MSA_PAGE, MSA_DIM)
+    amax = torch.zeros(2, device=device)
+    gv = _gen(device, wl.seed * 100 + 2)
+    for s0 in range(0, T, chunk_tokens):
+        s1 = min(T, s0 + chunk_tokens)
+        x = torch.randn((s1 - s0, MSA_GROUPS, 2, MSA_DIM), generator=gv, device=device)
+        amax = torch.maximum(amax, x.abs().amax(dim=(0, 1, 3)))
+    k_scale, v_scale = (float(a) / 448.0 if float(a) > 0 else 1.0 for a in amax.tolist())
+    scale = torch.tensor([k_scale, v_scale], device=device).view(1, 1, 2, 1)
+    gv = _gen(device, wl.seed * 100 + 2)
+    for s0 in range(0, T, chunk_tokens):
+        s1 = min(T, s0 + chunk_tokens)
+        x = torch.randn((s1 - s0, MSA_GROUPS, 2, MSA_DIM), generator=gv, device=device)
+        kv_v[pg[s0:s1], :, :, j[s0:s1]] = e4m3_codes(x / scale)
+
+    R = wl.num_rows
+    gq = _gen(device, wl.seed * 100 + 3)
+    q_idx = e4m3_codes(torch.randn((R, MSA_GROUPS, MSA_DIM), generator=gq, device=device))
+    q = torch.randn((R, MSA_GROUPS * wl.heads_per_group, MSA_DIM), generator=gq, device=device).to(
+        torch.bfloat16).view(torch.int16)
+    return MsaInputs(wl, idx_pool, kv_pool, k_scale, v_scale, torch.from_numpy(bt_np).to(device),
+                     torch.from_numpy(wl.row_req()).to(device), torch.from_numpy(wl.row_ctx()).to(device), q_idx, q)
+
+
+def small_msa_workload(name: str, ctx: list[int], rows_per_req: int = 1, rows_per_group: int = 1,
+                       heads_per_group: int = 16, seed: int = 7, extra_pages: float = 0.5) -> MsaWorkload:
+    """An ad-hoc MSA workload for tests."""
+    return MsaWorkload(name, list(ctx), rows_per_req, rows_per_group, heads_per_group, seed, extra_pages)

@@ -430,6 +430,183 @@ def pin_cache_insert(lib):
             assert np.array_equal(kv[:, 512:], wantr), "NVFP4 RoPE dims"
 
 
+# ------------------------------------------------------------------ MSA
+#
+# The block-sparse variant (vLLM blog "Day-0 support for MiniMax-M3.1-Flash",
+# section "MSA primer"): block scores against numpy brute force, the block
+# selection against the properties that make it unique, attention against
+# numpy softmax and torch's grouped-query scaled_dot_product_attention.
+
+def _msa_inputs(ctx=(300, 2200), rows=2, hpg=4, seed=5):
+    wl = I.small_msa_workload("pin", list(ctx), rows_per_req=rows, rows_per_group=rows, heads_per_group=hpg,
+                              seed=seed)
+    return I.make_msa_inputs(wl)
+
+
+def _msa_slots(bt, req, L):
+    t = np.arange(L, dtype=np.int64)
+    return bt[req, t // 128].astype(np.int64) * 128 + t % 128
+
+
+def ref_msa_keys(idx_pool, slots):
+    return ref_e4m3(np.asarray(idx_pool).reshape(-1, 128, 128)[slots // 128, slots % 128])
+
+
+def ref_msa_kv(kv_pool, slots, g, which):
+    return ref_e4m3(np.asarray(kv_pool).reshape(-1, 4, 2, 128, 128)[slots // 128, g, which, slots % 128])
+
+
+def pin_msa_block_scores(lib):
+    inp = _msa_inputs()
+    pool, bt, rq, rc, qi = (inp.np(n) for n in ("idx_pool", "block_table", "row_req", "row_ctx", "q_idx"))
+    # a key just past row 0's causal edge (visible to row 1 only) that would win its block
+    edge = int(_msa_slots(bt, rq[1], rc[1])[-1])
+    pool = pool.copy()
+    pool.reshape(-1, 128, 128)[edge // 128, edge % 128] = np.where(ref_e4m3(qi[1, 0]) > 0, 0x7E, 0xFE)
+    got = oracle.msa_block_scores(pool, bt, rq, rc, qi, lib=lib)
+    for r in range(len(rc)):
+        L = int(rc[r])
+        k = ref_msa_keys(pool, _msa_slots(bt, rq[r], L))
+        s = ref_e4m3(qi[r]) @ k.T                      # [4, L]
+        nb = (L + 127) // 128
+        pad = np.full((4, nb * 128), -np.inf)
+        pad[:, :L] = s
+        want = pad.reshape(4, nb, 128).max(axis=-1)
+        assert np.allclose(got[r, :, :nb], want, rtol=1e-13, atol=0), "MSA block scores"
+        assert np.all(np.isnan(got[r, :, nb:])), "MSA blocks past the context"
+    assert got[1, 0, 2] > 1e4 and got[0, 0, 2] < 1e3, "MSA causal edge"
+    # paging invariance: the same tokens on other pages score the same
+    perm = np.random.default_rng(1).permutation(pool.shape[0])
+    pool2 = np.empty_like(pool)
+    pool2[perm] = pool
+    got2 = oracle.msa_block_scores(pool2, perm[bt].astype(np.int32), rq, rc, qi, lib=lib)
+    assert np.array_equal(np.nan_to_num(got, nan=7.0), np.nan_to_num(got2, nan=7.0)), "MSA paging"
+
+
+def _check_msa_selection(S, nb, sel):
+    """The selection is the unique list with these properties."""
+    sel = [int(b) for b in sel]
+    chosen = [b for b in sel if b >= 0]
+    assert sel[len(chosen):] == [-1] * (16 - len(chosen)), "MSA -1 padding"
+    assert chosen == sorted(set(chosen)), "MSA ascending, distinct"
+    assert len(chosen) == min(nb, 16), "MSA block count"
+    if nb == 0:
+        return
+    assert chosen[-1] == nb - 1, "MSA recent block kept"
+    key = lambda b: (-(S[b] if S[b] == S[b] else -np.inf), b)
+    order = np.lexsort((np.arange(nb - 1), [key(b)[0] for b in range(nb - 1)]))
+    assert sorted(chosen[:-1]) == sorted(int(b) for b in order[:len(chosen) - 1]), "MSA best others"
+    others = set(chosen[:-1])
+    for u in range(nb - 1):
+        if u in others:
+            continue
+        for c in others:
+            assert key(c) < key(u), "MSA dominance"
+
+
+def pin_msa_select(lib):
+    rng = np.random.default_rng(9)
+    cases = [0, 1, 5, 16, 17, 18, 40, 129]
+    R = len(cases)
+    W = max(cases)
+    S = rng.integers(0, 6, size=(R, 4, W)).astype(np.float64)  # many ties
+    S[3, 1, :] = 2.0                                             # all equal
+    S[5, 2, 16] = -50.0                                          # recent block scores worst
+    S[6, 0, 7] = np.nan                                          # a NaN never beats a number
+    row_ctx = np.array([c * 128 - (c % 3) * 40 if c else 0 for c in cases], dtype=np.int32)
+    nbs = [(int(L) + 127) // 128 for L in row_ctx]
+    for dt in (np.float64, np.float32):
+        sel = oracle.msa_select(S.astype(dt), row_ctx, lib=lib)
+        for r in range(R):
+            for g in range(4):
+                _check_msa_selection(S[r, g], nbs[r], sel[r, g])
+    assert 7 not in oracle.msa_select(S, row_ctx, lib=lib)[6, 0], "MSA NaN block"
+
+
+def _msa_dense(inp, r, blocks, sm_scale):
+    """numpy softmax attention of row r over its selected blocks."""
+    bt, rq, rc = inp.np("block_table"), inp.np("row_req"), inp.np("row_ctx")
+    q = ref_bf16(inp.np("q")[r])
+    H = q.shape[0]
+    hpg = H // 4
+    L = int(rc[r])
+    out, lse = np.zeros((H, 128)), np.full(H, -np.inf)
+    for g in range(4):
+        t = np.concatenate([np.arange(b * 128, min(b * 128 + 128, L)) for b in blocks[g] if b >= 0] or
+                           [np.zeros(0, np.int64)])
+        if t.size == 0:
+            continue
+        sl = bt[rq[r], t // 128].astype(np.int64) * 128 + t % 128
+        K = ref_msa_kv(inp.kv_pool.numpy(), sl, g, 0) * inp.k_scale
+        V = ref_msa_kv(inp.kv_pool.numpy(), sl, g, 1) * inp.v_scale
+        s = sm_scale * (q[g * hpg:(g + 1) * hpg] @ K.T)
+        m = s.max(axis=1, keepdims=True)
+        p = np.exp(s - m)
+        out[g * hpg:(g + 1) * hpg] = (p @ V) / p.sum(axis=1, keepdims=True)
+        lse[g * hpg:(g + 1) * hpg] = m[:, 0] + np.log(p.sum(axis=1))
+    return out, lse
+
+
+def pin_msa_attention(lib):
+    inp = _msa_inputs(ctx=(300, 2200), rows=2, hpg=4)
+    rc = inp.np("row_ctx")
+    sc = oracle.msa_block_scores(inp.np("idx_pool"), inp.np("block_table"), inp.np("row_req"), rc,
+                                 inp.np("q_idx"), lib=lib)
+    blocks = oracle.msa_select(sc, rc, lib=lib)
+    blocks[3, 2, :] = -1                                  # an empty group
+    sm = 128 ** -0.5
+    out, lse = oracle.msa_attention(inp.np("kv_pool"), inp.k_scale, inp.v_scale, inp.np("block_table"),
+                                    inp.np("row_req"), rc, inp.np("q"), blocks, sm, lib=lib)
+    for r in range(len(rc)):
+        o, l = _msa_dense(inp, r, blocks[r], sm)
+        assert np.allclose(out[r], o, rtol=1e-10, atol=1e-12) and np.allclose(lse[r], l, rtol=1e-12), "MSA attention"
+    assert np.all(out[3, 8:12] == 0) and np.all(np.isneginf(lse[3, 8:12])), "MSA empty group"
+
+
+def pin_msa_full_selection_is_gqa_attention(lib):
+    """nb <= 16: every block is selected, so MSA is dense causal grouped-query
+    attention, as torch computes it (head h reads KV head h // (H / 4))."""
+    inp = _msa_inputs(ctx=(700, 2048), rows=3, hpg=4, seed=8)
+    rc, H = inp.np("row_ctx"), inp.q.shape[1]
+    blocks = np.full((len(rc), 4, 16), -1, np.int32)
+    for r, L in enumerate(rc):
+        blocks[r, :, :(L + 127) // 128] = np.arange((L + 127) // 128)
+    sm = 0.09
+    out, lse = oracle.msa_attention(inp.np("kv_pool"), inp.k_scale, inp.v_scale, inp.np("block_table"),
+                                    inp.np("row_req"), rc, inp.np("q"), blocks, sm, lib=lib)
+    bt, rq = inp.np("block_table"), inp.np("row_req")
+    for r, L in enumerate(rc):
+        sl = _msa_slots(bt, rq[r], int(L))
+        K = np.stack([ref_msa_kv(inp.kv_pool.numpy(), sl, g, 0) for g in range(4)]) * inp.k_scale
+        V = np.stack([ref_msa_kv(inp.kv_pool.numpy(), sl, g, 1) for g in range(4)]) * inp.v_scale
+        q = torch.from_numpy(ref_bf16(inp.np("q")[r]))[None, :, None, :]
+        want = torch.nn.functional.scaled_dot_product_attention(
+            q, torch.from_numpy(K)[None], torch.from_numpy(V)[None], scale=sm, enable_gqa=True)[0, :, 0]
+        assert np.allclose(out[r], want.numpy(), rtol=1e-9, atol=1e-12), "MSA = dense GQA attention"
+    assert out.shape[1] == H
+
+
+def pin_msa_closed_forms(lib):
+    inp = _msa_inputs(ctx=(1, 900), rows=1, hpg=2, seed=4)
+    rc = inp.np("row_ctx")
+    q0 = np.zeros_like(inp.np("q"))                      # equal scores -> mean of V, lse = log n
+    blocks = np.full((2, 4, 16), -1, np.int32)
+    blocks[0, :, 0] = 0
+    blocks[1, :, :3] = [0, 4, 7]
+    out, lse = oracle.msa_attention(inp.np("kv_pool"), inp.k_scale, inp.v_scale, inp.np("block_table"),
+                                    inp.np("row_req"), rc, q0, blocks, 0.1, lib=lib)
+    bt, rq = inp.np("block_table"), inp.np("row_req")
+    t1 = np.concatenate([np.arange(0, 128), np.arange(512, 640), np.arange(896, 900)])
+    for g in range(4):
+        v0 = ref_msa_kv(inp.kv_pool.numpy(), _msa_slots(bt, rq[0], 1), g, 1)[0] * inp.v_scale
+        assert np.allclose(out[0, 2 * g:2 * g + 2], v0, rtol=1e-13, atol=0), "MSA single token = its value"
+        sl = bt[rq[1], t1 // 128].astype(np.int64) * 128 + t1 % 128
+        vm = ref_msa_kv(inp.kv_pool.numpy(), sl, g, 1).mean(axis=0) * inp.v_scale
+        assert np.allclose(out[1, 2 * g:2 * g + 2], vm, rtol=1e-11, atol=1e-14), "MSA equal scores = mean"
+    assert np.allclose(lse[1], np.log(len(t1)), rtol=1e-13), "MSA lse of equal scores"
+    assert np.allclose(lse[0], 0.0, atol=1e-15), "MSA lse of one token"
+
+
 ALL_PINS = {
     "e4m3": pin_e4m3,
     "e2m1": pin_e2m1,
@@ -450,4 +627,9 @@ ALL_PINS = {
     "e4m3_encode": pin_e4m3_encode,
     "e2m1_encode": pin_e2m1_encode,
     "cache_insert": pin_cache_insert,
+    "msa_block_scores": pin_msa_block_scores,
+    "msa_select": pin_msa_select,
+    "msa_attention": pin_msa_attention,
+    "msa_full_selection": pin_msa_full_selection_is_gqa_attention,
+    "msa_closed_forms": pin_msa_closed_forms,
 }

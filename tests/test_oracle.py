@@ -63,6 +63,23 @@ MUTATIONS = [
     ("FP8 key scale over 240", "float sc = amax > 0.0f ? amax / 448.0f : 1.0f;", "float sc = amax > 0.0f ? amax / 240.0f : 1.0f;"),
     ("MX exponent offset", "E = (e - 1) - 2 + 127;", "E = (e - 1) - 1 + 127;"),
     ("NVFP4 scale over 4", "uint8_t scode = oracle_e4m3_encode(amax / 6.0f);", "uint8_t scode = oracle_e4m3_encode(amax / 4.0f);"),
+    ("MSA block score keeps the last key", "if (dot > best[g]) best[g] = dot;", "best[g] = dot;"),
+    ("MSA block score past the causal edge", "for (int t = b * OR_MSA_PAGE; t < L && t < (b + 1) * OR_MSA_PAGE; ++t) {\n                    const uint8_t *key",
+     "for (int t = b * OR_MSA_PAGE; t <= L && t < (b + 1) * OR_MSA_PAGE; ++t) {\n                    const uint8_t *key"),
+    ("MSA index key row of a 64-token page", "(int64_t)(t % OR_MSA_PAGE) * OR_MSA_DIM;", "(int64_t)(t % 64) * OR_MSA_DIM;"),
+    ("MSA recent block not forced", "out[m++] = nb - 1;", "out[m++] = buf[OR_MSA_BLOCKS - 1].t;"),
+    ("MSA 16 best others, recent dropped", "for (int i = 0; i < OR_MSA_BLOCKS - 1; ++i) out[m++] = buf[i].t;\n        out[m++] = nb - 1;",
+     "for (int i = 0; i < OR_MSA_BLOCKS; ++i) out[m++] = buf[i].t;"),
+    ("MSA head groups interleaved", "const int h = g * heads_per_group + hh;", "const int h = hh * OR_MSA_GROUPS + g;"),
+    ("MSA value read from K", "V[(int64_t)n * OR_MSA_DIM + d] = oracle_e4m3_decode(vp[j * OR_MSA_DIM + d]) * v_scale;",
+     "V[(int64_t)n * OR_MSA_DIM + d] = oracle_e4m3_decode(kp[j * OR_MSA_DIM + d]) * v_scale;"),
+    ("MSA key scale dropped", "K[(int64_t)n * OR_MSA_DIM + d] = oracle_e4m3_decode(kp[j * OR_MSA_DIM + d]) * k_scale;",
+     "K[(int64_t)n * OR_MSA_DIM + d] = oracle_e4m3_decode(kp[j * OR_MSA_DIM + d]);"),
+    ("MSA V of the next head", "const uint8_t *vp = kp + OR_MSA_PAGE * OR_MSA_DIM;", "const uint8_t *vp = kp + 2 * OR_MSA_PAGE * OR_MSA_DIM;"),
+    ("MSA attention past the causal edge", "for (int t = b * OR_MSA_PAGE; t < L && t < (b + 1) * OR_MSA_PAGE; ++t, ++n) {",
+     "for (int t = b * OR_MSA_PAGE; t < (b + 1) * OR_MSA_PAGE; ++t, ++n) {"),
+    ("MSA softmax scale dropped", "sc[t] = s * sm_scale;", "sc[t] = s;"),
+    ("MSA output not normalised", "o[d] = o[d] / l;", "o[d] = o[d] / 1.0;"),
     ("insert nibble order", "codes[(16 * b + d) / 2] = (uint8_t)(lo | (hi << 4));", "codes[(16 * b + d) / 2] = (uint8_t)(hi | (lo << 4));"),
 ]
 
