@@ -89,7 +89,7 @@ def load(path: str | None = None):
         lib.oracle_msa_select_f32.restype = I32
         lib.oracle_msa_select_f32.argtypes = [P, I64, P, I32, P]
         lib.oracle_msa_attention.restype = I32
-        lib.oracle_msa_attention.argtypes = [P, I64, D, D, P, I64, P, P, I32, P, I32, P, D, P, P]
+        lib.oracle_msa_attention.argtypes = [P, I64, D, D, P, I64, P, P, I32, P, D, I32, P, D, P, P]
         lib.oracle_num_threads.restype = I32
         lib.oracle_set_num_threads.argtypes = [I32]
         if path is None:
@@ -256,19 +256,21 @@ def msa_select(scores, row_ctx, lib=None):
     return out
 
 
-def msa_attention(kv_pool, k_scale, v_scale, block_table, row_req, row_ctx, q_bf16_bits, blocks, sm_scale, lib=None):
-    """q_bf16_bits: uint16 [R, 4 * hpg, 128]; blocks: int32 [R, 4, 16].
+def msa_attention(kv_pool, k_scale, v_scale, block_table, row_req, row_ctx, q_codes, q_scale, blocks, sm_scale,
+                  lib=None):
+    """q_codes: uint8 e4m3 [R, 4 * hpg, 128] (times q_scale); blocks: int32 [R, 4, 16].
     Returns (out float64 [R, H, 128], lse float64 [R, H])."""
     lib = lib or load()
     pool = _c(kv_pool, np.uint8)
     bt, rq, rc = _c(block_table, np.int32), _c(row_req, np.int32), _c(row_ctx, np.int32)
-    q, bl = _c(q_bf16_bits, np.uint16), _c(blocks, np.int32)
+    q, bl = _c(q_codes, np.uint8), _c(blocks, np.int32)
     R, H, _ = q.shape
     out = np.empty((R, H, 128), dtype=np.float64)
     lse = np.empty((R, H), dtype=np.float64)
     num_pages = pool.size // lib.oracle_msa_kv_page_bytes()
     rcode = lib.oracle_msa_attention(_p(pool), num_pages, float(k_scale), float(v_scale), _p(bt), bt.shape[1],
-                                     _p(rq), _p(rc), R, _p(q), H // MSA_GROUPS, _p(bl), float(sm_scale), _p(out),
+                                     _p(rq), _p(rc), R, _p(q), float(q_scale), H // MSA_GROUPS, _p(bl),
+                                     float(sm_scale), _p(out),
                                      _p(lse))
     if rcode != OK:
         raise ValueError(f"oracle_msa_attention failed: {rcode}")

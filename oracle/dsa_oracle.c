@@ -497,7 +497,9 @@ int oracle_cache_insert(uint8_t *idx_pool, int key_fmt, uint8_t *lat_pool, int l
  *              nb - 1 and the 15 highest S among blocks 0 .. nb - 2, ties to
  *              the lower block.  Listed ascending, -1 padded to 16.
  *   attention  O[r,h,:] = sum_t softmax_t(sm_scale * <q[r,h,:], K_g,t>) V_g,t
- *              over t < L_r in the selected blocks of group g = h / (H / 4)
+ *              over t < L_r in the selected blocks of group g = h / (H / 4);
+ *              the query stays in FP8 (section "Blackwell-optimised MSA
+ *              kernels"): e4m3 codes times one per-tensor fp32 scale
  *
  * Byte layouts of one 128-token MSA page (the block is the page; the index
  * key is 128 B/token and K/V are 4 KV heads x 128 dims in FP8, 1,024 B/token,
@@ -602,13 +604,13 @@ int oracle_msa_select_f32(const float *scores, int64_t stride, const int32_t *ro
     return OR_OK;
 }
 
-/* q: [R, 4 * hpg, 128] bf16 bits; blocks: [R, 4, 16] logical block ids (-1
+/* q: [R, 4 * hpg, 128] e4m3 codes (times q_scale); blocks: [R, 4, 16] logical block ids (-1
  * unused).  out: [R, 4 * hpg, 128], lse: [R, 4 * hpg] (natural log).  A head
  * with no visible selected token gets out = 0, lse = -inf.  A block id at or
  * past ceil(L_r / 128), or a page id outside the pool, is OR_ERR_BOUNDS. */
 int oracle_msa_attention(const uint8_t *kv_pool, int64_t num_pages, double k_scale, double v_scale,
                          const int32_t *block_table, int64_t bt_stride, const int32_t *row_req,
-                         const int32_t *row_ctx, int num_rows, const uint16_t *q, int heads_per_group,
+                         const int32_t *row_ctx, int num_rows, const uint8_t *q, double q_scale, int heads_per_group,
                          const int32_t *blocks, double sm_scale, double *out, double *lse) {
     if (heads_per_group <= 0) return OR_ERR_ARG;
     const int H = OR_MSA_GROUPS * heads_per_group;
@@ -645,7 +647,7 @@ int oracle_msa_attention(const uint8_t *kv_pool, int64_t num_pages, double k_sca
             for (int hh = 0; hh < heads_per_group; ++hh) {
                 const int h = g * heads_per_group + hh;
                 double qh[OR_MSA_DIM];
-                for (int d = 0; d < OR_MSA_DIM; ++d) qh[d] = oracle_bf16_decode(q[((int64_t)r * H + h) * OR_MSA_DIM + d]);
+                for (int d = 0; d < OR_MSA_DIM; ++d) qh[d] = oracle_e4m3_decode(q[((int64_t)r * H + h) * OR_MSA_DIM + d]) * q_scale;
                 double *o = out + ((int64_t)r * H + h) * OR_MSA_DIM;
                 for (int d = 0; d < OR_MSA_DIM; ++d) o[d] = 0.0;
                 if (n == 0) {

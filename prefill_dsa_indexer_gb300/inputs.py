@@ -335,8 +335,10 @@ def small_workload(name: str, ctx: list[int], rows_per_req: int = 1, rows_per_gr
 # section "MSA primer"): 128-token blocks, which are also the cache pages; one
 # shared index-key head of 128 FP8 values per token (128 B, no scale); K and V
 # of 4 KV heads x 128 dims in FP8 with one per-tensor scale each (1,024 B per
-# token); one FP8 index query per GQA group; bf16 attention queries,
-# heads_per_group of them per group.  Values are N(0,1) before encoding.
+# token); one FP8 index query per GQA group; FP8 attention queries with one
+# per-tensor scale (section "Blackwell-optimised MSA kernels": the queries stay
+# FP8), heads_per_group of them per group.  Values are N(0,1) before encoding;
+# per-tensor scales are amax / 448.
 
 MSA_PAGE, MSA_DIM, MSA_GROUPS, MSA_BLOCKS = 128, 128, 4, 16
 MSA_INDEX_PAGE_BYTES = MSA_PAGE * MSA_DIM
@@ -391,7 +393,8 @@ class MsaInputs:
     row_req: torch.Tensor         # int32 [R]
     row_ctx: torch.Tensor         # int32 [R]
     q_idx: torch.Tensor           # uint8 [R, 4, 128] e4m3 codes
-    q: torch.Tensor               # int16 [R, 4 * heads_per_group, 128] bf16 bits
+    q: torch.Tensor               # uint8 [R, 4 * heads_per_group, 128] e4m3 codes (times q_scale)
+    q_scale: float
 
     @property
     def max_ctx(self) -> int:
@@ -399,12 +402,12 @@ class MsaInputs:
 
     def np(self, name: str) -> np.ndarray:
         t = getattr(self, name)
-        return t.cpu().numpy().view(np.uint16) if name == "q" else t.cpu().numpy()
+        return t.cpu().numpy()
 
     def to(self, device) -> "MsaInputs":
         mv = {n: getattr(self, n).to(device) for n in
               ("idx_pool", "kv_pool", "block_table", "row_req", "row_ctx", "q_idx", "q")}
-        return MsaInputs(self.wl, k_scale=self.k_scale, v_scale=self.v_scale, **mv)
+        return MsaInputs(self.wl, k_scale=self.k_scale, v_scale=self.v_scale, q_scale=self.q_scale, **mv)
 
 
 def make_msa_inputs(wl: MsaWorkload, device="cpu", chunk_tokens: int = 1 << 16) -> MsaInputs:
@@ -446,10 +449,13 @@ def make_msa_inputs(wl: MsaWorkload, device="cpu", chunk_tokens: int = 1 << 16) 
     R = wl.num_rows
     gq = _gen(device, wl.seed * 100 + 3)
     q_idx = e4m3_codes(torch.randn((R, MSA_GROUPS, MSA_DIM), generator=gq, device=device))
-    q = torch.randn((R, MSA_GROUPS * wl.heads_per_group, MSA_DIM), generator=gq, device=device).to(
-        torch.bfloat16).view(torch.int16)
+    x = torch.randn((R, MSA_GROUPS * wl.heads_per_group, MSA_DIM), generator=gq, device=device)
+    am = float(x.abs().amax()) if x.numel() else 0.0
+    q_scale = am / 448.0 if am > 0 else 1.0
+    q = e4m3_codes(x / q_scale)
     return MsaInputs(wl, idx_pool, kv_pool, k_scale, v_scale, torch.from_numpy(bt_np).to(device),
-                     torch.from_numpy(wl.row_req()).to(device), torch.from_numpy(wl.row_ctx()).to(device), q_idx, q)
+                     torch.from_numpy(wl.row_req()).to(device), torch.from_numpy(wl.row_ctx()).to(device), q_idx, q,
+                     q_scale)
 
 
 def small_msa_workload(name: str, ctx: list[int], rows_per_req: int = 1, rows_per_group: int = 1,

@@ -526,7 +526,7 @@ def pin_msa_select(lib):
 def _msa_dense(inp, r, blocks, sm_scale):
     """numpy softmax attention of row r over its selected blocks."""
     bt, rq, rc = inp.np("block_table"), inp.np("row_req"), inp.np("row_ctx")
-    q = ref_bf16(inp.np("q")[r])
+    q = ref_e4m3(inp.np("q")[r]) * inp.q_scale
     H = q.shape[0]
     hpg = H // 4
     L = int(rc[r])
@@ -556,7 +556,7 @@ def pin_msa_attention(lib):
     blocks[3, 2, :] = -1                                  # an empty group
     sm = 128 ** -0.5
     out, lse = oracle.msa_attention(inp.np("kv_pool"), inp.k_scale, inp.v_scale, inp.np("block_table"),
-                                    inp.np("row_req"), rc, inp.np("q"), blocks, sm, lib=lib)
+                                    inp.np("row_req"), rc, inp.np("q"), inp.q_scale, blocks, sm, lib=lib)
     for r in range(len(rc)):
         o, l = _msa_dense(inp, r, blocks[r], sm)
         assert np.allclose(out[r], o, rtol=1e-10, atol=1e-12) and np.allclose(lse[r], l, rtol=1e-12), "MSA attention"
@@ -573,13 +573,13 @@ def pin_msa_full_selection_is_gqa_attention(lib):
         blocks[r, :, :(L + 127) // 128] = np.arange((L + 127) // 128)
     sm = 0.09
     out, lse = oracle.msa_attention(inp.np("kv_pool"), inp.k_scale, inp.v_scale, inp.np("block_table"),
-                                    inp.np("row_req"), rc, inp.np("q"), blocks, sm, lib=lib)
+                                    inp.np("row_req"), rc, inp.np("q"), inp.q_scale, blocks, sm, lib=lib)
     bt, rq = inp.np("block_table"), inp.np("row_req")
     for r, L in enumerate(rc):
         sl = _msa_slots(bt, rq[r], int(L))
         K = np.stack([ref_msa_kv(inp.kv_pool.numpy(), sl, g, 0) for g in range(4)]) * inp.k_scale
         V = np.stack([ref_msa_kv(inp.kv_pool.numpy(), sl, g, 1) for g in range(4)]) * inp.v_scale
-        q = torch.from_numpy(ref_bf16(inp.np("q")[r]))[None, :, None, :]
+        q = torch.from_numpy(ref_e4m3(inp.np("q")[r]) * inp.q_scale)[None, :, None, :]
         want = torch.nn.functional.scaled_dot_product_attention(
             q, torch.from_numpy(K)[None], torch.from_numpy(V)[None], scale=sm, enable_gqa=True)[0, :, 0]
         assert np.allclose(out[r], want.numpy(), rtol=1e-9, atol=1e-12), "MSA = dense GQA attention"
@@ -594,7 +594,7 @@ def pin_msa_closed_forms(lib):
     blocks[0, :, 0] = 0
     blocks[1, :, :3] = [0, 4, 7]
     out, lse = oracle.msa_attention(inp.np("kv_pool"), inp.k_scale, inp.v_scale, inp.np("block_table"),
-                                    inp.np("row_req"), rc, q0, blocks, 0.1, lib=lib)
+                                    inp.np("row_req"), rc, q0, inp.q_scale, blocks, 0.1, lib=lib)
     bt, rq = inp.np("block_table"), inp.np("row_req")
     t1 = np.concatenate([np.arange(0, 128), np.arange(512, 640), np.arange(896, 900)])
     for g in range(4):

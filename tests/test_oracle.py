@@ -73,6 +73,8 @@ MUTATIONS = [
     ("MSA head groups interleaved", "const int h = g * heads_per_group + hh;", "const int h = hh * OR_MSA_GROUPS + g;"),
     ("MSA value read from K", "V[(int64_t)n * OR_MSA_DIM + d] = oracle_e4m3_decode(vp[j * OR_MSA_DIM + d]) * v_scale;",
      "V[(int64_t)n * OR_MSA_DIM + d] = oracle_e4m3_decode(kp[j * OR_MSA_DIM + d]) * v_scale;"),
+    ("MSA query scale dropped", "oracle_e4m3_decode(q[((int64_t)r * H + h) * OR_MSA_DIM + d]) * q_scale;",
+     "oracle_e4m3_decode(q[((int64_t)r * H + h) * OR_MSA_DIM + d]);"),
     ("MSA key scale dropped", "K[(int64_t)n * OR_MSA_DIM + d] = oracle_e4m3_decode(kp[j * OR_MSA_DIM + d]) * k_scale;",
      "K[(int64_t)n * OR_MSA_DIM + d] = oracle_e4m3_decode(kp[j * OR_MSA_DIM + d]);"),
     ("MSA V of the next head", "const uint8_t *vp = kp + OR_MSA_PAGE * OR_MSA_DIM;", "const uint8_t *vp = kp + 2 * OR_MSA_PAGE * OR_MSA_DIM;"),
