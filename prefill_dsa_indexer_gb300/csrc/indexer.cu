@@ -20,11 +20,13 @@
 //     ring of up to 8 TMEM accumulators, so the MMA runs ahead of the
 //     read-out; a group's G rows (speculative-verify rows or a prefill query
 //     block) share every key read;
-//   * 8 epilogue warps read one key lane each from TMEM (two sets of four
-//     taking alternate tiles, or for G = 8 splitting a tile's rows), so the
-//     head reduction sum_h w_h * relu(acc_h) runs in registers, scale by s_t
-//     (s_t > 0 commutes with the relu), mask t >= L_r and write coalesced
-//     fp32 logits; the warps that read a tile also release its stage.
+//   * epilogue warps read one key lane each from TMEM, so the head reduction
+//     sum_h w_h * relu(acc_h) runs in registers, scale by s_t (s_t > 0
+//     commutes with the relu), mask t >= L_r and write coalesced fp32
+//     logits; the warps that read a tile also release its stage.  Decode and
+//     verify use two sets of four warps on alternate tiles; prefill (G = 8),
+//     where the head reduction costs as much as the MMA, uses 16 warps of
+//     two rows each, packed fp32x2 FMAs, and per-warp waits and releases.
 #include "indexer_common.cuh"
 
 namespace dsa {
@@ -34,6 +36,29 @@ namespace {
 constexpr int kIdxPageBytes = DSA_PAGE_SIZE * (DSA_INDEX_DIM + 4);  // 8448
 constexpr int kIdxPageRows = kIdxPageBytes / 128;                    // 66 rows of 128 B
 
+// sum_h w[h] * max(0, acc[h]) over the 32 indexer heads of one (row, key), with packed
+// two-wide fp32 FMAs (the weights are a shared-memory broadcast, 16-byte aligned).  Half of the
+// ReLUs are a max (integer/ALU pipe) and half are x + |x| = 2 max(0, x), exact, on the FMA
+// pipe; those terms are halved at the end (exact), which balances the two pipes.
+__device__ __forceinline__ float head_relu_sum(const uint32_t (&acc)[32], const float *w) {
+    float2 a0 = make_float2(0.f, 0.f), a1 = a0, b0 = a0, b1 = a0;
+    auto rl = [&](int h) { return fmaxf(__uint_as_float(acc[h]), 0.f); };
+    auto r2 = [&](int h) {
+        const float x = __uint_as_float(acc[h]);
+        return x + fabsf(x);
+    };
+#pragma unroll
+    for (int h = 0; h < 32; h += 8) {
+        const float4 wa = *reinterpret_cast<const float4 *>(w + h);
+        const float4 wb = *reinterpret_cast<const float4 *>(w + h + 4);
+        a0 = __ffma2_rn(make_float2(wa.x, wa.y), make_float2(rl(h), rl(h + 1)), a0);
+        b0 = __ffma2_rn(make_float2(wa.z, wa.w), make_float2(r2(h + 2), r2(h + 3)), b0);
+        a1 = __ffma2_rn(make_float2(wb.x, wb.y), make_float2(rl(h + 4), rl(h + 5)), a1);
+        b1 = __ffma2_rn(make_float2(wb.z, wb.w), make_float2(r2(h + 6), r2(h + 7)), b1);
+    }
+    return fmaf(0.5f, (b0.x + b0.y) + (b1.x + b1.y), (a0.x + a0.y) + (a1.x + a1.y));
+}
+
 template <int G>
 struct IdxCfg {
     static constexpr int N = 32 * G;
@@ -42,14 +67,22 @@ struct IdxCfg {
     static constexpr int kTileKeys = G >= 8 ? 128 : 256;
     static constexpr int kPagesPerTile = kTileKeys / DSA_PAGE_SIZE;
     static constexpr int kHalves = kTileKeys / 128;
-    // Epilogue: 8 warps.  G = 8 splits a tile's rows over two sets of 4 warps; smaller G lets
-    // two sets of 4 warps take alternate tiles, so one tile's TMEM read-out overlaps the next.
-    static constexpr int kEpiSplit = G >= 8 ? 2 : 1;
+    // Epilogue.  G < 8 (decode, verify): two sets of 4 warps take alternate tiles, so one
+    // tile's TMEM read-out overlaps the next; one thread of a set waits and named barriers pass
+    // the acquire and the release on.  G = 8 (prefill, tensor-bound): the head reduction is as
+    // much work as the MMA, so 16 warps split a tile's rows (two rows per warp, four warps per
+    // TMEM lane quadrant) and each warp waits for and releases a tile by itself.
+    static constexpr bool kWarpSync = G >= 8;
+    static constexpr int kEpiSplit = G >= 8 ? 4 : 1;
     static constexpr int kEpiGroups = G >= 8 ? 1 : 2;
     static constexpr int kWarpsPerTile = 4 * kEpiSplit;
     static constexpr int kEpiWarps = kWarpsPerTile * kEpiGroups;
     static constexpr int kRowsPerEpiWarp = G / kEpiSplit;
     static constexpr int kThreads = 128 + 32 * kEpiWarps;
+    // arrivals that release a stage or an accumulator
+    static constexpr uint32_t kRelease = kWarpSync ? kWarpsPerTile : 1;
+    // head weights in shared memory: per set, two groups' worth (G < 8); per warp, its own rows
+    static constexpr int kWFloats = kWarpSync ? kEpiWarps * kRowsPerEpiWarp * 32 : kEpiGroups * 2 * N;
     // TMEM accumulators (kHalves x N columns each): enough that the MMA runs several tiles ahead
     static constexpr int kAccCols = kHalves * N;
     static constexpr int kAcc = (512 / kAccCols) < 8 ? (512 / kAccCols) : 8;
@@ -59,7 +92,7 @@ struct IdxCfg {
     static constexpr int kNumBarsFor(int st) { return 2 * st + 2 * kAcc + 5; }
     // shared memory for `st` key stages (layout below)
     static constexpr int smem_for(int st) {
-        return st * kKeyBytes + 2 * kQBytes + st * kTileKeys * 4 + kEpiGroups * 2 * N * 4 +
+        return st * kKeyBytes + 2 * kQBytes + st * kTileKeys * 4 + kWFloats * 4 +
                (kIndexerMaxGroups + 4) * 4 + 2 * kIndexerMaxGroups * 4 + kNumBarsFor(st) * 8 + 64 + 1024;
     }
     // as many key stages as fit (up to 12 x 128 keys)
@@ -73,7 +106,7 @@ struct IdxCfg {
     static constexpr int OFF_Q = OFF_KEYS + kStages * kKeyBytes;
     static constexpr int OFF_SCALES = OFF_Q + 2 * kQBytes;
     static constexpr int OFF_W = OFF_SCALES + kStages * kTileKeys * 4;
-    static constexpr int OFF_PREFIX = OFF_W + kEpiGroups * 2 * N * 4;
+    static constexpr int OFF_PREFIX = OFF_W + kWFloats * 4;
     static constexpr int OFF_GREQ = OFF_PREFIX + (kIndexerMaxGroups + 4) * 4;
     static constexpr int OFF_GMAX = OFF_GREQ + kIndexerMaxGroups * 4;
     static constexpr int OFF_BARS = OFF_GMAX + kIndexerMaxGroups * 4;
@@ -122,13 +155,13 @@ __global__ void __launch_bounds__(IdxCfg<G>::kThreads, 1)
         *abort = 0;
         for (int s = 0; s < C::kStages; ++s) {
             mbar_init(&full[s], 1);
-            // the epilogue set that read a tile releases its stage: it saw the MMA's
-            // completion (so the keys are consumed) and has read the scales
-            mbar_init(&empty[s], 1);
+            // the epilogue set (or each of its warps) that read a tile releases its stage: it
+            // saw the MMA's completion (so the keys are consumed) and has read the scales
+            mbar_init(&empty[s], C::kRelease);
         }
         for (int i = 0; i < C::kAcc; ++i) {
             mbar_init(&tfull[i], 1);
-            mbar_init(&tempty[i], 1);
+            mbar_init(&tempty[i], C::kRelease);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&qfull[i], 1);
@@ -287,6 +320,77 @@ __global__ void __launch_bounds__(IdxCfg<G>::kThreads, 1)
             }
             mma_commit(mma_done);
             mbar_wait(mma_done, 0, abort, a.status);
+        } else if (warp >= 4 && C::kWarpSync) {
+          if constexpr (C::kWarpSync) {
+            // ------------------------------------------------ epilogue, one warp = two rows of a tile
+            // Each warp waits for a tile by itself, reads its rows' accumulator columns, releases
+            // the accumulator and the stage at once (so the MMA two tiles ahead can start), and
+            // only then reduces the heads.
+            const int e = warp - 4;
+            const int quad = warp & 3;  // TMEM lane quadrant this warp may read
+            const int rbeg = (e >> 2) * C::kRowsPerEpiWarp;
+            const int key_lane = quad * 32 + lane;
+            float *wp = wbuf + e * (C::kRowsPerEpiWarp * 32);  // this warp's rows' head weights
+            TileWalker wk{prefix, 0};
+            wk.seek(w_begin, ng);
+            int cur = -1;
+            int ctx[C::kRowsPerEpiWarp];
+            int64_t row_off[C::kRowsPerEpiWarp];
+            int hrow[C::kRowsPerEpiWarp];  // global row of each of this warp's rows
+            int32_t it = 0;
+            for (int32_t w = w_begin; w < w_end; ++w, ++it) {
+                wk.advance(w);
+                const int g = wk.g;
+                if (g != cur) {
+                    cur = g;
+                    const int row0 = (a.group0 + g) * G + rbeg;
+                    __syncwarp();  // every lane is done with the previous group's weights
+#pragma unroll
+                    for (int j = 0; j < C::kRowsPerEpiWarp; ++j) {
+                        wp[j * 32 + lane] = a.head_w[static_cast<int64_t>(row0 + j) * DSA_INDEX_HEADS + lane];
+                        ctx[j] = min(a.row_ctx[row0 + j], a.max_ctx);
+                        row_off[j] = static_cast<int64_t>(row0 + j) * a.logits_stride;
+                        hrow[j] = row0 + j;
+                    }
+                    __syncwarp();
+                }
+                const int stage = it % C::kStages, b = it % C::kAcc;
+                // lane 0 waits for the accumulator and for the stage (its bulk-copied scales); the
+                // stage cannot be re-armed before every warp of the tile has released it
+                int ok = 1;
+                if (lane == 0)
+                    ok = mbar_wait(&tfull[b], (it / C::kAcc) & 1, abort, a.status) &&
+                         mbar_wait(&full[stage], (it / C::kStages) & 1, abort, a.status);
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                __syncwarp();
+                if (!ok) break;
+                tc_fence_after();
+                uint32_t acc[C::kRowsPerEpiWarp][32];
+#pragma unroll
+                for (int j = 0; j < C::kRowsPerEpiWarp; ++j)
+                    tmem_ld32(tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + b * C::kAccCols + (rbeg + j) * 32, acc[j]);
+                tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < C::kRowsPerEpiWarp; ++j) reg_fence(acc[j]);
+                const float s_t = scales[stage * C::kTileKeys + key_lane];
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(&empty[stage]);
+                    mbar_arrive(&tempty[b]);
+                }
+                const int t = (w - prefix[g]) * C::kTileKeys + key_lane;
+#pragma unroll
+                for (int j = 0; j < C::kRowsPerEpiWarp; ++j) {
+                    const float v = head_relu_sum(acc[j], wp + j * 32) * s_t;
+                    if (t < ctx[j]) {
+                        a.logits[row_off[j] + t] = v;
+                        if constexpr (kHist)
+                            atomicAdd(a.hist + static_cast<int64_t>(hrow[j]) * kHistBins + (order_key(v) >> 16), 1u);
+                    }
+                }
+            }
+          }
         } else if (warp >= 4) {
             // ------------------------------------------------ epilogue
             const int e = warp - 4;
