@@ -9,24 +9,25 @@
 // Design (GB300): the scan over all cached index keys is the dominant HBM
 // stream of the layer (132 B per token per row group), so the kernel is a
 // persistent, key-balanced pipeline:
-//   * work = (row group g, 128-key tile); the tiles of all groups form one
-//     list that is split evenly over one CTA per SM (the blog's scorer is
-//     "key-balanced" too, section "Low-latency decode");
-//   * warp 0 streams key tiles with TMA (two 64-token pages -> one 128-row,
-//     128-byte-swizzled operand) plus the pages' fp32 scales into a ring of
+//   * work = (row group g, key tile of 256 keys, 128 for prefill); the tiles
+//     of all groups form one list that is split evenly over the CTAs (the
+//     blog's scorer is "key-balanced" too, section "Low-latency decode").
+//     Decode runs two CTAs per SM: one CTA's bulk-copy stream alone stays
+//     below the SM's share of HBM bandwidth;
+//   * warp 0 streams key tiles with TMA (one 64-row, 128-byte-swizzled box
+//     per 64-token page) plus the pages' fp32 scales into a ring of
 //     shared-memory stages;
 //   * warp 1 issues tcgen05.mma kind::f8f6f4 (e4m3 x e4m3 -> fp32) with the
 //     KEYS on M = 128 and the group's G rows x 32 heads on N, K = 128, into a
-//     ring of up to 8 TMEM accumulators, so the MMA runs ahead of the
-//     read-out; a group's G rows (speculative-verify rows or a prefill query
-//     block) share every key read;
-//   * epilogue warps read one key lane each from TMEM, so the head reduction
-//     sum_h w_h * relu(acc_h) runs in registers, scale by s_t (s_t > 0
-//     commutes with the relu), mask t >= L_r and write coalesced fp32
-//     logits; the warps that read a tile also release its stage.  Decode and
-//     verify use two sets of four warps on alternate tiles; prefill (G = 8),
-//     where the head reduction costs as much as the MMA, uses 16 warps of
-//     two rows each, packed fp32x2 FMAs, and per-warp waits and releases.
+//     ring of TMEM accumulators, so the MMA runs ahead of the read-out; a
+//     group's G rows (speculative-verify rows or a prefill query block) share
+//     every key read;
+//   * 4, 8 or 16 epilogue warps read one key lane each from TMEM, two
+//     32-column items per warp and tile; each warp waits for its tile, reads
+//     both items, releases the stage and the accumulator at once, and only
+//     then reduces sum_h w_h * relu(acc_h) in registers (packed fp32x2 FMAs),
+//     scales by s_t (s_t > 0 commutes with the relu), masks t >= L_r and
+//     writes coalesced fp32 logits.
 #include "indexer_common.cuh"
 
 namespace dsa {
@@ -62,67 +63,76 @@ __device__ __forceinline__ float head_relu_sum(const uint32_t (&acc)[32], const 
 template <int G>
 struct IdxCfg {
     static constexpr int N = 32 * G;
+    // Decode (G <= 2) streams every key from HBM with a light epilogue: two CTAs share each SM,
+    // because one CTA's bulk-copy stream tops out below the SM's share of HBM bandwidth however
+    // many stages it keeps in flight.  Each CTA then gets half of the TMEM and of the shared
+    // memory.  Verify (G = 4) and prefill (G = 8) need more epilogue warps, registers and TMEM
+    // per key: one CTA per SM.
+    static constexpr int kCtasPerSm = G <= 2 ? 2 : 1;
+    static constexpr int kMaxGroups = kCtasPerSm == 2 ? 256 : kIndexerMaxGroups;  // groups per launch
+    static constexpr int kSmemBudget = kCtasPerSm == 2 ? 228 * 1024 / 2 - 1024 : 227 * 1024;
     // keys per tile: 256 (four pages, two M = 128 products) halves every per-tile cost of the
     // pipeline for decode and verify; prefill's N = 256 accumulators keep 128-key tiles
     static constexpr int kTileKeys = G >= 8 ? 128 : 256;
     static constexpr int kPagesPerTile = kTileKeys / DSA_PAGE_SIZE;
     static constexpr int kHalves = kTileKeys / 128;
-    // Epilogue.  G < 8 (decode, verify): two sets of 4 warps take alternate tiles, so one
-    // tile's TMEM read-out overlaps the next; one thread of a set waits and named barriers pass
-    // the acquire and the release on.  G = 8 (prefill, tensor-bound): the head reduction is as
-    // much work as the MMA, so 16 warps split a tile's rows (two rows per warp, four warps per
-    // TMEM lane quadrant) and each warp waits for and releases a tile by itself.
-    static constexpr bool kWarpSync = G >= 8;
-    static constexpr int kEpiSplit = G >= 8 ? 4 : 1;
-    static constexpr int kEpiGroups = G >= 8 ? 1 : 2;
-    static constexpr int kWarpsPerTile = 4 * kEpiSplit;
-    static constexpr int kEpiWarps = kWarpsPerTile * kEpiGroups;
+    // query buffers: two, so the next group's query loads during this group's last tiles, except
+    // where a second one would cost a key stage (G = 4 at two CTAs per SM; few groups per CTA)
+    static constexpr int kQBufs = (G == 4 && kCtasPerSm == 2) ? 1 : 2;
+    // Epilogue: kEpiSplit warps per TMEM lane quadrant split the group's rows, so that every
+    // warp reads exactly two 32-column items of a tile (two rows, or one row over two 128-key
+    // halves).  Each warp waits for a tile by itself, reads both items, releases the accumulator
+    // and the stage at once (so the MMA can run ahead) and only then reduces the heads.
+    static constexpr int kEpiSplit = G * (kTileKeys / 128) / 2;
+    static constexpr int kEpiWarps = 4 * kEpiSplit;
     static constexpr int kRowsPerEpiWarp = G / kEpiSplit;
     static constexpr int kThreads = 128 + 32 * kEpiWarps;
-    // arrivals that release a stage or an accumulator
-    static constexpr uint32_t kRelease = kWarpSync ? kWarpsPerTile : 1;
-    // head weights in shared memory: per set, two groups' worth (G < 8); per warp, its own rows
-    static constexpr int kWFloats = kWarpSync ? kEpiWarps * kRowsPerEpiWarp * 32 : kEpiGroups * 2 * N;
+    // arrivals that release a stage or an accumulator: one per epilogue warp
+    static constexpr uint32_t kRelease = kEpiWarps;
+    // head weights in shared memory, per warp: its own rows
+    static constexpr int kWFloats = kEpiWarps * kRowsPerEpiWarp * 32;
     // TMEM accumulators (kHalves x N columns each): enough that the MMA runs several tiles ahead
     static constexpr int kAccCols = kHalves * N;
-    static constexpr int kAcc = (512 / kAccCols) < 8 ? (512 / kAccCols) : 8;
+    static constexpr int kTmemBudget = 512 / kCtasPerSm;
+    static constexpr int kAcc = (kTmemBudget / kAccCols) < 8 ? (kTmemBudget / kAccCols) : 8;
     static constexpr uint32_t kTmemCols = static_cast<uint32_t>(kAcc * kAccCols);
     static constexpr int kKeyBytes = kTileKeys * 128;
     static constexpr int kQBytes = N * 128;
     static constexpr int kNumBarsFor(int st) { return 2 * st + 2 * kAcc + 5; }
     // shared memory for `st` key stages (layout below)
     static constexpr int smem_for(int st) {
-        return st * kKeyBytes + 2 * kQBytes + st * kTileKeys * 4 + kWFloats * 4 +
-               (kIndexerMaxGroups + 4) * 4 + 2 * kIndexerMaxGroups * 4 + kNumBarsFor(st) * 8 + 64 + 1024;
+        return st * kKeyBytes + kQBufs * kQBytes + st * kTileKeys * 4 + kWFloats * 4 + (kMaxGroups + 4) * 4 +
+               2 * kMaxGroups * 4 + kNumBarsFor(st) * 8 + 64 + 1024;
     }
     // as many key stages as fit (up to 12 x 128 keys)
     static constexpr int pick_stages() {
         int st = 12 / kHalves;
-        while (smem_for(st) > 227 * 1024) --st;
+        while (smem_for(st) > kSmemBudget) --st;
         return st;
     }
     static constexpr int kStages = pick_stages();
     static constexpr int OFF_KEYS = 0;
     static constexpr int OFF_Q = OFF_KEYS + kStages * kKeyBytes;
-    static constexpr int OFF_SCALES = OFF_Q + 2 * kQBytes;
+    static constexpr int OFF_SCALES = OFF_Q + kQBufs * kQBytes;
     static constexpr int OFF_W = OFF_SCALES + kStages * kTileKeys * 4;
     static constexpr int OFF_PREFIX = OFF_W + kWFloats * 4;
-    static constexpr int OFF_GREQ = OFF_PREFIX + (kIndexerMaxGroups + 4) * 4;
-    static constexpr int OFF_GMAX = OFF_GREQ + kIndexerMaxGroups * 4;
-    static constexpr int OFF_BARS = OFF_GMAX + kIndexerMaxGroups * 4;
+    static constexpr int OFF_GREQ = OFF_PREFIX + (kMaxGroups + 4) * 4;
+    static constexpr int OFF_GMAX = OFF_GREQ + kMaxGroups * 4;
+    static constexpr int OFF_BARS = OFF_GMAX + kMaxGroups * 4;
     static constexpr int kNumBars = kNumBarsFor(kStages);
     static constexpr int OFF_MISC = OFF_BARS + kNumBars * 8;
     static constexpr int kSmemBytes = OFF_MISC + 64 + 1024;  // + slack for 1024-byte alignment
     static_assert(kTmemCols == 32 || kTmemCols == 64 || kTmemCols == 128 || kTmemCols == 256 ||
                       kTmemCols == 512,
                   "TMEM allocation must be a power of two >= 32");
-    static_assert(kAcc % kEpiGroups == 0, "an accumulator always belongs to the same epilogue set");
-    static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+    static_assert(kHalves * kRowsPerEpiWarp == 2, "two TMEM items per epilogue warp and tile");
+    static_assert(kSmemBytes <= kSmemBudget, "shared memory budget");
+    static_assert(kTmemCols <= static_cast<uint32_t>(kTmemBudget), "TMEM budget of a CTA");
     static_assert(kSmemBytes == smem_for(kStages), "stage sizing matches the layout");
 };
 
 template <int G, bool kHist>
-__global__ void __launch_bounds__(IdxCfg<G>::kThreads, 1)
+__global__ void __launch_bounds__(IdxCfg<G>::kThreads, IdxCfg<G>::kCtasPerSm)
     indexer_fp8_kernel(const __grid_constant__ CUtensorMap key_map, const __grid_constant__ CUtensorMap q_map,
                        const IndexerArgs a) {
     using C = IdxCfg<G>;
@@ -145,7 +155,6 @@ __global__ void __launch_bounds__(IdxCfg<G>::kThreads, 1)
     uint64_t *mma_done = qempty + 2;             // [1] all MMAs retired
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
     volatile int *abort = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 4);
-    volatile int *epi_ok = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 8);  // [2]
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int ng = a.num_groups;
@@ -242,9 +251,10 @@ __global__ void __launch_bounds__(IdxCfg<G>::kThreads, 1)
                     if (g != cur) {
                         ++gc;
                         cur = g;
-                        const int qb = gc & 1;
+                        const int qb = gc % C::kQBufs;
                         int got = 0;
-                        if (lane == 0) got = mbar_wait(&qempty[qb], ((gc >> 1) & 1) ^ 1, abort, a.status);
+                        if (lane == 0)
+                            got = mbar_wait(&qempty[qb], ((gc / C::kQBufs) & 1) ^ 1, abort, a.status);
                         if (!__shfl_sync(0xffffffffu, got, 0)) {
                             ok = false;
                             break;
@@ -293,9 +303,9 @@ __global__ void __launch_bounds__(IdxCfg<G>::kThreads, 1)
                 if (g != cur) {
                     ++gc;
                     cur = g;
-                    if (!mbar_wait(&qfull[gc & 1], (gc >> 1) & 1, abort, a.status)) break;
+                    if (!mbar_wait(&qfull[gc % C::kQBufs], (gc / C::kQBufs) & 1, abort, a.status)) break;
                 }
-                const int qb = gc & 1;
+                const int qb = gc % C::kQBufs;
                 const int stage = it % C::kStages, b = it % C::kAcc;
                 if (!mbar_wait(&tempty[b], ((it / C::kAcc) & 1) ^ 1, abort, a.status)) break;
                 if (!mbar_wait(&full[stage], (it / C::kStages) & 1, abort, a.status)) break;
@@ -320,23 +330,20 @@ __global__ void __launch_bounds__(IdxCfg<G>::kThreads, 1)
             }
             mma_commit(mma_done);
             mbar_wait(mma_done, 0, abort, a.status);
-        } else if (warp >= 4 && C::kWarpSync) {
-          if constexpr (C::kWarpSync) {
-            // ------------------------------------------------ epilogue, one warp = two rows of a tile
-            // Each warp waits for a tile by itself, reads its rows' accumulator columns, releases
-            // the accumulator and the stage at once (so the MMA two tiles ahead can start), and
-            // only then reduces the heads.
+        } else if (warp >= 4) {
+            // ------------------------------------------------ epilogue: two TMEM items per warp and tile
+            constexpr int R = C::kRowsPerEpiWarp;
             const int e = warp - 4;
             const int quad = warp & 3;  // TMEM lane quadrant this warp may read
-            const int rbeg = (e >> 2) * C::kRowsPerEpiWarp;
+            const int rbeg = (e >> 2) * R;
             const int key_lane = quad * 32 + lane;
-            float *wp = wbuf + e * (C::kRowsPerEpiWarp * 32);  // this warp's rows' head weights
+            float *wp = wbuf + e * (R * 32);  // this warp's rows' head weights
             TileWalker wk{prefix, 0};
             wk.seek(w_begin, ng);
             int cur = -1;
-            int ctx[C::kRowsPerEpiWarp];
-            int64_t row_off[C::kRowsPerEpiWarp];
-            int hrow[C::kRowsPerEpiWarp];  // global row of each of this warp's rows
+            int ctx[R];
+            int64_t row_off[R];
+            int hrow[R];  // global row of each of this warp's rows
             int32_t it = 0;
             for (int32_t w = w_begin; w < w_end; ++w, ++it) {
                 wk.advance(w);
@@ -346,7 +353,7 @@ __global__ void __launch_bounds__(IdxCfg<G>::kThreads, 1)
                     const int row0 = (a.group0 + g) * G + rbeg;
                     __syncwarp();  // every lane is done with the previous group's weights
 #pragma unroll
-                    for (int j = 0; j < C::kRowsPerEpiWarp; ++j) {
+                    for (int j = 0; j < R; ++j) {
                         wp[j * 32 + lane] = a.head_w[static_cast<int64_t>(row0 + j) * DSA_INDEX_HEADS + lane];
                         ctx[j] = min(a.row_ctx[row0 + j], a.max_ctx);
                         row_off[j] = static_cast<int64_t>(row0 + j) * a.logits_stride;
@@ -365,111 +372,37 @@ __global__ void __launch_bounds__(IdxCfg<G>::kThreads, 1)
                 __syncwarp();
                 if (!ok) break;
                 tc_fence_after();
-                uint32_t acc[C::kRowsPerEpiWarp][32];
+                // item k: half k / R of the tile, row k % R of this warp.  A half past the
+                // context's end was neither loaded nor computed; its lanes are never stored.
+                uint32_t acc[2][32];
 #pragma unroll
-                for (int j = 0; j < C::kRowsPerEpiWarp; ++j)
-                    tmem_ld32(tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + b * C::kAccCols + (rbeg + j) * 32, acc[j]);
+                for (int k = 0; k < 2; ++k)
+                    tmem_ld32(tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + b * C::kAccCols + (k / R) * C::N +
+                                  (rbeg + k % R) * 32,
+                              acc[k]);
                 tmem_ld_wait();
+                reg_fence(acc[0]);
+                reg_fence(acc[1]);
+                float s_t[C::kHalves];
 #pragma unroll
-                for (int j = 0; j < C::kRowsPerEpiWarp; ++j) reg_fence(acc[j]);
-                const float s_t = scales[stage * C::kTileKeys + key_lane];
+                for (int hf = 0; hf < C::kHalves; ++hf) s_t[hf] = scales[stage * C::kTileKeys + hf * 128 + key_lane];
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) {
                     mbar_arrive(&empty[stage]);
                     mbar_arrive(&tempty[b]);
                 }
-                const int t = (w - prefix[g]) * C::kTileKeys + key_lane;
+                const int t0 = (w - prefix[g]) * C::kTileKeys + key_lane;
 #pragma unroll
-                for (int j = 0; j < C::kRowsPerEpiWarp; ++j) {
-                    const float v = head_relu_sum(acc[j], wp + j * 32) * s_t;
+                for (int k = 0; k < 2; ++k) {
+                    const int j = k % R, hf = k / R;
+                    const float v = head_relu_sum(acc[k], wp + j * 32) * s_t[hf];
+                    const int t = t0 + hf * 128;
                     if (t < ctx[j]) {
                         a.logits[row_off[j] + t] = v;
                         if constexpr (kHist)
                             atomicAdd(a.hist + static_cast<int64_t>(hrow[j]) * kHistBins + (order_key(v) >> 16), 1u);
                     }
-                }
-            }
-          }
-        } else if (warp >= 4) {
-            // ------------------------------------------------ epilogue
-            const int e = warp - 4;
-            const int grp = e / C::kWarpsPerTile;  // this set takes tiles it = grp (mod kEpiGroups)
-            const int sub = e % C::kWarpsPerTile;
-            const int quad = warp & 3;             // TMEM lane quadrant this warp may read
-            const int rbeg = (sub >> 2) * C::kRowsPerEpiWarp;
-            const int key_lane = quad * 32 + lane;
-            TileWalker wk{prefix, 0};
-            wk.seek(w_begin, ng);
-            int cur = -1, gc = -1;
-            int ctx[C::kRowsPerEpiWarp];
-            int64_t row_off[C::kRowsPerEpiWarp];
-            int hrow[C::kRowsPerEpiWarp];  // global row of each of this warp's rows
-            for (int32_t it = grp, w = w_begin + grp; w < w_end; it += C::kEpiGroups, w += C::kEpiGroups) {
-                wk.advance(w);
-                const int g = wk.g;
-                if (g != cur) {
-                    ++gc;
-                    cur = g;
-                    float *wb = wbuf + (grp * 2 + (gc & 1)) * C::N;
-                    const int row0 = (a.group0 + g) * G;
-                    for (int i = sub * 32 + lane; i < C::N; i += 32 * C::kWarpsPerTile)
-                        wb[i] = a.head_w[static_cast<int64_t>(row0) * DSA_INDEX_HEADS + i];
-                    named_bar_sync(1 + grp, 32 * C::kWarpsPerTile);
-#pragma unroll
-                    for (int j = 0; j < C::kRowsPerEpiWarp; ++j) {
-                        ctx[j] = min(a.row_ctx[row0 + rbeg + j], a.max_ctx);
-                        row_off[j] = static_cast<int64_t>(row0 + rbeg + j) * a.logits_stride;
-                        hrow[j] = row0 + rbeg + j;
-                    }
-                }
-                const float *wb = wbuf + (grp * 2 + (gc & 1)) * C::N;
-                const int stage = it % C::kStages, b = it % C::kAcc;
-                // one thread of the set waits for the accumulator and the stage (the stage's TMA
-                // phase is complete, as the MMA waited for it, and cannot be re-armed before this
-                // set releases it; waiting on it orders the bulk-copied scales); the set's
-                // named barrier passes the acquire on to the other warps
-                if (sub == 0 && lane == 0) {
-                    const bool ok = mbar_wait(&tfull[b], (it / C::kAcc) & 1, abort, a.status) &&
-                                    mbar_wait(&full[stage], (it / C::kStages) & 1, abort, a.status);
-                    epi_ok[grp] = ok ? 1 : 0;
-                }
-                named_bar_sync(1 + grp, 32 * C::kWarpsPerTile);
-                if (!epi_ok[grp]) break;
-                tc_fence_after();
-                const int t0 = (w - prefix[g]) * C::kTileKeys;
-                const int nkeys = min(C::kTileKeys, gmax[g] - t0);
-#pragma unroll
-                for (int hf = 0; hf < C::kHalves; ++hf) {
-                    if (hf * 128 >= nkeys) break;  // never computed (and never loaded)
-                    const float s_t = scales[stage * C::kTileKeys + hf * 128 + key_lane];
-                    const int t = t0 + hf * 128 + key_lane;
-#pragma unroll
-                    for (int j = 0; j < C::kRowsPerEpiWarp; ++j) {
-                        uint32_t acc[32];
-                        tmem_ld32(tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + b * C::kAccCols + hf * C::N +
-                                      (rbeg + j) * 32,
-                                  acc);
-                        tmem_ld_wait();
-                        const float *wr = wb + (rbeg + j) * 32;
-                        float s4[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                        for (int h = 0; h < 32; ++h)
-                            s4[h & 3] = fmaf(wr[h], fmaxf(__uint_as_float(acc[h]), 0.f), s4[h & 3]);
-                        const float sum = (s4[0] + s4[1]) + (s4[2] + s4[3]);
-                        if (t < ctx[j]) {
-                            const float v = sum * s_t;
-                            a.logits[row_off[j] + t] = v;
-                            if constexpr (kHist)
-                                atomicAdd(a.hist + static_cast<int64_t>(hrow[j]) * kHistBins + (order_key(v) >> 16), 1u);
-                        }
-                    }
-                }
-                tc_fence_before();
-                named_bar_sync(1 + grp, 32 * C::kWarpsPerTile);  // the set is done with the stage and the accumulator
-                if (sub == 0 && lane == 0) {
-                    mbar_arrive(&empty[stage]);
-                    mbar_arrive(&tempty[b]);
                 }
             }
         }
@@ -494,8 +427,16 @@ cudaError_t launch_gh(const CUtensorMap &key_map, const CUtensorMap &q_map, cons
         if (e != cudaSuccess) return e;
         configured_device = dev;
     }
-    indexer_fp8_kernel<G, kHist><<<num_sms, C::kThreads, C::kSmemBytes, s>>>(key_map, q_map, a);
-    return cudaGetLastError();
+    // the caller's range of groups, in launches of at most kMaxGroups (the planning arrays)
+    IndexerArgs b = a;
+    for (int done = 0; done < a.num_groups; done += C::kMaxGroups) {
+        b.group0 = a.group0 + done;
+        b.num_groups = a.num_groups - done < C::kMaxGroups ? a.num_groups - done : C::kMaxGroups;
+        indexer_fp8_kernel<G, kHist><<<num_sms * C::kCtasPerSm, C::kThreads, C::kSmemBytes, s>>>(key_map, q_map, b);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
 }
 
 template <int G>
