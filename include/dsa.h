@@ -311,6 +311,76 @@ int dsa_cache_insert(const dsa_cache *index_cache, const dsa_cache *latent_cache
 /* Workspace bytes dsa_sparse_mla_decode needs for num_rows rows of k slots. */
 size_t dsa_sparse_mla_workspace_size(int32_t num_rows, int32_t num_heads, int32_t k);
 
+/*
+ * ---- MSA, the block-sparse variant (vLLM blog "Day-0 support for
+ * MiniMax-M3.1-Flash", section "MSA primer" and its Fig. 1; FP8 queries over an
+ * FP8 K/V cache, section "Blackwell-optimised MSA kernels").  The cache is cut
+ * into 128-token blocks, which are also its pages; one index query per GQA
+ * group (4 groups = 4 KV heads) scores every visible token against the one
+ * 128-B index key all groups share, the scores are max-pooled per block, each
+ * group keeps its most recent block and the 15 best others, and the group's
+ * query heads attend exactly to the tokens of those blocks.
+ *
+ * Page layouts (128 tokens; the widths are the blog's, the arrangement inside
+ * a page is this library's):
+ *   index  [128 x 128 B e4m3]                                          16384 B
+ *   kv     [4 KV heads] x ([K: 128 x 128 B e4m3] [V: 128 x 128 B e4m3]) 131072 B
+ * For these calls dsa_rows.block_table holds 128-token page ids (bt_stride >=
+ * ceil(max_ctx / 128)); token t of a request is row t % 128 of page
+ * block_table[req][t / 128].  Pools and queries are 16-byte aligned.
+ */
+#define DSA_MSA_PAGE 128
+#define DSA_MSA_DIM 128
+#define DSA_MSA_GROUPS 4
+#define DSA_MSA_BLOCKS 16   /* blocks kept per (row, group): the most recent + the 15 best others */
+#define DSA_MSA_MAX_HPG 64  /* query heads per group: a multiple of 16, at most this */
+
+/*
+ * Block scores: scores[(r * 4 + g) * score_stride + b] = max over tokens t of
+ * block b with t < row_ctx[r] of <q_idx[r, g, :], k_t> (e4m3 codes; the index
+ * key has no scale), for b < ceil(row_ctx[r] / 128); other entries are not
+ * written.  q_idx: [num_rows, 4, 128] e4m3.  rows->rows_per_group (1, 2, 4 or
+ * 8) consecutive rows of one request share each read of the keys.  Products
+ * are exact and accumulate in fp32 on the tensor cores.  score_stride >=
+ * ceil(max_ctx / 128).  A page id outside [0, num_pages) or a bad row is
+ * DSA_ERR_BOUNDS on dev_status.
+ */
+int dsa_msa_block_scores(const void *index_pool, int64_t num_pages, const dsa_rows *rows, const uint8_t *q_idx,
+                         float *scores, int64_t score_stride, int32_t *dev_status, void *stream);
+
+/*
+ * Block selection, per (row r, group g), nb = ceil(row_ctx[r] / 128): nb <= 16
+ * keeps every block; otherwise block nb - 1 and the 15 highest scores among
+ * blocks 0 .. nb - 2, ties to the lower block, a NaN score counting as -inf.
+ * blocks[(r * 4 + g) * 16 + i] lists them ascending, -1 padded.  row_ctx
+ * outside [0, max_ctx] is DSA_ERR_BOUNDS (clamped).
+ */
+int dsa_msa_select(const float *scores, int64_t score_stride, const int32_t *row_ctx, int32_t num_rows,
+                   int32_t max_ctx, int32_t *blocks, int32_t *dev_status, void *stream);
+
+/*
+ * Block-sparse GQA attention: head h of row r belongs to group g = h / hpg
+ * (hpg = heads_per_group) and attends to the visible tokens (t < row_ctx[r])
+ * of its group's selected blocks:
+ *   out[r, h, :] = sum_t softmax_t(sm_scale * <q_scale q[r,h,:], k_scale K_g,t>) v_scale V_g,t
+ *   lse[r, h]    = natural log of the softmax denominator's sum, with the max folded in
+ * q: [num_rows, 4 * hpg, 128] e4m3 codes; out: fp32 [num_rows, 4 * hpg, 128];
+ * lse: fp32 [num_rows, 4 * hpg] or NULL.  A head with no visible selected
+ * token gets out = 0 and lse = -inf.  S = Q K^T runs on FP8 tensor cores
+ * (exact products, fp32 accumulation); P is fp16 and V is decoded exactly to
+ * fp16 for P V.  The workspace (dsa_msa_attention_workspace_size bytes,
+ * 256-byte aligned) holds one normalised part per selected block, merged by
+ * log-sum-exp.  A selected block at or past ceil(row_ctx / 128) or a page id
+ * outside the pool is DSA_ERR_BOUNDS.
+ */
+int dsa_msa_attention(const void *kv_pool, int64_t num_pages, float k_scale, float v_scale, const dsa_rows *rows,
+                      const uint8_t *q, float q_scale, int32_t heads_per_group, const int32_t *blocks, float sm_scale,
+                      float *out, float *lse, void *workspace, size_t workspace_bytes, int32_t *dev_status,
+                      void *stream);
+
+/* Workspace bytes dsa_msa_attention needs for num_rows rows. */
+size_t dsa_msa_attention_workspace_size(int32_t num_rows, int32_t heads_per_group);
+
 /* Human-readable text of a status code (static storage). */
 const char *dsa_status_string(int status);
 

@@ -95,6 +95,15 @@ def load_library(path: str | None = None):
     lib.dsa_sparse_mla_decode_prepared.restype = ctypes.c_int
     lib.dsa_sparse_mla_decode_prepared.argtypes = [ctypes.POINTER(_Cache), P, I32, P, I32, I32, F, P, P, P, P,
                                                    ctypes.c_size_t, P]
+    lib.dsa_msa_block_scores.restype = ctypes.c_int
+    lib.dsa_msa_block_scores.argtypes = [P, I64, ctypes.POINTER(_Rows), P, P, I64, P, P]
+    lib.dsa_msa_select.restype = ctypes.c_int
+    lib.dsa_msa_select.argtypes = [P, I64, P, I32, I32, P, P, P]
+    lib.dsa_msa_attention.restype = ctypes.c_int
+    lib.dsa_msa_attention.argtypes = [P, I64, F, F, ctypes.POINTER(_Rows), P, F, I32, P, F, P, P, P,
+                                      ctypes.c_size_t, P, P]
+    lib.dsa_msa_attention_workspace_size.restype = ctypes.c_size_t
+    lib.dsa_msa_attention_workspace_size.argtypes = [I32, I32]
     if path is None:
         _lib = lib
     return lib
@@ -104,7 +113,8 @@ EXPORTED = ("dsa_version", "dsa_status_string", "dsa_indexer_logits", "dsa_topk"
             "dsa_sparse_mla_decode", "dsa_sparse_mla_prefill", "dsa_sparse_mla_workspace_size",
             "dsa_sparse_mla_decode_noalloc", "dsa_cache_insert", "dsa_indexer_logits_hist", "dsa_topk_hist",
             "dsa_indexer_topk", "dsa_indexer_topk_workspace_size", "dsa_topk_slots",
-            "dsa_sparse_mla_decode_prepare", "dsa_sparse_mla_decode_prepared")
+            "dsa_sparse_mla_decode_prepare", "dsa_sparse_mla_decode_prepared", "dsa_msa_block_scores",
+            "dsa_msa_select", "dsa_msa_attention", "dsa_msa_attention_workspace_size")
 HIST_BINS = 65536
 NOALLOC_MAX_ROWS = 8
 
@@ -324,6 +334,60 @@ def sparse_mla_prefill(lat_pool, lat_fmt, tensor_scale, q, slots, sm_scale=DEFAU
                        status=None, stream=None):
     return _mla("dsa_sparse_mla_prefill", lat_pool, lat_fmt, tensor_scale, q, slots, sm_scale, out, lse, None,
                 status, stream)
+
+
+# ------------------------------------------------------------------ MSA block-sparse variant
+MSA_PAGE, MSA_GROUPS, MSA_BLOCKS = 128, 4, 16
+
+
+def msa_block_scores(idx_pool, block_table, row_req, row_ctx, max_ctx, q_idx, rows_per_group=1, scores=None,
+                     status=None, stream=None):
+    """dsa_msa_block_scores: fp32 [R, 4, ceil(max_ctx / 128)] block-max index scores."""
+    R = row_ctx.shape[0]
+    nb = max((int(max_ctx) + MSA_PAGE - 1) // MSA_PAGE, 1)
+    if scores is None:
+        scores = torch.empty((R, MSA_GROUPS, nb), dtype=torch.float32, device=q_idx.device)
+    r = _rows(block_table, row_req, row_ctx, max_ctx, rows_per_group)
+    rc = load_library().dsa_msa_block_scores(_ptr(idx_pool), idx_pool.shape[0], ctypes.byref(r), _ptr(q_idx),
+                                             _ptr(scores), scores.shape[-1], _ptr(status), _stream(stream))
+    _check(rc, "dsa_msa_block_scores")
+    return scores
+
+
+def msa_select(scores, row_ctx, max_ctx, blocks=None, status=None, stream=None):
+    """dsa_msa_select: int32 [R, 4, 16] selected blocks, ascending, -1 padded."""
+    R = row_ctx.shape[0]
+    if blocks is None:
+        blocks = torch.empty((R, MSA_GROUPS, MSA_BLOCKS), dtype=torch.int32, device=scores.device)
+    rc = load_library().dsa_msa_select(_ptr(scores), scores.shape[-1], _ptr(row_ctx), R, int(max_ctx), _ptr(blocks),
+                                       _ptr(status), _stream(stream))
+    _check(rc, "dsa_msa_select")
+    return blocks
+
+
+def msa_attention_workspace_size(num_rows, heads_per_group) -> int:
+    return int(load_library().dsa_msa_attention_workspace_size(int(num_rows), int(heads_per_group)))
+
+
+def msa_attention(kv_pool, k_scale, v_scale, block_table, row_req, row_ctx, max_ctx, q, q_scale, blocks, sm_scale,
+                  out=None, lse=None, workspace=None, status=None, stream=None):
+    """dsa_msa_attention: (out fp32 [R, H, 128], lse fp32 [R, H]); q is e4m3 codes [R, H, 128]."""
+    R, H, _ = q.shape
+    hpg = H // MSA_GROUPS
+    if out is None:
+        out = torch.empty((R, H, 128), dtype=torch.float32, device=q.device)
+    if lse is None:
+        lse = torch.empty((R, H), dtype=torch.float32, device=q.device)
+    if workspace is None:
+        workspace = torch.empty(max(msa_attention_workspace_size(R, hpg), 1), dtype=torch.uint8, device=q.device)
+    r = _rows(block_table, row_req, row_ctx, max_ctx)
+    rc = load_library().dsa_msa_attention(_ptr(kv_pool), kv_pool.shape[0], float(k_scale), float(v_scale),
+                                          ctypes.byref(r), _ptr(q), float(q_scale), hpg, _ptr(blocks),
+                                          float(sm_scale), _ptr(out), _ptr(lse), _ptr(workspace),
+                                          workspace.numel() * workspace.element_size(), _ptr(status),
+                                          _stream(stream))
+    _check(rc, "dsa_msa_attention")
+    return out, lse
 
 
 class Layer:

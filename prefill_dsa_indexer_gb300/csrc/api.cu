@@ -65,6 +65,10 @@ int launch_status(cudaError_t e) { return e == cudaSuccess ? DSA_OK : DSA_ERR_CU
 
 }  // namespace
 
+bool encode_rows128_map(CUtensorMap *map, const void *base, uint64_t rows, uint32_t box_rows) {
+    return encode_rows128(map, base, rows, box_rows);
+}
+
 int device_sm_count() {
     static int counts[64] = {0};
     int dev = 0;
@@ -367,6 +371,126 @@ int dsa_cache_insert(const dsa_cache *index_cache, const dsa_cache *latent_cache
     a.latents = latents;
     a.status = dev_status;
     return launch_status(launch_cache_insert(a, static_cast<cudaStream_t>(stream)));
+}
+
+// ------------------------------------------------------------------ MSA block-sparse variant
+
+static int msa_check_rows(const dsa_rows *rows) {
+    if (rows == nullptr) return DSA_ERR_INVALID_ARG;
+    if (rows->num_rows < 0 || rows->max_ctx < 0 || rows->num_requests < 0) return DSA_ERR_INVALID_ARG;
+    if (rows->num_rows == 0) return DSA_OK;
+    if (!rows->block_table || !rows->row_req || !rows->row_ctx) return DSA_ERR_INVALID_ARG;
+    const int64_t need_pages = (static_cast<int64_t>(rows->max_ctx) + DSA_MSA_PAGE - 1) / DSA_MSA_PAGE;
+    if (rows->bt_stride < need_pages) return DSA_ERR_INVALID_ARG;
+    return DSA_OK;
+}
+
+int dsa_msa_block_scores(const void *index_pool, int64_t num_pages, const dsa_rows *rows, const uint8_t *q_idx,
+                         float *scores, int64_t score_stride, int32_t *dev_status, void *stream) {
+    int rc = msa_check_rows(rows);
+    if (rc != DSA_OK || rows->num_rows == 0) return rc;
+    const int G = rows->rows_per_group;
+    if (G != 1 && G != 2 && G != 4 && G != 8) return DSA_ERR_UNSUPPORTED;
+    if (rows->num_rows % G != 0) return DSA_ERR_INVALID_ARG;
+    if (!index_pool || num_pages <= 0 || !q_idx || !scores) return DSA_ERR_INVALID_ARG;
+    if (!aligned(index_pool, 16) || !aligned(q_idx, 16)) return DSA_ERR_INVALID_ARG;
+    const int64_t max_blocks = (static_cast<int64_t>(rows->max_ctx) + DSA_MSA_PAGE - 1) / DSA_MSA_PAGE;
+    if (score_stride < max_blocks) return DSA_ERR_INVALID_ARG;
+    const uint64_t pool_rows = static_cast<uint64_t>(num_pages) * DSA_MSA_PAGE;
+    if (pool_rows >= (1ull << 31)) return DSA_ERR_UNSUPPORTED;
+    const int sms = device_sm_count();
+    if (sms <= 0) return DSA_ERR_CUDA;
+    CUtensorMap key_map, q_map;
+    const uint32_t q_box = static_cast<uint32_t>(G * DSA_MSA_GROUPS < 16 ? 16 : G * DSA_MSA_GROUPS);
+    if (!encode_rows128(&key_map, index_pool, pool_rows, DSA_MSA_PAGE)) return DSA_ERR_CUDA;
+    if (!encode_rows128(&q_map, q_idx, static_cast<uint64_t>(rows->num_rows) * DSA_MSA_GROUPS, q_box))
+        return DSA_ERR_CUDA;
+    const int num_groups = rows->num_rows / G;
+    // pages per CTA: two CTAs per SM cover the rows' pages in about one wave (4..64 pages each)
+    const int64_t total_pages = static_cast<int64_t>(num_groups) * (max_blocks > 0 ? max_blocks : 1);
+    int64_t cp = (total_pages + 2 * sms - 1) / (2 * sms);
+    cp = cp < 4 ? 4 : (cp > 64 ? 64 : cp);
+    MsaScoreArgs a;
+    a.num_pages = num_pages;
+    a.block_table = rows->block_table;
+    a.bt_stride = rows->bt_stride;
+    a.num_requests = rows->num_requests;
+    a.row_req = rows->row_req;
+    a.row_ctx = rows->row_ctx;
+    a.max_ctx = rows->max_ctx;
+    a.chunk_pages = static_cast<int32_t>(cp);
+    a.chunks = static_cast<int32_t>(max_blocks > 0 ? (max_blocks + cp - 1) / cp : 1);
+    a.scores = scores;
+    a.score_stride = score_stride;
+    a.status = dev_status;
+    return launch_status(launch_msa_scores(key_map, q_map, a, num_groups, G, static_cast<cudaStream_t>(stream)));
+}
+
+int dsa_msa_select(const float *scores, int64_t score_stride, const int32_t *row_ctx, int32_t num_rows,
+                   int32_t max_ctx, int32_t *blocks, int32_t *dev_status, void *stream) {
+    if (num_rows < 0 || max_ctx < 0) return DSA_ERR_INVALID_ARG;
+    if (num_rows == 0) return DSA_OK;
+    if (!scores || !row_ctx || !blocks) return DSA_ERR_INVALID_ARG;
+    const int64_t max_blocks = (static_cast<int64_t>(max_ctx) + DSA_MSA_PAGE - 1) / DSA_MSA_PAGE;
+    if (score_stride < max_blocks) return DSA_ERR_INVALID_ARG;
+    if (max_blocks > 16384) return DSA_ERR_UNSUPPORTED;  // candidate keys live in shared memory
+    MsaSelectArgs a;
+    a.scores = scores;
+    a.score_stride = score_stride;
+    a.row_ctx = row_ctx;
+    a.max_ctx = max_ctx;
+    a.blocks = blocks;
+    a.status = dev_status;
+    return launch_status(launch_msa_select(a, num_rows, static_cast<cudaStream_t>(stream)));
+}
+
+size_t dsa_msa_attention_workspace_size(int32_t num_rows, int32_t heads_per_group) {
+    if (num_rows <= 0 || heads_per_group <= 0) return 0;
+    return msa_attention_workspace_bytes(static_cast<size_t>(num_rows), static_cast<size_t>(heads_per_group));
+}
+
+int dsa_msa_attention(const void *kv_pool, int64_t num_pages, float k_scale, float v_scale, const dsa_rows *rows,
+                      const uint8_t *q, float q_scale, int32_t heads_per_group, const int32_t *blocks, float sm_scale,
+                      float *out, float *lse, void *workspace, size_t workspace_bytes, int32_t *dev_status,
+                      void *stream) {
+    int rc = msa_check_rows(rows);
+    if (rc != DSA_OK || rows->num_rows == 0) return rc;
+    const int hpg = heads_per_group;
+    if (hpg < 16 || hpg > DSA_MSA_MAX_HPG || hpg % 16 != 0) return DSA_ERR_UNSUPPORTED;
+    if (!kv_pool || num_pages <= 0 || !q || !blocks || !out) return DSA_ERR_INVALID_ARG;
+    if (!aligned(kv_pool, 16) || !aligned(q, 16)) return DSA_ERR_INVALID_ARG;
+    for (float v : {k_scale, v_scale, q_scale, sm_scale})
+        if (!std::isfinite(v) || !(v > 0.f)) return DSA_ERR_INVALID_ARG;
+    const size_t need = msa_attention_workspace_bytes(static_cast<size_t>(rows->num_rows), static_cast<size_t>(hpg));
+    if (workspace == nullptr || workspace_bytes < need) return DSA_ERR_WORKSPACE;
+    if (!aligned(workspace, 256)) return DSA_ERR_INVALID_ARG;
+    const uint64_t kv_rows = static_cast<uint64_t>(num_pages) * DSA_MSA_GROUPS * 2 * DSA_MSA_PAGE;
+    if (kv_rows >= (1ull << 31)) return DSA_ERR_UNSUPPORTED;
+    CUtensorMap kv_map, q_map;
+    if (!encode_rows128(&kv_map, kv_pool, kv_rows, DSA_MSA_PAGE)) return DSA_ERR_CUDA;
+    if (!encode_rows128(&q_map, q, static_cast<uint64_t>(rows->num_rows) * DSA_MSA_GROUPS * hpg,
+                        static_cast<uint32_t>(hpg)))
+        return DSA_ERR_CUDA;
+    const size_t parts = static_cast<size_t>(rows->num_rows) * DSA_MSA_GROUPS * DSA_MSA_BLOCKS * hpg;
+    MsaAttnArgs a;
+    a.num_pages = num_pages;
+    a.block_table = rows->block_table;
+    a.bt_stride = rows->bt_stride;
+    a.num_requests = rows->num_requests;
+    a.row_req = rows->row_req;
+    a.row_ctx = rows->row_ctx;
+    a.max_ctx = rows->max_ctx;
+    a.heads_per_group = hpg;
+    a.blocks = blocks;
+    a.s_scale = static_cast<float>(static_cast<double>(sm_scale) * q_scale * k_scale * 1.4426950408889634);
+    a.v_scale = v_scale;
+    a.part_o = static_cast<float *>(workspace);
+    a.part_ml = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) +
+                                          (parts * DSA_MSA_DIM * sizeof(float) + 255) / 256 * 256);
+    a.out = out;
+    a.lse = lse;
+    a.status = dev_status;
+    return launch_status(launch_msa_attention(kv_map, q_map, a, rows->num_rows, static_cast<cudaStream_t>(stream)));
 }
 
 }  // extern "C"

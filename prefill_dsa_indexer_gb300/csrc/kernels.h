@@ -112,6 +112,60 @@ struct MlaArgs {
     bool q_prepared;    // decode: the query images are already in qprep (no prep launch)
 };
 
+// ---- MSA block-sparse variant (msa.cu)
+struct MsaScoreArgs {
+    int64_t num_pages;
+    const int32_t *block_table;  // 128-token pages
+    int64_t bt_stride;
+    int32_t num_requests;
+    const int32_t *row_req;
+    const int32_t *row_ctx;
+    int32_t max_ctx;
+    int32_t chunks;       // CTAs per row group
+    int32_t chunk_pages;  // pages per CTA
+    float *scores;        // [R, 4, score_stride]
+    int64_t score_stride;
+    int32_t *status;
+};
+
+struct MsaSelectArgs {
+    const float *scores;
+    int64_t score_stride;
+    const int32_t *row_ctx;
+    int32_t max_ctx;
+    int32_t *blocks;  // [R, 4, 16]
+    int32_t *status;
+};
+
+struct MsaAttnArgs {
+    int64_t num_pages;
+    const int32_t *block_table;
+    int64_t bt_stride;
+    int32_t num_requests;
+    const int32_t *row_req;
+    const int32_t *row_ctx;
+    int32_t max_ctx;
+    int32_t heads_per_group;
+    const int32_t *blocks;
+    float s_scale;   // sm_scale * q_scale * k_scale * log2(e)
+    float v_scale;
+    float *part_o;   // [R, 4, 16, hpg, 128] normalised block parts
+    float *part_ml;  // [R, 4, 16, hpg, 2] (max in log2 units, sum)
+    float *out;
+    float *lse;
+    int32_t *status;
+};
+
+cudaError_t launch_msa_scores(const CUtensorMap &key_map, const CUtensorMap &q_map, const MsaScoreArgs &a,
+                              int num_groups, int rows_per_group, cudaStream_t s);
+cudaError_t launch_msa_select(const MsaSelectArgs &a, int num_rows, cudaStream_t s);
+cudaError_t launch_msa_attention(const CUtensorMap &kv_map, const CUtensorMap &q_map, const MsaAttnArgs &a,
+                                 int num_rows, cudaStream_t s);
+size_t msa_attention_workspace_bytes(size_t num_rows, size_t heads_per_group);
+
+// 2D byte tensor [rows, 128 B] with a [box_rows, 128 B] box, 128-byte swizzle (api.cu).
+bool encode_rows128_map(CUtensorMap *map, const void *base, uint64_t rows, uint32_t box_rows);
+
 // Decode query preparation alone (bf16 query -> the fp16 operand images in a.qprep).
 cudaError_t launch_mla_qprep(const MlaArgs &a, cudaStream_t s);
 
