@@ -230,6 +230,170 @@ def cpu_baseline(wl, inp, budget_s=12.0):
                       f"{t_used:.1f} s"}
 
 
+def msa_score_bytes(wl) -> int:
+    """Bytes the MSA block-score scan must move per launch: every visible index key of every
+    row group once (128 B/token), the block-table entries, the index queries and the fp32
+    block scores it writes."""
+    rc = wl.row_ctx()
+    G = wl.rows_per_group
+    tot = 0
+    for g in range(wl.num_rows // G):
+        Lg = int(rc[g * G:(g + 1) * G].max())
+        tot += 128 * Lg + 4 * ((Lg + 127) // 128)
+    return tot + wl.num_rows * 4 * 128 + 4 * 4 * int(((rc + 127) // 128).sum())
+
+
+def msa_layer_bytes(wl) -> int:
+    """The MSA step's own traffic: index keys once per row group, each (row, group)'s
+    selected K and V (min(L, 2048) tokens x 256 B), queries, outputs and lse."""
+    rc = wl.row_ctx()
+    H = 4 * wl.heads_per_group
+    tot = msa_score_bytes(wl)
+    tot += sum(4 * 256 * min(int(L), 2048) for L in rc)
+    tot += wl.num_rows * H * 128                # FP8 attention queries
+    tot += wl.num_rows * H * (128 + 1) * 4      # output + lse (fp32)
+    return tot
+
+
+def run_msa(args, rank, world, local, dist):
+    """One MSA block-sparse step (block scores -> selection -> attention) per query row batch."""
+    from prefill_dsa_indexer_gb300 import inputs as I
+    wl = I.msa_workload(args.workload)
+    metric = "MSA decode query-tokens/s per layer; achieved HBM GB/s of the block-score scan"
+    torch.cuda.set_device(local)
+    import __graft_entry__
+    __graft_entry__.build()
+    import prefill_dsa_indexer_gb300 as P
+    inp = I.make_msa_inputs(wl, device="cuda")
+    R, H = wl.num_rows, 4 * wl.heads_per_group
+    sm = 1.0 / np.sqrt(128.0)
+    copies = max(1, args.copies)
+    pools = [(inp.idx_pool, inp.kv_pool)] + [(inp.idx_pool.clone(), inp.kv_pool.clone()) for _ in range(copies - 1)]
+    nb = (inp.max_ctx + 127) // 128
+    scores = torch.empty((R, 4, nb), dtype=torch.float32, device="cuda")
+    blocks = torch.empty((R, 4, 16), dtype=torch.int32, device="cuda")
+    out = torch.empty((R, H, 128), dtype=torch.float32, device="cuda")
+    lse = torch.empty((R, H), dtype=torch.float32, device="cuda")
+    ws = torch.empty(P.msa_attention_workspace_size(R, wl.heads_per_group), dtype=torch.uint8, device="cuda")
+    st = P.new_status()
+
+    def step(i, q=inp.q, q_idx=inp.q_idx, ev=None, s=None):
+        ip, kp = pools[i % len(pools)]
+        if ev is not None:
+            ev[0].record(s)
+        P.msa_block_scores(ip, inp.block_table, inp.row_req, inp.row_ctx, inp.max_ctx, q_idx, wl.rows_per_group,
+                           scores=scores, status=st, stream=s)
+        if ev is not None:
+            ev[1].record(s)
+        P.msa_select(scores, inp.row_ctx, inp.max_ctx, blocks=blocks, status=st, stream=s)
+        P.msa_attention(kp, inp.k_scale, inp.v_scale, inp.block_table, inp.row_req, inp.row_ctx, inp.max_ctx, q,
+                        inp.q_scale, blocks, sm, out=out, lse=lse, workspace=ws, status=st, stream=s)
+
+    stream = torch.cuda.current_stream()
+    for i in range(args.warmup):
+        step(i, s=stream)
+    torch.cuda.synchronize()
+    P.check_status(st, "warm-up")
+    # CUDA graphs of 16 x copies consecutive steps, event nodes around every block-score launch
+    cap = torch.cuda.Stream()
+    cap.wait_stream(stream)
+    n = 16 * copies
+    g = torch.cuda.CUDAGraph()
+    evp = [(torch.cuda.Event(enable_timing=True, external=True), torch.cuda.Event(enable_timing=True, external=True))
+           for _ in range(n)]
+    with torch.cuda.stream(cap):
+        with torch.cuda.graph(g, stream=cap):
+            for k in range(n):
+                step(k, ev=evp[k], s=cap)
+    stream.wait_stream(cap)
+    g.replay()
+    torch.cuda.synchronize()
+    reps = max(1, args.steps // n)
+    steps = reps * n
+    if dist is not None:
+        dist.barrier()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        clk.wait_first()
+        h0 = time.time()
+        t0.record(stream)
+        for _ in range(reps):
+            g.replay()
+        t1.record(stream)
+        torch.cuda.synchronize()
+        h1 = time.time()
+    if dist is not None:
+        dist.barrier()
+    total_ms = t0.elapsed_time(t1)
+    if dist is not None:
+        t = torch.tensor([total_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    P.check_status(st, "timed steps")
+    score_ms = sum(a.elapsed_time(b) for a, b in evp) / len(evp)
+    value = world * R * steps / (total_ms / 1000.0)
+    # end to end: queries in from pinned host memory, outputs back, inside the timed region
+    hq, hqi = inp.q.cpu().pin_memory(), inp.q_idx.cpu().pin_memory()
+    dq, dqi = torch.empty_like(inp.q), torch.empty_like(inp.q_idx)
+    ho, hl = torch.empty(out.shape, dtype=torch.float32).pin_memory(), torch.empty(lse.shape).pin_memory()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for i in range(args.warmup + args.steps):
+        if i == args.warmup:
+            e0.record(stream)
+        dq.copy_(hq, non_blocking=True)
+        dqi.copy_(hqi, non_blocking=True)
+        step(i, q=dq, q_idx=dqi, s=stream)
+        ho.copy_(out, non_blocking=True)
+        hl.copy_(lse, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    P.check_status(st, "e2e steps")
+    e2e_ms = e0.elapsed_time(e1)
+    hbm_peak, _, peak_kind = _peaks()
+    sb = msa_score_bytes(wl)
+    achieved = sb / (score_ms / 1000.0) / 1e9
+    lb = msa_layer_bytes(wl)
+    line = {
+        "metric": metric, "value": value, "unit": UNIT, "n_gpus": world, "steps": steps, "warmup": args.warmup,
+        "ms_per_step": total_ms / steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "e4m3xe4m3->f32 (scores, S), f16xf16->f32 (PV)", "data": "synthetic",
+        "config": {"workload": wl.name, "batch": len(wl.ctx), "rows": R, "ctx": wl.ctx[0], "groups": 4,
+                   "heads_per_group": wl.heads_per_group, "blocks": 16, "page": 128,
+                   "l2": f"inputs > L2: {copies} rotating copies of the caches "
+                         f"({(inp.idx_pool.numel() + inp.kv_pool.numel()) * copies / 1e9:.2f} GB)"},
+        "layer_hbm_gbs": lb / (total_ms / steps / 1000.0) / 1e9, "layer_algorithmic_bytes": lb,
+        "roofline": {"kernel": f"msa_scores_kernel<{wl.rows_per_group}>", "bound": "hbm", "achieved": achieved,
+                     "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak, "peak_kind": peak_kind,
+                     "algorithmic_bytes": sb, "ms_per_launch": score_ms, "traffic": None},
+        "e2e": {"value": world * R * args.steps / (e2e_ms / 1000.0), "unit": UNIT,
+                "h2d_bytes_per_step": hq.numel() + hqi.numel(), "d2h_bytes_per_step": (ho.numel() + hl.numel()) * 4,
+                "ms_per_step": e2e_ms / args.steps},
+        "gpu_launches": 4 * steps,
+        "launch": f"CUDA graphs of {n} consecutive steps; block scores timed by event nodes inside the graph",
+        "clocks": clk.summary(h0, h1),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+        host = {k: inp.np(k) for k in ("idx_pool", "kv_pool", "block_table", "row_req", "row_ctx", "q_idx", "q")}
+        done, used = 0, 0.0
+        while used < 12.0:
+            rows = np.array([done % R])
+            ta = time.perf_counter()
+            sc = oracle.msa_block_scores(host["idx_pool"], host["block_table"], host["row_req"][rows],
+                                         host["row_ctx"][rows], host["q_idx"][rows])
+            bl = oracle.msa_select(sc, host["row_ctx"][rows])
+            oracle.msa_attention(host["kv_pool"], inp.k_scale, inp.v_scale, host["block_table"],
+                                 host["row_req"][rows], host["row_ctx"][rows], host["q"][rows], inp.q_scale, bl, sm)
+            used += time.perf_counter() - ta
+            done += 1
+        line["cpu_baseline"] = {"value": done / used, "unit": UNIT, "cores": 1, "kind": "oracle",
+                                "sample": f"{done} whole query rows of {wl.name} (block scores over every key, "
+                                          f"selection, attention of all heads), one row per call, {used:.1f} s"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -252,6 +416,12 @@ def main():
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl" if args.impl == "ours" else "gloo")
+
+    if args.workload.startswith("msa_") and args.impl == "ours":
+        run_msa(args, rank, world, local, dist)
+        if dist is not None:
+            dist.destroy_process_group()
+        return
 
     from prefill_dsa_indexer_gb300 import inputs as I
     wl = I.workload(args.workload)
