@@ -23,7 +23,8 @@
 //     over TMEM lanes with warp shuffles; the MMA's commit releases the stage.
 //   * selection: one CTA per (row, group); the candidates' 64-bit keys
 //     (order-preserving score bits, then the inverted block id) stay in shared
-//     memory; 15 block-wide argmax rounds pick the winners.
+//     memory; each warp takes the 15 best of its slice by warp argmax rounds,
+//     and one warp takes the 15 best of those.
 //   * attention: one CTA per (row, group, selected block).  TMA brings the
 //     group's FP8 queries and the block's FP8 K and V (16 KB each); S = Q K^T
 //     runs on kind::f8f6f4 (queries on M, padded to 128 rows, tokens on N =
@@ -279,10 +280,39 @@ __device__ __forceinline__ unsigned long long msa_select_key(float s, int b) {
 }
 
 constexpr int kSelThreads = 256;
+constexpr int kSelWarps = kSelThreads / 32;
+
+// One warp's argmax over keys[lo, hi) (shared memory), 15 times: the winners' keys go to
+// top[0..14] in decreasing order (0 once the range is exhausted) and are zeroed in keys.
+// Candidate keys are > 0 and distinct (the block id is in the low bits), so each round's
+// winner sits at exactly one position, which the lane that saw it clears.
+__device__ __forceinline__ void warp_top15(unsigned long long *keys, int lo, int hi, unsigned long long *top,
+                                           int lane) {
+    for (int round = 0; round < kMsaBlocks - 1; ++round) {
+        unsigned long long mine = 0ull;
+        int at = -1;
+        for (int b = lo + lane; b < hi; b += 32) {
+            const unsigned long long k = keys[b];
+            if (k > mine) {
+                mine = k;
+                at = b;
+            }
+        }
+        // 64-bit warp max as two 32-bit reductions: the score half, then the block half among
+        // the lanes holding that score
+        const uint32_t hi = static_cast<uint32_t>(mine >> 32), lo = static_cast<uint32_t>(mine);
+        const uint32_t bh = __reduce_max_sync(0xffffffffu, hi);
+        const uint32_t bl = __reduce_max_sync(0xffffffffu, hi == bh ? lo : 0u);
+        const unsigned long long best = (static_cast<unsigned long long>(bh) << 32) | bl;
+        if (lane == 0) top[round] = best;
+        if (best != 0ull && mine == best) keys[at] = 0ull;
+        __syncwarp();
+    }
+}
 
 __global__ void __launch_bounds__(kSelThreads) msa_select_kernel(const MsaSelectArgs a) {
     extern __shared__ unsigned long long cand[];  // [nb - 1] keys; a taken key becomes 0
-    __shared__ unsigned long long wbest[kSelThreads / 32];
+    __shared__ unsigned long long wtop[kSelWarps * (kMsaBlocks - 1)];
     __shared__ int32_t won[kMsaBlocks];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int r = blockIdx.x / kMsaGroups;
@@ -301,37 +331,27 @@ __global__ void __launch_bounds__(kSelThreads) msa_select_kernel(const MsaSelect
     const int m = nb - 1;  // candidates: every block but the most recent one
     for (int b = tid; b < m; b += kSelThreads) cand[b] = msa_select_key(sc[b], b);
     __syncthreads();
-    for (int round = 0; round < kMsaBlocks - 1; ++round) {
-        unsigned long long best = 0ull;
-        for (int b = tid; b < m; b += kSelThreads) best = max(best, cand[b]);
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) best = max(best, __shfl_xor_sync(0xffffffffu, best, o));
-        if (lane == 0) wbest[warp] = best;
-        __syncthreads();
-        if (warp == 0) {
-            unsigned long long v = lane < kSelThreads / 32 ? wbest[lane] : 0ull;
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, o));
-            if (lane == 0) {
-                // every candidate key is > 0 and distinct, so the winner is unique
-                const int b = static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(v & 0xFFFFFFFFull));
-                won[round] = b;
-                cand[b] = 0ull;
+    // each warp takes the 15 best of its slice; the 15 best of those 8 x 15 are the row's 15 best
+    const int per = (m + kSelWarps - 1) / kSelWarps;
+    warp_top15(cand, min(m, warp * per), min(m, (warp + 1) * per), wtop + warp * (kMsaBlocks - 1), lane);
+    __syncthreads();
+    if (warp == 0) {
+        unsigned long long top[kMsaBlocks - 1];
+        warp_top15(wtop, 0, kSelWarps * (kMsaBlocks - 1), top, lane);
+        if (lane == 0) {
+            for (int i = 0; i < kMsaBlocks - 1; ++i)
+                won[i] = static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(top[i] & 0xFFFFFFFFull));
+            won[kMsaBlocks - 1] = nb - 1;
+            // ascending block order (insertion sort of 16 ids)
+            for (int i = 1; i < kMsaBlocks; ++i) {
+                const int v = won[i];
+                int j = i - 1;
+                while (j >= 0 && won[j] > v) {
+                    won[j + 1] = won[j];
+                    --j;
+                }
+                won[j + 1] = v;
             }
-        }
-        __syncthreads();
-    }
-    if (tid == 0) {
-        won[kMsaBlocks - 1] = nb - 1;
-        // ascending block order (insertion sort of 16 ids)
-        for (int i = 1; i < kMsaBlocks; ++i) {
-            const int v = won[i];
-            int j = i - 1;
-            while (j >= 0 && won[j] > v) {
-                won[j + 1] = won[j];
-                --j;
-            }
-            won[j + 1] = v;
         }
     }
     __syncthreads();
@@ -573,31 +593,52 @@ __global__ void __launch_bounds__(kAttThreads, 2)
     }
 }
 
-// Merge the 16 block parts of each (row, head): O = sum_i w_i O_i / sum_i w_i with
-// w_i = l_i 2^(m_i - M), M = max_i m_i (log2 units); lse in natural log.
+// Merge the 16 block parts of four heads of one (row, group): O = sum_i w_i O_i / sum_i w_i
+// with w_i = l_i 2^(m_i - M), M = max_i m_i (log2 units); lse in natural log.  A part with
+// no weight (unused slot, never written) contributes through a select, so its bytes never
+// reach the sum.
+constexpr int kCombHeads = 4;
+
 __global__ void __launch_bounds__(kMsaDim) msa_combine_kernel(const MsaAttnArgs a) {
+    __shared__ float wgt[kCombHeads][kMsaBlocks];  // w_i / sum_i w_i
     const int hpg = a.heads_per_group, H = kMsaGroups * hpg;
-    const int r = blockIdx.x / H, h = blockIdx.x % H;
-    const int g = h / hpg, hh = h % hpg;
-    const int d = threadIdx.x;
-    const int64_t base = (static_cast<int64_t>(r) * kMsaGroups + g) * kMsaBlocks;
-    float M = -INFINITY;
-    for (int i = 0; i < kMsaBlocks; ++i) M = fmaxf(M, a.part_ml[((base + i) * hpg + hh) * 2]);
-    float ws = 0.f, o = 0.f;
-    if (M > -INFINITY) {
-        for (int i = 0; i < kMsaBlocks; ++i) {
-            const float mi = a.part_ml[((base + i) * hpg + hh) * 2];
-            const float li = a.part_ml[((base + i) * hpg + hh) * 2 + 1];
-            if (li > 0.f) {
-                const float w = li * msa_exp2(mi - M);
-                ws += w;
-                o += w * a.part_o[((base + i) * hpg + hh) * kMsaDim + d];
-            }
-        }
+    const int quads = hpg / kCombHeads;
+    const int rg = blockIdx.x / quads, h0 = (blockIdx.x % quads) * kCombHeads;
+    const int r = rg / kMsaGroups, g = rg % kMsaGroups;
+    const int64_t base = static_cast<int64_t>(rg) * kMsaBlocks;  // part of slot 0
+    const int tid = threadIdx.x;
+    if (tid < kCombHeads * kMsaBlocks) {
+        // one thread per (head, part); the head's 16 threads share M and the sum by shuffles
+        const int hh = tid / kMsaBlocks, i = tid % kMsaBlocks;
+        const float mi = a.part_ml[((base + i) * hpg + h0 + hh) * 2];
+        const float li = a.part_ml[((base + i) * hpg + h0 + hh) * 2 + 1];
+        float M = mi;
+#pragma unroll
+        for (int o = 8; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o, kMsaBlocks));
+        const float w = (M > -INFINITY && li > 0.f) ? li * msa_exp2(mi - M) : 0.f;
+        float ws = w;
+#pragma unroll
+        for (int o = 8; o > 0; o >>= 1) ws += __shfl_xor_sync(0xffffffffu, ws, o, kMsaBlocks);
+        wgt[hh][i] = ws > 0.f ? w / ws : 0.f;
+        if (i == 0 && a.lse != nullptr)
+            a.lse[static_cast<int64_t>(r) * H + g * hpg + h0 + hh] =
+                ws > 0.f ? (M + log2f(ws)) * 0.6931471805599453f : -INFINITY;
     }
-    a.out[(static_cast<int64_t>(r) * H + h) * kMsaDim + d] = ws > 0.f ? o / ws : 0.f;
-    if (d == 0 && a.lse != nullptr)
-        a.lse[static_cast<int64_t>(r) * H + h] = ws > 0.f ? (M + log2f(ws)) * 0.6931471805599453f : -INFINITY;
+    __syncthreads();
+    const int d = tid;
+#pragma unroll
+    for (int hh = 0; hh < kCombHeads; ++hh) {
+        float x[kMsaBlocks];
+#pragma unroll
+        for (int i = 0; i < kMsaBlocks; ++i) x[i] = a.part_o[((base + i) * hpg + h0 + hh) * kMsaDim + d];
+        float o = 0.f;
+#pragma unroll
+        for (int i = 0; i < kMsaBlocks; ++i) {
+            const float w = wgt[hh][i];
+            o += w != 0.f ? w * x[i] : 0.f;
+        }
+        a.out[(static_cast<int64_t>(r) * H + g * hpg + h0 + hh) * kMsaDim + d] = o;
+    }
 }
 
 template <int G>
@@ -667,7 +708,7 @@ cudaError_t launch_msa_attention(const CUtensorMap &kv_map, const CUtensorMap &q
     msa_attention_kernel<<<num_rows * kMsaGroups * kMsaBlocks, kAttThreads, kAttSmemBytes, s>>>(kv_map, q_map, a);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    msa_combine_kernel<<<num_rows * kMsaGroups * a.heads_per_group, kMsaDim, 0, s>>>(a);
+    msa_combine_kernel<<<num_rows * kMsaGroups * (a.heads_per_group / kCombHeads), kMsaDim, 0, s>>>(a);
     return cudaGetLastError();
 }
 
