@@ -354,6 +354,11 @@ def run_msa(args, rank, world, local, dist):
     sb = msa_score_bytes(wl)
     achieved = sb / (score_ms / 1000.0) / 1e9
     lb = msa_layer_bytes(wl)
+    msa_traffic = None
+    tfile = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(tfile):
+        with open(tfile) as f:
+            msa_traffic = json.load(f).get(wl.name)
     line = {
         "metric": metric, "value": value, "unit": UNIT, "n_gpus": world, "steps": steps, "warmup": args.warmup,
         "ms_per_step": total_ms / steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
@@ -365,7 +370,7 @@ def run_msa(args, rank, world, local, dist):
         "layer_hbm_gbs": lb / (total_ms / steps / 1000.0) / 1e9, "layer_algorithmic_bytes": lb,
         "roofline": {"kernel": f"msa_scores_kernel<{wl.rows_per_group}>", "bound": "hbm", "achieved": achieved,
                      "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak, "peak_kind": peak_kind,
-                     "algorithmic_bytes": sb, "ms_per_launch": score_ms, "traffic": None},
+                     "algorithmic_bytes": sb, "ms_per_launch": score_ms, "traffic": msa_traffic},
         "e2e": {"value": world * R * args.steps / (e2e_ms / 1000.0), "unit": UNIT,
                 "h2d_bytes_per_step": hq.numel() + hqi.numel(), "d2h_bytes_per_step": (ho.numel() + hl.numel()) * 4,
                 "ms_per_step": e2e_ms / args.steps},
