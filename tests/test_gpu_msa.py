@@ -44,6 +44,8 @@ CASES = {
     "verify_g4": _wl("verify", [3000, 6000], rows=4, group=4),
     "verify_g8": _wl("verify8", [2600, 9000], rows=8, group=8, hpg=32),
     "heads64": _wl("h64", [3000, 20000], hpg=64),
+    "heads48": _wl("h48", [5000], hpg=48),
+    "long_128k": _wl("long", [131072 - 5]),  # 1024 blocks: every selection warp holds 128 candidates
 }
 
 

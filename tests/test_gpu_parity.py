@@ -39,6 +39,8 @@ def _wl(name, ctx, rows=1, group=1, lat=I.LATENT_FP8, heads=96, k=2048, seed=5, 
 INDEXER_CASES = {
     "tiny_4k": I.workload("decode_tiny_4k"),
     "ragged": _wl("ragged", [1, 63, 64, 65, 127, 128, 129, 193, 255, 256, 257, 2047, 2048, 2049, 3000, 5000]),
+    # more row groups than one decode launch plans for: the call splits into several launches
+    "many_rows": _wl("many", [200 + 37 * (i % 11) for i in range(300)]),
     "verify_g4": _wl("verify", [3000, 4100], rows=4, group=4),
     "pairs_g2": _wl("pairs", [700, 1500, 2500], rows=2, group=2),
     "prefill_g8": _wl("prefill", [3000], rows=64, group=8),
