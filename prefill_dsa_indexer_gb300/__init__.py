@@ -408,8 +408,10 @@ class Layer:
         self.logits = torch.empty((R, max(self.max_ctx, 1)), dtype=torch.float32, device=device)
         self.idx = torch.empty((R, self.k), dtype=torch.int32, device=device)
         self.slots = torch.empty((R, self.k), dtype=torch.int32, device=device)
-        self.out = torch.empty((R, H, VALUE_DIM), dtype=torch.float32, device=device)
-        self.lse = torch.empty((R, H), dtype=torch.float32, device=device)
+        # outputs and log-sum-exps in one buffer, so one copy moves a step's results
+        self.outputs = torch.empty(R * H * (VALUE_DIM + 1), dtype=torch.float32, device=device)
+        self.out = self.outputs[:R * H * VALUE_DIM].view(R, H, VALUE_DIM)
+        self.lse = self.outputs[R * H * VALUE_DIM:].view(R, H)
         need = 0 if prefill else sparse_mla_workspace_size(R, H, self.k)
         self.workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=device)
         self.status = new_status(device)
