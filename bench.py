@@ -53,6 +53,22 @@ def _peaks():
     return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS * FP8_OVER_BF16, "fallback"
 
 
+def max_over_ranks(v: float, dist) -> float:
+    """The largest of every rank's value (the slowest rank's time); `dist` None = one process."""
+    if dist is None:
+        return float(v)
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(v)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_throughput(world: int, rows: int, steps: int, ms: float) -> float:
+    """Whole-job query-tokens/s of `world` replicas that each ran `steps` steps of `rows` query
+    rows in `ms` (the slowest rank's) milliseconds."""
+    return world * rows * steps / (ms / 1000.0)
+
+
 def indexer_flops(wl) -> int:
     """2 * 32 heads * 128 dims per (query row, visible key) pair."""
     return int(2 * 32 * 128 * int(wl.row_ctx().astype(np.int64).sum()))
@@ -326,13 +342,10 @@ def run_msa(args, rank, world, local, dist):
     if dist is not None:
         dist.barrier()
     total_ms = t0.elapsed_time(t1)
-    if dist is not None:
-        t = torch.tensor([total_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, dist)
     P.check_status(st, "timed steps")
     score_ms = sum(a.elapsed_time(b) for a, b in evp) / len(evp)
-    value = world * R * steps / (total_ms / 1000.0)
+    value = replica_throughput(world, R, steps, total_ms)
     # end to end: queries in from pinned host memory, outputs back, inside the timed region
     hq, hqi = inp.q.cpu().pin_memory(), inp.q_idx.cpu().pin_memory()
     dq, dqi = torch.empty_like(inp.q), torch.empty_like(inp.q_idx)
@@ -371,7 +384,7 @@ def run_msa(args, rank, world, local, dist):
         "roofline": {"kernel": f"msa_scores_kernel<{wl.rows_per_group}>", "bound": "hbm", "achieved": achieved,
                      "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak, "peak_kind": peak_kind,
                      "algorithmic_bytes": sb, "ms_per_launch": score_ms, "traffic": msa_traffic},
-        "e2e": {"value": world * R * args.steps / (e2e_ms / 1000.0), "unit": UNIT,
+        "e2e": {"value": replica_throughput(world, R, args.steps, e2e_ms), "unit": UNIT,
                 "h2d_bytes_per_step": hq.numel() + hqi.numel(), "d2h_bytes_per_step": (ho.numel() + hl.numel()) * 4,
                 "ms_per_step": e2e_ms / args.steps},
         "gpu_launches": 4 * steps,
@@ -584,12 +597,9 @@ def main():
     idx_ms = sum(samples) / len(samples)
     for L in layers:
         P.check_status(L.status, "timed steps")
-    if dist is not None:
-        t = torch.tensor([total_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, dist)
     ms_per_step = total_ms / args.steps
-    value = world * wl.num_rows * args.steps / (total_ms / 1000.0)
+    value = replica_throughput(world, wl.num_rows, args.steps, total_ms)
 
     # ---- end to end through the C ABI with host buffers.  Every step copies its inputs from
     # pinned host memory and its outputs back; the copies run on their own streams, double
@@ -662,13 +672,10 @@ def main():
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1)
-    if dist is not None:
-        t = torch.tensor([e2e_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e2e_ms, dist)
     for L in layers:
         P.check_status(L.status, "e2e steps")
-    e2e_value = world * wl.num_rows * args.steps / (e2e_ms / 1000.0)
+    e2e_value = replica_throughput(world, wl.num_rows, args.steps, e2e_ms)
 
     idx_tok = I.INDEX_TOKEN_BYTES[wl.key_fmt]
     lat_tok = I.LATENT_TOKEN_BYTES[wl.lat_fmt]
