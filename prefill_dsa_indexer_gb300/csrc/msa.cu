@@ -593,52 +593,37 @@ __global__ void __launch_bounds__(kAttThreads, 2)
     }
 }
 
-// Merge the 16 block parts of four heads of one (row, group): O = sum_i w_i O_i / sum_i w_i
-// with w_i = l_i 2^(m_i - M), M = max_i m_i (log2 units); lse in natural log.  A part with
-// no weight (unused slot, never written) contributes through a select, so its bytes never
-// reach the sum.
-constexpr int kCombHeads = 4;
-
+// Merge the 16 block parts of one (row, head): O = sum_i w_i O_i / sum_i w_i with
+// w_i = l_i 2^(m_i - M), M = max_i m_i (log2 units); lse in natural log.  One thread per
+// output dim; every part's load is issued before any is used, and a part with no weight
+// (unused slot, never written) enters through a select, so its bytes never reach the sum.
 __global__ void __launch_bounds__(kMsaDim) msa_combine_kernel(const MsaAttnArgs a) {
-    __shared__ float wgt[kCombHeads][kMsaBlocks];  // w_i / sum_i w_i
     const int hpg = a.heads_per_group, H = kMsaGroups * hpg;
-    const int quads = hpg / kCombHeads;
-    const int rg = blockIdx.x / quads, h0 = (blockIdx.x % quads) * kCombHeads;
-    const int r = rg / kMsaGroups, g = rg % kMsaGroups;
-    const int64_t base = static_cast<int64_t>(rg) * kMsaBlocks;  // part of slot 0
-    const int tid = threadIdx.x;
-    if (tid < kCombHeads * kMsaBlocks) {
-        // one thread per (head, part); the head's 16 threads share M and the sum by shuffles
-        const int hh = tid / kMsaBlocks, i = tid % kMsaBlocks;
-        const float mi = a.part_ml[((base + i) * hpg + h0 + hh) * 2];
-        const float li = a.part_ml[((base + i) * hpg + h0 + hh) * 2 + 1];
-        float M = mi;
+    const int r = blockIdx.x / H, h = blockIdx.x % H;
+    const int g = h / hpg, hh = h % hpg;
+    const int d = threadIdx.x;
+    const int64_t base = (static_cast<int64_t>(r) * kMsaGroups + g) * kMsaBlocks;  // part of slot 0
+    float mi[kMsaBlocks], li[kMsaBlocks], x[kMsaBlocks];
 #pragma unroll
-        for (int o = 8; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o, kMsaBlocks));
-        const float w = (M > -INFINITY && li > 0.f) ? li * msa_exp2(mi - M) : 0.f;
-        float ws = w;
-#pragma unroll
-        for (int o = 8; o > 0; o >>= 1) ws += __shfl_xor_sync(0xffffffffu, ws, o, kMsaBlocks);
-        wgt[hh][i] = ws > 0.f ? w / ws : 0.f;
-        if (i == 0 && a.lse != nullptr)
-            a.lse[static_cast<int64_t>(r) * H + g * hpg + h0 + hh] =
-                ws > 0.f ? (M + log2f(ws)) * 0.6931471805599453f : -INFINITY;
+    for (int i = 0; i < kMsaBlocks; ++i) {
+        mi[i] = a.part_ml[((base + i) * hpg + hh) * 2];
+        li[i] = a.part_ml[((base + i) * hpg + hh) * 2 + 1];
+        x[i] = a.part_o[((base + i) * hpg + hh) * kMsaDim + d];
     }
-    __syncthreads();
-    const int d = tid;
+    float M = -INFINITY;
 #pragma unroll
-    for (int hh = 0; hh < kCombHeads; ++hh) {
-        float x[kMsaBlocks];
+    for (int i = 0; i < kMsaBlocks; ++i) M = fmaxf(M, mi[i]);
+    float ws = 0.f, o = 0.f;
 #pragma unroll
-        for (int i = 0; i < kMsaBlocks; ++i) x[i] = a.part_o[((base + i) * hpg + h0 + hh) * kMsaDim + d];
-        float o = 0.f;
-#pragma unroll
-        for (int i = 0; i < kMsaBlocks; ++i) {
-            const float w = wgt[hh][i];
-            o += w != 0.f ? w * x[i] : 0.f;
-        }
-        a.out[(static_cast<int64_t>(r) * H + g * hpg + h0 + hh) * kMsaDim + d] = o;
+    for (int i = 0; i < kMsaBlocks; ++i) {
+        const bool on = M > -INFINITY && li[i] > 0.f;
+        const float w = on ? li[i] * msa_exp2(mi[i] - M) : 0.f;
+        ws += w;
+        o += on ? w * x[i] : 0.f;
     }
+    a.out[(static_cast<int64_t>(r) * H + h) * kMsaDim + d] = ws > 0.f ? o / ws : 0.f;
+    if (d == 0 && a.lse != nullptr)
+        a.lse[static_cast<int64_t>(r) * H + h] = ws > 0.f ? (M + log2f(ws)) * 0.6931471805599453f : -INFINITY;
 }
 
 template <int G>
@@ -708,7 +693,7 @@ cudaError_t launch_msa_attention(const CUtensorMap &kv_map, const CUtensorMap &q
     msa_attention_kernel<<<num_rows * kMsaGroups * kMsaBlocks, kAttThreads, kAttSmemBytes, s>>>(kv_map, q_map, a);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    msa_combine_kernel<<<num_rows * kMsaGroups * (a.heads_per_group / kCombHeads), kMsaDim, 0, s>>>(a);
+    msa_combine_kernel<<<num_rows * kMsaGroups * a.heads_per_group, kMsaDim, 0, s>>>(a);
     return cudaGetLastError();
 }
 
