@@ -153,6 +153,19 @@ int dsa_topk_slots(const float *logits, int64_t logits_stride, const dsa_rows *r
                    int32_t *idx_out, int32_t *slots_out, int32_t *dev_status, void *stream);
 
 /*
+ * dsa_topk_slots whose output pass also warms L2 with the selected tokens'
+ * latents, so that the sparse attention launched next gathers them from L2
+ * instead of HBM (the fused decode path of blog section "Low-latency decode"
+ * hands attention the physical rows to read as soon as they are chosen).
+ * latent_cache: the latent pool the slots index (its num_pages bounds the
+ * slots).  FP8 latents (576 contiguous bytes per slot) are prefetched; an
+ * NVFP4 pool gets the plain dsa_topk_slots result.  Outputs are identical to
+ * dsa_topk_slots.
+ */
+int dsa_topk_slots_warm(const float *logits, int64_t logits_stride, const dsa_rows *rows, const dsa_cache *latent_cache,
+                        int32_t k, int32_t *idx_out, int32_t *slots_out, int32_t *dev_status, void *stream);
+
+/*
  * Single-pass scorer + top-k (blog section "Low-latency decode: fused DSA
  * decode path": the scorer feeds a batch-invariant exact top-k; here the
  * scorer's epilogue also builds the histogram the selection starts from).

@@ -90,6 +90,8 @@ def load_library(path: str | None = None):
     lib.dsa_indexer_topk_workspace_size.argtypes = [I32, I32]
     lib.dsa_topk_slots.restype = ctypes.c_int
     lib.dsa_topk_slots.argtypes = [P, I64, ctypes.POINTER(_Rows), I64, I32, P, P, P, P]
+    lib.dsa_topk_slots_warm.restype = ctypes.c_int
+    lib.dsa_topk_slots_warm.argtypes = [P, I64, ctypes.POINTER(_Rows), ctypes.POINTER(_Cache), I32, P, P, P, P]
     lib.dsa_sparse_mla_decode_prepare.restype = ctypes.c_int
     lib.dsa_sparse_mla_decode_prepare.argtypes = [ctypes.POINTER(_Cache), P, I32, I32, I32, P, P, ctypes.c_size_t, P]
     lib.dsa_sparse_mla_decode_prepared.restype = ctypes.c_int
@@ -114,7 +116,7 @@ EXPORTED = ("dsa_version", "dsa_status_string", "dsa_indexer_logits", "dsa_topk"
             "dsa_sparse_mla_decode_noalloc", "dsa_cache_insert", "dsa_indexer_logits_hist", "dsa_topk_hist",
             "dsa_indexer_topk", "dsa_indexer_topk_workspace_size", "dsa_topk_slots",
             "dsa_sparse_mla_decode_prepare", "dsa_sparse_mla_decode_prepared", "dsa_msa_block_scores",
-            "dsa_msa_select", "dsa_msa_attention", "dsa_msa_attention_workspace_size")
+            "dsa_msa_select", "dsa_msa_attention", "dsa_msa_attention_workspace_size", "dsa_topk_slots_warm")
 HIST_BINS = 65536
 NOALLOC_MAX_ROWS = 8
 
@@ -244,6 +246,22 @@ def topk_slots(logits, block_table, row_req, row_ctx, max_ctx, pool_pages, k=204
     rc = load_library().dsa_topk_slots(_ptr(logits), logits.stride(0), ctypes.byref(r), int(pool_pages), int(k),
                                        _ptr(out), _ptr(slots), _ptr(status), _stream(stream))
     _check(rc, "dsa_topk_slots")
+    return out, slots
+
+
+def topk_slots_warm(logits, block_table, row_req, row_ctx, max_ctx, lat_pool, lat_fmt, k=2048, out=None,
+                    slots=None, status=None, stream=None):
+    """dsa_topk_slots_warm: topk_slots whose output pass also prefetches the selected FP8 latents into L2."""
+    R = row_ctx.shape[0]
+    if out is None:
+        out = torch.empty((R, k), dtype=torch.int32, device=logits.device)
+    if slots is None:
+        slots = torch.empty((R, k), dtype=torch.int32, device=logits.device)
+    r = _rows(block_table, row_req, row_ctx, max_ctx)
+    c = _cache(lat_pool, lat_fmt)
+    rc = load_library().dsa_topk_slots_warm(_ptr(logits), logits.stride(0), ctypes.byref(r), ctypes.byref(c), int(k),
+                                            _ptr(out), _ptr(slots), _ptr(status), _stream(stream))
+    _check(rc, "dsa_topk_slots_warm")
     return out, slots
 
 
@@ -437,6 +455,9 @@ class Layer:
                       stream=stream)
             page_to_slot(self.block_table, row_req, row_ctx, self.max_ctx, self.lat_pool.shape[0], self.idx,
                          out=self.slots, status=self.status, stream=stream)
+        elif not self.prefill:  # decode: top-k with page -> slot, warming L2 with the chosen latents
+            topk_slots_warm(self.logits, self.block_table, row_req, row_ctx, self.max_ctx, self.lat_pool,
+                            self.lat_fmt, self.k, out=self.idx, slots=self.slots, status=self.status, stream=stream)
         else:  # top-k with the page -> slot translation in its output pass
             topk_slots(self.logits, self.block_table, row_req, row_ctx, self.max_ctx, self.lat_pool.shape[0], self.k,
                        out=self.idx, slots=self.slots, status=self.status, stream=stream)

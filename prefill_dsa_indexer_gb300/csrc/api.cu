@@ -172,7 +172,7 @@ int dsa_indexer_logits_hist(const dsa_cache *index_cache, const dsa_rows *rows, 
 static int topk_common(const float *logits, int64_t logits_stride, const int32_t *row_ctx, int32_t num_rows,
                        int32_t max_ctx, int32_t k, uint32_t *hist, bool discard, int32_t *idx_out,
                        int32_t *dev_status, void *stream, const dsa_rows *slot_rows = nullptr,
-                       int64_t pool_pages = 0, int32_t *slots_out = nullptr) {
+                       int64_t pool_pages = 0, int32_t *slots_out = nullptr, const uint8_t *warm_pool = nullptr) {
     if (num_rows < 0 || max_ctx < 0) return DSA_ERR_INVALID_ARG;
     if (k < 1 || k > DSA_MAX_TOPK) return DSA_ERR_UNSUPPORTED;
     if (num_rows == 0) return DSA_OK;
@@ -188,8 +188,24 @@ static int topk_common(const float *logits, int64_t logits_stride, const int32_t
         a.row_req = slot_rows->row_req;
         a.num_requests = slot_rows->num_requests;
         a.pool_pages = pool_pages;
+        a.warm_pool = warm_pool;
     }
     return launch_status(launch_topk(a, static_cast<cudaStream_t>(stream)));
+}
+
+int dsa_topk_slots_warm(const float *logits, int64_t logits_stride, const dsa_rows *rows, const dsa_cache *latent_cache,
+                        int32_t k, int32_t *idx_out, int32_t *slots_out, int32_t *dev_status, void *stream) {
+    int rc = check_rows(rows);
+    if (rc != DSA_OK) return rc;
+    if (latent_cache == nullptr || latent_cache->page_size != DSA_PAGE_SIZE) return DSA_ERR_INVALID_ARG;
+    if (rows->num_rows > 0 && (slots_out == nullptr || latent_cache->base == nullptr)) return DSA_ERR_INVALID_ARG;
+    if (!aligned(latent_cache->base, 16)) return DSA_ERR_INVALID_ARG;
+    // FP8 rows are one contiguous 576-byte run each; NVFP4 tokens are spread over a page, not warmed
+    const uint8_t *warm =
+        latent_cache->format == DSA_LATENT_FP8 ? static_cast<const uint8_t *>(latent_cache->base) : nullptr;
+    if (latent_cache->format != DSA_LATENT_FP8 && latent_cache->format != DSA_LATENT_NVFP4) return DSA_ERR_UNSUPPORTED;
+    return topk_common(logits, logits_stride, rows->row_ctx, rows->num_rows, rows->max_ctx, k, nullptr, false,
+                       idx_out, dev_status, stream, rows, latent_cache->num_pages, slots_out, warm);
 }
 
 int dsa_topk_slots(const float *logits, int64_t logits_stride, const dsa_rows *rows, int64_t pool_pages, int32_t k,

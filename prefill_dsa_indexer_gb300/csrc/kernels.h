@@ -70,6 +70,9 @@ struct TopkArgs {
     const int32_t *row_req;
     int32_t num_requests;
     int64_t pool_pages;
+    // optional: FP8 latent pool whose selected rows (576 B per slot) are prefetched into L2 as
+    // the slots are written, so the attention that follows gathers from L2
+    const uint8_t *warm_pool;
 };
 
 cudaError_t launch_topk(const TopkArgs &a, cudaStream_t s);

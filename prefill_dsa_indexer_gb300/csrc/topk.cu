@@ -275,7 +275,12 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const TopkArgs a) {
         if (crank == 0)
             for (int i = tid; i < k; i += kThreads) {
                 out[i] = i < n ? i : -1;
-                if constexpr (kSlots) sout[i] = i < n ? slot_of(a, bt_row, nullptr, 0, 0, i) : -1;
+                if constexpr (kSlots) {
+                    const int32_t sl = i < n ? slot_of(a, bt_row, nullptr, 0, 0, i) : -1;
+                    sout[i] = sl;
+                    if (a.warm_pool != nullptr && sl >= 0)
+                        bulk_prefetch_l2(a.warm_pool + static_cast<int64_t>(sl) * DSA_LATENT_DIM, DSA_LATENT_DIM);
+                }
             }
         if constexpr (kHist)  // leave the scorer's histogram zeroed for the next call
             for (int b = tid; b < hspan; b += kThreads) hrow[crank * hspan + b] = 0u;
@@ -723,7 +728,12 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const TopkArgs a) {
                 const uint32_t pos = gb + min(eb, need);
                 if (pos < static_cast<uint32_t>(k)) {
                     out[pos] = c0 + i + q;
-                    if constexpr (kSlots) sout[pos] = slot_of(a, bt_row, s.bt_cache, pg0, npg, c0 + i + q);
+                    if constexpr (kSlots) {
+                        const int32_t sl = slot_of(a, bt_row, s.bt_cache, pg0, npg, c0 + i + q);
+                        sout[pos] = sl;
+                        if (a.warm_pool != nullptr && sl >= 0)
+                            bulk_prefetch_l2(a.warm_pool + static_cast<int64_t>(sl) * DSA_LATENT_DIM, DSA_LATENT_DIM);
+                    }
                 } else {
                     report(a.status, DSA_ERR_BOUNDS);  // inconsistent counts: never expected
                 }

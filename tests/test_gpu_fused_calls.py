@@ -1,6 +1,7 @@
 """Calls that merge or split steps of the path: top-k with the page -> slot
 translation in its output pass (equal to dsa_topk then dsa_page_to_slot, and
-to the oracle's selection and slots), and the decode attention split into
+to the oracle's selection and slots; with the L2 warm-up of the chosen
+latents, equal to it bit for bit), and the decode attention split into
 query preparation + attention (equal bit for bit to the single call)."""
 import numpy as np
 import pytest
@@ -52,6 +53,22 @@ def test_topk_slots_on_indexer_logits():
     ref = oracle.topk_f32(lg.cpu().numpy(), inp.np("row_ctx"), 2048)
     assert np.array_equal(idx.cpu().numpy(), ref)
     assert np.array_equal(slots.cpu().numpy(), oracle.page_to_slot(inp.np("block_table"), inp.np("row_req"), ref))
+
+
+@pytest.mark.parametrize("lat", [I.LATENT_FP8, I.LATENT_NVFP4])
+@pytest.mark.parametrize("k", [2048, 100])
+def test_topk_slots_warm_equals_topk_slots(lat, k):
+    # warming L2 with the chosen latents changes no output
+    inp = U.gpu_inputs(_wl("warm", [1, 100, 2048, 2049, 5000, 9000], lat=lat, k=k, seed=29))
+    lg = U.run_indexer(inp)
+    st = P.new_status()
+    a_idx, a_sl = P.topk_slots(lg, inp.block_table, inp.row_req, inp.row_ctx, inp.max_ctx, inp.lat_pool.shape[0], k,
+                               status=st)
+    b_idx, b_sl = P.topk_slots_warm(lg, inp.block_table, inp.row_req, inp.row_ctx, inp.max_ctx, inp.lat_pool,
+                                    inp.wl.lat_fmt, k, status=st)
+    torch.cuda.synchronize()
+    P.check_status(st)
+    assert torch.equal(a_idx, b_idx) and torch.equal(a_sl, b_sl)
 
 
 @pytest.mark.parametrize("lat", [I.LATENT_FP8, I.LATENT_NVFP4])
