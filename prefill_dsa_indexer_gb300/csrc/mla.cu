@@ -133,18 +133,20 @@ __device__ __forceinline__ void gather_load_fp8(const MlaArgs &a, const int32_t 
         }
     }
     g.slot = slot;
-    const int4 z = make_int4(0, 0, 0, 0);
+    // Predicated loads into zeroed registers: nothing consumes a result before the store pass,
+    // so all 18 loads are in flight together (a select on each result would wait for it).
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
         const int32_t sj = __shfl_sync(0xffffffffu, slot, j);
-        g.v[j] = sj >= 0 ? ldg_nc_v4(a.pool + static_cast<int64_t>(sj) * DSA_LATENT_DIM + lane * 16) : z;
+        g.v[j] = make_int4(0, 0, 0, 0);
+        ldg_nc_v4_if(a.pool + static_cast<int64_t>(max(sj, 0)) * DSA_LATENT_DIM + lane * 16, sj >= 0, g.v[j]);
     }
 #pragma unroll
     for (int b = 0; b < 2; ++b) {
         const int32_t sj = __shfl_sync(0xffffffffu, slot, 8 * b + (lane >> 2));
-        g.v[16 + b] = sj >= 0 ? ldg_nc_v4(a.pool + static_cast<int64_t>(sj) * DSA_LATENT_DIM + DSA_VALUE_DIM +
-                                          (lane & 3) * 16)
-                              : z;
+        g.v[16 + b] = make_int4(0, 0, 0, 0);
+        ldg_nc_v4_if(a.pool + static_cast<int64_t>(max(sj, 0)) * DSA_LATENT_DIM + DSA_VALUE_DIM + (lane & 3) * 16,
+                     sj >= 0, g.v[16 + b]);
     }
 }
 

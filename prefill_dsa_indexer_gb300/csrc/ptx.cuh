@@ -277,6 +277,16 @@ __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
+// 16-byte read-only load into v when `pred` holds (v keeps its value otherwise); the
+// registers are not read until they are used, so a run of these stays in flight.
+__device__ __forceinline__ void ldg_nc_v4_if(const void *p, bool pred, int4 &v) {
+    asm volatile(
+        "{\n\t.reg .pred q;\n\tsetp.ne.u32 q, %5, 0;\n\t"
+        "@q ld.global.nc.L1::no_allocate.v4.s32 {%0, %1, %2, %3}, [%4];\n\t}\n"
+        : "+r"(v.x), "+r"(v.y), "+r"(v.z), "+r"(v.w)
+        : "l"(p), "r"(static_cast<uint32_t>(pred)));
+}
+
 __device__ __forceinline__ int4 ldg_nc_v4(const void *p) {
     int4 v;
     asm volatile("ld.global.nc.L1::no_allocate.v4.s32 {%0, %1, %2, %3}, [%4];"
