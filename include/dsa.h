@@ -394,6 +394,17 @@ int dsa_msa_attention(const void *kv_pool, int64_t num_pages, float k_scale, flo
 /* Workspace bytes dsa_msa_attention needs for num_rows rows. */
 size_t dsa_msa_attention_workspace_size(int32_t num_rows, int32_t heads_per_group);
 
+/*
+ * Failure-path self-test (no counterpart on the pages): one CTA whose
+ * threads wait on a barrier that nothing ever arrives on.  The wait is the
+ * bounded wait every kernel of the library uses; it gives up after the
+ * library's wait limit (4e9 SM cycles, about two seconds), writes
+ * DSA_ERR_TIMEOUT to dev_status (required), and every other waiter of the CTA
+ * then leaves at once.  The kernel exits normally: nothing faults or hangs,
+ * and the context stays usable.  Returns DSA_OK once launched.
+ */
+int dsa_selftest_wait_timeout(int32_t *dev_status, void *stream);
+
 /* Human-readable text of a status code (static storage). */
 const char *dsa_status_string(int status);
 

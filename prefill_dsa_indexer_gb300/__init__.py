@@ -90,6 +90,8 @@ def load_library(path: str | None = None):
     lib.dsa_indexer_topk_workspace_size.argtypes = [I32, I32]
     lib.dsa_topk_slots.restype = ctypes.c_int
     lib.dsa_topk_slots.argtypes = [P, I64, ctypes.POINTER(_Rows), I64, I32, P, P, P, P]
+    lib.dsa_selftest_wait_timeout.restype = ctypes.c_int
+    lib.dsa_selftest_wait_timeout.argtypes = [P, P]
     lib.dsa_topk_slots_warm.restype = ctypes.c_int
     lib.dsa_topk_slots_warm.argtypes = [P, I64, ctypes.POINTER(_Rows), ctypes.POINTER(_Cache), I32, P, P, P, P]
     lib.dsa_sparse_mla_decode_prepare.restype = ctypes.c_int
@@ -116,7 +118,8 @@ EXPORTED = ("dsa_version", "dsa_status_string", "dsa_indexer_logits", "dsa_topk"
             "dsa_sparse_mla_decode_noalloc", "dsa_cache_insert", "dsa_indexer_logits_hist", "dsa_topk_hist",
             "dsa_indexer_topk", "dsa_indexer_topk_workspace_size", "dsa_topk_slots",
             "dsa_sparse_mla_decode_prepare", "dsa_sparse_mla_decode_prepared", "dsa_msa_block_scores",
-            "dsa_msa_select", "dsa_msa_attention", "dsa_msa_attention_workspace_size", "dsa_topk_slots_warm")
+            "dsa_msa_select", "dsa_msa_attention", "dsa_msa_attention_workspace_size", "dsa_topk_slots_warm",
+            "dsa_selftest_wait_timeout")
 HIST_BINS = 65536
 NOALLOC_MAX_ROWS = 8
 
@@ -352,6 +355,11 @@ def sparse_mla_prefill(lat_pool, lat_fmt, tensor_scale, q, slots, sm_scale=DEFAU
                        status=None, stream=None):
     return _mla("dsa_sparse_mla_prefill", lat_pool, lat_fmt, tensor_scale, q, slots, sm_scale, out, lse, None,
                 status, stream)
+
+
+def selftest_wait_timeout(status, stream=None):
+    """dsa_selftest_wait_timeout: a kernel whose bounded wait runs out; status gets DSA_ERR_TIMEOUT."""
+    _check(load_library().dsa_selftest_wait_timeout(_ptr(status), _stream(stream)), "dsa_selftest_wait_timeout")
 
 
 # ------------------------------------------------------------------ MSA block-sparse variant

@@ -14,6 +14,7 @@
 
 #include "../../include/dsa.h"
 #include "kernels.h"
+#include "ptx.cuh"
 
 namespace dsa {
 
@@ -387,6 +388,29 @@ int dsa_cache_insert(const dsa_cache *index_cache, const dsa_cache *latent_cache
     a.latents = latents;
     a.status = dev_status;
     return launch_status(launch_cache_insert(a, static_cast<cudaStream_t>(stream)));
+}
+
+// ------------------------------------------------------------------ failure-path self-test
+
+static __global__ void wait_timeout_kernel(int32_t *status) {
+    __shared__ uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        abort_flag = 0;
+        mbar_init(&bar, 1);  // one arrival that never comes
+        fence_mbar_init();
+    }
+    __syncthreads();
+    // lane 0 of every warp waits: the first to reach the limit reports and raises the abort
+    // flag, the others then return at once
+    if ((threadIdx.x & 31) == 0) mbar_wait(&bar, 0, &abort_flag, status);
+    __syncthreads();
+}
+
+int dsa_selftest_wait_timeout(int32_t *dev_status, void *stream) {
+    if (dev_status == nullptr) return DSA_ERR_INVALID_ARG;
+    wait_timeout_kernel<<<1, 128, 0, static_cast<cudaStream_t>(stream)>>>(dev_status);
+    return launch_status(cudaGetLastError());
 }
 
 // ------------------------------------------------------------------ MSA block-sparse variant
