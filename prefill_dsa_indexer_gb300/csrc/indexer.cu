@@ -37,29 +37,6 @@ namespace {
 constexpr int kIdxPageBytes = DSA_PAGE_SIZE * (DSA_INDEX_DIM + 4);  // 8448
 constexpr int kIdxPageRows = kIdxPageBytes / 128;                    // 66 rows of 128 B
 
-// sum_h w[h] * max(0, acc[h]) over the 32 indexer heads of one (row, key), with packed
-// two-wide fp32 FMAs (the weights are a shared-memory broadcast, 16-byte aligned).  Half of the
-// ReLUs are a max (integer/ALU pipe) and half are x + |x| = 2 max(0, x), exact, on the FMA
-// pipe; those terms are halved at the end (exact), which balances the two pipes.
-__device__ __forceinline__ float head_relu_sum(const uint32_t (&acc)[32], const float *w) {
-    float2 a0 = make_float2(0.f, 0.f), a1 = a0, b0 = a0, b1 = a0;
-    auto rl = [&](int h) { return fmaxf(__uint_as_float(acc[h]), 0.f); };
-    auto r2 = [&](int h) {
-        const float x = __uint_as_float(acc[h]);
-        return x + fabsf(x);
-    };
-#pragma unroll
-    for (int h = 0; h < 32; h += 8) {
-        const float4 wa = *reinterpret_cast<const float4 *>(w + h);
-        const float4 wb = *reinterpret_cast<const float4 *>(w + h + 4);
-        a0 = __ffma2_rn(make_float2(wa.x, wa.y), make_float2(rl(h), rl(h + 1)), a0);
-        b0 = __ffma2_rn(make_float2(wa.z, wa.w), make_float2(r2(h + 2), r2(h + 3)), b0);
-        a1 = __ffma2_rn(make_float2(wb.x, wb.y), make_float2(rl(h + 4), rl(h + 5)), a1);
-        b1 = __ffma2_rn(make_float2(wb.z, wb.w), make_float2(r2(h + 6), r2(h + 7)), b1);
-    }
-    return fmaf(0.5f, (b0.x + b0.y) + (b1.x + b1.y), (a0.x + a0.y) + (a1.x + a1.y));
-}
-
 template <int G>
 struct IdxCfg {
     static constexpr int N = 32 * G;

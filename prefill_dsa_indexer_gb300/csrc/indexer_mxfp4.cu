@@ -431,12 +431,7 @@ __global__ void __launch_bounds__(MxCfg<G>::kThreads, 1)
                                       (rbeg + jj) * 32,
                                   acc);
                         tmem_ld_wait();
-                        const float *wr = wb + (rbeg + jj) * 32;
-                        float s4[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                        for (int h = 0; h < 32; ++h)
-                            s4[h & 3] = fmaf(wr[h], fmaxf(__uint_as_float(acc[h]), 0.f), s4[h & 3]);
-                        const float sum = (s4[0] + s4[1]) + (s4[2] + s4[3]);
+                        const float sum = head_relu_sum(acc, wb + (rbeg + jj) * 32);
                         if (t < ctx[jj]) {
                             const float v = sum * s_t;
                             a.logits[row_off[jj] + t] = v;
