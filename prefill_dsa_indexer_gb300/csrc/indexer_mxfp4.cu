@@ -7,7 +7,7 @@
 //
 // The key stream is half the bytes of the FP8 keys, so the kernel stays
 // HBM-bound as long as the dequantisation keeps up.  Raw pages arrive by plain
-// bulk copies; four converter warps (four lanes per key, one 32-value block
+// bulk copies; eight converter warps (four lanes per key, one 32-value block
 // each, so every shared-memory read is a contiguous 512 bytes per warp)
 // rewrite each key exactly as e4m3 codes times a per-token power of two:
 //     e2m1 * 2^(E_b-127) = [e2m1 * 2^(6 - (E_max - E_b))] * 2^(E_max - 133)
