@@ -44,6 +44,7 @@ constexpr int kWarps = kThreads / 32;
 constexpr int kBins = 2048;
 constexpr int kCacheElems = 40960;
 constexpr int kCandCap = 4096;
+static_assert(DSA_MAX_TOPK <= kCandCap, "a chunk's selections are staged in cand_all");
 constexpr int kMaxCluster = 16;
 constexpr int kMinChunk = 4096;  // a row is not cut into chunks shorter than this
 constexpr int kBtCache = 1026;   // block-table entries of a chunk kept in shared memory (64K keys)
@@ -676,8 +677,11 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const TopkArgs a) {
 
     // ---- 4. ordered compaction.  Warp w owns a contiguous segment of the chunk and walks it
     // 128 keys at a time, four consecutive keys per lane (lane order = position order):
-    // pass 1 counts keys > T and == T per warp, pass 2 writes positions after the lower
-    // warps' and lower chunks' selections.
+    // pass 1 counts keys > T and == T per warp, pass 2 places each selected position after
+    // the lower warps' and lower chunks' selections.  A selection's output index is its rank
+    // among the row's selections in position order, so this chunk's selections fill one
+    // contiguous range [p0, p1): pass 2 stages them in shared memory (cand_all, free by now)
+    // and all threads then write the outputs (and slots) of that range together.
     const int seg = ((nloc + kWarps - 1) / kWarps + 127) & ~127;
     const int w0 = min(nloc, warp * seg), w1 = min(nloc, w0 + seg);
     uint32_t ngt = 0, neq = 0;
@@ -699,9 +703,13 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const TopkArgs a) {
         s.weq[warp] = neq;
     }
     __syncthreads();
+    uint32_t p0, p1;
     {
         const uint32_t vg = s.wgt[lane], ve = s.weq[lane];
         const uint32_t ig = warp_incl_scan32(vg, lane), ie = warp_incl_scan32(ve, lane);
+        const uint32_t tg = __shfl_sync(0xffffffffu, ig, 31), te = __shfl_sync(0xffffffffu, ie, 31);
+        p0 = gt_before + min(eq_before, need);            // selections in the lower chunks
+        p1 = gt_before + tg + min(eq_before + te, need);  // ... and in this one
         gt_before += __shfl_sync(0xffffffffu, ig - vg, warp);
         eq_before += __shfl_sync(0xffffffffu, ie - ve, warp);
     }
@@ -726,23 +734,28 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const TopkArgs a) {
             const bool gt = in && kq[q] > T, eq = in && kq[q] == T;
             if (gt || (eq && eb < need)) {
                 const uint32_t pos = gb + min(eb, need);
-                if (pos < static_cast<uint32_t>(k)) {
-                    out[pos] = c0 + i + q;
-                    if constexpr (kSlots) {
-                        const int32_t sl = slot_of(a, bt_row, s.bt_cache, pg0, npg, c0 + i + q);
-                        sout[pos] = sl;
-                        if (a.warm_pool != nullptr && sl >= 0)
-                            bulk_prefetch_l2(a.warm_pool + static_cast<int64_t>(sl) * DSA_LATENT_DIM, DSA_LATENT_DIM);
-                    }
-                } else {
+                if (pos >= p0 && pos < p1 && pos < static_cast<uint32_t>(k))
+                    s.cand_all[pos - p0] = static_cast<uint32_t>(c0 + i + q);
+                else
                     report(a.status, DSA_ERR_BOUNDS);  // inconsistent counts: never expected
-                }
             }
             gb += gt ? 1u : 0u;
             eb += eq ? 1u : 0u;
         }
         gt_before += tot & 0xffffu;
         eq_before += tot >> 16;
+    }
+    __syncthreads();
+    const uint32_t pe = min(p1, static_cast<uint32_t>(k));  // p1 - p0 <= k <= kCandCap
+    for (uint32_t j = p0 + tid; j < pe; j += kThreads) {
+        const int32_t t = static_cast<int32_t>(s.cand_all[j - p0]);
+        out[j] = t;
+        if constexpr (kSlots) {
+            const int32_t sl = slot_of(a, bt_row, s.bt_cache, pg0, npg, t);
+            sout[j] = sl;
+            if (a.warm_pool != nullptr && sl >= 0)
+                bulk_prefetch_l2(a.warm_pool + static_cast<int64_t>(sl) * DSA_LATENT_DIM, DSA_LATENT_DIM);
+        }
     }
     cluster_wait();  // no CTA leaves while a peer may still read its shared memory
 }
