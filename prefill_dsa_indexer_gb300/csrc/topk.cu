@@ -676,74 +676,138 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const TopkArgs a) {
     const uint32_t T = base;  // exact threshold key; `need` keys equal to T are taken (lowest positions)
 
     // ---- 4. ordered compaction.  Warp w owns a contiguous segment of the chunk and walks it
-    // 128 keys at a time, four consecutive keys per lane (lane order = position order):
-    // pass 1 counts keys > T and == T per warp, pass 2 places each selected position after
-    // the lower warps' and lower chunks' selections.  A selection's output index is its rank
-    // among the row's selections in position order, so this chunk's selections fill one
-    // contiguous range [p0, p1): pass 2 stages them in shared memory (cand_all, free by now)
-    // and all threads then write the outputs (and slots) of that range together.
+    // 128 keys at a time, four consecutive keys per lane (lane order = position order).  A
+    // selection's output index is its rank among the row's selections in position order, so
+    // this chunk's selections fill one contiguous range [p0, p1); they are staged in shared
+    // memory (cand_all, free by now) and all threads then write the outputs (and slots) of
+    // that range together.
     const int seg = ((nloc + kWarps - 1) / kWarps + 127) & ~127;
     const int w0 = min(nloc, warp * seg), w1 = min(nloc, w0 + seg);
-    uint32_t ngt = 0, neq = 0;
-    for (int i0 = w0; i0 < w1; i0 += 128) {
-        const int i = i0 + 4 * lane;
-        uint32_t kq[4];
-        keys4(s, chunk, i, w1, kq);
-        uint32_t g = 0, e = 0;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            g += (i + q < w1 && kq[q] > T) ? 1u : 0u;
-            e += (i + q < w1 && kq[q] == T) ? 1u : 0u;
-        }
-        ngt += __reduce_add_sync(0xffffffffu, g);
-        neq += __reduce_add_sync(0xffffffffu, e);
-    }
-    if (lane == 0) {
-        s.wgt[warp] = ngt;
-        s.weq[warp] = neq;
-    }
-    __syncthreads();
     uint32_t p0, p1;
-    {
-        const uint32_t vg = s.wgt[lane], ve = s.weq[lane];
-        const uint32_t ig = warp_incl_scan32(vg, lane), ie = warp_incl_scan32(ve, lane);
-        const uint32_t tg = __shfl_sync(0xffffffffu, ig, 31), te = __shfl_sync(0xffffffffu, ie, 31);
-        p0 = gt_before + min(eq_before, need);            // selections in the lower chunks
-        p1 = gt_before + tg + min(eq_before + te, need);  // ... and in this one
-        gt_before += __shfl_sync(0xffffffffu, ig - vg, warp);
-        eq_before += __shfl_sync(0xffffffffu, ie - ve, warp);
-    }
-    for (int i0 = w0; i0 < w1; i0 += 128) {
-        const int i = i0 + 4 * lane;
-        uint32_t kq[4];
-        keys4(s, chunk, i, w1, kq);
-        uint32_t g = 0, e = 0;
+    if (chunk.ncache == nloc) {
+        // One pass: each warp stages the positions of its keys >= T (bit 31 marks == T) in
+        // order at the start of its own segment of the shared-memory copy, overwriting keys
+        // it has already read (a step's writes end before the step's last key, and every lane
+        // has read its keys before the scan that places the writes).  Then each warp walks
+        // its short list and keeps the keys > T and the first `need` keys == T of the row.
+        uint32_t ns = 0, ngt = 0, neq = 0;
+        for (int i0 = w0; i0 < w1; i0 += 128) {
+            const int i = i0 + 4 * lane;
+            uint32_t kq[4];
+            keys4(s, chunk, i, w1, kq);
+            uint32_t g = 0, e = 0;
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            g += (i + q < w1 && kq[q] > T) ? 1u : 0u;
-            e += (i + q < w1 && kq[q] == T) ? 1u : 0u;
+            for (int q = 0; q < 4; ++q) {
+                g += (i + q < w1 && kq[q] > T) ? 1u : 0u;
+                e += (i + q < w1 && kq[q] == T) ? 1u : 0u;
+            }
+            const uint32_t packed = g | (e << 16);  // at most 128 each per warp step
+            const uint32_t incl = warp_incl_scan32(packed, lane);
+            const uint32_t tot = __shfl_sync(0xffffffffu, incl, 31);
+            const uint32_t ex = incl - packed;
+            uint32_t at = static_cast<uint32_t>(w0) + ns + (ex & 0xffffu) + (ex >> 16);
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                if (i + q < w1 && kq[q] >= T)
+                    s.cache[at++] = static_cast<uint32_t>(c0 + i + q) | (kq[q] == T ? 0x80000000u : 0u);
+            ngt += tot & 0xffffu;
+            neq += tot >> 16;
+            ns += (tot & 0xffffu) + (tot >> 16);
         }
-        // counts of >T and ==T packed in one word: at most 128 each per warp step
-        const uint32_t packed = g | (e << 16);
-        const uint32_t incl = warp_incl_scan32(packed, lane);
-        const uint32_t tot = __shfl_sync(0xffffffffu, incl, 31);
-        uint32_t gb = gt_before + ((incl - packed) & 0xffffu), eb = eq_before + ((incl - packed) >> 16);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const bool in = i + q < w1;
-            const bool gt = in && kq[q] > T, eq = in && kq[q] == T;
-            if (gt || (eq && eb < need)) {
+        if (lane == 0) {
+            s.wgt[warp] = ngt;
+            s.weq[warp] = neq;
+        }
+        __syncthreads();
+        {
+            const uint32_t vg = s.wgt[lane], ve = s.weq[lane];
+            const uint32_t ig = warp_incl_scan32(vg, lane), ie = warp_incl_scan32(ve, lane);
+            const uint32_t tg = __shfl_sync(0xffffffffu, ig, 31), te = __shfl_sync(0xffffffffu, ie, 31);
+            p0 = gt_before + min(eq_before, need);            // selections in the lower chunks
+            p1 = gt_before + tg + min(eq_before + te, need);  // ... and in this one
+            gt_before += __shfl_sync(0xffffffffu, ig - vg, warp);
+            eq_before += __shfl_sync(0xffffffffu, ie - ve, warp);
+        }
+        const unsigned lt = (1u << lane) - 1u;
+        for (uint32_t j0 = 0; j0 < ns; j0 += 32) {
+            const uint32_t j = j0 + lane;
+            const uint32_t v = j < ns ? s.cache[w0 + j] : 0u;
+            const bool is_eq = j < ns && (v >> 31) != 0u, is_gt = j < ns && (v >> 31) == 0u;
+            const unsigned bg = __ballot_sync(0xffffffffu, is_gt), be = __ballot_sync(0xffffffffu, is_eq);
+            const uint32_t gb = gt_before + __popc(bg & lt), eb = eq_before + __popc(be & lt);
+            if (is_gt || (is_eq && eb < need)) {
                 const uint32_t pos = gb + min(eb, need);
                 if (pos >= p0 && pos < p1 && pos < static_cast<uint32_t>(k))
-                    s.cand_all[pos - p0] = static_cast<uint32_t>(c0 + i + q);
+                    s.cand_all[pos - p0] = v & 0x7fffffffu;
                 else
                     report(a.status, DSA_ERR_BOUNDS);  // inconsistent counts: never expected
             }
-            gb += gt ? 1u : 0u;
-            eb += eq ? 1u : 0u;
+            gt_before += __popc(bg);
+            eq_before += __popc(be);
         }
-        gt_before += tot & 0xffffu;
-        eq_before += tot >> 16;
+    } else {
+        // Chunk larger than the shared-memory copy: pass 1 counts keys > T and == T per warp,
+        // pass 2 places each selected position after the lower warps' and chunks' selections.
+        uint32_t ngt = 0, neq = 0;
+        for (int i0 = w0; i0 < w1; i0 += 128) {
+            const int i = i0 + 4 * lane;
+            uint32_t kq[4];
+            keys4(s, chunk, i, w1, kq);
+            uint32_t g = 0, e = 0;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                g += (i + q < w1 && kq[q] > T) ? 1u : 0u;
+                e += (i + q < w1 && kq[q] == T) ? 1u : 0u;
+            }
+            ngt += __reduce_add_sync(0xffffffffu, g);
+            neq += __reduce_add_sync(0xffffffffu, e);
+        }
+        if (lane == 0) {
+            s.wgt[warp] = ngt;
+            s.weq[warp] = neq;
+        }
+        __syncthreads();
+        {
+            const uint32_t vg = s.wgt[lane], ve = s.weq[lane];
+            const uint32_t ig = warp_incl_scan32(vg, lane), ie = warp_incl_scan32(ve, lane);
+            const uint32_t tg = __shfl_sync(0xffffffffu, ig, 31), te = __shfl_sync(0xffffffffu, ie, 31);
+            p0 = gt_before + min(eq_before, need);            // selections in the lower chunks
+            p1 = gt_before + tg + min(eq_before + te, need);  // ... and in this one
+            gt_before += __shfl_sync(0xffffffffu, ig - vg, warp);
+            eq_before += __shfl_sync(0xffffffffu, ie - ve, warp);
+        }
+        for (int i0 = w0; i0 < w1; i0 += 128) {
+            const int i = i0 + 4 * lane;
+            uint32_t kq[4];
+            keys4(s, chunk, i, w1, kq);
+            uint32_t g = 0, e = 0;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                g += (i + q < w1 && kq[q] > T) ? 1u : 0u;
+                e += (i + q < w1 && kq[q] == T) ? 1u : 0u;
+            }
+            // counts of >T and ==T packed in one word: at most 128 each per warp step
+            const uint32_t packed = g | (e << 16);
+            const uint32_t incl = warp_incl_scan32(packed, lane);
+            const uint32_t tot = __shfl_sync(0xffffffffu, incl, 31);
+            uint32_t gb = gt_before + ((incl - packed) & 0xffffu), eb = eq_before + ((incl - packed) >> 16);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const bool in = i + q < w1;
+                const bool gt = in && kq[q] > T, eq = in && kq[q] == T;
+                if (gt || (eq && eb < need)) {
+                    const uint32_t pos = gb + min(eb, need);
+                    if (pos >= p0 && pos < p1 && pos < static_cast<uint32_t>(k))
+                        s.cand_all[pos - p0] = static_cast<uint32_t>(c0 + i + q);
+                    else
+                        report(a.status, DSA_ERR_BOUNDS);  // inconsistent counts: never expected
+                }
+                gb += gt ? 1u : 0u;
+                eb += eq ? 1u : 0u;
+            }
+            gt_before += tot & 0xffffu;
+            eq_before += tot >> 16;
+        }
     }
     __syncthreads();
     const uint32_t pe = min(p1, static_cast<uint32_t>(k));  // p1 - p0 <= k <= kCandCap
