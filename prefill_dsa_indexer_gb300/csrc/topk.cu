@@ -44,6 +44,7 @@ constexpr int kWarps = kThreads / 32;
 constexpr int kBins = 2048;
 constexpr int kCacheElems = 40960;
 constexpr int kCandCap = 4096;
+constexpr int kRankMax = 256;  // up to this many gathered candidates, the threshold is found by ranking
 static_assert(DSA_MAX_TOPK <= kCandCap, "a chunk's selections are staged in cand_all");
 constexpr int kMaxCluster = 16;
 constexpr int kMinChunk = 4096;  // a row is not cut into chunks shorter than this
@@ -69,6 +70,7 @@ struct TopkSmem {
     uint32_t hpub;       // histogram path: this CTA's slice total (read by the cluster)
     uint32_t hsel[2];    // histogram path: owner rank, the cluster's keys above its slice
     uint32_t hres[3];    // histogram path, owner: the bin, the cluster's keys above it / in it
+    uint32_t rank_t[2];  // ranking: the threshold key and the candidates above it ([1] = ~0: none)
     int32_t bad;
 };
 
@@ -295,6 +297,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const TopkArgs a) {
     if (tid == 0) {
         s.bad = 0;
         s.ncand = 0;
+        s.rank_t[1] = 0xffffffffu;
     }
     for (int b = tid; b < kBins; b += kThreads) s.hist[b] = 0;
     // the chunk's block-table entries, read now so that writing slots at the end stays local
@@ -607,6 +610,36 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const TopkArgs a) {
     uint32_t gt_before = 0, eq_before = 0;
     if (gathered) {
         const int nc = static_cast<int>(min(s.roff[CL], static_cast<uint32_t>(kCandCap)));
+        if (top > base && nc <= kRankMax) {
+            // Few candidates (all inside [base, top]): the threshold is the candidate with fewer
+            // than `need` candidates above it and at least `need` at or above it.  Every thread
+            // holding that key writes the same two values.
+            if (tid < nc) {
+                const uint32_t key = s.cand_all[tid];
+                uint32_t gt = 0, ge = 0;
+                const int nc4 = nc & ~3;
+                for (int j = 0; j < nc4; j += 4) {
+                    const uint4 v = *reinterpret_cast<const uint4 *>(&s.cand_all[j]);
+                    gt += (v.x > key ? 1u : 0u) + (v.y > key ? 1u : 0u) + (v.z > key ? 1u : 0u) + (v.w > key ? 1u : 0u);
+                    ge += (v.x >= key ? 1u : 0u) + (v.y >= key ? 1u : 0u) + (v.z >= key ? 1u : 0u) +
+                          (v.w >= key ? 1u : 0u);
+                }
+                for (int j = nc4; j < nc; ++j) {
+                    const uint32_t v = s.cand_all[j];
+                    gt += v > key ? 1u : 0u;
+                    ge += v >= key ? 1u : 0u;
+                }
+                if (gt < need && need <= ge) {
+                    s.rank_t[0] = key;
+                    s.rank_t[1] = gt;
+                }
+            }
+            __syncthreads();
+            if (s.rank_t[1] != 0xffffffffu) {  // else (inconsistent counts) the rounds below decide
+                base = top = s.rank_t[0];
+                need -= s.rank_t[1];
+            }
+        }
         while (top > base) {
             const uint32_t span = top - base;
             const int bits = 32 - __clz(span);
