@@ -660,27 +660,33 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const TopkArgs a) {
         const uint32_t T = base;
         const int lower = static_cast<int>(min(s.roff[crank], static_cast<uint32_t>(kCandCap)));
         uint32_t g = 0, e = 0;
-        for (int i = tid; i < lower; i += kThreads) {
-            const uint32_t key = s.cand_all[i];
-            g += key > T;
-            e += key == T;
-        }
+        if (lower <= kThreads) {  // one candidate per thread: the barrier counts them
+            const uint32_t key = tid < lower ? s.cand_all[tid] : 0u;
+            g = static_cast<uint32_t>(__syncthreads_count(tid < lower && key > T));
+            e = static_cast<uint32_t>(__syncthreads_count(tid < lower && key == T));
+        } else {
+            for (int i = tid; i < lower; i += kThreads) {
+                const uint32_t key = s.cand_all[i];
+                g += key > T;
+                e += key == T;
+            }
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            g += __shfl_xor_sync(0xffffffffu, g, o);
-            e += __shfl_xor_sync(0xffffffffu, e, o);
-        }
-        if (lane == 0) {
-            s.red[warp] = g;
-            s.red[kWarps + warp] = e;
-        }
-        __syncthreads();
-        g = s.red[lane];
-        e = s.red[kWarps + lane];
+            for (int o = 16; o > 0; o >>= 1) {
+                g += __shfl_xor_sync(0xffffffffu, g, o);
+                e += __shfl_xor_sync(0xffffffffu, e, o);
+            }
+            if (lane == 0) {
+                s.red[warp] = g;
+                s.red[kWarps + warp] = e;
+            }
+            __syncthreads();
+            g = s.red[lane];
+            e = s.red[kWarps + lane];
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            g += __shfl_xor_sync(0xffffffffu, g, o);
-            e += __shfl_xor_sync(0xffffffffu, e, o);
+            for (int o = 16; o > 0; o >>= 1) {
+                g += __shfl_xor_sync(0xffffffffu, g, o);
+                e += __shfl_xor_sync(0xffffffffu, e, o);
+            }
         }
         gt_before = s.before[0] + g;
         eq_before = e;
