@@ -104,6 +104,12 @@ def _topk_cases():
     tb[2, :] = 1.0
     tb[2, rng.choice(100000, 50, replace=False)] = 9.0
     cases["ties_beyond_candidates"] = (tb, np.array([20000, 100000, 100000], dtype=np.int32), 2048)
+    # a threshold bin of ~1,500 equal keys in a row cut over several CTAs: the cluster gathers
+    # many candidates from its peers and refines them by histogram rounds, not by ranking
+    tp = rng.uniform(0.0, 1.0, (2, 100000)).astype(np.float32)
+    tp[:, rng.choice(100000, 1500, replace=False)] = 2.0
+    tp[0, rng.choice(100000, 1000, replace=False)] = 3.0
+    cases["ties_many_candidates"] = (tp, np.array([100000, 99999], dtype=np.int32), 2048)
     s = rng.standard_normal((3, 3000)).astype(np.float32)
     cases["small_k"] = (s, np.array([3000, 10, 1], dtype=np.int32), 5)
     w = np.concatenate([np.full((1, 3000), 1e30, np.float32), np.full((1, 3000), -1e30, np.float32)])
