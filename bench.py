@@ -691,7 +691,8 @@ def main():
                 "algorithmic_flops": flops, "ms_per_launch": idx_ms}
     else:
         achieved = idx_bytes / (idx_ms / 1000.0) / 1e9
-        roof = {"kernel": "indexer_fp8_kernel<1>" if wl.key_fmt == I.KEY_FP8 else "indexer_mxfp4_kernel<1>",
+        kname = "indexer_fp8_kernel" if wl.key_fmt == I.KEY_FP8 else "indexer_mxfp4_kernel"
+        roof = {"kernel": f"{kname}<{wl.rows_per_group}>",
                 "bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
                 "peak_kind": peak_kind, "algorithmic_bytes": idx_bytes, "ms_per_launch": idx_ms}
     traffic = None
