@@ -310,19 +310,24 @@ def run_msa(args, rank, world, local, dist):
         step(i, s=stream)
     torch.cuda.synchronize()
     P.check_status(st, "warm-up")
-    # CUDA graphs of 16 x copies consecutive steps, event nodes around every block-score launch
+    # CUDA graphs of 16 x copies consecutive steps; a second graph of the same steps carries event
+    # nodes around every block-score launch and is replayed after the timed loop to time them
     cap = torch.cuda.Stream()
     cap.wait_stream(stream)
     n = 16 * copies
-    g = torch.cuda.CUDAGraph()
+    g, gp = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
     evp = [(torch.cuda.Event(enable_timing=True, external=True), torch.cuda.Event(enable_timing=True, external=True))
            for _ in range(n)]
     with torch.cuda.stream(cap):
         with torch.cuda.graph(g, stream=cap):
             for k in range(n):
+                step(k, s=cap)
+        with torch.cuda.graph(gp, stream=cap):
+            for k in range(n):
                 step(k, ev=evp[k], s=cap)
     stream.wait_stream(cap)
     g.replay()
+    gp.replay()
     torch.cuda.synchronize()
     reps = max(1, args.steps // n)
     steps = reps * n
@@ -344,19 +349,32 @@ def run_msa(args, rank, world, local, dist):
     total_ms = t0.elapsed_time(t1)
     total_ms = max_over_ranks(total_ms, dist)
     P.check_status(st, "timed steps")
+    for _ in range(3):
+        gp.replay()
+    torch.cuda.synchronize()
     score_ms = sum(a.elapsed_time(b) for a, b in evp) / len(evp)
     value = replica_throughput(world, R, steps, total_ms)
     # end to end: queries in from pinned host memory, outputs back, inside the timed region
     hq, hqi = inp.q.cpu().pin_memory(), inp.q_idx.cpu().pin_memory()
     dq, dqi = torch.empty_like(inp.q), torch.empty_like(inp.q_idx)
     ho, hl = torch.empty(out.shape, dtype=torch.float32).pin_memory(), torch.empty(lse.shape).pin_memory()
+    # one CUDA graph per cache copy for the step between the copies
+    ge = [torch.cuda.CUDAGraph() for _ in range(copies)]
+    cap.wait_stream(stream)
+    with torch.cuda.stream(cap):
+        for c in range(copies):
+            with torch.cuda.graph(ge[c], stream=cap):
+                step(c, q=dq, q_idx=dqi, s=cap)
+    stream.wait_stream(cap)
+    torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     for i in range(args.warmup + args.steps):
         if i == args.warmup:
             e0.record(stream)
         dq.copy_(hq, non_blocking=True)
         dqi.copy_(hqi, non_blocking=True)
-        step(i, q=dq, q_idx=dqi, s=stream)
+        with torch.cuda.stream(stream):
+            ge[i % copies].replay()
         ho.copy_(out, non_blocking=True)
         hl.copy_(lse, non_blocking=True)
     e1.record(stream)
@@ -388,7 +406,8 @@ def run_msa(args, rank, world, local, dist):
                 "h2d_bytes_per_step": hq.numel() + hqi.numel(), "d2h_bytes_per_step": (ho.numel() + hl.numel()) * 4,
                 "ms_per_step": e2e_ms / args.steps},
         "gpu_launches": 4 * steps,
-        "launch": f"CUDA graphs of {n} consecutive steps; block scores timed by event nodes inside the graph",
+        "launch": f"CUDA graphs of {n} consecutive steps; block scores timed after the timed loop by event "
+                  f"nodes around each launch in a replay of the same steps",
         "clocks": clk.summary(h0, h1),
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -511,11 +530,12 @@ def main():
 
         side = torch.cuda.Stream()
 
-        def capture(n):
+        def capture(n, events):
             # per step: the decode query prep forks onto a side branch (it needs only the query)
-            # and joins before the attention; scorer -> top-k+slots -> attention on the main branch
+            # and joins before the attention; scorer -> top-k+slots -> attention on the main branch.
+            # events: event nodes around every scorer launch (the indexer timing graph only)
             g = torch.cuda.CUDAGraph()
-            evp = [(ext_event(), ext_event()) for _ in range(n)]
+            evp = [(ext_event(), ext_event()) for _ in range(n)] if events else []
             with torch.cuda.stream(cap):
                 with torch.cuda.graph(g, stream=cap):
                     for k in range(n):
@@ -525,9 +545,11 @@ def main():
                             side.wait_stream(cap)
                             with torch.cuda.stream(side):
                                 L.prepare(inp.q_mla)
-                        evp[k][0].record(cap)
+                        if events:
+                            evp[k][0].record(cap)
                         indexer(L)
-                        evp[k][1].record(cap)
+                        if events:
+                            evp[k][1].record(cap)
                         if fork:
                             cap.wait_stream(side)
                         L.select(inp.row_req, inp.row_ctx, inp.q_mla, prepared=fork)
@@ -536,9 +558,12 @@ def main():
         if graph_mode == "multi-step":
             full, tail = divmod(args.steps, per_graph)
             if full:
-                runs.append((capture(per_graph), full))
+                runs.append((capture(per_graph, False), full))
             if tail:
-                runs.append((capture(tail), 1))
+                runs.append((capture(tail, False), 1))
+            # the indexer's launches are timed in a separate replay of the same steps with event
+            # nodes around each scorer launch, after the timed loop
+            probe = capture(min(per_graph, args.steps), True)
         else:
             pairs = []
             for c in range(len(layers)):
@@ -553,6 +578,8 @@ def main():
         torch.cuda.synchronize()
         for (g, _), _n in runs:  # graph warm-up: one replay of each run
             g.replay()
+        if graph_mode == "multi-step":
+            probe[0].replay()
         if graph_mode == "two-graphs":
             for i in range(args.warmup):
                 g_idx, g_rest = pairs[i % len(pairs)]
@@ -590,8 +617,10 @@ def main():
         dist.barrier()
     total_ms = t_start.elapsed_time(t_stop)
     if graph_mode == "multi-step":
-        # every step of each run's last replay (the final 16 x copies steps of the timed loop)
-        samples = [a.elapsed_time(b) for (g, evp), _r in runs for a, b in evp]
+        for _r in range(3):
+            probe[0].replay()
+        torch.cuda.synchronize()
+        samples = [a.elapsed_time(b) for a, b in probe[1]]  # every step of the last replay
     else:
         samples = [a.elapsed_time(b) for a, b in evs]
     idx_ms = sum(samples) / len(samples)
@@ -630,10 +659,14 @@ def main():
     d2h = host_res[0].numel() * 4
     h2d_s, d2h_s = torch.cuda.Stream(), torch.cuda.Stream()
 
-    def e2e_run(n_steps):
+    def e2e_issue(n_steps, main, body):
+        # n_steps steps: step i's inputs copy in on h2d_s while step i - 1 computes on `main`, and
+        # its results copy out on d2h_s while step i + 1 computes; events carry the buffer reuse
         in_ready = [torch.cuda.Event() for _ in range(n_steps)]
         done = [torch.cuda.Event() for _ in range(n_steps)]
         out_copied = [torch.cuda.Event() for _ in range(n_steps)]
+        h2d_s.wait_stream(main)
+        d2h_s.wait_stream(main)
 
         def h2d_copy(i):
             with torch.cuda.stream(h2d_s):
@@ -647,28 +680,69 @@ def main():
             if i + 1 < n_steps:
                 h2d_copy(i + 1)
             L = layers[i % len(layers)]
-            stream.wait_event(in_ready[i])
+            main.wait_event(in_ready[i])
             if i >= len(layers):
-                stream.wait_event(out_copied[i - len(layers)])  # this layer's outputs were copied out
-            d = dev_in[i % 2]
-            L.run(d["row_req"], d["row_ctx"], d["q_idx"], d["head_w"], d["q_mla"], stream=stream)
-            done[i].record(stream)
+                main.wait_event(out_copied[i - len(layers)])  # this layer's outputs were copied out
+            with torch.cuda.stream(main):
+                body(i, L, dev_in[i % 2])
+            done[i].record(main)
             with torch.cuda.stream(d2h_s):
                 d2h_s.wait_event(done[i])
                 if i >= 2:
                     d2h_s.wait_event(out_copied[i - 2])  # host buffer i % 2 is free again
                 host_res[i % 2].copy_(L.outputs, non_blocking=True)
                 out_copied[i].record(d2h_s)
-        stream.wait_stream(d2h_s)
+        main.wait_stream(d2h_s)
+        main.wait_stream(h2d_s)
 
-    e2e_run(args.warmup)
+    def eager_body(i, L, d):
+        L.run(d["row_req"], d["row_ctx"], d["q_idx"], d["head_w"], d["q_mla"], stream=torch.cuda.current_stream())
+
+    side_e = torch.cuda.Stream()
+
+    def graph_body(i, L, d):  # the query prep forks onto a parallel branch
+        cur = torch.cuda.current_stream()
+        fork = not L.prefill
+        if fork:
+            side_e.wait_stream(cur)
+            with torch.cuda.stream(side_e):
+                L.prepare(d["q_mla"])
+        L.score(d["row_req"], d["row_ctx"], d["q_idx"], d["head_w"])
+        if fork:
+            cur.wait_stream(side_e)
+        L.select(d["row_req"], d["row_ctx"], d["q_mla"], prepared=fork)
+
+    # With graphs, each step between its copies is one replay of a graph of that step's calls,
+    # one graph per input buffer and cache copy.  (Capturing the copies too, as memcpy nodes in
+    # graphs of many steps, was no faster for decode and slower for the prefill's large copies.)
+    e2e_graphs = None
+    if graph_mode != "eager":
+        cap_e = torch.cuda.Stream()
+        cap_e.wait_stream(stream)
+        e2e_graphs = []
+        for b in range(2):
+            row = []
+            for L in layers:
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.stream(cap_e):
+                    with torch.cuda.graph(g, stream=cap_e):
+                        graph_body(0, L, dev_in[b])
+                row.append(g)
+            e2e_graphs.append(row)
+        stream.wait_stream(cap_e)
+        torch.cuda.synchronize()
+
+    def replay_body(i, L, d):
+        e2e_graphs[i % 2][i % len(layers)].replay()
+
+    body = replay_body if e2e_graphs is not None else eager_body
+    e2e_issue(args.warmup, stream, body)
     torch.cuda.synchronize()
     if dist is not None:
         dist.barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    h2d_s.wait_stream(stream)
-    e2e_run(args.steps)
+    e2e_issue(args.steps, stream, body)
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1)
@@ -720,10 +794,13 @@ def main():
         "layer_frac_of_8tbs": layer_bytes / (ms_per_step / 1000.0) / 8e12,
         "roofline": dict(roof, traffic=traffic),
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "ms_per_step": e2e_ms / args.steps},
+                "ms_per_step": e2e_ms / args.steps,
+                "launch": "one CUDA-graph replay per step between its copies" if e2e_graphs is not None
+                else "eager launches between the copies"},
         "gpu_launches": launches_per_step * args.steps,
         "launch": {"multi-step": f"CUDA graphs of {16 * copies} consecutive steps (decode query prep on a "
-                                 f"parallel branch); indexer timed by event nodes inside the graph "
+                                 f"parallel branch); indexer timed after the timed loop by event nodes "
+                                 f"around each scorer launch in a replay of the same steps "
                                  f"({len(samples)} launches sampled)",
                    "two-graphs": "CUDA-graph replay (indexer graph + rest-of-step graph), stream events between",
                    "eager": "eager launches, stream events around the indexer"}[graph_mode],
