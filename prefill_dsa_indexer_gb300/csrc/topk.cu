@@ -22,12 +22,16 @@
 //   3. Once the interval holds at most kCandCap keys, every CTA publishes its
 //      keys inside it (its candidates) and its count above it; every CTA then
 //      gathers all of them in rank order and refines alone (identically) down
-//      to the exact threshold key T and the number of keys equal to T to take.
-//      The gathered candidates also give every CTA the number of selected keys
-//      in the lower-ranked chunks, so no further cluster barrier is needed.
-//   4. The selection is written in position order: warp-contiguous segments,
-//      ballot counts, warp prefix sums.  Output order and values never depend
-//      on timing.
+//      to the exact threshold key T and the number of keys equal to T to take:
+//      by ranking when there are at most kRankMax candidates (each counts the
+//      candidates above and at it), else by further histogram rounds.  The
+//      gathered candidates also give every CTA the number of selected keys in
+//      the lower-ranked chunks, so no further cluster barrier is needed.
+//   4. The selection is written in position order.  A chunk's selections fill
+//      one contiguous range of the output; each warp stages its segment's keys
+//      >= T in order (one pass when the chunk is in shared memory, else a
+//      counting pass and a placing pass), and all threads then write the
+//      range.  Output order and values never depend on timing.
 #include <cooperative_groups.h>
 
 #include "kernels.h"
