@@ -104,3 +104,9 @@ def test_python_binding_refuses_cpu_tensors():
     x = torch.zeros(4, 8)
     with pytest.raises(P.DsaError):
         P.topk(x, torch.zeros(4, dtype=torch.int32), 8, 4)
+
+
+def test_missing_library_raises_instead_of_falling_back(tmp_path):
+    import prefill_dsa_indexer_gb300 as P
+    with pytest.raises(P.DsaError):
+        P.load_library(str(tmp_path / "libdsa.so"))
