@@ -110,3 +110,48 @@ def test_missing_library_raises_instead_of_falling_back(tmp_path):
     import prefill_dsa_indexer_gb300 as P
     with pytest.raises(P.DsaError):
         P.load_library(str(tmp_path / "libdsa.so"))
+
+
+def test_host_validation_of_the_msa_insert_and_warm_calls(lib):
+    import prefill_dsa_indexer_gb300 as P
+    fake, odd = ctypes.c_void_p(0x10000), ctypes.c_void_p(0x10004)
+    rows = lambda n, ctx, stride, g=1: P._Rows(fake, stride, 1, fake, fake, n, ctx, g)
+    # MSA block scores: row groups of 1, 2, 4 or 8; block table, scores and alignment checked
+    r = rows(3, 256, 2, 3)
+    assert lib.dsa_msa_block_scores(fake, 10, ctypes.byref(r), fake, fake, 2, None, None) == P.ERR_UNSUPPORTED
+    r = rows(1, 1024, 2)
+    assert lib.dsa_msa_block_scores(fake, 10, ctypes.byref(r), fake, fake, 8, None, None) == P.ERR_INVALID_ARG
+    r = rows(1, 256, 2)
+    assert lib.dsa_msa_block_scores(fake, 10, ctypes.byref(r), fake, fake, 1, None, None) == P.ERR_INVALID_ARG
+    assert lib.dsa_msa_block_scores(odd, 10, ctypes.byref(r), fake, fake, 2, None, None) == P.ERR_INVALID_ARG
+    assert lib.dsa_msa_block_scores(fake, 10, ctypes.byref(rows(0, 256, 2)), fake, fake, 2, None, None) == P.OK
+    # MSA selection: counts, score stride, the shared-memory bound on blocks per row
+    assert lib.dsa_msa_select(fake, 2, fake, -1, 256, fake, None, None) == P.ERR_INVALID_ARG
+    assert lib.dsa_msa_select(fake, 1, fake, 1, 256, fake, None, None) == P.ERR_INVALID_ARG
+    assert lib.dsa_msa_select(fake, 1 << 20, fake, 1, (1 << 21) + 128, fake, None, None) == P.ERR_UNSUPPORTED
+    assert lib.dsa_msa_select(None, 0, None, 0, 0, None, None, None) == P.OK
+    # MSA attention: heads per group a multiple of 16 in [16, 64]; positive finite scales; workspace
+    r = rows(1, 256, 2)
+    for hpg in (8, 24, 80):
+        assert lib.dsa_msa_attention(fake, 10, 1.0, 1.0, ctypes.byref(r), fake, 1.0, hpg, fake, 0.09, fake, fake,
+                                     fake, 1 << 30, None, None) == P.ERR_UNSUPPORTED
+    assert lib.dsa_msa_attention(fake, 10, 0.0, 1.0, ctypes.byref(r), fake, 1.0, 16, fake, 0.09, fake, fake,
+                                 fake, 1 << 30, None, None) == P.ERR_INVALID_ARG
+    assert lib.dsa_msa_attention(fake, 10, 1.0, 1.0, ctypes.byref(r), fake, 1.0, 16, fake, 0.09, fake, fake,
+                                 None, 0, None, None) == P.ERR_WORKSPACE
+    # cache insert: page size, formats, matching pools, a positive latent scale
+    ic, lc = P._Cache(fake, P.KEY_FP8, 64, 10, 1.0), P._Cache(fake, P.LATENT_FP8, 64, 10, 0.01)
+    assert lib.dsa_cache_insert(ctypes.byref(P._Cache(fake, P.KEY_FP8, 32, 10, 1.0)), ctypes.byref(lc), fake, 1,
+                                fake, fake, None, None) == P.ERR_UNSUPPORTED
+    assert lib.dsa_cache_insert(ctypes.byref(P._Cache(fake, P.LATENT_FP8, 64, 10, 1.0)), ctypes.byref(lc), fake, 1,
+                                fake, fake, None, None) == P.ERR_UNSUPPORTED
+    assert lib.dsa_cache_insert(ctypes.byref(ic), ctypes.byref(P._Cache(fake, P.LATENT_FP8, 64, 11, 0.01)), fake,
+                                1, fake, fake, None, None) == P.ERR_INVALID_ARG
+    assert lib.dsa_cache_insert(ctypes.byref(ic), ctypes.byref(P._Cache(fake, P.LATENT_FP8, 64, 10, 0.0)), fake,
+                                1, fake, fake, None, None) == P.ERR_INVALID_ARG
+    assert lib.dsa_cache_insert(ctypes.byref(ic), ctypes.byref(lc), fake, 0, fake, fake, None, None) == P.OK
+    # warm top-k: needs the latent pool, and only FP8 / NVFP4 latent formats
+    r = rows(1, 4096, 64)
+    assert lib.dsa_topk_slots_warm(fake, 4096, ctypes.byref(r), None, 16, fake, fake, None, None) == P.ERR_INVALID_ARG
+    assert lib.dsa_topk_slots_warm(fake, 4096, ctypes.byref(r), ctypes.byref(P._Cache(fake, 9, 64, 10, 0.01)), 16,
+                                   fake, fake, None, None) == P.ERR_UNSUPPORTED
