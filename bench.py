@@ -6,12 +6,14 @@ Prints ONE JSON line (rank 0).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
 
-value      query-tokens/s of the whole job (inputs resident in HBM)
+value      query-tokens/s of the whole job (inputs resident in HBM), timed over CUDA
+           graphs of consecutive steps that carry no event nodes
 e2e        the same through the C ABI with host buffers: pinned host -> device
            copies of the step's queries and metadata and device -> host copies of
-           the outputs inside the timed region
+           the outputs inside the timed region, one graph replay per step between them
 roofline   the indexer (the dominant kernel): algorithmic bytes per launch /
-           its CUDA-event time, against the measured HBM copy bandwidth
+           its CUDA-event time (event nodes around each launch, in a replay of the
+           same steps after the timed loop), against the measured HBM copy bandwidth
 cpu_baseline  the CPU oracle on a bounded sample of the same workload
 """
 from __future__ import annotations
