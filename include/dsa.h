@@ -289,7 +289,9 @@ int dsa_sparse_mla_decode_prepared(const dsa_cache *latent_cache, const uint16_t
  * that loads the library until the process exits).  Larger calls return
  * DSA_ERR_WORKSPACE without launching.  The first call on a device looks up
  * the array's address with that device current; make it before capturing
- * any stream.  All calls share the array: calls whose kernels may overlap on
+ * any stream.  That address belongs to the device's primary context: after a
+ * cudaDeviceReset of the device this call must not be used again in the
+ * process.  Shape errors return the statuses dsa_sparse_mla_decode returns.  All calls share the array: calls whose kernels may overlap on
  * the GPU (unordered streams) race on it; calls ordered on one stream do not.
  * No part of the array needs to start zeroed.
  */

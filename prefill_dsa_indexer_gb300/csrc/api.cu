@@ -50,6 +50,22 @@ bool encode_rows128(CUtensorMap *map, const void *base, uint64_t rows, uint32_t 
     return r == CUDA_SUCCESS;
 }
 
+// 2D tensor of 4-bit values [rows, 128] with 64-byte rows (MXFP4 index keys), a [box_rows, 128]
+// box landing in shared memory as 128-byte rows (each 16 values in the low 8 bytes of a 16-byte
+// unit, the layout 4-bit tensor-core operands take), 128-byte swizzle.  Base: 32-byte aligned.
+bool encode_fp4_rows64(CUtensorMap *map, const void *base, uint64_t rows, uint32_t box_rows) {
+    auto enc = get_encoder();
+    if (enc == nullptr) return false;
+    const cuuint64_t dims[2] = {128, rows};
+    const cuuint64_t strides[1] = {64};
+    const cuuint32_t box[2] = {128, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 2, const_cast<void *>(base), dims, strides, box,
+                     estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 int check_rows(const dsa_rows *rows) {
@@ -120,15 +136,17 @@ static int indexer_common(const dsa_cache *index_cache, const dsa_rows *rows, co
     if (rows->num_rows == 0) return DSA_OK;
     if (!index_cache->base || index_cache->num_pages <= 0 || !q_idx || !head_w || !logits)
         return DSA_ERR_INVALID_ARG;
-    if (!aligned(index_cache->base, 16) || !aligned(q_idx, 16)) return DSA_ERR_INVALID_ARG;
+    if (!aligned(index_cache->base, mx ? 32 : 16) || !aligned(q_idx, 16)) return DSA_ERR_INVALID_ARG;
     if (logits_stride < rows->max_ctx) return DSA_ERR_INVALID_ARG;
-    const uint64_t pool_rows = static_cast<uint64_t>(index_cache->num_pages) * 66u;
+    const uint64_t pool_rows = static_cast<uint64_t>(index_cache->num_pages) * (mx ? 68u : 66u);
     if (pool_rows >= (1ull << 31)) return DSA_ERR_UNSUPPORTED;
     const int sms = device_sm_count();
     if (sms <= 0) return DSA_ERR_CUDA;
 
     CUtensorMap key_map, q_map;
-    if (!mx && !encode_rows128(&key_map, index_cache->base, pool_rows, DSA_PAGE_SIZE)) return DSA_ERR_CUDA;
+    if (mx ? !encode_fp4_rows64(&key_map, index_cache->base, pool_rows, DSA_PAGE_SIZE)
+           : !encode_rows128(&key_map, index_cache->base, pool_rows, DSA_PAGE_SIZE))
+        return DSA_ERR_CUDA;
     if (!encode_rows128(&q_map, q_idx, static_cast<uint64_t>(rows->num_rows) * DSA_INDEX_HEADS,
                         static_cast<uint32_t>(G * DSA_INDEX_HEADS)))
         return DSA_ERR_CUDA;
@@ -150,8 +168,7 @@ static int indexer_common(const dsa_cache *index_cache, const dsa_rows *rows, co
     for (int g0 = 0; g0 < num_groups; g0 += kIndexerMaxGroups) {
         a.group0 = g0;
         a.num_groups = num_groups - g0 < kIndexerMaxGroups ? num_groups - g0 : kIndexerMaxGroups;
-        cudaError_t e = mx ? launch_indexer_mxfp4(q_map, a, G, sms, static_cast<cudaStream_t>(stream))
-                           : launch_indexer_fp8(key_map, q_map, a, G, sms, static_cast<cudaStream_t>(stream));
+        cudaError_t e = launch_indexer(key_map, q_map, a, mx, G, sms, static_cast<cudaStream_t>(stream));
         if (e != cudaSuccess) return DSA_ERR_CUDA;
     }
     return DSA_OK;

@@ -44,13 +44,10 @@ __device__ __forceinline__ uint32_t order_key(float f) {
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-// Launch the FP8-key indexer for groups of `rows_per_group` rows.
-cudaError_t launch_indexer_fp8(const CUtensorMap &key_map, const CUtensorMap &q_map, const IndexerArgs &a,
-                               int rows_per_group, int num_sms, cudaStream_t s);
-
-// Launch the MXFP4-key indexer (in-kernel dequantisation to e4m3).
-cudaError_t launch_indexer_mxfp4(const CUtensorMap &q_map, const IndexerArgs &a, int rows_per_group, int num_sms,
-                                 cudaStream_t s);
+// Launch the indexer for groups of `rows_per_group` rows.  key_map: FP8 keys, the pool as a byte
+// tensor [pages * 66, 128]; MXFP4 keys, the pool as 4-bit values [pages * 68, 128] (64-byte rows).
+cudaError_t launch_indexer(const CUtensorMap &key_map, const CUtensorMap &q_map, const IndexerArgs &a,
+                           bool mxfp4_keys, int rows_per_group, int num_sms, cudaStream_t s);
 
 struct TopkArgs {
     const float *logits;

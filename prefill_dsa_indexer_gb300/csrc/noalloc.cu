@@ -14,9 +14,11 @@
 // library holds kNoAllocScratchBytes of it until the process exits.  The
 // first call on a device looks up the array's device address (with that
 // device current) and caches it; make that first call before capturing any
-// stream.  All calls share the one array, so calls whose kernels overlap on
-// the GPU (different streams, no ordering between them) race on it; calls
-// ordered on one stream are fine.  Nothing in the scratch needs to start at
+// stream.  The cached address belongs to the device's primary context: a
+// cudaDeviceReset voids it, so this entry point must not be called again in a
+// process that has reset the device.  All calls share the one array, so calls
+// whose kernels overlap on the GPU (different streams, no ordering between
+// them) race on it; calls ordered on one stream are fine.  Nothing in the scratch needs to start at
 // zero: every call overwrites every partial it later reads.
 #include <cuda_runtime.h>
 
@@ -59,7 +61,10 @@ int scratch_address(void **out) {
 extern "C" int dsa_sparse_mla_decode_noalloc(const dsa_cache *latent_cache, const uint16_t *q, int32_t num_heads,
                                              const int32_t *slots, int32_t num_rows, int32_t k, float sm_scale,
                                              float *out, float *lse, int32_t *dev_status, void *stream) {
-    if (num_rows < 0 || num_heads <= 0 || k < 1) return DSA_ERR_INVALID_ARG;
+    // the shape checks of dsa_sparse_mla_decode first, so a bad shape gets the same status as there
+    if (latent_cache == nullptr || num_rows < 0 || k < 1) return DSA_ERR_INVALID_ARG;
+    if (num_heads < 16 || num_heads > 96 || num_heads % 16 != 0) return DSA_ERR_UNSUPPORTED;
+    if (dsa::mla_splits(static_cast<size_t>(k)) > static_cast<size_t>(dsa::kMlaMaxSplits)) return DSA_ERR_UNSUPPORTED;
     if (num_rows > DSA_NOALLOC_MAX_ROWS) return DSA_ERR_WORKSPACE;
     const size_t need = dsa::mla_workspace_bytes(num_rows, num_heads, k);
     if (need > dsa::kNoAllocScratchBytes) return DSA_ERR_WORKSPACE;

@@ -200,6 +200,43 @@ __host__ __device__ constexpr uint32_t make_idesc(int m, int n, uint32_t afmt, u
            (static_cast<uint32_t>(m >> 4) << 24);
 }
 
+// Shared-memory matrix descriptor without swizzle, for a tcgen05.cp source of 16-byte rows:
+// `sbo` is the distance between 8-row groups (128 B for dense rows).
+__device__ __forceinline__ uint64_t sdesc_plain(uint32_t saddr, uint32_t sbo) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
+    d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+    d |= static_cast<uint64_t>(1) << 46;  // descriptor version for tcgen05; layout bits 0 = no swizzle
+    return d;
+}
+
+// Instruction descriptor of a block-scaled MMA (kind::mxf8f6f4): fp32 accumulator, dense, K-major
+// A/B of the given format codes (0 = e4m3, 5 = e2m1), ue8m0 scale factors, and which byte of each
+// 32-bit scale-factor cell (one per 32 K values) this MMA's A and B rows use.
+__host__ __device__ constexpr uint32_t make_idesc_bs(int m, int n, uint32_t afmt, uint32_t bfmt, uint32_t a_sf_id,
+                                                     uint32_t b_sf_id) {
+    return (b_sf_id << 4) | (afmt << 7) | (bfmt << 10) | (static_cast<uint32_t>(n >> 3) << 17) | (1u << 23) |
+           (static_cast<uint32_t>(m >> 4) << 24) | (a_sf_id << 29);
+}
+
+// Copy 32 rows of 16 bytes from shared memory into TMEM columns [col, col + 4) of all 128 lanes
+// (row i to lane i of every 32-lane quadrant).  Ordered before later tcgen05.mma of this thread.
+__device__ __forceinline__ void tmem_cp_32x128b_x4(uint32_t taddr, uint64_t sdesc) {
+    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
+// D[tmem] (+)= (A * 2^(sfa - 127)) x (B * 2^(sfb - 127))^T per 32-value block of K, K = 32 per call:
+// A and B are e4m3 or e2m1 (4-bit values stored as 16 per 16-byte unit with an 8-byte gap), the
+// ue8m0 scale factors sit in TMEM at sfa / sfb.
+__device__ __forceinline__ void mma_mx(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                       uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}\n"
+        ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate));
+}
+
 // D[tmem] (+)= A[smem] x B[smem]^T, FP8 (e4m3) operands, K = 32 per call.
 __device__ __forceinline__ void mma_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                        uint32_t accumulate) {

@@ -93,6 +93,15 @@ def test_host_validation_rejects_before_launch(lib):
     bad = P._Cache(fake, 9, 64, 10, 0.01)
     assert lib.dsa_sparse_mla_prefill(ctypes.byref(bad), fake, 96, fake, 1, 2048, 0.07, fake, fake, None, None, 0,
                                       None) == P.ERR_UNSUPPORTED
+    # no-alloc decode: shape errors get dsa_sparse_mla_decode's statuses before any scratch check
+    na = lib.dsa_sparse_mla_decode_noalloc
+    assert na(ctypes.byref(lc), fake, 96, fake, 8, 2049, 0.07, fake, fake, None, None) == P.ERR_UNSUPPORTED
+    for H in (8, 100, 112, 128):
+        assert na(ctypes.byref(lc), fake, H, fake, 1, 2048, 0.07, fake, fake, None, None) == P.ERR_UNSUPPORTED
+    assert na(None, fake, 96, fake, 1, 2048, 0.07, fake, fake, None, None) == P.ERR_INVALID_ARG
+    assert na(ctypes.byref(lc), fake, 96, fake, 1, 0, 0.07, fake, fake, None, None) == P.ERR_INVALID_ARG
+    assert na(ctypes.byref(lc), fake, 96, fake, P.NOALLOC_MAX_ROWS + 1, 2048, 0.07, fake, fake, None,
+              None) == P.ERR_WORKSPACE
     # page -> slot: k < 1
     r = P._Rows(fake, 1, 1, fake, fake, 1, 64, 1)
     assert lib.dsa_page_to_slot(ctypes.byref(r), 10, fake, 0, fake, None, None) == P.ERR_INVALID_ARG

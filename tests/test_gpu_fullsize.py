@@ -26,6 +26,7 @@ CASES = {
     "verify_b4_256k": [2, 13],
     "prefill_8k_on_56k": [0, 4097, 8191],
     "verify_b1_1m": [3],
+    "decode_b8_128k_fp4": [2, 7],
 }
 
 
@@ -63,8 +64,11 @@ def test_fullsize_sampled(name):
         assert np.all(d <= bound[r]), (r, float((d / bound[r]).max()))
         ok, nd = U.set_diff_within_band(idx[r], ora_idx[i], ref_lg[i], wl.k)
         assert ok, (r, nd)
+    # every row: the slots are the oracle's translation of the GPU's selection
+    all_slots = layer.slots.cpu().numpy()
+    assert np.array_equal(all_slots, oracle.page_to_slot(inp.np("block_table"), inp.np("row_req"), idx))
     # attention on the GPU's own selection for the sampled rows
-    gslots = layer.slots.cpu().numpy()[rows]
+    gslots = all_slots[rows]
     ref_o, ref_l = oracle.sparse_mla(inp.np("lat_pool"), U.ORACLE_FMT[wl.lat_fmt], inp.tensor_scale,
                                      inp.np("q_mla")[rows], gslots, U.SM_SCALE)
     tol = 3e-2 if wl.lat_fmt == I.LATENT_NVFP4 else 1e-2

@@ -8,6 +8,7 @@ import torch
 import oracle
 import prefill_dsa_indexer_gb300 as P
 from prefill_dsa_indexer_gb300 import inputs as I
+from tests import gpu_util as U
 
 pytestmark = pytest.mark.gpu
 
@@ -68,4 +69,6 @@ def test_insert_then_layer_reads_it():
     torch.cuda.synchronize()
     ref = oracle.indexer_logits(inp.np("idx_pool"), 1, inp.np("block_table"), inp.np("row_req"), inp.np("row_ctx"),
                                 inp.np("q_idx"), inp.np("head_w"))
-    np.testing.assert_allclose(lg.cpu().numpy()[0, :700], ref[0, :700], rtol=1e-3, atol=1e-3)
+    bound = U.logit_bound(inp, [0])[0]
+    d = np.abs(lg.cpu().numpy()[0, :700].astype(np.float64) - ref[0, :700])
+    assert np.all(d <= bound[:700]), float((d / bound[:700]).max())

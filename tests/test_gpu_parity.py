@@ -47,6 +47,12 @@ INDEXER_CASES = {
     "mxfp4_ragged": _wl("mx", [1, 64, 65, 129, 2049, 5000], key=I.KEY_MXFP4),
     "mxfp4_verify_g4": _wl("mxv", [3000, 4100], rows=4, group=4, key=I.KEY_MXFP4),
     "mxfp4_prefill_g8": _wl("mxp", [2500], rows=32, group=8, key=I.KEY_MXFP4),
+    # steady state of the persistent MXFP4 grid: every CTA runs several tiles, so the stage,
+    # accumulator and scale-factor rings all wrap (8 x 80K keys = 2,560 tiles of 256 for G = 1;
+    # 4 x 4 rows x 40K = 1,252 tiles of 128 for G = 4; 3 x 2 rows x 60K for G = 2)
+    "mxfp4_steady_g1": _wl("mxs1", [80000 + 997 * i for i in range(8)], key=I.KEY_MXFP4, seed=61),
+    "mxfp4_steady_g4": _wl("mxs4", [40000, 39001, 40013, 38500], rows=4, group=4, key=I.KEY_MXFP4, seed=62),
+    "mxfp4_steady_g2": _wl("mxs2", [60000, 59003, 61111], rows=2, group=2, key=I.KEY_MXFP4, seed=63),
 }
 
 
@@ -68,6 +74,48 @@ def test_indexer_logits(case):
     torch.cuda.synchronize()
     P.check_status(st)
     _check_logits(inp, lg.cpu().numpy())
+
+
+def _mx_scale_bytes(inp, rows_tokens):
+    """(byte offsets of each listed token's four e8m0 scales) in the MXFP4 index pool."""
+    bt, rq = inp.np("block_table"), inp.np("row_req")
+    offs = []
+    for r, t in rows_tokens:
+        slot = int(bt[rq[r], t // 64]) * 64 + t % 64
+        offs.append((slot // 64) * I.index_page_bytes(I.KEY_MXFP4) + 64 * 64 + (slot % 64) * 4)
+    return offs
+
+
+def test_mxfp4_keys_exact_over_wide_block_exponent_spread():
+    # keys whose four 32-value blocks sit up to 130 binades apart: each block's partial product is
+    # scaled on its own, so the logits stay within the accumulation bound of the exact values
+    inp = U.gpu_inputs(_wl("mxw", [5000, 3000], key=I.KEY_MXFP4, seed=64))
+    rng = np.random.default_rng(64)
+    pool = inp.idx_pool.cpu().numpy().reshape(-1)
+    toks = [(0, int(t)) for t in rng.choice(5000, 1500, replace=False)] + \
+           [(1, int(t)) for t in rng.choice(3000, 900, replace=False)]
+    spreads = np.array([[131, 109, 97, 128], [127, 27, 147, 60], [20, 150, 85, 126], [140, 140, 10, 139]])
+    for i, off in enumerate(_mx_scale_bytes(inp, toks)):
+        pool[off:off + 4] = spreads[i % 4]
+    inp.idx_pool.copy_(torch.from_numpy(pool.reshape(inp.idx_pool.shape)))
+    st = P.new_status()
+    lg = U.run_indexer(inp, st)
+    torch.cuda.synchronize()
+    P.check_status(st)
+    _check_logits(inp, lg.cpu().numpy())
+
+
+def test_mxfp4_nan_scale_of_a_visible_key_is_range_error():
+    # the e8m0 code 0xff is NaN in the MX format: a visible key that carries it is reported
+    inp = U.gpu_inputs(_wl("mxn", [3000], key=I.KEY_MXFP4, seed=65))
+    pool = inp.idx_pool.cpu().numpy().reshape(-1)
+    off = _mx_scale_bytes(inp, [(0, 1234)])[0]
+    pool[off + 2] = 0xFF
+    inp.idx_pool.copy_(torch.from_numpy(pool.reshape(inp.idx_pool.shape)))
+    st = P.new_status()
+    U.run_indexer(inp, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == P.ERR_RANGE
 
 
 def test_indexer_leaves_masked_entries_untouched():
@@ -244,8 +292,10 @@ def test_layer_end_to_end(name):
     for r in range(wl.num_rows):
         ok, nd = U.set_diff_within_band(gpu_idx[r], ora_idx[r], ref_lg[r], wl.k)
         assert ok, (r, nd)
-    # attention parity on the GPU's own selection
+    # the slots the attention read are the oracle's translation of the GPU's selection
     gslots = layer.slots.cpu().numpy()
+    assert np.array_equal(gslots, oracle.page_to_slot(inp.np("block_table"), inp.np("row_req"), gpu_idx))
+    # attention parity on the GPU's own selection
     ref_o, _ = oracle.sparse_mla(inp.np("lat_pool"), U.ORACLE_FMT[wl.lat_fmt], inp.tensor_scale, inp.np("q_mla"),
                                  gslots, U.SM_SCALE)
     max_abs, rel = U.mla_errors(out.cpu().numpy(), ref_o)
