@@ -285,7 +285,7 @@ int dsa_sparse_mla_decode_prepared(const dsa_cache *latent_cache, const uint16_t
  * Same arguments, semantics and results as dsa_sparse_mla_decode, minus the
  * workspace.  The split-K partial outputs live in a fixed array in the
  * library's own device memory, sized for DSA_NOALLOC_MAX_ROWS rows of
- * k <= 2048 tokens and num_heads <= 96 (13,565,952 bytes, held by every GPU
+ * k <= 2048 tokens and num_heads <= 96 (13,569,024 bytes, held by every GPU
  * that loads the library until the process exits).  Larger calls return
  * DSA_ERR_WORKSPACE without launching.  The first call on a device looks up
  * the array's address with that device current; make it before capturing

@@ -107,7 +107,9 @@ struct MlaArgs {
     int32_t *status;
     uint16_t *part_o;   // decode: [R, splits, H, 512] fp16 partial outputs (normalised by their own sum)
     float *part_ml;     // decode: [R, splits, H, 2] running max (log2 units) and sum
-    uint8_t *qprep;     // decode: [R, 9 * H * 128] fp16 query images, laid out as the kernel's operand
+    uint8_t *qprep;     // decode: per row (mla_qprep_row_bytes(H) apart) the query image laid out as the
+                        // kernel's operand: fp16 [9 x H x 128 B] (NVFP4 latents), or e4m3 hi x 4, lo x 4,
+                        // RoPE hi|lo blocks [9 x H x 128 B] then H fp32 factors 2^-e_h (FP8 latents)
     int32_t splits;     // 1 = write the final output directly
     bool q_prepared;    // decode: the query images are already in qprep (no prep launch)
 };
@@ -169,6 +171,14 @@ bool encode_rows128_map(CUtensorMap *map, const void *base, uint64_t rows, uint3
 // Decode query preparation alone (bf16 query -> the fp16 operand images in a.qprep).
 cudaError_t launch_mla_qprep(const MlaArgs &a, cudaStream_t s);
 
+// Merge of a decode's split partials (a.part_o, a.part_ml) into a.out / a.lse.
+cudaError_t launch_mla_combine(const MlaArgs &a, cudaStream_t s);
+
+// FP8-latent decode on FP8 tensor cores (mla_fp8.cu): query preparation alone, and the whole call
+// (preparation unless a.q_prepared, one CTA per 128-token part, merge).  Needs a.splits >= 2.
+cudaError_t launch_mla_qprep_fp8(const MlaArgs &a, cudaStream_t s);
+cudaError_t launch_sparse_mla_fp8_decode(const MlaArgs &a, cudaStream_t s);
+
 // Decode splits every row's selected tokens into parts of this many tokens (fixed, so a row's
 // result does not depend on the batch), merged by log-sum-exp.
 constexpr int kMlaTokensPerSplit = 128;
@@ -177,7 +187,8 @@ constexpr int kMlaMaxSplits = 16;
 constexpr size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 constexpr size_t mla_part_o_bytes(size_t R, size_t H, size_t S) { return align256(R * S * H * 512 * 2); }
 constexpr size_t mla_part_ml_bytes(size_t R, size_t H, size_t S) { return align256(R * S * H * 2 * 4); }
-constexpr size_t mla_qprep_bytes(size_t R, size_t H) { return align256(R * 9 * H * 128); }
+__host__ __device__ constexpr size_t mla_qprep_row_bytes(size_t H) { return 9 * H * 128 + 4 * H; }
+constexpr size_t mla_qprep_bytes(size_t R, size_t H) { return align256(R * mla_qprep_row_bytes(H)); }
 constexpr size_t mla_splits(size_t k) { return (k + kMlaTokensPerSplit - 1) / kMlaTokensPerSplit; }
 constexpr size_t mla_workspace_bytes_for(size_t R, size_t H, size_t k) {
     return mla_splits(k) <= 1 ? 0

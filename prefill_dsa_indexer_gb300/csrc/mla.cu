@@ -369,7 +369,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const MlaArgs a
     if (a.qprep != nullptr) {
         if (tid == 0 && n_tiles > 0) {
             const uint32_t blk = static_cast<uint32_t>(H) * 128;
-            const uint8_t *src = a.qprep + static_cast<int64_t>(row) * kChunks * blk;
+            const uint8_t *src = a.qprep + static_cast<int64_t>(row) * mla_qprep_row_bytes(H);
             mbar_arrive_expect_tx(q_full, kChunks * blk);
             for (int c = 0; c < kChunks; ++c) bulk_load(qs + c * blk, src + c * blk, blk, q_full);
         }
@@ -743,7 +743,7 @@ __global__ void __launch_bounds__(256) mla_qprep_kernel(const MlaArgs a) {
         const int4 v = *reinterpret_cast<const int4 *>(a.q + e * 8);
         const float sc = (u >= DSA_VALUE_DIM / 8) ? q_rope_scale : 1.0f;
         const int c = u >> 3, uu = u & 7;
-        uint8_t *dst = a.qprep + row * (kChunks * H * 128) + c * H * 128 + sw128(h, uu);
+        uint8_t *dst = a.qprep + row * static_cast<int64_t>(mla_qprep_row_bytes(H)) + c * H * 128 + sw128(h, uu);
         *reinterpret_cast<int4 *>(dst) = q_unit_to_f16(v, sc, range_err);
     }
     if (range_err) report(a.status, DSA_ERR_RANGE);
@@ -778,6 +778,12 @@ cudaError_t launch_mla_qprep(const MlaArgs &a, cudaStream_t s) {
     const int64_t units = static_cast<int64_t>(a.num_rows) * a.num_heads * (DSA_LATENT_DIM / 8);
     const int blocks = static_cast<int>(units / 256 < 4096 ? (units + 255) / 256 : 4096);
     mla_qprep_kernel<<<blocks, 256, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_mla_combine(const MlaArgs &a, cudaStream_t s) {
+    if (a.num_rows == 0 || a.splits < 2) return cudaSuccess;
+    mla_combine_kernel<<<a.num_rows * a.num_heads, DSA_VALUE_DIM / 4, 0, s>>>(a);
     return cudaGetLastError();
 }
 

@@ -33,7 +33,7 @@ namespace {
 // Sized for DSA_NOALLOC_MAX_ROWS rows of k <= 2048 selected tokens and <= 96 heads (the
 // split partial outputs, their maxima and sums, and the rows' prepared queries).
 constexpr size_t kNoAllocScratchBytes = mla_workspace_bytes_for(DSA_NOALLOC_MAX_ROWS, 96, 2048);
-static_assert(kNoAllocScratchBytes == 13565952, "the size the header documents");
+static_assert(kNoAllocScratchBytes == 13569024, "the size the header documents");
 
 static __device__ __align__(256) unsigned char g_mla_scratch[kNoAllocScratchBytes];
 
