@@ -533,8 +533,9 @@ def main():
         side = torch.cuda.Stream()
 
         def capture(n, events):
-            # per step: the decode query prep forks onto a side branch (it needs only the query)
-            # and joins before the attention; scorer -> top-k+slots -> attention on the main branch.
+            # per step: scorer -> top-k+slots -> attention on the main branch; the decode query
+            # prep (it needs only the query) forks onto a side branch after the scorer, runs beside
+            # the top-k (which occupies few SMs) and joins before the attention.
             # events: event nodes around every scorer launch (the indexer timing graph only)
             g = torch.cuda.CUDAGraph()
             evp = [(ext_event(), ext_event()) for _ in range(n)] if events else []
@@ -543,18 +544,19 @@ def main():
                     for k in range(n):
                         L = layers[k % len(layers)]
                         fork = not L.prefill
-                        if fork:
-                            side.wait_stream(cap)
-                            with torch.cuda.stream(side):
-                                L.prepare(inp.q_mla)
                         if events:
                             evp[k][0].record(cap)
                         indexer(L)
                         if events:
                             evp[k][1].record(cap)
                         if fork:
+                            side.wait_stream(cap)
+                            with torch.cuda.stream(side):
+                                L.prepare(inp.q_mla)
+                        L.select_tokens(inp.row_req, inp.row_ctx)
+                        if fork:
                             cap.wait_stream(side)
-                        L.select(inp.row_req, inp.row_ctx, inp.q_mla, prepared=fork)
+                        L.attend(inp.q_mla, prepared=fork)
             return g, evp
 
         if graph_mode == "multi-step":
@@ -702,17 +704,18 @@ def main():
 
     side_e = torch.cuda.Stream()
 
-    def graph_body(i, L, d):  # the query prep forks onto a parallel branch
+    def graph_body(i, L, d):  # the query prep forks onto a parallel branch beside the top-k
         cur = torch.cuda.current_stream()
         fork = not L.prefill
+        L.score(d["row_req"], d["row_ctx"], d["q_idx"], d["head_w"])
         if fork:
             side_e.wait_stream(cur)
             with torch.cuda.stream(side_e):
                 L.prepare(d["q_mla"])
-        L.score(d["row_req"], d["row_ctx"], d["q_idx"], d["head_w"])
+        L.select_tokens(d["row_req"], d["row_ctx"])
         if fork:
             cur.wait_stream(side_e)
-        L.select(d["row_req"], d["row_ctx"], d["q_mla"], prepared=fork)
+        L.attend(d["q_mla"], prepared=fork)
 
     # With graphs, each step between its copies is one replay of a graph of that step's calls,
     # one graph per input buffer and cache copy.  (Capturing the copies too, as memcpy nodes in
@@ -801,7 +804,7 @@ def main():
                 else "eager launches between the copies"},
         "gpu_launches": launches_per_step * args.steps,
         "launch": {"multi-step": f"CUDA graphs of {16 * copies} consecutive steps (decode query prep on a "
-                                 f"parallel branch); indexer timed after the timed loop by event nodes "
+                                 f"parallel branch beside the top-k); indexer timed after the timed loop by event nodes "
                                  f"around each scorer launch in a replay of the same steps "
                                  f"({len(samples)} launches sampled)",
                    "two-graphs": "CUDA-graph replay (indexer graph + rest-of-step graph), stream events between",

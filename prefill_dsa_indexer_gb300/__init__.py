@@ -458,6 +458,11 @@ class Layer:
 
     def select(self, row_req, row_ctx, q_mla, stream=None, prepared=False):
         """Top-k, page -> slot and sparse MLA over the scored logits (`prepared`: prepare() ran already)."""
+        self.select_tokens(row_req, row_ctx, stream=stream)
+        return self.attend(q_mla, stream=stream, prepared=prepared)
+
+    def select_tokens(self, row_req, row_ctx, stream=None):
+        """Top-k and page -> slot over the scored logits (into self.idx, self.slots)."""
         if self.single_pass:
             topk_hist(self.logits, row_ctx, self.max_ctx, self.hist, self.k, out=self.idx, status=self.status,
                       stream=stream)
@@ -469,6 +474,9 @@ class Layer:
         else:  # top-k with the page -> slot translation in its output pass
             topk_slots(self.logits, self.block_table, row_req, row_ctx, self.max_ctx, self.lat_pool.shape[0], self.k,
                        out=self.idx, slots=self.slots, status=self.status, stream=stream)
+
+    def attend(self, q_mla, stream=None, prepared=False):
+        """Sparse MLA over self.slots (`prepared`: prepare() ran already for these queries)."""
         if self.prefill:
             sparse_mla_prefill(self.lat_pool, self.lat_fmt, self.tensor_scale, q_mla, self.slots, self.sm_scale,
                                out=self.out, lse=self.lse, status=self.status, stream=stream)
@@ -483,7 +491,8 @@ class Layer:
         return self.out, self.lse
 
     def prepare(self, q_mla, stream=None):
-        """Decode query conversion (independent of the scorer and the top-k; may run beside them)."""
+        """Decode query conversion (independent of the scorer and the top-k; may run beside the top-k,
+        which leaves most SMs free, and must be ordered before attend(prepared=True))."""
         if not self.prefill:
             sparse_mla_decode_prepare(self.lat_pool, self.lat_fmt, self.tensor_scale, q_mla, self.k, self.workspace,
                                       status=self.status, stream=stream)

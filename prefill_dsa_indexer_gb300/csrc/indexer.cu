@@ -170,7 +170,6 @@ __global__ void __launch_bounds__(IdxCfg<G, kMx>::kThreads, IdxCfg<G, kMx>::kCta
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int ng = a.num_groups;
 
-    plan_groups<G, C::kTileKeys>(a, prefix, greq, gmax);
     if constexpr (kMx) {
         // the queries carry no scale: their scale factors are all 2^0 (ue8m0 code 127)
         for (int i = tid; i < C::kUnitSfBytes / 4; i += blockDim.x) unit_sf[i] = 0x7f7f7f7fu;
@@ -199,6 +198,10 @@ __global__ void __launch_bounds__(IdxCfg<G, kMx>::kThreads, IdxCfg<G, kMx>::kCta
         tmem_alloc(tmem_slot, C::kTmemCols);
         tmem_relinquish();
     }
+    // on-chip set-up above; global memory from here on, once the previous kernel has finished
+    pdl_launch_dependents();
+    pdl_wait();
+    plan_groups<G, C::kTileKeys>(a, prefix, greq, gmax);
     __syncthreads();
     if (warp == 0) plan_scan(prefix, ng, lane);
     __syncthreads();
@@ -515,8 +518,8 @@ cudaError_t launch_gh(const CUtensorMap &key_map, const CUtensorMap &q_map, cons
     for (int done = 0; done < a.num_groups; done += C::kMaxGroups) {
         b.group0 = a.group0 + done;
         b.num_groups = a.num_groups - done < C::kMaxGroups ? a.num_groups - done : C::kMaxGroups;
-        indexer_kernel<G, kHist, kMx><<<num_sms * C::kCtasPerSm, C::kThreads, C::kSmemBytes, s>>>(key_map, q_map, b);
-        cudaError_t e = cudaGetLastError();
+        cudaError_t e = launch_pdl(indexer_kernel<G, kHist, kMx>, dim3(num_sms * C::kCtasPerSm), dim3(C::kThreads),
+                                   C::kSmemBytes, s, key_map, q_map, b);
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;

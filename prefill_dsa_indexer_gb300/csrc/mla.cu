@@ -678,6 +678,8 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const MlaArgs a
 // w_s = l_s 2^(m_s - M), M = max_s m_s (log2 units), O_s the split's normalised
 // fp16 output.  One CTA per (row, head), four output dims per thread.
 __global__ void __launch_bounds__(128) mla_combine_kernel(const MlaArgs a) {
+    pdl_launch_dependents();
+    pdl_wait();
     const int H = a.num_heads, S = a.splits;
     const int row = blockIdx.x / H, h = blockIdx.x % H;
     const float *ml = a.part_ml + static_cast<int64_t>(row) * S * H * 2;
@@ -767,8 +769,7 @@ cudaError_t launch_fmt(const MlaArgs &a, cudaStream_t s) {
     sparse_mla_kernel<FMT><<<a.num_rows * a.splits, kThreads, kSmemBytes, s>>>(a);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess || a.splits == 1) return e;
-    mla_combine_kernel<<<a.num_rows * a.num_heads, DSA_VALUE_DIM / 4, 0, s>>>(a);
-    return cudaGetLastError();
+    return launch_mla_combine(a, s);
 }
 
 }  // namespace
@@ -783,8 +784,7 @@ cudaError_t launch_mla_qprep(const MlaArgs &a, cudaStream_t s) {
 
 cudaError_t launch_mla_combine(const MlaArgs &a, cudaStream_t s) {
     if (a.num_rows == 0 || a.splits < 2) return cudaSuccess;
-    mla_combine_kernel<<<a.num_rows * a.num_heads, DSA_VALUE_DIM / 4, 0, s>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(mla_combine_kernel, dim3(a.num_rows * a.num_heads), dim3(DSA_VALUE_DIM / 4), 0, s, a);
 }
 
 size_t mla_workspace_bytes(int32_t num_rows, int32_t num_heads, int32_t k) {

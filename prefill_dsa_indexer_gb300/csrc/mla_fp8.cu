@@ -110,11 +110,21 @@ __device__ __forceinline__ void cp_async_wait() {
 
 // ---------------------------------------------------------------- query preparation
 // One warp per (row, head): the head's 576 bf16 values become hi + lo e4m3 at 2^e_h, written as
-// the kernel's 128-byte-swizzled K-major operand blocks, plus 2^-e_h after the image.
+// the kernel's 128-byte-swizzled K-major operand blocks, plus 2^-e_h after the image.  A warp
+// takes kQprepHeads heads, so the kernel occupies few SMs (it runs beside the top-k).
+constexpr int kQprepHeads = 4;
+__device__ __forceinline__ void qprep_head(const MlaArgs &a, int64_t w, int lane);
 __global__ void __launch_bounds__(256) mla_qprep_fp8_kernel(const MlaArgs a) {
-    const int H = a.num_heads, lane = threadIdx.x & 31;
-    const int64_t w = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
-    if (w >= static_cast<int64_t>(a.num_rows) * H) return;
+    pdl_launch_dependents();
+    pdl_wait();
+    const int64_t w0 = (static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5)) * kQprepHeads;
+#pragma unroll
+    for (int i = 0; i < kQprepHeads; ++i)
+        if (w0 + i < static_cast<int64_t>(a.num_rows) * a.num_heads) qprep_head(a, w0 + i, threadIdx.x & 31);
+}
+
+__device__ __forceinline__ void qprep_head(const MlaArgs &a, int64_t w, int lane) {
+    const int H = a.num_heads;
     const int64_t row = w / H;
     const int h = static_cast<int>(w % H);
     const uint16_t *q = a.q + w * DSA_LATENT_DIM;
@@ -225,6 +235,9 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_fp8_kernel(const MlaAr
         tmem_relinquish();
     }
     if (tid < 4) mask[tid] = 0u;
+    // on-chip set-up above; global memory from here on, once the previous kernel has finished
+    pdl_launch_dependents();
+    pdl_wait();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
@@ -465,9 +478,8 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_fp8_kernel(const MlaAr
 
 cudaError_t launch_mla_qprep_fp8(const MlaArgs &a, cudaStream_t s) {
     if (a.num_rows == 0 || a.qprep == nullptr) return cudaSuccess;
-    const int64_t warps = static_cast<int64_t>(a.num_rows) * a.num_heads;
-    mla_qprep_fp8_kernel<<<static_cast<int>((warps + 7) / 8), 256, 0, s>>>(a);
-    return cudaGetLastError();
+    const int64_t warps = (static_cast<int64_t>(a.num_rows) * a.num_heads + kQprepHeads - 1) / kQprepHeads;
+    return launch_pdl(mla_qprep_fp8_kernel, dim3(static_cast<unsigned>((warps + 7) / 8)), dim3(256), 0, s, a);
 }
 
 cudaError_t launch_sparse_mla_fp8_decode(const MlaArgs &a, cudaStream_t s) {
@@ -487,8 +499,7 @@ cudaError_t launch_sparse_mla_fp8_decode(const MlaArgs &a, cudaStream_t s) {
         cudaError_t e = launch_mla_qprep_fp8(a, s);
         if (e != cudaSuccess) return e;
     }
-    sparse_mla_fp8_kernel<<<a.num_rows * a.splits, kThreads, kSmemBytes, s>>>(a);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_pdl(sparse_mla_fp8_kernel, dim3(a.num_rows * a.splits), dim3(kThreads), kSmemBytes, s, a);
     if (e != cudaSuccess) return e;
     return launch_mla_combine(a, s);
 }

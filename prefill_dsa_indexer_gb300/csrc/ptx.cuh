@@ -308,6 +308,18 @@ __device__ __forceinline__ void reg_fence(uint32_t (&r)[N]) {
 
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
+// ------------------------------------------------------------------ programmatic dependent launch
+
+// Lets the next kernel of the stream (launched with programmatic stream serialization) start its
+// CTAs once every CTA of this grid has issued this or exited.
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Waits until the grids this one depends on have completed and their memory is visible.  Kernels
+// launched with programmatic stream serialization do only on-chip set-up before this.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ------------------------------------------------------------------ misc
 
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {

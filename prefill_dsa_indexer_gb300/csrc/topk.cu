@@ -264,6 +264,9 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const TopkArgs a) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int row = blockIdx.x / CL;
     const int k = a.k;
+    // nothing to set up on chip: global memory from here on, once the previous kernel has finished
+    pdl_launch_dependents();
+    pdl_wait();
     int32_t *out = a.idx_out + static_cast<int64_t>(row) * k;
     int32_t *sout = kSlots ? a.slots_out + static_cast<int64_t>(row) * k : nullptr;
     const int32_t *bt_row = nullptr;  // this row's block-table row, when slots are wanted
@@ -917,13 +920,15 @@ cudaError_t launch_variant(const TopkArgs &a, cudaStream_t s) {
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = sizeof(TopkSmem);
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = cl;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // see launch_pdl
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, kern, a);
 }
 

@@ -43,12 +43,14 @@ def test_graph_replay_equals_eager_calls():
     g = torch.cuda.CUDAGraph()
     with torch.cuda.stream(cap):
         with torch.cuda.graph(g, stream=cap):
+            # the shape bench.py times: scorer, then the query prep on a side branch beside the top-k
+            layer.score(d["row_req"], d["row_ctx"], d["q_idx"], d["head_w"])
             side.wait_stream(cap)
             with torch.cuda.stream(side):
                 layer.prepare(d["q_mla"])
-            layer.score(d["row_req"], d["row_ctx"], d["q_idx"], d["head_w"])
+            layer.select_tokens(d["row_req"], d["row_ctx"])
             cap.wait_stream(side)
-            layer.select(d["row_req"], d["row_ctx"], d["q_mla"], prepared=True)
+            layer.attend(d["q_mla"], prepared=True)
     torch.cuda.current_stream().wait_stream(cap)
 
     def replayed(src):
