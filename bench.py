@@ -7,13 +7,16 @@ Prints ONE JSON line (rank 0).
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
 
 value      query-tokens/s of the whole job (inputs resident in HBM), timed over CUDA
-           graphs of consecutive steps that carry no event nodes
+           graphs of consecutive steps that carry no event nodes: the median of 5 timed
+           regions of exactly K steps each (all five in `repeats_ms_per_step`)
+clocks     nvidia-smi samples over the timed regions and 0.6 s more of the same steps
 e2e        the same through the C ABI with host buffers: pinned host -> device
            copies of the step's queries and metadata and device -> host copies of
            the outputs inside the timed region, one graph replay per step between them
 roofline   the indexer (the dominant kernel): algorithmic bytes per launch /
            its CUDA-event time (event nodes around each launch, in a replay of the
-           same steps after the timed loop), against the measured HBM copy bandwidth
+           same steps after the timed loop), against the measured HBM copy bandwidth;
+           prefill: FLOP per launch against the FP8 GEMM peak measured in the run
 cpu_baseline  the CPU oracle on a bounded sample of the same workload
 """
 from __future__ import annotations
@@ -136,6 +139,81 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+REPEATS = 5  # timed regions of K steps each; the line reports their median
+
+
+def dsa_config(wl, copies: int, cache_bytes: int, world: int, single_pass: bool) -> dict:
+    """The `config` object of a DSA line (the GPU arm and the reference arm print the same one)."""
+    from prefill_dsa_indexer_gb300 import inputs as I
+    return {"workload": wl.name, "batch": len(wl.ctx), "rows": wl.num_rows, "ctx": wl.ctx[0], "k": wl.k,
+            "heads": wl.heads, "index_heads": 32, "page": 64, "key_bytes": I.INDEX_TOKEN_BYTES[wl.key_fmt],
+            "latent_bytes": I.LATENT_TOKEN_BYTES[wl.lat_fmt],
+            "parallelism": f"replicas{world}" if world > 1 else "single-gpu",
+            "topk": "single pass (scorer histogram)" if single_pass else "cluster radix select",
+            "l2": f"inputs > L2: {copies} rotating copies of the caches ({cache_bytes * copies / 1e9:.2f} GB)"}
+
+
+def measure_fp8_peak(n: int = 8192, reps: int = 10, sustain_s: float = 1.0) -> dict:
+    """Dense e4m3 x e4m3 -> bf16 GEMM throughput of this GPU through the library (torch._scaled_mm,
+    cuBLASLt), n^3: the best of `reps` timed calls (burst) and the mean over back-to-back calls for
+    about `sustain_s` seconds (sustained), in TFLOP/s (2 n^3 per call)."""
+    a = torch.randn(n, n, device="cuda").to(torch.float8_e4m3fn)
+    b = torch.randn(n, n, device="cuda").to(torch.float8_e4m3fn).t()  # column-major operand
+    one = torch.ones((), device="cuda", dtype=torch.float32)
+
+    def mm():
+        return torch._scaled_mm(a, b, scale_a=one, scale_b=one, out_dtype=torch.bfloat16, use_fast_accum=True)
+
+    for _ in range(3):
+        mm()
+    torch.cuda.synchronize()
+    best = float("inf")
+    for _ in range(reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        mm()
+        e1.record()
+        torch.cuda.synchronize()
+        best = min(best, e0.elapsed_time(e1))
+    flop = 2.0 * n ** 3
+    calls, t0 = 0, time.perf_counter()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    while time.perf_counter() - t0 < sustain_s:
+        for _ in range(20):
+            mm()
+        calls += 20
+        torch.cuda.synchronize()
+    e1.record()
+    torch.cuda.synchronize()
+    return {"burst_tflops": flop / (best / 1e3) / 1e12, "sustained_tflops": flop * calls / (e0.elapsed_time(e1) / 1e3) / 1e12,
+            "how": f"torch._scaled_mm e4m3 x e4m3 -> bf16, {n}^3, best of {reps} (burst), {calls} back-to-back "
+                   f"calls (sustained)"}
+
+
+def oracle_single_thread_ms(workload: str = "decode_tiny_4k") -> dict:
+    """One whole step of the smallest workload (indexer, top-k, slots, attention) on one host thread."""
+    import oracle
+    from prefill_dsa_indexer_gb300 import inputs as I
+    wl = I.workload(workload)
+    inp = I.make_inputs(wl, device="cpu")
+    h = {n: inp.np(n) for n in ("idx_pool", "lat_pool", "block_table", "row_req", "row_ctx", "q_idx", "head_w", "q_mla")}
+    lib = oracle.load()
+    before = lib.oracle_num_threads()
+    lib.oracle_set_num_threads(1)
+    try:
+        t0 = time.perf_counter()
+        lg = oracle.indexer_logits(h["idx_pool"], wl.key_fmt, h["block_table"], h["row_req"], h["row_ctx"], h["q_idx"],
+                                   h["head_w"])
+        idx = oracle.topk_f64(lg, h["row_ctx"], wl.k)
+        sl = oracle.page_to_slot(h["block_table"], h["row_req"], idx)
+        oracle.sparse_mla(h["lat_pool"], wl.lat_fmt, inp.tensor_scale, h["q_mla"], sl, 1.0 / np.sqrt(192.0))
+        ms = (time.perf_counter() - t0) * 1e3
+    finally:
+        lib.oracle_set_num_threads(before)
+    return {"workload": workload, "ms_per_step": ms, "threads": 1}
+
+
 def indexer_algorithmic_bytes(wl, token_bytes: int) -> int:
     """Bytes the indexer must move per launch: every cached key of every row group once
     (132 B/token FP8), the block-table entries, the queries and head weights, and the
@@ -169,11 +247,11 @@ def layer_algorithmic_bytes(wl, idx_bytes: int, lat_bytes: int) -> int:
 def run_reference(args, wl, rank):
     """The CPU oracle, as it stands, on a bounded sample per step of the same workload.
 
-    Each step takes one query row: the indexer scan over a contiguous slice of S of its
-    cached keys, the top-k and slots of that slice, and the sparse MLA of H_s of its heads
-    over the 2048 selected tokens.  S and H_s are sized so the K + W steps take about two
-    and a half minutes; the row's full cost is extrapolated linearly in keys (indexer,
-    top-k) and in heads (MLA)."""
+    Each step takes one whole query row (indexer scan over all its cached keys, top-k, slots,
+    sparse MLA of all heads) on every host thread.  Only when a whole row would not fit the
+    time budget (K + W steps in about two and a half minutes) does a step take the indexer
+    over the first S keys and the MLA of H_s heads, the row's cost then extrapolated linearly
+    in keys and heads (said in the line's `sample`)."""
     import oracle
     from prefill_dsa_indexer_gb300 import inputs as I
     inp = I.make_inputs(wl, device="cuda" if torch.cuda.is_available() else "cpu")
@@ -182,6 +260,7 @@ def run_reference(args, wl, rank):
     L = int(host["row_ctx"][0])
     H = wl.heads
     sm = 1.0 / np.sqrt(192.0)
+    cores = oracle.num_threads()  # the row's indexer chunks and attention heads run on every thread
 
     def part(S, Hs, r=0):
         rr = np.array([r])
@@ -198,9 +277,12 @@ def run_reference(args, wl, rank):
         return t1 - t0, t2 - t1
 
     budget = max(0.01, min(2.0, 150.0 / max(1, args.steps + args.warmup)))
-    ti, tm = part(min(L, 8192), 1)
-    S = int(min(L, max(wl.k, (0.5 * budget / max(ti, 1e-6)) * min(L, 8192))))
-    Hs = int(max(1, min(H, (0.5 * budget / max(tm, 1e-6)))))
+    ti, tm = part(L, H)
+    if ti + tm <= budget:  # whole rows fit the budget: nothing is extrapolated
+        S, Hs = L, H
+    else:
+        S = int(min(L, max(wl.k, (0.5 * budget / max(ti, 1e-6)) * L)))
+        Hs = int(max(1, min(H, (0.5 * budget / max(tm, 1e-6)) * H)))
     for _ in range(args.warmup):
         part(S, Hs)
     est, wall = 0.0, 0.0
@@ -210,14 +292,15 @@ def run_reference(args, wl, rank):
         est += a * L / S + b * H / Hs
     wall = time.perf_counter() - t0
     value = args.steps / est
-    cores = 1  # one query row per step: the oracle's OpenMP loop over rows runs one thread
     sample = (f"per step 1 of {wl.num_rows} query rows of {wl.name}: indexer + top-k over {S} of its {L} keys, "
-              f"sparse MLA of {Hs} of {H} heads over the selected tokens; full-row time extrapolated linearly "
-              f"(keys, heads); {wall:.1f} s of CPU work")
+              f"sparse MLA of {Hs} of {H} heads over the selected tokens"
+              + ("" if (S, Hs) == (L, H) else "; full-row time extrapolated linearly (keys, heads)")
+              + f"; {cores} threads, {wall:.1f} s of CPU work")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * est / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": wl.name, "rows": wl.num_rows, "ctx": wl.ctx[0], "k": wl.k, "heads": wl.heads},
+            "config": dsa_config(wl, max(1, args.copies), inp.idx_pool.numel() + inp.lat_pool.numel(), args.gpus,
+                                 args.single_pass),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     if rank == 0:
@@ -225,13 +308,14 @@ def run_reference(args, wl, rank):
 
 
 def cpu_baseline(wl, inp, budget_s=12.0):
-    """The oracle on whole rows of the workload (all host threads, OpenMP over rows), cycling
-    over the rows until about budget_s of wall time."""
+    """The oracle on whole rows of the workload, cycling over the rows until about budget_s of wall
+    time, on every host thread (OpenMP over (row, token chunk) for the indexer, (row, head) for the
+    attention)."""
     import oracle
     host = {n: inp.np(n) for n in ("idx_pool", "lat_pool", "block_table", "row_req", "row_ctx", "q_idx", "head_w",
                                     "q_mla")}
     threads = oracle.num_threads()
-    done, t_used, n = 0, 0.0, max(1, min(threads, wl.num_rows))
+    done, t_used, n = 0, 0.0, 1
     while t_used < budget_s:
         rows = (np.arange(n) + done) % wl.num_rows
         t0 = time.perf_counter()
@@ -243,9 +327,10 @@ def cpu_baseline(wl, inp, budget_s=12.0):
                           1.0 / np.sqrt(192.0))
         t_used += time.perf_counter() - t0
         done += len(rows)
-    return {"value": done / t_used, "unit": UNIT, "cores": n, "kind": "oracle",
-            "sample": f"{done} query rows of {wl.name} (whole rows: full indexer scan, top-k, MLA), "
-                      f"{t_used:.1f} s"}
+    return {"value": done / t_used, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": f"{done} query rows of {wl.name} (whole rows: full indexer scan, top-k, MLA), one row "
+                      f"per call on {threads} threads, {t_used:.1f} s",
+            "single_thread": oracle_single_thread_ms()}
 
 
 def msa_score_bytes(wl) -> int:
@@ -333,22 +418,29 @@ def run_msa(args, rank, world, local, dist):
     torch.cuda.synchronize()
     reps = max(1, args.steps // n)
     steps = reps * n
-    if dist is not None:
-        dist.barrier()
-    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    torch.cuda.synchronize()
-    with ClockSampler(local) as clk:
+    rep_ms = []
+    with ClockSampler(local) as clk:  # REPEATS timed regions, then >= 0.6 s more of the same steps
         clk.wait_first()
         h0 = time.time()
-        t0.record(stream)
-        for _ in range(reps):
-            g.replay()
-        t1.record(stream)
-        torch.cuda.synchronize()
+        for _rep in range(REPEATS):
+            t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            if dist is not None:
+                dist.barrier()
+            torch.cuda.synchronize()
+            t0.record(stream)
+            for _ in range(reps):
+                g.replay()
+            t1.record(stream)
+            torch.cuda.synchronize()
+            if dist is not None:
+                dist.barrier()
+            rep_ms.append(t0.elapsed_time(t1))
         h1 = time.time()
-    if dist is not None:
-        dist.barrier()
-    total_ms = t0.elapsed_time(t1)
+        while time.time() - h1 < 0.6:
+            g.replay()
+            torch.cuda.synchronize()
+        h2 = time.time()
+    total_ms = statistics.median(rep_ms)
     total_ms = max_over_ranks(total_ms, dist)
     P.check_status(st, "timed steps")
     for _ in range(3):
@@ -410,7 +502,9 @@ def run_msa(args, rank, world, local, dist):
         "gpu_launches": 4 * steps,
         "launch": f"CUDA graphs of {n} consecutive steps; block scores timed after the timed loop by event "
                   f"nodes around each launch in a replay of the same steps",
-        "clocks": clk.summary(h0, h1),
+        "repeats_ms_per_step": [m / steps for m in rep_ms],
+        "clocks": dict(clk.summary(h0, h2), window=f"the {REPEATS} timed regions and {h2 - h1:.2f} s of the "
+                                                       f"same steps right after them"),
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         import oracle
@@ -592,14 +686,8 @@ def main():
         torch.cuda.synchronize()
 
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    t_start, t_stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    if dist is not None:
-        dist.barrier()
-    torch.cuda.synchronize()
-    with ClockSampler(local) as clk:
-        clk.wait_first()
-        h0 = time.time()
-        t_start.record(stream)
+
+    def timed_steps():  # exactly args.steps steps
         if graph_mode == "multi-step":
             for (g, _), reps in runs:
                 for _r in range(reps):
@@ -614,12 +702,33 @@ def main():
         else:
             for i in range(args.steps):
                 step(i, evs[i])
-        t_stop.record(stream)
-        torch.cuda.synchronize()
+
+    # REPEATS timed regions of exactly args.steps steps, each bracketed by a barrier and a device
+    # synchronisation; the line reports their median.  nvidia-smi samples the clocks throughout and
+    # over a further >= 0.6 s of the same steps right after, so short timed regions still come with
+    # clock samples under the same load.
+    rep_ms = []
+    with ClockSampler(local) as clk:
+        clk.wait_first()
+        h0 = time.time()
+        for _rep in range(REPEATS):
+            t_start, t_stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            if dist is not None:
+                dist.barrier()
+            torch.cuda.synchronize()
+            t_start.record(stream)
+            timed_steps()
+            t_stop.record(stream)
+            torch.cuda.synchronize()
+            if dist is not None:
+                dist.barrier()
+            rep_ms.append(t_start.elapsed_time(t_stop))
         h1 = time.time()
-    if dist is not None:
-        dist.barrier()
-    total_ms = t_start.elapsed_time(t_stop)
+        while time.time() - h1 < 0.6:
+            timed_steps()
+            torch.cuda.synchronize()
+        h2 = time.time()
+    total_ms = statistics.median(rep_ms)
     if graph_mode == "multi-step":
         for _r in range(3):
             probe[0].replay()
@@ -764,14 +873,16 @@ def main():
     if prefill:
         flops = indexer_flops(wl)
         achieved = flops / (idx_ms / 1000.0) / 1e12
-        roof = {"kernel": "indexer_fp8_kernel<8>", "bound": "tensor", "achieved": achieved, "peak": fp8_peak,
-                "unit": "TFLOP/s", "frac": achieved / fp8_peak,
-                "peak_kind": f"{peak_kind} bf16 burst x {FP8_OVER_BF16} (FP8/bf16 nominal)",
-                "algorithmic_flops": flops, "ms_per_launch": idx_ms}
+        fp8 = measure_fp8_peak()
+        roof = {"kernel": "indexer_kernel<8, fp8 keys>", "bound": "tensor", "achieved": achieved,
+                "peak": fp8["burst_tflops"], "unit": "TFLOP/s", "frac": achieved / fp8["burst_tflops"],
+                "peak_kind": f"measured in this run: {fp8['how']}",
+                "frac_of_sustained": achieved / fp8["sustained_tflops"], "peak_sustained": fp8["sustained_tflops"],
+                "frac_of_bf16_x2": achieved / fp8_peak, "algorithmic_flops": flops, "ms_per_launch": idx_ms}
     else:
         achieved = idx_bytes / (idx_ms / 1000.0) / 1e9
-        kname = "indexer_fp8_kernel" if wl.key_fmt == I.KEY_FP8 else "indexer_mxfp4_kernel"
-        roof = {"kernel": f"{kname}<{wl.rows_per_group}>",
+        kname = "fp8 keys" if wl.key_fmt == I.KEY_FP8 else "mxfp4 keys"
+        roof = {"kernel": f"indexer_kernel<{wl.rows_per_group}, {kname}>",
                 "bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
                 "peak_kind": peak_kind, "algorithmic_bytes": idx_bytes, "ms_per_launch": idx_ms}
     traffic = None
@@ -788,12 +899,8 @@ def main():
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "e4m3xe4m3->f32 (indexer), f16xf16->f32 (mla)", "data": "synthetic",
-        "config": {"workload": wl.name, "batch": len(wl.ctx), "rows": wl.num_rows, "ctx": wl.ctx[0], "k": wl.k,
-                   "heads": wl.heads, "index_heads": 32, "page": 64, "key_bytes": idx_tok, "latent_bytes": lat_tok,
-                   "parallelism": f"replicas{world}" if world > 1 else "single-gpu",
-                   "topk": "single pass (scorer histogram)" if args.single_pass else "cluster radix select",
-                   "l2": f"inputs > L2: {copies} rotating copies of the caches "
-                         f"({(inp.idx_pool.numel() + inp.lat_pool.numel()) * copies / 1e9:.2f} GB)"},
+        "config": dsa_config(wl, copies, inp.idx_pool.numel() + inp.lat_pool.numel(), world, args.single_pass),
+        "repeats_ms_per_step": [m / args.steps for m in rep_ms],
         "layer_hbm_gbs": layer_bytes / (ms_per_step / 1000.0) / 1e9,
         "layer_algorithmic_bytes": layer_bytes,
         "layer_frac_of_8tbs": layer_bytes / (ms_per_step / 1000.0) / 8e12,
@@ -809,7 +916,8 @@ def main():
                                  f"({len(samples)} launches sampled)",
                    "two-graphs": "CUDA-graph replay (indexer graph + rest-of-step graph), stream events between",
                    "eager": "eager launches, stream events around the indexer"}[graph_mode],
-        "clocks": clk.summary(h0, h1),
+        "clocks": dict(clk.summary(h0, h2), window=f"the {REPEATS} timed regions and {h2 - h1:.2f} s of the "
+                                                       f"same steps right after them"),
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl, inp)

@@ -47,6 +47,9 @@
 
 #ifdef _OPENMP
 #include <omp.h>
+
+/* tokens per indexer work item (a row is cut into such chunks for the threads) */
+#define OR_CHUNK 4096
 #endif
 
 #define OR_OK 0
@@ -177,14 +180,22 @@ int oracle_indexer_logits(const uint8_t *pool, int fmt, int64_t num_pages,
                           double *logits, int64_t stride) {
     if (oracle_index_page_bytes(fmt) < 0) return OR_ERR_ARG;
     int err = OR_OK;
+    /* work items: (row, chunk of OR_CHUNK tokens); each logit is computed alone, in the same
+     * order whatever the thread count */
+    int max_ctx = 0;
+    for (int r = 0; r < num_rows; ++r) max_ctx = row_ctx[r] > max_ctx ? row_ctx[r] : max_ctx;
+    const int chunks = (max_ctx + OR_CHUNK - 1) / OR_CHUNK;
 #pragma omp parallel for schedule(dynamic, 1)
-    for (int r = 0; r < num_rows; ++r) {
+    for (int64_t item = 0; item < (int64_t)num_rows * chunks; ++item) {
+        const int r = (int)(item / chunks), c = (int)(item % chunks);
+        const int t0 = c * OR_CHUNK, t1 = row_ctx[r] < t0 + OR_CHUNK ? row_ctx[r] : t0 + OR_CHUNK;
+        if (t0 >= t1) continue;
         double q[OR_IDX_HEADS][OR_IDX_DIM], k[OR_IDX_DIM], s;
         for (int h = 0; h < OR_IDX_HEADS; ++h)
             for (int i = 0; i < OR_IDX_DIM; ++i)
                 q[h][i] = oracle_e4m3_decode(q_idx[((int64_t)r * OR_IDX_HEADS + h) * OR_IDX_DIM + i]);
         const int32_t *bt = block_table + (int64_t)row_req[r] * bt_stride;
-        for (int t = 0; t < row_ctx[r]; ++t) {
+        for (int t = t0; t < t1; ++t) {
             int64_t page = bt[t / OR_PAGE];
             if (page < 0 || page >= num_pages) {
 #pragma omp atomic write
@@ -291,13 +302,16 @@ int oracle_sparse_mla(const uint8_t *pool, int fmt, int64_t num_pages, double te
                       double sm_scale, double *out, double *lse) {
     if (oracle_latent_page_bytes(fmt) < 0 || num_heads <= 0) return OR_ERR_ARG;
     int err = OR_OK;
+    /* first every row's selected latents, decoded (rows in parallel); then every (row, head)
+     * alone, in the same order whatever the thread count */
+    double **kvs = (double **)calloc((size_t)(num_rows > 0 ? num_rows : 1), sizeof(double *));
+    int *ns = (int *)calloc((size_t)(num_rows > 0 ? num_rows : 1), sizeof(int));
 #pragma omp parallel for schedule(dynamic, 1)
     for (int r = 0; r < num_rows; ++r) {
         const int32_t *sl = slots + (int64_t)r * k;
         int n = 0;
         for (int i = 0; i < k; ++i) n += sl[i] >= 0;
         double *kv = (double *)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1) * OR_LAT_DIM);
-        double *sc = (double *)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1));
         int j = 0;
         for (int i = 0; i < k; ++i) {
             if (sl[i] < 0) continue;
@@ -309,8 +323,16 @@ int oracle_sparse_mla(const uint8_t *pool, int fmt, int64_t num_pages, double te
             decode_latent(pool, fmt, sl[i], tensor_scale, kv + (int64_t)j * OR_LAT_DIM);
             ++j;
         }
-        n = j;
-        for (int h = 0; h < num_heads; ++h) {
+        kvs[r] = kv;
+        ns[r] = j;
+    }
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t item = 0; item < (int64_t)num_rows * num_heads; ++item) {
+        const int r = (int)(item / num_heads), h = (int)(item % num_heads);
+        const int n = ns[r];
+        const double *kv = kvs[r];
+        double *sc = (double *)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1));
+        {
             double qh[OR_LAT_DIM];
             const uint16_t *qp = q + ((int64_t)r * num_heads + h) * OR_LAT_DIM;
             for (int i = 0; i < OR_LAT_DIM; ++i) qh[i] = oracle_bf16_decode(qp[i]);
@@ -318,6 +340,7 @@ int oracle_sparse_mla(const uint8_t *pool, int fmt, int64_t num_pages, double te
             for (int d = 0; d < OR_V_DIM; ++d) o[d] = 0.0;
             if (n == 0) {
                 if (lse) lse[(int64_t)r * num_heads + h] = -INFINITY;
+                free(sc);
                 continue;
             }
             double m = -INFINITY;
@@ -336,9 +359,11 @@ int oracle_sparse_mla(const uint8_t *pool, int fmt, int64_t num_pages, double te
             for (int d = 0; d < OR_V_DIM; ++d) o[d] /= l;
             if (lse) lse[(int64_t)r * num_heads + h] = m + log(l);
         }
-        free(kv);
         free(sc);
     }
+    for (int r = 0; r < num_rows; ++r) free(kvs[r]);
+    free(kvs);
+    free(ns);
     return err;
 }
 

@@ -39,7 +39,8 @@ MUTATIONS = [
     ("relu dropped", "(a > 0.0 ? a : 0.0)", "a"),
     ("head weight index", "w[(int64_t)r * OR_IDX_HEADS + h]", "w[(int64_t)r * OR_IDX_HEADS + (h ^ 1)]"),
     ("query head transposed", "q[h][i] * k[i]", "q[i % OR_IDX_HEADS][(i + h) % OR_IDX_DIM] * k[i]"),
-    ("causal extent off by one", "for (int t = 0; t < row_ctx[r]; ++t) {", "for (int t = 0; t + 1 < row_ctx[r]; ++t) {"),
+    ("causal extent off by one", "t1 = row_ctx[r] < t0 + OR_CHUNK ? row_ctx[r] : t0 + OR_CHUNK;",
+     "t1 = row_ctx[r] - 1 < t0 + OR_CHUNK ? row_ctx[r] - 1 : t0 + OR_CHUNK;"),
     ("tie break to higher index", "return (x->t > y->t) - (x->t < y->t);", "return (x->t < y->t) - (x->t > y->t);"),
     ("top-k ascending", "if (x->v > y->v) return -1;", "if (x->v < y->v) return -1;"),
     ("slot offset", "bt[t / OR_PAGE] * OR_PAGE + t % OR_PAGE", "bt[t / OR_PAGE] * OR_PAGE + t / OR_PAGE"),
