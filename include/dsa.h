@@ -137,9 +137,25 @@ int dsa_indexer_logits(const dsa_cache *index_cache, const dsa_rows *rows, const
  * Logits compare as floats (-0 == +0); they must be finite.  k in
  * [1, DSA_MAX_TOPK].  Exact and deterministic: given identical logits the
  * result is bit-identical.
+ *
+ * workspace (device, 256-byte aligned, no initial contents) may be NULL.
+ * With workspace_bytes >= dsa_topk_workspace_size(num_rows, max_ctx, k) > 0
+ * (a few long rows), the selection runs in two phases: independent CTAs
+ * reduce chunks of each row to their best candidates (in position order),
+ * and one CTA per row selects among them, checking that no chunk may hold
+ * more selected keys than it passed on; when one may (scores concentrated in
+ * one chunk, or tied at the threshold across chunks), that row is selected
+ * from its whole logits instead.  Without it (NULL, or a size of 0 for this
+ * shape), one thread-block cluster per row selects.  A workspace smaller than
+ * the size is DSA_ERR_WORKSPACE.  The result is the same either way.
  */
 int dsa_topk(const float *logits, int64_t logits_stride, const int32_t *row_ctx, int32_t num_rows,
-             int32_t max_ctx, int32_t k, int32_t *idx_out, int32_t *dev_status, void *stream);
+             int32_t max_ctx, int32_t k, int32_t *idx_out, int32_t *dev_status, void *workspace,
+             size_t workspace_bytes, void *stream);
+
+/* Workspace bytes of the two-phase top-k for this batch on the current device; 0 when the shape
+ * (more than 64 rows, or rows of at most 262,144 keys) takes the cluster selection, which needs none. */
+size_t dsa_topk_workspace_size(int32_t num_rows, int32_t max_ctx, int32_t k);
 
 /*
  * Top-k and page -> slot in one call (the two steps below, dsa_topk then
@@ -147,10 +163,12 @@ int dsa_topk(const float *logits, int64_t logits_stride, const int32_t *row_ctx,
  * written): idx_out as dsa_topk over rows->row_ctx / rows->max_ctx, and
  * slots_out[r, i] = block_table[row_req[r]][t / 64] * 64 + t % 64 for each
  * selected t = idx_out[r, i] (-1 where idx_out is -1).  A page id outside
- * [0, pool_pages) or a bad row_req is DSA_ERR_BOUNDS with slot -1.
+ * [0, pool_pages) or a bad row_req is DSA_ERR_BOUNDS with slot -1.  workspace
+ * as for dsa_topk.
  */
 int dsa_topk_slots(const float *logits, int64_t logits_stride, const dsa_rows *rows, int64_t pool_pages, int32_t k,
-                   int32_t *idx_out, int32_t *slots_out, int32_t *dev_status, void *stream);
+                   int32_t *idx_out, int32_t *slots_out, int32_t *dev_status, void *workspace, size_t workspace_bytes,
+                   void *stream);
 
 /*
  * dsa_topk_slots whose output pass also warms L2 with the selected tokens'
@@ -160,10 +178,11 @@ int dsa_topk_slots(const float *logits, int64_t logits_stride, const dsa_rows *r
  * latent_cache: the latent pool the slots index (its num_pages bounds the
  * slots).  FP8 latents (576 contiguous bytes per slot) are prefetched; an
  * NVFP4 pool gets the plain dsa_topk_slots result.  Outputs are identical to
- * dsa_topk_slots.
+ * dsa_topk_slots.  workspace as for dsa_topk.
  */
 int dsa_topk_slots_warm(const float *logits, int64_t logits_stride, const dsa_rows *rows, const dsa_cache *latent_cache,
-                        int32_t k, int32_t *idx_out, int32_t *slots_out, int32_t *dev_status, void *stream);
+                        int32_t k, int32_t *idx_out, int32_t *slots_out, int32_t *dev_status, void *workspace,
+                        size_t workspace_bytes, void *stream);
 
 /*
  * Single-pass scorer + top-k (blog section "Low-latency decode: fused DSA

@@ -66,7 +66,9 @@ def load_library(path: str | None = None):
     lib.dsa_indexer_logits.restype = ctypes.c_int
     lib.dsa_indexer_logits.argtypes = [ctypes.POINTER(_Cache), ctypes.POINTER(_Rows), P, P, P, I64, P, P]
     lib.dsa_topk.restype = ctypes.c_int
-    lib.dsa_topk.argtypes = [P, I64, P, I32, I32, I32, P, P, P]
+    lib.dsa_topk.argtypes = [P, I64, P, I32, I32, I32, P, P, P, ctypes.c_size_t, P]
+    lib.dsa_topk_workspace_size.restype = ctypes.c_size_t
+    lib.dsa_topk_workspace_size.argtypes = [I32, I32, I32]
     lib.dsa_page_to_slot.restype = ctypes.c_int
     lib.dsa_page_to_slot.argtypes = [ctypes.POINTER(_Rows), I64, P, I32, P, P, P]
     for name in ("dsa_sparse_mla_decode", "dsa_sparse_mla_prefill"):
@@ -89,11 +91,12 @@ def load_library(path: str | None = None):
     lib.dsa_indexer_topk_workspace_size.restype = ctypes.c_size_t
     lib.dsa_indexer_topk_workspace_size.argtypes = [I32, I32]
     lib.dsa_topk_slots.restype = ctypes.c_int
-    lib.dsa_topk_slots.argtypes = [P, I64, ctypes.POINTER(_Rows), I64, I32, P, P, P, P]
+    lib.dsa_topk_slots.argtypes = [P, I64, ctypes.POINTER(_Rows), I64, I32, P, P, P, P, ctypes.c_size_t, P]
     lib.dsa_selftest_wait_timeout.restype = ctypes.c_int
     lib.dsa_selftest_wait_timeout.argtypes = [P, P]
     lib.dsa_topk_slots_warm.restype = ctypes.c_int
-    lib.dsa_topk_slots_warm.argtypes = [P, I64, ctypes.POINTER(_Rows), ctypes.POINTER(_Cache), I32, P, P, P, P]
+    lib.dsa_topk_slots_warm.argtypes = [P, I64, ctypes.POINTER(_Rows), ctypes.POINTER(_Cache), I32, P, P, P, P,
+                                        ctypes.c_size_t, P]
     lib.dsa_sparse_mla_decode_prepare.restype = ctypes.c_int
     lib.dsa_sparse_mla_decode_prepare.argtypes = [ctypes.POINTER(_Cache), P, I32, I32, I32, P, P, ctypes.c_size_t, P]
     lib.dsa_sparse_mla_decode_prepared.restype = ctypes.c_int
@@ -116,7 +119,7 @@ def load_library(path: str | None = None):
 EXPORTED = ("dsa_version", "dsa_status_string", "dsa_indexer_logits", "dsa_topk", "dsa_page_to_slot",
             "dsa_sparse_mla_decode", "dsa_sparse_mla_prefill", "dsa_sparse_mla_workspace_size",
             "dsa_sparse_mla_decode_noalloc", "dsa_cache_insert", "dsa_indexer_logits_hist", "dsa_topk_hist",
-            "dsa_indexer_topk", "dsa_indexer_topk_workspace_size", "dsa_topk_slots",
+            "dsa_indexer_topk", "dsa_indexer_topk_workspace_size", "dsa_topk_slots", "dsa_topk_workspace_size",
             "dsa_sparse_mla_decode_prepare", "dsa_sparse_mla_decode_prepared", "dsa_msa_block_scores",
             "dsa_msa_select", "dsa_msa_attention", "dsa_msa_attention_workspace_size", "dsa_topk_slots_warm",
             "dsa_selftest_wait_timeout")
@@ -178,13 +181,24 @@ def indexer_logits(index_pool, key_fmt, block_table, row_req, row_ctx, max_ctx, 
     return logits
 
 
-def topk(logits, row_ctx, max_ctx, k=2048, out=None, status=None, stream=None):
-    """dsa_topk: int32 [R, k] selected positions, ascending, -1 padded."""
+def topk_workspace_size(num_rows: int, max_ctx: int, k: int = 2048) -> int:
+    """dsa_topk_workspace_size: bytes of the two-phase top-k's workspace (0: the shape needs none)."""
+    return int(load_library().dsa_topk_workspace_size(num_rows, max_ctx, k))
+
+
+def _ws(workspace):
+    return (_ptr(workspace), workspace.numel() * workspace.element_size()) if workspace is not None else (None, 0)
+
+
+def topk(logits, row_ctx, max_ctx, k=2048, out=None, status=None, stream=None, workspace=None):
+    """dsa_topk: int32 [R, k] selected positions, ascending, -1 padded (`workspace`: optional, see
+    topk_workspace_size)."""
     R = row_ctx.shape[0]
     if out is None:
         out = torch.empty((R, k), dtype=torch.int32, device=logits.device)
+    wp, wb = _ws(workspace)
     rc = load_library().dsa_topk(_ptr(logits), logits.stride(0), _ptr(row_ctx), R, int(max_ctx), int(k), _ptr(out),
-                                 _ptr(status), _stream(stream))
+                                 _ptr(status), wp, wb, _stream(stream))
     _check(rc, "dsa_topk")
     return out
 
@@ -238,7 +252,7 @@ def indexer_topk(index_pool, key_fmt, block_table, row_req, row_ctx, max_ctx, q_
 
 
 def topk_slots(logits, block_table, row_req, row_ctx, max_ctx, pool_pages, k=2048, out=None, slots=None,
-               status=None, stream=None):
+               status=None, stream=None, workspace=None):
     """dsa_topk_slots: (idx int32 [R, k], slots int32 [R, k]) — top-k with the page -> slot translation."""
     R = row_ctx.shape[0]
     if out is None:
@@ -246,14 +260,15 @@ def topk_slots(logits, block_table, row_req, row_ctx, max_ctx, pool_pages, k=204
     if slots is None:
         slots = torch.empty((R, k), dtype=torch.int32, device=logits.device)
     r = _rows(block_table, row_req, row_ctx, max_ctx)
+    wp, wb = _ws(workspace)
     rc = load_library().dsa_topk_slots(_ptr(logits), logits.stride(0), ctypes.byref(r), int(pool_pages), int(k),
-                                       _ptr(out), _ptr(slots), _ptr(status), _stream(stream))
+                                       _ptr(out), _ptr(slots), _ptr(status), wp, wb, _stream(stream))
     _check(rc, "dsa_topk_slots")
     return out, slots
 
 
 def topk_slots_warm(logits, block_table, row_req, row_ctx, max_ctx, lat_pool, lat_fmt, k=2048, out=None,
-                    slots=None, status=None, stream=None):
+                    slots=None, status=None, stream=None, workspace=None):
     """dsa_topk_slots_warm: topk_slots whose output pass also prefetches the selected FP8 latents into L2."""
     R = row_ctx.shape[0]
     if out is None:
@@ -262,8 +277,9 @@ def topk_slots_warm(logits, block_table, row_req, row_ctx, max_ctx, lat_pool, la
         slots = torch.empty((R, k), dtype=torch.int32, device=logits.device)
     r = _rows(block_table, row_req, row_ctx, max_ctx)
     c = _cache(lat_pool, lat_fmt)
+    wp, wb = _ws(workspace)
     rc = load_library().dsa_topk_slots_warm(_ptr(logits), logits.stride(0), ctypes.byref(r), ctypes.byref(c), int(k),
-                                            _ptr(out), _ptr(slots), _ptr(status), _stream(stream))
+                                            _ptr(out), _ptr(slots), _ptr(status), wp, wb, _stream(stream))
     _check(rc, "dsa_topk_slots_warm")
     return out, slots
 
@@ -440,6 +456,9 @@ class Layer:
         self.lse = self.outputs[R * H * VALUE_DIM:].view(R, H)
         need = 0 if prefill else sparse_mla_workspace_size(R, H, self.k)
         self.workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=device)
+        # the two-phase top-k's candidates (few long rows; none otherwise)
+        tk = topk_workspace_size(R, self.max_ctx, self.k)
+        self.topk_workspace = torch.empty(tk, dtype=torch.uint8, device=device) if tk > 0 else None
         self.status = new_status(device)
         # single pass: the scorer builds each row's histogram and the top-k starts from it (opt-in:
         # on one GB300 the scorer's histogram atomics cost more than the selection saves)
@@ -470,10 +489,12 @@ class Layer:
                          out=self.slots, status=self.status, stream=stream)
         elif not self.prefill:  # decode: top-k with page -> slot, warming L2 with the chosen latents
             topk_slots_warm(self.logits, self.block_table, row_req, row_ctx, self.max_ctx, self.lat_pool,
-                            self.lat_fmt, self.k, out=self.idx, slots=self.slots, status=self.status, stream=stream)
+                            self.lat_fmt, self.k, out=self.idx, slots=self.slots, status=self.status, stream=stream,
+                            workspace=self.topk_workspace)
         else:  # top-k with the page -> slot translation in its output pass
             topk_slots(self.logits, self.block_table, row_req, row_ctx, self.max_ctx, self.lat_pool.shape[0], self.k,
-                       out=self.idx, slots=self.slots, status=self.status, stream=stream)
+                       out=self.idx, slots=self.slots, status=self.status, stream=stream,
+                       workspace=self.topk_workspace)
 
     def attend(self, q_mla, stream=None, prepared=False):
         """Sparse MLA over self.slots (`prepared`: prepare() ran already for these queries)."""

@@ -190,13 +190,33 @@ int dsa_indexer_logits_hist(const dsa_cache *index_cache, const dsa_rows *rows, 
 static int topk_common(const float *logits, int64_t logits_stride, const int32_t *row_ctx, int32_t num_rows,
                        int32_t max_ctx, int32_t k, uint32_t *hist, bool discard, int32_t *idx_out,
                        int32_t *dev_status, void *stream, const dsa_rows *slot_rows = nullptr,
-                       int64_t pool_pages = 0, int32_t *slots_out = nullptr, const uint8_t *warm_pool = nullptr) {
+                       int64_t pool_pages = 0, int32_t *slots_out = nullptr, const uint8_t *warm_pool = nullptr,
+                       void *workspace = nullptr, size_t workspace_bytes = 0) {
     if (num_rows < 0 || max_ctx < 0) return DSA_ERR_INVALID_ARG;
     if (k < 1 || k > DSA_MAX_TOPK) return DSA_ERR_UNSUPPORTED;
     if (num_rows == 0) return DSA_OK;
     if (!logits || !row_ctx || !idx_out || logits_stride < max_ctx) return DSA_ERR_INVALID_ARG;
     TopkArgs a{logits, logits_stride, row_ctx, num_rows, max_ctx, k, idx_out, dev_status, hist, discard,
                nullptr, nullptr, 0, nullptr, 0, 0};
+    if (workspace != nullptr && hist == nullptr) {
+        // with a large enough workspace, few long rows take the two-phase selection
+        const TopkChunkPlan p = topk_chunk_plan(num_rows, max_ctx, k, device_sm_count());
+        if (p.bytes > 0) {
+            if (workspace_bytes < p.bytes) return DSA_ERR_WORKSPACE;
+            if (!aligned(workspace, 256)) return DSA_ERR_INVALID_ARG;
+            const size_t cand = align256(static_cast<size_t>(num_rows) * p.chunks * p.kcap * 4);
+            uint8_t *w = static_cast<uint8_t *>(workspace);
+            a.cand_key = reinterpret_cast<uint32_t *>(w);
+            a.cand_pos = reinterpret_cast<int32_t *>(w + cand);
+            a.cand_meta = reinterpret_cast<uint32_t *>(w + 2 * cand);
+            a.chunks = p.chunks;
+            a.chunk_len = p.chunk_len;
+            a.keep = p.keep;
+            a.keep_last = p.keep_last;
+            a.kcap = p.kcap;
+            a.merge_max = p.merge_max;
+        }
+    }
     if (slots_out != nullptr) {
         if (slot_rows == nullptr || pool_pages <= 0) return DSA_ERR_INVALID_ARG;
         if (pool_pages * DSA_PAGE_SIZE > INT32_MAX) return DSA_ERR_UNSUPPORTED;
@@ -211,8 +231,13 @@ static int topk_common(const float *logits, int64_t logits_stride, const int32_t
     return launch_status(launch_topk(a, static_cast<cudaStream_t>(stream)));
 }
 
+size_t dsa_topk_workspace_size(int32_t num_rows, int32_t max_ctx, int32_t k) {
+    return topk_chunk_plan(num_rows, max_ctx, k, device_sm_count()).bytes;
+}
+
 int dsa_topk_slots_warm(const float *logits, int64_t logits_stride, const dsa_rows *rows, const dsa_cache *latent_cache,
-                        int32_t k, int32_t *idx_out, int32_t *slots_out, int32_t *dev_status, void *stream) {
+                        int32_t k, int32_t *idx_out, int32_t *slots_out, int32_t *dev_status, void *workspace,
+                        size_t workspace_bytes, void *stream) {
     int rc = check_rows(rows);
     if (rc != DSA_OK) return rc;
     if (latent_cache == nullptr || latent_cache->page_size != DSA_PAGE_SIZE) return DSA_ERR_INVALID_ARG;
@@ -223,22 +248,25 @@ int dsa_topk_slots_warm(const float *logits, int64_t logits_stride, const dsa_ro
         latent_cache->format == DSA_LATENT_FP8 ? static_cast<const uint8_t *>(latent_cache->base) : nullptr;
     if (latent_cache->format != DSA_LATENT_FP8 && latent_cache->format != DSA_LATENT_NVFP4) return DSA_ERR_UNSUPPORTED;
     return topk_common(logits, logits_stride, rows->row_ctx, rows->num_rows, rows->max_ctx, k, nullptr, false,
-                       idx_out, dev_status, stream, rows, latent_cache->num_pages, slots_out, warm);
+                       idx_out, dev_status, stream, rows, latent_cache->num_pages, slots_out, warm, workspace,
+                       workspace_bytes);
 }
 
 int dsa_topk_slots(const float *logits, int64_t logits_stride, const dsa_rows *rows, int64_t pool_pages, int32_t k,
-                   int32_t *idx_out, int32_t *slots_out, int32_t *dev_status, void *stream) {
+                   int32_t *idx_out, int32_t *slots_out, int32_t *dev_status, void *workspace, size_t workspace_bytes,
+                   void *stream) {
     int rc = check_rows(rows);
     if (rc != DSA_OK) return rc;
     if (rows->num_rows > 0 && slots_out == nullptr) return DSA_ERR_INVALID_ARG;
     return topk_common(logits, logits_stride, rows->row_ctx, rows->num_rows, rows->max_ctx, k, nullptr, false,
-                       idx_out, dev_status, stream, rows, pool_pages, slots_out);
+                       idx_out, dev_status, stream, rows, pool_pages, slots_out, nullptr, workspace, workspace_bytes);
 }
 
 int dsa_topk(const float *logits, int64_t logits_stride, const int32_t *row_ctx, int32_t num_rows,
-             int32_t max_ctx, int32_t k, int32_t *idx_out, int32_t *dev_status, void *stream) {
+             int32_t max_ctx, int32_t k, int32_t *idx_out, int32_t *dev_status, void *workspace,
+             size_t workspace_bytes, void *stream) {
     return topk_common(logits, logits_stride, row_ctx, num_rows, max_ctx, k, nullptr, false, idx_out, dev_status,
-                       stream);
+                       stream, nullptr, 0, nullptr, nullptr, workspace, workspace_bytes);
 }
 
 int dsa_topk_hist(const float *logits, int64_t logits_stride, const int32_t *row_ctx, int32_t num_rows,

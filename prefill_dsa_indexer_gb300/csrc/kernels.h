@@ -91,9 +91,31 @@ struct TopkArgs {
     // optional: FP8 latent pool whose selected rows (576 B per slot) are prefetched into L2 as
     // the slots are written, so the attention that follows gathers from L2
     const uint8_t *warm_pool;
+    // optional two-phase selection (chunks > 0; see topk_chunk_plan): per-chunk candidates in a
+    // caller workspace, [rows][chunks][kcap] keys and positions, [rows][chunks][4] meta
+    uint32_t *cand_key;
+    int32_t *cand_pos;
+    uint32_t *cand_meta;
+    int32_t chunks, chunk_len, keep, keep_last, kcap, merge_max;
 };
 
 cudaError_t launch_topk(const TopkArgs &a, cudaStream_t s);
+
+// Two-phase top-k of decode rows: limits, and the plan for a batch (bytes == 0: not used).  Its two
+// kernels each run several block-wide rounds of about a microsecond; measured on a GB300, that beats
+// the cluster selection only once the rows are longer than a 16-CTA cluster keeps in shared memory
+// (1M keys: 97.7 vs 104.1 us per verify step; 128K keys: 76.3 vs 62.2 us per decode step).
+constexpr int kChunkedMaxRows = 64;
+constexpr int kChunkedMinCtx = 262144;
+constexpr int kChunkMinKeys = 2048;
+constexpr int kChunkedMaxChunks = 96;
+constexpr int kChunkMaxKeys = 16384;
+constexpr int kMergeMaxKeys = 16384;
+struct TopkChunkPlan {
+    int32_t chunks, chunk_len, keep, keep_last, kcap, merge_max;
+    size_t bytes;
+};
+TopkChunkPlan topk_chunk_plan(int32_t num_rows, int32_t max_ctx, int32_t k, int sms);
 
 struct SlotArgs {
     const int32_t *block_table;

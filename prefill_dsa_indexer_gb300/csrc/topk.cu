@@ -130,25 +130,55 @@ __device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.w
 struct Chunk {
     const float *src;
     int n, ncache;
+    bool vec;  // src is 16-byte aligned
     __device__ __forceinline__ uint32_t key(const TopkSmem &s, int i) const {
         bool nan = false;
         return i < ncache ? s.cache[i] : f2key(src[i], nan);
     }
 };
 
-// Keys i .. i+3 of the chunk (i a multiple of 4); positions >= lim read as 0 and are
-// flagged out of range.
-__device__ __forceinline__ void keys4(const TopkSmem &s, const Chunk &c, int i, int lim, uint32_t (&k)[4]) {
+// Keys i .. i+3 of the chunk (i a multiple of 4), in two steps so that a loop can start the next
+// step's loads before it uses the current keys: keys4_load issues the reads (shared memory, or
+// the raw fp32 logits of the part of a long chunk beyond the shared-memory copy: `raw`), and
+// keys4_finish turns raw logits into keys.  Positions >= lim read as key 0.
+__device__ __forceinline__ void keys4_load(const TopkSmem &s, const Chunk &c, int i, int lim, uint32_t (&k)[4],
+                                           bool &raw) {
+    raw = false;
     if (i + 3 < c.ncache && i + 3 < lim) {
         const uint4 v = *reinterpret_cast<const uint4 *>(&s.cache[i]);
         k[0] = v.x;
         k[1] = v.y;
         k[2] = v.z;
         k[3] = v.w;
-    } else {
+    } else if (i >= c.ncache) {
+        raw = true;
+        if (c.vec && i + 3 < lim) {
+            const int4 v = ldg_nc_v4(c.src + i);
+            k[0] = static_cast<uint32_t>(v.x);
+            k[1] = static_cast<uint32_t>(v.y);
+            k[2] = static_cast<uint32_t>(v.z);
+            k[3] = static_cast<uint32_t>(v.w);
+        } else {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) k[q] = (i + q < lim) ? __float_as_uint(__ldg(c.src + i + q)) : 0u;
+        }
+    } else {  // straddles the end of the shared-memory copy
 #pragma unroll
         for (int q = 0; q < 4; ++q) k[q] = (i + q < lim) ? c.key(s, i + q) : 0u;
     }
+}
+
+__device__ __forceinline__ void keys4_finish(uint32_t (&k)[4], bool raw, int i, int lim) {
+    if (!raw) return;
+    bool nan = false;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) k[q] = (i + q < lim) ? f2key(__uint_as_float(k[q]), nan) : 0u;
+}
+
+__device__ __forceinline__ void keys4(const TopkSmem &s, const Chunk &c, int i, int lim, uint32_t (&k)[4]) {
+    bool raw;
+    keys4_load(s, c, i, lim, k, raw);
+    keys4_finish(k, raw, i, lim);
 }
 
 // First pass: reads every key of the chunk (16-byte loads, four per thread in
@@ -198,7 +228,23 @@ __device__ __forceinline__ void each_key(const TopkSmem &s, const Chunk &c, F &&
         f(k4.z);
         f(k4.w);
     }
-    for (int i = nc4 + threadIdx.x; i < c.n; i += kThreads) f(c.key(s, i));
+    // the part beyond the shared-memory copy: eight loads per thread in flight before any use
+    for (int i0 = nc4; i0 < c.n; i0 += 8 * kThreads) {
+        float v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int i = i0 + u * kThreads + threadIdx.x;
+            v[u] = i < c.n ? (i < c.ncache ? 0.f : __ldg(c.src + i)) : 0.f;
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int i = i0 + u * kThreads + threadIdx.x;
+            if (i < c.n) {
+                bool nan = false;
+                f(i < c.ncache ? s.cache[i] : f2key(v[u], nan));
+            }
+        }
+    }
 }
 
 // Finds the bin holding the need-th largest key, scanning bins from the top.
@@ -300,7 +346,8 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const TopkArgs a) {
     const int ch = ((n + CL - 1) / CL + 3) & ~3;
     const int c0 = min(n, crank * ch);
     const int nloc = min(n, c0 + ch) - c0;
-    Chunk chunk{a.logits + static_cast<int64_t>(row) * a.logits_stride + c0, nloc, min(nloc, kCacheElems)};
+    const float *csrc = a.logits + static_cast<int64_t>(row) * a.logits_stride + c0;
+    Chunk chunk{csrc, nloc, min(nloc, kCacheElems), (reinterpret_cast<uintptr_t>(csrc) & 15) == 0};
     if (tid == 0) {
         s.bad = 0;
         s.ncand = 0;
@@ -559,8 +606,8 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const TopkArgs a) {
         if (CL > 1) {
             cluster.sync();  // every chunk's histogram is complete
             // reduce-scatter: this CTA sums bin slice `crank` over the cluster, writes it to all
-            const int slice = kBins / CL;
-            if (tid < slice) {
+            const int slice = (kBins + CL - 1) / CL;
+            if (tid < slice && crank * slice + tid < kBins) {
                 const int b = crank * slice + tid;
                 uint32_t v[kMaxCluster];
 #pragma unroll
@@ -591,10 +638,15 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const TopkArgs a) {
         if (top > base && sc <= static_cast<uint32_t>(kCandCap)) {
             // publish this chunk's keys inside [base, top] (one shared atomic per warp) and its
             // count above, then gather every CTA's share in rank order
+            uint32_t nk[4];
+            bool nraw;
+            keys4_load(s, chunk, 4 * tid, nloc, nk, nraw);
             for (int i0 = 0; i0 < nloc; i0 += 4 * kThreads) {
                 const int i = i0 + 4 * tid;
-                uint32_t kq[4];
-                keys4(s, chunk, i, nloc, kq);
+                uint32_t kq[4] = {nk[0], nk[1], nk[2], nk[3]};
+                const bool raw = nraw;
+                if (i0 + 4 * kThreads < nloc) keys4_load(s, chunk, i + 4 * kThreads, nloc, nk, nraw);
+                keys4_finish(kq, raw, i, nloc);
                 uint32_t c = 0;
 #pragma unroll
                 for (int q = 0; q < 4; ++q) c += (i + q < nloc && kq[q] >= base && kq[q] <= top) ? 1u : 0u;
@@ -737,10 +789,15 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const TopkArgs a) {
         // has read its keys before the scan that places the writes).  Then each warp walks
         // its short list and keeps the keys > T and the first `need` keys == T of the row.
         uint32_t ns = 0, ngt = 0, neq = 0;
+        uint32_t nk[4];
+        bool nraw;
+        keys4_load(s, chunk, w0 + 4 * lane, w1, nk, nraw);
         for (int i0 = w0; i0 < w1; i0 += 128) {
             const int i = i0 + 4 * lane;
-            uint32_t kq[4];
-            keys4(s, chunk, i, w1, kq);
+            uint32_t kq[4] = {nk[0], nk[1], nk[2], nk[3]};
+            const bool raw = nraw;
+            if (i0 + 128 < w1) keys4_load(s, chunk, i + 128, w1, nk, nraw);
+            keys4_finish(kq, raw, i, w1);
             uint32_t g = 0, e = 0;
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
@@ -795,10 +852,15 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const TopkArgs a) {
         // Chunk larger than the shared-memory copy: pass 1 counts keys > T and == T per warp,
         // pass 2 places each selected position after the lower warps' and chunks' selections.
         uint32_t ngt = 0, neq = 0;
+        uint32_t nk[4];
+        bool nraw;
+        keys4_load(s, chunk, w0 + 4 * lane, w1, nk, nraw);
         for (int i0 = w0; i0 < w1; i0 += 128) {
             const int i = i0 + 4 * lane;
-            uint32_t kq[4];
-            keys4(s, chunk, i, w1, kq);
+            uint32_t kq[4] = {nk[0], nk[1], nk[2], nk[3]};
+            const bool raw = nraw;
+            if (i0 + 128 < w1) keys4_load(s, chunk, i + 128, w1, nk, nraw);
+            keys4_finish(kq, raw, i, w1);
             uint32_t g = 0, e = 0;
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
@@ -822,10 +884,13 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const TopkArgs a) {
             gt_before += __shfl_sync(0xffffffffu, ig - vg, warp);
             eq_before += __shfl_sync(0xffffffffu, ie - ve, warp);
         }
+        keys4_load(s, chunk, w0 + 4 * lane, w1, nk, nraw);
         for (int i0 = w0; i0 < w1; i0 += 128) {
             const int i = i0 + 4 * lane;
-            uint32_t kq[4];
-            keys4(s, chunk, i, w1, kq);
+            uint32_t kq[4] = {nk[0], nk[1], nk[2], nk[3]};
+            const bool raw = nraw;
+            if (i0 + 128 < w1) keys4_load(s, chunk, i + 128, w1, nk, nraw);
+            keys4_finish(kq, raw, i, w1);
             uint32_t g = 0, e = 0;
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
@@ -872,16 +937,24 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const TopkArgs a) {
 
 struct ClusterLimits {
     int device = -1;
-    int max16 = 0;  // co-resident clusters of 16 (0: not available)
+    int max_clusters[kMaxCluster + 1] = {0};  // co-resident clusters of each size (0: not launchable)
 };
 
-int cluster_size_for(const TopkArgs &a, int sms, int max16) {
-    int cl = 1;  // enough CTAs that a chunk fits the shared-memory copy
-    while (cl < kMaxCluster && (a.max_ctx + cl - 1) / cl > kCacheElems) cl *= 2;
-    int par = 1;  // enough CTAs that the batch covers the SMs, chunks not shorter than kMinChunk
-    while (par < kMaxCluster && 2 * par * a.num_rows <= sms && a.max_ctx / (2 * par) >= kMinChunk) par *= 2;
-    cl = max(cl, par);
-    if (cl == 16 && max16 < a.num_rows) cl = 8;  // clusters of 16 would not all be co-resident
+// CTAs per row: at least enough that a chunk fits the shared-memory copy, as many as keep the
+// batch within the SMs (chunks not shorter than kMinChunk), and no more than the GPU holds
+// `num_rows` co-resident clusters of (a second wave would double the time).  The histogram-seeded
+// variant splits the 65,536 scorer bins evenly over the cluster: powers of two only.
+int cluster_size_for(const TopkArgs &a, int sms, const ClusterLimits &lim, bool pow2_only) {
+    int fit = 1;
+    while (fit < kMaxCluster && (a.max_ctx + fit - 1) / fit > kCacheElems) fit = pow2_only ? 2 * fit : fit + 1;
+    int par = 1;
+    while (true) {
+        const int nxt = pow2_only ? 2 * par : par + 1;
+        if (nxt > kMaxCluster || nxt * a.num_rows > sms || a.max_ctx / nxt < kMinChunk) break;
+        par = nxt;
+    }
+    int cl = fit > par ? fit : par;
+    while (cl > 1 && lim.max_clusters[cl] < a.num_rows) cl = pow2_only ? cl / 2 : cl - 1;
     return cl;
 }
 
@@ -894,27 +967,29 @@ cudaError_t launch_variant(const TopkArgs &a, cudaStream_t s) {
     if (lim.device != dev) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, sizeof(TopkSmem));
         if (e != cudaSuccess) return e;
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-        int max16 = 0;
-        if (e == cudaSuccess) {
+        const bool nonportable = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
+                                 cudaSuccess;
+        for (int c = 1; c <= kMaxCluster; ++c) {
+            lim.max_clusters[c] = 0;
+            if (c > 8 && !nonportable) continue;
             cudaLaunchConfig_t probe = {};
-            probe.gridDim = dim3(16);
+            probe.gridDim = dim3(c);
             probe.blockDim = dim3(kThreads);
             probe.dynamicSmemBytes = sizeof(TopkSmem);
             cudaLaunchAttribute at[1];
             at[0].id = cudaLaunchAttributeClusterDimension;
-            at[0].val.clusterDim.x = 16;
+            at[0].val.clusterDim.x = c;
             at[0].val.clusterDim.y = 1;
             at[0].val.clusterDim.z = 1;
             probe.attrs = at;
             probe.numAttrs = 1;
-            if (cudaOccupancyMaxActiveClusters(&max16, kern, &probe) != cudaSuccess) max16 = 0;
+            int n = 0;
+            if (cudaOccupancyMaxActiveClusters(&n, kern, &probe) == cudaSuccess) lim.max_clusters[c] = n;
         }
         cudaGetLastError();  // a refused cluster size only disables it
-        lim.max16 = max16;
         lim.device = dev;
     }
-    const int cl = cluster_size_for(a, device_sm_count(), lim.max16);
+    const int cl = cluster_size_for(a, device_sm_count(), lim, kHist);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(a.num_rows * cl));
     cfg.blockDim = dim3(kThreads);
@@ -932,10 +1007,449 @@ cudaError_t launch_variant(const TopkArgs &a, cudaStream_t s) {
     return cudaLaunchKernelEx(&cfg, kern, a);
 }
 
+// ---------------------------------------------------------------- two-phase selection
+//
+// For a few long rows (decode), with a caller workspace: phase A cuts each row into chunks that
+// independent CTAs (no clusters, several per SM) reduce to their own exact top candidates, in
+// position order; phase B merges each row's candidates in one CTA.  The candidates of every chunk
+// are the chunk's best `keep` keys by (key desc, position asc) (up to k for the chunk holding the
+// row's most recent tokens), so the row's selection equals the candidates' selection unless a chunk
+// that dropped keys kept a threshold key at or above the merged threshold T: such a chunk may hold
+// more selected keys than it passed on.  Phase B checks this for every chunk and, when it happens
+// (concentrated or heavily tied scores), selects from the whole row's logits itself (slower, exact).
+
+constexpr int kAThreads = 512;
+constexpr int kBThreads = 1024;
+
+// Block-wide: the bin holding the need-th largest key of `hist` (kBins counts, scanned from the
+// top): res[0] = bin, res[1] = keys above it, res[2] = keys in it.
+template <int NT>
+__device__ void find_bin(const uint32_t *hist, uint32_t need, uint32_t *wred, uint32_t *res) {
+    constexpr int per = kBins / NT;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int b_hi = kBins - 1 - per * tid;  // this thread: bins b_hi, b_hi - 1, ..., b_hi - per + 1
+    uint32_t c[per], tsum = 0;
+#pragma unroll
+    for (int q = 0; q < per; ++q) {
+        c[q] = hist[b_hi - q];
+        tsum += c[q];
+    }
+    const uint32_t incl = warp_incl_scan32(tsum, lane);
+    if (lane == 31) wred[warp] = incl;
+    __syncthreads();
+    const uint32_t wincl = warp_incl_scan32(lane < NT / 32 ? wred[lane] : 0u, lane);
+    const uint32_t wex = warp == 0 ? 0u : __shfl_sync(0xffffffffu, wincl, (warp + 31) & 31);
+    const uint32_t above = wex + incl - tsum;
+    if (above < need && need <= above + tsum) {
+        uint32_t acc = above;
+#pragma unroll
+        for (int q = 0; q < per; ++q) {
+            if (acc < need && need <= acc + c[q]) {
+                res[0] = static_cast<uint32_t>(b_hi - q);
+                res[1] = acc;
+                res[2] = c[q];
+            }
+            acc += c[q];
+        }
+    }
+    __syncthreads();
+}
+
+// The need-th largest of items 0 .. n-1 (their keys from key_at, all within [lo, hi]), exactly:
+// T and need_eq = how many items with key T the selection takes (it takes every key above T).
+template <int NT, typename KeyAt>
+__device__ void find_threshold(int n, KeyAt key_at, uint32_t lo, uint32_t hi, uint32_t need, uint32_t *hist,
+                               uint32_t *wred, uint32_t *res, uint32_t &T, uint32_t &need_eq) {
+    uint32_t base = lo, top = hi;
+    while (top > base) {
+        const uint32_t span = top - base;
+        const int bits = 32 - __clz(span);
+        const int shift = bits > 11 ? bits - 11 : 0;  // (span >> shift) < 2048 bins
+        for (int b = threadIdx.x; b < kBins; b += NT) hist[b] = 0u;
+        __syncthreads();
+        for (int i = threadIdx.x; i < n; i += NT) {
+            const uint32_t key = key_at(i);
+            if (key >= base && key <= top) atomicAdd(&hist[(key - base) >> shift], 1u);
+        }
+        __syncthreads();
+        find_bin<NT>(hist, need, wred, res);
+        need -= res[1];
+        const uint32_t nbase = base + (res[0] << shift);
+        const unsigned long long bin_top = static_cast<unsigned long long>(nbase) + (1ull << shift) - 1ull;
+        base = nbase;
+        top = static_cast<uint32_t>(min(static_cast<unsigned long long>(top), bin_top));
+        __syncthreads();  // res is rewritten by the next round
+    }
+    T = base;
+    need_eq = need;
+}
+
+// Calls emit(j, i), in item order, for every item whose key is above T and for the first need_eq
+// items whose key equals T; j is the item's rank among the emitted ones (its output index).
+// Warps own contiguous item segments: one pass counts, the second places.
+template <int NT, typename KeyAt, typename Emit>
+__device__ void emit_ordered(int n, KeyAt key_at, uint32_t T, uint32_t need_eq, uint32_t *wgt, uint32_t *weq,
+                             Emit emit) {
+    constexpr int NW = NT / 32;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int seg = (((n + NW - 1) / NW) + 31) & ~31;
+    const int w0 = min(n, warp * seg), w1 = min(n, w0 + seg);
+    uint32_t g = 0, e = 0;
+    for (int i0 = w0; i0 < w1; i0 += 32) {
+        const int i = i0 + lane;
+        const uint32_t key = i < w1 ? key_at(i) : 0u;
+        g += __popc(__ballot_sync(0xffffffffu, i < w1 && key > T));
+        e += __popc(__ballot_sync(0xffffffffu, i < w1 && key == T));
+    }
+    if (lane == 0) {
+        wgt[warp] = g;
+        weq[warp] = e;
+    }
+    __syncthreads();
+    uint32_t gb = 0, eb = 0;  // the lower warps' counts
+    for (int w = 0; w < warp; ++w) {
+        gb += wgt[w];
+        eb += weq[w];
+    }
+    const unsigned lt = (1u << lane) - 1u;
+    for (int i0 = w0; i0 < w1; i0 += 32) {
+        const int i = i0 + lane;
+        const uint32_t key = i < w1 ? key_at(i) : 0u;
+        const bool is_gt = i < w1 && key > T, is_eq = i < w1 && key == T;
+        const unsigned bg = __ballot_sync(0xffffffffu, is_gt), be = __ballot_sync(0xffffffffu, is_eq);
+        const uint32_t eq_rank = eb + __popc(be & lt);
+        if (is_gt || (is_eq && eq_rank < need_eq)) emit(gb + __popc(bg & lt) + min(eq_rank, need_eq), i);
+        gb += __popc(bg);
+        eb += __popc(be);
+    }
+    __syncthreads();
+}
+
+// Block-wide min and max of (lo, hi) over the threads, into res[0], res[1].
+template <int NT>
+__device__ void block_minmax(uint32_t lo, uint32_t hi, uint32_t *wred, uint32_t *res) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+        hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+    }
+    if (lane == 0) {
+        wred[warp] = lo;
+        wred[32 + warp] = hi;
+    }
+    __syncthreads();
+    if (warp == 0) {
+        lo = lane < NT / 32 ? wred[lane] : 0xffffffffu;
+        hi = lane < NT / 32 ? wred[32 + lane] : 0u;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+            hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+        }
+        if (lane == 0) {
+            res[0] = lo;
+            res[1] = hi;
+        }
+    }
+    __syncthreads();
+}
+
+// Candidates chunk c of a row of L keys passes on: twice its share of k plus a margin (the row's
+// own chunk count sets the share), up to k for the chunk of the most recent tokens; at most kcap.
+__device__ __forceinline__ int chunk_keep(const TopkArgs &a, int L, int c) {
+    const int nch = (L + a.chunk_len - 1) / a.chunk_len;
+    int kp = (c == nch - 1) ? a.k : ((2 * a.k + nch - 1) / nch + 64 + 31) / 32 * 32;
+    kp = min(kp, a.k);
+    kp = min(kp, a.chunk_len);
+    return min(kp, a.kcap);
+}
+
+// Phase A: CTA (row, c) writes chunk c's best keys (all of them if the chunk has no more than its
+// keep) with their positions, in position order, and meta = {count, threshold key, complete}.
+__global__ void __launch_bounds__(kAThreads, 2) topk_chunk_kernel(const TopkArgs a) {
+    extern __shared__ uint32_t ka_smem[];
+    uint32_t *keys = ka_smem;                 // [chunk_len]
+    uint32_t *hist = keys + a.chunk_len;      // [kBins]
+    uint32_t *wred = hist + kBins;            // [64]
+    uint32_t *wgt = wred + 64, *weq = wgt + 32, *res = weq + 32;
+    pdl_launch_dependents();
+    pdl_wait();
+    const int row = blockIdx.x / a.chunks, c = blockIdx.x % a.chunks;
+    const int L = min(max(a.row_ctx[row], 0), a.max_ctx);
+    if (L <= a.k) return;  // phase B writes such rows whole
+    const int c0 = c * a.chunk_len;
+    const int n = max(0, min(L, c0 + a.chunk_len) - c0);
+    const int kp = chunk_keep(a, L, c);
+    const int64_t slot = static_cast<int64_t>(row) * a.chunks + c;
+    uint32_t *ck = a.cand_key + slot * a.kcap;
+    int32_t *cp = a.cand_pos + slot * a.kcap;
+    uint32_t *meta = a.cand_meta + slot * 4;
+    const float *src = a.logits + static_cast<int64_t>(row) * a.logits_stride + c0;
+    bool nan = false;
+    uint32_t lo = 0xffffffffu, hi = 0u;
+    for (int i0 = 0; i0 < n; i0 += 8 * kAThreads) {  // eight loads per thread in flight
+        float v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int i = i0 + u * kAThreads + threadIdx.x;
+            v[u] = i < n ? __ldg(src + i) : 0.f;
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int i = i0 + u * kAThreads + threadIdx.x;
+            if (i < n) {
+                const uint32_t key = f2key(v[u], nan);
+                keys[i] = key;
+                lo = min(lo, key);
+                hi = max(hi, key);
+            }
+        }
+    }
+    if (nan) report(a.status, DSA_ERR_RANGE);
+    block_minmax<kAThreads>(lo, hi, wred, res);
+    lo = res[0];
+    hi = res[1];
+    __syncthreads();
+    if (n <= kp) {  // the whole chunk is a candidate
+        for (int i = threadIdx.x; i < n; i += kAThreads) {
+            ck[i] = keys[i];
+            cp[i] = c0 + i;
+        }
+        if (threadIdx.x == 0) {
+            meta[0] = static_cast<uint32_t>(n);
+            meta[1] = 0u;
+            meta[2] = 1u;
+        }
+        return;
+    }
+    uint32_t T, need_eq;
+    auto key_at = [&](int i) { return keys[i]; };
+    find_threshold<kAThreads>(n, key_at, lo, hi, static_cast<uint32_t>(kp), hist, wred, res, T, need_eq);
+    emit_ordered<kAThreads>(n, key_at, T, need_eq, wgt, weq, [&](uint32_t j, int i) {
+        if (j < static_cast<uint32_t>(kp)) {
+            ck[j] = keys[i];
+            cp[j] = c0 + i;
+        }
+    });
+    if (threadIdx.x == 0) {
+        meta[0] = static_cast<uint32_t>(kp);
+        meta[1] = T;
+        meta[2] = 0u;
+    }
+}
+
+// Phase B: one CTA per row merges the chunks' candidates (they lie in position order, so candidate
+// order breaks ties like position order), checks that no chunk may hold more, and writes the row's
+// selection (ascending positions), its slots and the latent prefetches.
+template <bool kSlots>
+__global__ void __launch_bounds__(kBThreads, 1) topk_merge_kernel(const TopkArgs a) {
+    extern __shared__ uint32_t kb_smem[];
+    uint32_t *mkey = kb_smem;                                         // [merge_max]
+    int32_t *mpos = reinterpret_cast<int32_t *>(mkey + a.merge_max);  // [merge_max]
+    uint32_t *hist = reinterpret_cast<uint32_t *>(mpos + a.merge_max);
+    uint32_t *wred = hist + kBins, *wgt = wred + 64, *weq = wgt + 32, *res = weq + 32;
+    uint32_t *coff = res + 8;  // [chunks + 1] candidate offsets of the row's chunks
+    pdl_launch_dependents();
+    pdl_wait();
+    const int tid = threadIdx.x, lane = tid & 31;
+    const int row = blockIdx.x, k = a.k;
+    int32_t *out = a.idx_out + static_cast<int64_t>(row) * k;
+    int32_t *sout = kSlots ? a.slots_out + static_cast<int64_t>(row) * k : nullptr;
+    const int32_t *bt_row = nullptr;
+    if constexpr (kSlots) {
+        const int32_t req = a.row_req[row];
+        if (req >= 0 && req < a.num_requests) bt_row = a.block_table + static_cast<int64_t>(req) * a.bt_stride;
+    }
+    // the selection is staged in shared memory, then written with its slots by every thread at once
+    // (the block-table reads of the slots all in flight together)
+    int32_t *sel = reinterpret_cast<int32_t *>(coff + a.chunks + 1);  // [k]
+    auto put = [&](uint32_t j, int32_t t) {
+        if (j < static_cast<uint32_t>(k)) sel[j] = t;
+    };
+    auto write_out = [&]() {
+        __syncthreads();
+        for (int j = tid; j < k; j += kBThreads) {
+            const int32_t t = sel[j];
+            out[j] = t;
+            if constexpr (kSlots) {
+                const int32_t sl = t >= 0 ? slot_of(a, bt_row, nullptr, 0, 0, t) : -1;
+                sout[j] = sl;
+                if (a.warm_pool != nullptr && sl >= 0)
+                    bulk_prefetch_l2(a.warm_pool + static_cast<int64_t>(sl) * DSA_LATENT_DIM, DSA_LATENT_DIM);
+            }
+        }
+    };
+    int n = a.row_ctx[row];
+    if (n < 0 || n > a.max_ctx) {
+        if (tid == 0) report(a.status, DSA_ERR_BOUNDS);
+        n = min(max(n, 0), a.max_ctx);
+    }
+    if (n <= k) {
+        for (int i = tid; i < k; i += kBThreads) put(static_cast<uint32_t>(i), i < n ? i : -1);
+        write_out();
+        return;
+    }
+    const int nch = (n + a.chunk_len - 1) / a.chunk_len;
+    const uint32_t *meta = a.cand_meta + static_cast<int64_t>(row) * a.chunks * 4;
+    if (tid < 32) {  // offsets of each chunk's candidates
+        uint32_t carry = 0;
+        for (int c0 = 0; c0 < nch; c0 += 32) {
+            const int c = c0 + lane;
+            const uint32_t cnt = c < nch ? min(meta[c * 4], static_cast<uint32_t>(a.kcap)) : 0u;
+            const uint32_t incl = warp_incl_scan32(cnt, lane);
+            if (c < nch) coff[c] = carry + incl - cnt;
+            carry += __shfl_sync(0xffffffffu, incl, 31);
+        }
+        if (lane == 0) coff[nch] = carry;
+    }
+    __syncthreads();
+    const int M = static_cast<int>(min(coff[nch], static_cast<uint32_t>(a.merge_max)));
+    uint32_t lo = 0xffffffffu, hi = 0u;
+    constexpr int kIn = 8;  // candidate loads per thread in flight
+    for (int j0 = 0; j0 < M; j0 += kIn * kBThreads) {
+        uint32_t kv[kIn];
+        int32_t pv[kIn];
+#pragma unroll
+        for (int u = 0; u < kIn; ++u) {
+            const int j = j0 + u * kBThreads + tid;
+            kv[u] = 0u;
+            pv[u] = 0;
+            if (j < M) {
+                // the chunk holding candidate j (coff[c] <= j < coff[c + 1]): a fixed-depth branch-free
+                // search, so the loads of all kIn candidates are issued before any is used
+                int c = 0;
+#pragma unroll
+                for (int step = 512; step > 0; step >>= 1)
+                    if (c + step < nch && coff[c + step] <= static_cast<uint32_t>(j)) c += step;
+                const int64_t at = (static_cast<int64_t>(row) * a.chunks + c) * a.kcap + (j - coff[c]);
+                kv[u] = __ldg(a.cand_key + at);
+                pv[u] = __ldg(a.cand_pos + at);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kIn; ++u) {
+            const int j = j0 + u * kBThreads + tid;
+            if (j < M) {
+                mkey[j] = kv[u];
+                mpos[j] = pv[u];
+                lo = min(lo, kv[u]);
+                hi = max(hi, kv[u]);
+            }
+        }
+    }
+    block_minmax<kBThreads>(lo, hi, wred, res);
+    lo = res[0];
+    hi = res[1];
+    uint32_t T = 0, need_eq = 0;
+    bool exact = M >= k && coff[nch] <= static_cast<uint32_t>(a.merge_max);
+    __syncthreads();
+    if (exact) {
+        find_threshold<kBThreads>(M, [&](int i) { return mkey[i]; }, lo, hi, static_cast<uint32_t>(k), hist, wred,
+                                  res, T, need_eq);
+        // a chunk that dropped keys below a threshold key not under T may hold more selected keys
+        bool more = false;
+        for (int c = tid; c < nch; c += kBThreads) more |= meta[c * 4 + 2] == 0u && meta[c * 4 + 1] >= T;
+        exact = !__syncthreads_or(more);
+    }
+    if (exact) {
+        emit_ordered<kBThreads>(M, [&](int i) { return mkey[i]; }, T, need_eq, wgt, weq,
+                                [&](uint32_t j, int i) { put(j, mpos[i]); });
+        write_out();
+        return;
+    }
+    // the candidates may miss selected keys: select from the whole row's logits
+    const float *src = a.logits + static_cast<int64_t>(row) * a.logits_stride;
+    auto gkey = [&](int i) {
+        bool nan = false;
+        return f2key(__ldg(src + i), nan);
+    };
+    lo = 0xffffffffu;
+    hi = 0u;
+    for (int i = tid; i < n; i += kBThreads) {
+        const uint32_t key = gkey(i);
+        lo = min(lo, key);
+        hi = max(hi, key);
+    }
+    block_minmax<kBThreads>(lo, hi, wred, res);
+    lo = res[0];
+    hi = res[1];
+    __syncthreads();
+    find_threshold<kBThreads>(n, gkey, lo, hi, static_cast<uint32_t>(k), hist, wred, res, T, need_eq);
+    emit_ordered<kBThreads>(n, gkey, T, need_eq, wgt, weq, [&](uint32_t j, int i) { put(j, i); });
+    write_out();
+}
+
+}  // namespace
+
+TopkChunkPlan topk_chunk_plan(int32_t num_rows, int32_t max_ctx, int32_t k, int sms) {
+    TopkChunkPlan p{};
+    if (num_rows <= 0 || num_rows > kChunkedMaxRows || max_ctx <= kChunkedMinCtx || k < 1 || k > DSA_MAX_TOPK ||
+        sms <= 0)
+        return p;
+    // chunks per row: about two CTAs per SM over the batch, chunks of at most kChunkMaxKeys keys
+    int C = (2 * sms + num_rows - 1) / num_rows;
+    C = C < kChunkedMaxChunks ? C : kChunkedMaxChunks;  // the merge of few rows stays within shared memory
+    const int by_len = (max_ctx + kChunkMaxKeys - 1) / kChunkMaxKeys;
+    C = C > by_len ? C : by_len;
+    int Lc = ((max_ctx + C - 1) / C + 63) / 64 * 64;
+    if (Lc < kChunkMinKeys) Lc = kChunkMinKeys;
+    C = (max_ctx + Lc - 1) / Lc;
+    // a row of nc chunks passes on at most (nc - 1) keep(nc) + k candidates (chunk_keep on the device),
+    // keep(nc) = min(k, Lc, round32(2k / nc + 64)); the merge holds the largest such total
+    const int kcap = k < Lc ? k : Lc;
+    int merge_max = 0;
+    for (int nc = 1; nc <= C; ++nc) {
+        int kp = ((2 * k + nc - 1) / nc + 64 + 31) / 32 * 32;
+        kp = kp < kcap ? kp : kcap;
+        const int tot = (nc - 1) * kp + kcap;
+        merge_max = tot > merge_max ? tot : merge_max;
+    }
+    if (merge_max > kMergeMaxKeys) return p;
+    p.chunks = C;
+    p.chunk_len = Lc;
+    p.keep = 0;  // per row: chunk_keep()
+    p.keep_last = kcap;
+    p.kcap = kcap;
+    p.merge_max = merge_max;
+    const size_t cand = static_cast<size_t>(num_rows) * C * p.kcap * 4;
+    p.bytes = align256(cand) * 2 + align256(static_cast<size_t>(num_rows) * C * 16);
+    return p;
+}
+
+namespace {
+
+template <bool kSlots>
+cudaError_t launch_two_phase(const TopkArgs &a, cudaStream_t s) {
+    static int configured_device = -1;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const size_t smem_a = (static_cast<size_t>(kChunkMaxKeys) + kBins + 64 + 32 + 32 + 8) * 4;
+    const size_t smem_b_max = (2 * static_cast<size_t>(kMergeMaxKeys) + kBins + 64 + 32 + 32 + 8 + 1024 +
+                               DSA_MAX_TOPK) * 4;
+    if (configured_device != dev) {
+        cudaError_t e = cudaFuncSetAttribute(topk_chunk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(smem_a));
+        if (e != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(topk_merge_kernel<kSlots>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(smem_b_max));
+        if (e != cudaSuccess) return e;
+        configured_device = dev;
+    }
+    const size_t sa = (static_cast<size_t>(a.chunk_len) + kBins + 64 + 32 + 32 + 8) * 4;
+    cudaError_t e = launch_pdl(topk_chunk_kernel, dim3(static_cast<unsigned>(a.num_rows * a.chunks)),
+                               dim3(kAThreads), sa, s, a);
+    if (e != cudaSuccess) return e;
+    const size_t sb = (2 * static_cast<size_t>(a.merge_max) + kBins + 64 + 32 + 32 + 8 + a.chunks + 1 + a.k) * 4;
+    return launch_pdl(topk_merge_kernel<kSlots>, dim3(static_cast<unsigned>(a.num_rows)), dim3(kBThreads), sb, s, a);
+}
+
 }  // namespace
 
 cudaError_t launch_topk(const TopkArgs &a, cudaStream_t s) {
     if (a.num_rows == 0) return cudaSuccess;
+    if (a.chunks > 0 && a.hist == nullptr)  // the caller planned the two-phase path
+        return a.slots_out != nullptr ? launch_two_phase<true>(a, s) : launch_two_phase<false>(a, s);
     const bool h = a.hist != nullptr, sl = a.slots_out != nullptr;
     if (h && sl) return launch_variant<true, true>(a, s);
     if (h) return launch_variant<true, false>(a, s);

@@ -67,12 +67,12 @@ def test_host_validation_rejects_before_launch(lib):
     import prefill_dsa_indexer_gb300 as P
     fake = ctypes.c_void_p(0x10000)
     # top-k: k outside [1, 2048]
-    assert lib.dsa_topk(fake, 4096, fake, 1, 4096, 0, fake, None, None) == P.ERR_UNSUPPORTED
-    assert lib.dsa_topk(fake, 4096, fake, 1, 4096, 4096, fake, None, None) == P.ERR_UNSUPPORTED
+    assert lib.dsa_topk(fake, 4096, fake, 1, 4096, 0, fake, None, None, 0, None) == P.ERR_UNSUPPORTED
+    assert lib.dsa_topk(fake, 4096, fake, 1, 4096, 4096, fake, None, None, 0, None) == P.ERR_UNSUPPORTED
     # top-k: logits stride shorter than max_ctx
-    assert lib.dsa_topk(fake, 100, fake, 1, 4096, 16, fake, None, None) == P.ERR_INVALID_ARG
+    assert lib.dsa_topk(fake, 100, fake, 1, 4096, 16, fake, None, None, 0, None) == P.ERR_INVALID_ARG
     # top-k: nothing to do
-    assert lib.dsa_topk(None, 0, None, 0, 0, 16, None, None, None) == P.OK
+    assert lib.dsa_topk(None, 0, None, 0, 0, 16, None, None, None, 0, None) == P.OK
     # indexer: unsupported page size, rows_per_group, bt too narrow, null cache
     c = P._Cache(fake, P.KEY_FP8, 32, 10, 1.0)
     r = P._Rows(fake, 1, 1, fake, fake, 1, 64, 1)
@@ -161,6 +161,11 @@ def test_host_validation_of_the_msa_insert_and_warm_calls(lib):
     assert lib.dsa_cache_insert(ctypes.byref(ic), ctypes.byref(lc), fake, 0, fake, fake, None, None) == P.OK
     # warm top-k: needs the latent pool, and only FP8 / NVFP4 latent formats
     r = rows(1, 4096, 64)
-    assert lib.dsa_topk_slots_warm(fake, 4096, ctypes.byref(r), None, 16, fake, fake, None, None) == P.ERR_INVALID_ARG
+    assert lib.dsa_topk_slots_warm(fake, 4096, ctypes.byref(r), None, 16, fake, fake, None, None, 0,
+                                   None) == P.ERR_INVALID_ARG
     assert lib.dsa_topk_slots_warm(fake, 4096, ctypes.byref(r), ctypes.byref(P._Cache(fake, 9, 64, 10, 0.01)), 16,
-                                   fake, fake, None, None) == P.ERR_UNSUPPORTED
+                                   fake, fake, None, None, 0, None) == P.ERR_UNSUPPORTED
+    # the two-phase top-k's workspace: none for short rows or many rows (or without a device)
+    assert lib.dsa_topk_workspace_size(8, 8192, 2048) == 0
+    assert lib.dsa_topk_workspace_size(65, 131072, 2048) == 0
+    assert lib.dsa_topk_workspace_size(0, 131072, 2048) == 0

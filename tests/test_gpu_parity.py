@@ -158,6 +158,10 @@ def _topk_cases():
     tp[:, rng.choice(100000, 1500, replace=False)] = 2.0
     tp[0, rng.choice(100000, 1000, replace=False)] = 3.0
     cases["ties_many_candidates"] = (tp, np.array([100000, 99999], dtype=np.int32), 2048)
+    # 12 rows of 150K keys: the co-residency check picks a cluster size that need not be a power of
+    # two, so the reduce-scatter's bin slices do not divide the histogram evenly
+    mid = rng.standard_normal((12, 150000)).astype(np.float32)
+    cases["twelve_rows_150k"] = (mid, np.array([150000 - 977 * i for i in range(12)], dtype=np.int32), 2048)
     s = rng.standard_normal((3, 3000)).astype(np.float32)
     cases["small_k"] = (s, np.array([3000, 10, 1], dtype=np.int32), 5)
     w = np.concatenate([np.full((1, 3000), 1e30, np.float32), np.full((1, 3000), -1e30, np.float32)])
@@ -178,6 +182,55 @@ def test_topk_bit_exact(case):
     P.check_status(st)
     ref = oracle.topk_f32(v, ctx, k)
     assert np.array_equal(got.cpu().numpy(), ref)
+
+
+def _two_phase_cases():
+    """Rows long enough for the two-phase top-k (a workspace is given): plain, tied and concentrated
+    scores, so both the merge and the whole-row fallback are exercised."""
+    rng = np.random.default_rng(17)
+    cases = {}
+    n = 300000  # longer than 256K keys: the two-phase path
+    v = rng.standard_normal((4, n)).astype(np.float32)
+    cases["normal_4x300k"] = (v, np.array([n - 4099 * i for i in range(4)], dtype=np.int32), 2048)
+    t = (rng.integers(0, 40, (3, n)) / 8).astype(np.float32)  # ties at the threshold across chunks
+    cases["ties"] = (t, np.array([n, 270000, 45000], dtype=np.int32), 2048)
+    c = rng.standard_normal((3, n)).astype(np.float32)
+    c[0, 10000:13000] += 50.0  # the whole selection inside one early chunk: it cannot pass it all on
+    c[1, n - 3000:] += 50.0  # inside the chunk of the most recent tokens
+    c[2, ::97] += 50.0  # spread evenly
+    cases["concentrated"] = (c, np.array([n, n, n], dtype=np.int32), 2048)
+    z = np.zeros((2, n), dtype=np.float32)
+    z[1, ::3] = -0.0
+    cases["all_equal"] = (z, np.array([n, n - 1], dtype=np.int32), 2048)
+    m = rng.standard_normal((5, n)).astype(np.float32)
+    cases["short_and_long"] = (m, np.array([n, 100, 2048, 2049, 33333], dtype=np.int32), 2048)
+    w = rng.standard_normal((4, n)).astype(np.float32)
+    cases["long_k100"] = (w, np.array([n, n - 1, 150000, 80000], dtype=np.int32), 100)
+    return cases
+
+
+TWO_PHASE_CASES = _two_phase_cases()
+
+
+@pytest.mark.parametrize("case", sorted(TWO_PHASE_CASES))
+def test_topk_two_phase_bit_exact(case):
+    v, ctx, k = TWO_PHASE_CASES[case]
+    R, width = v.shape
+    need = P.topk_workspace_size(R, width, k)
+    assert need > 0  # these shapes take the two-phase path
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    st = P.new_status()
+    got = P.topk(torch.from_numpy(v).cuda(), torch.from_numpy(ctx).cuda(), width, k, status=st, workspace=ws)
+    torch.cuda.synchronize()
+    P.check_status(st)
+    assert np.array_equal(got.cpu().numpy(), oracle.topk_f32(v, ctx, k))
+
+
+def test_topk_two_phase_rejects_a_small_workspace():
+    v, ctx, k = TWO_PHASE_CASES["normal_4x300k"]
+    ws = torch.empty(P.topk_workspace_size(v.shape[0], v.shape[1], k) - 256, dtype=torch.uint8, device="cuda")
+    with pytest.raises(P.DsaError, match="workspace"):
+        P.topk(torch.from_numpy(v).cuda(), torch.from_numpy(ctx).cuda(), v.shape[1], k, workspace=ws)
 
 
 def test_topk_on_indexer_logits_bit_exact():
