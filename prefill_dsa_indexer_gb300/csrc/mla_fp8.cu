@@ -111,8 +111,8 @@ __device__ __forceinline__ void cp_async_wait() {
 // ---------------------------------------------------------------- query preparation
 // One warp per (row, head): the head's 576 bf16 values become hi + lo e4m3 at 2^e_h, written as
 // the kernel's 128-byte-swizzled K-major operand blocks, plus 2^-e_h after the image.  A warp
-// takes kQprepHeads heads, so the kernel occupies few SMs (it runs beside the top-k).
-constexpr int kQprepHeads = 4;
+// takes kQprepHeads heads (more heads per warp occupy fewer SMs but take proportionally longer).
+constexpr int kQprepHeads = 1;
 __device__ __forceinline__ void qprep_head(const MlaArgs &a, int64_t w, int lane);
 __global__ void __launch_bounds__(256) mla_qprep_fp8_kernel(const MlaArgs a) {
     pdl_launch_dependents();
