@@ -83,7 +83,8 @@ extern "C" {
 
 /* One paged cache pool (index keys or latents). */
 typedef struct dsa_cache {
-    const void *base;     /* device, num_pages * page bytes, 16-byte aligned */
+    const void *base;     /* device, num_pages * page bytes, 16-byte aligned (DSA_KEY_MXFP4: 32-byte
+                             aligned, the rule of the 4-bit tensor copies; else DSA_ERR_INVALID_ARG) */
     int32_t format;       /* DSA_KEY_* for an index pool, DSA_LATENT_* for a latent pool */
     int32_t page_size;    /* must be DSA_PAGE_SIZE */
     int64_t num_pages;
@@ -120,6 +121,9 @@ typedef struct dsa_rows {
  * row stride logits_stride >= max_ctx.  Entries at t >= row_ctx[r] are not
  * written.  Products are exact and accumulate in fp32 on the tensor cores,
  * so a logit differs from an exact evaluation by accumulation rounding only.
+ * MXFP4 keys multiply their e2m1 codes by the block scales inside the MMA
+ * (block-scaled e2m1 x e4m3); a visible key with the e8m0 NaN code 0xff is
+ * DSA_ERR_RANGE (its logits are then unspecified).
  */
 int dsa_indexer_logits(const dsa_cache *index_cache, const dsa_rows *rows, const uint8_t *q_idx,
                        const float *head_w, float *logits, int64_t logits_stride, int32_t *dev_status,
@@ -252,9 +256,16 @@ int dsa_page_to_slot(const dsa_rows *rows, int64_t pool_pages, const int32_t *id
  * RoPE dims).  q: [num_rows, num_heads, 576] bf16 bits, num_heads a multiple
  * of 16 and <= 96; slots: [num_rows, k] int32, -1 = unused; out:
  * [num_rows, num_heads, 512] fp32; lse: [num_rows, num_heads] fp32 or NULL.
- * A row with no valid slot gets out = 0 and lse = -inf.  The contraction
- * runs on the tensor cores in fp16 x fp16 -> fp32: latents decode to fp16
- * exactly, q rounds from bf16 to fp16 (|q| > 65504 is DSA_ERR_RANGE).
+ * A row with no valid slot gets out = 0 and lse = -inf.  Precision:
+ *   - _decode over FP8 latents (k > 128) contracts e4m3 x e4m3 -> fp32 on the
+ *     latents as stored.  Each head's query is scaled by a power of two and
+ *     written as the sum of two e4m3 terms (exact for bf16 values within
+ *     about 2^10 of the head's largest |q|; smaller ones keep an absolute
+ *     error of at most 2^-17 of that largest), and the softmax weights likewise
+ *     (about 8 significant bits).  A non-finite q is DSA_ERR_RANGE.
+ *   - NVFP4 latents, _prefill, and decode with k <= 128 contract
+ *     fp16 x fp16 -> fp32: latents decode to fp16 exactly, q rounds from bf16
+ *     to fp16 (|q| > 65504 is DSA_ERR_RANGE), weights are fp16.
  *
  * _decode splits each row's k tokens into parts of 128 (k <= 2048, else
  * DSA_ERR_UNSUPPORTED), one CTA per part, keeps each part's normalised
