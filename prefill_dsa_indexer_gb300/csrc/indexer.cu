@@ -55,19 +55,19 @@ constexpr int kMxPageRows = kMxPageBytes / 64;                                  
 template <int G, bool kMx>
 struct IdxCfg {
     static constexpr int N = 32 * G;
-    // Decode (G <= 2) streams every key from HBM with a light epilogue: two CTAs share each SM,
-    // because one CTA's bulk-copy stream tops out below the SM's share of HBM bandwidth however
-    // many stages it keeps in flight.  Each CTA then gets half of the TMEM and of the shared
-    // memory.  Verify (G = 4) and prefill (G = 8) need more epilogue warps, registers and TMEM
-    // per key: one CTA per SM.
+    // Decode and verify (G <= 4) stream every key from HBM with a light epilogue: two CTAs share
+    // each SM, because one CTA's bulk-copy stream tops out below the SM's share of HBM bandwidth
+    // however many stages it keeps in flight.  Each CTA then gets half of the TMEM and of the
+    // shared memory.  Prefill (G = 8) needs more epilogue warps, registers and TMEM per key: one
+    // CTA per SM.
     // (MXFP4 keys: two CTAs only for G = 1, whose accumulators leave room for the scale factors.)
-    static constexpr int kCtasPerSm = kMx ? (G == 1 ? 2 : 1) : (G <= 2 ? 2 : 1);
+    static constexpr int kCtasPerSm = kMx ? (G == 1 ? 2 : 1) : (G <= 4 ? 2 : 1);
     static constexpr int kMaxGroups = kCtasPerSm == 2 ? 256 : kIndexerMaxGroups;  // groups per launch
     static constexpr int kSmemBudget = kCtasPerSm == 2 ? 228 * 1024 / 2 - 1024 : 227 * 1024;
     // keys per tile: 256 (four pages, two M = 128 products) halves every per-tile cost of the
-    // pipeline for decode and verify; prefill's N = 256 accumulators keep 128-key tiles
-    // (MXFP4 keys from G = 4 on: 128-key tiles leave TMEM room for the scale factors)
-    static constexpr int kTileKeys = (G >= 8 || (kMx && G >= 4)) ? 128 : 256;
+    // pipeline for decode; from G = 4 on (N >= 128) 128-key tiles leave TMEM room for two or more
+    // accumulators in half of an SM's TMEM (verify) and for prefill's N = 256 ring
+    static constexpr int kTileKeys = G >= 4 ? 128 : 256;
     static constexpr int kPagesPerTile = kTileKeys / DSA_PAGE_SIZE;
     static constexpr int kHalves = kTileKeys / 128;
     // query buffers: two, so the next group's query loads during this group's last tiles, except
@@ -80,7 +80,12 @@ struct IdxCfg {
     static constexpr int kEpiSplit = G * (kTileKeys / 128) / 2;
     static constexpr int kEpiWarps = 4 * kEpiSplit;
     static constexpr int kRowsPerEpiWarp = G / kEpiSplit;
-    static constexpr int kThreads = 128 + 32 * kEpiWarps;
+    // warp 0 producer, warp 1 MMA, then the epilogue warps (warp w reads TMEM lane quadrant w % 4;
+    // any four consecutive epilogue warps cover the four quadrants).  They start at warp 2, so that
+    // two CTAs of 4 or 8 epilogue warps hold 20 warps per SM and 96 registers a thread; prefill's
+    // 16 epilogue warps start at warp 4 (18 or 20 warps give the same registers; 20 spill less).
+    static constexpr int kEpiWarp0 = G >= 8 ? 4 : 2;
+    static constexpr int kThreads = 32 * (kEpiWarp0 + kEpiWarps);
     // arrivals that release a stage or an accumulator: one per epilogue warp
     static constexpr uint32_t kRelease = kEpiWarps;
     // head weights in shared memory, per warp: its own rows
@@ -413,10 +418,10 @@ __global__ void __launch_bounds__(IdxCfg<G, kMx>::kThreads, IdxCfg<G, kMx>::kCta
                 mma_commit(mma_done);
                 mbar_wait(mma_done, 0, abort, a.status);
             }
-        } else if (warp >= 4) {
+        } else if (warp >= C::kEpiWarp0) {
             // ------------------------------------------------ epilogue: two TMEM items per warp and tile
             constexpr int R = C::kRowsPerEpiWarp;
-            const int e = warp - 4;
+            const int e = warp - C::kEpiWarp0;
             const int quad = warp & 3;  // TMEM lane quadrant this warp may read
             const int rbeg = (e >> 2) * R;
             const int key_lane = quad * 32 + lane;
