@@ -35,14 +35,13 @@
 //   * S (128 TMEM columns) and O^T (4 x H columns) share the 512 columns;
 //     the part's output is normalised by its own sum, stored in fp16 with its
 //     (max, sum), and merged by mla_combine_kernel as in mla.cu.
-#include <cuda_fp16.h>
-
-#include "kernels.h"
-#include "ptx.cuh"
+#include "mla_fp8_common.cuh"
 
 namespace dsa {
 
 namespace {
+
+using namespace fp8mla;
 
 constexpr int kTok = kMlaTokensPerSplit;  // 128 tokens: the whole part
 constexpr int kMaxH = 96;
@@ -65,49 +64,6 @@ static_assert(OFF_KV % 1024 == 0 && OFF_P % 1024 == 0, "operand blocks at 1024-b
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemO = kTok;  // O^T after the S accumulator
 
-__device__ __forceinline__ uint32_t sw128(int row, int u) {
-    return static_cast<uint32_t>(row * 128 + ((u ^ (row & 7)) << 4));
-}
-
-// Two fp32 -> two e4m3 (round to nearest even, saturating): lo value in the low byte.
-__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
-    uint16_t r;
-    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
-    return r;
-}
-
-// The two e4m3 values of the low 16 bits back to fp32 (exact).
-__device__ __forceinline__ float2 e4m3x2_to_f2(uint32_t v) {
-    uint32_t h;
-    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"(static_cast<uint16_t>(v)));
-    return __half22float2(*reinterpret_cast<__half2 *>(&h));
-}
-
-// x = hi + lo with hi = e4m3(x) and lo = e4m3(x - hi), for a pair: returns (hi pair, lo pair).
-__device__ __forceinline__ uint2 split_pair(float x0, float x1) {
-    const uint32_t hi = e4m3x2(x0, x1);
-    const float2 d = e4m3x2_to_f2(hi);
-    return make_uint2(hi, e4m3x2(x0 - d.x, x1 - d.y));
-}
-
-__device__ __forceinline__ float fast_exp2(float x) {
-    float y;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
-
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, bool valid) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(valid ? 16 : 0)
-                 : "memory");
-}
-
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-
 // ---------------------------------------------------------------- query preparation
 // One warp per (row, head): the head's 576 bf16 values become hi + lo e4m3 at 2^e_h, written as
 // the kernel's 128-byte-swizzled K-major operand blocks, plus 2^-e_h after the image.  A warp
@@ -127,70 +83,10 @@ __device__ __forceinline__ void qprep_head(const MlaArgs &a, int64_t w, int lane
     const int H = a.num_heads;
     const int64_t row = w / H;
     const int h = static_cast<int>(w % H);
-    const uint16_t *q = a.q + w * DSA_LATENT_DIM;
     uint8_t *img = a.qprep + row * mla_qprep_row_bytes(H);
-    // lane l holds 16-value units l and l + 32 (units 32..35 are the RoPE dims)
-    float v[2][16];
-    float amax = 0.f;
-    bool bad = false;  // a NaN or an infinity among this lane's values
-#pragma unroll
-    for (int k = 0; k < 2; ++k) {
-        const int unit = lane + 32 * k;
-        if (unit < DSA_LATENT_DIM / 16) {
-            const int4 x0 = *reinterpret_cast<const int4 *>(q + unit * 16);
-            const int4 x1 = *reinterpret_cast<const int4 *>(q + unit * 16 + 8);
-            const uint32_t wd[8] = {static_cast<uint32_t>(x0.x), static_cast<uint32_t>(x0.y),
-                                    static_cast<uint32_t>(x0.z), static_cast<uint32_t>(x0.w),
-                                    static_cast<uint32_t>(x1.x), static_cast<uint32_t>(x1.y),
-                                    static_cast<uint32_t>(x1.z), static_cast<uint32_t>(x1.w)};
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                v[k][2 * j] = __uint_as_float(wd[j] << 16);
-                v[k][2 * j + 1] = __uint_as_float(wd[j] & 0xffff0000u);
-                amax = fmaxf(amax, fmaxf(fabsf(v[k][2 * j]), fabsf(v[k][2 * j + 1])));
-                bad |= !(fabsf(v[k][2 * j]) <= 3.4e38f) || !(fabsf(v[k][2 * j + 1]) <= 3.4e38f);
-            }
-        }
-    }
-    if (__any_sync(0xffffffffu, bad) && lane == 0) report(a.status, DSA_ERR_RANGE);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-    // 2^e with the head's largest |q| * 2^e in (224, 448]
-    int e = 0;
-    if (amax > 0.f && amax <= 3.4e38f) {
-        int x;
-        const float f = frexpf(amax, &x);  // amax = f 2^x, f in [0.5, 1)
-        e = (f <= 0.875f ? 9 : 8) - x;
-        e = max(-120, min(120, e));
-    }
-    const float sc = ldexpf(1.0f, e);
-    const int H128 = H * 128;
-#pragma unroll
-    for (int k = 0; k < 2; ++k) {
-        const int unit = lane + 32 * k;
-        if (unit >= DSA_LATENT_DIM / 16) continue;
-        uint32_t hi[4], lo[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const uint2 p0 = split_pair(v[k][4 * j] * sc, v[k][4 * j + 1] * sc);
-            const uint2 p1 = split_pair(v[k][4 * j + 2] * sc, v[k][4 * j + 3] * sc);
-            hi[j] = p0.x | (p1.x << 16);
-            lo[j] = p0.y | (p1.y << 16);
-        }
-        uint8_t *dh, *dl;
-        if (unit < 32) {  // latent dims: chunk unit / 8, 16-byte unit unit % 8 of the head's row
-            const int c = unit >> 3, u = unit & 7;
-            dh = img + c * H128 + sw128(h, u);
-            dl = img + (4 + c) * H128 + sw128(h, u);
-        } else {  // RoPE dims: units 0..3 (hi) and 4..7 (lo) of the head's row of the last block
-            const int r = unit - 32;
-            dh = img + 8 * H128 + sw128(h, r);
-            dl = img + 8 * H128 + sw128(h, 4 + r);
-        }
-        *reinterpret_cast<uint4 *>(dh) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-        *reinterpret_cast<uint4 *>(dl) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-    }
-    if (lane == 0) reinterpret_cast<float *>(img + 9 * H128)[h] = ldexpf(1.0f, -e);
+    int4 x[4];
+    load_q_head(a.q + w * DSA_LATENT_DIM, lane, x);
+    convert_q_head(x, h, H, img, reinterpret_cast<float *>(img + 9 * H * 128) + h, a.status, lane);
 }
 
 // ---------------------------------------------------------------- attention over one part
@@ -379,18 +275,15 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_fp8_kernel(const MlaAr
                     uint32_t hw[8], lw[8];
 #pragma unroll
                     for (int j = 0; j < 32; j += 4) {
-                        float hi[4], lo[4];
+                        float p[4];
 #pragma unroll
                         for (int x = 0; x < 4; ++x) {
-                            const float p = ((mk[c] >> (j + x)) & 1u)
-                                                ? fast_exp2(__uint_as_float(sr[j + x]) * s_scale - msub)
-                                                : 0.f;
-                            ls[x] += p;
-                            hi[x] = __uint_as_float((__float_as_uint(p) + 0x80000u) & 0xfff00000u);
-                            lo[x] = p - hi[x];
+                            p[x] = ((mk[c] >> (j + x)) & 1u)
+                                       ? fast_exp2(__uint_as_float(sr[j + x]) * s_scale - msub)
+                                       : 0.f;
+                            ls[x] += p[x];
                         }
-                        hw[j / 4] = e4m3x2(hi[0], hi[1]) | (e4m3x2(hi[2], hi[3]) << 16);
-                        lw[j / 4] = e4m3x2(lo[0], lo[1]) | (e4m3x2(lo[2], lo[3]) << 16);
+                        p_split4(p, hw[j / 4], lw[j / 4]);
                     }
                     if (h < H) {
                         const int u = 4 * half + 2 * c;

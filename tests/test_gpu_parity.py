@@ -315,6 +315,57 @@ def test_sparse_mla(case):
     assert np.all(np.abs(gl[fin] - ref_l[fin]) <= 2e-3)
 
 
+def _mla_check(inp, wl, slots, mode, q=None):
+    """Run one attention call and compare it with the oracle on the same selection."""
+    q = inp.q_mla if q is None else q
+    st = P.new_status()
+    fn = P.sparse_mla_decode if mode == "decode" else P.sparse_mla_prefill
+    out, lse = fn(inp.lat_pool, wl.lat_fmt, inp.tensor_scale, q, torch.from_numpy(slots).cuda(), U.SM_SCALE,
+                  status=st)
+    torch.cuda.synchronize()
+    P.check_status(st)
+    ref_o, ref_l = oracle.sparse_mla(inp.np("lat_pool"), U.ORACLE_FMT[wl.lat_fmt], inp.tensor_scale,
+                                     q.cpu().numpy(), slots, U.SM_SCALE)
+    max_abs, rel = U.mla_errors(out.cpu().numpy(), ref_o)
+    assert max_abs <= 2e-2 and rel <= 1e-2, (max_abs, rel)
+    gl = lse.cpu().numpy()
+    assert np.array_equal(np.isneginf(gl), np.isneginf(ref_l))
+    fin = np.isfinite(ref_l)
+    assert np.all(np.abs(gl[fin] - ref_l[fin]) <= 2e-3 * np.maximum(1.0, np.abs(ref_l[fin])))
+
+
+@pytest.mark.parametrize("qmul", [4.0, 16.0])
+def test_fp8_rows_scores_spread_over_many_binades(qmul):
+    """Queries scaled by a power of two (exact in bf16) spread each head's scores over tens of log2 units,
+    so along a row of 64-token tiles the one-CTA-per-row kernel's reference max moves up many times and
+    the accumulated output and sum of those heads are rescaled in place."""
+    wl = _wl("spread", [3000, 2600, 2300], seed=11)
+    inp = U.gpu_inputs(wl)
+    slots = _mla_case(inp, 2048, seed=3)
+    q = (inp.q_mla.view(torch.bfloat16) * qmul).view(torch.int16)
+    _mla_check(inp, wl, slots, "prefill", q)
+
+
+def test_fp8_rows_leading_tiles_without_tokens():
+    """The first three tiles of a row hold only unused slots (-1), a middle tile is partly empty, and
+    the row ends in a ragged tile: the reference max is set by the first valid token."""
+    wl = _wl("lead", [3000, 3000], seed=12)
+    inp = U.gpu_inputs(wl)
+    slots = _mla_case(inp, 1000, seed=4)
+    slots = np.concatenate([np.full((2, 192), -1, np.int32), slots], axis=1)  # 1192 = 18 tiles + 40
+    slots[0, 500:530] = -1
+    _mla_check(inp, wl, slots, "prefill")
+
+
+@pytest.mark.parametrize("k", [1, 64, 100, 128])
+def test_fp8_decode_single_part(k):
+    """Decode rows whose selection fits one 128-token part take the one-CTA-per-row kernel."""
+    wl = _wl("single", [3000, 90, 2048], seed=13)
+    inp = U.gpu_inputs(wl)
+    slots = _mla_case(inp, k, seed=5)
+    _mla_check(inp, wl, slots, "decode")
+
+
 def test_sparse_mla_empty_rows():
     inp = U.gpu_inputs(_wl("e", [300, 300]))
     slots = np.full((2, 2048), -1, dtype=np.int32)
