@@ -324,6 +324,7 @@ size_t dsa_sparse_mla_workspace_size(int32_t num_rows, int32_t num_heads, int32_
     return mla_workspace_bytes(num_rows, num_heads, k);
 }
 
+
 enum class MlaMode { kPrefill, kDecode, kDecodePrepareOnly, kDecodePrepared };
 
 static int sparse_mla_common(const dsa_cache *lat, const uint16_t *q, int32_t num_heads, const int32_t *slots,
@@ -371,16 +372,13 @@ static int sparse_mla_common(const dsa_cache *lat, const uint16_t *q, int32_t nu
             a.splits = static_cast<int32_t>(splits);
         }
     }
-    // FP8 latents run on the FP8 tensor cores: split decode as parts merged by log-sum-exp
-    // (mla_fp8.cu), prefill and single-part decode as one CTA per row (mla_fp8_prefill.cu).  NVFP4
-    // latents decode to fp16 (mla.cu).
-    const bool fp8 = lat->format == DSA_LATENT_FP8;
-    const bool fp8_decode = fp8 && decode && a.splits > 1;
+    // split decode over FP8 latents runs on the FP8 tensor cores (mla_fp8.cu); NVFP4 latents,
+    // prefill and single-part decode decode the latents to fp16 (mla.cu)
+    const bool fp8_decode = decode && a.splits > 1 && lat->format == DSA_LATENT_FP8;
     const cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (prep_only) return launch_status(fp8_decode ? launch_mla_qprep_fp8(a, st) : launch_mla_qprep(a, st));
     a.q_prepared = mode == MlaMode::kDecodePrepared;
-    if (fp8) return launch_status(fp8_decode ? launch_sparse_mla_fp8_decode(a, st) : launch_sparse_mla_fp8_rows(a, st));
-    return launch_status(launch_sparse_mla(a, st));
+    return launch_status(fp8_decode ? launch_sparse_mla_fp8_decode(a, st) : launch_sparse_mla(a, st));
 }
 
 int dsa_sparse_mla_decode(const dsa_cache *latent_cache, const uint16_t *q, int32_t num_heads,

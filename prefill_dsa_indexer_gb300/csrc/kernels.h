@@ -221,8 +221,6 @@ cudaError_t launch_mla_combine(const MlaArgs &a, cudaStream_t s);
 // (preparation unless a.q_prepared, one CTA per 128-token part, merge).  Needs a.splits >= 2.
 cudaError_t launch_mla_qprep_fp8(const MlaArgs &a, cudaStream_t s);
 cudaError_t launch_sparse_mla_fp8_decode(const MlaArgs &a, cudaStream_t s);
-// FP8 latents, one CTA per row over the whole selection (prefill, and decode rows of one part)
-cudaError_t launch_sparse_mla_fp8_rows(const MlaArgs &a, cudaStream_t s);
 
 // Decode splits every row's selected tokens into parts of this many tokens (fixed, so a row's
 // result does not depend on the batch), merged by log-sum-exp.

@@ -1,7 +1,6 @@
-// mla_fp8_common.cuh -- pieces shared by the FP8-latent attention kernels (mla_fp8.cu: split
-// decode; mla_fp8_prefill.cu: one CTA per row).
+// mla_fp8_common.cuh -- the FP8-latent attention's query image and operand helpers (mla_fp8.cu).
 //
-// Both run S = Q . KV^T and O^T += V^T . P^T as e4m3 x e4m3 -> fp32 MMAs on the latents exactly as
+// The split decode kernel runs S = Q . KV^T and O^T += V^T . P^T as e4m3 x e4m3 -> fp32 MMAs on the latents exactly as
 // stored (vLLM blog "Day-0 support for Kimi K3.1 Pro", section "One KV cache, three states": the
 // 576-byte FP8 latent).  An e4m3 value has 4 significant bits, a bf16 query 8, so each query head
 // is written as the sum of two e4m3 terms at a power of two per head, and the softmax weights P

@@ -335,10 +335,10 @@ def _mla_check(inp, wl, slots, mode, q=None):
 
 
 @pytest.mark.parametrize("qmul", [4.0, 16.0])
-def test_fp8_rows_scores_spread_over_many_binades(qmul):
+def test_prefill_scores_spread_over_many_binades(qmul):
     """Queries scaled by a power of two (exact in bf16) spread each head's scores over tens of log2 units,
-    so along a row of 64-token tiles the one-CTA-per-row kernel's reference max moves up many times and
-    the accumulated output and sum of those heads are rescaled in place."""
+    so along a row of 64-token tiles the running max moves up many times and the accumulated output and
+    sum of those heads are rescaled."""
     wl = _wl("spread", [3000, 2600, 2300], seed=11)
     inp = U.gpu_inputs(wl)
     slots = _mla_case(inp, 2048, seed=3)
@@ -346,9 +346,9 @@ def test_fp8_rows_scores_spread_over_many_binades(qmul):
     _mla_check(inp, wl, slots, "prefill", q)
 
 
-def test_fp8_rows_leading_tiles_without_tokens():
+def test_prefill_leading_tiles_without_tokens():
     """The first three tiles of a row hold only unused slots (-1), a middle tile is partly empty, and
-    the row ends in a ragged tile: the reference max is set by the first valid token."""
+    the row ends in a ragged tile: the running max starts at the first valid token."""
     wl = _wl("lead", [3000, 3000], seed=12)
     inp = U.gpu_inputs(wl)
     slots = _mla_case(inp, 1000, seed=4)
@@ -359,7 +359,7 @@ def test_fp8_rows_leading_tiles_without_tokens():
 
 @pytest.mark.parametrize("k", [1, 64, 100, 128])
 def test_fp8_decode_single_part(k):
-    """Decode rows whose selection fits one 128-token part take the one-CTA-per-row kernel."""
+    """Decode rows whose selection fits one 128-token part run as one CTA per row (no split merge)."""
     wl = _wl("single", [3000, 90, 2048], seed=13)
     inp = U.gpu_inputs(wl)
     slots = _mla_case(inp, k, seed=5)
