@@ -25,10 +25,10 @@
 //     rounded; about 8 significant bits, the precision of bf16), and O^T[dims x heads] += V^T . P^T runs as 2 x 16 MMAs with the
 //     latents read MN-major from the same shared-memory tile (M = 128 dims,
 //     N = H heads, K = 32 tokens);
-//   * 8 gather warps fill the tile with 16-byte cp.async copies in five
-//     128-byte column chunks (four latent chunks, then the doubled RoPE
-//     chunk), one mbarrier per chunk, so the S MMAs of a chunk start as soon
-//     as it has landed; unused slots (-1) are zero-filled and masked;
+//   * 8 gather warps fill the tile's four latent chunks (128-byte columns) with 16-byte cp.async
+//     copies, one mbarrier per chunk, so the S MMAs of a chunk start as soon as it has landed;
+//     three more warps fetch the RoPE chunk (each token's 64 RoPE bytes written twice across its
+//     row) at the same time; unused slots (-1) are zero-filled and masked;
 //   * the softmax runs on the 8 gather warps, two per TMEM lane quadrant, each
 //     thread one head over 64 tokens; the two halves of a head swap their max and
 //     sum through shared memory;
@@ -100,7 +100,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_fp8_kernel(const MlaAr
     float *red = reinterpret_cast<float *>(smem + OFF_RED);
     uint32_t *mask = reinterpret_cast<uint32_t *>(smem + OFF_MASK);  // [4] valid-token bits
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + OFF_BARS);
-    uint64_t *kv_full = bars;       // [5] gather chunk c -> MMA (count: 8 gather warps)
+    uint64_t *kv_full = bars;       // [5] gather chunk c -> MMA (latent chunks: 8 warps; RoPE: 3)
     uint64_t *q_full = bars + 5;    // bulk copy of the prepared Q -> MMA
     uint64_t *s_full = bars + 6;    // MMA -> softmax (commit)
     uint64_t *p_full = bars + 7;    // softmax -> MMA (count 8)
@@ -118,7 +118,8 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_fp8_kernel(const MlaAr
 
     if (tid == 0) {
         *abort = 0;
-        for (int c = 0; c < 5; ++c) mbar_init(&kv_full[c], 8);
+        for (int c = 0; c < 4; ++c) mbar_init(&kv_full[c], 8);  // latent chunks: warps 4-11
+        mbar_init(&kv_full[4], 3);                                // RoPE chunk: warps 1-3
         mbar_init(q_full, 1);
         mbar_init(s_full, 1);
         mbar_init(p_full, 8);
@@ -185,6 +186,22 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_fp8_kernel(const MlaAr
                 mma_commit(pv_done);
             }
         }
+    } else if (warp < 4) {
+        // ---------------------------------------------------------------- gather of the RoPE chunk
+        // (warps 1-3): each token's 64 RoPE bytes, written twice across its 128-byte row
+        const uint32_t kvb = smem_u32(kv) + 4 * kChunk;
+        for (int e = tid - 32; e < kTok * 8; e += 96) {
+            const int t = e >> 3, u = e & 7;
+            int32_t s = t < n_tok ? row_slots[t] : -1;
+            if (s >= 0 && static_cast<int64_t>(s) >= a.num_pages * DSA_PAGE_SIZE) s = -1;  // reported by warps 4-11
+            const uint8_t *src = a.pool + static_cast<int64_t>(max(s, 0)) * DSA_LATENT_DIM + DSA_VALUE_DIM + (u & 3) * 16;
+            cp_async16(kvb + sw128(t, u), src, s >= 0);
+        }
+        cp_async_commit();
+        cp_async_wait<0>();
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&kv_full[4]);
     } else if (warp >= 4) {
         const int gtid = tid - 128;      // 0..255
         const int quad = warp & 3;
@@ -209,38 +226,36 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_fp8_kernel(const MlaAr
             }
             const uint32_t kvb = smem_u32(kv);
 #pragma unroll
-            for (int c = 0; c < 5; ++c) {
+            for (int c = 0; c < 4; ++c) {
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     const int t = t0 + 32 * i;
-                    const int src_off = c < 4 ? c * 128 + u * 16 : DSA_VALUE_DIM + (u & 3) * 16;
-                    const uint8_t *src = a.pool + static_cast<int64_t>(max(slot[i], 0)) * DSA_LATENT_DIM + src_off;
+                    const uint8_t *src = a.pool + static_cast<int64_t>(max(slot[i], 0)) * DSA_LATENT_DIM + c * 128 + u * 16;
                     cp_async16(kvb + c * kChunk + sw128(t, u), src, slot[i] >= 0);
                 }
                 cp_async_commit();
             }
-            // chunk c is complete once all but the 4 - c later groups have landed
+            // chunk c is complete once all but the 3 - c later groups have landed (the valid-token
+            // mask above is complete once chunk 3 is)
             auto done = [&](int c) {
                 fence_async_smem();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&kv_full[c]);
             };
-            cp_async_wait<4>();
-            done(0);
             cp_async_wait<3>();
-            done(1);
+            done(0);
             cp_async_wait<2>();
-            done(2);
+            done(1);
             cp_async_wait<1>();
-            done(3);
+            done(2);
             cp_async_wait<0>();
-            done(4);
+            done(3);
         }
         {
             // ------------------------------------------------------------ softmax, 8 warps: thread
             // (half, h) takes head h = 32 quad + lane over tokens [64 half, 64 half + 64)
             const int h = quad * 32 + lane, half = (warp - 4) >> 2;
-            ok = mbar_wait_warp(s_full, 0, abort, a.status) && mbar_wait_warp(&kv_full[4], 0, abort, a.status);
+            ok = mbar_wait_warp(s_full, 0, abort, a.status) && mbar_wait_warp(&kv_full[3], 0, abort, a.status);
             float m = -INFINITY, l = 0.f, lp = 0.f;
             const float hs = h < H ? reinterpret_cast<const float *>(qimg + 9 * H * 128)[h] : 0.f;
             const float s_scale = a.tensor_scale * a.sm_scale * 1.4426950408889634f * hs;
