@@ -675,56 +675,59 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_kernel(const MlaArgs a
 }
 
 // Merge the splits of each (row, head): O = o_scale * sum_s w_s O_s / sum_s w_s with
-// w_s = l_s 2^(m_s - M), M = max_s m_s (log2 units), O_s the split's normalised
-// fp16 output.  One CTA per (row, head), four output dims per thread.
+// w_s = l_s 2^(m_s - M), M = max_s m_s (log2 units), O_s the split's normalised fp16 output.
+// One CTA per (row, head): warp 0 turns the splits' (max, sum) into the normalised weights once,
+// every thread then sums four output dims over the splits (its partial loads issued first).
 __global__ void __launch_bounds__(128) mla_combine_kernel(const MlaArgs a) {
+    __shared__ float wn[kMlaMaxSplits];
     pdl_launch_dependents();
     pdl_wait();
     const int H = a.num_heads, S = a.splits;
     const int row = blockIdx.x / H, h = blockIdx.x % H;
-    const float *ml = a.part_ml + static_cast<int64_t>(row) * S * H * 2;
-    const float o_scale = a.format == DSA_LATENT_FP8 ? a.tensor_scale : 1.0f;
+    const int tid = threadIdx.x;
     // all partial loads in flight at once
     uint2 o[kMlaMaxSplits];
-    float ms[kMlaMaxSplits], ls[kMlaMaxSplits];
-#pragma unroll
-    for (int s = 0; s < kMlaMaxSplits; ++s) {
-        if (s < S) {
-            ms[s] = ml[(s * H + h) * 2];
-            ls[s] = ml[(s * H + h) * 2 + 1];
-            o[s] = reinterpret_cast<const uint2 *>(
-                a.part_o + ((static_cast<int64_t>(row) * S + s) * H + h) * DSA_VALUE_DIM)[threadIdx.x];
-        }
-    }
-    float M = -INFINITY;
 #pragma unroll
     for (int s = 0; s < kMlaMaxSplits; ++s)
-        if (s < S) M = fmaxf(M, ms[s]);
-    float wsum = 0.f;
+        if (s < S)
+            o[s] = reinterpret_cast<const uint2 *>(
+                a.part_o + ((static_cast<int64_t>(row) * S + s) * H + h) * DSA_VALUE_DIM)[tid];
+    if (tid < 32) {
+        const float *ml = a.part_ml + static_cast<int64_t>(row) * S * H * 2;
+        const float m = tid < S ? ml[(tid * H + h) * 2] : -INFINITY;
+        const float l = tid < S ? ml[(tid * H + h) * 2 + 1] : 0.f;
+        float M = m;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+        const float w = (m == -INFINITY) ? 0.f : l * exp2f(m - M);
+        float W = w;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) W += __shfl_xor_sync(0xffffffffu, W, off);
+        const float o_scale = a.format == DSA_LATENT_FP8 ? a.tensor_scale : 1.0f;
+        if (tid < S) wn[tid] = W > 0.f ? w * (o_scale / W) : 0.f;
+        if (tid == 0 && a.lse)
+            a.lse[static_cast<int64_t>(row) * H + h] = W > 0.f ? (M + log2f(W)) * 0.6931471805599453f : -INFINITY;
+    }
+    __syncthreads();
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
     for (int s = 0; s < kMlaMaxSplits; ++s) {
-        if (s >= S || ms[s] == -INFINITY) continue;
-        const float w = ls[s] * exp2f(ms[s] - M);
+        if (s >= S) continue;
+        const float w = wn[s];
         const float2 lo = __half22float2(*reinterpret_cast<const __half2 *>(&o[s].x));
         const float2 hi = __half22float2(*reinterpret_cast<const __half2 *>(&o[s].y));
-        wsum += w;
         acc.x = fmaf(w, lo.x, acc.x);
         acc.y = fmaf(w, lo.y, acc.y);
         acc.z = fmaf(w, hi.x, acc.z);
         acc.w = fmaf(w, hi.y, acc.w);
     }
-    const float inv = wsum > 0.f ? o_scale / wsum : 0.f;
-    reinterpret_cast<float4 *>(a.out + (static_cast<int64_t>(row) * H + h) * DSA_VALUE_DIM)[threadIdx.x] =
-        make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+    reinterpret_cast<float4 *>(a.out + (static_cast<int64_t>(row) * H + h) * DSA_VALUE_DIM)[tid] = acc;
     // The partials are workspace scratch, dead once read: drop their L2 lines unwritten
     // (S x 8 lines of 128 B for this head) so they cost no HBM write-back.
     __syncthreads();
-    if (threadIdx.x < S * 8)
-        l2_discard_line(a.part_o + ((static_cast<int64_t>(row) * S + (threadIdx.x >> 3)) * H + h) * DSA_VALUE_DIM +
-                        (threadIdx.x & 7) * 64);
-    if (threadIdx.x == 0 && a.lse)
-        a.lse[static_cast<int64_t>(row) * H + h] = wsum > 0.f ? (M + log2f(wsum)) * 0.6931471805599453f : -INFINITY;
+    if (tid < S * 8)
+        l2_discard_line(a.part_o + ((static_cast<int64_t>(row) * S + (tid >> 3)) * H + h) * DSA_VALUE_DIM +
+                        (tid & 7) * 64);
 }
 
 // Decode query preparation: each row's bf16 query becomes, once, the exact fp16 shared-memory
