@@ -354,12 +354,17 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const TopkArgs a) {
         s.rank_t[1] = 0xffffffffu;
     }
     for (int b = tid; b < kBins; b += kThreads) s.hist[b] = 0;
-    // the chunk's block-table entries, read now so that writing slots at the end stays local
+    // the chunk's block-table entries, so that writing slots at the end stays local: loaded into
+    // registers now, stored after the first pass (the loads overlap it)
     const int pg0 = c0 / DSA_PAGE_SIZE;
     const int npg = (bt_row != nullptr && nloc > 0)
                         ? min(kBtCache, (c0 + nloc - 1) / DSA_PAGE_SIZE - pg0 + 1)
                         : 0;
-    for (int i = tid; i < npg; i += kThreads) s.bt_cache[i] = bt_row[pg0 + i];
+    static_assert(kBtCache <= 2 * kThreads, "two block-table entries per thread");
+    int32_t btr[2] = {0, 0};
+#pragma unroll
+    for (int q = 0; q < 2; ++q)
+        if (tid + q * kThreads < npg) btr[q] = bt_row[pg0 + tid + q * kThreads];
     __syncthreads();
 
     uint32_t base = 0, top = 0;
@@ -537,6 +542,9 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(const TopkArgs a) {
             base = s.range[0];
             top = s.range[1];
     }
+#pragma unroll
+    for (int q = 0; q < 2; ++q)
+        if (tid + q * kThreads < npg) s.bt_cache[tid + q * kThreads] = btr[q];
     if (a.discard_logits && chunk.ncache == nloc) {
         // the chunk now lives in shared memory and the logits are scratch: drop the L2 lines
         // that lie wholly inside this chunk, unwritten
