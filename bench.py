@@ -921,9 +921,11 @@ def main():
         with open(tfile) as f:
             traffic = json.load(f).get(wl.name)
     # scorer, top-k (with page -> slot unless single pass, which launches it apart), sparse MLA;
-    # decode with split rows adds the query prep and the merge
+    # decode with split rows adds the query prep and the merge; the histogram top-k of few long
+    # rows runs as three launches
     launches_per_step = 3 + (1 if args.single_pass else 0) + (
-        2 if (not prefill and P.sparse_mla_workspace_size(wl.num_rows, wl.heads, wl.k) > 0) else 0)
+        2 if (not prefill and P.sparse_mla_workspace_size(wl.num_rows, wl.heads, wl.k) > 0) else 0) + (
+        2 if (not args.single_pass and P.topk_workspace_size(wl.num_rows, inp.max_ctx, wl.k) > 0) else 0)
 
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,

@@ -144,21 +144,25 @@ int dsa_indexer_logits(const dsa_cache *index_cache, const dsa_rows *rows, const
  *
  * workspace (device, 256-byte aligned, no initial contents) may be NULL.
  * With workspace_bytes >= dsa_topk_workspace_size(num_rows, max_ctx, k) > 0
- * (a few long rows), the selection runs in two phases: independent CTAs
- * reduce chunks of each row to their best candidates (in position order),
- * and one CTA per row selects among them, checking that no chunk may hold
- * more selected keys than it passed on; when one may (scores concentrated in
- * one chunk, or tied at the threshold across chunks), that row is selected
- * from its whole logits instead.  Without it (NULL, or a size of 0 for this
- * shape), one thread-block cluster per row selects.  A workspace smaller than
- * the size is DSA_ERR_WORKSPACE.  The result is the same either way.
+ * (at most 64 rows, max_ctx above 131,072), the selection runs as three launches of
+ * independent CTAs over chunks of each row: every chunk counts its keys in
+ * 4096 bins (the top 12 bits of the order-preserving key: one bin per 1/8
+ * binade); every chunk sums its row's counts, finds the bin holding the k-th
+ * largest key and passes on its keys at or above that bin, in position order;
+ * every chunk then finds the exact threshold among the row's keys in that bin
+ * and writes its share of the selection.  A row whose threshold bin holds more
+ * than 12,288 keys (heavy ties, or scores within 1/8 binade of each other) is
+ * selected from its whole logits by one CTA instead (slower).  Without it
+ * (NULL, or a size of 0 for this shape), one thread-block cluster per row
+ * selects.  A workspace smaller than the size is DSA_ERR_WORKSPACE.  The
+ * result is the same either way.
  */
 int dsa_topk(const float *logits, int64_t logits_stride, const int32_t *row_ctx, int32_t num_rows,
              int32_t max_ctx, int32_t k, int32_t *idx_out, int32_t *dev_status, void *workspace,
              size_t workspace_bytes, void *stream);
 
-/* Workspace bytes of the two-phase top-k for this batch on the current device; 0 when the shape
- * (more than 64 rows, or rows of at most 262,144 keys) takes the cluster selection, which needs none. */
+/* Workspace bytes of the histogram top-k for this batch on the current device; 0 when the shape
+ * (more than 64 rows, or rows of at most 131,072 keys) takes the cluster selection, which needs none. */
 size_t dsa_topk_workspace_size(int32_t num_rows, int32_t max_ctx, int32_t k);
 
 /*

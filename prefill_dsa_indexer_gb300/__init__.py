@@ -182,7 +182,7 @@ def indexer_logits(index_pool, key_fmt, block_table, row_req, row_ctx, max_ctx, 
 
 
 def topk_workspace_size(num_rows: int, max_ctx: int, k: int = 2048) -> int:
-    """dsa_topk_workspace_size: bytes of the two-phase top-k's workspace (0: the shape needs none)."""
+    """dsa_topk_workspace_size: bytes of the histogram top-k's workspace (0: the shape needs none)."""
     return int(load_library().dsa_topk_workspace_size(num_rows, max_ctx, k))
 
 
@@ -456,7 +456,7 @@ class Layer:
         self.lse = self.outputs[R * H * VALUE_DIM:].view(R, H)
         need = 0 if prefill else sparse_mla_workspace_size(R, H, self.k)
         self.workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=device)
-        # the two-phase top-k's candidates (few long rows; none otherwise)
+        # the histogram top-k's counts and candidates (few long rows; none otherwise)
         tk = topk_workspace_size(R, self.max_ctx, self.k)
         self.topk_workspace = torch.empty(tk, dtype=torch.uint8, device=device) if tk > 0 else None
         self.status = new_status(device)

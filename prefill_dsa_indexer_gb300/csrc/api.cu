@@ -199,22 +199,12 @@ static int topk_common(const float *logits, int64_t logits_stride, const int32_t
     TopkArgs a{logits, logits_stride, row_ctx, num_rows, max_ctx, k, idx_out, dev_status, hist, discard,
                nullptr, nullptr, 0, nullptr, 0, 0};
     if (workspace != nullptr && hist == nullptr) {
-        // with a large enough workspace, few long rows take the two-phase selection
+        // with a large enough workspace, few long rows take the histogram selection
         const TopkChunkPlan p = topk_chunk_plan(num_rows, max_ctx, k, device_sm_count());
         if (p.bytes > 0) {
             if (workspace_bytes < p.bytes) return DSA_ERR_WORKSPACE;
             if (!aligned(workspace, 256)) return DSA_ERR_INVALID_ARG;
-            const size_t cand = align256(static_cast<size_t>(num_rows) * p.chunks * p.kcap * 4);
-            uint8_t *w = static_cast<uint8_t *>(workspace);
-            a.cand_key = reinterpret_cast<uint32_t *>(w);
-            a.cand_pos = reinterpret_cast<int32_t *>(w + cand);
-            a.cand_meta = reinterpret_cast<uint32_t *>(w + 2 * cand);
-            a.chunks = p.chunks;
-            a.chunk_len = p.chunk_len;
-            a.keep = p.keep;
-            a.keep_last = p.keep_last;
-            a.kcap = p.kcap;
-            a.merge_max = p.merge_max;
+            topk_chunk_bind(a, p, workspace);
         }
     }
     if (slots_out != nullptr) {

@@ -91,31 +91,36 @@ struct TopkArgs {
     // optional: FP8 latent pool whose selected rows (576 B per slot) are prefetched into L2 as
     // the slots are written, so the attention that follows gathers from L2
     const uint8_t *warm_pool;
-    // optional two-phase selection (chunks > 0; see topk_chunk_plan): per-chunk candidates in a
-    // caller workspace, [rows][chunks][kcap] keys and positions, [rows][chunks][4] meta
-    uint32_t *cand_key;
-    int32_t *cand_pos;
-    uint32_t *cand_meta;
-    int32_t chunks, chunk_len, keep, keep_last, kcap, merge_max;
+    // optional histogram selection (chunks > 0; see topk_chunk_plan and topk_chunk_bind), in a caller
+    // workspace
+    uint32_t *hs_list;   // [rows][chunks][4096] each chunk's nonzero bins, ascending: bin << 20 | count
+    uint32_t *hs_nlist;  // [rows][chunks] their numbers
+    uint32_t *hs_key;    // [rows][row_cap] the row's keys in bins >= the threshold bin, position order
+    int32_t *hs_pos;     // [rows][row_cap] their positions
+    uint32_t *hs_chunk;  // [rows][chunks][2] each chunk's offset and count in hs_key
+    uint32_t *hs_row;    // [rows][4] the threshold bin, the keys above it, the keys in it
+    int32_t chunks, chunk_len, row_cap;
 };
 
 cudaError_t launch_topk(const TopkArgs &a, cudaStream_t s);
 
-// Two-phase top-k of decode rows: limits, and the plan for a batch (bytes == 0: not used).  Its two
-// kernels each run several block-wide rounds of about a microsecond; measured on a GB300, that beats
-// the cluster selection only once the rows are longer than a 16-CTA cluster keeps in shared memory
-// (1M keys: 97.7 vs 104.1 us per verify step; 128K keys: 76.3 vs 62.2 us per decode step).
+// Histogram selection of few long rows: limits, the plan for a batch (bytes == 0: not used) and the
+// binding of a workspace of plan.bytes to the arguments.  Its three launches of independent CTAs
+// beat the cluster selection once rows are longer than a cluster keeps in shared memory; measured
+// on a GB300 per step: 256K keys 90.0 vs 102.1 us, 1M keys 76.6 vs 93.5 us, but 128K keys 62.6 vs
+// 60.7 us (its chain of barrier-separated phases costs more than the cluster's there).
 constexpr int kChunkedMaxRows = 64;
-constexpr int kChunkedMinCtx = 262144;
+constexpr int kChunkedMinCtx = 131072;
 constexpr int kChunkMinKeys = 2048;
 constexpr int kChunkedMaxChunks = 96;
 constexpr int kChunkMaxKeys = 16384;
-constexpr int kMergeMaxKeys = 16384;
+constexpr int kHsInCap = 12288;  // keys of a row's threshold bin the select kernel holds
 struct TopkChunkPlan {
-    int32_t chunks, chunk_len, keep, keep_last, kcap, merge_max;
+    int32_t chunks, chunk_len, row_cap;
     size_t bytes;
 };
 TopkChunkPlan topk_chunk_plan(int32_t num_rows, int32_t max_ctx, int32_t k, int sms);
+void topk_chunk_bind(TopkArgs &a, const TopkChunkPlan &p, void *workspace);
 
 struct SlotArgs {
     const int32_t *block_table;

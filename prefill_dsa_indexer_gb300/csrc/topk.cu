@@ -32,6 +32,10 @@
 //      >= T in order (one pass when the chunk is in shared memory, else a
 //      counting pass and a placing pass), and all threads then write the
 //      range.  Output order and values never depend on timing.
+//
+// A few rows longer than 128K keys, with a caller workspace, take the histogram selection at the end
+// of this file instead: three launches of independent CTAs over chunks of each row (bin counts, the
+// threshold bin's candidates, the exact threshold and the output), no clusters.
 #include <cooperative_groups.h>
 
 #include "kernels.h"
@@ -1015,27 +1019,41 @@ cudaError_t launch_variant(const TopkArgs &a, cudaStream_t s) {
     return cudaLaunchKernelEx(&cfg, kern, a);
 }
 
-// ---------------------------------------------------------------- two-phase selection
+// ---------------------------------------------------------------- histogram selection
 //
-// For a few long rows (decode), with a caller workspace: phase A cuts each row into chunks that
-// independent CTAs (no clusters, several per SM) reduce to their own exact top candidates, in
-// position order; phase B merges each row's candidates in one CTA.  The candidates of every chunk
-// are the chunk's best `keep` keys by (key desc, position asc) (up to k for the chunk holding the
-// row's most recent tokens), so the row's selection equals the candidates' selection unless a chunk
-// that dropped keys kept a threshold key at or above the merged threshold T: such a chunk may hold
-// more selected keys than it passed on.  Phase B checks this for every chunk and, when it happens
-// (concentrated or heavily tied scores), selects from the whole row's logits itself (slower, exact).
+// For a few long rows, with a caller workspace.  Each row is cut into chunks that independent CTAs
+// (no clusters, two per SM) handle in three launches:
+//   count:   each chunk counts its keys' top 12 bits (sign, exponent and 3 mantissa bits of the
+//            logit: one bin per 1/8 binade) and writes its nonzero bins as a short list;
+//   collect: each chunk adds its row's lists into the row's histogram, finds the bin B that holds
+//            the row's k-th largest key, and writes its own keys in bins >= B, in position order,
+//            to the row's candidate array (at the offset the lists give for the chunks before it);
+//   select:  each chunk finds the exact threshold T among the row's candidates in bin B and writes
+//            its share of the selection (its keys above T, and keys equal to T while the row's
+//            ties last) at the offset that the candidates of the chunks before it give, with the
+//            slots and the latent prefetches.
+// By construction that is the whole row's selection by (key desc, position asc).  A row whose bin B
+// holds more than kHsInCap keys (ties, or scores within 1/8 binade) is selected from its whole
+// logits by one CTA instead: slower, exact.
 
-constexpr int kAThreads = 512;
-constexpr int kBThreads = 1024;
+constexpr int kHsThreads = 512;
+constexpr int kHsWarps = kHsThreads / 32;
+constexpr int kHsBins = 4096;
+constexpr int kHsShift = 20;  // bin of a key: key >> kHsShift
+constexpr uint32_t kHsCountMask = (1u << kHsShift) - 1u;
+static_assert(kChunkMaxKeys <= static_cast<int>(kHsCountMask), "a list entry holds a chunk's count");
+constexpr int kHsCacheChunks = 96;  // the collect kernel keeps the first kHsCacheLen entries of
+constexpr int kHsCacheLen = 64;     // the lists of this many chunks in shared memory
+constexpr int kHsMaxChunks = 1024;
 
-// Block-wide: the bin holding the need-th largest key of `hist` (kBins counts, scanned from the
+// Block-wide: the bin holding the need-th largest key of `hist` (NB counts, scanned from the
 // top): res[0] = bin, res[1] = keys above it, res[2] = keys in it.
-template <int NT>
+template <int NT, int NB = kBins>
 __device__ void find_bin(const uint32_t *hist, uint32_t need, uint32_t *wred, uint32_t *res) {
-    constexpr int per = kBins / NT;
+    constexpr int per = NB / NT;
+    static_assert(per >= 1 && NB % NT == 0, "whole bins per thread");
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int b_hi = kBins - 1 - per * tid;  // this thread: bins b_hi, b_hi - 1, ..., b_hi - per + 1
+    const int b_hi = NB - 1 - per * tid;  // this thread: bins b_hi, b_hi - 1, ..., b_hi - per + 1
     uint32_t c[per], tsum = 0;
 #pragma unroll
     for (int q = 0; q < per; ++q) {
@@ -1163,105 +1181,348 @@ __device__ void block_minmax(uint32_t lo, uint32_t hi, uint32_t *wred, uint32_t 
     __syncthreads();
 }
 
-// Candidates chunk c of a row of L keys passes on: twice its share of k plus a margin (the row's
-// own chunk count sets the share), up to k for the chunk of the most recent tokens; at most kcap.
-__device__ __forceinline__ int chunk_keep(const TopkArgs &a, int L, int c) {
-    const int nch = (L + a.chunk_len - 1) / a.chunk_len;
-    int kp = (c == nch - 1) ? a.k : ((2 * a.k + nch - 1) / nch + 64 + 31) / 32 * 32;
-    kp = min(kp, a.k);
-    kp = min(kp, a.chunk_len);
-    return min(kp, a.kcap);
+
+// Warp-wide sums of two counters.
+__device__ __forceinline__ void warp_sum2(uint32_t &x, uint32_t &y) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        x += __shfl_xor_sync(0xffffffffu, x, o);
+        y += __shfl_xor_sync(0xffffffffu, y, o);
+    }
 }
 
-// Phase A: CTA (row, c) writes chunk c's best keys (all of them if the chunk has no more than its
-// keep) with their positions, in position order, and meta = {count, threshold key, complete}.
-__global__ void __launch_bounds__(kAThreads, 2) topk_chunk_kernel(const TopkArgs a) {
-    extern __shared__ uint32_t ka_smem[];
-    uint32_t *keys = ka_smem;                 // [chunk_len]
-    uint32_t *hist = keys + a.chunk_len;      // [kBins]
-    uint32_t *wred = hist + kBins;            // [64]
-    uint32_t *wgt = wred + 64, *weq = wgt + 32, *res = weq + 32;
+// Logits i .. i+3 of a chunk (i a multiple of 4), 0 at or past lim: one 16-byte load when all four
+// are below lim and the chunk start is 16-byte aligned (vec), else one load per logit.
+__device__ __forceinline__ float4 ld4(const float *src, int i, int lim, bool vec) {
+    if (vec && i + 3 < lim) return __ldg(reinterpret_cast<const float4 *>(src + i));
+    float4 v;
+    v.x = i < lim ? __ldg(src + i) : 0.f;
+    v.y = i + 1 < lim ? __ldg(src + i + 1) : 0.f;
+    v.z = i + 2 < lim ? __ldg(src + i + 2) : 0.f;
+    v.w = i + 3 < lim ? __ldg(src + i + 3) : 0.f;
+    return v;
+}
+
+constexpr int kHsUnroll = 8;  // 16-byte loads per thread in flight
+
+// Asynchronous global -> shared copies (cp.async) of 16 bytes (both addresses 16-byte aligned) or
+// 4 bytes, committed as a group and waited for all together.
+__device__ __forceinline__ void cp_async_16(void *dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_4(void *dst, const void *src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit_group() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait_groups() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// Count: CTA (row, c) writes chunk c's nonzero bins, ascending, as bin << kHsShift | count.
+__global__ void __launch_bounds__(kHsThreads, 2) topk_hs_count_kernel(const TopkArgs a) {
+    __shared__ uint32_t hist[kHsBins];
+    __shared__ uint32_t wsum[kHsWarps];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    for (int b = tid; b < kHsBins; b += kHsThreads) hist[b] = 0u;
     pdl_launch_dependents();
     pdl_wait();
     const int row = blockIdx.x / a.chunks, c = blockIdx.x % a.chunks;
     const int L = min(max(a.row_ctx[row], 0), a.max_ctx);
-    if (L <= a.k) return;  // phase B writes such rows whole
+    if (L <= a.k) return;  // the select kernel writes such rows whole
     const int c0 = c * a.chunk_len;
     const int n = max(0, min(L, c0 + a.chunk_len) - c0);
-    const int kp = chunk_keep(a, L, c);
     const int64_t slot = static_cast<int64_t>(row) * a.chunks + c;
-    uint32_t *ck = a.cand_key + slot * a.kcap;
-    int32_t *cp = a.cand_pos + slot * a.kcap;
-    uint32_t *meta = a.cand_meta + slot * 4;
     const float *src = a.logits + static_cast<int64_t>(row) * a.logits_stride + c0;
+    const bool vec = (reinterpret_cast<uintptr_t>(src) & 15u) == 0u;
+    __syncthreads();  // hist is zeroed
     bool nan = false;
-    uint32_t lo = 0xffffffffu, hi = 0u;
-    for (int i0 = 0; i0 < n; i0 += 8 * kAThreads) {  // eight loads per thread in flight
-        float v[8];
+    for (int i0 = 0; i0 < n; i0 += kHsUnroll * 4 * kHsThreads) {
+        float4 v[kHsUnroll];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            const int i = i0 + u * kAThreads + threadIdx.x;
-            v[u] = i < n ? __ldg(src + i) : 0.f;
-        }
+        for (int u = 0; u < kHsUnroll; ++u) v[u] = ld4(src, i0 + (u * kHsThreads + tid) * 4, n, vec);
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            const int i = i0 + u * kAThreads + threadIdx.x;
-            if (i < n) {
-                const uint32_t key = f2key(v[u], nan);
-                keys[i] = key;
-                lo = min(lo, key);
-                hi = max(hi, key);
-            }
+        for (int u = 0; u < kHsUnroll; ++u) {
+            const int i = i0 + (u * kHsThreads + tid) * 4;
+            const float x[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                if (i + q < n) atomicAdd(&hist[f2key(x[q], nan) >> kHsShift], 1u);
         }
     }
     if (nan) report(a.status, DSA_ERR_RANGE);
-    block_minmax<kAThreads>(lo, hi, wred, res);
-    lo = res[0];
-    hi = res[1];
     __syncthreads();
-    if (n <= kp) {  // the whole chunk is a candidate
-        for (int i = threadIdx.x; i < n; i += kAThreads) {
-            ck[i] = keys[i];
-            cp[i] = c0 + i;
+    constexpr int per = kHsBins / kHsThreads;  // thread t: bins per * t .. per * t + per - 1
+    uint32_t cnt[per], nz = 0;
+#pragma unroll
+    for (int q = 0; q < per; ++q) {
+        cnt[q] = hist[per * tid + q];
+        nz += cnt[q] != 0u ? 1u : 0u;
+    }
+    const uint32_t incl = warp_incl_scan32(nz, lane);
+    if (lane == 31) wsum[warp] = incl;
+    __syncthreads();
+    uint32_t at = incl - nz;
+    for (int w = 0; w < warp; ++w) at += wsum[w];
+    uint32_t *list = a.hs_list + slot * kHsBins;
+#pragma unroll
+    for (int q = 0; q < per; ++q)
+        if (cnt[q] != 0u) list[at++] = static_cast<uint32_t>(per * tid + q) << kHsShift | cnt[q];
+    if (tid == kHsThreads - 1) a.hs_nlist[slot] = at;
+}
+
+// Collect: CTA (row, c) sums the row's lists, finds the threshold bin B (the row's meta is written
+// by chunk 0), and writes chunk c's keys in bins >= B with their positions, in position order, at
+// the row's candidates before which the chunks 0 .. c-1 put theirs.
+__global__ void __launch_bounds__(kHsThreads, 2) topk_hs_collect_kernel(const TopkArgs a) {
+    extern __shared__ __align__(16) uint32_t hc_smem[];
+    uint32_t *hist = hc_smem;                   // [kHsBins]
+    uint32_t *keys = hist + kHsBins;            // [chunk_len] the chunk's keys
+    uint32_t *lcache = keys + a.chunk_len;      // [kHsCacheChunks][kHsCacheLen] the lists' first entries
+    uint32_t *nl = lcache + kHsCacheChunks * kHsCacheLen;  // [chunks] the lists' lengths
+    __shared__ uint32_t wred[64], res[8], wcnt[kHsWarps], before;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    for (int b = tid; b < kHsBins; b += kHsThreads) hist[b] = 0u;
+    if (tid == 0) before = 0u;
+    pdl_launch_dependents();
+    pdl_wait();
+    const int row = blockIdx.x / a.chunks, c = blockIdx.x % a.chunks;
+    const int L = min(max(a.row_ctx[row], 0), a.max_ctx);
+    if (L <= a.k) return;
+    const int nch = (L + a.chunk_len - 1) / a.chunk_len;
+    if (c >= nch) return;
+    const int64_t rslot = static_cast<int64_t>(row) * a.chunks;
+    const uint32_t *lists = a.hs_list + rslot * kHsBins;
+    // the chunk's logits into shared memory (as raw floats), copied while the lists are read
+    const int c0 = c * a.chunk_len;
+    const int n = min(L, c0 + a.chunk_len) - c0;
+    {
+        const float *src = a.logits + static_cast<int64_t>(row) * a.logits_stride + c0;
+        int i = tid;
+        if ((reinterpret_cast<uintptr_t>(src) & 15u) == 0u) {
+            const int n4 = n >> 2;
+            for (; i < n4; i += kHsThreads) cp_async_16(keys + 4 * i, src + 4 * i);
+            i = 4 * n4 + tid;
         }
-        if (threadIdx.x == 0) {
-            meta[0] = static_cast<uint32_t>(n);
-            meta[1] = 0u;
-            meta[2] = 1u;
+        for (; i < n; i += kHsThreads) cp_async_4(keys + i, src + i);
+        cp_async_commit_group();
+    }
+    __syncthreads();  // hist and before are zeroed
+    // the row's histogram from the chunks' lists: warp w takes chunks w, w + kHsWarps, ...; a lane
+    // loads a list's length with its entries lane and lane + 32 in one round, four lists at a time
+    // (entries past the length are not used), and the rest of longer lists after
+    for (int cc0 = warp; cc0 < nch; cc0 += 4 * kHsWarps) {
+        uint32_t m[4], e0[4], e1[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int cc = cc0 + q * kHsWarps;
+            m[q] = e0[q] = e1[q] = 0u;
+            if (cc < nch) {
+                const uint32_t *l = lists + static_cast<int64_t>(cc) * kHsBins;
+                m[q] = __ldg(a.hs_nlist + rslot + cc);
+                e0[q] = __ldg(l + lane);
+                e1[q] = __ldg(l + lane + 32);
+            }
         }
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int cc = cc0 + q * kHsWarps;
+            if (cc >= nch) continue;
+            const int mm = static_cast<int>(min(m[q], static_cast<uint32_t>(kHsBins)));
+            const bool keep = cc < kHsCacheChunks;
+            if (lane == 0) nl[cc] = static_cast<uint32_t>(mm);
+            if (lane < mm) {
+                atomicAdd(&hist[e0[q] >> kHsShift], e0[q] & kHsCountMask);
+                if (keep) lcache[cc * kHsCacheLen + lane] = e0[q];
+            }
+            if (lane + 32 < mm) {
+                atomicAdd(&hist[e1[q] >> kHsShift], e1[q] & kHsCountMask);
+                if (keep) lcache[cc * kHsCacheLen + lane + 32] = e1[q];
+            }
+            for (int j = kHsCacheLen + lane; j < mm; j += 32) {
+                const uint32_t e = __ldg(lists + static_cast<int64_t>(cc) * kHsBins + j);
+                atomicAdd(&hist[e >> kHsShift], e & kHsCountMask);
+            }
+        }
+    }
+    __syncthreads();
+    find_bin<kHsThreads, kHsBins>(hist, static_cast<uint32_t>(a.k), wred, res);
+    const uint32_t B = res[0], inb = res[2];
+    if (c == 0 && tid == 0) {
+        uint32_t *rm = a.hs_row + static_cast<int64_t>(row) * 4;
+        rm[0] = B;
+        rm[1] = res[1];
+        rm[2] = inb;
+    }
+    if (inb > static_cast<uint32_t>(kHsInCap)) {  // the select kernel takes the row from its logits
+        cp_async_wait_all();
         return;
     }
-    uint32_t T, need_eq;
-    auto key_at = [&](int i) { return keys[i]; };
-    find_threshold<kAThreads>(n, key_at, lo, hi, static_cast<uint32_t>(kp), hist, wred, res, T, need_eq);
-    emit_ordered<kAThreads>(n, key_at, T, need_eq, wgt, weq, [&](uint32_t j, int i) {
-        if (j < static_cast<uint32_t>(kp)) {
-            ck[j] = keys[i];
-            cp[j] = c0 + i;
+    // the candidates of chunks 0 .. c-1: their lists' counts in bins >= B
+    uint32_t part = 0;
+    for (int cc = warp; cc < c; cc += kHsWarps) {
+        const int mm = static_cast<int>(nl[cc]);
+        for (int j = lane; j < mm; j += 32) {
+            const uint32_t e = (j < kHsCacheLen && cc < kHsCacheChunks)
+                                   ? lcache[cc * kHsCacheLen + j]
+                                   : __ldg(lists + static_cast<int64_t>(cc) * kHsBins + j);
+            if ((e >> kHsShift) >= B) part += e & kHsCountMask;
         }
-    });
-    if (threadIdx.x == 0) {
-        meta[0] = static_cast<uint32_t>(kp);
-        meta[1] = T;
-        meta[2] = 0u;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+    if (lane == 0 && part != 0u) atomicAdd(&before, part);
+    // this chunk's keys in bins >= B: warps own contiguous segments (multiples of 128 keys); one
+    // pass turns the copied logits into keys and counts, the second places
+    const uint32_t thr = B << kHsShift;
+    const int seg = (((n + kHsWarps - 1) / kHsWarps) + 127) & ~127;
+    const int w0 = min(n, warp * seg), w1 = min(n, w0 + seg);
+    bool nan = false;  // reported by the count kernel
+    uint32_t g = 0;
+    cp_async_wait_all();
+    __syncthreads();  // every thread's copies have landed
+    for (int i = w0 + 4 * lane; i < w1; i += 128) {
+        if (i + 3 < w1) {
+            const uint4 f = *reinterpret_cast<const uint4 *>(keys + i);
+            const uint4 k4 = make_uint4(f2key(__uint_as_float(f.x), nan), f2key(__uint_as_float(f.y), nan),
+                                        f2key(__uint_as_float(f.z), nan), f2key(__uint_as_float(f.w), nan));
+            *reinterpret_cast<uint4 *>(keys + i) = k4;
+            g += (k4.x >= thr ? 1u : 0u) + (k4.y >= thr ? 1u : 0u) + (k4.z >= thr ? 1u : 0u) + (k4.w >= thr ? 1u : 0u);
+        } else {
+            for (int q = i; q < w1; ++q) {
+                const uint32_t key = f2key(__uint_as_float(keys[q]), nan);
+                keys[q] = key;
+                g += key >= thr ? 1u : 0u;
+            }
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) g += __shfl_xor_sync(0xffffffffu, g, o);
+    if (lane == 0) wcnt[warp] = g;
+    __syncthreads();
+    const uint32_t off = before;
+    uint32_t base = off, total = 0;
+    for (int w = 0; w < kHsWarps; ++w) {
+        base += w < warp ? wcnt[w] : 0u;
+        total += wcnt[w];
+    }
+    const int64_t rbase = static_cast<int64_t>(row) * a.row_cap;
+    const unsigned lt = (1u << lane) - 1u;
+    for (int i0 = w0; i0 < w1; i0 += 32) {
+        const int i = i0 + lane;
+        const uint32_t key = i < w1 ? keys[i] : 0u;
+        const bool take = i < w1 && key >= thr;
+        const unsigned m = __ballot_sync(0xffffffffu, take);
+        const uint32_t at = base + __popc(m & lt);
+        if (take && at < static_cast<uint32_t>(a.row_cap)) {
+            a.hs_key[rbase + at] = key;
+            a.hs_pos[rbase + at] = c0 + i;
+        }
+        base += __popc(m);
+    }
+    if (tid == 0) {
+        a.hs_chunk[(rslot + c) * 2] = off;
+        a.hs_chunk[(rslot + c) * 2 + 1] = total;
     }
 }
 
-// Phase B: one CTA per row merges the chunks' candidates (they lie in position order, so candidate
-// order breaks ties like position order), checks that no chunk may hold more, and writes the row's
-// selection (ascending positions), its slots and the latent prefetches.
+constexpr int kHsBtCache = kChunkMaxKeys / DSA_PAGE_SIZE;  // block-table entries of a chunk
+constexpr int kHsSpecKeys = 4096;  // candidates the select kernel copies before their number is known
+constexpr int kHsRankMax = 64;     // a threshold sub-bin of up to this many keys is resolved by ranking
+
+// The need-th largest key among those of ckey[0 .. M) that lie in bin B (1 <= need <= their number),
+// exactly: T, and need_eq = how many keys equal to T the selection takes.  One round counts 2048
+// sub-bins of 512 keys each; the keys of the chosen sub-bin are then ranked against each other
+// when they are few, else counted in a second round of 512 bins.  Block-wide; the caller has
+// zeroed hist[0 .. kBins) and res[4], with a barrier since.
+__device__ void threshold_in_bin(const uint32_t *ckey, int M, uint32_t B, uint32_t need, uint32_t *hist,
+                                 uint32_t *wred, uint32_t *res, uint32_t &T, uint32_t &need_eq) {
+    const int tid = threadIdx.x, lane = tid & 31;
+    for (int j = tid; j < M; j += kHsThreads) {
+        const uint32_t key = ckey[j];
+        if ((key >> kHsShift) == B) atomicAdd(&hist[(key >> 9) & (kBins - 1)], 1u);
+    }
+    __syncthreads();
+    find_bin<kHsThreads>(hist, need, wred, res);
+    const uint32_t sub = ((B << kHsShift) | (res[0] << 9)) >> 9;  // the sub-bin: keys >> 9 == sub
+    const uint32_t n_in = res[2];
+    need -= res[1];
+    if (n_in <= static_cast<uint32_t>(kHsRankMax)) {
+        uint32_t *cand = hist;  // the sub-bin's keys, in any order
+        const unsigned lt = (1u << lane) - 1u;
+        for (int j0 = 0; j0 < M; j0 += kHsThreads) {
+            const int j = j0 + tid;
+            const uint32_t key = j < M ? ckey[j] : 0u;
+            const bool in = j < M && (key >> 9) == sub;
+            const unsigned m = __ballot_sync(0xffffffffu, in);
+            uint32_t p = 0;
+            if (lane == 0 && m != 0u) p = atomicAdd(&res[4], static_cast<uint32_t>(__popc(m)));
+            p = __shfl_sync(0xffffffffu, p, 0) + __popc(m & lt);
+            if (in && p < static_cast<uint32_t>(kHsRankMax)) cand[p] = key;
+        }
+        __syncthreads();
+        if (tid < static_cast<int>(n_in)) {
+            const uint32_t x = cand[tid];
+            uint32_t gt = 0, eq = 0;
+            for (int i = 0; i < static_cast<int>(n_in); ++i) {
+                gt += cand[i] > x ? 1u : 0u;
+                eq += cand[i] == x ? 1u : 0u;
+            }
+            if (gt < need && need <= gt + eq) {  // every key equal to x writes the same values
+                res[5] = x;
+                res[6] = need - gt;
+            }
+        }
+        __syncthreads();
+        T = res[5];
+        need_eq = res[6];
+    } else {
+        for (int b = tid; b < 512; b += kHsThreads) hist[b] = 0u;
+        __syncthreads();
+        for (int j = tid; j < M; j += kHsThreads) {
+            const uint32_t key = ckey[j];
+            if ((key >> 9) == sub) atomicAdd(&hist[key & 511u], 1u);
+        }
+        __syncthreads();
+        find_bin<kHsThreads, 512>(hist, need, wred, res);
+        T = (sub << 9) | res[0];
+        need_eq = need - res[1];
+    }
+    __syncthreads();  // res and hist are reused
+}
+
+// Select: CTA (row, c) writes chunk c's share of the row's selection (ascending positions), its
+// slots and the latent prefetches; CTA (row, 0) writes rows of at most k keys, and rows whose
+// threshold bin overflowed, whole.
 template <bool kSlots>
-__global__ void __launch_bounds__(kBThreads, 1) topk_merge_kernel(const TopkArgs a) {
-    extern __shared__ uint32_t kb_smem[];
-    uint32_t *mkey = kb_smem;                                         // [merge_max]
-    int32_t *mpos = reinterpret_cast<int32_t *>(mkey + a.merge_max);  // [merge_max]
-    uint32_t *hist = reinterpret_cast<uint32_t *>(mpos + a.merge_max);
-    uint32_t *wred = hist + kBins, *wgt = wred + 64, *weq = wgt + 32, *res = weq + 32;
-    uint32_t *coff = res + 8;  // [chunks + 1] candidate offsets of the row's chunks
+__global__ void __launch_bounds__(kHsThreads, 2) topk_hs_select_kernel(const TopkArgs a) {
+    extern __shared__ __align__(16) uint32_t hsel_smem[];
+    uint32_t *ckey = hsel_smem;                                // [row_cap] the row's candidates' keys
+    uint32_t *hist = ckey + a.row_cap;                         // [kBins]
+    int32_t *sel = reinterpret_cast<int32_t *>(hist + kBins);  // [k] the chunk's first candidate positions
+    int32_t *btc = sel + a.k;                                  // [kHsBtCache] the chunk's page ids
+    __shared__ uint32_t wred[64], res[8], wgt[32], weq[32], cnt[2];
+    const int tid = threadIdx.x, lane = tid & 31;
+    for (int b = tid; b < kBins; b += kHsThreads) hist[b] = 0u;  // for threshold_in_bin
+    if (tid == 0) res[4] = 0u;
     pdl_launch_dependents();
     pdl_wait();
-    const int tid = threadIdx.x, lane = tid & 31;
-    const int row = blockIdx.x, k = a.k;
+    const int row = blockIdx.x / a.chunks, c = blockIdx.x % a.chunks, k = a.k;
+    const int64_t rbase = static_cast<int64_t>(row) * a.row_cap;
+    const uint32_t *rk = a.hs_key + rbase;
+    const int32_t *rp = a.hs_pos + rbase;
+    // the row's first candidates are copied before their number is known (most rows have fewer;
+    // the rest follow), and what the CTA reads next is loaded meanwhile (the meta of rows and
+    // chunks without candidates is not used)
+    const int spec = min(kHsSpecKeys, a.row_cap);
+    for (int j = tid; 4 * j < spec; j += kHsThreads) cp_async_16(ckey + 4 * j, rk + 4 * j);
+    cp_async_commit_group();
+    int n = a.row_ctx[row];
+    const uint32_t *rm = a.hs_row + static_cast<int64_t>(row) * 4;
+    const uint32_t *cm = a.hs_chunk + (static_cast<int64_t>(row) * a.chunks + c) * 2;
+    const uint32_t B = rm[0], above = rm[1], inb = rm[2];
+    const uint32_t off_raw = cm[0], own_raw = cm[1];
     int32_t *out = a.idx_out + static_cast<int64_t>(row) * k;
     int32_t *sout = kSlots ? a.slots_out + static_cast<int64_t>(row) * k : nullptr;
     const int32_t *bt_row = nullptr;
@@ -1269,123 +1530,104 @@ __global__ void __launch_bounds__(kBThreads, 1) topk_merge_kernel(const TopkArgs
         const int32_t req = a.row_req[row];
         if (req >= 0 && req < a.num_requests) bt_row = a.block_table + static_cast<int64_t>(req) * a.bt_stride;
     }
-    // the selection is staged in shared memory, then written with its slots by every thread at once
-    // (the block-table reads of the slots all in flight together)
-    int32_t *sel = reinterpret_cast<int32_t *>(coff + a.chunks + 1);  // [k]
-    auto put = [&](uint32_t j, int32_t t) {
-        if (j < static_cast<uint32_t>(k)) sel[j] = t;
-    };
-    auto write_out = [&]() {
-        __syncthreads();
-        for (int j = tid; j < k; j += kBThreads) {
-            const int32_t t = sel[j];
-            out[j] = t;
-            if constexpr (kSlots) {
-                const int32_t sl = t >= 0 ? slot_of(a, bt_row, nullptr, 0, 0, t) : -1;
-                sout[j] = sl;
-                if (a.warm_pool != nullptr && sl >= 0)
-                    bulk_prefetch_l2(a.warm_pool + static_cast<int64_t>(sl) * DSA_LATENT_DIM, DSA_LATENT_DIM);
-            }
+    int pg0 = 0, npg = 0;  // pages of the block-table cache
+    auto put_out = [&](int j, int32_t t) {  // output j of the row: token t (-1: none)
+        out[j] = t;
+        if constexpr (kSlots) {
+            const int32_t sl = t >= 0 ? slot_of(a, bt_row, btc, pg0, npg, t) : -1;
+            sout[j] = sl;
+            if (a.warm_pool != nullptr && sl >= 0)
+                bulk_prefetch_l2(a.warm_pool + static_cast<int64_t>(sl) * DSA_LATENT_DIM, DSA_LATENT_DIM);
         }
     };
-    int n = a.row_ctx[row];
     if (n < 0 || n > a.max_ctx) {
-        if (tid == 0) report(a.status, DSA_ERR_BOUNDS);
+        if (c == 0 && tid == 0) report(a.status, DSA_ERR_BOUNDS);
         n = min(max(n, 0), a.max_ctx);
     }
     if (n <= k) {
-        for (int i = tid; i < k; i += kBThreads) put(static_cast<uint32_t>(i), i < n ? i : -1);
-        write_out();
+        if (c == 0)
+            for (int j = tid; j < k; j += kHsThreads) put_out(j, j < n ? j : -1);
+        cp_async_wait_all();
         return;
     }
     const int nch = (n + a.chunk_len - 1) / a.chunk_len;
-    const uint32_t *meta = a.cand_meta + static_cast<int64_t>(row) * a.chunks * 4;
-    if (tid < 32) {  // offsets of each chunk's candidates
-        uint32_t carry = 0;
-        for (int c0 = 0; c0 < nch; c0 += 32) {
-            const int c = c0 + lane;
-            const uint32_t cnt = c < nch ? min(meta[c * 4], static_cast<uint32_t>(a.kcap)) : 0u;
-            const uint32_t incl = warp_incl_scan32(cnt, lane);
-            if (c < nch) coff[c] = carry + incl - cnt;
-            carry += __shfl_sync(0xffffffffu, incl, 31);
-        }
-        if (lane == 0) coff[nch] = carry;
-    }
-    __syncthreads();
-    const int M = static_cast<int>(min(coff[nch], static_cast<uint32_t>(a.merge_max)));
-    uint32_t lo = 0xffffffffu, hi = 0u;
-    constexpr int kIn = 8;  // candidate loads per thread in flight
-    for (int j0 = 0; j0 < M; j0 += kIn * kBThreads) {
-        uint32_t kv[kIn];
-        int32_t pv[kIn];
-#pragma unroll
-        for (int u = 0; u < kIn; ++u) {
-            const int j = j0 + u * kBThreads + tid;
-            kv[u] = 0u;
-            pv[u] = 0;
-            if (j < M) {
-                // the chunk holding candidate j (coff[c] <= j < coff[c + 1]): a fixed-depth branch-free
-                // search, so the loads of all kIn candidates are issued before any is used
-                int c = 0;
-#pragma unroll
-                for (int step = 512; step > 0; step >>= 1)
-                    if (c + step < nch && coff[c + step] <= static_cast<uint32_t>(j)) c += step;
-                const int64_t at = (static_cast<int64_t>(row) * a.chunks + c) * a.kcap + (j - coff[c]);
-                kv[u] = __ldg(a.cand_key + at);
-                pv[u] = __ldg(a.cand_pos + at);
-            }
-        }
-#pragma unroll
-        for (int u = 0; u < kIn; ++u) {
-            const int j = j0 + u * kBThreads + tid;
-            if (j < M) {
-                mkey[j] = kv[u];
-                mpos[j] = pv[u];
-                lo = min(lo, kv[u]);
-                hi = max(hi, kv[u]);
-            }
-        }
-    }
-    block_minmax<kBThreads>(lo, hi, wred, res);
-    lo = res[0];
-    hi = res[1];
-    uint32_t T = 0, need_eq = 0;
-    bool exact = M >= k && coff[nch] <= static_cast<uint32_t>(a.merge_max);
-    __syncthreads();
-    if (exact) {
-        find_threshold<kBThreads>(M, [&](int i) { return mkey[i]; }, lo, hi, static_cast<uint32_t>(k), hist, wred,
-                                  res, T, need_eq);
-        // a chunk that dropped keys below a threshold key not under T may hold more selected keys
-        bool more = false;
-        for (int c = tid; c < nch; c += kBThreads) more |= meta[c * 4 + 2] == 0u && meta[c * 4 + 1] >= T;
-        exact = !__syncthreads_or(more);
-    }
-    if (exact) {
-        emit_ordered<kBThreads>(M, [&](int i) { return mkey[i]; }, T, need_eq, wgt, weq,
-                                [&](uint32_t j, int i) { put(j, mpos[i]); });
-        write_out();
+    if (c >= nch || (inb > static_cast<uint32_t>(kHsInCap) && c != 0)) {
+        cp_async_wait_all();
         return;
     }
-    // the candidates may miss selected keys: select from the whole row's logits
-    const float *src = a.logits + static_cast<int64_t>(row) * a.logits_stride;
-    auto gkey = [&](int i) {
-        bool nan = false;
-        return f2key(__ldg(src + i), nan);
-    };
-    lo = 0xffffffffu;
-    hi = 0u;
-    for (int i = tid; i < n; i += kBThreads) {
-        const uint32_t key = gkey(i);
-        lo = min(lo, key);
-        hi = max(hi, key);
+    if (inb > static_cast<uint32_t>(kHsInCap)) {
+        // the row's whole logits (the candidates were not written)
+        const float *src = a.logits + static_cast<int64_t>(row) * a.logits_stride;
+        auto gkey = [&](int i) {
+            bool nan = false;
+            return f2key(__ldg(src + i), nan);
+        };
+        uint32_t lo = 0xffffffffu, hi = 0u;
+        for (int i = tid; i < n; i += kHsThreads) {
+            const uint32_t key = gkey(i);
+            lo = min(lo, key);
+            hi = max(hi, key);
+        }
+        block_minmax<kHsThreads>(lo, hi, wred, res);
+        lo = res[0];
+        hi = res[1];
+        __syncthreads();
+        uint32_t T, need_eq;
+        find_threshold<kHsThreads>(n, gkey, lo, hi, static_cast<uint32_t>(k), hist, wred, res, T, need_eq);
+        emit_ordered<kHsThreads>(n, gkey, T, need_eq, wgt, weq, [&](uint32_t j, int i) {
+            if (j < static_cast<uint32_t>(k)) sel[j] = i;
+        });
+        for (int j = tid; j < k; j += kHsThreads) put_out(j, sel[j]);
+        cp_async_wait_all();
+        return;
     }
-    block_minmax<kBThreads>(lo, hi, wred, res);
-    lo = res[0];
-    hi = res[1];
-    __syncthreads();
-    find_threshold<kBThreads>(n, gkey, lo, hi, static_cast<uint32_t>(k), hist, wred, res, T, need_eq);
-    emit_ordered<kBThreads>(n, gkey, T, need_eq, wgt, weq, [&](uint32_t j, int i) { put(j, i); });
-    write_out();
+    const int M = min(static_cast<int>(above + inb), a.row_cap);
+    const int off = min(static_cast<int>(off_raw), M), own = min(static_cast<int>(own_raw), M - off);
+    if (tid < 2) cnt[tid] = 0u;
+    // the rest of the candidates; then the chunk's first k candidate positions and its block-table
+    // entries, needed only once the threshold is known
+    for (int j = spec + tid; j < M; j += kHsThreads) cp_async_4(ckey + j, rk + j);
+    cp_async_commit_group();
+    const int ocache = min(own, k);
+    for (int i = tid; i < ocache; i += kHsThreads) cp_async_4(sel + i, rp + off + i);
+    if constexpr (kSlots) {
+        const int c0 = c * a.chunk_len;
+        pg0 = c0 / DSA_PAGE_SIZE;
+        npg = min((min(n, c0 + a.chunk_len) - c0 + DSA_PAGE_SIZE - 1) / DSA_PAGE_SIZE, kHsBtCache);
+        if (bt_row != nullptr)
+            for (int i = tid; i < npg; i += kHsThreads) cp_async_4(btc + i, bt_row + pg0 + i);
+        else
+            npg = 0;
+    }
+    cp_async_commit_group();
+    cp_async_wait_groups<1>();
+    __syncthreads();  // the candidates have landed
+    // the exact threshold among the candidates in bin B
+    uint32_t T, need_eq;
+    threshold_in_bin(ckey, M, B, static_cast<uint32_t>(k) - above, hist, wred, res, T, need_eq);
+    // keys above T and equal to T among the candidates of the chunks before this one
+    uint32_t g = 0, e = 0;
+    for (int j = tid; j < off; j += kHsThreads) {
+        const uint32_t key = ckey[j];
+        g += key > T ? 1u : 0u;
+        e += key == T ? 1u : 0u;
+    }
+    warp_sum2(g, e);
+    if (lane == 0 && (g | e) != 0u) {
+        atomicAdd(&cnt[0], g);
+        atomicAdd(&cnt[1], e);
+    }
+    cp_async_wait_all();
+    __syncthreads();  // the counts, the positions and the block-table entries
+    const uint32_t gb = cnt[0], eb = cnt[1];
+    const uint32_t eq_left = need_eq > eb ? need_eq - eb : 0u;
+    const uint32_t obase = gb + min(eb, need_eq);
+    emit_ordered<kHsThreads>(own, [&](int i) { return ckey[off + i]; }, T, eq_left, wgt, weq,
+                             [&](uint32_t j, int i) {
+                                 const uint32_t o = obase + j;
+                                 if (o < static_cast<uint32_t>(k))
+                                     put_out(static_cast<int>(o), i < ocache ? sel[i] : __ldg(rp + off + i));
+                             });
 }
 
 }  // namespace
@@ -1397,67 +1639,77 @@ TopkChunkPlan topk_chunk_plan(int32_t num_rows, int32_t max_ctx, int32_t k, int 
         return p;
     // chunks per row: about two CTAs per SM over the batch, chunks of at most kChunkMaxKeys keys
     int C = (2 * sms + num_rows - 1) / num_rows;
-    C = C < kChunkedMaxChunks ? C : kChunkedMaxChunks;  // the merge of few rows stays within shared memory
+    C = C < kChunkedMaxChunks ? C : kChunkedMaxChunks;  // each collect CTA adds up its row's lists
     const int by_len = (max_ctx + kChunkMaxKeys - 1) / kChunkMaxKeys;
     C = C > by_len ? C : by_len;
     int Lc = ((max_ctx + C - 1) / C + 63) / 64 * 64;
     if (Lc < kChunkMinKeys) Lc = kChunkMinKeys;
     C = (max_ctx + Lc - 1) / Lc;
-    // a row of nc chunks passes on at most (nc - 1) keep(nc) + k candidates (chunk_keep on the device),
-    // keep(nc) = min(k, Lc, round32(2k / nc + 64)); the merge holds the largest such total
-    const int kcap = k < Lc ? k : Lc;
-    int merge_max = 0;
-    for (int nc = 1; nc <= C; ++nc) {
-        int kp = ((2 * k + nc - 1) / nc + 64 + 31) / 32 * 32;
-        kp = kp < kcap ? kp : kcap;
-        const int tot = (nc - 1) * kp + kcap;
-        merge_max = tot > merge_max ? tot : merge_max;
-    }
-    if (merge_max > kMergeMaxKeys) return p;
+    if (C > kHsMaxChunks) return p;  // rows of more than 16M keys: the cluster selection
     p.chunks = C;
     p.chunk_len = Lc;
-    p.keep = 0;  // per row: chunk_keep()
-    p.keep_last = kcap;
-    p.kcap = kcap;
-    p.merge_max = merge_max;
-    const size_t cand = static_cast<size_t>(num_rows) * C * p.kcap * 4;
-    p.bytes = align256(cand) * 2 + align256(static_cast<size_t>(num_rows) * C * 16);
+    // a row's candidates: fewer than k above the threshold bin, and the bin's keys (16-byte rows)
+    p.row_cap = (k + kHsInCap + 3) / 4 * 4;
+    const size_t rc = static_cast<size_t>(num_rows) * C;
+    p.bytes = align256(rc * kHsBins * 4) + align256(rc * 4) + 2 * align256(static_cast<size_t>(num_rows) * p.row_cap * 4) +
+              align256(rc * 8) + align256(static_cast<size_t>(num_rows) * 16);
     return p;
+}
+
+void topk_chunk_bind(TopkArgs &a, const TopkChunkPlan &p, void *workspace) {
+    const size_t rc = static_cast<size_t>(a.num_rows) * p.chunks;
+    uint8_t *w = static_cast<uint8_t *>(workspace);
+    a.hs_list = reinterpret_cast<uint32_t *>(w);
+    w += align256(rc * kHsBins * 4);
+    a.hs_nlist = reinterpret_cast<uint32_t *>(w);
+    w += align256(rc * 4);
+    a.hs_key = reinterpret_cast<uint32_t *>(w);
+    w += align256(static_cast<size_t>(a.num_rows) * p.row_cap * 4);
+    a.hs_pos = reinterpret_cast<int32_t *>(w);
+    w += align256(static_cast<size_t>(a.num_rows) * p.row_cap * 4);
+    a.hs_chunk = reinterpret_cast<uint32_t *>(w);
+    w += align256(rc * 8);
+    a.hs_row = reinterpret_cast<uint32_t *>(w);
+    a.chunks = p.chunks;
+    a.chunk_len = p.chunk_len;
+    a.row_cap = p.row_cap;
 }
 
 namespace {
 
 template <bool kSlots>
-cudaError_t launch_two_phase(const TopkArgs &a, cudaStream_t s) {
+cudaError_t launch_hist_select(const TopkArgs &a, cudaStream_t s) {
     static int configured_device = -1;
     int dev = 0;
     cudaGetDevice(&dev);
-    const size_t smem_a = (static_cast<size_t>(kChunkMaxKeys) + kBins + 64 + 32 + 32 + 8) * 4;
-    const size_t smem_b_max = (2 * static_cast<size_t>(kMergeMaxKeys) + kBins + 64 + 32 + 32 + 8 + 1024 +
-                               DSA_MAX_TOPK) * 4;
+    const size_t smem_collect_max = (static_cast<size_t>(kHsBins) + kChunkMaxKeys + kHsCacheChunks * kHsCacheLen + kHsMaxChunks) *
+                                     4;
+    const size_t smem_select_max = (static_cast<size_t>(DSA_MAX_TOPK) + kHsInCap + kBins + DSA_MAX_TOPK + kHsBtCache) * 4;
     if (configured_device != dev) {
-        cudaError_t e = cudaFuncSetAttribute(topk_chunk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(smem_a));
+        cudaError_t e = cudaFuncSetAttribute(topk_hs_collect_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(smem_collect_max));
         if (e != cudaSuccess) return e;
-        e = cudaFuncSetAttribute(topk_merge_kernel<kSlots>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(smem_b_max));
+        e = cudaFuncSetAttribute(topk_hs_select_kernel<kSlots>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(smem_select_max));
         if (e != cudaSuccess) return e;
         configured_device = dev;
     }
-    const size_t sa = (static_cast<size_t>(a.chunk_len) + kBins + 64 + 32 + 32 + 8) * 4;
-    cudaError_t e = launch_pdl(topk_chunk_kernel, dim3(static_cast<unsigned>(a.num_rows * a.chunks)),
-                               dim3(kAThreads), sa, s, a);
+    const dim3 grid(static_cast<unsigned>(a.num_rows * a.chunks));
+    cudaError_t e = launch_pdl(topk_hs_count_kernel, grid, dim3(kHsThreads), 0, s, a);
     if (e != cudaSuccess) return e;
-    const size_t sb = (2 * static_cast<size_t>(a.merge_max) + kBins + 64 + 32 + 32 + 8 + a.chunks + 1 + a.k) * 4;
-    return launch_pdl(topk_merge_kernel<kSlots>, dim3(static_cast<unsigned>(a.num_rows)), dim3(kBThreads), sb, s, a);
+    e = launch_pdl(topk_hs_collect_kernel, grid, dim3(kHsThreads),
+                   (static_cast<size_t>(kHsBins) + a.chunk_len + kHsCacheChunks * kHsCacheLen + a.chunks) * 4, s, a);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(topk_hs_select_kernel<kSlots>, grid, dim3(kHsThreads),
+                      (static_cast<size_t>(a.row_cap) + kBins + a.k + kHsBtCache) * 4, s, a);
 }
 
 }  // namespace
 
 cudaError_t launch_topk(const TopkArgs &a, cudaStream_t s) {
     if (a.num_rows == 0) return cudaSuccess;
-    if (a.chunks > 0 && a.hist == nullptr)  // the caller planned the two-phase path
-        return a.slots_out != nullptr ? launch_two_phase<true>(a, s) : launch_two_phase<false>(a, s);
+    if (a.chunks > 0 && a.hist == nullptr)  // the caller planned the histogram selection
+        return a.slots_out != nullptr ? launch_hist_select<true>(a, s) : launch_hist_select<false>(a, s);
     const bool h = a.hist != nullptr, sl = a.slots_out != nullptr;
     if (h && sl) return launch_variant<true, true>(a, s);
     if (h) return launch_variant<true, false>(a, s);

@@ -165,7 +165,7 @@ def test_host_validation_of_the_msa_insert_and_warm_calls(lib):
                                    None) == P.ERR_INVALID_ARG
     assert lib.dsa_topk_slots_warm(fake, 4096, ctypes.byref(r), ctypes.byref(P._Cache(fake, 9, 64, 10, 0.01)), 16,
                                    fake, fake, None, None, 0, None) == P.ERR_UNSUPPORTED
-    # the two-phase top-k's workspace: none for short rows or many rows (or without a device)
+    # the histogram top-k's workspace: none for short rows or many rows (or without a device)
     assert lib.dsa_topk_workspace_size(8, 8192, 2048) == 0
     assert lib.dsa_topk_workspace_size(65, 131072, 2048) == 0
     assert lib.dsa_topk_workspace_size(0, 131072, 2048) == 0

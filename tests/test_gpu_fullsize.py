@@ -3,7 +3,8 @@
 oracle can afford one by one:
 
   * indexer logits of a sampled row within the accumulation bound;
-  * the row's top-k set equals the oracle's up to ties inside the 1e-3 band;
+  * the row's top-k set equals the oracle's up to ties inside the 1e-3 band,
+    and is bit-exactly the oracle's selection over the GPU's own logits;
   * the row's attention output within the FP8 (NVFP4) tolerance, on the
     GPU's own selection;
   * every row: selection sorted ascending, in range, no duplicates.
@@ -59,6 +60,8 @@ def test_fullsize_sampled(name):
     gpu_lg = layer.logits.cpu().numpy()
     bound = U.logit_bound(inp, rows)
     ora_idx = oracle.topk_f64(np.nan_to_num(ref_lg, nan=-np.inf), rc[rows], wl.k)
+    # the selection of the sampled rows is exactly the oracle's over the GPU's own logits
+    assert np.array_equal(idx[rows], oracle.topk_f32(gpu_lg[rows], rc[rows], wl.k))
     for i, r in enumerate(rows):
         d = np.abs(gpu_lg[r, :rc[r]].astype(np.float64) - ref_lg[i, :rc[r]])
         assert np.all(d <= bound[r]), (r, float((d / bound[r]).max()))

@@ -184,12 +184,13 @@ def test_topk_bit_exact(case):
     assert np.array_equal(got.cpu().numpy(), ref)
 
 
-def _two_phase_cases():
-    """Rows long enough for the two-phase top-k (a workspace is given): plain, tied and concentrated
-    scores, so both the merge and the whole-row fallback are exercised."""
+def _hist_select_cases():
+    """Rows long enough for the histogram selection (a workspace is given): plain, tied and
+    concentrated scores, so both the candidate path and the whole-row fallback (a threshold bin of
+    more keys than the select kernel holds) are exercised."""
     rng = np.random.default_rng(17)
     cases = {}
-    n = 300000  # longer than 256K keys: the two-phase path
+    n = 300000  # more chunks than the select kernel's rows get CTAs at two per SM
     v = rng.standard_normal((4, n)).astype(np.float32)
     cases["normal_4x300k"] = (v, np.array([n - 4099 * i for i in range(4)], dtype=np.int32), 2048)
     t = (rng.integers(0, 40, (3, n)) / 8).astype(np.float32)  # ties at the threshold across chunks
@@ -206,18 +207,20 @@ def _two_phase_cases():
     cases["short_and_long"] = (m, np.array([n, 100, 2048, 2049, 33333], dtype=np.int32), 2048)
     w = rng.standard_normal((4, n)).astype(np.float32)
     cases["long_k100"] = (w, np.array([n, n - 1, 150000, 80000], dtype=np.int32), 100)
+    b = rng.standard_normal((8, 140000)).astype(np.float32) * 40.0 + 150.0  # a decode batch of 8 long rows
+    cases["b8_140k"] = (b, np.array([140000] * 6 + [131073, 70001], dtype=np.int32), 2048)
     return cases
 
 
-TWO_PHASE_CASES = _two_phase_cases()
+HIST_SELECT_CASES = _hist_select_cases()
 
 
-@pytest.mark.parametrize("case", sorted(TWO_PHASE_CASES))
-def test_topk_two_phase_bit_exact(case):
-    v, ctx, k = TWO_PHASE_CASES[case]
+@pytest.mark.parametrize("case", sorted(HIST_SELECT_CASES))
+def test_topk_hist_select_bit_exact(case):
+    v, ctx, k = HIST_SELECT_CASES[case]
     R, width = v.shape
     need = P.topk_workspace_size(R, width, k)
-    assert need > 0  # these shapes take the two-phase path
+    assert need > 0  # these shapes take the histogram selection
     ws = torch.empty(need, dtype=torch.uint8, device="cuda")
     st = P.new_status()
     got = P.topk(torch.from_numpy(v).cuda(), torch.from_numpy(ctx).cuda(), width, k, status=st, workspace=ws)
@@ -226,8 +229,8 @@ def test_topk_two_phase_bit_exact(case):
     assert np.array_equal(got.cpu().numpy(), oracle.topk_f32(v, ctx, k))
 
 
-def test_topk_two_phase_rejects_a_small_workspace():
-    v, ctx, k = TWO_PHASE_CASES["normal_4x300k"]
+def test_topk_hist_select_rejects_a_small_workspace():
+    v, ctx, k = HIST_SELECT_CASES["normal_4x300k"]
     ws = torch.empty(P.topk_workspace_size(v.shape[0], v.shape[1], k) - 256, dtype=torch.uint8, device="cuda")
     with pytest.raises(P.DsaError, match="workspace"):
         P.topk(torch.from_numpy(v).cuda(), torch.from_numpy(ctx).cuda(), v.shape[1], k, workspace=ws)
