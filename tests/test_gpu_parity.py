@@ -236,6 +236,38 @@ def test_topk_hist_select_rejects_a_small_workspace():
         P.topk(torch.from_numpy(v).cuda(), torch.from_numpy(ctx).cuda(), v.shape[1], k, workspace=ws)
 
 
+def _topk_ws(R, n, k):
+    need = P.topk_workspace_size(R, n, k)
+    assert need > 0  # the histogram selection
+    return torch.empty(need, dtype=torch.uint8, device="cuda")
+
+
+@pytest.mark.parametrize("n,long_rows", [(5000, False), (300000, True)])
+def test_topk_reports_a_nan_logit(n, long_rows):
+    """A NaN logit is DSA_ERR_RANGE on both selection paths; the other rows stay exact."""
+    v = np.random.default_rng(3).standard_normal((2, n)).astype(np.float32)
+    v[1, n // 2] = np.nan
+    ctx = np.array([n, n], dtype=np.int32)
+    st = P.new_status()
+    got = P.topk(torch.from_numpy(v).cuda(), torch.from_numpy(ctx).cuda(), n, 2048, status=st,
+                 workspace=_topk_ws(2, n, 2048) if long_rows else None)
+    torch.cuda.synchronize()
+    assert int(st.item()) == P.ERR_RANGE
+    assert np.array_equal(got.cpu().numpy()[0], oracle.topk_f32(v[:1], ctx[:1], 2048)[0])
+
+
+@pytest.mark.parametrize("n,long_rows", [(5000, False), (300000, True)])
+def test_topk_clamps_and_reports_a_row_past_max_ctx(n, long_rows):
+    """row_ctx above max_ctx is DSA_ERR_BOUNDS; that row is selected over max_ctx keys."""
+    v = np.random.default_rng(4).standard_normal((2, n)).astype(np.float32)
+    st = P.new_status()
+    got = P.topk(torch.from_numpy(v).cuda(), torch.tensor([n, n + 7], dtype=torch.int32, device="cuda"), n, 2048,
+                 status=st, workspace=_topk_ws(2, n, 2048) if long_rows else None)
+    torch.cuda.synchronize()
+    assert int(st.item()) == P.ERR_BOUNDS
+    assert np.array_equal(got.cpu().numpy(), oracle.topk_f32(v, np.array([n, n], dtype=np.int32), 2048))
+
+
 def test_topk_on_indexer_logits_bit_exact():
     inp = U.gpu_inputs(INDEXER_CASES["ragged"])
     lg = U.run_indexer(inp)
