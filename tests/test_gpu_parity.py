@@ -209,6 +209,8 @@ def _hist_select_cases():
     cases["long_k100"] = (w, np.array([n, n - 1, 150000, 80000], dtype=np.int32), 100)
     b = rng.standard_normal((8, 140000)).astype(np.float32) * 40.0 + 150.0  # a decode batch of 8 long rows
     cases["b8_140k"] = (b, np.array([140000] * 6 + [131073, 70001], dtype=np.int32), 2048)
+    o = rng.standard_normal((3, 262147)).astype(np.float32)  # odd row stride: unaligned rows, ragged tails
+    cases["odd_stride"] = (o, np.array([262147, 200001, 150003], dtype=np.int32), 2048)
     return cases
 
 
