@@ -107,8 +107,8 @@ cudaError_t launch_topk(const TopkArgs &a, cudaStream_t s);
 // Histogram selection of few long rows: limits, the plan for a batch (bytes == 0: not used) and the
 // binding of a workspace of plan.bytes to the arguments.  Its three launches of independent CTAs
 // beat the cluster selection once rows are longer than a cluster keeps in shared memory; measured
-// on a GB300 per step: 256K keys 90.0 vs 102.1 us, 1M keys 76.6 vs 93.5 us, but 128K keys 62.6 vs
-// 60.7 us (its chain of barrier-separated phases costs more than the cluster's there).
+// on a GB300 per step: 256K keys 90.0 vs 102.1 us, 1M keys 76.6 vs 93.5 us; at 128K keys the two are
+// even (61.2-61.4 us each, measured back to back on one GPU), and the cluster path needs no workspace.
 constexpr int kChunkedMaxRows = 64;
 constexpr int kChunkedMinCtx = 131072;
 constexpr int kChunkMinKeys = 2048;
